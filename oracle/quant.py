@@ -1,0 +1,159 @@
+"""Quantized K/V formats: INT8 per token, KIVI-style INT4, and their ledgers.
+
+Test infrastructure only (see ``oracle/__init__.py``).
+
+Follows "M8.6 Live-Data Quantization: Activations and KV Cache":
+
+* §0x02A  stored-scale conventions: ties-to-even rounding, encode with the
+          re-read stored qparams, a sentinel scale of one for a row with no
+          range, and no subnormal stored scale;
+* §0x03A-C scale placement (per-token K/V scales, per-channel K scales);
+* §0x04A-B byte ledger M_served = codes + qparams + residual (+ pages);
+* §0x05B  per-token scaling is append-local;
+* §0x06A-B KIVI: K per channel over groups of G tokens, V per token, a
+          full-precision residual whose oldest G rows close while it holds
+          more than R rows; §0x06E  G = 32, R = 128;
+* §0x09C  the asymmetric floating-offset ABI (an offset stored as a value,
+          not clamped to the code range).
+
+Formats (the reading of the pages that the library documents):
+
+* INT8: per (token, kv head), separately for K and V, over the d channels:
+  mn = min, mx = max (exact in fp32); s = fp16((mx - mn) / 255) computed with
+  an fp32 divide, z = fp16(mn).  mx == mn stores the sentinel s = 1; a
+  stored scale below 2^-14 (zero or subnormal fp16) is raised to 2^-14.
+  code = clip(rint_even((x - z) / s), 0, 255) in fp32 with the RE-READ
+  stored s and z.  Decoding is x_hat = code * s + z.
+* INT4 KIVI: the same quantizer with 15 levels.  K: one (s, z) per
+  (G-token group, channel).  V: one (s, z) per (token, Gv-channel group).
+  Two codes per byte along d, the even channel in the low nibble.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+F16_MIN_NORMAL = np.float16(2.0 ** -14)
+
+
+# ---- bf16 / fp16 conversions -------------------------------------------------
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of bf16 bit patterns (uint16) as float64."""
+    b = np.asarray(bits).astype(np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    b = np.asarray(bits).astype(np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+def f16_bits_to_f64(bits) -> np.ndarray:
+    return np.asarray(bits).astype(np.uint16).view(np.float16).astype(np.float64)
+
+
+# ---- one affine group (vectorised: one group per slice of the last axis) ------
+
+def affine_qparams(x_f32, qmax: int):
+    """Stored (s, z) float16 for each group along the last axis  (M8.6 §0x02A, §0x09C)."""
+    x = np.asarray(x_f32, dtype=np.float32)
+    mn = x.min(axis=-1)
+    mx = x.max(axis=-1)
+    s = ((mx - mn) / np.float32(qmax)).astype(np.float16)     # fp32 divide, RNE to fp16
+    s = np.where(s < F16_MIN_NORMAL, F16_MIN_NORMAL, s)
+    s = np.where(mx == mn, np.float16(1.0), s).astype(np.float16)
+    z = mn.astype(np.float16)
+    return s, z
+
+
+def affine_encode(x_f32, s16, z16, qmax: int) -> np.ndarray:
+    """codes = clip(rint_even((x - z) / s), 0, qmax) in fp32 with the re-read stored s, z."""
+    x = np.asarray(x_f32, dtype=np.float32)
+    s = np.asarray(s16, dtype=np.float16).astype(np.float32)[..., None]
+    z = np.asarray(z16, dtype=np.float16).astype(np.float32)[..., None]
+    r = np.rint((x - z) / s)          # each operation rounded in fp32, ties to even
+    return np.clip(r, 0, qmax).astype(np.uint8)
+
+
+def affine_decode(codes, s16, z16) -> np.ndarray:
+    """x_hat = code * s + z in float64 (s, z broadcast over the group's last axis)."""
+    s = np.asarray(s16, dtype=np.float16).astype(np.float64)[..., None]
+    z = np.asarray(z16, dtype=np.float16).astype(np.float64)[..., None]
+    return np.asarray(codes, dtype=np.float64) * s + z
+
+
+# ---- INT8 per token ----------------------------------------------------------
+
+def int8_token_quantize(x_f32):
+    """(token, head) rows [..., d] -> codes uint8 [..., d], s, z fp16 [...]  (M8.6 §0x05B)."""
+    s, z = affine_qparams(x_f32, 255)
+    return affine_encode(x_f32, s, z, 255), s, z
+
+
+# ---- KIVI INT4 ---------------------------------------------------------------
+
+def kivi_k_group_quantize(k_rows_f32):
+    """K group [..., G, d] -> codes [..., G, d], s [..., d], z [..., d]: one scale per channel
+    over the group's G tokens  (M8.6 §0x06A)."""
+    k = np.swapaxes(np.asarray(k_rows_f32, dtype=np.float32), -1, -2)   # [..., d, G]
+    s, z = affine_qparams(k, 15)
+    codes = affine_encode(k, s, z, 15)
+    return np.swapaxes(codes, -1, -2), s, z
+
+
+def kivi_v_token_quantize(v_row_f32, group: int):
+    """V rows [..., d] -> codes [..., d], s [..., d/Gv], z [..., d/Gv]: per token, per Gv
+    channels  (M8.6 §0x06A)."""
+    v = np.asarray(v_row_f32, dtype=np.float32)
+    d = v.shape[-1]
+    vg = v.reshape(v.shape[:-1] + (d // group, group))
+    s, z = affine_qparams(vg, 15)
+    codes = affine_encode(vg, s, z, 15)
+    return codes.reshape(v.shape), s, z
+
+
+def kivi_quantized_prefix(T: int, G: int = 32, R: int = 128) -> int:
+    """Rows already closed into INT4 groups after T appends  (M8.6 §0x06B).
+
+    The KIVILayerState loop closes the oldest G residual rows while the
+    residual holds more than R rows.  Replaying it append by append keeps the
+    residual in (R - G, R] once T > R.
+    """
+    closed = 0
+    for t in range(1, T + 1):
+        while t - closed > R:
+            closed += G
+    return closed
+
+
+def pack_int4(codes) -> np.ndarray:
+    """Two codes per byte along the last axis, the even channel in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def unpack_int4(packed) -> np.ndarray:
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+# ---- byte ledger, M8.6 §0x04A-B ---------------------------------------------
+
+def served_bytes(T: int, L: int, H_kv: int, d_h: int, bits: int, G_t: int, G_d: int,
+                 b_s: int, b_z: int, residual: int, b_res: int):
+    """Code payload + K qparams + V qparams + residual for a synchronised tail (M8.6 §0x04B).
+
+    Only the T - residual closed tokens carry codes and qparams.  K groups are
+    per channel over G_t tokens; V groups per token over G_d channels.
+    """
+    n_q = T - residual
+    codes = 2 * n_q * L * H_kv * d_h * bits // 8
+    k_qp = (n_q // G_t) * L * H_kv * d_h * (b_s + b_z)
+    v_qp = n_q * L * H_kv * (d_h // G_d) * (b_s + b_z)
+    res = 2 * residual * L * H_kv * d_h * b_res
+    return {"codes": codes, "k_qparams": k_qp, "v_qparams": v_qp, "residual": res,
+            "total": codes + k_qp + v_qp + res}

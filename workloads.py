@@ -1,0 +1,244 @@
+"""Seeded synthetic inputs for split-KV decode attention.
+
+This module only draws and lays out inputs: it holds none of the method's
+arithmetic (no scores, softmax, merging, quantisation or masking).  Both the
+CUDA path and the CPU oracle consume exactly the tensors it returns.
+
+Recipe (shapes and distributions of the five workloads):
+
+1. tiny contiguous decode (seed 0): B=1, S_q=1, H_q=8, H_kv=2, d=64, 256
+   visible rows; Q, K, V ~ N(0,1) rounded to bf16; contiguous [B, T, H_kv, d]
+   cache; 4 fixed splits.
+2. paged ragged GQA decode (seed 1): B=16, S_q=1, H_q=32, H_kv=8, d=128;
+   lengths uniform integers in [1024, 8192]; K, V ~ N(0,1) bf16 with 4
+   distinct outlier channels per kv head (K only) scaled by 8; 16-token
+   pages; the page list is the first sum(ceil(T_b/16)) entries of a random
+   permutation of a 10,000-page pool, concatenated request by request.
+3. long-context split-heavy decode (seed 2): B=4, H_q=64, H_kv=8, d=128;
+   lengths {131072, 100003, 65537, 1}; 64-token pages; pool = exactly the
+   pages needed, permuted; S_q = 1 or 4 (bottom-right causal rows).
+4. retention programs (seed 3): B=8, S_q=1, H_q=32, H_kv=8, d=128, 32768
+   stored rows each, 16-token pages.  (a) 4 sinks + 4096 recent rows.
+   (b) per (request, kv head) sorted index lists of 2048 positions: sinks
+   [0, 64), recent [F-512, F) and the top 1472 of [64, F-512) ranked by a
+   Gumbel(0,1) draw per (request, kv head, position), G = -ln(-ln U).
+5. quantized KV (seed 4): B=32, S_q=1, H_q=32, H_kv=8, d=128; lengths
+   uniform in [2048, 32768]; K, V ~ N(0,1) bf16 with 4 K outlier channels
+   per kv head scaled by 8; 16-token pages; the history is handed over as
+   packed ragged bf16 rows for the cache writer (kv_append) to encode.
+
+Everywhere: Q ~ N(0,1) bf16 of shape [B, S_q, H_q, d]; metadata (lengths,
+permutations, outlier channels, index lists) is drawn on the CPU from
+``torch.Generator`` seeded with the workload seed; K/V/Q values are drawn on
+the requested device from a generator seeded with ``seed + 1000``.  Pool
+pages that no request references and page rows past a request's length are
+filled with NaN ("poison"), so a visibility leak shows up as NaN.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+NAN_BF16 = float("nan")
+
+
+@dataclass
+class Workload:
+    name: str
+    problem: dict
+    q: torch.Tensor
+    kv_len: torch.Tensor                      # int32 [B] on the CPU
+    k: torch.Tensor = None                    # bf16 cache (paged pool or contiguous)
+    v: torch.Tensor = None
+    page_indptr: torch.Tensor = None          # int32 [B+1] CPU
+    page_indices: torch.Tensor = None         # int32 CPU
+    cache_batch_idx: torch.Tensor = None
+    index_indptr: torch.Tensor = None         # int32 [B*H_kv+1] CPU
+    index_list: torch.Tensor = None           # int32 CPU
+    rows_indptr: torch.Tensor = None          # packed ragged history (quantized workloads)
+    k_rows: torch.Tensor = None
+    v_rows: torch.Tensor = None
+    meta: dict = field(default_factory=dict)
+
+
+def _gens(seed: int, device):
+    meta = torch.Generator().manual_seed(seed)
+    vals = torch.Generator(device=device).manual_seed(seed + 1000)
+    return meta, vals
+
+
+def _normal_bf16(shape, gen, device, outliers=None):
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if outliers is not None:
+        # outliers: [H_kv, n] channel ids; the head axis is -3 for pools [.., H, P, d]
+        # and -2 for rows [.., H, d]; callers pass ``outlier_axis``.
+        head_axis, chans = outliers
+        for h in range(chans.shape[0]):
+            idx = [slice(None)] * x.dim()
+            idx[head_axis] = h
+            idx[-1] = chans[h].to(device)
+            x[tuple(idx)] *= 8.0
+    return x.to(torch.bfloat16)
+
+
+def _outlier_channels(H_kv, d, meta):
+    return torch.stack([torch.randperm(d, generator=meta)[:4] for _ in range(H_kv)])
+
+
+def _page_tables(lens, P, pool_pages, meta):
+    n_pages = [-(-int(T) // P) for T in lens]
+    total = sum(n_pages)
+    if pool_pages is None:
+        pool_pages = total
+    assert total <= pool_pages, "pool too small"
+    perm = torch.randperm(pool_pages, generator=meta)
+    indptr = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    indptr[1:] = torch.cumsum(torch.tensor(n_pages, dtype=torch.int64), 0).to(torch.int32)
+    return indptr, perm[:total].to(torch.int32).contiguous(), pool_pages
+
+
+def _poison_pool(pool, lens, indptr, indices, P):
+    """NaN every unreferenced page and every row past a request's length."""
+    used = torch.zeros(pool.shape[0], dtype=torch.bool)
+    used[indices.long()] = True
+    pool[(~used).nonzero().flatten().to(pool.device)] = NAN_BF16
+    for b, T in enumerate(lens):
+        T = int(T)
+        n = int(indptr[b + 1] - indptr[b])
+        if n and T % P:
+            last = int(indices[int(indptr[b + 1]) - 1])
+            pool[last, :, T % P:, :] = NAN_BF16
+
+
+def paged_bf16(name, *, B, S_q, H_q, H_kv, d, lens, P, seed, device, pool_pages=None,
+               outliers=False, mask="causal", **mask_args) -> Workload:
+    """Paged HND bf16 pools [N_pages, H_kv, P, d] filled with N(0,1) history."""
+    meta, vals = _gens(seed, device)
+    lens = [int(t) for t in lens]
+    indptr, indices, pool_pages = _page_tables(lens, P, pool_pages, meta)
+    och = _outlier_channels(H_kv, d, meta) if outliers else None
+    k = _normal_bf16((pool_pages, H_kv, P, d), vals, device, (-3, och) if outliers else None)
+    v = _normal_bf16((pool_pages, H_kv, P, d), vals, device)
+    q = _normal_bf16((B, S_q, H_q, d), vals, device)
+    _poison_pool(k, lens, indptr, indices, P)
+    _poison_pool(v, lens, indptr, indices, P)
+    problem = dict(B=B, S_q=S_q, H_q=H_q, H_kv=H_kv, d=d, layout="paged", fmt="bf16", P=P,
+                   num_pages=pool_pages, mask=mask, **mask_args)
+    return Workload(name, problem, q, torch.tensor(lens, dtype=torch.int32), k=k, v=v,
+                    page_indptr=indptr, page_indices=indices,
+                    meta={"outlier_channels": och, "seed": seed})
+
+
+def contiguous_bf16(name, *, B, S_q, H_q, H_kv, d, lens, T_cap, seed, device, B_cache=None,
+                    cache_batch_idx=None, **extra) -> Workload:
+    """Contiguous NHD cache [B_cache, T_cap, H_kv, d]; rows past each length are NaN."""
+    meta, vals = _gens(seed, device)
+    B_cache = B_cache or B
+    k = _normal_bf16((B_cache, T_cap, H_kv, d), vals, device)
+    v = _normal_bf16((B_cache, T_cap, H_kv, d), vals, device)
+    q = _normal_bf16((B, S_q, H_q, d), vals, device)
+    cbi = list(range(B)) if cache_batch_idx is None else list(cache_batch_idx)
+    used = set()
+    for b, T in enumerate(lens):
+        k[cbi[b], int(T):] = NAN_BF16
+        v[cbi[b], int(T):] = NAN_BF16
+        used.add(cbi[b])
+    for c in range(B_cache):
+        if c not in used:
+            k[c] = NAN_BF16
+            v[c] = NAN_BF16
+    problem = dict(B=B, S_q=S_q, H_q=H_q, H_kv=H_kv, d=d, layout="contig", fmt="bf16",
+                   T_cap=T_cap, B_cache=B_cache, mask="causal", **extra)
+    return Workload(name, problem, q, torch.tensor([int(t) for t in lens], dtype=torch.int32),
+                    k=k, v=v,
+                    cache_batch_idx=None if cache_batch_idx is None
+                    else torch.tensor(cbi, dtype=torch.int32),
+                    meta={"seed": seed})
+
+
+def quantized_history(name, *, B, S_q, H_q, H_kv, d, lens, P, seed, device, fmt,
+                      outliers=True, pool_pages=None) -> Workload:
+    """Packed ragged bf16 history rows [sum T_b, H_kv, d] plus page tables for a cache writer."""
+    meta, vals = _gens(seed, device)
+    lens = [int(t) for t in lens]
+    indptr, indices, pool_pages = _page_tables(lens, P, pool_pages, meta)
+    och = _outlier_channels(H_kv, d, meta) if outliers else None
+    n = sum(lens)
+    k_rows = _normal_bf16((n, H_kv, d), vals, device, (-2, och) if outliers else None)
+    v_rows = _normal_bf16((n, H_kv, d), vals, device)
+    q = _normal_bf16((B, S_q, H_q, d), vals, device)
+    rows_indptr = torch.zeros(B + 1, dtype=torch.int32)
+    rows_indptr[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    problem = dict(B=B, S_q=S_q, H_q=H_q, H_kv=H_kv, d=d, layout="paged", fmt=fmt, P=P,
+                   num_pages=pool_pages, mask="causal", kivi_group=32, kivi_v_group=32,
+                   kivi_residual=128)
+    return Workload(name, problem, q, torch.tensor(lens, dtype=torch.int32),
+                    page_indptr=indptr, page_indices=indices, rows_indptr=rows_indptr,
+                    k_rows=k_rows, v_rows=v_rows, meta={"outlier_channels": och, "seed": seed})
+
+
+def h2o_index_lists(lens, H_kv, budget, n_sink, n_recent, meta):
+    """Per (request, kv head) sorted lists: sinks + recent + top-k by a Gumbel draw.
+
+    The heavy part takes the ``budget - n_sink - n_recent`` positions of
+    [n_sink, F - n_recent) with the largest G = -ln(-ln U), U ~ U(0,1) drawn per
+    position (ties, of probability zero, go to the lower position).
+    """
+    lists, indptr = [], [0]
+    for T in lens:
+        T = int(T)
+        for _ in range(H_kv):
+            sink = torch.arange(0, min(n_sink, T))
+            recent = torch.arange(max(min(n_sink, T), T - n_recent), T)
+            lo, hi = min(n_sink, T), max(min(n_sink, T), T - n_recent)
+            k = max(0, min(budget - len(sink) - len(recent), hi - lo))
+            u = torch.rand(hi - lo, generator=meta, dtype=torch.float64).clamp_min(1e-300)
+            g = -torch.log(-torch.log(u))
+            heavy = lo + torch.topk(g, k, sorted=False).indices if k else torch.arange(0)
+            lst = torch.sort(torch.cat([sink, heavy, recent]).unique()).values
+            lists.append(lst.to(torch.int32))
+            indptr.append(indptr[-1] + len(lst))
+    return torch.tensor(indptr, dtype=torch.int32), torch.cat(lists).contiguous()
+
+
+# ---- the five workloads ------------------------------------------------------
+
+def tiny_contiguous(device="cpu"):
+    return contiguous_bf16("tiny contiguous decode B=1 H_q=8 H_kv=2 d=64 S_k=256", B=1, S_q=1,
+                           H_q=8, H_kv=2, d=64, lens=[256], T_cap=256, seed=0, device=device,
+                           fixed_splits=4)
+
+
+def paged_ragged_gqa(device="cpu", B=16, lo=1024, hi=8192, pool_pages=10000):
+    meta = torch.Generator().manual_seed(1)
+    lens = torch.randint(lo, hi + 1, (B,), generator=meta).tolist()
+    return paged_bf16(f"paged ragged GQA decode B={B} H_q=32 H_kv=8 d=128 P=16 T~U[{lo},{hi}]",
+                      B=B, S_q=1, H_q=32, H_kv=8, d=128, lens=lens, P=16, seed=1, device=device,
+                      pool_pages=pool_pages, outliers=True)
+
+
+def long_context(device="cpu", S_q=1, lens=(131072, 100003, 65537, 1)):
+    return paged_bf16(f"long-context decode B=4 H_q=64 H_kv=8 d=128 P=64 S_q={S_q}", B=len(lens),
+                      S_q=S_q, H_q=64, H_kv=8, d=128, lens=list(lens), P=64, seed=2, device=device)
+
+
+def retention(device="cpu", program="sink_window", B=8, T=32768):
+    lens = [T] * B
+    if program == "sink_window":
+        return paged_bf16(f"sink 4 + window 4096 B={B} T={T}", B=B, S_q=1, H_q=32, H_kv=8, d=128,
+                          lens=lens, P=16, seed=3, device=device, mask="sink_window", n_sink=4,
+                          window=4096)
+    w = paged_bf16(f"H2O-style index lists 2048/kv-head B={B} T={T}", B=B, S_q=1, H_q=32, H_kv=8,
+                   d=128, lens=lens, P=16, seed=3, device=device, mask="index_list")
+    meta = torch.Generator().manual_seed(3 + 77)
+    w.index_indptr, w.index_list = h2o_index_lists(lens, 8, 2048, 64, 512, meta)
+    return w
+
+
+def quantized(device="cpu", fmt="int8", B=32, lo=2048, hi=32768):
+    meta = torch.Generator().manual_seed(4)
+    lens = torch.randint(lo, hi + 1, (B,), generator=meta).tolist()
+    return quantized_history(f"quantized KV ({fmt}) B={B} T~U[{lo},{hi}]", B=B, S_q=1, H_q=32,
+                             H_kv=8, d=128, lens=lens, P=16, seed=4, device=device, fmt=fmt)
