@@ -1,0 +1,285 @@
+/*
+ * dattn.h - C ABI of libdattn, split-KV decode attention for GB300 (sm_103a).
+ *
+ * One or a few query rows per request attend over a long K/V history held in
+ * a contiguous or paged cache, with grouped-query (GQA) heads.  The K/V
+ * sequence axis is cut into chunks; each chunk produces an exact partial
+ * softmax state (m, l, u) and an LSE merge folds the states into the global
+ * softmax ("M4.5 Decode Attention Kernels, Mask Programs, and Backend
+ * Boundaries", §0x01-§0x03).  Retention mask programs ("M5.4 Long-Context KV
+ * Policies", §0x04-§0x06) and quantized K/V formats ("M8.6 Live-Data
+ * Quantization", §0x05-§0x06) run through the same kernels.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns every buffer.  The library never allocates
+ *    device memory; a plan owns only host memory.  Pointers marked "device"
+ *    must be device (or managed) memory, "host" ones host memory.
+ *  - Errors: every call returns a dattn_status.  Nothing aborts, nothing
+ *    throws across the ABI and nothing falls back to another path.  All
+ *    validation runs before any launch or any write to a cache
+ *    (M4.5 §0x07A semantic pre-checks, §0x08C append transaction).
+ *    dattn_last_error() returns a text with every failed check of the last
+ *    failing call on the calling thread (the rejection vector of M4.5 §0x07B).
+ *  - Streams: "stream" is a cudaStream_t passed as void*.  Device work is
+ *    enqueued on it and the library never synchronises the device, except in
+ *    dattn_device_status, which reads back one word.
+ *  - Numbers: scores, maxima, sums and partial states are fp32; O is bf16
+ *    rounded to nearest even; LSE is fp32 in natural-log units.  A query row
+ *    with no visible key gets O = 0 and LSE = -inf (M4.5 §0x02C).
+ */
+#ifndef DATTN_H
+#define DATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DATTN_OK = 0,
+  DATTN_EINVAL = 1,          /* malformed call: a semantic pre-check failed             */
+  DATTN_EUNSUPPORTED = 2,    /* well formed, but outside what this library implements   */
+  DATTN_EWORKSPACE = 3,      /* workspace NULL, too small or not 256-byte aligned        */
+  DATTN_ESTALE_PLAN = 4,     /* run-time problem differs from the plan's key (§0x07F)    */
+  DATTN_ECUDA = 5,           /* a CUDA runtime call or launch failed                     */
+  DATTN_EDEVICE_CHECK = 6    /* a device-side bounds check fired (dattn_device_status)   */
+} dattn_status;
+
+/* K/V storage (M4.5 §0x04B, §0x04D).
+ *  DATTN_KV_CONTIG_NHD: K, V bf16 [B_cache, T_cap, H_kv, d]; request b uses
+ *      cache row cache_batch_idx[b] (b when the pointer is NULL).
+ *  DATTN_KV_PAGED_HND:  pools [num_pages, H_kv, P, d] (format-dependent element,
+ *      see dattn_format); request b's logical block j = t / P lives in page
+ *      page_indices[page_indptr[b] + j] at page row t mod P (CSR page list). */
+typedef enum { DATTN_KV_CONTIG_NHD = 0, DATTN_KV_PAGED_HND = 1 } dattn_layout;
+
+/* K/V element formats (M8.6 §0x05B, §0x06A-B).  Paged layout only for INT8/INT4.
+ *  DATTN_FMT_BF16:       K, V bf16.
+ *  DATTN_FMT_INT8_TOKEN: K, V uint8 codes [num_pages, H_kv, P, d];
+ *      k_qparams, v_qparams fp16 pairs (s, z) [num_pages, H_kv, P, 2], one per
+ *      (token, kv head); x_hat = code * s + z.
+ *  DATTN_FMT_INT4_KIVI:  K, V uint8 [num_pages, H_kv, P, d/2], two 4-bit codes
+ *      per byte, the even channel in the low nibble.
+ *      k_qparams fp16 (s, z) [num_pages, H_kv, max(1, P/G), d, 2]: one pair per
+ *      (G-token group, channel), stored on the page of the group's first token
+ *      at slot (first_token mod P) / G (slot 0 when P < G).
+ *      v_qparams fp16 (s, z) [num_pages, H_kv, P, d/Gv, 2]: per (token, Gv channels).
+ *      k_residual, v_residual bf16 [B, R, H_kv, d]: token t >= n_q(T_b) of
+ *      request b sits in slot t mod R, where n_q(T) = G * ceil(max(0, T - R) / G)
+ *      (the residual holds at most R rows; its oldest G rows close into a
+ *      group while it holds more than R, M8.6 §0x06B). */
+typedef enum { DATTN_FMT_BF16 = 0, DATTN_FMT_INT8_TOKEN = 1, DATTN_FMT_INT4_KIVI = 2 } dattn_format;
+
+/* Visibility programs.  Query row i of request b sits at position
+ * p_i = T_b - S_q + i and has frontier F_i = max(0, min(T_b, p_i + 1))
+ * (bottom-right alignment, M4.5 §0x08B).
+ *  DATTN_MASK_CAUSAL:      keys [0, F_i).
+ *  DATTN_MASK_SINK_WINDOW: keys [0, min(n_sink, F_i)) U [max(0, F_i - window), F_i)
+ *                          (M5.4 §0x05 union, never double counted).
+ *  DATTN_MASK_INDEX_LIST:  keys of the sorted list of (b, h_kv) that are < F_i
+ *                          (per-kv-head retained sets, M5.4 §0x06E shape). */
+typedef enum { DATTN_MASK_CAUSAL = 0, DATTN_MASK_SINK_WINDOW = 1, DATTN_MASK_INDEX_LIST = 2 } dattn_mask_kind;
+
+/* Tile classes of M4.5 §0x05C. */
+typedef enum { DATTN_TILE_SKIP = 0, DATTN_TILE_FULL = 1, DATTN_TILE_PARTIAL = 2 } dattn_tile_class;
+
+/* The static problem: the dispatch/plan key of M4.5 §0x07A and §0x07F. */
+typedef struct {
+  int32_t B;              /* requests (>= 1)                                        */
+  int32_t S_q;            /* query rows per request (>= 1)                          */
+  int32_t H_q, H_kv;      /* heads; H_q % H_kv == 0, g = H_q / H_kv, g * S_q <= 32  */
+  int32_t d_h;            /* head width, 64 or 128 (d_v = d_h)                      */
+  int32_t layout;         /* dattn_layout                                           */
+  int32_t fmt;            /* dattn_format                                           */
+  int32_t page_size;      /* P >= 1 (paged); ignored for contiguous                  */
+  int32_t num_pages;      /* pool pages (paged): every page id must be < num_pages  */
+  int32_t T_cap;          /* token capacity per contiguous cache row                */
+  int32_t B_cache;        /* contiguous cache rows                                  */
+  int32_t kivi_group;     /* G  (INT4 KIVI, K tokens per group), e.g. 32            */
+  int32_t kivi_v_group;   /* Gv (INT4 KIVI, V channels per group), e.g. 32          */
+  int32_t kivi_residual;  /* R  (INT4 KIVI, residual rows), multiple of G           */
+  int32_t mask;           /* dattn_mask_kind                                        */
+  int32_t n_sink;         /* SINK_WINDOW: sink rows (>= 0)                          */
+  int32_t window;         /* SINK_WINDOW: recent rows (>= 1)                        */
+  float   sm_scale;       /* softmax scale; 0 selects 1 / sqrt(d_h)                 */
+  int32_t fixed_splits;   /* > 0: that many balanced splits per (request, kv head)
+                             (M4.5 §0x03B); 0: the planner chooses chunks          */
+} dattn_problem;
+
+/* Host-side inputs of the planner. */
+typedef struct {
+  const int32_t* kv_len;        /* host [B]: stored rows T_b (>= 0)                       */
+  const int32_t* page_indptr;   /* host [B+1] or NULL: checked against ceil(T_b / P)      */
+  const int32_t* index_indptr;  /* host [B*H_kv+1], INDEX_LIST only: list of (b, h_kv) is
+                                   index_list[index_indptr[b*H_kv+h] : ...[b*H_kv+h+1]]  */
+  const int32_t* index_list;    /* host or NULL; when given, every list is checked to be
+                                   strictly increasing and inside [0, T_b)               */
+  int32_t num_sms;              /* SMs to plan for (>= 1)                                 */
+  int32_t ctas_per_sm;          /* resident CTAs per SM to plan for; 0 = library default  */
+  int32_t chunk_tokens;         /* chunk width in keys; 0 = planner default               */
+} dattn_plan_inputs;
+
+typedef struct dattn_plan_s dattn_plan_t;
+
+/* Device buffers of one call.  Unused pointers may be NULL. */
+typedef struct {
+  const void* q;                 /* device bf16 [B, S_q, H_q, d]                          */
+  const void* k;                 /* device K cache (layout / format above)                */
+  const void* v;                 /* device V cache                                        */
+  const void* k_qparams;         /* device, INT8 / INT4 KIVI                              */
+  const void* v_qparams;
+  const void* k_residual;        /* device, INT4 KIVI                                     */
+  const void* v_residual;
+  const int32_t* page_indptr;    /* device [B+1], paged                                   */
+  const int32_t* page_indices;   /* device, paged                                         */
+  const int32_t* cache_batch_idx;/* device [B] or NULL, contiguous                        */
+  const int32_t* index_indptr;   /* device [B*H_kv+1], INDEX_LIST                          */
+  const int32_t* index_list;     /* device, INDEX_LIST                                     */
+  void* o;                       /* device bf16 [B, S_q, H_q, d] (output)                  */
+  float* lse;                    /* device fp32 [B, S_q, H_q] (output) or NULL             */
+} dattn_tensors;
+
+/* Summary of a plan, for reporting (split counts of M4.5 §0x0AC). */
+typedef struct {
+  int64_t workspace_bytes;  /* bytes dattn_run needs                                   */
+  int64_t blob_bytes;       /* of which: work list copied host->device on every run    */
+  int32_t n_items;          /* work items (request, kv head, key chunk)                */
+  int32_t n_ctas;           /* CTAs of the partial kernel                              */
+  int32_t n_slots;          /* partial-state slots (items that do not write O directly) */
+  int32_t n_merge_groups;   /* (request, kv head) groups with more than one item       */
+  int32_t max_splits;       /* largest number of items of one group                    */
+  int32_t rows;             /* query rows per group, g * S_q                           */
+  int64_t stream_keys;      /* keys read by all groups (sum of visible streams)        */
+  int64_t max_cta_keys;     /* keys of the most loaded CTA                             */
+} dattn_plan_info;
+
+/* One work item as planned: keys [a, e) of the visible stream of (b, h_kv).
+ * slot < 0: the item writes O/LSE directly; else it writes partial slot "slot". */
+typedef struct {
+  int32_t b, h_kv, a, e, slot, cta;
+} dattn_work_item;
+
+/* ---- planning (host only; usable without a GPU) ------------------------------------ */
+
+/* Validates the call, builds the visible key stream of every (request, kv
+ * head), cuts it into chunks (balanced quotient/remainder bounds when
+ * fixed_splits > 0, M4.5 §0x03B; otherwise chunks of equal width assigned
+ * longest-first to the least-loaded CTA, the planner of M4.5 §0x09E), and
+ * sizes the workspace (M4.5 §0x03D-§0x03E).  *out receives a plan owned by the
+ * caller (free it with dattn_plan_destroy); *workspace_bytes the bytes that
+ * dattn_run needs.  Returns EINVAL / EUNSUPPORTED with every failed check in
+ * dattn_last_error(). */
+dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_inputs* in,
+                        dattn_plan_t** out, size_t* workspace_bytes);
+
+void dattn_plan_destroy(dattn_plan_t* plan);
+
+/* Copies the plan summary into *info. */
+dattn_status dattn_plan_get_info(const dattn_plan_t* plan, dattn_plan_info* info);
+
+/* Copies up to "capacity" planned items into "items" (host) in item order and
+ * stores the item count in *count. */
+dattn_status dattn_plan_get_items(const dattn_plan_t* plan, dattn_work_item* items,
+                                  int32_t capacity, int32_t* count);
+
+/* ---- execution ---------------------------------------------------------------------- */
+
+/* Runs one decode step: copies the plan's work list into the head of
+ * "workspace" (device, >= info.workspace_bytes, 256-byte aligned), launches
+ * the partial kernel (one producer warp streaming K/V pages through shared
+ * memory with bulk copies, consumer warps updating exact (m, l, u) states)
+ * and, when some group has several chunks, the LSE-merge kernel
+ * (M4.5 §0x03I two-launch schedule).  "prob" must equal the planned problem
+ * (else ESTALE_PLAN).  Device-side bounds checks (page id < num_pages, block
+ * inside the request's page list, list entry inside [0, T_b), cache row <
+ * B_cache) skip the offending rows and raise a flag that dattn_device_status
+ * reports. */
+dattn_status dattn_run(const dattn_plan_t* plan, const dattn_problem* prob,
+                       const dattn_tensors* t, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* dattn_run that also records CUDA events (cudaEvent_t passed as void*, created
+ * by the caller; NULL entries are skipped) on "stream": events[0] before the
+ * partial kernel, events[1] after it, events[2] after the merge kernel.  Used
+ * to time each kernel of the step on the stream it runs on. */
+dattn_status dattn_run_with_events(const dattn_plan_t* plan, const dattn_problem* prob,
+                                   const dattn_tensors* t, void* workspace, size_t workspace_bytes,
+                                   void* stream, void* const* events);
+
+/* Reads the device status word of the last run that used "workspace"
+ * (synchronises "stream").  *flags = 0 when no device check fired. */
+dattn_status dattn_device_status(const void* workspace, int32_t* flags, void* stream);
+
+/* ---- cache writer ---------------------------------------------------------------------- */
+
+typedef struct {
+  const int32_t* kv_len_old;   /* host [B]: committed rows before the append            */
+  const int32_t* new_indptr;   /* host [B+1]: request b appends rows
+                                  new_indptr[b] .. new_indptr[b+1]-1 of k_new / v_new    */
+  const int32_t* page_indptr;  /* host [B+1]: same contents as the device page_indptr   */
+} dattn_append_inputs;
+
+/* Bytes of scratch kv_append needs for B requests. */
+size_t kv_append_workspace_bytes(const dattn_problem* prob);
+
+/* Appends bf16 rows k_new, v_new (device, packed [sum n_b, H_kv, d]) at
+ * positions kv_len_old[b] .. kv_len_old[b] + n_b - 1 of each request, writing
+ * codes and qparams together (M8.6 §0x05B, §0x06B):
+ *  - BF16: rows copied into their pages.
+ *  - INT8: per (token, kv head) s = fp16((max - min) / 255) (fp32 divide),
+ *    z = fp16(min), s = 1 when max == min, s raised to 2^-14 when smaller;
+ *    code = clip(rint_even((x - z) / s), 0, 255) with the re-read stored s, z.
+ *  - INT4 KIVI: every K group of G tokens that closes gets per-channel (s, z)
+ *    with 15 levels, its V rows per-token (s, z) per Gv channels; rows that
+ *    stay inside the residual are written to the residual ring.  The ring must
+ *    hold the request's previous residual rows (as this function leaves them).
+ * Capacity (page list long enough for the new length) and arguments are
+ * checked on the host before any write.  The caller advances its lengths
+ * after the stream reaches this point.  "workspace" (device,
+ * kv_append_workspace_bytes) holds the per-request descriptors. */
+dattn_status kv_append(const dattn_problem* prob, const dattn_append_inputs* in,
+                       const dattn_tensors* cache, const void* k_new, const void* v_new,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- bit-exact debug hooks (same device functions as the kernels) -------------------- */
+
+/* For n coordinates (b, t, h_q, x) (device int32 [n, 4]) writes the element
+ * offset of K[b, t, h_kv(h_q), x] in the K cache (device int64 [n]), or -1 when
+ * the coordinate is outside the request's stored rows or its page list
+ * (M4.5 §0x04A-§0x04F, the four invariants of §0x04H). */
+dattn_status dattn_debug_translate(const dattn_problem* prob, const dattn_tensors* t,
+                                   const int32_t* kv_len, const int32_t* coords, int32_t n,
+                                   int64_t* out, void* stream);
+
+/* For n tiles (b, h_kv, j) (device int32 [n, 3]) writes the exact class
+ * (dattn_tile_class, device int32 [n]) of the tile "every query row of the
+ * group x keys [j P, (j + 1) P)", using the visibility program of "prob"
+ * (M4.5 §0x05C; keys >= T_b are masked).  kv_len is device int32 [B]. */
+dattn_status dattn_debug_classify(const dattn_problem* prob, const dattn_tensors* t,
+                                  const int32_t* kv_len, const int32_t* tiles, int32_t n,
+                                  int32_t* out, void* stream);
+
+/* Writes, for group (b, h_kv), the logical key positions that the planned
+ * items read, in stream order (device int32, capacity entries), and the
+ * number of positions in *count (host).  Uses the plan's work list, which it
+ * copies into "workspace" like dattn_run. */
+dattn_status dattn_debug_gather(const dattn_plan_t* plan, const dattn_problem* prob,
+                                const dattn_tensors* t, void* workspace, size_t workspace_bytes,
+                                int32_t b, int32_t h_kv, int32_t* out, int32_t capacity,
+                                int32_t* count, void* stream);
+
+/* ---- misc ---------------------------------------------------------------------------- */
+
+/* Text listing every failed check of the last failing call on this thread. */
+const char* dattn_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t dattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DATTN_H */

@@ -1,0 +1,320 @@
+"""Python binding of libdattn: split-KV decode attention for GB300 (sm_103a).
+
+A thin ctypes layer over the C ABI declared in ``include/dattn.h``.  Every
+function keeps the C name and only marshals arguments (torch tensors become
+device pointers, dicts become ``dattn_problem``); every step of the decode
+path runs in the library's CUDA kernels.  There is no fallback: when the
+library cannot be built or loaded, or a call fails, a ``DattnError`` is
+raised.  PyTorch only provides device memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+
+from . import build as _build
+
+__all__ = [
+    "DattnError", "Problem", "load", "make_problem", "dattn_plan", "dattn_plan_get_info",
+    "dattn_plan_get_items", "dattn_run", "dattn_run_with_events", "dattn_device_status", "kv_append",
+    "kv_append_workspace_bytes", "dattn_debug_translate", "dattn_debug_classify",
+    "dattn_debug_gather", "dattn_last_error", "dattn_version", "tensors_from", "decode",
+    "LAYOUTS", "FORMATS", "MASKS", "TILE_CLASSES", "STATUS",
+]
+
+STATUS = {0: "DATTN_OK", 1: "DATTN_EINVAL", 2: "DATTN_EUNSUPPORTED", 3: "DATTN_EWORKSPACE",
+          4: "DATTN_ESTALE_PLAN", 5: "DATTN_ECUDA", 6: "DATTN_EDEVICE_CHECK"}
+LAYOUTS = {"contig": 0, "paged": 1}
+FORMATS = {"bf16": 0, "int8": 1, "int4_kivi": 2}
+MASKS = {"causal": 0, "sink_window": 1, "index_list": 2}
+TILE_CLASSES = {0: "SKIP", 1: "FULL", 2: "PARTIAL"}
+
+
+class DattnError(RuntimeError):
+    def __init__(self, status, where, text):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {text}")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "B", "S_q", "H_q", "H_kv", "d_h", "layout", "fmt", "page_size", "num_pages", "T_cap",
+        "B_cache", "kivi_group", "kivi_v_group", "kivi_residual", "mask", "n_sink", "window")] + [
+        ("sm_scale", ctypes.c_float), ("fixed_splits", ctypes.c_int32)]
+
+
+class PlanInputs(ctypes.Structure):
+    _fields_ = [("kv_len", ctypes.c_void_p), ("page_indptr", ctypes.c_void_p),
+                ("index_indptr", ctypes.c_void_p), ("index_list", ctypes.c_void_p),
+                ("num_sms", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+                ("chunk_tokens", ctypes.c_int32)]
+
+
+class Tensors(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "q", "k", "v", "k_qparams", "v_qparams", "k_residual", "v_residual", "page_indptr",
+        "page_indices", "cache_batch_idx", "index_indptr", "index_list", "o", "lse")]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("workspace_bytes", ctypes.c_int64), ("blob_bytes", ctypes.c_int64),
+                ("n_items", ctypes.c_int32), ("n_ctas", ctypes.c_int32), ("n_slots", ctypes.c_int32),
+                ("n_merge_groups", ctypes.c_int32), ("max_splits", ctypes.c_int32),
+                ("rows", ctypes.c_int32), ("stream_keys", ctypes.c_int64),
+                ("max_cta_keys", ctypes.c_int64)]
+
+
+class WorkItem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("b", "h_kv", "a", "e", "slot", "cta")]
+
+
+class AppendInputs(ctypes.Structure):
+    _fields_ = [("kv_len_old", ctypes.c_void_p), ("new_indptr", ctypes.c_void_p),
+                ("page_indptr", ctypes.c_void_p)]
+
+
+_LIB = None
+_VP = ctypes.c_void_p
+_ST = ctypes.c_int
+
+
+def load():
+    """Build (if stale) and load libdattn.so; raises when that is impossible."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.build()
+    lib = ctypes.CDLL(path)
+    sig = {
+        "dattn_plan": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(PlanInputs), ctypes.POINTER(_VP),
+                             ctypes.POINTER(ctypes.c_size_t)]),
+        "dattn_plan_destroy": (None, [_VP]),
+        "dattn_plan_get_info": (_ST, [_VP, ctypes.POINTER(PlanInfo)]),
+        "dattn_plan_get_items": (_ST, [_VP, ctypes.POINTER(WorkItem), ctypes.c_int32,
+                                       ctypes.POINTER(ctypes.c_int32)]),
+        "dattn_run": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP, ctypes.c_size_t, _VP]),
+        "dattn_run_with_events": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP,
+                                        ctypes.c_size_t, _VP, ctypes.POINTER(_VP)]),
+        "dattn_device_status": (_ST, [_VP, ctypes.POINTER(ctypes.c_int32), _VP]),
+        "kv_append_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Problem)]),
+        "kv_append": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(AppendInputs), ctypes.POINTER(Tensors),
+                            _VP, _VP, _VP, ctypes.c_size_t, _VP]),
+        "dattn_debug_translate": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP, _VP,
+                                        ctypes.c_int32, _VP, _VP]),
+        "dattn_debug_classify": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP, _VP,
+                                       ctypes.c_int32, _VP, _VP]),
+        "dattn_debug_gather": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP,
+                                     ctypes.c_size_t, ctypes.c_int32, ctypes.c_int32, _VP, ctypes.c_int32,
+                                     ctypes.POINTER(ctypes.c_int32), _VP]),
+        "dattn_last_error": (ctypes.c_char_p, []),
+        "dattn_version": (ctypes.c_int32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def dattn_last_error() -> str:
+    return load().dattn_last_error().decode()
+
+
+def dattn_version() -> int:
+    return load().dattn_version()
+
+
+def _check(status, where):
+    if status != 0:
+        raise DattnError(status, where, dattn_last_error())
+
+
+def make_problem(d: dict) -> Problem:
+    """dattn_problem from a dict with the keys of ``workloads.Workload.problem``."""
+    p = Problem()
+    p.B, p.S_q, p.H_q, p.H_kv = d["B"], d["S_q"], d["H_q"], d["H_kv"]
+    p.d_h = d["d"]
+    p.layout = LAYOUTS[d.get("layout", "paged")]
+    p.fmt = FORMATS[d.get("fmt", "bf16")]
+    p.page_size = d.get("P", 0)
+    p.num_pages = d.get("num_pages", 0)
+    p.T_cap = d.get("T_cap", 0)
+    p.B_cache = d.get("B_cache", 0)
+    p.kivi_group = d.get("kivi_group", 32)
+    p.kivi_v_group = d.get("kivi_v_group", 32)
+    p.kivi_residual = d.get("kivi_residual", 128)
+    p.mask = MASKS[d.get("mask", "causal")]
+    p.n_sink = d.get("n_sink", 0)
+    p.window = d.get("window", 0)
+    p.sm_scale = d.get("sm_scale", 0.0) or 0.0
+    p.fixed_splits = d.get("fixed_splits", 0)
+    return p
+
+
+def _i32_host(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        return a.ctypes.data
+    return a.data_ptr()
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+class Plan:
+    """Owns a dattn_plan_t; destroyed with the object."""
+
+    def __init__(self, handle, problem, ws_bytes):
+        self.handle = handle
+        self.problem = problem
+        self.workspace_bytes = ws_bytes
+
+    @property
+    def info(self) -> dict:
+        return dattn_plan_get_info(self)
+
+    def items(self):
+        return dattn_plan_get_items(self)
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _LIB is not None:
+            _LIB.dattn_plan_destroy(self.handle)
+            self.handle = None
+
+
+def dattn_plan(problem, kv_len, *, page_indptr=None, index_indptr=None, index_list=None, num_sms=None,
+               ctas_per_sm=0, chunk_tokens=0) -> Plan:
+    """Host-only planning (see dattn_plan in dattn.h).  Arrays are host int32."""
+    lib = load()
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    if num_sms is None:
+        import torch
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    keep = [_i32_host(kv_len), _i32_host(page_indptr), _i32_host(index_indptr), _i32_host(index_list)]
+    inp = PlanInputs(_ptr(keep[0]), _ptr(keep[1]), _ptr(keep[2]), _ptr(keep[3]), int(num_sms),
+                     int(ctas_per_sm), int(chunk_tokens))
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(lib.dattn_plan(ctypes.byref(prob), ctypes.byref(inp), ctypes.byref(handle), ctypes.byref(ws)),
+           "dattn_plan")
+    return Plan(handle, prob, ws.value)
+
+
+def dattn_plan_get_info(plan: Plan) -> dict:
+    info = PlanInfo()
+    _check(load().dattn_plan_get_info(plan.handle, ctypes.byref(info)), "dattn_plan_get_info")
+    return {n: getattr(info, n) for n, _ in PlanInfo._fields_}
+
+
+def dattn_plan_get_items(plan: Plan):
+    lib = load()
+    n = ctypes.c_int32()
+    _check(lib.dattn_plan_get_items(plan.handle, None, 0, ctypes.byref(n)), "dattn_plan_get_items")
+    arr = (WorkItem * max(1, n.value))()
+    _check(lib.dattn_plan_get_items(plan.handle, arr, n.value, ctypes.byref(n)), "dattn_plan_get_items")
+    return [{f: getattr(arr[i], f) for f, _ in WorkItem._fields_} for i in range(n.value)]
+
+
+def tensors_from(**kw) -> Tensors:
+    """dattn_tensors from torch tensors (or None) keyed by the C field names."""
+    t = Tensors()
+    for name, _ in Tensors._fields_:
+        v = kw.pop(name, None)
+        setattr(t, name, None if v is None else v.data_ptr())
+    if kw:
+        raise TypeError(f"unknown tensor fields {sorted(kw)}")
+    return t
+
+
+def dattn_run(plan: Plan, problem, tensors: Tensors, workspace, stream=None) -> None:
+    """Enqueue one decode step on ``stream`` (see dattn_run in dattn.h)."""
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    _check(load().dattn_run(plan.handle, ctypes.byref(prob), ctypes.byref(tensors), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), _stream_ptr(stream)), "dattn_run")
+
+
+def dattn_run_with_events(plan: Plan, problem, tensors: Tensors, workspace, events, stream=None) -> None:
+    """dattn_run that records three caller-created torch.cuda.Events around its kernels
+    (before the partial kernel, after it, after the merge kernel)."""
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    arr = (_VP * 3)(*[None if e is None else ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(load().dattn_run_with_events(plan.handle, ctypes.byref(prob), ctypes.byref(tensors),
+                                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                        _stream_ptr(stream), arr), "dattn_run_with_events")
+
+
+def dattn_device_status(workspace, stream=None) -> int:
+    flags = ctypes.c_int32()
+    st = load().dattn_device_status(workspace.data_ptr(), ctypes.byref(flags), _stream_ptr(stream))
+    if st not in (0, 6):
+        _check(st, "dattn_device_status")
+    return flags.value
+
+
+def kv_append_workspace_bytes(problem) -> int:
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    return load().kv_append_workspace_bytes(ctypes.byref(prob))
+
+
+def kv_append(problem, cache: Tensors, k_new, v_new, kv_len_old, new_indptr, page_indptr, workspace,
+              stream=None) -> None:
+    """Append packed bf16 rows (device) at kv_len_old (host int32 arrays)."""
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    keep = [_i32_host(kv_len_old), _i32_host(new_indptr), _i32_host(page_indptr)]
+    inp = AppendInputs(_ptr(keep[0]), _ptr(keep[1]), _ptr(keep[2]))
+    _check(load().kv_append(ctypes.byref(prob), ctypes.byref(inp), ctypes.byref(cache),
+                            None if k_new is None else k_new.data_ptr(),
+                            None if v_new is None else v_new.data_ptr(),
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _stream_ptr(stream)), "kv_append")
+
+
+def dattn_debug_translate(problem, tensors: Tensors, kv_len_dev, coords_dev, out_dev, stream=None) -> None:
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    _check(load().dattn_debug_translate(ctypes.byref(prob), ctypes.byref(tensors), kv_len_dev.data_ptr(),
+                                        coords_dev.data_ptr(), coords_dev.shape[0], out_dev.data_ptr(),
+                                        _stream_ptr(stream)), "dattn_debug_translate")
+
+
+def dattn_debug_classify(problem, tensors: Tensors, kv_len_dev, tiles_dev, out_dev, stream=None) -> None:
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    _check(load().dattn_debug_classify(ctypes.byref(prob), ctypes.byref(tensors), kv_len_dev.data_ptr(),
+                                       tiles_dev.data_ptr(), tiles_dev.shape[0], out_dev.data_ptr(),
+                                       _stream_ptr(stream)), "dattn_debug_classify")
+
+
+def dattn_debug_gather(plan: Plan, problem, tensors: Tensors, workspace, b, h_kv, out_dev, stream=None) -> int:
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    n = ctypes.c_int32()
+    _check(load().dattn_debug_gather(plan.handle, ctypes.byref(prob), ctypes.byref(tensors), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), int(b), int(h_kv),
+                                     out_dev.data_ptr(), out_dev.numel(), ctypes.byref(n), _stream_ptr(stream)),
+           "dattn_debug_gather")
+    return n.value
+
+
+def decode(problem, plan: Plan, workspace, *, q, o, lse=None, stream=None, **cache) -> None:
+    """Convenience: dattn_run with tensors given as keyword arguments."""
+    dattn_run(plan, problem, tensors_from(q=q, o=o, lse=lse, **cache), workspace, stream)
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

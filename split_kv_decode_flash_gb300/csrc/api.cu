@@ -1,0 +1,329 @@
+// C entry points of libdattn that touch the device: dattn_run,
+// dattn_device_status and the bit-exact debug hooks.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <string>
+
+#include "device.cuh"
+#include "plan.h"
+
+namespace dattn {
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Pointer checks of one call (the tensor part of the admission vector, M4.5 §0x07B).
+void check_tensors(const dattn_problem& p, const dattn_tensors* t, bool need_q_o, Checker& c) {
+  if (!t) {
+    c.fail(DATTN_EINVAL, "tensors are NULL");
+    return;
+  }
+  if (need_q_o) {
+    if (!t->q || !aligned16(t->q)) c.fail(DATTN_EINVAL, "q must be a 16-byte aligned device pointer");
+    if (!t->o || !aligned16(t->o)) c.fail(DATTN_EINVAL, "o must be a 16-byte aligned device pointer");
+  }
+  if (!t->k || !aligned16(t->k)) c.fail(DATTN_EINVAL, "k must be a 16-byte aligned device pointer");
+  if (!t->v || !aligned16(t->v)) c.fail(DATTN_EINVAL, "v must be a 16-byte aligned device pointer");
+  if (p.layout == DATTN_KV_PAGED_HND && (!t->page_indptr || !t->page_indices))
+    c.fail(DATTN_EINVAL, "paged layout needs page_indptr and page_indices");
+  if (p.mask == DATTN_MASK_INDEX_LIST && (!t->index_indptr || !t->index_list))
+    c.fail(DATTN_EINVAL, "index_list mask needs index_indptr and index_list");
+  if (p.fmt != DATTN_FMT_BF16) {
+    if (!t->k_qparams || !t->v_qparams || !aligned16(t->k_qparams) || !aligned16(t->v_qparams))
+      c.fail(DATTN_EINVAL, "quantized formats need 16-byte aligned k_qparams and v_qparams");
+  }
+  if (p.fmt == DATTN_FMT_INT4_KIVI) {
+    if (!t->k_residual || !t->v_residual || !aligned16(t->k_residual) || !aligned16(t->v_residual))
+      c.fail(DATTN_EINVAL, "INT4 KIVI needs 16-byte aligned k_residual and v_residual");
+  }
+}
+
+void fill_common(const dattn_problem& p, const dattn_tensors& t, PartialParams& k) {
+  std::memset(&k, 0, sizeof(k));
+  k.q = t.q;
+  k.k = t.k;
+  k.v = t.v;
+  k.kqp = t.k_qparams;
+  k.vqp = t.v_qparams;
+  k.kres = t.k_residual;
+  k.vres = t.v_residual;
+  k.page_indptr = t.page_indptr;
+  k.page_indices = t.page_indices;
+  k.cache_batch_idx = t.cache_batch_idx;
+  k.index_indptr = t.index_indptr;
+  k.index_list = t.index_list;
+  k.o = t.o;
+  k.lse = t.lse;
+  k.B = p.B;
+  k.S_q = p.S_q;
+  k.H_q = p.H_q;
+  k.H_kv = p.H_kv;
+  k.g = p.H_q / p.H_kv;
+  k.rows = group_rows(p);
+  k.layout = p.layout;
+  k.fmt = p.fmt;
+  k.mask = p.mask;
+  k.P = p.page_size;
+  k.num_pages = p.num_pages;
+  k.T_cap = p.T_cap;
+  k.B_cache = p.B_cache;
+  k.n_sink = p.n_sink;
+  k.window = p.window;
+  k.kivi_G = p.kivi_group;
+  k.kivi_Gv = p.kivi_v_group;
+  k.kivi_R = p.kivi_residual;
+  const float scale = p.sm_scale > 0.f ? p.sm_scale : 1.f / std::sqrt(static_cast<float>(p.d_h));
+  k.scale_log2 = scale * 1.4426950408889634f;
+}
+
+dattn_status cuda_fail(const char* where, int err) {
+  set_error(std::string(where) + ": CUDA error " + cudaGetErrorString(static_cast<cudaError_t>(err)));
+  return DATTN_ECUDA;
+}
+
+// ---- debug kernels (same device functions as the partial kernel) ---------------------
+
+__global__ void translate_kernel(PartialParams p, int d, const int32_t* kv_len, const int32_t* coords, int n,
+                                 int64_t* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int b = coords[4 * i], t = coords[4 * i + 1], hq = coords[4 * i + 2], x = coords[4 * i + 3];
+  long long off = -1;
+  if (b >= 0 && b < p.B && hq >= 0 && hq < p.H_q && x >= 0 && x < d && t >= 0 && t < kv_len[b]) {
+    const int h = hq / p.g;
+    if (p.layout == DATTN_KV_PAGED_HND) {
+      const int pi = page_of(p.page_indptr, p.page_indices, b, t / p.P, p.num_pages, nullptr);
+      if (pi >= 0) off = paged_hnd_offset(pi, t % p.P, h, x, p.P, p.H_kv, d);
+    } else {
+      const int c = cache_row(p.cache_batch_idx, b, p.B_cache, nullptr);
+      if (c >= 0 && t < p.T_cap) off = contig_nhd_offset(c, t, h, x, p.T_cap, p.H_kv, d);
+    }
+  }
+  out[i] = off;
+}
+
+__global__ void classify_kernel(PartialParams p, const int32_t* kv_len, const int32_t* tiles, int n, int width,
+                                int32_t* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int b = tiles[3 * i], h = tiles[3 * i + 1], j = tiles[3 * i + 2];
+  if (b < 0 || b >= p.B || h < 0 || h >= p.H_kv || j < 0) {
+    out[i] = -1;
+    return;
+  }
+  const MaskCtx mc{p.mask, p.S_q, kv_len[b], p.n_sink, p.window};
+  const int32_t* list = nullptr;
+  int list_n = 0;
+  if (p.mask == DATTN_MASK_INDEX_LIST) {
+    const int g = b * p.H_kv + h;
+    list = p.index_list + p.index_indptr[g];
+    list_n = p.index_indptr[g + 1] - p.index_indptr[g];
+  }
+  out[i] = classify_keys(mc, j * width, (j + 1) * width, list, list_n);
+}
+
+__global__ void gather_kernel(PartialParams p, int item, int out_off, int32_t* out, int capacity) {
+  const WorkItem it = p.items[item];
+  for (int j = it.a + threadIdx.x; j < it.e; j += blockDim.x) {
+    const int o = out_off + (j - it.a);
+    if (o < capacity) out[o] = stream_key(it, p.mask, p.index_list, j);
+  }
+}
+
+dattn_status upload_blob(const dattn_plan_t* plan, void* ws, size_t ws_bytes, cudaStream_t s,
+                         PartialParams& k) {
+  const BlobHeader* h = reinterpret_cast<const BlobHeader*>(plan->blob.data());
+  cudaError_t err = cudaMemcpyAsync(ws, plan->blob.data(), plan->blob.size(), cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return cuda_fail("copy of the work list", err);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  k.items = reinterpret_cast<const WorkItem*>(base + h->off_items);
+  k.cta_indptr = reinterpret_cast<const int32_t*>(base + h->off_cta_indptr);
+  k.cta_items = reinterpret_cast<const int32_t*>(base + h->off_cta_items);
+  k.ml = reinterpret_cast<float2*>(base + h->off_ml);
+  k.u = reinterpret_cast<float*>(base + h->off_u);
+  k.status = reinterpret_cast<int32_t*>(base + offsetof(BlobHeader, status));
+  (void)ws_bytes;
+  return DATTN_OK;
+}
+
+dattn_status check_run_args(const dattn_plan_t* plan, const dattn_problem* prob, const dattn_tensors* t,
+                            void* ws, size_t ws_bytes, bool need_q_o, const char* where) {
+  Checker c;
+  if (!plan) c.fail(DATTN_EINVAL, "plan is NULL");
+  check_problem(prob, c);
+  if (c.status != DATTN_OK) return c.finish(where);
+  if (!same_problem(plan->prob, *prob)) {
+    c.fail(DATTN_ESTALE_PLAN, "problem differs from the planned problem");
+    c.status = DATTN_ESTALE_PLAN;
+    return c.finish(where);
+  }
+  check_tensors(*prob, t, need_q_o, c);
+  if (c.status != DATTN_OK) return c.finish(where);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kWsAlign) ||
+      ws_bytes < static_cast<size_t>(plan->info.workspace_bytes)) {
+    c.fail(DATTN_EWORKSPACE, "workspace must be 256-byte aligned and hold " +
+                                 std::to_string(plan->info.workspace_bytes) + " bytes");
+    c.status = DATTN_EWORKSPACE;
+    return c.finish(where);
+  }
+  if (prob->fmt != DATTN_FMT_BF16) {
+    c.fail(DATTN_EUNSUPPORTED, "this build reads bf16 K/V only");
+    return c.finish(where);
+  }
+  return DATTN_OK;
+}
+
+}  // namespace
+}  // namespace dattn
+
+using namespace dattn;
+
+namespace {
+
+dattn_status record(void* const* events, int i, cudaStream_t s) {
+  if (!events || !events[i]) return DATTN_OK;
+  const cudaError_t err = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+  return err == cudaSuccess ? DATTN_OK : cuda_fail("dattn_run_with_events", err);
+}
+
+dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const dattn_tensors* t, void* workspace,
+                      size_t workspace_bytes, void* stream, void* const* events, const char* where) {
+  dattn_status st = check_run_args(plan, prob, t, workspace, workspace_bytes, true, where);
+  if (st != DATTN_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PartialParams k;
+  fill_common(*prob, *t, k);
+  st = upload_blob(plan, workspace, workspace_bytes, s, k);
+  if (st != DATTN_OK) return st;
+  if ((st = record(events, 0, s)) != DATTN_OK) return st;
+  if (plan->info.n_ctas > 0) {
+    const int err = launch_partial(k, prob->d_h, plan->info.n_ctas, stream);
+    if (err != cudaSuccess) return cuda_fail("dattn_run partial kernel", err);
+  }
+  if ((st = record(events, 1, s)) != DATTN_OK) return st;
+  if (plan->info.n_merge_groups > 0) {
+    const BlobHeader* h = reinterpret_cast<const BlobHeader*>(plan->blob.data());
+    MergeParams m{};
+    m.groups = reinterpret_cast<const MergeGroup*>(static_cast<uint8_t*>(workspace) + h->off_merge);
+    m.ml = k.ml;
+    m.u = k.u;
+    m.o = t->o;
+    m.lse = t->lse;
+    m.status = k.status;
+    m.n_groups = plan->info.n_merge_groups;
+    m.rows = k.rows;
+    m.g = k.g;
+    m.S_q = k.S_q;
+    m.H_q = k.H_q;
+    const int err = launch_merge(m, prob->d_h, stream);
+    if (err != cudaSuccess) return cuda_fail("dattn_run merge kernel", err);
+  }
+  return record(events, 2, s);
+}
+
+}  // namespace
+
+extern "C" dattn_status dattn_run(const dattn_plan_t* plan, const dattn_problem* prob, const dattn_tensors* t,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  return run_impl(plan, prob, t, workspace, workspace_bytes, stream, nullptr, "dattn_run");
+}
+
+extern "C" dattn_status dattn_run_with_events(const dattn_plan_t* plan, const dattn_problem* prob,
+                                              const dattn_tensors* t, void* workspace, size_t workspace_bytes,
+                                              void* stream, void* const* events) {
+  return run_impl(plan, prob, t, workspace, workspace_bytes, stream, events, "dattn_run_with_events");
+}
+
+extern "C" dattn_status dattn_device_status(const void* workspace, int32_t* flags, void* stream) {
+  if (!workspace || !flags) {
+    set_error("dattn_device_status: NULL argument");
+    return DATTN_EINVAL;
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemcpyAsync(flags, static_cast<const uint8_t*>(workspace) + offsetof(BlobHeader, status),
+                                    sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return cuda_fail("dattn_device_status", err);
+  return *flags ? DATTN_EDEVICE_CHECK : DATTN_OK;
+}
+
+extern "C" dattn_status dattn_debug_translate(const dattn_problem* prob, const dattn_tensors* t,
+                                              const int32_t* kv_len, const int32_t* coords, int32_t n,
+                                              int64_t* out, void* stream) {
+  Checker c;
+  check_problem(prob, c);
+  if (c.status == DATTN_OK) check_tensors(*prob, t, false, c);
+  if (!kv_len || (n > 0 && (!coords || !out))) c.fail(DATTN_EINVAL, "kv_len, coords and out are required");
+  if (n < 0) c.fail(DATTN_EINVAL, "n must be >= 0");
+  if (c.status != DATTN_OK) return c.finish("dattn_debug_translate");
+  if (n == 0) return DATTN_OK;
+  PartialParams k;
+  fill_common(*prob, *t, k);
+  translate_kernel<<<(n + 127) / 128, 128, 0, static_cast<cudaStream_t>(stream)>>>(k, prob->d_h, kv_len, coords,
+                                                                                   n, out);
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? DATTN_OK : cuda_fail("dattn_debug_translate", err);
+}
+
+extern "C" dattn_status dattn_debug_classify(const dattn_problem* prob, const dattn_tensors* t,
+                                             const int32_t* kv_len, const int32_t* tiles, int32_t n, int32_t* out,
+                                             void* stream) {
+  Checker c;
+  check_problem(prob, c);
+  if (c.status == DATTN_OK && prob->page_size < 1) c.fail(DATTN_EINVAL, "classification tiles are page_size keys wide");
+  if (!kv_len || (n > 0 && (!tiles || !out))) c.fail(DATTN_EINVAL, "kv_len, tiles and out are required");
+  if (c.status == DATTN_OK && prob->mask == DATTN_MASK_INDEX_LIST && (!t || !t->index_indptr || !t->index_list))
+    c.fail(DATTN_EINVAL, "index_list mask needs index_indptr and index_list");
+  if (n < 0) c.fail(DATTN_EINVAL, "n must be >= 0");
+  if (c.status != DATTN_OK) return c.finish("dattn_debug_classify");
+  if (n == 0) return DATTN_OK;
+  PartialParams k;
+  dattn_tensors empty{};
+  fill_common(*prob, t ? *t : empty, k);
+  classify_kernel<<<(n + 127) / 128, 128, 0, static_cast<cudaStream_t>(stream)>>>(k, kv_len, tiles, n,
+                                                                                  prob->page_size, out);
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? DATTN_OK : cuda_fail("dattn_debug_classify", err);
+}
+
+extern "C" dattn_status dattn_debug_gather(const dattn_plan_t* plan, const dattn_problem* prob,
+                                           const dattn_tensors* t, void* workspace, size_t workspace_bytes,
+                                           int32_t b, int32_t h_kv, int32_t* out, int32_t capacity, int32_t* count,
+                                           void* stream) {
+  Checker c;
+  if (!plan) c.fail(DATTN_EINVAL, "plan is NULL");
+  check_problem(prob, c);
+  if (c.status != DATTN_OK) return c.finish("dattn_debug_gather");
+  if (!same_problem(plan->prob, *prob)) {
+    c.fail(DATTN_ESTALE_PLAN, "problem differs from the planned problem");
+    c.status = DATTN_ESTALE_PLAN;
+    return c.finish("dattn_debug_gather");
+  }
+  if (!count || (capacity > 0 && !out) || b < 0 || b >= prob->B || h_kv < 0 || h_kv >= prob->H_kv)
+    c.fail(DATTN_EINVAL, "bad group or output");
+  if (prob->mask == DATTN_MASK_INDEX_LIST && (!t || !t->index_list)) c.fail(DATTN_EINVAL, "index_list is required");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) ||
+      workspace_bytes < static_cast<size_t>(plan->info.workspace_bytes)) {
+    c.fail(DATTN_EWORKSPACE, "workspace too small or misaligned");
+  }
+  if (c.status != DATTN_OK) return c.finish("dattn_debug_gather");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PartialParams k;
+  dattn_tensors empty{};
+  fill_common(*prob, t ? *t : empty, k);
+  dattn_status st = upload_blob(plan, workspace, workspace_bytes, s, k);
+  if (st != DATTN_OK) return st;
+  int total = 0;
+  for (size_t i = 0; i < plan->items.size(); ++i) {
+    const WorkItem& w = plan->items[i];
+    if (w.b != b || w.h != h_kv) continue;
+    if (w.e > w.a) gather_kernel<<<1, 256, 0, s>>>(k, static_cast<int>(i), total, out, capacity);
+    total += w.e - w.a;
+  }
+  *count = total;
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? DATTN_OK : cuda_fail("dattn_debug_gather", err);
+}

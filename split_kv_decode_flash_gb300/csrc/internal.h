@@ -1,0 +1,97 @@
+// Internal definitions shared by the host planner and the CUDA kernels of libdattn.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <vector_types.h>
+
+#include "dattn.h"
+
+namespace dattn {
+
+// ---- kernel geometry ---------------------------------------------------------------
+constexpr int kTK = 64;              // keys per pipeline stage
+constexpr int kStages = 4;           // shared-memory ring depth
+constexpr int kConsumerWarps = 8;    // warps that compute; one more warp produces
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kMaxRows = 32;         // g * S_q rows per (request, kv head) group
+constexpr int kDefaultCtasPerSm = 1;
+constexpr int kWsAlign = 256;
+constexpr uint32_t kBlobMagic = 0x64617474u;  // "datt"
+
+// Device status bits (workspace header word).
+enum StatusBits : int32_t {
+  kStPageRange = 1,     // page id outside [0, num_pages)
+  kStBlockRange = 2,    // logical block outside the request's page list
+  kStListRange = 4,     // index-list entry outside [0, T_b) or list length mismatch
+  kStRowRange = 8,      // contiguous cache row / token outside its capacity
+  kStTimeout = 16,      // a bounded barrier wait gave up
+  kStAppend = 32,       // kv_append met an inconsistent descriptor
+};
+
+// One unit of producer work: keys [a, e) of the visible stream of group (b, h).
+// Interval programs: stream index j maps to position j < x0 ? j : x1 + (j - x0).
+// Index lists: x0 is the list offset of the group, position = index_list[x0 + j].
+struct WorkItem {
+  int32_t b, h, a, e, slot, T, x0, x1;
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+
+struct MergeGroup {
+  int32_t b, h, slot0, n;
+};
+
+// Head of the plan blob, copied to the start of the workspace by every run.
+struct BlobHeader {
+  uint32_t magic;
+  int32_t status;        // device status word, zeroed by the copy
+  int32_t n_items, n_ctas, n_merge, rows, n_slots, pad;
+  int64_t off_items, off_cta_indptr, off_cta_items, off_merge, off_ml, off_u;
+};
+static_assert(sizeof(BlobHeader) == 80, "BlobHeader layout");
+
+// Arguments of the partial kernel (passed by value as a grid constant).
+struct PartialParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* kqp;
+  const void* vqp;
+  const void* kres;
+  const void* vres;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  const int32_t* cache_batch_idx;
+  const int32_t* index_indptr;
+  const int32_t* index_list;
+  void* o;
+  float* lse;
+  const WorkItem* items;
+  const int32_t* cta_indptr;
+  const int32_t* cta_items;
+  float2* ml;            // [n_slots * rows] (m in log2 units, l)
+  float* u;              // [n_slots * rows * d]
+  int32_t* status;
+  int32_t B, S_q, H_q, H_kv, g, rows;
+  int32_t layout, fmt, mask, P, num_pages, T_cap, B_cache;
+  int32_t n_sink, window, kivi_G, kivi_Gv, kivi_R;
+  float scale_log2;      // sm_scale * log2(e)
+};
+
+struct MergeParams {
+  const MergeGroup* groups;
+  const float2* ml;
+  const float* u;
+  void* o;
+  float* lse;
+  int32_t* status;
+  int32_t n_groups, rows, g, S_q, H_q;
+};
+
+// Kernel launchers (partial.cu, merge.cu); return cudaError_t as int.
+int launch_partial(const PartialParams& p, int d, int n_ctas, void* stream);
+int launch_merge(const MergeParams& p, int d, void* stream);
+size_t partial_smem_bytes(int d, int fmt);
+
+}  // namespace dattn

@@ -1,0 +1,360 @@
+// Host planner of libdattn: call validation, visible key streams, chunking,
+// CTA assignment and workspace sizing.  Plain C++, no CUDA calls, so it runs
+// (and is tested) on a machine without a GPU.
+//
+// "M4.5 Decode Attention Kernels, Mask Programs, and Backend Boundaries":
+//  - §0x07A semantic pre-checks and §0x07B the full rejection vector;
+//  - §0x03B balanced quotient/remainder split bounds (fixed split counts) and
+//    fixed-width chunks (planner mode);
+//  - §0x09E / §0x09G the paper planner: chunks no wider than a bound, sorted
+//    longest first and each given to the least-loaded CTA, deterministically;
+//  - §0x0AD request_indices / kv_tile_indices / o_indptr: here the work items
+//    and the merge groups;
+//  - §0x03D-§0x03E workspace: (m, l, u) fp32 per (slot, row), validity
+//    encoded as l = 0 with m = -inf.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "plan.h"
+
+namespace {
+thread_local std::string g_last_error;
+}
+
+namespace dattn {
+
+void set_error(const std::string& s) { g_last_error = s; }
+
+void Checker::fail(dattn_status st, const std::string& why) {
+  if (status == DATTN_OK || (status == DATTN_EUNSUPPORTED && st == DATTN_EINVAL)) status = st;
+  if (!reasons.empty()) reasons += "; ";
+  reasons += why;
+}
+
+dattn_status Checker::finish(const char* where) {
+  if (status != DATTN_OK) set_error(std::string(where) + ": " + reasons);
+  return status;
+}
+
+int group_rows(const dattn_problem& p) { return (p.H_q / std::max(1, p.H_kv)) * p.S_q; }
+
+void check_problem(const dattn_problem* p, Checker& c) {
+  if (!p) {
+    c.fail(DATTN_EINVAL, "problem is NULL");
+    return;
+  }
+  if (p->B < 1) c.fail(DATTN_EINVAL, "B must be >= 1");
+  if (p->S_q < 1) c.fail(DATTN_EINVAL, "S_q must be >= 1 (q_len > 0)");
+  if (p->H_q < 1 || p->H_kv < 1) c.fail(DATTN_EINVAL, "H_q and H_kv must be >= 1");
+  else if (p->H_q % p->H_kv) c.fail(DATTN_EINVAL, "H_q must be a multiple of H_kv (GQA group)");
+  else if (p->S_q >= 1 && group_rows(*p) > kMaxRows)
+    c.fail(DATTN_EUNSUPPORTED, "g * S_q query rows per kv head must be <= 32");
+  if (p->d_h != 64 && p->d_h != 128) c.fail(DATTN_EUNSUPPORTED, "d_h must be 64 or 128");
+  if (p->layout != DATTN_KV_CONTIG_NHD && p->layout != DATTN_KV_PAGED_HND)
+    c.fail(DATTN_EINVAL, "unknown layout");
+  if (p->fmt < DATTN_FMT_BF16 || p->fmt > DATTN_FMT_INT4_KIVI) c.fail(DATTN_EINVAL, "unknown format");
+  if (p->mask < DATTN_MASK_CAUSAL || p->mask > DATTN_MASK_INDEX_LIST) c.fail(DATTN_EINVAL, "unknown mask");
+  if (p->layout == DATTN_KV_PAGED_HND) {
+    if (p->page_size < 1) c.fail(DATTN_EINVAL, "paged layout needs page_size >= 1");
+    if (p->num_pages < 1) c.fail(DATTN_EINVAL, "paged layout needs num_pages >= 1");
+  } else if (p->layout == DATTN_KV_CONTIG_NHD) {
+    if (p->fmt != DATTN_FMT_BF16) c.fail(DATTN_EUNSUPPORTED, "quantized formats need the paged layout");
+    if (p->T_cap < 1) c.fail(DATTN_EINVAL, "contiguous layout needs T_cap >= 1");
+    if (p->B_cache < 1) c.fail(DATTN_EINVAL, "contiguous layout needs B_cache >= 1");
+  }
+  if (p->fmt == DATTN_FMT_INT4_KIVI) {
+    const int G = p->kivi_group, Gv = p->kivi_v_group, R = p->kivi_residual;
+    if (G != 16 && G != 32 && G != 64) c.fail(DATTN_EUNSUPPORTED, "kivi_group must be 16, 32 or 64");
+    if (Gv != 16 && Gv != 32 && Gv != 64 && Gv != 128) c.fail(DATTN_EUNSUPPORTED, "kivi_v_group must be 16, 32, 64 or 128");
+    else if (Gv > p->d_h) c.fail(DATTN_EINVAL, "kivi_v_group must divide d_h");
+    if (G >= 1 && (R < G || R % G)) c.fail(DATTN_EINVAL, "kivi_residual must be a positive multiple of kivi_group");
+    if (G >= 1 && p->page_size >= 1 && p->page_size % G && G % p->page_size)
+      c.fail(DATTN_EUNSUPPORTED, "page_size and kivi_group must divide one another");
+  }
+  if (p->mask == DATTN_MASK_SINK_WINDOW) {
+    if (p->n_sink < 0) c.fail(DATTN_EINVAL, "n_sink must be >= 0");
+    if (p->window < 1) c.fail(DATTN_EINVAL, "window must be >= 1");
+  }
+  if (!(p->sm_scale >= 0.f) || !std::isfinite(p->sm_scale)) c.fail(DATTN_EINVAL, "sm_scale must be finite and >= 0");
+  if (p->fixed_splits < 0) c.fail(DATTN_EINVAL, "fixed_splits must be >= 0");
+}
+
+bool same_problem(const dattn_problem& a, const dattn_problem& b) {
+  return std::memcmp(&a, &b, sizeof(dattn_problem)) == 0;
+}
+
+// Visible key stream of one group: length and the two-interval map.
+static void stream_of(const dattn_problem& p, int T, int list_len, int list_off, int& n, int& x0,
+                      int& x1) {
+  if (p.mask == DATTN_MASK_INDEX_LIST) {
+    n = list_len;
+    x0 = list_off;
+    x1 = 0;
+    return;
+  }
+  if (p.mask == DATTN_MASK_SINK_WINDOW) {
+    // Union over rows of [0, min(n_sink, F_i)) U [max(0, F_i - W), F_i)
+    // with F_i = max(0, min(T, T - S_q + i + 1)); F_i grows with i.
+    const int f_max = std::max(0, T);
+    const int f_min = std::max(0, std::min(T, T - p.S_q + 1));
+    const int sink_end = std::min(p.n_sink, f_max);
+    const int win_start = std::max(0, f_min - p.window);
+    if (win_start <= sink_end) {
+      n = f_max;
+      x0 = f_max;
+      x1 = 0;
+    } else {
+      n = sink_end + (f_max - win_start);
+      x0 = sink_end;
+      x1 = win_start;
+    }
+    return;
+  }
+  n = std::max(0, T);  // causal: union over rows is every stored key
+  x0 = n;
+  x1 = 0;
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace dattn
+
+using namespace dattn;
+
+extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_inputs* in,
+                                   dattn_plan_t** out, size_t* workspace_bytes) {
+  Checker c;
+  check_problem(prob, c);
+  if (!in) c.fail(DATTN_EINVAL, "plan inputs are NULL");
+  if (!out) c.fail(DATTN_EINVAL, "out is NULL");
+  if (c.status != DATTN_OK) return c.finish("dattn_plan");
+  const dattn_problem& p = *prob;
+  if (!in->kv_len) c.fail(DATTN_EINVAL, "kv_len is NULL");
+  if (in->num_sms < 1) c.fail(DATTN_EINVAL, "num_sms must be >= 1");
+  if (in->ctas_per_sm < 0) c.fail(DATTN_EINVAL, "ctas_per_sm must be >= 0");
+  if (in->chunk_tokens < 0) c.fail(DATTN_EINVAL, "chunk_tokens must be >= 0");
+  if (p.mask == DATTN_MASK_INDEX_LIST && !in->index_indptr)
+    c.fail(DATTN_EINVAL, "index_list mask needs index_indptr");
+  if (c.status != DATTN_OK) return c.finish("dattn_plan");
+
+  const int B = p.B, H = p.H_kv;
+  for (int b = 0; b < B; ++b) {
+    const int T = in->kv_len[b];
+    if (T < 0) c.fail(DATTN_EINVAL, "kv_len[" + std::to_string(b) + "] < 0");
+    if (p.layout == DATTN_KV_CONTIG_NHD && T > p.T_cap)
+      c.fail(DATTN_EINVAL, "kv_len[" + std::to_string(b) + "] > T_cap");
+    if (p.layout == DATTN_KV_PAGED_HND && in->page_indptr && T >= 0 && p.page_size >= 1) {
+      const int have = in->page_indptr[b + 1] - in->page_indptr[b];
+      const long need = (static_cast<long>(T) + p.page_size - 1) / p.page_size;
+      if (have < 0) c.fail(DATTN_EINVAL, "page_indptr must be non-decreasing");
+      else if (have < need)
+        c.fail(DATTN_EINVAL, "request " + std::to_string(b) + " has " + std::to_string(have) +
+                                 " pages but needs " + std::to_string(need));
+    }
+    if (p.mask == DATTN_MASK_INDEX_LIST) {
+      for (int h = 0; h < H; ++h) {
+        const int k = b * H + h;
+        const int n = in->index_indptr[k + 1] - in->index_indptr[k];
+        if (n < 0) {
+          c.fail(DATTN_EINVAL, "index_indptr must be non-decreasing");
+          continue;
+        }
+        if (n > std::max(0, T)) c.fail(DATTN_EINVAL, "index list of (" + std::to_string(b) + "," +
+                                                         std::to_string(h) + ") longer than T_b");
+        if (in->index_list) {
+          const int32_t* L = in->index_list + in->index_indptr[k];
+          for (int i = 0; i < n; ++i) {
+            if (L[i] < 0 || L[i] >= T) {
+              c.fail(DATTN_EINVAL, "index list of (" + std::to_string(b) + "," + std::to_string(h) +
+                                       ") has an entry outside [0, T_b)");
+              break;
+            }
+            if (i && L[i] <= L[i - 1]) {
+              c.fail(DATTN_EINVAL, "index list of (" + std::to_string(b) + "," + std::to_string(h) +
+                                       ") is not strictly increasing");
+              break;
+            }
+          }
+        }
+      }
+    }
+  }
+  if (p.mask == DATTN_MASK_INDEX_LIST && in->index_indptr[0] != 0)
+    c.fail(DATTN_EINVAL, "index_indptr[0] must be 0");
+  if (c.status != DATTN_OK) return c.finish("dattn_plan");
+
+  auto* plan = new dattn_plan_s();
+  plan->prob = p;
+  plan->kv_len.assign(in->kv_len, in->kv_len + B);
+  const int rows = group_rows(p);
+  const int n_groups = B * H;
+
+  // 1. visible key stream of every group
+  std::vector<int> gn(n_groups), gx0(n_groups), gx1(n_groups);
+  long long W = 0;
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h) {
+      const int k = b * H + h;
+      int len = 0, off = 0;
+      if (p.mask == DATTN_MASK_INDEX_LIST) {
+        off = in->index_indptr[k];
+        len = in->index_indptr[k + 1] - off;
+      }
+      stream_of(p, in->kv_len[b], len, off, gn[k], gx0[k], gx1[k]);
+      W += gn[k];
+    }
+
+  // 2. chunks
+  const int cps = in->ctas_per_sm > 0 ? in->ctas_per_sm : kDefaultCtasPerSm;
+  const long long cta_target = static_cast<long long>(in->num_sms) * cps;
+  long long L = in->chunk_tokens;
+  if (L <= 0) {
+    const long long per = (W + 4 * cta_target - 1) / (4 * cta_target);
+    L = std::max<long long>(kTK, (per + kTK - 1) / kTK * kTK);
+  }
+  std::vector<int> group_first(n_groups + 1, 0);
+  auto& items = plan->items;
+  for (int k = 0; k < n_groups; ++k) {
+    group_first[k] = static_cast<int>(items.size());
+    const int b = k / H, h = k % H, n = gn[k];
+    auto add = [&](int a, int e) {
+      items.push_back(WorkItem{b, h, a, e, -1, plan->kv_len[b], gx0[k], gx1[k]});
+    };
+    if (p.fixed_splits > 0) {
+      const int S = p.fixed_splits, q = n / S, r = n % S;
+      for (int s = 0; s < S; ++s) {
+        const int a = s * q + std::min(s, r);
+        add(a, a + q + (s < r ? 1 : 0));
+      }
+    } else if (n == 0) {
+      add(0, 0);
+    } else {
+      for (long long a = 0; a < n; a += L) add(static_cast<int>(a), static_cast<int>(std::min<long long>(n, a + L)));
+    }
+  }
+  group_first[n_groups] = static_cast<int>(items.size());
+
+  // 3. partial slots and merge groups (o_indptr)
+  std::vector<MergeGroup> merges;
+  int n_slots = 0, max_splits = 0;
+  for (int k = 0; k < n_groups; ++k) {
+    const int n = group_first[k + 1] - group_first[k];
+    max_splits = std::max(max_splits, n);
+    if (n > 1) {
+      merges.push_back(MergeGroup{k / H, k % H, n_slots, n});
+      for (int i = 0; i < n; ++i) items[group_first[k] + i].slot = n_slots + i;
+      n_slots += n;
+    }
+  }
+
+  // 4. longest-first, least-loaded CTA assignment (deterministic ties)
+  const int n_items = static_cast<int>(items.size());
+  const int n_ctas = static_cast<int>(std::min<long long>(cta_target, n_items));
+  std::vector<int> order(n_items);
+  for (int i = 0; i < n_items; ++i) order[i] = i;
+  auto cost = [&](int i) { return static_cast<long long>(items[i].e - items[i].a) + 16; };
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost(x) > cost(y); });
+  using Slot = std::pair<long long, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int cta = 0; cta < n_ctas; ++cta) heap.push({0, cta});
+  std::vector<std::vector<int>> per_cta(n_ctas);
+  std::vector<long long> keys_of(n_ctas, 0);
+  plan->item_cta.assign(n_items, 0);
+  for (int i : order) {
+    auto [load, cta] = heap.top();
+    heap.pop();
+    per_cta[cta].push_back(i);
+    plan->item_cta[i] = cta;
+    keys_of[cta] += items[i].e - items[i].a;
+    heap.push({load + cost(i), cta});
+  }
+
+  // 5. blob and workspace
+  BlobHeader hdr{};
+  hdr.magic = kBlobMagic;
+  hdr.n_items = n_items;
+  hdr.n_ctas = n_ctas;
+  hdr.n_merge = static_cast<int>(merges.size());
+  hdr.rows = rows;
+  hdr.n_slots = n_slots;
+  size_t off = align_up(sizeof(BlobHeader), 16);
+  hdr.off_items = off;
+  off = align_up(off + sizeof(WorkItem) * n_items, 16);
+  hdr.off_cta_indptr = off;
+  off = align_up(off + sizeof(int32_t) * (n_ctas + 1), 16);
+  hdr.off_cta_items = off;
+  off = align_up(off + sizeof(int32_t) * n_items, 16);
+  hdr.off_merge = off;
+  off = align_up(off + sizeof(MergeGroup) * merges.size(), kWsAlign);
+  const size_t blob_bytes = off;
+  hdr.off_ml = off;
+  off = align_up(off + sizeof(float) * 2 * static_cast<size_t>(n_slots) * rows, kWsAlign);
+  hdr.off_u = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(n_slots) * rows * p.d_h, kWsAlign);
+  const size_t ws_bytes = off;
+
+  plan->blob.assign(blob_bytes, 0);
+  uint8_t* base = plan->blob.data();
+  std::memcpy(base, &hdr, sizeof(hdr));
+  std::memcpy(base + hdr.off_items, items.data(), sizeof(WorkItem) * n_items);
+  auto* cta_indptr = reinterpret_cast<int32_t*>(base + hdr.off_cta_indptr);
+  auto* cta_items = reinterpret_cast<int32_t*>(base + hdr.off_cta_items);
+  int pos = 0;
+  for (int cta = 0; cta < n_ctas; ++cta) {
+    cta_indptr[cta] = pos;
+    for (int i : per_cta[cta]) cta_items[pos++] = i;
+  }
+  cta_indptr[n_ctas] = pos;
+  if (!merges.empty()) std::memcpy(base + hdr.off_merge, merges.data(), sizeof(MergeGroup) * merges.size());
+
+  dattn_plan_info& info = plan->info;
+  info.workspace_bytes = static_cast<int64_t>(ws_bytes);
+  info.blob_bytes = static_cast<int64_t>(blob_bytes);
+  info.n_items = n_items;
+  info.n_ctas = n_ctas;
+  info.n_slots = n_slots;
+  info.n_merge_groups = static_cast<int>(merges.size());
+  info.max_splits = max_splits;
+  info.rows = rows;
+  info.stream_keys = W;
+  info.max_cta_keys = keys_of.empty() ? 0 : *std::max_element(keys_of.begin(), keys_of.end());
+
+  *out = plan;
+  if (workspace_bytes) *workspace_bytes = ws_bytes;
+  return DATTN_OK;
+}
+
+extern "C" void dattn_plan_destroy(dattn_plan_t* plan) { delete plan; }
+
+extern "C" dattn_status dattn_plan_get_info(const dattn_plan_t* plan, dattn_plan_info* info) {
+  if (!plan || !info) {
+    set_error("dattn_plan_get_info: NULL argument");
+    return DATTN_EINVAL;
+  }
+  *info = plan->info;
+  return DATTN_OK;
+}
+
+extern "C" dattn_status dattn_plan_get_items(const dattn_plan_t* plan, dattn_work_item* items,
+                                             int32_t capacity, int32_t* count) {
+  if (!plan || !count || (capacity > 0 && !items)) {
+    set_error("dattn_plan_get_items: NULL argument");
+    return DATTN_EINVAL;
+  }
+  const int n = static_cast<int>(plan->items.size());
+  *count = n;
+  for (int i = 0; i < std::min(n, capacity); ++i) {
+    const WorkItem& w = plan->items[i];
+    items[i] = dattn_work_item{w.b, w.h, w.a, w.e, w.slot, plan->item_cta[i]};
+  }
+  return DATTN_OK;
+}
+
+extern "C" const char* dattn_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int32_t dattn_version(void) { return 100; }

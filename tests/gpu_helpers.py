@@ -1,0 +1,127 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI,
+build the oracle's view of the same inputs, compare within the tolerance.
+
+Tolerance (bf16 output, fp32 LSE), fixed by the decode contract:
+  |O - O_ref| <= 4e-3 + 1e-2 |O_ref|  elementwise;
+  |LSE - LSE_ref| <= 1e-4 max(1, |LSE_ref|);
+  rows without a visible key: O exactly 0 and LSE exactly -inf on both sides.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import split_kv_decode_flash_gb300 as dattn
+from oracle import attention
+from oracle import cache as ocache
+
+O_ATOL, O_RTOL, LSE_RTOL = 4e-3, 1e-2, 1e-4
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 bit patterns on the host."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_cache(w) -> ocache.Cache:
+    p = w.problem
+    if p["layout"] == "contig":
+        c = ocache.Cache("contig", "bf16", p["H_kv"], p["d"], T_c=p["T_cap"], k=bits(w.k), v=bits(w.v),
+                         kv_len=w.kv_len.numpy().astype(np.int64))
+        if w.cache_batch_idx is not None:
+            c.cache_batch_idx = w.cache_batch_idx.numpy()
+        return c
+    return ocache.Cache("paged", "bf16", p["H_kv"], p["d"], P=p["P"], k=bits(w.k), v=bits(w.v),
+                        page_indptr=w.page_indptr.numpy().astype(np.int64),
+                        page_indices=w.page_indices.numpy().astype(np.int64),
+                        kv_len=w.kv_len.numpy().astype(np.int64))
+
+
+def oracle_problem(w) -> dict:
+    p = dict(w.problem)
+    if w.index_list is not None:
+        p["index_indptr"] = w.index_indptr.numpy()
+        p["index_list"] = w.index_list.numpy()
+    return p
+
+
+def device_tensors(w, o, lse, dev="cuda"):
+    kw = dict(q=w.q.to(dev), k=w.k.to(dev), v=w.v.to(dev), o=o, lse=lse)
+    if w.page_indptr is not None:
+        kw["page_indptr"] = w.page_indptr.to(dev)
+        kw["page_indices"] = w.page_indices.to(dev)
+    if w.cache_batch_idx is not None:
+        kw["cache_batch_idx"] = w.cache_batch_idx.to(dev)
+    if w.index_list is not None:
+        kw["index_indptr"] = w.index_indptr.to(dev)
+        kw["index_list"] = w.index_list.to(dev)
+    return kw
+
+
+def run_gpu(w, *, num_sms=None, ctas_per_sm=0, chunk_tokens=0, problem=None, keep=None):
+    """One dattn_run over workload ``w``; returns (O fp32 cpu, LSE cpu, plan info, status flags)."""
+    p = problem or w.problem
+    B, S_q, H_q, d = p["B"], p["S_q"], p["H_q"], p["d"]
+    plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, index_indptr=w.index_indptr,
+                            index_list=w.index_list, num_sms=num_sms, ctas_per_sm=ctas_per_sm,
+                            chunk_tokens=chunk_tokens)
+    o = torch.full((B, S_q, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, S_q, H_q), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(256, plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+    kw = device_tensors(w, o, lse)
+    dattn.dattn_run(plan, p, dattn.tensors_from(**kw), ws)
+    torch.cuda.synchronize()
+    flags = dattn.dattn_device_status(ws)
+    if keep is not None:
+        keep.update(plan=plan, ws=ws, kw=kw)
+    return o.float().cpu(), lse.cpu(), plan.info, flags
+
+
+def all_rows(p):
+    return [(b, i, h) for b in range(p["B"]) for i in range(p["S_q"]) for h in range(p["H_q"])]
+
+
+def compare(O, LSE, w, rows=None, cache=None):
+    """Element-by-element comparison of the GPU rows against the oracle; returns max errors."""
+    p = oracle_problem(w)
+    rows = rows or all_rows(p)
+    cache = cache or oracle_cache(w)
+    Oref, Lref = attention.decode_rows(p, cache, bits(w.q), rows)
+    og = np.stack([O[b, i, h].numpy() for b, i, h in rows]).astype(np.float64)
+    lg = np.array([LSE[b, i, h].item() for b, i, h in rows], dtype=np.float64)
+    masked = np.isneginf(Lref)
+    assert np.array_equal(np.isneginf(lg), masked), "all-masked rows differ"
+    assert not og[masked].any(), "masked rows must give exactly zero output"
+    assert np.isfinite(og).all(), "non-finite output"
+    err = np.abs(og - Oref)
+    bound = O_ATOL + O_RTOL * np.abs(Oref)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), f"O error {err[worst]:.3g} > {bound[worst]:.3g} at row {rows[worst[0]]}"
+    fin = ~masked
+    lerr = np.abs(lg[fin] - Lref[fin])
+    assert (lerr <= LSE_RTOL * np.maximum(1.0, np.abs(Lref[fin]))).all(), f"LSE error {lerr.max():.3g}"
+    return {"max_abs_O": float(err.max()), "max_abs_LSE": float(lerr.max()) if lerr.size else 0.0,
+            "rows": len(rows)}
+
+
+def sample_rows(p, n, seed=0, must=()):
+    rng = np.random.default_rng(seed)
+    rows = set(must)
+    allr = all_rows(p)
+    for k in rng.choice(len(allr), size=min(n, len(allr)), replace=False):
+        rows.add(allr[k])
+    return sorted(rows)
+
+
+def finite_or_masked(O, LSE):
+    o = O.numpy()
+    assert np.isfinite(o).all()
+    assert not np.isnan(LSE.numpy()).any()
+    return True
+
+
+def inf():
+    return math.inf

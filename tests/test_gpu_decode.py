@@ -1,0 +1,249 @@
+"""GPU parity of the decode path (bf16 K/V) against the fp64 oracle, through the C ABI.
+
+Small cases are compared on every output row; the full-size workloads (the
+launch configuration the benchmark times) on sampled rows, plus
+"every output finite or exactly masked" over all rows.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import split_kv_decode_flash_gb300 as dattn
+import workloads as W
+from oracle import address, masks
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dattn.load()
+
+
+def test_tiny_contiguous_four_fixed_splits():
+    w = W.tiny_contiguous("cuda")
+    O, L, info, flags = H.run_gpu(w)
+    assert flags == 0
+    assert info["n_items"] == 2 * 4 and info["n_merge_groups"] == 2 and info["max_splits"] == 4
+    H.compare(O, L, w)
+
+
+@pytest.mark.parametrize("chunk,num_sms", [(0, 152), (64, 7), (128, 3), (192, 152), (100000, 152)])
+def test_paged_ragged_small_all_rows(chunk, num_sms):
+    w = W.paged_ragged_gqa("cuda", B=5, lo=1, hi=700, pool_pages=400)
+    O, L, info, flags = H.run_gpu(w, chunk_tokens=chunk, num_sms=num_sms)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+def test_paged_ragged_full_size_sampled_rows():
+    w = W.paged_ragged_gqa("cuda")
+    O, L, info, flags = H.run_gpu(w)
+    assert flags == 0 and info["n_merge_groups"] > 0
+    H.finite_or_masked(O, L)
+    rows = H.sample_rows(w.problem, 96, seed=1, must=[(0, 0, 0), (15, 0, 31)])
+    H.compare(O, L, w, rows)
+
+
+@pytest.mark.parametrize("lens,P,fixed", [([0, 1, 2, 17], 16, 0), ([0, 3, 5], 16, 8), ([33, 1, 64], 1, 0),
+                                          ([200, 129, 64], 64, 3), ([1000], 16, 64)])
+def test_edge_lengths_pages_and_splits(lens, P, fixed):
+    pool = sum(-(-t // P) for t in lens) + 3
+    w = W.paged_bf16("edge", B=len(lens), S_q=1, H_q=8, H_kv=2, d=128, lens=lens, P=P, seed=9, device="cuda",
+                     pool_pages=pool, fixed_splits=fixed)
+    O, L, info, flags = H.run_gpu(w, num_sms=5, chunk_tokens=64)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+def test_head_width_64_paged():
+    w = W.paged_bf16("d64", B=3, S_q=1, H_q=16, H_kv=4, d=64, lens=[300, 77, 1], P=16, seed=5, device="cuda",
+                     pool_pages=60)
+    O, L, info, flags = H.run_gpu(w, num_sms=4, chunk_tokens=128)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+def test_contiguous_cache_row_remap_and_capacity_tail():
+    w = W.contiguous_bf16("remap", B=3, S_q=1, H_q=8, H_kv=2, d=64, lens=[100, 7, 64], T_cap=128, seed=6,
+                          device="cuda", B_cache=5, cache_batch_idx=[4, 0, 2])
+    O, L, info, flags = H.run_gpu(w, num_sms=3, chunk_tokens=64)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+@pytest.mark.parametrize("S_q,lens", [(4, [1, 2, 3, 4, 70]), (2, [1, 65]), (3, [130, 5])])
+def test_causal_verify_rows_small(S_q, lens):
+    w = W.paged_bf16("verify", B=len(lens), S_q=S_q, H_q=16, H_kv=2, d=128, lens=lens, P=16, seed=7,
+                     device="cuda", pool_pages=sum(-(-t // 16) for t in lens) + 2)
+    O, L, info, flags = H.run_gpu(w, num_sms=4, chunk_tokens=64)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+@pytest.mark.parametrize("S_q", [1, 4])
+def test_long_context_full_size_sampled(S_q):
+    w = W.long_context("cuda", S_q=S_q)
+    O, L, info, flags = H.run_gpu(w)
+    assert flags == 0
+    H.finite_or_masked(O, L)
+    must = [(3, i, h) for i in range(S_q) for h in (0, 63)] + [(0, S_q - 1, 5), (2, 0, 40)]
+    H.compare(O, L, w, H.sample_rows(w.problem, 24, seed=2, must=must))
+    if S_q == 4:      # request of length 1: rows 0..2 see nothing
+        assert np.isneginf(L[3, :3].numpy()).all() and not O[3, :3].any()
+
+
+@pytest.mark.parametrize("n_sink,window,lens", [(4, 64, [5, 60, 64, 65, 300]), (0, 16, [40, 1]),
+                                                (3, 100, [1000, 99])])
+def test_sink_window_small(n_sink, window, lens):
+    w = W.paged_bf16("sw", B=len(lens), S_q=1, H_q=8, H_kv=2, d=128, lens=lens, P=16, seed=8, device="cuda",
+                     pool_pages=sum(-(-t // 16) for t in lens) + 2, mask="sink_window", n_sink=n_sink,
+                     window=window)
+    O, L, info, flags = H.run_gpu(w, num_sms=3, chunk_tokens=64)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+def test_sink_window_multi_row():
+    w = W.paged_bf16("sw4", B=2, S_q=4, H_q=8, H_kv=2, d=128, lens=[90, 6], P=16, seed=10, device="cuda",
+                     pool_pages=12, mask="sink_window", n_sink=2, window=9)
+    O, L, info, flags = H.run_gpu(w, num_sms=2, chunk_tokens=64)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+def test_retention_sink_window_full_size_sampled():
+    w = W.retention("cuda", "sink_window")
+    O, L, info, flags = H.run_gpu(w)
+    assert flags == 0 and info["stream_keys"] == 8 * 8 * 4100
+    H.finite_or_masked(O, L)
+    H.compare(O, L, w, H.sample_rows(w.problem, 32, seed=3))
+
+
+def test_index_lists_small():
+    w = W.retention("cuda", "index_list", B=3, T=3000)
+    O, L, info, flags = H.run_gpu(w, num_sms=5, chunk_tokens=128)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+def test_index_lists_full_size_sampled():
+    w = W.retention("cuda", "index_list")
+    O, L, info, flags = H.run_gpu(w)
+    assert flags == 0 and info["stream_keys"] == 8 * 8 * 2048
+    H.finite_or_masked(O, L)
+    H.compare(O, L, w, H.sample_rows(w.problem, 32, seed=4))
+
+
+# ---- bit-exact debug hooks --------------------------------------------------------------
+
+def test_debug_translate_matches_oracle_offsets():
+    w = W.paged_ragged_gqa("cuda", B=3, lo=1, hi=90, pool_pages=40)
+    p = w.problem
+    rng = np.random.default_rng(0)
+    coords = []
+    for _ in range(3000):
+        b = int(rng.integers(0, p["B"]))
+        coords.append([b, int(rng.integers(-2, int(w.kv_len[b]) + 3)), int(rng.integers(0, p["H_q"])),
+                       int(rng.integers(0, p["d"]))])
+    c = torch.tensor(coords, dtype=torch.int32, device="cuda")
+    out = torch.empty(len(coords), dtype=torch.int64, device="cuda")
+    t = dattn.tensors_from(**H.device_tensors(w, None, None))
+    dattn.dattn_debug_translate(p, t, w.kv_len.cuda(), c, out)
+    got = out.cpu().numpy()
+    ind, ptr = w.page_indices.numpy(), w.page_indptr.numpy()
+    for (b, tt, hq, x), g in zip(coords, got):
+        if 0 <= tt < int(w.kv_len[b]):
+            pi = address.page_csr(ptr, ind, b, tt // p["P"])
+            want = address.offset_paged_hnd(pi, tt % p["P"], address.kv_head(hq, p["H_q"], p["H_kv"]), x,
+                                            p["P"], p["H_kv"], p["d"])
+        else:
+            want = -1
+        assert g == want
+
+
+def test_debug_translate_contiguous_remap():
+    w = W.contiguous_bf16("remap", B=2, S_q=1, H_q=4, H_kv=2, d=64, lens=[12, 5], T_cap=12, seed=1,
+                          device="cuda", B_cache=4, cache_batch_idx=[2, 0])
+    p = w.problem
+    coords = [[0, 3, 3, 2], [1, 4, 0, 63], [1, 5, 0, 0]]
+    out = torch.empty(3, dtype=torch.int64, device="cuda")
+    dattn.dattn_debug_translate(p, dattn.tensors_from(**H.device_tensors(w, None, None)), w.kv_len.cuda(),
+                                torch.tensor(coords, dtype=torch.int32, device="cuda"), out)
+    got = out.cpu().tolist()
+    assert got[0] == address.offset_contig_nhd(2, 3, 1, 2, 12, 2, 64)
+    assert got[1] == address.offset_contig_nhd(0, 4, 0, 63, 12, 2, 64)
+    assert got[2] == -1
+
+
+@pytest.mark.parametrize("mask,S_q,extra", [("causal", 4, {}), ("sink_window", 1, dict(n_sink=4, window=4096)),
+                                            ("sink_window", 3, dict(n_sink=5, window=20)),
+                                            ("index_list", 1, {}), ("index_list", 2, {})])
+def test_debug_classify_matches_oracle_tile_classes(mask, S_q, extra):
+    lens = [5000, 17, 0, 4100]
+    w = W.paged_bf16("cls", B=4, S_q=S_q, H_q=8, H_kv=2, d=128, lens=lens, P=16, seed=2, device="cuda",
+                     pool_pages=sum(-(-t // 16) for t in lens), mask=mask, **extra)
+    if mask == "index_list":
+        meta = torch.Generator().manual_seed(5)
+        w.index_indptr, w.index_list = W.h2o_index_lists(lens, 2, 300, 8, 40, meta)
+    p = H.oracle_problem(w)
+    tiles, want = [], []
+    for b, T in enumerate(lens):
+        for h in range(2):
+            lst = None
+            if mask == "index_list":
+                k = b * 2 + h
+                lst = p["index_list"][p["index_indptr"][k]:p["index_indptr"][k + 1]]
+            sets = [masks.visible_positions(mask, T, S_q, i, n_sink=extra.get("n_sink", 0),
+                                            window=extra.get("window", 0), index_list=lst) for i in range(S_q)]
+            for j in range(0, T // 16 + 2):
+                tiles.append([b, h, j])
+                want.append(masks.tile_class(sets, 16 * j, 16 * (j + 1)))
+    out = torch.empty(len(tiles), dtype=torch.int32, device="cuda")
+    dattn.dattn_debug_classify(w.problem, dattn.tensors_from(**H.device_tensors(w, None, None)), w.kv_len.cuda(),
+                               torch.tensor(tiles, dtype=torch.int32, device="cuda"), out)
+    got = [dattn.TILE_CLASSES[x] for x in out.cpu().tolist()]
+    assert got == want
+
+
+@pytest.mark.parametrize("mask", ["causal", "sink_window", "index_list"])
+def test_debug_gather_equals_visible_union(mask):
+    lens = [3000, 5, 4200]
+    extra = dict(n_sink=4, window=1000) if mask == "sink_window" else {}
+    w = W.paged_bf16("gather", B=3, S_q=2, H_q=8, H_kv=2, d=128, lens=lens, P=16, seed=3, device="cuda",
+                     pool_pages=sum(-(-t // 16) for t in lens), mask=mask, **extra)
+    if mask == "index_list":
+        w.index_indptr, w.index_list = W.h2o_index_lists(lens, 2, 500, 8, 64, torch.Generator().manual_seed(6))
+    keep = {}
+    H.run_gpu(w, num_sms=3, chunk_tokens=256, keep=keep)
+    p = H.oracle_problem(w)
+    out = torch.empty(5000, dtype=torch.int32, device="cuda")
+    for b, T in enumerate(lens):
+        for h in range(2):
+            n = dattn.dattn_debug_gather(keep["plan"], w.problem, dattn.tensors_from(**keep["kw"]), keep["ws"], b, h,
+                                         out)
+            got = out[:n].cpu().numpy()
+            lst = None
+            if mask == "index_list":
+                k = b * 2 + h
+                lst = p["index_list"][p["index_indptr"][k]:p["index_indptr"][k + 1]]
+            want = np.unique(np.concatenate([masks.visible_positions(mask, T, 2, i, n_sink=extra.get("n_sink", 0),
+                                                                     window=extra.get("window", 0), index_list=lst)
+                                             for i in range(2)]))
+            assert np.array_equal(got, want)
+
+
+def test_device_bounds_check_flags_out_of_pool_page_without_reading_it():
+    """A page id >= num_pages is caught by the kernel's own check before any address is formed."""
+    w = W.paged_bf16("oob", B=2, S_q=1, H_q=8, H_kv=2, d=128, lens=[40, 40], P=16, seed=4, device="cuda",
+                     pool_pages=6)
+    w.page_indices = w.page_indices.clone()
+    w.page_indices[1] = 6          # one past the pool: request 0, logical block 1
+    O, L, info, flags = H.run_gpu(w, num_sms=2)
+    assert flags & 1               # kStPageRange
+    # request 1 is untouched by the bad entry and still matches the oracle
+    H.compare(O, L, w, [(1, 0, h) for h in range(8)])

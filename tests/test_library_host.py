@@ -1,0 +1,229 @@
+"""Host-side tests of libdattn (no GPU): exports, planner pins, call validation.
+
+The planner is plain host code, so its split bounds, chunking, CTA
+assignment and workspace sizing are checked here against the pages' printed
+values (M4.5 §0x03B, §0x03E, §0x03G, §0x09G) and against the oracle's
+visible sets.  Each validation gets a one-field-mutation negative test
+(M4.5 §0x07A-§0x07B).
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import split_kv_decode_flash_gb300 as dattn
+from oracle import masks
+from oracle import split_state as ss
+from tests.conftest import ROOT, golden
+
+HEADER = os.path.join(ROOT, "include", "dattn.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_]+)\s*\(", text)) - {"sizeof"})
+
+
+def test_library_exports_every_declared_symbol():
+    lib = dattn.load()
+    names = _declared_functions()
+    assert "dattn_plan" in names and "dattn_run" in names and "kv_append" in names
+    for n in names:
+        assert hasattr(lib, n), f"libdattn.so does not export {n}"
+    assert dattn.dattn_version() >= 100
+
+
+def _problem(**kw):
+    base = dict(B=2, S_q=1, H_q=8, H_kv=2, d=128, layout="paged", fmt="bf16", P=16, num_pages=1000,
+                mask="causal")
+    base.update(kw)
+    return base
+
+
+def _coverage(items, groups, n_of):
+    by = {}
+    for it in items:
+        by.setdefault((it["b"], it["h_kv"]), []).append((it["a"], it["e"]))
+    assert set(by) == set(groups)
+    for g, ranges in by.items():
+        ranges.sort()
+        pos = 0
+        for a, e in ranges:
+            assert a == pos and e >= a
+            pos = e
+        assert pos == n_of(g)
+
+
+def test_fixed_split_bounds_match_balanced_formula():
+    g = golden("split_ledgers.json")
+    T = g["call"]["T"]
+    plan = dattn.dattn_plan(_problem(fixed_splits=8), T, num_sms=152)
+    items = plan.items()
+    for b, t in enumerate(T):
+        got = [(it["a"], it["e"]) for it in items if it["b"] == b and it["h_kv"] == 0]
+        assert got == ss.balanced_split_bounds(t, 8)
+        assert [e - a for a, e in got] == g["split_lengths"][str(t)]
+    info = plan.info
+    assert info["n_items"] == 2 * 2 * 8 and info["n_merge_groups"] == 4 and info["max_splits"] == 8
+
+
+def test_capacity_fixture_empty_splits_are_planned_identity_items():
+    g = golden("split_ledgers.json")["capacity_fixture"]
+    plan = dattn.dattn_plan(_problem(B=2, H_q=4, H_kv=4, fixed_splits=g["S"]), g["T"], num_sms=8)
+    items = plan.items()
+    lens0 = [it["e"] - it["a"] for it in items if it["b"] == 0 and it["h_kv"] == 0]
+    assert lens0 == g["request0_lengths"]
+    active = sum(1 for it in items if it["e"] > it["a"])
+    assert active == g["active"] // 1            # 12 = 3 non-empty splits x 4 heads
+    assert all(it["slot"] >= 0 for it in items)  # every slot the reducer reads is written
+
+
+def test_work_schedule_pin_least_loaded_planner():
+    g = golden("work_schedule.json")
+    prob = _problem(B=2, H_q=1, H_kv=1, P=1, num_pages=6000)
+    plan = dattn.dattn_plan(prob, g["outputs"], num_sms=g["workers"], chunk_tokens=g["chunk_limit"])
+    items = plan.items()
+    assert sorted((it["e"] - it["a"] for it in items), reverse=True) == g["planned_chunks_sorted"]
+    loads = [0] * g["workers"]
+    for it in items:
+        loads[it["cta"]] += it["e"] - it["a"]
+    assert loads == g["planned_loads"]
+    assert plan.info["max_cta_keys"] == max(g["planned_loads"])
+    # the fixed four-way split of the same workload is unbalanced: max/mean 1.6
+    fixed = dattn.dattn_plan(dict(prob, fixed_splits=g["fixed_splits"]), g["outputs"], num_sms=g["workers"])
+    lens = sorted((it["e"] - it["a"] for it in fixed.items()), reverse=True)
+    assert lens == g["fixed_loads"]
+    assert max(lens) / (sum(lens) / g["workers"]) == g["rho"]
+
+
+def test_sink_window_stream_is_the_union_of_visible_sets():
+    T = [5, 6, 7, 4100, 9000, 0, 1]
+    prob = _problem(B=len(T), H_q=4, H_kv=1, mask="sink_window", n_sink=4, window=4096)
+    plan = dattn.dattn_plan(prob, T, num_sms=4, chunk_tokens=64)
+    _coverage(plan.items(), [(b, 0) for b in range(len(T))],
+              lambda g: len(masks.sink_recent(T[g[0]], 4, 4096)))
+    assert plan.info["stream_keys"] == sum(len(masks.sink_recent(t, 4, 4096)) for t in T)
+
+
+def test_multi_row_sink_window_stream_covers_every_row():
+    T, S_q = [50, 3], 4
+    prob = _problem(B=2, S_q=S_q, H_q=4, H_kv=2, mask="sink_window", n_sink=2, window=5)
+    plan = dattn.dattn_plan(prob, T, num_sms=4)
+    want = [len(np.unique(np.concatenate([masks.visible_positions("sink_window", t, S_q, i, n_sink=2, window=5)
+                                          for i in range(S_q)]))) for t in T]
+    _coverage(plan.items(), [(b, h) for b in range(2) for h in range(2)], lambda g: want[g[0]])
+
+
+def test_index_list_stream_and_single_chunk_direct_write():
+    T = [100, 40]
+    lists = [np.arange(0, 100, 3), np.array([1, 5, 99]), np.arange(40), np.array([], np.int32)]
+    indptr = np.concatenate([[0], np.cumsum([len(x) for x in lists])])
+    prob = _problem(B=2, H_q=4, H_kv=2, mask="index_list")
+    plan = dattn.dattn_plan(prob, T, index_indptr=indptr, index_list=np.concatenate(lists), num_sms=2,
+                            chunk_tokens=64)
+    items = plan.items()
+    _coverage(items, [(b, h) for b in range(2) for h in range(2)], lambda g: len(lists[g[0] * 2 + g[1]]))
+    for it in items:
+        n_items = sum(1 for x in items if (x["b"], x["h_kv"]) == (it["b"], it["h_kv"]))
+        assert (it["slot"] < 0) == (n_items == 1)
+
+
+def test_default_planner_covers_ragged_batch_and_balances():
+    rng = np.random.default_rng(1)
+    T = rng.integers(1024, 8193, 16).tolist()
+    plan = dattn.dattn_plan(_problem(B=16, H_q=32, H_kv=8), T, num_sms=152)
+    _coverage(plan.items(), [(b, h) for b in range(16) for h in range(8)], lambda g: T[g[0]])
+    info = plan.info
+    mean = info["stream_keys"] / info["n_ctas"]
+    assert info["max_cta_keys"] <= 1.5 * mean
+    assert info["n_ctas"] <= 152
+
+
+def test_workspace_bytes_follow_the_mlu_ledger():
+    """Partial area = n_slots * rows * (d * 4 + 2 * 4): the (m, l, u) ABI without a validity byte."""
+    T = [4096, 3587]
+    plan = dattn.dattn_plan(_problem(fixed_splits=8), T, num_sms=152)
+    info = plan.info
+    rows = info["rows"]
+    partial = info["n_slots"] * rows * (128 * 4 + 2 * 4)
+    assert partial == ss.workspace_mlu_bytes(info["n_slots"] * rows, 128, b_valid=0)
+    assert info["workspace_bytes"] >= info["blob_bytes"] + partial
+    assert info["workspace_bytes"] - info["blob_bytes"] - partial < 2 * 256
+
+
+@pytest.mark.parametrize("field,value,status,reason", [
+    ("H_kv", 3, "DATTN_EINVAL", "multiple of H_kv"),
+    ("S_q", 0, "DATTN_EINVAL", "S_q"),
+    ("d", 80, "DATTN_EUNSUPPORTED", "d_h"),
+    ("P", 0, "DATTN_EINVAL", "page_size"),
+    ("num_pages", 0, "DATTN_EINVAL", "num_pages"),
+    ("S_q", 16, "DATTN_EUNSUPPORTED", "<= 32"),
+    ("window", 0, "DATTN_EINVAL", "window"),
+    ("fixed_splits", -1, "DATTN_EINVAL", "fixed_splits"),
+])
+def test_plan_rejects_one_mutated_field(field, value, status, reason):
+    prob = _problem(mask="sink_window", n_sink=1, window=4)
+    prob[field] = value
+    with pytest.raises(dattn.DattnError) as e:
+        dattn.dattn_plan(prob, [10, 20], num_sms=4)
+    assert dattn.STATUS[e.value.status] == status
+    assert reason in str(e.value)
+
+
+def test_plan_rejects_bad_lengths_pages_and_lists():
+    with pytest.raises(dattn.DattnError, match="kv_len"):
+        dattn.dattn_plan(_problem(), [10, -1], num_sms=4)
+    with pytest.raises(dattn.DattnError, match="needs 2"):
+        dattn.dattn_plan(_problem(), [10, 20], page_indptr=[0, 1, 2], num_sms=4)
+    prob = _problem(B=1, H_kv=2, mask="index_list")
+    with pytest.raises(dattn.DattnError, match="strictly increasing"):
+        dattn.dattn_plan(prob, [10], index_indptr=[0, 2, 4], index_list=[1, 1, 2, 3], num_sms=4)
+    with pytest.raises(dattn.DattnError, match="outside"):
+        dattn.dattn_plan(prob, [10], index_indptr=[0, 2, 4], index_list=[1, 2, 3, 10], num_sms=4)
+    with pytest.raises(dattn.DattnError, match="T_cap"):
+        dattn.dattn_plan(dict(_problem(layout="contig", T_cap=8, B_cache=2)), [8, 9], num_sms=4)
+    with pytest.raises(dattn.DattnError, match="paged layout"):
+        dattn.dattn_plan(dict(_problem(layout="contig", fmt="int8", T_cap=8, B_cache=2)), [8, 8], num_sms=4)
+
+
+def test_rejection_vector_lists_every_failed_check():
+    prob = _problem(H_kv=3, d=96, P=0)
+    with pytest.raises(dattn.DattnError) as e:
+        dattn.dattn_plan(prob, [1, 1], num_sms=4)
+    text = str(e.value)
+    assert "multiple of H_kv" in text and "d_h" in text and "page_size" in text
+    assert dattn.STATUS[e.value.status] == "DATTN_EINVAL"
+
+
+def test_run_rejects_stale_plan_and_small_workspace_without_a_gpu():
+    """Admission runs before any CUDA call, so these errors are reported on any host."""
+    plan = dattn.dattn_plan(_problem(), [10, 20], num_sms=4)
+
+    class Fake:
+        def __init__(self, n):
+            self._n = n
+            self._buf = (ctypes.c_uint8 * (n + 256))()
+
+        def data_ptr(self):
+            return (ctypes.addressof(self._buf) + 255) // 256 * 256
+
+        def numel(self):
+            return self._n
+
+        def element_size(self):
+            return 1
+
+    t = dattn.Tensors()
+    buf = Fake(1 << 16)
+    for f in ("q", "k", "v", "o", "page_indptr", "page_indices"):
+        setattr(t, f, buf.data_ptr())
+    with pytest.raises(dattn.DattnError) as e:
+        dattn.dattn_run(plan, _problem(H_q=16), t, Fake(plan.workspace_bytes), stream=0)
+    assert dattn.STATUS[e.value.status] == "DATTN_ESTALE_PLAN"
+    with pytest.raises(dattn.DattnError) as e:
+        dattn.dattn_run(plan, _problem(), t, Fake(plan.workspace_bytes - 256), stream=0)
+    assert dattn.STATUS[e.value.status] == "DATTN_EWORKSPACE"
