@@ -165,8 +165,10 @@ def _cpu_child(args):
     from oracle import attention
     from oracle import cache as ocache
     path, groups = args[0], [tuple(map(int, g.split(":"))) for g in args[1:]]
-    z = np.load(path, mmap_mode="r", allow_pickle=False)
-    meta = json.loads(str(z["meta"]))
+    z = {n: np.load(os.path.join(path, n + ".npy"), mmap_mode="r")
+         for n in ("k", "v", "q", "page_indptr", "page_indices", "kv_len")}
+    with open(os.path.join(path, "meta.json")) as f:
+        meta = json.load(f)
     c = ocache.Cache("paged", "bf16", meta["H_kv"], meta["d"], P=meta["P"], k=z["k"], v=z["v"],
                      page_indptr=z["page_indptr"], page_indices=z["page_indices"], kv_len=z["kv_len"])
     g = meta["H_q"] // meta["H_kv"]
@@ -189,12 +191,14 @@ def cpu_oracle_time(w, groups_per_worker, workers, tmpdir):
         return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
     p = w.problem
-    path = os.path.join(tmpdir, "workload.npz")
-    if not os.path.exists(path):
-        meta = dict(B=p["B"], S_q=p["S_q"], H_q=p["H_q"], H_kv=p["H_kv"], d=p["d"], P=p["P"])
-        np.savez(path, k=bits(w.k), v=bits(w.v), q=bits(w.q), page_indptr=w.page_indptr.numpy().astype(np.int64),
-                 page_indices=w.page_indices.numpy().astype(np.int64), kv_len=w.kv_len.numpy().astype(np.int64),
-                 meta=json.dumps(meta))
+    path = tmpdir
+    if not os.path.exists(os.path.join(path, "meta.json")):
+        arrays = dict(k=bits(w.k), v=bits(w.v), q=bits(w.q), page_indptr=w.page_indptr.numpy().astype(np.int64),
+                      page_indices=w.page_indices.numpy().astype(np.int64), kv_len=w.kv_len.numpy().astype(np.int64))
+        for n, a in arrays.items():
+            np.save(os.path.join(path, n + ".npy"), a)
+        with open(os.path.join(path, "meta.json"), "w") as f:
+            json.dump(dict(B=p["B"], S_q=p["S_q"], H_q=p["H_q"], H_kv=p["H_kv"], d=p["d"], P=p["P"]), f)
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     procs = []
     t0 = time.perf_counter()
