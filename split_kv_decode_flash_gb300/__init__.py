@@ -234,13 +234,21 @@ def dattn_plan_get_items(plan: Plan):
 
 
 def tensors_from(**kw) -> Tensors:
-    """dattn_tensors from torch tensors (or None) keyed by the C field names."""
+    """dattn_tensors from torch tensors (or None) keyed by the C field names.
+
+    The returned struct holds references to the tensors, so their device
+    memory stays allocated while the struct (and any work queued with it)
+    is alive."""
     t = Tensors()
+    keep = []
     for name, _ in Tensors._fields_:
         v = kw.pop(name, None)
         setattr(t, name, None if v is None else v.data_ptr())
+        if v is not None:
+            keep.append(v)
     if kw:
         raise TypeError(f"unknown tensor fields {sorted(kw)}")
+    t._keep = keep
     return t
 
 

@@ -153,7 +153,8 @@ def test_debug_translate_matches_oracle_offsets():
     c = torch.tensor(coords, dtype=torch.int32, device="cuda")
     out = torch.empty(len(coords), dtype=torch.int64, device="cuda")
     t = dattn.tensors_from(**H.device_tensors(w, None, None))
-    dattn.dattn_debug_translate(p, t, w.kv_len.cuda(), c, out)
+    kv_len = w.kv_len.cuda()
+    dattn.dattn_debug_translate(p, t, kv_len, c, out)
     got = out.cpu().numpy()
     ind, ptr = w.page_indices.numpy(), w.page_indptr.numpy()
     for (b, tt, hq, x), g in zip(coords, got):
@@ -172,8 +173,10 @@ def test_debug_translate_contiguous_remap():
     p = w.problem
     coords = [[0, 3, 3, 2], [1, 4, 0, 63], [1, 5, 0, 0]]
     out = torch.empty(3, dtype=torch.int64, device="cuda")
-    dattn.dattn_debug_translate(p, dattn.tensors_from(**H.device_tensors(w, None, None)), w.kv_len.cuda(),
-                                torch.tensor(coords, dtype=torch.int32, device="cuda"), out)
+    t = dattn.tensors_from(**H.device_tensors(w, None, None))
+    kv_len = w.kv_len.cuda()
+    cd = torch.tensor(coords, dtype=torch.int32, device="cuda")
+    dattn.dattn_debug_translate(p, t, kv_len, cd, out)
     got = out.cpu().tolist()
     assert got[0] == address.offset_contig_nhd(2, 3, 1, 2, 12, 2, 64)
     assert got[1] == address.offset_contig_nhd(0, 4, 0, 63, 12, 2, 64)
@@ -204,8 +207,10 @@ def test_debug_classify_matches_oracle_tile_classes(mask, S_q, extra):
                 tiles.append([b, h, j])
                 want.append(masks.tile_class(sets, 16 * j, 16 * (j + 1)))
     out = torch.empty(len(tiles), dtype=torch.int32, device="cuda")
-    dattn.dattn_debug_classify(w.problem, dattn.tensors_from(**H.device_tensors(w, None, None)), w.kv_len.cuda(),
-                               torch.tensor(tiles, dtype=torch.int32, device="cuda"), out)
+    t = dattn.tensors_from(**H.device_tensors(w, None, None))
+    kv_len = w.kv_len.cuda()
+    td = torch.tensor(tiles, dtype=torch.int32, device="cuda")
+    dattn.dattn_debug_classify(w.problem, t, kv_len, td, out)
     got = [dattn.TILE_CLASSES[x] for x in out.cpu().tolist()]
     assert got == want
 
