@@ -200,13 +200,28 @@ dattn_status dattn_run(const dattn_plan_t* plan, const dattn_problem* prob,
                        const dattn_tensors* t, void* workspace, size_t workspace_bytes,
                        void* stream);
 
-/* dattn_run that also records CUDA events (cudaEvent_t passed as void*, created
- * by the caller; NULL entries are skipped) on "stream": events[0] before the
- * partial kernel, events[1] after it, events[2] after the merge kernel.  Used
- * to time each kernel of the step on the stream it runs on. */
-dattn_status dattn_run_with_events(const dattn_plan_t* plan, const dattn_problem* prob,
-                                   const dattn_tensors* t, void* workspace, size_t workspace_bytes,
-                                   void* stream, void* const* events);
+/* Options of dattn_run_ex. */
+#define DATTN_RUN_REUSE_UPLOAD 1u  /* the workspace already holds this plan's work list
+                                      (dattn_plan_upload or an earlier run with this plan and
+                                      workspace); skip the host->device copy. The caller
+                                      guarantees that nothing overwrote the workspace since. */
+typedef struct {
+  uint32_t flags;     /* DATTN_RUN_* bits                                                  */
+  void* events[3];    /* cudaEvent_t (as void*) recorded on "stream" before the partial
+                         kernel, after it and after the merge kernel; NULL entries skipped */
+} dattn_run_options;
+
+/* Copies the plan's work list into the head of "workspace" (stream-ordered).
+ * A plan is typically built once per decode step and then run by every layer
+ * of the model with DATTN_RUN_REUSE_UPLOAD (the FlashInfer plan/run split,
+ * M4.5 §0x0AD), so the copy happens once per step. */
+dattn_status dattn_plan_upload(const dattn_plan_t* plan, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* dattn_run with options (NULL = dattn_run). */
+dattn_status dattn_run_ex(const dattn_plan_t* plan, const dattn_problem* prob,
+                          const dattn_tensors* t, void* workspace, size_t workspace_bytes,
+                          void* stream, const dattn_run_options* options);
 
 /* Reads the device status word of the last run that used "workspace"
  * (synchronises "stream").  *flags = 0 when no device check fired. */

@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "DattnError", "Problem", "load", "make_problem", "dattn_plan", "dattn_plan_get_info",
-    "dattn_plan_get_items", "dattn_run", "dattn_run_with_events", "dattn_device_status", "kv_append",
+    "dattn_plan_get_items", "dattn_run", "dattn_run_ex", "dattn_plan_upload", "dattn_device_status", "kv_append",
     "kv_append_workspace_bytes", "dattn_debug_translate", "dattn_debug_classify",
     "dattn_debug_gather", "dattn_last_error", "dattn_version", "tensors_from", "decode",
     "LAYOUTS", "FORMATS", "MASKS", "TILE_CLASSES", "STATUS",
@@ -72,6 +72,13 @@ class WorkItem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("b", "h_kv", "a", "e", "slot", "cta")]
 
 
+class RunOptions(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_uint32), ("events", ctypes.c_void_p * 3)]
+
+
+RUN_REUSE_UPLOAD = 1
+
+
 class AppendInputs(ctypes.Structure):
     _fields_ = [("kv_len_old", ctypes.c_void_p), ("new_indptr", ctypes.c_void_p),
                 ("page_indptr", ctypes.c_void_p)]
@@ -97,8 +104,9 @@ def load():
         "dattn_plan_get_items": (_ST, [_VP, ctypes.POINTER(WorkItem), ctypes.c_int32,
                                        ctypes.POINTER(ctypes.c_int32)]),
         "dattn_run": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP, ctypes.c_size_t, _VP]),
-        "dattn_run_with_events": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP,
-                                        ctypes.c_size_t, _VP, ctypes.POINTER(_VP)]),
+        "dattn_run_ex": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP,
+                               ctypes.c_size_t, _VP, ctypes.POINTER(RunOptions)]),
+        "dattn_plan_upload": (_ST, [_VP, _VP, ctypes.c_size_t, _VP]),
         "dattn_device_status": (_ST, [_VP, ctypes.POINTER(ctypes.c_int32), _VP]),
         "kv_append_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Problem)]),
         "kv_append": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(AppendInputs), ctypes.POINTER(Tensors),
@@ -259,14 +267,24 @@ def dattn_run(plan: Plan, problem, tensors: Tensors, workspace, stream=None) -> 
                             workspace.numel() * workspace.element_size(), _stream_ptr(stream)), "dattn_run")
 
 
-def dattn_run_with_events(plan: Plan, problem, tensors: Tensors, workspace, events, stream=None) -> None:
-    """dattn_run that records three caller-created torch.cuda.Events around its kernels
+def dattn_plan_upload(plan: Plan, workspace, stream=None) -> None:
+    """Copy the plan's work list into ``workspace`` (see dattn_plan_upload in dattn.h)."""
+    _check(load().dattn_plan_upload(plan.handle, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    _stream_ptr(stream)), "dattn_plan_upload")
+
+
+def dattn_run_ex(plan: Plan, problem, tensors: Tensors, workspace, *, reuse_upload=False, events=None,
+                 stream=None) -> None:
+    """dattn_run with options: reuse an uploaded work list, record three torch.cuda.Events
     (before the partial kernel, after it, after the merge kernel)."""
     prob = problem if isinstance(problem, Problem) else make_problem(problem)
-    arr = (_VP * 3)(*[None if e is None else ctypes.c_void_p(e.cuda_event) for e in events])
-    _check(load().dattn_run_with_events(plan.handle, ctypes.byref(prob), ctypes.byref(tensors),
-                                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                        _stream_ptr(stream), arr), "dattn_run_with_events")
+    opt = RunOptions()
+    opt.flags = RUN_REUSE_UPLOAD if reuse_upload else 0
+    for i, e in enumerate(events or ()):
+        opt.events[i] = None if e is None else e.cuda_event
+    _check(load().dattn_run_ex(plan.handle, ctypes.byref(prob), ctypes.byref(tensors), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_ptr(stream), ctypes.byref(opt)),
+           "dattn_run_ex")
 
 
 def dattn_device_status(workspace, stream=None) -> int:

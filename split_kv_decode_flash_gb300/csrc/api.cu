@@ -133,11 +133,9 @@ __global__ void gather_kernel(PartialParams p, int item, int out_off, int32_t* o
   }
 }
 
-dattn_status upload_blob(const dattn_plan_t* plan, void* ws, size_t ws_bytes, cudaStream_t s,
-                         PartialParams& k) {
+// Device pointers of the plan's arrays inside "ws".
+void bind_blob(const dattn_plan_t* plan, void* ws, PartialParams& k) {
   const BlobHeader* h = reinterpret_cast<const BlobHeader*>(plan->blob.data());
-  cudaError_t err = cudaMemcpyAsync(ws, plan->blob.data(), plan->blob.size(), cudaMemcpyHostToDevice, s);
-  if (err != cudaSuccess) return cuda_fail("copy of the work list", err);
   uint8_t* base = static_cast<uint8_t*>(ws);
   k.items = reinterpret_cast<const WorkItem*>(base + h->off_items);
   k.cta_indptr = reinterpret_cast<const int32_t*>(base + h->off_cta_indptr);
@@ -145,7 +143,12 @@ dattn_status upload_blob(const dattn_plan_t* plan, void* ws, size_t ws_bytes, cu
   k.ml = reinterpret_cast<float2*>(base + h->off_ml);
   k.u = reinterpret_cast<float*>(base + h->off_u);
   k.status = reinterpret_cast<int32_t*>(base + offsetof(BlobHeader, status));
-  (void)ws_bytes;
+}
+
+dattn_status upload_blob(const dattn_plan_t* plan, void* ws, cudaStream_t s, PartialParams& k) {
+  cudaError_t err = cudaMemcpyAsync(ws, plan->blob.data(), plan->blob.size(), cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return cuda_fail("copy of the work list", err);
+  bind_blob(plan, ws, k);
   return DATTN_OK;
 }
 
@@ -169,10 +172,6 @@ dattn_status check_run_args(const dattn_plan_t* plan, const dattn_problem* prob,
     c.status = DATTN_EWORKSPACE;
     return c.finish(where);
   }
-  if (prob->fmt != DATTN_FMT_BF16) {
-    c.fail(DATTN_EUNSUPPORTED, "this build reads bf16 K/V only");
-    return c.finish(where);
-  }
   return DATTN_OK;
 }
 
@@ -190,14 +189,19 @@ dattn_status record(void* const* events, int i, cudaStream_t s) {
 }
 
 dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const dattn_tensors* t, void* workspace,
-                      size_t workspace_bytes, void* stream, void* const* events, const char* where) {
+                      size_t workspace_bytes, void* stream, const dattn_run_options* opt, const char* where) {
   dattn_status st = check_run_args(plan, prob, t, workspace, workspace_bytes, true, where);
   if (st != DATTN_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* const* events = opt ? opt->events : nullptr;
   PartialParams k;
   fill_common(*prob, *t, k);
-  st = upload_blob(plan, workspace, workspace_bytes, s, k);
-  if (st != DATTN_OK) return st;
+  if (opt && (opt->flags & DATTN_RUN_REUSE_UPLOAD)) {
+    bind_blob(plan, workspace, k);
+  } else {
+    st = upload_blob(plan, workspace, s, k);
+    if (st != DATTN_OK) return st;
+  }
   if ((st = record(events, 0, s)) != DATTN_OK) return st;
   if (plan->info.n_ctas > 0) {
     const int err = launch_partial(k, prob->d_h, plan->info.n_ctas, stream);
@@ -231,10 +235,22 @@ extern "C" dattn_status dattn_run(const dattn_plan_t* plan, const dattn_problem*
   return run_impl(plan, prob, t, workspace, workspace_bytes, stream, nullptr, "dattn_run");
 }
 
-extern "C" dattn_status dattn_run_with_events(const dattn_plan_t* plan, const dattn_problem* prob,
-                                              const dattn_tensors* t, void* workspace, size_t workspace_bytes,
-                                              void* stream, void* const* events) {
-  return run_impl(plan, prob, t, workspace, workspace_bytes, stream, events, "dattn_run_with_events");
+extern "C" dattn_status dattn_run_ex(const dattn_plan_t* plan, const dattn_problem* prob, const dattn_tensors* t,
+                                     void* workspace, size_t workspace_bytes, void* stream,
+                                     const dattn_run_options* options) {
+  return run_impl(plan, prob, t, workspace, workspace_bytes, stream, options, "dattn_run_ex");
+}
+
+extern "C" dattn_status dattn_plan_upload(const dattn_plan_t* plan, void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+  if (!plan || !workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) ||
+      workspace_bytes < static_cast<size_t>(plan->info.workspace_bytes)) {
+    set_error("dattn_plan_upload: plan missing or workspace too small / misaligned");
+    return plan ? DATTN_EWORKSPACE : DATTN_EINVAL;
+  }
+  PartialParams k;
+  std::memset(&k, 0, sizeof(k));
+  return upload_blob(plan, workspace, static_cast<cudaStream_t>(stream), k);
 }
 
 extern "C" dattn_status dattn_device_status(const void* workspace, int32_t* flags, void* stream) {
@@ -314,7 +330,7 @@ extern "C" dattn_status dattn_debug_gather(const dattn_plan_t* plan, const dattn
   PartialParams k;
   dattn_tensors empty{};
   fill_common(*prob, t ? *t : empty, k);
-  dattn_status st = upload_blob(plan, workspace, workspace_bytes, s, k);
+  dattn_status st = upload_blob(plan, workspace, s, k);
   if (st != DATTN_OK) return st;
   int total = 0;
   for (size_t i = 0; i < plan->items.size(); ++i) {

@@ -1,25 +1,37 @@
-// Partial kernel of split-KV decode attention (bf16 K/V).
+// Partial kernel of split-KV decode attention: bf16, INT8 per-token and
+// KIVI INT4 K/V.
 //
 // One persistent CTA per SM walks its list of work items (request b, kv head
-// h, keys [a, e) of the group's visible stream).  A producer warp turns every
-// 64-key stage of an item into page segments (M4.5 §0x04E), translates each
-// logical block through the CSR page list (§0x04D), and issues one bulk
-// (TMA-engine) copy per segment and per K/V into a 4-deep shared-memory ring
-// guarded by mbarriers.  It also classifies the stage (FULL / PARTIAL,
-// §0x05C) so that FULL stages skip the per-element predicate; keys outside the
-// visible stream (SKIP tiles) are never loaded at all (§0x05D).
+// h, keys [a, e) of the group's visible stream).
+//
+// Producer warp.  Every 64-key stage is described per key slot (logical key
+// t, physical page pi) one stage ahead, so the dependent loads of the page
+// walk (list entry -> page id, M4.5 §0x04D) overlap the wait for a free ring
+// slot.  Slots whose keys are consecutive inside one page are merged into one
+// run with two warp ballots (the page segments of §0x04E); each run becomes
+// one bulk (TMA-engine) copy per tensor into a shared-memory ring guarded by
+// mbarriers.  Keys outside the visible stream (SKIP tiles) are never loaded;
+// each stage is classified FULL or PARTIAL (§0x05C) so FULL stages skip the
+// per-element predicate.  Quantized formats also stage their qparams: INT8
+// per-token (s, z) as 16-byte aligned chunks packed by a warp scan; KIVI the
+// per-channel K group qparams and per-token V qparams (M8.6 §0x06A); KIVI
+// residual keys come from the bf16 ring in stages of their own.
 //
 // Eight consumer warps share every K/V tile across the GQA group (§0x03A):
 // each warp owns 4 query rows (a row block) and a slice of the stage's keys.
 // Lanes form 4 key groups x 8 lanes; a lane holds 16 (d=128) or 8 (d=64)
-// channels of its key and of the 4 query rows, so q.k is 16 packed-fp32 FMAs
-// plus a 3-step shuffle reduction.  The online softmax (§0x02B) is updated
-// every 8 keys with exp2 in log2 units; masked scores become -inf before the
-// maximum and the sums (§0x05C).  At the end of an item the warps of a row
-// block merge their states through shared memory with the same (m, l, u)
-// rule and write either O / LSE directly (single-chunk groups, as in
-// FlashInfer's unpartitioned path, §0x0AD) or an fp32 partial state.
+// channels of its key and of the 4 query rows, so q.k is a handful of packed
+// fp32 FMAs plus a 3-step shuffle reduction.  Scales stay where M8.6 §0x03A-C
+// puts them: a per-token K scale multiplies the finished dot product, a
+// per-channel K scale is applied while dequantising, a per-token V scale is
+// folded into the probability and its offset into a per-row sum.  The online
+// softmax (§0x02B) runs every 8 keys in log2 units; masked scores are -inf
+// before the maximum and the sums.  At the end of an item the warps of a row
+// block merge their states through shared memory and write either O / LSE
+// (single-chunk groups) or an fp32 partial state.
 #include <cuda_runtime.h>
+
+#include <climits>
 
 #include "device.cuh"
 
@@ -27,36 +39,68 @@ namespace dattn {
 
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned kAll = 0xffffffffu;
+constexpr int kMaxKGroups = 6;      // KIVI K groups per stage (G >= 32, at most two runs)
+constexpr int kQpEntries = 512;     // INT8 qparam entries per stage and tensor
 
-template <int D>
-struct Layout {
-  static constexpr int kTileBytes = kTK * D * 2;            // one K (or V) tile
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kPos = kStages * kStageBytes;         // int32 [kStages][kTK]
-  static constexpr int kCls = kPos + kStages * kTK * 4;      // int32 [kStages]
-  static constexpr int kFullBar = (kCls + kStages * 4 + 15) / 16 * 16;
-  static constexpr int kEmptyBar = kFullBar + kStages * 8;
-  static constexpr int kAbort = kEmptyBar + kStages * 8;
-  static constexpr int kScratch = (kAbort + 16 + 15) / 16 * 16;
-  // per consumer warp: 4 rows x D values of u, then 4 x (m, l)
-  static constexpr int kScratchWarp = 4 * D * 4 + 4 * 8;
+constexpr int align16(int x) { return (x + 15) / 16 * 16; }
+
+template <int D, int FMT>
+struct Cfg {
+  static constexpr bool kI8 = FMT == DATTN_FMT_INT8_TOKEN;
+  static constexpr bool kI4 = FMT == DATTN_FMT_INT4_KIVI;
+  static constexpr int kStagesN = FMT == DATTN_FMT_BF16 ? 6 : 5;
+  static constexpr int kTile = kTK * D * 2;                                  // bf16-sized tile
+  static constexpr int kKQ = kI8 ? kQpEntries * 4 : kI4 ? kMaxKGroups * D * 4 : 0;
+  static constexpr int kVQ = kI8 ? kQpEntries * 4 : kI4 ? kTK * (D / 16) * 4 : 0;
+  static constexpr int kStage = 2 * kTile + kKQ + kVQ;
+  static constexpr int kPos = kStagesN * kStage;                             // int32 [stages][kTK]
+  static constexpr int kQsel = kPos + kStagesN * kTK * 4;                    // int32 [stages][kTK]
+  static constexpr int kFlags = kQsel + kStagesN * kTK * 4;                  // int32 [stages]
+  static constexpr int kFullBar = align16(kFlags + kStagesN * 4);
+  static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
+  static constexpr int kAbort = kEmptyBar + kStagesN * 8;
+  static constexpr int kScratch = align16(kAbort + 16);
+  static constexpr int kScratchWarp = 4 * D * 4 + 4 * 8;                   // 4 rows of u, then (m, l)
   static constexpr int kTotal = kScratch + kConsumerWarps * kScratchWarp;
+  // channel map: bf16 splits a lane's 16 channels in two 8-channel chunks
+  // (conflict-free 16-byte reads of 256-byte rows); the byte formats keep
+  // them contiguous.
+  static constexpr bool kSplit = FMT == DATTN_FMT_BF16 && D == 128;
+  static __device__ __forceinline__ int chan(int j, int v) {   // first channel of float2 slot v
+    return kSplit ? (v >> 2) * 64 + 8 * j + 2 * (v & 3) : (D / 8) * j + 2 * v;
+  }
 };
+
+constexpr int kFlagFull = 1, kFlagResidual = 2;
+
+__device__ __forceinline__ int kivi_prefix(int T, int G, int R) { return T > R ? (T - R + G - 1) / G * G : 0; }
+
+// Stream index where KIVI residual keys begin (INT_MAX for other formats).
+__device__ __forceinline__ int residual_start(const PartialParams& p, const WorkItem& it) {
+  if (p.fmt != DATTN_FMT_INT4_KIVI) return INT_MAX;
+  const int nq = kivi_prefix(it.T, p.kivi_G, p.kivi_R);
+  return nq <= it.x0 ? nq : it.x0 + max(0, nq - it.x1);
+}
+
+__device__ __forceinline__ int stage_end(const WorkItem& it, int j0, int jq) {
+  int j1 = min(j0 + kTK, it.e);
+  if (j0 < jq) j1 = min(j1, jq);
+  return j1;
+}
 
 struct Run {
-  int p0, p1, s0;  // positions [p0, p1) land in slots s0 ...
+  int p0, p1;
 };
 
-// Runs of consecutive positions covered by stream [j0, j1) of an interval item
-// (at most two: the sink interval and the window / causal interval).
+// Position runs of stream [j0, j1) of an interval item (at most two).
 __device__ __forceinline__ int item_runs(const WorkItem& it, int j0, int j1, Run& r0, Run& r1) {
   int n = 0;
-  Run a{0, 0, 0}, b{0, 0, 0};
-  if (j0 < it.x0) a = Run{j0, min(j1, it.x0), 0}, n = 1;
+  Run a{0, 0}, b{0, 0};
+  if (j0 < it.x0) a = Run{j0, min(j1, it.x0)}, n = 1;
   if (j1 > it.x0) {
     const int s = max(j0, it.x0);
-    const Run x{it.x1 + (s - it.x0), it.x1 + (j1 - it.x0), s - j0};
+    const Run x{it.x1 + (s - it.x0), it.x1 + (j1 - it.x0)};
     if (n == 0) a = x; else b = x;
     ++n;
   }
@@ -65,194 +109,353 @@ __device__ __forceinline__ int item_runs(const WorkItem& it, int j0, int j1, Run
   return n;
 }
 
-__device__ __forceinline__ int run_segments(const Run& r, int P) {
-  return r.p1 > r.p0 ? (r.p1 - 1) / P - r.p0 / P + 1 : 0;
+__device__ __forceinline__ float2 u8_pair(uint32_t w, int pair) {
+  const uint32_t a = __byte_perm(w, 0x4B000000u, 0x7540u | (2 * pair));
+  const uint32_t b = __byte_perm(w, 0x4B000000u, 0x7540u | (2 * pair + 1));
+  return __fadd2_rn(make_float2(__uint_as_float(a), __uint_as_float(b)), make_float2(-8388608.f, -8388608.f));
 }
 
-// Segment "sg" of the runs: page block jb and positions [sp0, sp1) landing in slot "slot".
-__device__ __forceinline__ void segment(const Run& r0, const Run& r1, int ns0, int sg, int P, int& jb, int& sp0,
-                                        int& sp1, int& slot) {
-  const bool first = sg < ns0;
-  const int p0 = first ? r0.p0 : r1.p0, p1 = first ? r0.p1 : r1.p1, s0 = first ? r0.s0 : r1.s0;
-  jb = p0 / P + (first ? sg : sg - ns0);
-  sp0 = max(p0, jb * P);
-  sp1 = min(p1, (jb + 1) * P);
-  slot = s0 + (sp0 - p0);
+__device__ __forceinline__ float2 u4_pair(uint32_t w, int pair) {   // nibbles 2*pair, 2*pair+1
+  const uint32_t a = ((w >> (8 * pair)) & 0xFu) | 0x4B000000u;
+  const uint32_t b = ((w >> (8 * pair + 4)) & 0xFu) | 0x4B000000u;
+  return __fadd2_rn(make_float2(__uint_as_float(a), __uint_as_float(b)), make_float2(-8388608.f, -8388608.f));
+}
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 // ---- producer ---------------------------------------------------------------------
 
-template <int D>
+struct Cursor {
+  int ii;           // position in the CTA's item list
+  WorkItem it;
+  int jq, lo, hi, crow;
+  int j0, j1;
+  bool valid;
+};
+
+__device__ __forceinline__ void load_item(const PartialParams& p, Cursor& c, int lane) {
+  c.it = p.items[p.cta_items[c.ii]];
+  c.jq = residual_start(p, c.it);
+  c.lo = c.hi = c.crow = 0;
+  if (p.layout == DATTN_KV_PAGED_HND) {
+    c.lo = p.page_indptr[c.it.b];
+    c.hi = p.page_indptr[c.it.b + 1];
+  } else {
+    c.crow = cache_row(p.cache_batch_idx, c.it.b, p.B_cache, lane == 0 ? p.status : nullptr);
+  }
+  if (p.mask == DATTN_MASK_INDEX_LIST) {
+    const int g = c.it.b * p.H_kv + c.it.h;
+    const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
+    if (lo != c.it.x0 || c.it.e > n) {
+      if (lane == 0) atomicOr(p.status, kStListRange);
+      c.it.e = c.it.a;          // drop the item's keys
+    }
+  }
+}
+
+// First stage at or after item position ii whose item has keys.
+__device__ __forceinline__ void seek(const PartialParams& p, Cursor& c, int it_end, int lane) {
+  c.valid = false;
+  for (; c.ii < it_end; ++c.ii) {
+    load_item(p, c, lane);
+    if (c.it.e > c.it.a) {
+      c.j0 = c.it.a;
+      c.j1 = stage_end(c.it, c.j0, c.jq);
+      c.valid = true;
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void advance(const PartialParams& p, Cursor& c, int it_end, int lane) {
+  if (c.j1 < c.it.e) {
+    c.j0 = c.j1;
+    c.j1 = stage_end(c.it, c.j0, c.jq);
+    return;
+  }
+  ++c.ii;
+  seek(p, c, it_end, lane);
+}
+
+struct Desc {
+  int t[2];     // logical key of slots lane, lane + 32 (-1: none)
+  int pg[2];    // physical page (paged), cache row (contiguous), 0 (residual)
+  int gpg[2];   // KIVI: page holding the key's K-group qparams
+};
+
+template <int FMT>
+__device__ __forceinline__ Desc describe(const PartialParams& p, const Cursor& c, int lane) {
+  Desc d;
+  const bool resid = c.j0 >= c.jq;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    const int j = c.j0 + s;
+    int t = -1, pg = -1, gpg = -1;
+    if (c.valid && j < c.j1) {
+      t = stream_key(c.it, p.mask, p.index_list, j);
+      if (p.mask == DATTN_MASK_INDEX_LIST && (t < 0 || t >= c.it.T)) {
+        atomicOr(p.status, kStListRange);
+        t = -1;
+      }
+      if (t >= 0) {
+        if (resid) {
+          pg = 0;
+        } else if (p.layout == DATTN_KV_PAGED_HND) {
+          const int blk = t / p.P;
+          if (blk < c.hi - c.lo) {
+            const int pi = p.page_indices[c.lo + blk];
+            if (pi >= 0 && pi < p.num_pages) pg = pi;
+            else atomicOr(p.status, kStPageRange);
+          } else {
+            atomicOr(p.status, kStBlockRange);
+          }
+          if (FMT == DATTN_FMT_INT4_KIVI && pg >= 0) {
+            const int gblk = (t / p.kivi_G) * p.kivi_G / p.P;
+            const int pi = p.page_indices[c.lo + gblk];
+            if (pi >= 0 && pi < p.num_pages) {
+              gpg = pi;
+            } else {
+              atomicOr(p.status, kStPageRange);
+              pg = -1;
+            }
+          }
+        } else {
+          if (c.crow >= 0 && t < p.T_cap) pg = c.crow;
+          else atomicOr(p.status, kStRowRange);
+        }
+        if (pg < 0) t = -1;
+      }
+    }
+    d.t[h] = t;
+    d.pg[h] = pg;
+    d.gpg[h] = gpg;
+  }
+  return d;
+}
+
+__device__ __forceinline__ int next_breaker_len(unsigned long long brk, int s) {
+  const unsigned long long rest = s < 63 ? brk >> (s + 1) : 0ull;
+  return rest ? __ffsll(static_cast<long long>(rest)) : 64 - s;
+}
+
+__device__ __forceinline__ unsigned long long ballot64(bool lo, bool hi) {
+  return static_cast<unsigned long long>(__ballot_sync(kAll, lo)) |
+         (static_cast<unsigned long long>(__ballot_sync(kAll, hi)) << 32);
+}
+
+__device__ __forceinline__ int rank_at(unsigned long long mask, int s) {   // set bits at or below s, minus one
+  return __popcll(static_cast<long long>(mask & ((2ull << s) - 1ull))) - 1;
+}
+
+template <int D, int FMT>
 __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int it_end, int lane) {
-  using L = Layout<D>;
-  int* pos_all = reinterpret_cast<int*>(smem + L::kPos);
-  int* cls_all = reinterpret_cast<int*>(smem + L::kCls);
-  const uint32_t full0 = smem_u32(smem + L::kFullBar);
-  const uint32_t empty0 = smem_u32(smem + L::kEmptyBar);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
-  const __nv_bfloat16* kbase = static_cast<const __nv_bfloat16*>(p.k);
-  const __nv_bfloat16* vbase = static_cast<const __nv_bfloat16*>(p.v);
+  using C = Cfg<D, FMT>;
+  const uint32_t full0 = smem_u32(smem + C::kFullBar);
+  const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
+  const uint8_t* kbase = static_cast<const uint8_t*>(p.k);
+  const uint8_t* vbase = static_cast<const uint8_t*>(p.v);
   const bool paged = p.layout == DATTN_KV_PAGED_HND;
   const bool listed = p.mask == DATTN_MASK_INDEX_LIST;
-  constexpr uint32_t kRowBytes = D * 2;
+  constexpr int kRowB = FMT == DATTN_FMT_BF16 ? D * 2 : FMT == DATTN_FMT_INT8_TOKEN ? D : D / 2;  // code row bytes
 
-  uint32_t k = 0;
-  for (int ii = it_begin; ii < it_end; ++ii) {
-    const WorkItem it = p.items[p.cta_items[ii]];
+  Cursor cur;
+  cur.ii = it_begin;
+  seek(p, cur, it_end, lane);
+  Desc dcur = describe<FMT>(p, cur, lane);
+  for (uint32_t k = 0; cur.valid; ++k) {
+    Cursor nxt = cur;
+    advance(p, nxt, it_end, lane);
+    const Desc dnxt = describe<FMT>(p, nxt, lane);      // loads in flight while we wait
+
+    const int st = k % C::kStagesN;
+    const uint32_t use = k / C::kStagesN;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) return;
+    uint8_t* stage = smem + st * C::kStage;
+    uint8_t* kt = stage;
+    uint8_t* vt = stage + C::kTile;
+    uint8_t* kq = stage + 2 * C::kTile;
+    uint8_t* vq = kq + C::kKQ;
+    int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
+    int* qsel = reinterpret_cast<int*>(smem + C::kQsel) + st * kTK;
+    const bool resid = cur.j0 >= cur.jq;
+    const WorkItem& it = cur.it;
+
+    // runs of consecutive keys in one page
+    const int t0 = dcur.t[0], t1 = dcur.t[1];
+    const int up0 = __shfl_up_sync(kAll, t0, 1), up1 = __shfl_up_sync(kAll, t1, 1);
+    const int last0 = __shfl_sync(kAll, t0, 31);
+    const int prev0 = lane ? up0 : -1, prev1 = lane ? up1 : last0;
+    const bool mergeable = paged && !resid;
+    const bool cont0 = mergeable && t0 >= 0 && prev0 >= 0 && t0 == prev0 + 1 && t0 % p.P != 0;
+    const bool cont1 = mergeable && t1 >= 0 && prev1 >= 0 && t1 == prev1 + 1 && t1 % p.P != 0;
+    const bool st0 = t0 >= 0 && !cont0, st1 = t1 >= 0 && !cont1;
+    const unsigned long long brk = ballot64(st0 || t0 < 0, st1 || t1 < 0);
+    const unsigned long long starts = ballot64(st0, st1);
+    const int nvalid = __popcll(static_cast<long long>(ballot64(t0 >= 0, t1 >= 0)));
+    const int len0 = st0 ? next_breaker_len(brk, lane) : 0;
+    const int len1 = st1 ? next_breaker_len(brk, lane + 32) : 0;
+    pos[lane] = t0;
+    pos[lane + 32] = t1;
+
+    uint32_t bytes = 0;
+    int qd0 = 0, qd1 = 0, qlo0 = 0, qlo1 = 0;
+    if (resid || FMT == DATTN_FMT_BF16) {
+      bytes = static_cast<uint32_t>(nvalid) * 2u * D * 2u;
+    } else if (FMT == DATTN_FMT_INT8_TOKEN) {
+      // qparam chunks [floor4(r0), ceil4(r0 + len)) packed by an exclusive scan in slot order
+      qlo0 = st0 ? (t0 % p.P) & ~3 : 0;
+      qlo1 = st1 ? (t1 % p.P) & ~3 : 0;
+      const int c0 = st0 ? (((t0 % p.P) + len0 + 3) & ~3) - qlo0 : 0;
+      const int c1 = st1 ? (((t1 % p.P) + len1 + 3) & ~3) - qlo1 : 0;
+      int inc0 = c0, inc1 = c1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(kAll, inc0, o), b = __shfl_up_sync(kAll, inc1, o);
+        if (lane >= o) inc0 += a, inc1 += b;
+      }
+      const int tot0 = __shfl_sync(kAll, inc0, 31), tot1 = __shfl_sync(kAll, inc1, 31);
+      qd0 = inc0 - c0;
+      qd1 = tot0 + inc1 - c1;
+      bytes = static_cast<uint32_t>(nvalid) * 2u * kRowB + 2u * 4u * (tot0 + tot1);
+      // every valid slot: entry of its row inside its run's chunk
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int s = lane + 32 * h, t = h ? t1 : t0;
+        const unsigned long long upto = starts & ((2ull << s) - 1ull);
+        const int ss = upto ? 63 - __clzll(static_cast<long long>(upto)) : 0;
+        const int dA = __shfl_sync(kAll, qd0, ss & 31), dB = __shfl_sync(kAll, qd1, ss & 31);
+        const int lA = __shfl_sync(kAll, qlo0, ss & 31), lB = __shfl_sync(kAll, qlo1, ss & 31);
+        if (t >= 0) qsel[s] = ((ss >> 5) ? dB : dA) + (t % p.P) - ((ss >> 5) ? lB : lA);
+      }
+    } else {  // KIVI quantized stage: one K-group qparam row per distinct group
+      const int g0 = t0 >= 0 ? t0 / p.kivi_G : -1, g1 = t1 >= 0 ? t1 / p.kivi_G : -1;
+      const int gu0 = __shfl_up_sync(kAll, g0, 1), gu1 = __shfl_up_sync(kAll, g1, 1);
+      const int gl0 = __shfl_sync(kAll, g0, 31);
+      const int gp0 = lane ? gu0 : -1, gp1 = lane ? gu1 : gl0;
+      const bool gs0 = g0 >= 0 && g0 != gp0, gs1 = g1 >= 0 && g1 != gp1;
+      const unsigned long long gst = ballot64(gs0, gs1);
+      const int ng = min(kMaxKGroups, __popcll(static_cast<long long>(gst)));
+      if (__popcll(static_cast<long long>(gst)) > kMaxKGroups && lane == 0) atomicOr(p.status, kStRowRange);
+      if (t0 >= 0) qsel[lane] = min(kMaxKGroups - 1, rank_at(gst, lane));
+      if (t1 >= 0) qsel[lane + 32] = min(kMaxKGroups - 1, rank_at(gst, lane + 32));
+      bytes = static_cast<uint32_t>(nvalid) * (2u * kRowB + (D / p.kivi_Gv) * 4u) + static_cast<uint32_t>(ng) * D * 4u;
+      qd0 = gs0 ? rank_at(gst, lane) : -1;
+      qd1 = gs1 ? rank_at(gst, lane + 32) : -1;
+    }
+
+    // stage class
+    int flags = resid ? kFlagResidual : 0;
+    bool full = true;
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
-    int list_n = 0;
-    bool list_ok = true;
     if (listed) {
-      const int g = it.b * p.H_kv + it.h;
-      list_n = p.index_indptr[g + 1] - p.index_indptr[g];
-      list_ok = p.index_indptr[g] == it.x0 && it.e <= list_n;
-      if (!list_ok && lane == 0) atomicOr(p.status, kStListRange);
-    }
-    int c_row = 0;
-    if (!paged) c_row = cache_row(p.cache_batch_idx, it.b, p.B_cache, lane == 0 ? p.status : nullptr);
-    for (int j0 = it.a; j0 < it.e; j0 += kTK, ++k) {
-      const int st = k % kStages;
-      const uint32_t use = k / kStages;
-      if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) return;
-      const int j1 = min(j0 + kTK, it.e);
-      const int n = j1 - j0;
-      int* pos = pos_all + st * kTK;
-      uint8_t* kt = smem + st * L::kStageBytes;
-      uint8_t* vt = kt + L::kTileBytes;
-
-      // pass 1: positions, validity and byte count
-      for (int s = lane; s < kTK; s += 32) {
-        int t = -1;
-        if (s < n && list_ok) {
-          t = stream_key(it, p.mask, p.index_list, j0 + s);
-          if (listed && (t < 0 || t >= it.T)) {
-            atomicOr(p.status, kStListRange);
-            t = -1;
-          }
-        }
-        pos[s] = t;
-      }
-      __syncwarp();
-      uint32_t bytes = 0;
-      if (paged && !listed) {
-        Run r0, r1;
-        const int nr = item_runs(it, j0, j1, r0, r1);
-        const int ns0 = nr > 0 ? run_segments(r0, p.P) : 0;
-        const int ns1 = nr > 1 ? run_segments(r1, p.P) : 0;
-        for (int sg = lane; sg < ns0 + ns1; sg += 32) {
-          int jb, sp0, sp1, slot;
-          segment(r0, r1, ns0, sg, p.P, jb, sp0, sp1, slot);
-          const int pi = page_of(p.page_indptr, p.page_indices, it.b, jb, p.num_pages, p.status);
-          if (pi < 0) {
-            for (int s = slot; s < slot + (sp1 - sp0); ++s) pos[s] = -1;
-          } else {
-            bytes += 2u * (sp1 - sp0) * kRowBytes;
-          }
-        }
-      } else {
-        for (int s = lane; s < n; s += 32) {
-          const int t = pos[s];
-          if (t < 0) continue;
-          bool ok;
-          if (paged) {
-            ok = page_of(p.page_indptr, p.page_indices, it.b, t / p.P, p.num_pages, p.status) >= 0;
-          } else {
-            ok = c_row >= 0 && t < p.T_cap;
-            if (!ok && c_row >= 0) atomicOr(p.status, kStRowRange);
-          }
-          if (ok) bytes += 2u * kRowBytes;
-          else pos[s] = -1;
-        }
-      }
-      bytes = __reduce_add_sync(kFull, bytes);
-
-      // stage class: FULL when every query row sees every key of the stage
-      if (lane == 0) {
-        bool full = true;
-        if (listed) {
-          full = n == 0 || pos[n - 1] < frontier(mc, 0);
-        } else {
-          Run r0, r1;
-          const int nr = item_runs(it, j0, j1, r0, r1);
-          for (int i = 0; i < p.S_q && full; ++i) {
-            if (nr > 0 && visible_in_run(mc, i, r0.p0, r0.p1) != r0.p1 - r0.p0) full = false;
-            if (nr > 1 && visible_in_run(mc, i, r1.p0, r1.p1) != r1.p1 - r1.p0) full = false;
-          }
-        }
-        cls_all[st] = full ? DATTN_TILE_FULL : DATTN_TILE_PARTIAL;
-      }
-      __syncwarp();
-      const uint32_t fb = full0 + 8 * st;
-      if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
-      __syncwarp();
-
-      // pass 2: issue the copies
-      if (paged && !listed) {
-        Run r0, r1;
-        const int nr = item_runs(it, j0, j1, r0, r1);
-        const int ns0 = nr > 0 ? run_segments(r0, p.P) : 0;
-        const int ns1 = nr > 1 ? run_segments(r1, p.P) : 0;
-        for (int sg = lane; sg < ns0 + ns1; sg += 32) {
-          int jb, sp0, sp1, slot;
-          segment(r0, r1, ns0, sg, p.P, jb, sp0, sp1, slot);
-          const int pi = page_of(p.page_indptr, p.page_indices, it.b, jb, p.num_pages, nullptr);
-          if (pi < 0) continue;
-          const long long off = paged_hnd_offset(pi, sp0 - jb * p.P, it.h, 0, p.P, p.H_kv, D);
-          const uint32_t nb = (sp1 - sp0) * kRowBytes;
-          bulk_g2s(smem_u32(kt + slot * kRowBytes), kbase + off, nb, fb);
-          bulk_g2s(smem_u32(vt + slot * kRowBytes), vbase + off, nb, fb);
-        }
-      } else {
-        for (int s = lane; s < n; s += 32) {
-          const int t = pos[s];
-          if (t < 0) continue;
-          long long off;
-          if (paged) {
-            const int pi = page_of(p.page_indptr, p.page_indices, it.b, t / p.P, p.num_pages, nullptr);
-            off = paged_hnd_offset(pi, t % p.P, it.h, 0, p.P, p.H_kv, D);
-          } else {
-            off = contig_nhd_offset(c_row, t, it.h, 0, p.T_cap, p.H_kv, D);
-          }
-          bulk_g2s(smem_u32(kt + s * kRowBytes), kbase + off, kRowBytes, fb);
-          bulk_g2s(smem_u32(vt + s * kRowBytes), vbase + off, kRowBytes, fb);
-        }
+      int mx = max(t0, t1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kAll, mx, o));
+      full = mx < frontier(mc, 0);
+    } else {
+      Run r0, r1;
+      const int nr = item_runs(it, cur.j0, cur.j1, r0, r1);
+      for (int i = 0; i < p.S_q && full; ++i) {
+        if (nr > 0 && visible_in_run(mc, i, r0.p0, r0.p1) != r0.p1 - r0.p0) full = false;
+        if (nr > 1 && visible_in_run(mc, i, r1.p0, r1.p1) != r1.p1 - r1.p0) full = false;
       }
     }
+    if (full) flags |= kFlagFull;
+    if (lane == 0) reinterpret_cast<int*>(smem + C::kFlags)[st] = flags;
+    __syncwarp();
+    const uint32_t fb = full0 + 8 * st;
+    if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+    __syncwarp();
+
+    // copies, one per run and tensor
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const bool is_start = h ? st1 : st0;
+      if (!is_start) continue;
+      const int s = lane + 32 * h;
+      const int t = h ? t1 : t0, pg = h ? dcur.pg[1] : dcur.pg[0];
+      const int len = h ? len1 : len0;
+      if (resid) {
+        const long long off = ((static_cast<long long>(it.b) * p.kivi_R + t % p.kivi_R) * p.H_kv + it.h) * D;
+        bulk_g2s(smem_u32(kt + s * D * 2), static_cast<const __nv_bfloat16*>(p.kres) + off, D * 2, fb);
+        bulk_g2s(smem_u32(vt + s * D * 2), static_cast<const __nv_bfloat16*>(p.vres) + off, D * 2, fb);
+        continue;
+      }
+      const long long row = paged ? (static_cast<long long>(pg) * p.H_kv + it.h) * p.P + t % p.P
+                                  : (static_cast<long long>(pg) * p.T_cap + t) * p.H_kv + it.h;
+      const uint32_t nb = static_cast<uint32_t>(len) * kRowB;
+      bulk_g2s(smem_u32(kt + s * kRowB), kbase + row * kRowB, nb, fb);
+      bulk_g2s(smem_u32(vt + s * kRowB), vbase + row * kRowB, nb, fb);
+      if (FMT == DATTN_FMT_INT8_TOKEN) {
+        const int qlo = h ? qlo1 : qlo0, qd = h ? qd1 : qd0;
+        const int cn = (((t % p.P) + len + 3) & ~3) - qlo;
+        const long long qrow = (static_cast<long long>(pg) * p.H_kv + it.h) * p.P + qlo;
+        bulk_g2s(smem_u32(kq + qd * 4), static_cast<const uint8_t*>(p.kqp) + qrow * 4, cn * 4, fb);
+        bulk_g2s(smem_u32(vq + qd * 4), static_cast<const uint8_t*>(p.vqp) + qrow * 4, cn * 4, fb);
+      }
+      if (FMT == DATTN_FMT_INT4_KIVI) {
+        const int vqb = (D / p.kivi_Gv) * 4;
+        bulk_g2s(smem_u32(vq + s * vqb), static_cast<const uint8_t*>(p.vqp) + row * vqb, len * vqb, fb);
+      }
+    }
+    if (FMT == DATTN_FMT_INT4_KIVI && !resid) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int gi = h ? qd1 : qd0;
+        if (gi < 0 || gi >= kMaxKGroups) continue;
+        const int t = h ? t1 : t0, gpg = h ? dcur.gpg[1] : dcur.gpg[0];
+        const int g0 = (t / p.kivi_G) * p.kivi_G;
+        const int slots = p.P >= p.kivi_G ? p.P / p.kivi_G : 1;
+        const int slot = p.P >= p.kivi_G ? (g0 % p.P) / p.kivi_G : 0;
+        const long long qrow = (static_cast<long long>(gpg) * p.H_kv + it.h) * slots + slot;
+        bulk_g2s(smem_u32(kq + gi * D * 4), static_cast<const uint8_t*>(p.kqp) + qrow * D * 4, D * 4, fb);
+      }
+    }
+    cur = nxt;
+    dcur = dnxt;
   }
 }
 
 // ---- consumers ---------------------------------------------------------------------
 
-template <int D>
+template <int D, int FMT>
 __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int it_end, int cw, int lane) {
-  using L = Layout<D>;
-  constexpr int NCH = D / 64;          // 8-channel chunks per lane
-  constexpr int NV = NCH * 4;          // float2 per row per lane
-  const int* pos_all = reinterpret_cast<const int*>(smem + L::kPos);
-  const int* cls_all = reinterpret_cast<const int*>(smem + L::kCls);
-  const uint32_t full0 = smem_u32(smem + L::kFullBar);
-  const uint32_t empty0 = smem_u32(smem + L::kEmptyBar);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
-  float* scratch = reinterpret_cast<float*>(smem + L::kScratch);
+  using C = Cfg<D, FMT>;
+  constexpr int NV = D / 16;             // float2 per row per lane
+  const uint32_t full0 = smem_u32(smem + C::kFullBar);
+  const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
+  float* scratch = reinterpret_cast<float*>(smem + C::kScratch);
 
   const int nrb = p.rows <= 4 ? 1 : p.rows <= 8 ? 2 : p.rows <= 16 ? 4 : 8;  // row blocks
   const int nts = kConsumerWarps / nrb;                                        // key slices
   const int rb = cw % nrb, ts = cw / nrb;
   const int keys_per_warp = kTK / nts;                                         // 8 * nrb
   const int tg = lane >> 3, j = lane & 7;
-  const int rr = j >> 1;                         // row (within block) this lane reduces to
+  const int rr = j >> 1;
   const int my_row = rb * 4 + rr;
-  const int my_qi = my_row / p.g;                // query index of that row
+  const int my_qi = my_row / p.g;
   const bool my_row_ok = my_row < p.rows;
+  const int vgroup = C::kI4 ? (D / 8) * j / p.kivi_Gv : 0;     // lane's V channel group (KIVI)
 
   uint32_t k = 0;
   bool dead = false;   // a bounded wait gave up: skip work but keep every named barrier
   for (int ii = it_begin; ii < it_end; ++ii) {
-    const WorkItem it = p.items[p.cta_items[ii]];
+    WorkItem it = p.items[p.cta_items[ii]];
+    if (p.mask == DATTN_MASK_INDEX_LIST) {       // mirror the producer's list check
+      const int g = it.b * p.H_kv + it.h;
+      const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
+      if (lo != it.x0 || it.e > n) it.e = it.a;
+    }
+    const int jq = residual_start(p, it);
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
 
-    // query rows of this block, pre-scaled by sm_scale * log2(e)
     float2 q[4][NV], o[4][NV];
+    float zacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int row = rb * 4 + r;
@@ -260,16 +463,16 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
       for (int x = 0; x < NV; ++x) o[r][x] = make_float2(0.f, 0.f);
       if (row < p.rows) {
         const int i = row / p.g, hq = it.h * p.g + row % p.g;
-        const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                         ((static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq) * D);
+        const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(p.q) +
+                                  ((static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq) * D;
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          const uint4 w = qp[c * 8 + j];
+        for (int x = 0; x < NV; x += 4) {
+          const uint4 w = *reinterpret_cast<const uint4*>(qp + C::chan(j, x));
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const float2 f = bf16x2_to_float2(ws[x]);
-            q[r][c * 4 + x] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+          for (int y = 0; y < 4; ++y) {
+            const float2 f = bf16x2_to_float2(ws[y]);
+            q[r][x + y] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
           }
         }
       } else {
@@ -277,19 +480,45 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
         for (int x = 0; x < NV; ++x) q[r][x] = make_float2(0.f, 0.f);
       }
     }
-    float m_run = -INFINITY, l_run = 0.f;
+    float qsum_my = 0.f;      // INT8: sum of the row's scaled query channels
+    if (C::kI8) {
+      float qs[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        float a = 0.f;
+#pragma unroll
+        for (int x = 0; x < NV; ++x) a += q[r][x].x + q[r][x].y;
+        a += __shfl_xor_sync(kAll, a, 1);
+        a += __shfl_xor_sync(kAll, a, 2);
+        a += __shfl_xor_sync(kAll, a, 4);
+        qs[r] = a;
+      }
+      qsum_my = rr == 0 ? qs[0] : rr == 1 ? qs[1] : rr == 2 ? qs[2] : qs[3];
+    }
+    float2 ks[NV], kz[NV];    // KIVI: per-channel K scale / offset of the current group
+    int cur_gid = -1;
+#pragma unroll
+    for (int x = 0; x < NV; ++x) ks[x] = kz[x] = make_float2(0.f, 0.f);
 
-    for (int j0 = it.a; j0 < it.e; j0 += kTK, ++k) {
-      const int st = k % kStages;
-      const uint32_t use = k / kStages;
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j0 = it.a; j0 < it.e; ++k) {
+      const int j1 = stage_end(it, j0, jq);
+      const int st = k % C::kStagesN;
+      const uint32_t use = k / C::kStagesN;
       if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
         dead = true;
         break;
       }
-      const int* pos = pos_all + st * kTK;
-      const bool stage_full = cls_all[st] == DATTN_TILE_FULL;
-      const uint8_t* kt = smem + st * L::kStageBytes;
-      const uint8_t* vt = kt + L::kTileBytes;
+      const uint8_t* stage = smem + st * C::kStage;
+      const uint8_t* kt = stage;
+      const uint8_t* vt = stage + C::kTile;
+      const uint8_t* kqs = stage + 2 * C::kTile;
+      const uint8_t* vqs = kqs + C::kKQ;
+      const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kTK;
+      const int* qsel = reinterpret_cast<const int*>(smem + C::kQsel) + st * kTK;
+      const int flags = reinterpret_cast<const int*>(smem + C::kFlags)[st];
+      const bool stage_full = flags & kFlagFull;
+      const bool resid = flags & kFlagResidual;
 
       for (int sub = 0; sub < nrb; ++sub) {
         float sv[2];
@@ -297,109 +526,189 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
         for (int pp = 0; pp < 2; ++pp) {
           const int slot = ts * keys_per_warp + sub * 8 + pp * 4 + tg;
           const int t = pos[slot];
-          const uint4* krow = reinterpret_cast<const uint4*>(kt + slot * D * 2);
           float2 acc[4];
 #pragma unroll
           for (int r = 0; r < 4; ++r) acc[r] = make_float2(0.f, 0.f);
+          if (FMT == DATTN_FMT_BF16 || resid) {
+            const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(kt) + slot * D;
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            const uint4 w = krow[c * 8 + j];
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            for (int x = 0; x < NV; x += 4) {
+              const uint4 w = *reinterpret_cast<const uint4*>(krow + C::chan(j, x));
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const float2 kf = bf16x2_to_float2(ws[x]);
+              for (int y = 0; y < 4; ++y) {
+                const float2 kf = bf16x2_to_float2(ws[y]);
 #pragma unroll
-              for (int r = 0; r < 4; ++r) acc[r] = __ffma2_rn(q[r][c * 4 + x], kf, acc[r]);
+                for (int r = 0; r < 4; ++r) acc[r] = __ffma2_rn(q[r][x + y], kf, acc[r]);
+              }
+            }
+          } else if (C::kI8) {
+            const uint8_t* krow = kt + slot * D + (D / 8) * j;
+#pragma unroll
+            for (int x = 0; x < NV; x += 2) {
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(krow + 2 * x);
+#pragma unroll
+              for (int y = 0; y < 2; ++y) {
+                const float2 kf = u8_pair(w, y);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[r] = __ffma2_rn(q[r][x + y], kf, acc[r]);
+              }
+            }
+          } else {  // KIVI quantized key: per-channel dequantisation inside the dot
+            if (t >= 0 && t / p.kivi_G != cur_gid) {
+              cur_gid = t / p.kivi_G;
+              const uint32_t* g = reinterpret_cast<const uint32_t*>(kqs + qsel[slot] * D * 4) + (D / 8) * j;
+#pragma unroll
+              for (int x = 0; x < NV; ++x) {
+                const float2 a = half2_to_float2(g[2 * x]), b = half2_to_float2(g[2 * x + 1]);
+                ks[x] = make_float2(a.x, b.x);
+                kz[x] = make_float2(a.y, b.y);
+              }
+            }
+            const uint8_t* krow = kt + slot * (D / 2) + (D / 16) * j;
+#pragma unroll
+            for (int x = 0; x < NV; x += 4) {
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(krow + x);   // 8 nibbles
+#pragma unroll
+              for (int y = 0; y < 4; ++y) {
+                const float2 kf = __ffma2_rn(u4_pair(w, y), ks[x + y], kz[x + y]);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[r] = __ffma2_rn(q[r][x + y], kf, acc[r]);
+              }
             }
           }
           float s[4];
 #pragma unroll
           for (int r = 0; r < 4; ++r) s[r] = acc[r].x + acc[r].y;
-          // 8-lane reduction: lane j ends with the full score of row j >> 1
+          // 8-lane reduction: lane j ends with the full dot product of row j >> 1
           const bool b2 = j & 4, b1 = j & 2;
           float k0 = b2 ? s[2] : s[0], k1 = b2 ? s[3] : s[1];
           const float x0 = b2 ? s[0] : s[2], x1 = b2 ? s[1] : s[3];
-          k0 += __shfl_xor_sync(kFull, x0, 4);
-          k1 += __shfl_xor_sync(kFull, x1, 4);
+          k0 += __shfl_xor_sync(kAll, x0, 4);
+          k1 += __shfl_xor_sync(kAll, x1, 4);
           float kk = b1 ? k1 : k0;
           const float xx = b1 ? k0 : k1;
-          kk += __shfl_xor_sync(kFull, xx, 2);
-          kk += __shfl_xor_sync(kFull, kk, 1);
+          kk += __shfl_xor_sync(kAll, xx, 2);
+          kk += __shfl_xor_sync(kAll, kk, 1);
+          if (C::kI8 && !resid && t >= 0) {         // per-token K scale outside the dot
+            const float2 sz = half2_to_float2(reinterpret_cast<const uint32_t*>(kqs)[qsel[slot]]);
+            kk = fmaf(sz.x, kk, sz.y * qsum_my);
+          }
           bool vis = t >= 0 && my_row_ok;
           if (vis && !stage_full) vis = key_visible(mc, my_qi, t);
           sv[pp] = vis ? kk : -INFINITY;
         }
         // online softmax update for this lane's row over 8 keys of the warp
         float mx = fmaxf(sv[0], sv[1]);
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 16));
         const float m_new = fmaxf(m_run, mx);
         const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
         const float p0 = sv[0] == -INFINITY ? 0.f : exp2f(sv[0] - m_new);
         const float p1 = sv[1] == -INFINITY ? 0.f : exp2f(sv[1] - m_new);
         l_run = l_run * alpha + p0 + p1;
         m_run = m_new;
-        if (__any_sync(kFull, alpha != 1.f)) {
+        if (__any_sync(kAll, alpha != 1.f)) {
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
-            const float a = __shfl_sync(kFull, alpha, 2 * r);
+            const float a = __shfl_sync(kAll, alpha, 2 * r);
             const float2 a2 = make_float2(a, a);
 #pragma unroll
             for (int x = 0; x < NV; ++x) o[r][x] = __fmul2_rn(o[r][x], a2);
+            zacc[r] *= a;
           }
         }
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
           const int slot = ts * keys_per_warp + sub * 8 + pp * 4 + tg;
           const float pv = pp ? p1 : p0;
-          float2 pr[4];
+          float pr[4];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const float a = __shfl_sync(kFull, pv, tg * 8 + 2 * r);
-            pr[r] = make_float2(a, a);
-          }
-          const uint4* vrow = reinterpret_cast<const uint4*>(vt + slot * D * 2);
+          for (int r = 0; r < 4; ++r) pr[r] = __shfl_sync(kAll, pv, tg * 8 + 2 * r);
+          if (FMT == DATTN_FMT_BF16 || resid) {
+            const __nv_bfloat16* vrow = reinterpret_cast<const __nv_bfloat16*>(vt) + slot * D;
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            const uint4 w = vrow[c * 8 + j];
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            for (int x = 0; x < NV; x += 4) {
+              const uint4 w = *reinterpret_cast<const uint4*>(vrow + C::chan(j, x));
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const float2 vf = bf16x2_to_float2(ws[x]);
+              for (int y = 0; y < 4; ++y) {
+                const float2 vf = bf16x2_to_float2(ws[y]);
 #pragma unroll
-              for (int r = 0; r < 4; ++r) o[r][c * 4 + x] = __ffma2_rn(pr[r], vf, o[r][c * 4 + x]);
+                for (int r = 0; r < 4; ++r) o[r][x + y] = __ffma2_rn(make_float2(pr[r], pr[r]), vf, o[r][x + y]);
+              }
+            }
+          } else {
+            // per-token V scale folded into the probability, offset into a per-row sum
+            float2 sz = make_float2(0.f, 0.f);
+            if (pos[slot] >= 0) {
+              if (C::kI8) sz = half2_to_float2(reinterpret_cast<const uint32_t*>(vqs)[qsel[slot]]);
+              else sz = half2_to_float2(reinterpret_cast<const uint32_t*>(vqs)[slot * (D / p.kivi_Gv) + vgroup]);
+            }
+            float2 ps[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              ps[r] = make_float2(pr[r] * sz.x, pr[r] * sz.x);
+              zacc[r] = fmaf(pr[r], sz.y, zacc[r]);
+            }
+            if (C::kI8) {
+              const uint8_t* vrow = vt + slot * D + (D / 8) * j;
+#pragma unroll
+              for (int x = 0; x < NV; x += 2) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(vrow + 2 * x);
+#pragma unroll
+                for (int y = 0; y < 2; ++y) {
+                  const float2 vf = u8_pair(w, y);
+#pragma unroll
+                  for (int r = 0; r < 4; ++r) o[r][x + y] = __ffma2_rn(ps[r], vf, o[r][x + y]);
+                }
+              }
+            } else {
+              const uint8_t* vrow = vt + slot * (D / 2) + (D / 16) * j;
+#pragma unroll
+              for (int x = 0; x < NV; x += 4) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(vrow + x);
+#pragma unroll
+                for (int y = 0; y < 4; ++y) {
+                  const float2 vf = u4_pair(w, y);
+#pragma unroll
+                  for (int r = 0; r < 4; ++r) o[r][x + y] = __ffma2_rn(ps[r], vf, o[r][x + y]);
+                }
+              }
             }
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      j0 = j1;
     }
 
     // ---- end of item: reduce over the 4 key groups, then across warps ----
-    l_run += __shfl_xor_sync(kFull, l_run, 8);
-    l_run += __shfl_xor_sync(kFull, l_run, 16);
+    l_run += __shfl_xor_sync(kAll, l_run, 8);
+    l_run += __shfl_xor_sync(kAll, l_run, 16);
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < 4; ++r) {
+      zacc[r] += __shfl_xor_sync(kAll, zacc[r], 8);
+      zacc[r] += __shfl_xor_sync(kAll, zacc[r], 16);
 #pragma unroll
       for (int x = 0; x < NV; ++x) {
-        o[r][x].x += __shfl_xor_sync(kFull, o[r][x].x, 8);
-        o[r][x].y += __shfl_xor_sync(kFull, o[r][x].y, 8);
-        o[r][x].x += __shfl_xor_sync(kFull, o[r][x].x, 16);
-        o[r][x].y += __shfl_xor_sync(kFull, o[r][x].y, 16);
+        o[r][x].x += __shfl_xor_sync(kAll, o[r][x].x, 8);
+        o[r][x].y += __shfl_xor_sync(kAll, o[r][x].y, 8);
+        o[r][x].x += __shfl_xor_sync(kAll, o[r][x].x, 16);
+        o[r][x].y += __shfl_xor_sync(kAll, o[r][x].y, 16);
       }
-    float* mine = scratch + cw * (L::kScratchWarp / 4);
+    }
+    float* mine = scratch + cw * (C::kScratchWarp / 4);
     if (tg == 0) {
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int dim = c * 64 + j * 8 + 2 * x;
-            mine[r * D + dim] = o[r][c * 4 + x].x;
-            mine[r * D + dim + 1] = o[r][c * 4 + x].y;
-          }
+        for (int x = 0; x < NV; ++x) {
+          const int dim = C::chan(j, x);
+          mine[r * D + dim] = o[r][x].x + zacc[r];
+          mine[r * D + dim + 1] = o[r][x].y + zacc[r];
+        }
       if ((j & 1) == 0) {
         mine[4 * D + 2 * rr] = m_run;
         mine[4 * D + 2 * rr + 1] = l_run;
@@ -415,13 +724,13 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
       if (row >= p.rows) continue;
       float M = -INFINITY;
       for (int s2 = 0; s2 < nts; ++s2) {
-        const float* w = scratch + (b_of + nrb * s2) * (L::kScratchWarp / 4);
+        const float* w = scratch + (b_of + nrb * s2) * (C::kScratchWarp / 4);
         M = fmaxf(M, w[4 * D + 2 * r_of]);
       }
       float Lsum = 0.f, U = 0.f;
       if (M != -INFINITY) {
         for (int s2 = 0; s2 < nts; ++s2) {
-          const float* w = scratch + (b_of + nrb * s2) * (L::kScratchWarp / 4);
+          const float* w = scratch + (b_of + nrb * s2) * (C::kScratchWarp / 4);
           const float mw = w[4 * D + 2 * r_of];
           if (mw == -INFINITY) continue;
           const float a = exp2f(mw - M);
@@ -446,19 +755,19 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_constant__ PartialParams p) {
-  using L = Layout<D>;
+template <int D, int FMT>
+__global__ void __launch_bounds__(kThreads, 1) partial_kernel(const __grid_constant__ PartialParams p) {
+  using C = Cfg<D, FMT>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  // zero the K/V ring so that slots never written hold finite values
-  for (int i = threadIdx.x; i < kStages * L::kStageBytes / 16; i += blockDim.x)
+  // zero the ring so that slots never written hold finite values
+  for (int i = threadIdx.x; i < C::kStagesN * C::kStage / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(smem + L::kFullBar + 8 * s), 1);
-      mbar_init(smem_u32(smem + L::kEmptyBar + 8 * s), kConsumerWarps);
+    for (int s = 0; s < C::kStagesN; ++s) {
+      mbar_init(smem_u32(smem + C::kFullBar + 8 * s), 1);
+      mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), kConsumerWarps);
     }
-    *reinterpret_cast<int*>(smem + L::kAbort) = 0;
+    *reinterpret_cast<int*>(smem + C::kAbort) = 0;
     fence_barrier_init();
   }
   fence_proxy_async_smem();
@@ -466,32 +775,44 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == kConsumerWarps) {
-    produce<D>(p, smem, it_begin, it_end, lane);
+    produce<D, FMT>(p, smem, it_begin, it_end, lane);
   } else {
-    consume<D>(p, smem, it_begin, it_end, warp, lane);
+    consume<D, FMT>(p, smem, it_begin, it_end, warp, lane);
   }
+}
+
+template <int D, int FMT>
+int launch_one(const PartialParams& p, int n_ctas, void* stream) {
+  const size_t smem = Cfg<D, FMT>::kTotal;
+  cudaError_t err = cudaFuncSetAttribute(partial_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  partial_kernel<D, FMT><<<n_ctas, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t partial_smem_bytes(int d, int fmt) {
-  (void)fmt;
-  return d == 64 ? Layout<64>::kTotal : Layout<128>::kTotal;
+  if (d == 64) {
+    return fmt == DATTN_FMT_BF16 ? Cfg<64, DATTN_FMT_BF16>::kTotal
+           : fmt == DATTN_FMT_INT8_TOKEN ? Cfg<64, DATTN_FMT_INT8_TOKEN>::kTotal
+                                         : Cfg<64, DATTN_FMT_INT4_KIVI>::kTotal;
+  }
+  return fmt == DATTN_FMT_BF16 ? Cfg<128, DATTN_FMT_BF16>::kTotal
+         : fmt == DATTN_FMT_INT8_TOKEN ? Cfg<128, DATTN_FMT_INT8_TOKEN>::kTotal
+                                       : Cfg<128, DATTN_FMT_INT4_KIVI>::kTotal;
 }
 
 int launch_partial(const PartialParams& p, int d, int n_ctas, void* stream) {
-  const size_t smem = partial_smem_bytes(d, p.fmt);
-  cudaError_t err;
   if (d == 64) {
-    err = cudaFuncSetAttribute(partial_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    partial_bf16_kernel<64><<<n_ctas, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
-  } else {
-    err = cudaFuncSetAttribute(partial_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    partial_bf16_kernel<128><<<n_ctas, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+    if (p.fmt == DATTN_FMT_BF16) return launch_one<64, DATTN_FMT_BF16>(p, n_ctas, stream);
+    if (p.fmt == DATTN_FMT_INT8_TOKEN) return launch_one<64, DATTN_FMT_INT8_TOKEN>(p, n_ctas, stream);
+    return launch_one<64, DATTN_FMT_INT4_KIVI>(p, n_ctas, stream);
   }
-  return cudaGetLastError();
+  if (p.fmt == DATTN_FMT_BF16) return launch_one<128, DATTN_FMT_BF16>(p, n_ctas, stream);
+  if (p.fmt == DATTN_FMT_INT8_TOKEN) return launch_one<128, DATTN_FMT_INT8_TOKEN>(p, n_ctas, stream);
+  return launch_one<128, DATTN_FMT_INT4_KIVI>(p, n_ctas, stream);
 }
 
 }  // namespace dattn

@@ -67,11 +67,14 @@ void check_problem(const dattn_problem* p, Checker& c) {
     if (p->T_cap < 1) c.fail(DATTN_EINVAL, "contiguous layout needs T_cap >= 1");
     if (p->B_cache < 1) c.fail(DATTN_EINVAL, "contiguous layout needs B_cache >= 1");
   }
+  if (p->fmt == DATTN_FMT_INT8_TOKEN && p->page_size >= 1 && (p->page_size % 4 || p->page_size > 256))
+    c.fail(DATTN_EUNSUPPORTED, "INT8 pages must hold a multiple of 4 rows, at most 256");
   if (p->fmt == DATTN_FMT_INT4_KIVI) {
     const int G = p->kivi_group, Gv = p->kivi_v_group, R = p->kivi_residual;
-    if (G != 16 && G != 32 && G != 64) c.fail(DATTN_EUNSUPPORTED, "kivi_group must be 16, 32 or 64");
-    if (Gv != 16 && Gv != 32 && Gv != 64 && Gv != 128) c.fail(DATTN_EUNSUPPORTED, "kivi_v_group must be 16, 32, 64 or 128");
-    else if (Gv > p->d_h) c.fail(DATTN_EINVAL, "kivi_v_group must divide d_h");
+    if (G != 32 && G != 64) c.fail(DATTN_EUNSUPPORTED, "kivi_group must be 32 or 64");
+    if (Gv != 16 && Gv != 32 && Gv != 64) c.fail(DATTN_EUNSUPPORTED, "kivi_v_group must be 16, 32 or 64");
+    else if (4 * Gv > p->d_h) c.fail(DATTN_EUNSUPPORTED, "kivi_v_group must be at most d_h / 4");
+    if (p->mask == DATTN_MASK_INDEX_LIST) c.fail(DATTN_EUNSUPPORTED, "INT4 KIVI reads causal or sink+window streams");
     if (G >= 1 && (R < G || R % G)) c.fail(DATTN_EINVAL, "kivi_residual must be a positive multiple of kivi_group");
     if (G >= 1 && p->page_size >= 1 && p->page_size % G && G % p->page_size)
       c.fail(DATTN_EUNSUPPORTED, "page_size and kivi_group must divide one another");

@@ -85,7 +85,8 @@ def append_history(w, fmt, cuts_per_request):
 
 def oracle_written(w, fmt):
     p = w.problem
-    c = ocache.empty_paged(fmt, p["num_pages"], p["H_kv"], p["P"], p["d"], p["B"])
+    c = ocache.empty_paged(fmt, p["num_pages"], p["H_kv"], p["P"], p["d"], p["B"], G=p["kivi_group"],
+                           Gv=p["kivi_v_group"], R=p["kivi_residual"])
     ocache.write_history(c, w.page_indptr.numpy(), w.page_indices.numpy(), w.rows_indptr.numpy(),
                          bits(w.k_rows), bits(w.v_rows))
     return c
@@ -143,6 +144,7 @@ def test_kivi_append_groups_residual_bit_exact(d, P):
     w = W.quantized_history("kivi", B=len(lens), S_q=1, H_q=8, H_kv=2, d=d, lens=lens, P=P, seed=13,
                             device="cuda", fmt="int4_kivi",
                             pool_pages=sum(-(-t // P) for t in lens) + 3)
+    w.problem["kivi_v_group"] = min(32, d // 4)
     p, cache = append_history(w, "int4_kivi", _cuts(lens, np.random.default_rng(2)))
     ref = oracle_written(w, "int4_kivi")
     got = {n: cache[n].cpu() for n in ("k", "v", "k_qparams", "v_qparams")}

@@ -1,0 +1,113 @@
+"""GPU parity of decode over INT8 and KIVI-INT4 caches (M8.6 §0x03, §0x05B, §0x06B-C).
+
+The GPU cache is written by kv_append; the oracle writes its own cache from
+the same bf16 history with its own quantiser and dequantises it in float64.
+(The two sets of codes are bit-identical by test_gpu_append, but nothing here
+relies on it: the comparison is between two independent pipelines.)
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import split_kv_decode_flash_gb300 as dattn
+import workloads as W
+from oracle import attention
+from oracle import cache as ocache
+from tests import gpu_helpers as H
+from tests.test_gpu_append import append_history
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dattn.load()
+
+
+def _oracle_cache(w, fmt, requests=None):
+    """Oracle cache for ``requests`` (all when None); other requests stay empty."""
+    p = w.problem
+    c = ocache.empty_paged(fmt, p["num_pages"], p["H_kv"], p["P"], p["d"], p["B"], G=p["kivi_group"],
+                           Gv=p["kivi_v_group"], R=p["kivi_residual"])
+    ri = w.rows_indptr.numpy().astype(np.int64)
+    lens = w.kv_len.numpy().astype(np.int64)
+    if requests is None:
+        return ocache.write_history(c, w.page_indptr.numpy(), w.page_indices.numpy(), ri,
+                                    H.bits(w.k_rows), H.bits(w.v_rows))
+    keep = np.zeros(p["B"], bool)
+    keep[list(requests)] = True
+    sub_len = np.where(keep, lens, 0)
+    sub_ptr = np.concatenate([[0], np.cumsum(sub_len)])
+    rows = np.concatenate([np.arange(ri[b], ri[b + 1]) for b in range(p["B"]) if keep[b]])
+    k = H.bits(w.k_rows[torch.as_tensor(rows, device=w.k_rows.device)])
+    v = H.bits(w.v_rows[torch.as_tensor(rows, device=w.v_rows.device)])
+    ocache.write_history(c, w.page_indptr.numpy(), w.page_indices.numpy(), sub_ptr, k, v)
+    c.kv_len = lens
+    return c
+
+
+def _run(w, fmt, p, cache, **plan_kw):
+    B, S_q, H_q, d = p["B"], p["S_q"], p["H_q"], p["d"]
+    plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, **plan_kw)
+    o = torch.full((B, S_q, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, S_q, H_q), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    t = dattn.tensors_from(q=w.q.cuda(), o=o, lse=lse, **cache)
+    dattn.dattn_run(plan, p, t, ws)
+    torch.cuda.synchronize()
+    assert dattn.dattn_device_status(ws) == 0
+    return o.float().cpu(), lse.cpu(), plan.info
+
+
+def _compare(O, L, w, p, cache_ref, rows):
+    w2 = W.Workload(w.name, p, w.q, w.kv_len)
+    return H.compare(O, L, w2, rows, cache=cache_ref)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4_kivi"])
+@pytest.mark.parametrize("chunk,num_sms", [(0, 152), (64, 5)])
+def test_quantized_decode_small_all_rows(fmt, chunk, num_sms):
+    lens = [700, 129, 128, 161, 40, 1]
+    w = W.quantized_history("q", B=len(lens), S_q=1, H_q=32, H_kv=8, d=128, lens=lens, P=16, seed=21,
+                            device="cuda", fmt=fmt, pool_pages=sum(-(-t // 16) for t in lens) + 2)
+    p, cache = append_history(w, fmt, [[] for _ in lens])
+    O, L, info, = _run(w, fmt, p, cache, chunk_tokens=chunk, num_sms=num_sms)[:3]
+    ref = _oracle_cache(w, fmt)
+    _compare(O, L, w, p, ref, H.all_rows(p))
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4_kivi"])
+def test_quantized_decode_d64_multi_row_sink_window(fmt):
+    lens = [500, 90]
+    w = W.quantized_history("q64", B=2, S_q=2, H_q=8, H_kv=2, d=64, lens=lens, P=16, seed=22, device="cuda",
+                            fmt=fmt, pool_pages=40)
+    p = dict(w.problem, mask="sink_window", n_sink=3, window=200, kivi_v_group=16)
+    w.problem = p
+    p, cache = append_history(w, fmt, [[100, 300], [60]])
+    O, L, info = _run(w, fmt, p, cache, chunk_tokens=64, num_sms=3)
+    _compare(O, L, w, p, _oracle_cache(w, fmt), H.all_rows(p))
+
+
+def test_int4_kivi_verify_rows_cross_the_residual_boundary():
+    lens = [300, 4]
+    w = W.quantized_history("q4", B=2, S_q=4, H_q=16, H_kv=2, d=128, lens=lens, P=16, seed=23, device="cuda",
+                            fmt="int4_kivi", pool_pages=25)
+    p, cache = append_history(w, "int4_kivi", [[150], [2]])
+    O, L, info = _run(w, "int4_kivi", p, cache, chunk_tokens=64, num_sms=2)
+    _compare(O, L, w, p, _oracle_cache(w, "int4_kivi"), H.all_rows(p))
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4_kivi"])
+def test_quantized_full_size_sampled(fmt):
+    """B=32, T ~ U[2048, 32768], K outlier channels: the full quantized workload."""
+    w = W.quantized("cuda", fmt=fmt)
+    p, cache = append_history(w, fmt, [[] for _ in range(w.problem["B"])])
+    O, L, info = _run(w, fmt, p, cache)
+    H.finite_or_masked(O, L)
+    rng = np.random.default_rng(7)
+    reqs = sorted(rng.choice(p["B"], size=4, replace=False).tolist())
+    rows = [(b, 0, h) for b in reqs for h in rng.choice(p["H_q"], size=6, replace=False).tolist()]
+    _compare(O, L, w, p, _oracle_cache(w, fmt, reqs), rows)
