@@ -626,6 +626,8 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
 #pragma unroll
           for (int r = 0; r < 4; ++r) pr[r] = __shfl_sync(kAll, pv, tg * 8 + 2 * r);
           if (FMT == DATTN_FMT_BF16 || resid) {
+            // a KIVI residual stage may hold stale code bytes (not bf16) in its unused slots
+            if (C::kI4 && pos[slot] < 0) continue;
             const __nv_bfloat16* vrow = reinterpret_cast<const __nv_bfloat16*>(vt) + slot * D;
 #pragma unroll
             for (int x = 0; x < NV; x += 4) {
