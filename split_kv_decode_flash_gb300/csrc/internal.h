@@ -13,8 +13,10 @@ namespace dattn {
 // ---- kernel geometry ---------------------------------------------------------------
 constexpr int kTK = 64;              // keys per pipeline stage
 constexpr int kStages = 4;           // shared-memory ring depth
-constexpr int kConsumerWarps = 8;    // warps that compute; one more warp produces
-constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kConsumerWarps = 8;    // two warpgroups that compute
+constexpr int kThreads = 32 * (kConsumerWarps + 4);   // + one producer warpgroup (one active warp)
+constexpr int kProducerRegs = 56;    // setmaxnreg split of the launch's register file:
+constexpr int kConsumerRegs = 224;   // 128 * 56 + 256 * 224 = 64512 = 384 threads * 168
 constexpr int kMaxRows = 32;         // g * S_q rows per (request, kv head) group
 constexpr int kDefaultCtasPerSm = 1;
 constexpr int kWsAlign = 256;

@@ -776,18 +776,28 @@ __global__ void __launch_bounds__(kThreads, 1) partial_kernel(const __grid_const
   __syncthreads();
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == kConsumerWarps) {
-    produce<D, FMT>(p, smem, it_begin, it_end, lane);
-  } else {
-    consume<D, FMT>(p, smem, it_begin, it_end, warp, lane);
+  if (warp >= kConsumerWarps) {
+    // the producer warpgroup hands registers to the consumers; one warp produces
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    if (warp == kConsumerWarps) produce<D, FMT>(p, smem, it_begin, it_end, lane);
+    return;
   }
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+  consume<D, FMT>(p, smem, it_begin, it_end, warp, lane);
 }
 
 template <int D, int FMT>
 int launch_one(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Cfg<D, FMT>::kTotal;
-  cudaError_t err = cudaFuncSetAttribute(partial_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  // The consumers' setmaxnreg.inc waits for registers released by the producer
+  // warpgroup; it can only complete if the launch holds enough of them.
+  cudaFuncAttributes attr;
+  cudaError_t err = cudaFuncGetAttributes(&attr, partial_kernel<D, FMT>);
+  if (err != cudaSuccess) return err;
+  if (attr.numRegs * kThreads < 128 * kProducerRegs + 32 * kConsumerWarps * kConsumerRegs)
+    return cudaErrorInvalidConfiguration;
+  err = cudaFuncSetAttribute(partial_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   partial_kernel<D, FMT><<<n_ctas, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError();
