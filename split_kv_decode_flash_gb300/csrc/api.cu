@@ -67,6 +67,11 @@ void fill_common(const dattn_problem& p, const dattn_tensors& t, PartialParams& 
   k.fmt = p.fmt;
   k.mask = p.mask;
   k.P = p.page_size;
+  k.P_shift = -1;
+  if (p.page_size > 0 && (p.page_size & (p.page_size - 1)) == 0) {
+    k.P_shift = 0;
+    while ((1 << k.P_shift) < p.page_size) ++k.P_shift;
+  }
   k.num_pages = p.num_pages;
   k.T_cap = p.T_cap;
   k.B_cache = p.B_cache;

@@ -14,7 +14,8 @@ namespace dattn {
 constexpr int kTK = 64;              // keys per pipeline stage
 constexpr int kStages = 4;           // shared-memory ring depth
 constexpr int kConsumerWarps = 8;    // two warpgroups that compute
-constexpr int kThreads = 32 * (kConsumerWarps + 4);   // + one producer warpgroup (one active warp)
+constexpr int kProducerWarps = 4;    // one warpgroup that fills the ring, a stage per warp in turn
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr int kProducerRegs = 56;    // setmaxnreg split of the launch's register file:
 constexpr int kConsumerRegs = 224;   // 128 * 56 + 256 * 224 = 64512 = 384 threads * 168
 constexpr int kMaxRows = 32;         // g * S_q rows per (request, kv head) group
@@ -78,6 +79,7 @@ struct PartialParams {
   int32_t B, S_q, H_q, H_kv, g, rows;
   int32_t layout, fmt, mask, P, num_pages, T_cap, B_cache;
   int32_t n_sink, window, kivi_G, kivi_Gv, kivi_R;
+  int32_t P_shift;       // log2(P) when P is a power of two, else -1
   float scale_log2;      // sm_scale * log2(e)
 };
 

@@ -125,6 +125,12 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
+// Logical block and page row of key t (shifts when P is a power of two).
+__device__ __forceinline__ int blk_of(const PartialParams& p, int t) { return p.P_shift >= 0 ? t >> p.P_shift : t / p.P; }
+__device__ __forceinline__ int row_of(const PartialParams& p, int t) {
+  return p.P_shift >= 0 ? t & (p.P - 1) : t % p.P;
+}
+
 // ---- producer ---------------------------------------------------------------------
 
 struct Cursor {
@@ -170,6 +176,7 @@ __device__ __forceinline__ void seek(const PartialParams& p, Cursor& c, int it_e
 }
 
 __device__ __forceinline__ void advance(const PartialParams& p, Cursor& c, int it_end, int lane) {
+  if (!c.valid) return;
   if (c.j1 < c.it.e) {
     c.j0 = c.j1;
     c.j1 = stage_end(c.it, c.j0, c.jq);
@@ -204,7 +211,7 @@ __device__ __forceinline__ Desc describe(const PartialParams& p, const Cursor& c
         if (resid) {
           pg = 0;
         } else if (p.layout == DATTN_KV_PAGED_HND) {
-          const int blk = t / p.P;
+          const int blk = blk_of(p, t);
           if (blk < c.hi - c.lo) {
             const int pi = p.page_indices[c.lo + blk];
             if (pi >= 0 && pi < p.num_pages) pg = pi;
@@ -213,7 +220,7 @@ __device__ __forceinline__ Desc describe(const PartialParams& p, const Cursor& c
             atomicOr(p.status, kStBlockRange);
           }
           if (FMT == DATTN_FMT_INT4_KIVI && pg >= 0) {
-            const int gblk = (t / p.kivi_G) * p.kivi_G / p.P;
+            const int gblk = blk_of(p, (t / p.kivi_G) * p.kivi_G);
             const int pi = p.page_indices[c.lo + gblk];
             if (pi >= 0 && pi < p.num_pages) {
               gpg = pi;
@@ -251,7 +258,7 @@ __device__ __forceinline__ int rank_at(unsigned long long mask, int s) {   // se
 }
 
 template <int D, int FMT>
-__device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int it_end, int lane) {
+__device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int it_end, int lane, int pw) {
   using C = Cfg<D, FMT>;
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
   const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
@@ -262,13 +269,15 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
   const bool listed = p.mask == DATTN_MASK_INDEX_LIST;
   constexpr int kRowB = FMT == DATTN_FMT_BF16 ? D * 2 : FMT == DATTN_FMT_INT8_TOKEN ? D : D / 2;  // code row bytes
 
+  // producer warp pw fills stages pw, pw + kProducerWarps, ... of the CTA's stage sequence
   Cursor cur;
   cur.ii = it_begin;
   seek(p, cur, it_end, lane);
+  for (int i = 0; i < pw; ++i) advance(p, cur, it_end, lane);
   Desc dcur = describe<FMT>(p, cur, lane);
-  for (uint32_t k = 0; cur.valid; ++k) {
+  for (uint32_t k = pw; cur.valid; k += kProducerWarps) {
     Cursor nxt = cur;
-    advance(p, nxt, it_end, lane);
+    for (int i = 0; i < kProducerWarps; ++i) advance(p, nxt, it_end, lane);
     const Desc dnxt = describe<FMT>(p, nxt, lane);      // loads in flight while we wait
 
     const int st = k % C::kStagesN;
@@ -290,8 +299,8 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
     const int last0 = __shfl_sync(kAll, t0, 31);
     const int prev0 = lane ? up0 : -1, prev1 = lane ? up1 : last0;
     const bool mergeable = paged && !resid;
-    const bool cont0 = mergeable && t0 >= 0 && prev0 >= 0 && t0 == prev0 + 1 && t0 % p.P != 0;
-    const bool cont1 = mergeable && t1 >= 0 && prev1 >= 0 && t1 == prev1 + 1 && t1 % p.P != 0;
+    const bool cont0 = mergeable && t0 >= 0 && prev0 >= 0 && t0 == prev0 + 1 && row_of(p, t0) != 0;
+    const bool cont1 = mergeable && t1 >= 0 && prev1 >= 0 && t1 == prev1 + 1 && row_of(p, t1) != 0;
     const bool st0 = t0 >= 0 && !cont0, st1 = t1 >= 0 && !cont1;
     const unsigned long long brk = ballot64(st0 || t0 < 0, st1 || t1 < 0);
     const unsigned long long starts = ballot64(st0, st1);
@@ -307,10 +316,10 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
       bytes = static_cast<uint32_t>(nvalid) * 2u * D * 2u;
     } else if (FMT == DATTN_FMT_INT8_TOKEN) {
       // qparam chunks [floor4(r0), ceil4(r0 + len)) packed by an exclusive scan in slot order
-      qlo0 = st0 ? (t0 % p.P) & ~3 : 0;
-      qlo1 = st1 ? (t1 % p.P) & ~3 : 0;
-      const int c0 = st0 ? (((t0 % p.P) + len0 + 3) & ~3) - qlo0 : 0;
-      const int c1 = st1 ? (((t1 % p.P) + len1 + 3) & ~3) - qlo1 : 0;
+      qlo0 = st0 ? row_of(p, t0) & ~3 : 0;
+      qlo1 = st1 ? row_of(p, t1) & ~3 : 0;
+      const int c0 = st0 ? ((row_of(p, t0) + len0 + 3) & ~3) - qlo0 : 0;
+      const int c1 = st1 ? ((row_of(p, t1) + len1 + 3) & ~3) - qlo1 : 0;
       int inc0 = c0, inc1 = c1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -329,7 +338,7 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
         const int ss = upto ? 63 - __clzll(static_cast<long long>(upto)) : 0;
         const int dA = __shfl_sync(kAll, qd0, ss & 31), dB = __shfl_sync(kAll, qd1, ss & 31);
         const int lA = __shfl_sync(kAll, qlo0, ss & 31), lB = __shfl_sync(kAll, qlo1, ss & 31);
-        if (t >= 0) qsel[s] = ((ss >> 5) ? dB : dA) + (t % p.P) - ((ss >> 5) ? lB : lA);
+        if (t >= 0) qsel[s] = ((ss >> 5) ? dB : dA) + row_of(p, t) - ((ss >> 5) ? lB : lA);
       }
     } else {  // KIVI quantized stage: one K-group qparam row per distinct group
       const int g0 = t0 >= 0 ? t0 / p.kivi_G : -1, g1 = t1 >= 0 ? t1 / p.kivi_G : -1;
@@ -385,14 +394,14 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
         bulk_g2s(smem_u32(vt + s * D * 2), static_cast<const __nv_bfloat16*>(p.vres) + off, D * 2, fb);
         continue;
       }
-      const long long row = paged ? (static_cast<long long>(pg) * p.H_kv + it.h) * p.P + t % p.P
+      const long long row = paged ? (static_cast<long long>(pg) * p.H_kv + it.h) * p.P + row_of(p, t)
                                   : (static_cast<long long>(pg) * p.T_cap + t) * p.H_kv + it.h;
       const uint32_t nb = static_cast<uint32_t>(len) * kRowB;
       bulk_g2s(smem_u32(kt + s * kRowB), kbase + row * kRowB, nb, fb);
       bulk_g2s(smem_u32(vt + s * kRowB), vbase + row * kRowB, nb, fb);
       if (FMT == DATTN_FMT_INT8_TOKEN) {
         const int qlo = h ? qlo1 : qlo0, qd = h ? qd1 : qd0;
-        const int cn = (((t % p.P) + len + 3) & ~3) - qlo;
+        const int cn = ((row_of(p, t) + len + 3) & ~3) - qlo;
         const long long qrow = (static_cast<long long>(pg) * p.H_kv + it.h) * p.P + qlo;
         bulk_g2s(smem_u32(kq + qd * 4), static_cast<const uint8_t*>(p.kqp) + qrow * 4, cn * 4, fb);
         bulk_g2s(smem_u32(vq + qd * 4), static_cast<const uint8_t*>(p.vqp) + qrow * 4, cn * 4, fb);
@@ -779,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_kernel(const __grid_const
   if (warp >= kConsumerWarps) {
     // the producer warpgroup hands registers to the consumers; one warp produces
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-    if (warp == kConsumerWarps) produce<D, FMT>(p, smem, it_begin, it_end, lane);
+    produce<D, FMT>(p, smem, it_begin, it_end, lane, warp - kConsumerWarps);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
