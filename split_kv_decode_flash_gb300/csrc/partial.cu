@@ -74,6 +74,10 @@ struct Cfg {
 
 constexpr int kFlagFull = 1, kFlagResidual = 2;
 
+// Consumer stage groups: with one 4-row block, two groups of four warps take
+// alternate stages (16 keys per warp and stage); otherwise all warps share a stage.
+__host__ __device__ __forceinline__ int stage_groups(int rows) { return rows <= 4 ? 2 : 1; }
+
 __device__ __forceinline__ int kivi_prefix(int T, int G, int R) { return T > R ? (T - R + G - 1) / G * G : 0; }
 
 // Stream index where KIVI residual keys begin (INT_MAX for other formats).
@@ -440,10 +444,15 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
   float* scratch = reinterpret_cast<float*>(smem + C::kScratch);
 
+  // Warps are split into stage groups that take turns on the ring's stages, row
+  // blocks of 4 query rows, and key slices of at least 16 keys per stage.
   const int nrb = p.rows <= 4 ? 1 : p.rows <= 8 ? 2 : p.rows <= 16 ? 4 : 8;  // row blocks
-  const int nts = kConsumerWarps / nrb;                                        // key slices
-  const int rb = cw % nrb, ts = cw / nrb;
-  const int keys_per_warp = kTK / nts;                                         // 8 * nrb
+  const int ng = stage_groups(p.rows);                                         // stage groups
+  const int wps = kConsumerWarps / ng;                                         // warps per stage
+  const int sgrp = cw / wps, wi = cw % wps;
+  const int rb = wi % nrb, ts = wi / nrb;
+  const int nts = wps / nrb;                                                   // key slices
+  const int keys_per_warp = kTK / nts;                                         // 16, 32 or 64
   const int tg = lane >> 3, j = lane & 7;
   const int rr = j >> 1;
   const int my_row = rb * 4 + rr;
@@ -512,6 +521,10 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
     float m_run = -INFINITY, l_run = 0.f;
     for (int j0 = it.a; j0 < it.e; ++k) {
       const int j1 = stage_end(it, j0, jq);
+      if (static_cast<int>(k % ng) != sgrp) {     // the other stage group's turn
+        j0 = j1;
+        continue;
+      }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
       if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
@@ -529,11 +542,11 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
       const bool stage_full = flags & kFlagFull;
       const bool resid = flags & kFlagResidual;
 
-      for (int sub = 0; sub < nrb; ++sub) {
-        float sv[2];
+      for (int sub = 0; sub < keys_per_warp / 16; ++sub) {
+        float sv[4];
 #pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-          const int slot = ts * keys_per_warp + sub * 8 + pp * 4 + tg;
+        for (int pp = 0; pp < 4; ++pp) {
+          const int slot = ts * keys_per_warp + sub * 16 + pp * 4 + tg;
           const int t = pos[slot];
           float2 acc[4];
 #pragma unroll
@@ -607,15 +620,16 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
           if (vis && !stage_full) vis = key_visible(mc, my_qi, t);
           sv[pp] = vis ? kk : -INFINITY;
         }
-        // online softmax update for this lane's row over 8 keys of the warp
-        float mx = fmaxf(sv[0], sv[1]);
+        // online softmax update for this lane's row over 16 keys of the warp
+        float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
         mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 16));
         const float m_new = fmaxf(m_run, mx);
         const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-        const float p0 = sv[0] == -INFINITY ? 0.f : exp2f(sv[0] - m_new);
-        const float p1 = sv[1] == -INFINITY ? 0.f : exp2f(sv[1] - m_new);
-        l_run = l_run * alpha + p0 + p1;
+        float pk[4];
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) pk[pp] = sv[pp] == -INFINITY ? 0.f : exp2f(sv[pp] - m_new);
+        l_run = l_run * alpha + ((pk[0] + pk[1]) + (pk[2] + pk[3]));
         m_run = m_new;
         if (__any_sync(kAll, alpha != 1.f)) {
 #pragma unroll
@@ -628,9 +642,9 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
           }
         }
 #pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-          const int slot = ts * keys_per_warp + sub * 8 + pp * 4 + tg;
-          const float pv = pp ? p1 : p0;
+        for (int pp = 0; pp < 4; ++pp) {
+          const int slot = ts * keys_per_warp + sub * 16 + pp * 4 + tg;
+          const float pv = pk[pp];
           float pr[4];
 #pragma unroll
           for (int r = 0; r < 4; ++r) pr[r] = __shfl_sync(kAll, pv, tg * 8 + 2 * r);
@@ -734,13 +748,13 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
       const int row = b_of * 4 + r_of;
       if (row >= p.rows) continue;
       float M = -INFINITY;
-      for (int s2 = 0; s2 < nts; ++s2) {
+      for (int s2 = 0; s2 < kConsumerWarps / nrb; ++s2) {
         const float* w = scratch + (b_of + nrb * s2) * (C::kScratchWarp / 4);
         M = fmaxf(M, w[4 * D + 2 * r_of]);
       }
       float Lsum = 0.f, U = 0.f;
       if (M != -INFINITY) {
-        for (int s2 = 0; s2 < nts; ++s2) {
+        for (int s2 = 0; s2 < kConsumerWarps / nrb; ++s2) {
           const float* w = scratch + (b_of + nrb * s2) * (C::kScratchWarp / 4);
           const float mw = w[4 * D + 2 * r_of];
           if (mw == -INFINITY) continue;
@@ -776,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStagesN; ++s) {
       mbar_init(smem_u32(smem + C::kFullBar + 8 * s), 1);
-      mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), kConsumerWarps);
+      mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), kConsumerWarps / stage_groups(p.rows));
     }
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
     fence_barrier_init();
