@@ -51,17 +51,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: gives up after ~2^22 polls (seconds), raising the abort flag
-// and the timeout status bit so that every warp of the CTA stops.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait.  The thread sleeps inside try_wait (hardware suspend, woken
+// by the phase completing) instead of spinning, so waiting warps leave the
+// issue slots to working ones.  After 2 s of wall time it raises the abort
+// flag and the timeout status bit, so that every warp of the CTA stops.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u && *abort_flag) return false;
-    if (it > (1u << 22)) {
-      *abort_flag = 1;
-      atomicOr(status, kStTimeout);
-      return false;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((it & 7u) == 7u) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > 2000000000ull) {
+        *abort_flag = 1;
+        atomicOr(status, kStTimeout);
+        return false;
+      }
     }
   }
 }

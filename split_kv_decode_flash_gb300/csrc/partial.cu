@@ -194,11 +194,34 @@ struct Desc {
   int t[2];     // logical key of slots lane, lane + 32 (-1: none)
   int pg[2];    // physical page (paged), cache row (contiguous), 0 (residual)
   int gpg[2];   // KIVI: page holding the key's K-group qparams
+  bool whole;   // page-aligned stage of consecutive keys: pg[0] is the page of lane's block
 };
+
+// A stage of consecutive keys that starts on a page boundary is described per
+// page (one lane per page) instead of per key.
+template <int FMT>
+__device__ __forceinline__ bool whole_pages(const PartialParams& p, const Cursor& c) {
+  return FMT != DATTN_FMT_INT4_KIVI && c.valid && p.layout == DATTN_KV_PAGED_HND &&
+         p.mask != DATTN_MASK_INDEX_LIST && p.P_shift >= 1 && p.P <= kTK && c.j1 <= c.it.x0 &&
+         (c.j0 & (p.P - 1)) == 0;
+}
 
 template <int FMT>
 __device__ __forceinline__ Desc describe(const PartialParams& p, const Cursor& c, int lane) {
   Desc d;
+  d.whole = whole_pages<FMT>(p, c);
+  if (d.whole) {
+    const int np = (c.j1 - c.j0 + p.P - 1) >> p.P_shift;
+    const int blk = (c.j0 >> p.P_shift) + lane;
+    int pg = -1;
+    if (lane < np) {
+      const int pi = blk < c.hi - c.lo ? p.page_indices[c.lo + blk] : -1;
+      pg = (pi >= 0 && pi < p.num_pages) ? pi : -1;
+    }
+    d.pg[0] = pg;
+    d.t[0] = d.t[1] = d.pg[1] = d.gpg[0] = d.gpg[1] = -1;
+    return d;
+  }
   const bool resid = c.j0 >= c.jq;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -296,6 +319,49 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
     int* qsel = reinterpret_cast<int*>(smem + C::kQsel) + st * kTK;
     const bool resid = cur.j0 >= cur.jq;
     const WorkItem& it = cur.it;
+
+    if (dcur.whole) {
+      // whole pages: lane l owns page l of the stage
+      const int n = cur.j1 - cur.j0;
+      const int np = (n + p.P - 1) >> p.P_shift;
+      const int pg = dcur.pg[0];
+      const int rows = lane < np ? min(p.P, n - (lane << p.P_shift)) : 0;
+      const bool bad = lane < np && pg < 0;
+      if (__any_sync(kAll, bad) && lane == 0) atomicOr(p.status, kStPageRange);
+      const unsigned badmask = __ballot_sync(kAll, bad);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int s = lane + 32 * h;
+        const bool ok = s < n && !((badmask >> (s >> p.P_shift)) & 1u);
+        pos[s] = ok ? cur.j0 + s : -1;
+        if (FMT == DATTN_FMT_INT8_TOKEN) qsel[s] = s;
+      }
+      const uint32_t good_rows = __reduce_add_sync(kAll, bad ? 0u : static_cast<uint32_t>(rows));
+      uint32_t bytes = good_rows * 2u * kRowB;
+      if (FMT == DATTN_FMT_INT8_TOKEN) bytes += 2u * 4u * p.P * __popc(__ballot_sync(kAll, lane < np && !bad));
+      int flags = kFlagFull;
+      const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+      for (int i = 0; i < p.S_q; ++i)
+        if (visible_in_run(mc, i, cur.j0, cur.j1) != n) flags = 0;
+      if (lane == 0) reinterpret_cast<int*>(smem + C::kFlags)[st] = flags;
+      __syncwarp();
+      const uint32_t fb = full0 + 8 * st;
+      if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+      __syncwarp();
+      if (lane < np && !bad) {
+        const long long row = (static_cast<long long>(pg) * p.H_kv + it.h) << p.P_shift;
+        const int s = lane << p.P_shift;
+        bulk_g2s(smem_u32(kt + s * kRowB), kbase + row * kRowB, rows * kRowB, fb);
+        bulk_g2s(smem_u32(vt + s * kRowB), vbase + row * kRowB, rows * kRowB, fb);
+        if (FMT == DATTN_FMT_INT8_TOKEN) {
+          bulk_g2s(smem_u32(kq + s * 4), static_cast<const uint8_t*>(p.kqp) + row * 4, p.P * 4, fb);
+          bulk_g2s(smem_u32(vq + s * 4), static_cast<const uint8_t*>(p.vqp) + row * 4, p.P * 4, fb);
+        }
+      }
+      cur = nxt;
+      dcur = dnxt;
+      continue;
+    }
 
     // runs of consecutive keys in one page
     const int t0 = dcur.t[0], t1 = dcur.t[1];
