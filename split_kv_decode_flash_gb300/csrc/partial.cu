@@ -348,14 +348,32 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
       const uint32_t fb = full0 + 8 * st;
       if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
       __syncwarp();
-      if (lane < np && !bad) {
-        const long long row = (static_cast<long long>(pg) * p.H_kv + it.h) << p.P_shift;
-        const int s = lane << p.P_shift;
-        bulk_g2s(smem_u32(kt + s * kRowB), kbase + row * kRowB, rows * kRowB, fb);
-        bulk_g2s(smem_u32(vt + s * kRowB), vbase + row * kRowB, rows * kRowB, fb);
-        if (FMT == DATTN_FMT_INT8_TOKEN) {
-          bulk_g2s(smem_u32(kq + s * 4), static_cast<const uint8_t*>(p.kqp) + row * 4, p.P * 4, fb);
-          bulk_g2s(smem_u32(vq + s * 4), static_cast<const uint8_t*>(p.vqp) + row * 4, p.P * 4, fb);
+      // Bulk copies issued by one thread complete one after another, so every
+      // page slab is cut into row pieces spread over the warp's 32 lanes: lane
+      // (page l, tensor z, piece q) copies rows [q rp, (q + 1) rp) of one slab.
+      const int per_page = 32 / np;                 // lanes per page (>= 1)
+      const bool both = per_page < 2;               // one lane copies both tensors of its page
+      const int pieces = both ? 1 : per_page >> 1;  // pieces per tensor slab
+      const int l = lane / per_page;
+      const int z = both ? 0 : (lane % per_page) / pieces, q = both ? 0 : (lane % per_page) % pieces;
+      const int pg_l = __shfl_sync(kAll, pg, min(l, 31));
+      const bool bad_l = l < np && ((badmask >> l) & 1u);
+      if (l < np && z < 2 && !bad_l) {
+        const int rows_l = min(p.P, n - (l << p.P_shift));
+        const int rp = (rows_l + pieces - 1) / pieces;
+        const int r0 = q * rp, r1 = min(rows_l, r0 + rp);
+        const long long prow = (static_cast<long long>(pg_l) * p.H_kv + it.h) << p.P_shift;
+        for (int zz = 0; zz < 2; ++zz) {
+          if (!both && zz != z) continue;
+          if (r1 > r0) {
+            const int s = (l << p.P_shift) + r0;
+            bulk_g2s(smem_u32((zz ? vt : kt) + s * kRowB), (zz ? vbase : kbase) + (prow + r0) * kRowB,
+                     (r1 - r0) * kRowB, fb);
+          }
+          if (FMT == DATTN_FMT_INT8_TOKEN && q == 0) {
+            const uint8_t* qb = static_cast<const uint8_t*>(zz ? p.vqp : p.kqp);
+            bulk_g2s(smem_u32((zz ? vq : kq) + (l << p.P_shift) * 4), qb + prow * 4, p.P * 4, fb);
+          }
         }
       }
       cur = nxt;

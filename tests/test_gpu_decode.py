@@ -50,7 +50,8 @@ def test_paged_ragged_full_size_sampled_rows():
 
 
 @pytest.mark.parametrize("lens,P,fixed", [([0, 1, 2, 17], 16, 0), ([0, 3, 5], 16, 8), ([33, 1, 64], 1, 0),
-                                          ([200, 129, 64], 64, 3), ([1000], 16, 64)])
+                                          ([200, 129, 64], 64, 3), ([1000], 16, 64), ([70, 3, 64], 2, 0),
+                                          ([130, 33], 4, 0), ([500, 65, 31], 32, 0)])
 def test_edge_lengths_pages_and_splits(lens, P, fixed):
     pool = sum(-(-t // P) for t in lens) + 3
     w = W.paged_bf16("edge", B=len(lens), S_q=1, H_q=8, H_kv=2, d=128, lens=lens, P=P, seed=9, device="cuda",

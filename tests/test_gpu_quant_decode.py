@@ -111,3 +111,13 @@ def test_quantized_full_size_sampled(fmt):
     reqs = sorted(rng.choice(p["B"], size=4, replace=False).tolist())
     rows = [(b, 0, h) for b in reqs for h in rng.choice(p["H_q"], size=6, replace=False).tolist()]
     _compare(O, L, w, p, _oracle_cache(w, fmt, reqs), rows)
+
+
+@pytest.mark.parametrize("P", [4, 64])
+def test_int8_decode_page_sizes(P):
+    lens = [300, 70, 5]
+    w = W.quantized_history("q8", B=3, S_q=1, H_q=16, H_kv=4, d=128, lens=lens, P=P, seed=24, device="cuda",
+                            fmt="int8", pool_pages=sum(-(-t // P) for t in lens) + 2)
+    p, cache = append_history(w, "int8", [[64, 200], [], []])
+    O, L, info = _run(w, "int8", p, cache, chunk_tokens=128, num_sms=3)
+    _compare(O, L, w, p, _oracle_cache(w, "int8"), H.all_rows(p))
