@@ -33,6 +33,12 @@ enum StatusBits : int32_t {
   kStAppend = 32,       // kv_append met an inconsistent descriptor
 };
 
+// Consumer warps are arranged in row blocks of 4 query rows; each warp keeps
+// the softmax state of its rows over its own share of an item's keys.  An
+// item therefore produces kConsumerWarps / row_blocks partial states per row.
+inline int row_blocks(int rows) { return rows <= 4 ? 1 : rows <= 8 ? 2 : rows <= 16 ? 4 : 8; }
+inline int states_per_item(int rows) { return kConsumerWarps / row_blocks(rows); }
+
 // One unit of producer work: keys [a, e) of the visible stream of group (b, h).
 // Interval programs: stream index j maps to position j < x0 ? j : x1 + (j - x0).
 // Index lists: x0 is the list offset of the group, position = index_list[x0 + j].

@@ -49,20 +49,19 @@ template <int D, int FMT>
 struct Cfg {
   static constexpr bool kI8 = FMT == DATTN_FMT_INT8_TOKEN;
   static constexpr bool kI4 = FMT == DATTN_FMT_INT4_KIVI;
-  static constexpr int kStagesN = FMT == DATTN_FMT_BF16 ? 6 : 5;
+  static constexpr int kStagesN = FMT == DATTN_FMT_BF16 ? 7 : 5;
   static constexpr int kTile = kTK * D * 2;                                  // bf16-sized tile
   static constexpr int kKQ = kI8 ? kQpEntries * 4 : kI4 ? kMaxKGroups * D * 4 : 0;
   static constexpr int kVQ = kI8 ? kQpEntries * 4 : kI4 ? kTK * (D / 16) * 4 : 0;
   static constexpr int kStage = 2 * kTile + kKQ + kVQ;
   static constexpr int kPos = kStagesN * kStage;                             // int32 [stages][kTK]
-  static constexpr int kQsel = kPos + kStagesN * kTK * 4;                    // int32 [stages][kTK]
-  static constexpr int kFlags = kQsel + kStagesN * kTK * 4;                  // int32 [stages]
+  static constexpr int kQsel = kPos + kStagesN * kTK * 4;                    // int32 [stages][kTK] (quantized)
+  static constexpr int kFlags = kQsel + (FMT == DATTN_FMT_BF16 ? 0 : kStagesN * kTK * 4);  // int32 [stages]
   static constexpr int kFullBar = align16(kFlags + kStagesN * 4);
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
   static constexpr int kAbort = kEmptyBar + kStagesN * 8;
-  static constexpr int kScratch = align16(kAbort + 16);
-  static constexpr int kScratchWarp = 4 * D * 4 + 4 * 8;                   // 4 rows of u, then (m, l)
-  static constexpr int kTotal = kScratch + kConsumerWarps * kScratchWarp;
+  static constexpr int kTotal = align16(kAbort + 16);
+  static_assert(kTotal <= 232448, "shared memory of one CTA");
   // channel map: bf16 splits a lane's 16 channels in two 8-channel chunks
   // (conflict-free 16-byte reads of 256-byte rows); the byte formats keep
   // them contiguous.
@@ -526,7 +525,6 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
   const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
-  float* scratch = reinterpret_cast<float*>(smem + C::kScratch);
 
   // Warps are split into stage groups that take turns on the ring's stages, row
   // blocks of 4 query rows, and key slices of at least 16 keys per stage.
@@ -543,6 +541,8 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
   const int my_qi = my_row / p.g;
   const bool my_row_ok = my_row < p.rows;
   const int vgroup = C::kI4 ? (D / 8) * j / p.kivi_Gv : 0;     // lane's V channel group (KIVI)
+  const int spi = kConsumerWarps / nrb;                         // states per item and row
+  const int my_state = (cw - rb) / nrb;                         // this warp's state among them
 
   uint32_t k = 0;
   bool dead = false;   // a bounded wait gave up: skip work but keep every named barrier
@@ -793,7 +793,7 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
       j0 = j1;
     }
 
-    // ---- end of item: reduce over the 4 key groups, then across warps ----
+    // ---- end of item: reduce over the 4 key groups and leave this warp's state ----
     l_run += __shfl_xor_sync(kAll, l_run, 8);
     l_run += __shfl_xor_sync(kAll, l_run, 16);
 #pragma unroll
@@ -808,59 +808,37 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
         o[r][x].y += __shfl_xor_sync(kAll, o[r][x].y, 16);
       }
     }
-    float* mine = scratch + cw * (C::kScratchWarp / 4);
-    if (tg == 0) {
+    // every key group now holds the totals; key group tg writes row tg of the block
+    const float m_mine = __shfl_sync(kAll, m_run, 2 * tg);      // row tg's (m, l) live in lane 2 tg
+    const float l_mine = __shfl_sync(kAll, l_run, 2 * tg);
+    const int row = rb * 4 + tg;
+    float2 ov[NV];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int x = 0; x < NV; ++x) {
-          const int dim = C::chan(j, x);
-          mine[r * D + dim] = o[r][x].x + zacc[r];
-          mine[r * D + dim + 1] = o[r][x].y + zacc[r];
-        }
-      if ((j & 1) == 0) {
-        mine[4 * D + 2 * rr] = m_run;
-        mine[4 * D + 2 * rr + 1] = l_run;
-      }
+    for (int x = 0; x < NV; ++x) {
+      const float2 v = tg == 0 ? o[0][x] : tg == 1 ? o[1][x] : tg == 2 ? o[2][x] : o[3][x];
+      const float z = tg == 0 ? zacc[0] : tg == 1 ? zacc[1] : tg == 2 ? zacc[2] : zacc[3];
+      ov[x] = make_float2(v.x + z, v.y + z);
     }
-    named_barrier(1, kConsumerWarps * 32);
-    const int tid = cw * 32 + lane;
-    const int n_out = nrb * 4 * D;
-    for (int e = tid; e < n_out; e += kConsumerWarps * 32) {
-      const int row_in = e / D, dim = e % D;
-      const int b_of = row_in >> 2, r_of = row_in & 3;
-      const int row = b_of * 4 + r_of;
-      if (row >= p.rows) continue;
-      float M = -INFINITY;
-      for (int s2 = 0; s2 < kConsumerWarps / nrb; ++s2) {
-        const float* w = scratch + (b_of + nrb * s2) * (C::kScratchWarp / 4);
-        M = fmaxf(M, w[4 * D + 2 * r_of]);
-      }
-      float Lsum = 0.f, U = 0.f;
-      if (M != -INFINITY) {
-        for (int s2 = 0; s2 < kConsumerWarps / nrb; ++s2) {
-          const float* w = scratch + (b_of + nrb * s2) * (C::kScratchWarp / 4);
-          const float mw = w[4 * D + 2 * r_of];
-          if (mw == -INFINITY) continue;
-          const float a = exp2f(mw - M);
-          Lsum += a * w[4 * D + 2 * r_of + 1];
-          U += a * w[r_of * D + dim];
-        }
-      }
+    if (row < p.rows && !dead) {
       const int i = row / p.g, hq = it.h * p.g + row % p.g;
       const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
-      if (it.slot < 0) {
-        const float val = Lsum > 0.f ? U / Lsum : 0.f;
-        static_cast<__nv_bfloat16*>(p.o)[orow * D + dim] = __float2bfloat16_rn(val);
-        if (dim == 0 && p.lse)
-          p.lse[orow] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+      if (it.slot < 0) {        // single state for the row: final output
+        const float inv = l_mine > 0.f ? 1.f / l_mine : 0.f;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
+#pragma unroll
+        for (int x = 0; x < NV; ++x)
+          *reinterpret_cast<__nv_bfloat162*>(out + C::chan(j, x)) = __floats2bfloat162_rn(ov[x].x * inv, ov[x].y * inv);
+        if (j == 0 && p.lse)
+          p.lse[orow] = l_mine > 0.f ? (m_mine + __log2f(l_mine)) * 0.69314718055994531f : -INFINITY;
       } else {
-        const long long srow = static_cast<long long>(it.slot) * p.rows + row;
-        p.u[srow * D + dim] = U;
-        if (dim == 0) p.ml[srow] = make_float2(Lsum > 0.f ? M : -INFINITY, Lsum);
+        const long long srow = static_cast<long long>(it.slot + my_state) * p.rows + row;
+        float* u = p.u + srow * D;
+#pragma unroll
+        for (int x = 0; x < NV; x += 2)
+          *reinterpret_cast<float4*>(u + C::chan(j, x)) = make_float4(ov[x].x, ov[x].y, ov[x + 1].x, ov[x + 1].y);
+        if (j == 0) p.ml[srow] = make_float2(l_mine > 0.f ? m_mine : -INFINITY, l_mine);
       }
     }
-    named_barrier(1, kConsumerWarps * 32);
   }
 }
 

@@ -242,16 +242,19 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   }
   group_first[n_groups] = static_cast<int>(items.size());
 
-  // 3. partial slots and merge groups (o_indptr)
+  // 3. partial-state slots and merge groups (o_indptr): every consumer warp of
+  //    an item leaves its own state, so an item owns states_per_item slots; a
+  //    group that is one item with one state per row writes O directly.
   std::vector<MergeGroup> merges;
+  const int spi = states_per_item(rows);
   int n_slots = 0, max_splits = 0;
   for (int k = 0; k < n_groups; ++k) {
     const int n = group_first[k + 1] - group_first[k];
     max_splits = std::max(max_splits, n);
-    if (n > 1) {
-      merges.push_back(MergeGroup{k / H, k % H, n_slots, n});
-      for (int i = 0; i < n; ++i) items[group_first[k] + i].slot = n_slots + i;
-      n_slots += n;
+    if (n * spi > 1) {
+      merges.push_back(MergeGroup{k / H, k % H, n_slots, n * spi});
+      for (int i = 0; i < n; ++i) items[group_first[k] + i].slot = n_slots + i * spi;
+      n_slots += n * spi;
     }
   }
 
