@@ -31,6 +31,7 @@ enum StatusBits : int32_t {
   kStRowRange = 8,      // contiguous cache row / token outside its capacity
   kStTimeout = 16,      // a bounded barrier wait gave up
   kStAppend = 32,       // kv_append met an inconsistent descriptor
+  kStPipeline = 64,     // a consumer found a ring stage stamped with another stage number
 };
 
 // Consumer warps are arranged in row blocks of 4 query rows; each warp keeps

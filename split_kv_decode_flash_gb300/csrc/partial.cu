@@ -49,7 +49,11 @@ template <int D, int FMT>
 struct Cfg {
   static constexpr bool kI8 = FMT == DATTN_FMT_INT8_TOKEN;
   static constexpr bool kI4 = FMT == DATTN_FMT_INT4_KIVI;
-  static constexpr int kStagesN = FMT == DATTN_FMT_BF16 ? 7 : 5;
+  // Even depth: with two consumer stage groups taking alternate stages, every
+  // ring slot then always belongs to the same group, so no group can wait for
+  // a slot two phases ahead (mbarrier parity would alias).
+  static constexpr int kStagesN = 6;
+  static_assert(kStagesN % 2 == 0, "ring depth must be even");
   static constexpr int kTile = kTK * D * 2;                                  // bf16-sized tile
   static constexpr int kKQ = kI8 ? kQpEntries * 4 : kI4 ? kMaxKGroups * D * 4 : 0;
   static constexpr int kVQ = kI8 ? kQpEntries * 4 : kI4 ? kTK * (D / 16) * 4 : 0;
@@ -57,7 +61,8 @@ struct Cfg {
   static constexpr int kPos = kStagesN * kStage;                             // int32 [stages][kTK]
   static constexpr int kQsel = kPos + kStagesN * kTK * 4;                    // int32 [stages][kTK] (quantized)
   static constexpr int kFlags = kQsel + (FMT == DATTN_FMT_BF16 ? 0 : kStagesN * kTK * 4);  // int32 [stages]
-  static constexpr int kFullBar = align16(kFlags + kStagesN * 4);
+  static constexpr int kSeq = kFlags + kStagesN * 4;                          // int32 [stages]: stage number
+  static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
   static constexpr int kAbort = kEmptyBar + kStagesN * 8;
   static constexpr int kTotal = align16(kAbort + 16);
@@ -342,7 +347,10 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
       const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
       for (int i = 0; i < p.S_q; ++i)
         if (visible_in_run(mc, i, cur.j0, cur.j1) != n) flags = 0;
-      if (lane == 0) reinterpret_cast<int*>(smem + C::kFlags)[st] = flags;
+      if (lane == 0) {
+        reinterpret_cast<int*>(smem + C::kFlags)[st] = flags;
+        reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
+      }
       __syncwarp();
       const uint32_t fb = full0 + 8 * st;
       if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
@@ -461,7 +469,10 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
       }
     }
     if (full) flags |= kFlagFull;
-    if (lane == 0) reinterpret_cast<int*>(smem + C::kFlags)[st] = flags;
+    if (lane == 0) {
+      reinterpret_cast<int*>(smem + C::kFlags)[st] = flags;
+      reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
+    }
     __syncwarp();
     const uint32_t fb = full0 + 8 * st;
     if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
@@ -612,6 +623,12 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
       if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+        dead = true;
+        break;
+      }
+      if (reinterpret_cast<const volatile int*>(smem + C::kSeq)[st] != static_cast<int>(k)) {
+        if (lane == 0) atomicOr(p.status, kStPipeline);   // wrong phase: stop, never consume stale data
+        *abort_flag = 1;
         dead = true;
         break;
       }
