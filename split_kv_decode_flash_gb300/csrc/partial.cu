@@ -552,7 +552,6 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
   const int my_qi = my_row / p.g;
   const bool my_row_ok = my_row < p.rows;
   const int vgroup = C::kI4 ? (D / 8) * j / p.kivi_Gv : 0;     // lane's V channel group (KIVI)
-  const int spi = kConsumerWarps / nrb;                         // states per item and row
   const int my_state = (cw - rb) / nrb;                         // this warp's state among them
 
   uint32_t k = 0;
