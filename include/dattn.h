@@ -223,6 +223,46 @@ dattn_status dattn_run_ex(const dattn_plan_t* plan, const dattn_problem* prob,
                           const dattn_tensors* t, void* workspace, size_t workspace_bytes,
                           void* stream, const dattn_run_options* options);
 
+/* Size of the library-owned scratch array that dattn_run_noalloc uses on each device. */
+#define DATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)  /* 16 MiB */
+
+/* dattn_run without a caller workspace; the pages have no counterpart of this
+ * call.  It serves callers that cannot allocate device memory or hand over a
+ * buffer at step time.  Examples: an engine that reserved all of HBM for its
+ * K/V page pool at start-up, and a latency-bound decode loop that cannot take
+ * the device synchronisation of cudaMalloc / cudaFree.
+ *
+ * Scratch array:
+ *  - The workspace is a file-scope device array of DATTN_NOALLOC_SCRATCH_BYTES
+ *    (256-byte aligned).
+ *  - Every GPU on which the library's device code is loaded holds that array
+ *    until the process exits.
+ *  - The call itself allocates nothing: no cudaMalloc, no cudaFree, no
+ *    allocating library routine.
+ *
+ * First call on a device:
+ *  - It looks up the array's address with cudaGetSymbolAddress on the current
+ *    device and keeps it for later calls.
+ *  - Make that call before any stream capture on that device.
+ *
+ * Sharing and races:
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents.
+ *  - The only part that must start at zero is the device status word. It is
+ *    cleared by the work-list copy that each call enqueues.
+ *  - Calls whose work overlaps on the GPU (different streams, or other host
+ *    threads) race on the array. Serialise them on one stream.
+ *
+ * Errors:
+ *  - A plan whose info.workspace_bytes exceeds DATTN_NOALLOC_SCRATCH_BYTES
+ *    gets DATTN_EWORKSPACE and a message; use dattn_run for it.
+ *  - Any other argument error is reported as dattn_run reports it.
+ *
+ * dattn_device_status cannot read this call's status word, because the caller
+ * holds no pointer to the array. */
+dattn_status dattn_run_noalloc(const dattn_plan_t* plan, const dattn_problem* prob,
+                               const dattn_tensors* t, void* stream);
+
 /* Reads the device status word of the last run that used "workspace"
  * (synchronises "stream").  *flags = 0 when no device check fired. */
 dattn_status dattn_device_status(const void* workspace, int32_t* flags, void* stream);

@@ -77,6 +77,7 @@ class RunOptions(ctypes.Structure):
 
 
 RUN_REUSE_UPLOAD = 1
+NOALLOC_SCRATCH_BYTES = 16 << 20  # DATTN_NOALLOC_SCRATCH_BYTES
 
 
 class AppendInputs(ctypes.Structure):
@@ -107,6 +108,7 @@ def load():
         "dattn_run_ex": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP,
                                ctypes.c_size_t, _VP, ctypes.POINTER(RunOptions)]),
         "dattn_plan_upload": (_ST, [_VP, _VP, ctypes.c_size_t, _VP]),
+        "dattn_run_noalloc": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP]),
         "dattn_device_status": (_ST, [_VP, ctypes.POINTER(ctypes.c_int32), _VP]),
         "kv_append_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Problem)]),
         "kv_append": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(AppendInputs), ctypes.POINTER(Tensors),
@@ -265,6 +267,15 @@ def dattn_run(plan: Plan, problem, tensors: Tensors, workspace, stream=None) -> 
     prob = problem if isinstance(problem, Problem) else make_problem(problem)
     _check(load().dattn_run(plan.handle, ctypes.byref(prob), ctypes.byref(tensors), workspace.data_ptr(),
                             workspace.numel() * workspace.element_size(), _stream_ptr(stream)), "dattn_run")
+
+
+def dattn_run_noalloc(plan: Plan, problem, tensors: Tensors, stream=None) -> None:
+    """dattn_run on the library's own static scratch array instead of a caller workspace
+    (see dattn_run_noalloc in dattn.h); raises DattnError when the plan's workspace
+    exceeds NOALLOC_SCRATCH_BYTES."""
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    _check(load().dattn_run_noalloc(plan.handle, ctypes.byref(prob), ctypes.byref(tensors), _stream_ptr(stream)),
+           "dattn_run_noalloc")
 
 
 def dattn_plan_upload(plan: Plan, workspace, stream=None) -> None:
