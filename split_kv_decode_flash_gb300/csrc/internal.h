@@ -12,7 +12,6 @@ namespace dattn {
 
 // ---- kernel geometry ---------------------------------------------------------------
 constexpr int kTK = 64;              // keys per pipeline stage
-constexpr int kStages = 4;           // shared-memory ring depth
 constexpr int kConsumerWarps = 8;    // two warpgroups that compute
 constexpr int kProducerWarps = 4;    // one warpgroup that fills the ring, a stage per warp in turn
 constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
@@ -34,11 +33,16 @@ enum StatusBits : int32_t {
   kStPipeline = 64,     // a consumer found a ring stage stamped with another stage number
 };
 
-// Consumer warps are arranged in row blocks of 4 query rows; each warp keeps
-// the softmax state of its rows over its own share of an item's keys.  An
-// item therefore produces kConsumerWarps / row_blocks partial states per row.
-inline int row_blocks(int rows) { return rows <= 4 ? 1 : rows <= 8 ? 2 : rows <= 16 ? 4 : 8; }
-inline int states_per_item(int rows) { return kConsumerWarps / row_blocks(rows); }
+// Consumer warps are arranged in row blocks; each warp keeps the softmax
+// state of its block's rows over its own share of an item's keys, so an item
+// produces kConsumerWarps / row_blocks partial states per row.  The bf16
+// tensor-core kernel uses blocks of 16 rows (one mma tile), the byte formats
+// blocks of 4 rows.
+inline int row_blocks(int rows, int fmt) {
+  if (fmt == DATTN_FMT_BF16) return rows <= 16 ? 1 : 2;
+  return rows <= 4 ? 1 : rows <= 8 ? 2 : rows <= 16 ? 4 : 8;
+}
+inline int states_per_item(int rows, int fmt) { return kConsumerWarps / row_blocks(rows, fmt); }
 
 // One unit of producer work: keys [a, e) of the visible stream of group (b, h).
 // Interval programs: stream index j maps to position j < x0 ? j : x1 + (j - x0).
@@ -102,7 +106,7 @@ struct MergeParams {
 
 // Kernel launchers (partial.cu, merge.cu); return cudaError_t as int.
 int launch_partial(const PartialParams& p, int d, int n_ctas, void* stream);
+int launch_partial_bf16(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_merge(const MergeParams& p, int d, void* stream);
-size_t partial_smem_bytes(int d, int fmt);
 
 }  // namespace dattn

@@ -1,10 +1,10 @@
-// Partial kernel of split-KV decode attention: bf16, INT8 per-token and
-// KIVI INT4 K/V.
+// Partial kernel of split-KV decode attention for the byte formats: INT8
+// per-token and KIVI INT4 K/V (bf16 K/V has a tensor-core kernel of its own).
 //
 // One persistent CTA per SM walks its list of work items (request b, kv head
 // h, keys [a, e) of the group's visible stream).
 //
-// Producer warp.  Every 64-key stage is described per key slot (logical key
+// Producer warps.  Every 64-key stage is described per key slot (logical key
 // t, physical page pi) one stage ahead, so the dependent loads of the page
 // walk (list entry -> page id, M4.5 §0x04D) overlap the wait for a free ring
 // slot.  Slots whose keys are consecutive inside one page are merged into one
@@ -12,7 +12,7 @@
 // one bulk (TMA-engine) copy per tensor into a shared-memory ring guarded by
 // mbarriers.  Keys outside the visible stream (SKIP tiles) are never loaded;
 // each stage is classified FULL or PARTIAL (§0x05C) so FULL stages skip the
-// per-element predicate.  Quantized formats also stage their qparams: INT8
+// per-element predicate.  The qparams are staged with the codes: INT8
 // per-token (s, z) as 16-byte aligned chunks packed by a warp scan; KIVI the
 // per-channel K group qparams and per-token V qparams (M8.6 §0x06A); KIVI
 // residual keys come from the bf16 ring in stages of their own.
@@ -25,15 +25,12 @@
 // puts them: a per-token K scale multiplies the finished dot product, a
 // per-channel K scale is applied while dequantising, a per-token V scale is
 // folded into the probability and its offset into a per-row sum.  The online
-// softmax (§0x02B) runs every 8 keys in log2 units; masked scores are -inf
-// before the maximum and the sums.  At the end of an item the warps of a row
-// block merge their states through shared memory and write either O / LSE
-// (single-chunk groups) or an fp32 partial state.
+// softmax (§0x02B) runs every 16 keys in log2 units; masked scores are -inf
+// before the maximum and the sums.  At the end of an item every warp leaves
+// its own fp32 partial state (or O / LSE when it is the group's only state).
 #include <cuda_runtime.h>
 
-#include <climits>
-
-#include "device.cuh"
+#include "stream.cuh"
 
 namespace dattn {
 
@@ -42,8 +39,6 @@ namespace {
 constexpr unsigned kAll = 0xffffffffu;
 constexpr int kMaxKGroups = 6;      // KIVI K groups per stage (G >= 32, at most two runs)
 constexpr int kQpEntries = 512;     // INT8 qparam entries per stage and tensor
-
-constexpr int align16(int x) { return (x + 15) / 16 * 16; }
 
 template <int D, int FMT>
 struct Cfg {
@@ -60,62 +55,21 @@ struct Cfg {
   static constexpr int kStage = 2 * kTile + kKQ + kVQ;
   static constexpr int kPos = kStagesN * kStage;                             // int32 [stages][kTK]
   static constexpr int kQsel = kPos + kStagesN * kTK * 4;                    // int32 [stages][kTK] (quantized)
-  static constexpr int kFlags = kQsel + (FMT == DATTN_FMT_BF16 ? 0 : kStagesN * kTK * 4);  // int32 [stages]
+  static constexpr int kFlags = kQsel + kStagesN * kTK * 4;                  // int32 [stages]
   static constexpr int kSeq = kFlags + kStagesN * 4;                          // int32 [stages]: stage number
   static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
   static constexpr int kAbort = kEmptyBar + kStagesN * 8;
   static constexpr int kTotal = align16(kAbort + 16);
   static_assert(kTotal <= 232448, "shared memory of one CTA");
-  // channel map: bf16 splits a lane's 16 channels in two 8-channel chunks
-  // (conflict-free 16-byte reads of 256-byte rows); the byte formats keep
-  // them contiguous.
-  static constexpr bool kSplit = FMT == DATTN_FMT_BF16 && D == 128;
-  static __device__ __forceinline__ int chan(int j, int v) {   // first channel of float2 slot v
-    return kSplit ? (v >> 2) * 64 + 8 * j + 2 * (v & 3) : (D / 8) * j + 2 * v;
-  }
+  // a lane's channels of a row are contiguous
+  static __device__ __forceinline__ int chan(int j, int v) { return (D / 8) * j + 2 * v; }
+  static_assert(FMT != DATTN_FMT_BF16, "bf16 K/V use the tensor-core kernel");
 };
-
-constexpr int kFlagFull = 1, kFlagResidual = 2;
 
 // Consumer stage groups: with one 4-row block, two groups of four warps take
 // alternate stages (16 keys per warp and stage); otherwise all warps share a stage.
 __host__ __device__ __forceinline__ int stage_groups(int rows) { return rows <= 4 ? 2 : 1; }
-
-__device__ __forceinline__ int kivi_prefix(int T, int G, int R) { return T > R ? (T - R + G - 1) / G * G : 0; }
-
-// Stream index where KIVI residual keys begin (INT_MAX for other formats).
-__device__ __forceinline__ int residual_start(const PartialParams& p, const WorkItem& it) {
-  if (p.fmt != DATTN_FMT_INT4_KIVI) return INT_MAX;
-  const int nq = kivi_prefix(it.T, p.kivi_G, p.kivi_R);
-  return nq <= it.x0 ? nq : it.x0 + max(0, nq - it.x1);
-}
-
-__device__ __forceinline__ int stage_end(const WorkItem& it, int j0, int jq) {
-  int j1 = min(j0 + kTK, it.e);
-  if (j0 < jq) j1 = min(j1, jq);
-  return j1;
-}
-
-struct Run {
-  int p0, p1;
-};
-
-// Position runs of stream [j0, j1) of an interval item (at most two).
-__device__ __forceinline__ int item_runs(const WorkItem& it, int j0, int j1, Run& r0, Run& r1) {
-  int n = 0;
-  Run a{0, 0}, b{0, 0};
-  if (j0 < it.x0) a = Run{j0, min(j1, it.x0)}, n = 1;
-  if (j1 > it.x0) {
-    const int s = max(j0, it.x0);
-    const Run x{it.x1 + (s - it.x0), it.x1 + (j1 - it.x0)};
-    if (n == 0) a = x; else b = x;
-    ++n;
-  }
-  r0 = a;
-  r1 = b;
-  return n;
-}
 
 __device__ __forceinline__ float2 u8_pair(uint32_t w, int pair) {
   const uint32_t a = __byte_perm(w, 0x4B000000u, 0x7540u | (2 * pair));
@@ -133,66 +87,7 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
-// Logical block and page row of key t (shifts when P is a power of two).
-__device__ __forceinline__ int blk_of(const PartialParams& p, int t) { return p.P_shift >= 0 ? t >> p.P_shift : t / p.P; }
-__device__ __forceinline__ int row_of(const PartialParams& p, int t) {
-  return p.P_shift >= 0 ? t & (p.P - 1) : t % p.P;
-}
-
 // ---- producer ---------------------------------------------------------------------
-
-struct Cursor {
-  int ii;           // position in the CTA's item list
-  WorkItem it;
-  int jq, lo, hi, crow;
-  int j0, j1;
-  bool valid;
-};
-
-__device__ __forceinline__ void load_item(const PartialParams& p, Cursor& c, int lane) {
-  c.it = p.items[p.cta_items[c.ii]];
-  c.jq = residual_start(p, c.it);
-  c.lo = c.hi = c.crow = 0;
-  if (p.layout == DATTN_KV_PAGED_HND) {
-    c.lo = p.page_indptr[c.it.b];
-    c.hi = p.page_indptr[c.it.b + 1];
-  } else {
-    c.crow = cache_row(p.cache_batch_idx, c.it.b, p.B_cache, lane == 0 ? p.status : nullptr);
-  }
-  if (p.mask == DATTN_MASK_INDEX_LIST) {
-    const int g = c.it.b * p.H_kv + c.it.h;
-    const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
-    if (lo != c.it.x0 || c.it.e > n) {
-      if (lane == 0) atomicOr(p.status, kStListRange);
-      c.it.e = c.it.a;          // drop the item's keys
-    }
-  }
-}
-
-// First stage at or after item position ii whose item has keys.
-__device__ __forceinline__ void seek(const PartialParams& p, Cursor& c, int it_end, int lane) {
-  c.valid = false;
-  for (; c.ii < it_end; ++c.ii) {
-    load_item(p, c, lane);
-    if (c.it.e > c.it.a) {
-      c.j0 = c.it.a;
-      c.j1 = stage_end(c.it, c.j0, c.jq);
-      c.valid = true;
-      return;
-    }
-  }
-}
-
-__device__ __forceinline__ void advance(const PartialParams& p, Cursor& c, int it_end, int lane) {
-  if (!c.valid) return;
-  if (c.j1 < c.it.e) {
-    c.j0 = c.j1;
-    c.j1 = stage_end(c.it, c.j0, c.jq);
-    return;
-  }
-  ++c.ii;
-  seek(p, c, it_end, lane);
-}
 
 struct Desc {
   int t[2];     // logical key of slots lane, lane + 32 (-1: none)
@@ -297,8 +192,7 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
   const uint8_t* kbase = static_cast<const uint8_t*>(p.k);
   const uint8_t* vbase = static_cast<const uint8_t*>(p.v);
   const bool paged = p.layout == DATTN_KV_PAGED_HND;
-  const bool listed = p.mask == DATTN_MASK_INDEX_LIST;
-  constexpr int kRowB = FMT == DATTN_FMT_BF16 ? D * 2 : FMT == DATTN_FMT_INT8_TOKEN ? D : D / 2;  // code row bytes
+  constexpr int kRowB = FMT == DATTN_FMT_INT8_TOKEN ? D : D / 2;  // code row bytes
 
   // producer warp pw fills stages pw, pw + kProducerWarps, ... of the CTA's stage sequence
   Cursor cur;
@@ -407,7 +301,7 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
 
     uint32_t bytes = 0;
     int qd0 = 0, qd1 = 0, qlo0 = 0, qlo1 = 0;
-    if (resid || FMT == DATTN_FMT_BF16) {
+    if (resid) {
       bytes = static_cast<uint32_t>(nvalid) * 2u * D * 2u;
     } else if (FMT == DATTN_FMT_INT8_TOKEN) {
       // qparam chunks [floor4(r0), ceil4(r0 + len)) packed by an exclusive scan in slot order
@@ -453,21 +347,7 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
 
     // stage class
     int flags = resid ? kFlagResidual : 0;
-    bool full = true;
-    const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
-    if (listed) {
-      int mx = max(t0, t1);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kAll, mx, o));
-      full = mx < frontier(mc, 0);
-    } else {
-      Run r0, r1;
-      const int nr = item_runs(it, cur.j0, cur.j1, r0, r1);
-      for (int i = 0; i < p.S_q && full; ++i) {
-        if (nr > 0 && visible_in_run(mc, i, r0.p0, r0.p1) != r0.p1 - r0.p0) full = false;
-        if (nr > 1 && visible_in_run(mc, i, r1.p0, r1.p1) != r1.p1 - r1.p0) full = false;
-      }
-    }
+    const bool full = stage_is_full(p, cur, t0, t1);
     if (full) flags |= kFlagFull;
     if (lane == 0) {
       reinterpret_cast<int*>(smem + C::kFlags)[st] = flags;
@@ -557,12 +437,7 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
   uint32_t k = 0;
   bool dead = false;   // a bounded wait gave up: skip work but keep every named barrier
   for (int ii = it_begin; ii < it_end; ++ii) {
-    WorkItem it = p.items[p.cta_items[ii]];
-    if (p.mask == DATTN_MASK_INDEX_LIST) {       // mirror the producer's list check
-      const int g = it.b * p.H_kv + it.h;
-      const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
-      if (lo != it.x0 || it.e > n) it.e = it.a;
-    }
+    const WorkItem it = read_item(p, p.cta_items[ii], false);
     const int jq = residual_start(p, it);
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
 
@@ -651,7 +526,7 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
           float2 acc[4];
 #pragma unroll
           for (int r = 0; r < 4; ++r) acc[r] = make_float2(0.f, 0.f);
-          if (FMT == DATTN_FMT_BF16 || resid) {
+          if (resid) {
             const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(kt) + slot * D;
 #pragma unroll
             for (int x = 0; x < NV; x += 4) {
@@ -748,7 +623,7 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
           float pr[4];
 #pragma unroll
           for (int r = 0; r < 4; ++r) pr[r] = __shfl_sync(kAll, pv, tg * 8 + 2 * r);
-          if (FMT == DATTN_FMT_BF16 || resid) {
+          if (resid) {
             // a KIVI residual stage may hold stale code bytes (not bf16) in its unused slots
             if (C::kI4 && pos[slot] < 0) continue;
             const __nv_bfloat16* vrow = reinterpret_cast<const __nv_bfloat16*>(vt) + slot * D;
@@ -906,24 +781,12 @@ int launch_one(const PartialParams& p, int n_ctas, void* stream) {
 
 }  // namespace
 
-size_t partial_smem_bytes(int d, int fmt) {
-  if (d == 64) {
-    return fmt == DATTN_FMT_BF16 ? Cfg<64, DATTN_FMT_BF16>::kTotal
-           : fmt == DATTN_FMT_INT8_TOKEN ? Cfg<64, DATTN_FMT_INT8_TOKEN>::kTotal
-                                         : Cfg<64, DATTN_FMT_INT4_KIVI>::kTotal;
-  }
-  return fmt == DATTN_FMT_BF16 ? Cfg<128, DATTN_FMT_BF16>::kTotal
-         : fmt == DATTN_FMT_INT8_TOKEN ? Cfg<128, DATTN_FMT_INT8_TOKEN>::kTotal
-                                       : Cfg<128, DATTN_FMT_INT4_KIVI>::kTotal;
-}
-
 int launch_partial(const PartialParams& p, int d, int n_ctas, void* stream) {
+  if (p.fmt == DATTN_FMT_BF16) return launch_partial_bf16(p, d, n_ctas, stream);
   if (d == 64) {
-    if (p.fmt == DATTN_FMT_BF16) return launch_one<64, DATTN_FMT_BF16>(p, n_ctas, stream);
     if (p.fmt == DATTN_FMT_INT8_TOKEN) return launch_one<64, DATTN_FMT_INT8_TOKEN>(p, n_ctas, stream);
     return launch_one<64, DATTN_FMT_INT4_KIVI>(p, n_ctas, stream);
   }
-  if (p.fmt == DATTN_FMT_BF16) return launch_one<128, DATTN_FMT_BF16>(p, n_ctas, stream);
   if (p.fmt == DATTN_FMT_INT8_TOKEN) return launch_one<128, DATTN_FMT_INT8_TOKEN>(p, n_ctas, stream);
   return launch_one<128, DATTN_FMT_INT4_KIVI>(p, n_ctas, stream);
 }

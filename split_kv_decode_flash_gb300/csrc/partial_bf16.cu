@@ -1,0 +1,442 @@
+// Partial kernel of split-KV decode attention for bf16 K/V, on the tensor
+// cores.
+//
+// One persistent CTA per SM walks its list of work items (request b, kv head
+// h, keys [a, e) of the group's visible stream), as in the byte-format
+// kernel; only the data movement and the arithmetic differ.
+//
+// Producer warps (4).  Warp w fills stages w, w + 4, ... of the CTA's stage
+// sequence.  A stage holds 64 key slots; each slot is described one stage
+// ahead by the logical key and its K/V row in the cache (the page walk of
+// M4.5 §0x04D, or the contiguous row with cache_batch_idx, §0x04A).  Every
+// key row is then copied with 16-byte cp.async operations (one warp
+// instruction moves two 256-byte rows) into a shared-memory ring whose
+// 16-byte chunks are XOR-swizzled by the slot's low three bits, so the
+// ldmatrix reads of the consumers never meet a bank conflict.  Empty slots
+// (stage tail, a key outside the cache) are zero-filled by the same copy
+// with a zero source size, so masked keys hold finite values.  Completion is
+// tracked by cp.async.mbarrier.arrive on the stage's full barrier; the ring
+// is guarded by full / empty mbarriers with bounded waits.
+//
+// Consumer warps (8).  The query rows of the group (g * S_q <= 32, the GQA
+// rows that share each K/V row, M4.5 §0x03A) form the M side of
+// mma.sync.m16n8k16 bf16 tiles (one tile of 16 rows, two for 32 rows).  A
+// warp takes 16 keys of a stage:
+//   S (16 rows x 16 keys) = Q K^T: K fragments by ldmatrix, fp32 accumulate;
+//   masked cells -> -inf, online softmax in log2 units (§0x02B) on the
+//   accumulator fragments, row maxima over the lane quad;
+//   O (16 rows x d) += P V: the S accumulators re-packed as the bf16 A
+//   operand, V fragments by ldmatrix.trans.
+// With one row tile, two groups of four warps take alternate stages.  At the
+// end of an item every warp leaves its own fp32 state (m, l, u) per row, or
+// O / LSE when it is the group's only state.
+#include <cuda_runtime.h>
+
+#include "stream.cuh"
+
+namespace dattn {
+
+namespace {
+
+constexpr unsigned kAll = 0xffffffffu;
+
+template <int D>
+struct Bf {
+  // Even depth: with two consumer stage groups taking alternate stages, every
+  // ring slot then always belongs to the same group (no mbarrier parity alias).
+  static constexpr int kStagesN = 6;
+  static_assert(kStagesN % 2 == 0, "ring depth must be even");
+  static constexpr int kRowB = D * 2;              // bytes of one key row
+  static constexpr int kChunks = kRowB / 16;       // 16-byte chunks per row
+  static constexpr int kTile = kTK * kRowB;        // one tensor's stage tile
+  static constexpr int kStage = 2 * kTile;
+  static constexpr int kPos = kStagesN * kStage;   // int32 [stages][kTK]: logical key or -1
+  static constexpr int kFlags = kPos + kStagesN * kTK * 4;
+  static constexpr int kSeq = kFlags + kStagesN * 4;   // int32 [stages]: stage number
+  static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
+  static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
+  static constexpr int kAbort = kEmptyBar + kStagesN * 8;
+  static constexpr int kTotal = align16(kAbort + 16);
+  static_assert(kTotal <= 232448, "shared memory of one CTA");
+};
+
+// Byte offset of 16-byte chunk c of key slot s inside a stage tile.
+template <int D>
+__device__ __forceinline__ uint32_t tile_off(int s, int c) {
+  return static_cast<uint32_t>(s * (D * 2) + ((c ^ (s & 7)) << 4));
+}
+
+// ---- PTX wrappers -----------------------------------------------------------------------
+
+// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on "bar" once every earlier cp.async of this thread has landed (the
+// pending count is raised first, so the barrier's expected count is unchanged).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+// c += a (16x16, row-major bf16) * b (16x8, column-major bf16), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// ---- producer ---------------------------------------------------------------------------
+
+struct SlotRows {
+  int t[2];          // logical key of slots lane and lane + 32 (-1: none)
+  long long row[2];  // K/V row of that key in the cache, in rows of d elements (-1: none)
+};
+
+__device__ __forceinline__ SlotRows describe_rows(const PartialParams& p, const Cursor& c, int lane) {
+  SlotRows d;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = c.j0 + lane + 32 * h;
+    int t = -1;
+    long long row = -1;
+    if (c.valid && j < c.j1) {
+      t = stream_key(c.it, p.mask, p.index_list, j);
+      if (p.mask == DATTN_MASK_INDEX_LIST && (t < 0 || t >= c.it.T)) {
+        atomicOr(p.status, kStListRange);
+        t = -1;
+      }
+      if (t >= 0) {
+        if (p.layout == DATTN_KV_PAGED_HND) {
+          const int blk = blk_of(p, t);
+          if (blk < c.hi - c.lo) {
+            const int pi = p.page_indices[c.lo + blk];
+            if (pi >= 0 && pi < p.num_pages)
+              row = (static_cast<long long>(pi) * p.H_kv + c.it.h) * p.P + row_of(p, t);
+            else
+              atomicOr(p.status, kStPageRange);
+          } else {
+            atomicOr(p.status, kStBlockRange);
+          }
+        } else if (c.crow >= 0 && t < p.T_cap) {
+          row = (static_cast<long long>(c.crow) * p.T_cap + t) * p.H_kv + c.it.h;
+        } else {
+          atomicOr(p.status, kStRowRange);
+        }
+        if (row < 0) t = -1;
+      }
+    }
+    d.t[h] = t;
+    d.row[h] = row;
+  }
+  return d;
+}
+
+template <int D>
+__device__ void produce_bf16(const PartialParams& p, uint8_t* smem, int it_begin, int it_end, int lane, int pw) {
+  using C = Bf<D>;
+  constexpr int kSlotsPerPass = 32 / C::kChunks;   // key rows per warp instruction
+  const uint32_t full0 = smem_u32(smem + C::kFullBar);
+  const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
+  const char* kbase = static_cast<const char*>(p.k);
+  const char* vbase = static_cast<const char*>(p.v);
+  const int sub = lane / C::kChunks, ch = lane % C::kChunks;
+
+  Cursor cur;
+  cur.ii = it_begin;
+  seek(p, cur, it_end, lane);
+  for (int i = 0; i < pw; ++i) advance(p, cur, it_end, lane);
+  SlotRows dcur = describe_rows(p, cur, lane);
+  for (uint32_t k = pw; cur.valid; k += kProducerWarps) {
+    Cursor nxt = cur;
+    for (int i = 0; i < kProducerWarps; ++i) advance(p, nxt, it_end, lane);
+    const SlotRows dnxt = describe_rows(p, nxt, lane);   // page-table loads in flight while we wait
+
+    const int st = k % C::kStagesN;
+    const uint32_t use = k / C::kStagesN;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
+    pos[lane] = dcur.t[0];
+    pos[lane + 32] = dcur.t[1];
+    const bool full = stage_is_full(p, cur, dcur.t[0], dcur.t[1]);
+    if (lane == 0) {
+      reinterpret_cast<int*>(smem + C::kFlags)[st] = full ? kFlagFull : 0;
+      reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
+    }
+    const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
+#pragma unroll 4
+    for (int s0 = 0; s0 < kTK; s0 += kSlotsPerPass) {
+      const int s = s0 + sub;
+      const long long row = __shfl_sync(kAll, s0 < 32 ? dcur.row[0] : dcur.row[1], s & 31);
+      const bool ok = row >= 0;
+      const long long off = (ok ? row : 0) * C::kRowB + ch * 16;
+      const uint32_t dst = tile_off<D>(s, ch);
+      cp_async16(kt + dst, kbase + off, ok ? 16u : 0u);
+      cp_async16(vt + dst, vbase + off, ok ? 16u : 0u);
+    }
+    const uint32_t fb = full0 + 8 * st;
+    cp_async_mbar_arrive(fb);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
+    cur = nxt;
+    dcur = dnxt;
+  }
+  asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
+}
+
+// ---- consumers --------------------------------------------------------------------------
+
+// Writes one query row of a warp's result: O / LSE when the item is its
+// group's only state, else the row's partial state (m in log2 units, l, u).
+template <int D>
+__device__ __forceinline__ void emit_row(const PartialParams& p, const WorkItem& it, int my_state, int row, float m,
+                                         float l, const float (&o)[D / 8][4], int half, int t4) {
+  const int i = row / p.g, hq = it.h * p.g + row % p.g;
+  const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
+  if (it.slot < 0) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n)
+      *reinterpret_cast<__nv_bfloat162*>(out + 8 * n + 2 * t4) =
+          __floats2bfloat162_rn(o[n][2 * half] * inv, o[n][2 * half + 1] * inv);
+    if (t4 == 0 && p.lse) p.lse[orow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+  } else {
+    const long long srow = static_cast<long long>(it.slot + my_state) * p.rows + row;
+    float* u = p.u + srow * D;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n)
+      *reinterpret_cast<float2*>(u + 8 * n + 2 * t4) = make_float2(o[n][2 * half], o[n][2 * half + 1]);
+    if (t4 == 0) p.ml[srow] = make_float2(l > 0.f ? m : -INFINITY, l);
+  }
+}
+
+template <int D>
+__device__ void consume_bf16(const PartialParams& p, uint8_t* smem, int it_begin, int it_end, int cw, int lane) {
+  using C = Bf<D>;
+  constexpr int KS = D / 16;   // k-steps of q.k
+  constexpr int NT = D / 8;    // 8-channel tiles of the output
+  const uint32_t full0 = smem_u32(smem + C::kFullBar);
+  const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
+
+  // Row blocks of 16 query rows; with one block, two stage groups of four
+  // warps take alternate stages.  Each warp owns 16 keys of its stages.
+  const int nrb = p.rows <= 16 ? 1 : 2;
+  const int ng = nrb == 1 ? 2 : 1;
+  const int wps = kConsumerWarps / ng;
+  const int sgrp = cw / wps, wi = cw % wps;
+  const int rb = wi % nrb, ts = wi / nrb;
+  const int my_state = (cw - rb) / nrb;
+  const int g4 = lane >> 2, t4 = lane & 3;
+  const int r0 = rb * 16 + g4, r1 = r0 + 8;   // the lane's two accumulator rows
+  const bool ok0 = r0 < p.rows, ok1 = r1 < p.rows;
+  const int qi0 = r0 / p.g, qi1 = r1 / p.g;
+  const int lrow = lane & 7, lmat = lane >> 3;   // ldmatrix address roles
+  const float sc = p.scale_log2;
+
+  uint32_t k = 0;
+  bool dead = false;   // a bounded wait gave up: stop consuming, write nothing
+  for (int ii = it_begin; ii < it_end; ++ii) {
+    const WorkItem it = read_item(p, p.cta_items[ii], false);
+    const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+
+    // query rows r0, r1 as A fragments (rows past the group are zero)
+    uint32_t qa[KS][4];
+    {
+      const uint32_t* q0 = static_cast<const uint32_t*>(p.q) +
+                           ((static_cast<long long>(it.b) * p.S_q + qi0) * p.H_q + it.h * p.g + r0 % p.g) * (D / 2);
+      const uint32_t* q1 = static_cast<const uint32_t*>(p.q) +
+                           ((static_cast<long long>(it.b) * p.S_q + qi1) * p.H_q + it.h * p.g + r1 % p.g) * (D / 2);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qa[kk][0] = ok0 ? q0[8 * kk + t4] : 0u;
+        qa[kk][1] = ok1 ? q1[8 * kk + t4] : 0u;
+        qa[kk][2] = ok0 ? q0[8 * kk + 4 + t4] : 0u;
+        qa[kk][3] = ok1 ? q1[8 * kk + 4 + t4] : 0u;
+      }
+    }
+    float o[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    for (int j0 = it.a; j0 < it.e; ++k) {
+      const int j1 = min(j0 + kTK, it.e);
+      if (static_cast<int>(k % ng) != sgrp) {     // the other stage group's turn
+        j0 = j1;
+        continue;
+      }
+      const int st = k % C::kStagesN;
+      const uint32_t use = k / C::kStagesN;
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+        dead = true;
+        break;
+      }
+      if (reinterpret_cast<const volatile int*>(smem + C::kSeq)[st] != static_cast<int>(k)) {
+        if (lane == 0) atomicOr(p.status, kStPipeline);   // wrong phase: stop, never consume stale data
+        *abort_flag = 1;
+        dead = true;
+        break;
+      }
+      const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kTK;
+      const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
+      const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
+      const int base = ts * 16;
+
+      // S = Q K^T over the warp's 16 keys (two 8-key tiles)
+      float s[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+        for (int m = 0; m < KS / 2; ++m) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kt + tile_off<D>(base + nt * 8 + lrow, 4 * m + lmat), b0, b1, b2, b3);
+          mma_bf16(s[nt], qa[2 * m], b0, b1);
+          mma_bf16(s[nt], qa[2 * m + 1], b2, b3);
+        }
+      }
+      // scale to log2 units, -inf where the key is absent or masked for the row
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = pos[base + nt * 8 + 2 * t4 + e];
+          const bool v0 = t >= 0 && ok0 && (full || key_visible(mc, qi0, t));
+          const bool v1 = t >= 0 && ok1 && (full || key_visible(mc, qi1, t));
+          s[nt][e] = v0 ? s[nt][e] * sc : -INFINITY;
+          s[nt][2 + e] = v1 ? s[nt][2 + e] * sc : -INFINITY;
+        }
+      }
+      // online softmax: row maxima over the lane quad
+      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 2));
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+      const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+      const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+      float pr[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        pr[nt][0] = exp2f(s[nt][0] - u0);
+        pr[nt][1] = exp2f(s[nt][1] - u0);
+        pr[nt][2] = exp2f(s[nt][2] - u1);
+        pr[nt][3] = exp2f(s[nt][3] - u1);
+      }
+      l0 = l0 * a0 + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
+      l1 = l1 * a1 + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+      m0 = n0;
+      m1 = n1;
+      if (__any_sync(kAll, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          o[n][0] *= a0;
+          o[n][1] *= a0;
+          o[n][2] *= a1;
+          o[n][3] *= a1;
+        }
+      }
+      // O += P V: the S fragments re-packed as the A operand (keys are the k index)
+      const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
+                              pack_bf16(pr[1][0], pr[1][1]), pack_bf16(pr[1][2], pr[1][3])};
+#pragma unroll
+      for (int n2 = 0; n2 < NT / 2; ++n2) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vt + tile_off<D>(base + (lmat & 1) * 8 + lrow, 2 * n2 + (lmat >> 1)), v0, v1, v2, v3);
+        mma_bf16(o[2 * n2], pa, v0, v1);
+        mma_bf16(o[2 * n2 + 1], pa, v2, v3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      j0 = j1;
+    }
+
+    // end of item: complete the row sums over the quad and leave the rows
+    l0 += __shfl_xor_sync(kAll, l0, 1);
+    l1 += __shfl_xor_sync(kAll, l1, 1);
+    l0 += __shfl_xor_sync(kAll, l0, 2);
+    l1 += __shfl_xor_sync(kAll, l1, 2);
+    if (!dead) {
+      if (ok0) emit_row<D>(p, it, my_state, r0, m0, l0, o, 0, t4);
+      if (ok1) emit_row<D>(p, it, my_state, r1, m1, l1, o, 1, t4);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_constant__ PartialParams p) {
+  using C = Bf<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (threadIdx.x == 0) {
+    const int warps_per_stage = p.rows <= 16 ? kConsumerWarps / 2 : kConsumerWarps;
+    for (int s = 0; s < C::kStagesN; ++s) {
+      mbar_init(smem_u32(smem + C::kFullBar + 8 * s), 1);
+      mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), warps_per_stage);
+    }
+    *reinterpret_cast<int*>(smem + C::kAbort) = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= kConsumerWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    produce_bf16<D>(p, smem, it_begin, it_end, lane, warp - kConsumerWarps);
+    return;
+  }
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+  consume_bf16<D>(p, smem, it_begin, it_end, warp, lane);
+}
+
+template <int D>
+int launch_bf16(const PartialParams& p, int n_ctas, void* stream) {
+  const size_t smem = Bf<D>::kTotal;
+  // The consumers' setmaxnreg.inc waits for registers released by the producer
+  // warpgroup; it can only complete if the launch holds enough of them.
+  cudaFuncAttributes attr;
+  cudaError_t err = cudaFuncGetAttributes(&attr, partial_bf16_kernel<D>);
+  if (err != cudaSuccess) return err;
+  if (attr.numRegs * kThreads < 128 * kProducerRegs + 32 * kConsumerWarps * kConsumerRegs)
+    return cudaErrorInvalidConfiguration;
+  err = cudaFuncSetAttribute(partial_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  partial_bf16_kernel<D><<<n_ctas, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_partial_bf16(const PartialParams& p, int d, int n_ctas, void* stream) {
+  return d == 64 ? launch_bf16<64>(p, n_ctas, stream) : launch_bf16<128>(p, n_ctas, stream);
+}
+
+}  // namespace dattn

@@ -246,7 +246,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   //    an item leaves its own state, so an item owns states_per_item slots; a
   //    group that is one item with one state per row writes O directly.
   std::vector<MergeGroup> merges;
-  const int spi = states_per_item(rows);
+  const int spi = states_per_item(rows, p.fmt);
   int n_slots = 0, max_splits = 0;
   for (int k = 0; k < n_groups; ++k) {
     const int n = group_first[k + 1] - group_first[k];
