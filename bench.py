@@ -81,7 +81,7 @@ def algorithmic_bytes(w, info, items):
 def kernel_hash():
     """Hash of the partial kernel's sources: DRAM counters taken on other sources are stale."""
     h = hashlib.sha256()
-    for f in ("device.cuh", "internal.h", "partial.cu"):
+    for f in ("device.cuh", "internal.h", "stream.cuh", "partial_bf16.cu"):
         with open(os.path.join(ROOT, "split_kv_decode_flash_gb300", "csrc", f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

@@ -39,6 +39,45 @@ namespace dattn {
 namespace {
 
 constexpr unsigned kAll = 0xffffffffu;
+constexpr int kItemCache = 256;       // work items of a CTA kept in shared memory
+// setmaxnreg split of the launch's 384 x 168 registers: the producer
+// warpgroup's description pipeline needs more than the byte-format kernel's.
+constexpr int kBfProducerRegs = 96;
+constexpr int kBfConsumerRegs = 200;
+static_assert(128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs <= kThreads * 168, "register split");
+constexpr uint32_t kNoRow = 0xFFFFFFFFu;
+
+// A work item as the kernel walks it, with its cache coordinates.
+struct ItemRec {
+  WorkItem it;      // keys dropped (e = a) when an index list disagrees with the plan
+  int lo, hi;       // paged: the request's page list [lo, hi)
+  int crow, pad;    // contiguous: cache row (-1: outside the cache)
+};
+static_assert(sizeof(ItemRec) == 48, "ItemRec layout");
+
+__device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int idx, bool report) {
+  ItemRec r;
+  r.it = read_item(p, idx, report);
+  r.lo = r.hi = r.crow = r.pad = 0;
+  if (p.layout == DATTN_KV_PAGED_HND) {
+    r.lo = p.page_indptr[r.it.b];
+    r.hi = p.page_indptr[r.it.b + 1];
+  } else {
+    r.crow = cache_row(p.cache_batch_idx, r.it.b, p.B_cache, report ? p.status : nullptr);
+  }
+  return r;
+}
+
+// The CTA's item list: the first kItemCache records come from shared memory
+// (filled once at kernel start), later ones from global memory.
+struct Walk {
+  const PartialParams& p;
+  const ItemRec* cache;
+  int begin, end;
+  __device__ __forceinline__ ItemRec rec(int ii) const {
+    return ii - begin < kItemCache ? cache[ii - begin] : load_rec(p, p.cta_items[ii], false);
+  }
+};
 
 template <int D>
 struct Bf {
@@ -56,7 +95,8 @@ struct Bf {
   static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
   static constexpr int kAbort = kEmptyBar + kStagesN * 8;
-  static constexpr int kTotal = align16(kAbort + 16);
+  static constexpr int kItems = align16(kAbort + 16);   // ItemRec [kItemCache]
+  static constexpr int kTotal = kItems + kItemCache * 48;
   static_assert(kTotal <= 232448, "shared memory of one CTA");
 };
 
@@ -110,53 +150,123 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // ---- producer ---------------------------------------------------------------------------
 
-struct SlotRows {
-  int t[2];          // logical key of slots lane and lane + 32 (-1: none)
-  long long row[2];  // K/V row of that key in the cache, in rows of d elements (-1: none)
+// A producer warp's position: stream keys [j0, j1) of item ii (ii == end: none).
+struct PCur {
+  int ii, j0, j1;
 };
 
-__device__ __forceinline__ SlotRows describe_rows(const PartialParams& p, const Cursor& c, int lane) {
-  SlotRows d;
+__device__ __forceinline__ void pc_seek(const Walk& w, PCur& c) {
+  for (; c.ii < w.end; ++c.ii) {
+    const WorkItem it = w.rec(c.ii).it;
+    if (it.e > it.a) {
+      c.j0 = it.a;
+      c.j1 = min(it.a + kTK, it.e);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void pc_advance(const Walk& w, PCur& c, int n) {
+  for (int i = 0; i < n && c.ii < w.end; ++i) {
+    const int e = w.rec(c.ii).it.e;
+    if (c.j1 < e) {
+      c.j0 = c.j1;
+      c.j1 = min(c.j0 + kTK, e);
+    } else {
+      ++c.ii;
+      pc_seek(w, c);
+    }
+  }
+}
+
+// The description of a stage is built in three steps, each issued one stage
+// of this warp ahead of the next, so no load result is awaited right after
+// it was issued: logical keys (index-list entries are loads), page ids of the
+// keys' blocks (page-list loads, M4.5 §0x04D), and finally the checked K/V
+// row of every slot.
+struct SlotKeys {
+  int t[2];      // logical key of slots lane and lane + 32 (-1: none)
+};
+struct SlotPages {
+  int pi[2];     // page id of the key's block (-2: block outside the page list)
+};
+struct SlotRows {
+  int t[2];           // logical key, -1 when the slot is empty or invalid
+  uint32_t row[2];    // K/V row in the cache in rows of d elements (kNoRow: none)
+  bool full;          // FULL stage class
+};
+
+__device__ __forceinline__ SlotKeys slot_keys(const Walk& w, const PCur& c, int lane) {
+  SlotKeys k;
+  k.t[0] = k.t[1] = -1;
+  if (c.ii >= w.end) return k;
+  const WorkItem it = w.rec(c.ii).it;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int j = c.j0 + lane + 32 * h;
-    int t = -1;
-    long long row = -1;
-    if (c.valid && j < c.j1) {
-      t = stream_key(c.it, p.mask, p.index_list, j);
-      if (p.mask == DATTN_MASK_INDEX_LIST && (t < 0 || t >= c.it.T)) {
-        atomicOr(p.status, kStListRange);
-        t = -1;
+    if (j < c.j1) k.t[h] = stream_key(it, w.p.mask, w.p.index_list, j);
+  }
+  return k;
+}
+
+__device__ __forceinline__ SlotPages slot_pages(const Walk& w, const PCur& c, const SlotKeys& k) {
+  SlotPages g;
+  g.pi[0] = g.pi[1] = -2;
+  if (c.ii >= w.end || w.p.layout != DATTN_KV_PAGED_HND) return g;
+  const ItemRec r = w.rec(c.ii);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = k.t[h];
+    if (t >= 0 && t < r.it.T) {
+      const int blk = blk_of(w.p, t);
+      if (blk < r.hi - r.lo) g.pi[h] = w.p.page_indices[r.lo + blk];
+    }
+  }
+  return g;
+}
+
+__device__ __forceinline__ SlotRows slot_rows(const Walk& w, const PCur& c, const SlotKeys& k, const SlotPages& g,
+                                              int lane) {
+  const PartialParams& p = w.p;
+  SlotRows d;
+  d.t[0] = d.t[1] = -1;
+  d.row[0] = d.row[1] = kNoRow;
+  d.full = false;
+  if (c.ii >= w.end) return d;
+  const ItemRec r = w.rec(c.ii);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    int t = k.t[h];
+    uint32_t row = kNoRow;
+    if (p.mask == DATTN_MASK_INDEX_LIST && c.j0 + lane + 32 * h < c.j1 &&
+        (t < 0 || t >= r.it.T)) {
+      atomicOr(p.status, kStListRange);
+      t = -1;
+    }
+    if (t >= 0) {
+      if (p.layout == DATTN_KV_PAGED_HND) {
+        const int pi = g.pi[h];
+        if (pi == -2) atomicOr(p.status, kStBlockRange);
+        else if (pi < 0 || pi >= p.num_pages) atomicOr(p.status, kStPageRange);
+        else row = (static_cast<uint32_t>(pi) * p.H_kv + r.it.h) * p.P + row_of(p, t);
+      } else if (r.crow >= 0 && t < p.T_cap) {
+        row = (static_cast<uint32_t>(r.crow) * p.T_cap + t) * p.H_kv + r.it.h;
+      } else {
+        atomicOr(p.status, kStRowRange);
       }
-      if (t >= 0) {
-        if (p.layout == DATTN_KV_PAGED_HND) {
-          const int blk = blk_of(p, t);
-          if (blk < c.hi - c.lo) {
-            const int pi = p.page_indices[c.lo + blk];
-            if (pi >= 0 && pi < p.num_pages)
-              row = (static_cast<long long>(pi) * p.H_kv + c.it.h) * p.P + row_of(p, t);
-            else
-              atomicOr(p.status, kStPageRange);
-          } else {
-            atomicOr(p.status, kStBlockRange);
-          }
-        } else if (c.crow >= 0 && t < p.T_cap) {
-          row = (static_cast<long long>(c.crow) * p.T_cap + t) * p.H_kv + c.it.h;
-        } else {
-          atomicOr(p.status, kStRowRange);
-        }
-        if (row < 0) t = -1;
-      }
+      if (row == kNoRow) t = -1;
     }
     d.t[h] = t;
     d.row[h] = row;
   }
+  d.full = stage_is_full(p, r.it, c.j0, c.j1, d.t[0], d.t[1]);
   return d;
 }
 
 template <int D>
-__device__ void produce_bf16(const PartialParams& p, uint8_t* smem, int it_begin, int it_end, int lane, int pw) {
+__device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
   using C = Bf<D>;
+  const PartialParams& p = w.p;
   constexpr int kSlotsPerPass = 32 / C::kChunks;   // key rows per warp instruction
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
   const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
@@ -165,34 +275,38 @@ __device__ void produce_bf16(const PartialParams& p, uint8_t* smem, int it_begin
   const char* vbase = static_cast<const char*>(p.v);
   const int sub = lane / C::kChunks, ch = lane % C::kChunks;
 
-  Cursor cur;
-  cur.ii = it_begin;
-  seek(p, cur, it_end, lane);
-  for (int i = 0; i < pw; ++i) advance(p, cur, it_end, lane);
-  SlotRows dcur = describe_rows(p, cur, lane);
-  for (uint32_t k = pw; cur.valid; k += kProducerWarps) {
-    Cursor nxt = cur;
-    for (int i = 0; i < kProducerWarps; ++i) advance(p, nxt, it_end, lane);
-    const SlotRows dnxt = describe_rows(p, nxt, lane);   // page-table loads in flight while we wait
+  // this warp's stages: pw, pw + 4, pw + 8, ... of the CTA's stage sequence
+  PCur c0{w.begin, 0, 0};
+  pc_seek(w, c0);
+  pc_advance(w, c0, pw);
+  PCur c1 = c0;
+  pc_advance(w, c1, kProducerWarps);
+  PCur c2 = c1;
+  pc_advance(w, c2, kProducerWarps);
+  const SlotKeys k0 = slot_keys(w, c0, lane);
+  SlotRows r0 = slot_rows(w, c0, k0, slot_pages(w, c0, k0), lane);
+  SlotKeys k1 = slot_keys(w, c1, lane);
+  SlotPages g1 = slot_pages(w, c1, k1);
+  SlotKeys k2 = slot_keys(w, c2, lane);
 
+  for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
     if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
-    pos[lane] = dcur.t[0];
-    pos[lane + 32] = dcur.t[1];
-    const bool full = stage_is_full(p, cur, dcur.t[0], dcur.t[1]);
+    pos[lane] = r0.t[0];
+    pos[lane + 32] = r0.t[1];
     if (lane == 0) {
-      reinterpret_cast<int*>(smem + C::kFlags)[st] = full ? kFlagFull : 0;
+      reinterpret_cast<int*>(smem + C::kFlags)[st] = r0.full ? kFlagFull : 0;
       reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
     }
     const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
-#pragma unroll 4
+#pragma unroll
     for (int s0 = 0; s0 < kTK; s0 += kSlotsPerPass) {
       const int s = s0 + sub;
-      const long long row = __shfl_sync(kAll, s0 < 32 ? dcur.row[0] : dcur.row[1], s & 31);
-      const bool ok = row >= 0;
-      const long long off = (ok ? row : 0) * C::kRowB + ch * 16;
+      const uint32_t row = __shfl_sync(kAll, s0 < 32 ? r0.row[0] : r0.row[1], s & 31);
+      const bool ok = row != kNoRow;
+      const size_t off = static_cast<size_t>(ok ? row : 0u) * C::kRowB + ch * 16;
       const uint32_t dst = tile_off<D>(s, ch);
       cp_async16(kt + dst, kbase + off, ok ? 16u : 0u);
       cp_async16(vt + dst, vbase + off, ok ? 16u : 0u);
@@ -201,8 +315,15 @@ __device__ void produce_bf16(const PartialParams& p, uint8_t* smem, int it_begin
     cp_async_mbar_arrive(fb);
     __syncwarp();
     if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
-    cur = nxt;
-    dcur = dnxt;
+
+    // move the description pipeline one stage of this warp forward
+    r0 = slot_rows(w, c1, k1, g1, lane);
+    c0 = c1;
+    g1 = slot_pages(w, c2, k2);
+    k1 = k2;
+    c1 = c2;
+    pc_advance(w, c2, kProducerWarps);
+    k2 = slot_keys(w, c2, lane);
   }
   asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
 }
@@ -234,9 +355,29 @@ __device__ __forceinline__ void emit_row(const PartialParams& p, const WorkItem&
   }
 }
 
+// The two accumulator rows r0, r1 of a lane, for item "it", as mma A
+// fragments (rows past the group are zero).
 template <int D>
-__device__ void consume_bf16(const PartialParams& p, uint8_t* smem, int it_begin, int it_end, int cw, int lane) {
+__device__ __forceinline__ void load_q(const PartialParams& p, const WorkItem& it, int r0, int r1, int t4,
+                                       uint32_t (&qa)[D / 16][4]) {
+  const bool ok0 = r0 < p.rows, ok1 = r1 < p.rows;
+  const uint32_t* q0 = static_cast<const uint32_t*>(p.q) +
+                       ((static_cast<long long>(it.b) * p.S_q + r0 / p.g) * p.H_q + it.h * p.g + r0 % p.g) * (D / 2);
+  const uint32_t* q1 = static_cast<const uint32_t*>(p.q) +
+                       ((static_cast<long long>(it.b) * p.S_q + r1 / p.g) * p.H_q + it.h * p.g + r1 % p.g) * (D / 2);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    qa[kk][0] = ok0 ? q0[8 * kk + t4] : 0u;
+    qa[kk][1] = ok1 ? q1[8 * kk + t4] : 0u;
+    qa[kk][2] = ok0 ? q0[8 * kk + 4 + t4] : 0u;
+    qa[kk][3] = ok1 ? q1[8 * kk + 4 + t4] : 0u;
+  }
+}
+
+template <int D>
+__device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane) {
   using C = Bf<D>;
+  const PartialParams& p = w.p;
   constexpr int KS = D / 16;   // k-steps of q.k
   constexpr int NT = D / 8;    // 8-channel tiles of the output
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
@@ -260,25 +401,18 @@ __device__ void consume_bf16(const PartialParams& p, uint8_t* smem, int it_begin
 
   uint32_t k = 0;
   bool dead = false;   // a bounded wait gave up: stop consuming, write nothing
-  for (int ii = it_begin; ii < it_end; ++ii) {
-    const WorkItem it = read_item(p, p.cta_items[ii], false);
+  // the next item's query fragments are loaded while the current item runs
+  uint32_t qn[KS][4];
+  if (w.begin < w.end) load_q<D>(p, w.rec(w.begin).it, r0, r1, t4, qn);
+  for (int ii = w.begin; ii < w.end; ++ii) {
+    const WorkItem it = w.rec(ii).it;
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
-
-    // query rows r0, r1 as A fragments (rows past the group are zero)
     uint32_t qa[KS][4];
-    {
-      const uint32_t* q0 = static_cast<const uint32_t*>(p.q) +
-                           ((static_cast<long long>(it.b) * p.S_q + qi0) * p.H_q + it.h * p.g + r0 % p.g) * (D / 2);
-      const uint32_t* q1 = static_cast<const uint32_t*>(p.q) +
-                           ((static_cast<long long>(it.b) * p.S_q + qi1) * p.H_q + it.h * p.g + r1 % p.g) * (D / 2);
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        qa[kk][0] = ok0 ? q0[8 * kk + t4] : 0u;
-        qa[kk][1] = ok1 ? q1[8 * kk + t4] : 0u;
-        qa[kk][2] = ok0 ? q0[8 * kk + 4 + t4] : 0u;
-        qa[kk][3] = ok1 ? q1[8 * kk + 4 + t4] : 0u;
-      }
-    }
+    for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) qa[kk][x] = qn[kk][x];
+    if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1).it, r0, r1, t4, qn);
     float o[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -395,6 +529,10 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_constant__ PartialParams p) {
   using C = Bf<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
+  const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
+  ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
+  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
+    cache[i] = load_rec(p, p.cta_items[it_begin + i], true);
   if (threadIdx.x == 0) {
     const int warps_per_stage = p.rows <= 16 ? kConsumerWarps / 2 : kConsumerWarps;
     for (int s = 0; s < C::kStagesN; ++s) {
@@ -405,15 +543,15 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
     fence_barrier_init();
   }
   __syncthreads();
-  const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
+  const Walk w{p, cache, it_begin, it_end};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-    produce_bf16<D>(p, smem, it_begin, it_end, lane, warp - kConsumerWarps);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBfProducerRegs));
+    produce_bf16<D>(w, smem, lane, warp - kConsumerWarps);
     return;
   }
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-  consume_bf16<D>(p, smem, it_begin, it_end, warp, lane);
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));
+  consume_bf16<D>(w, smem, warp, lane);
 }
 
 template <int D>
@@ -424,7 +562,7 @@ int launch_bf16(const PartialParams& p, int n_ctas, void* stream) {
   cudaFuncAttributes attr;
   cudaError_t err = cudaFuncGetAttributes(&attr, partial_bf16_kernel<D>);
   if (err != cudaSuccess) return err;
-  if (attr.numRegs * kThreads < 128 * kProducerRegs + 32 * kConsumerWarps * kConsumerRegs)
+  if (attr.numRegs * kThreads < 128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs)
     return cudaErrorInvalidConfiguration;
   err = cudaFuncSetAttribute(partial_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));

@@ -59,13 +59,21 @@ void check_problem(const dattn_problem* p, Checker& c) {
     c.fail(DATTN_EINVAL, "unknown layout");
   if (p->fmt < DATTN_FMT_BF16 || p->fmt > DATTN_FMT_INT4_KIVI) c.fail(DATTN_EINVAL, "unknown format");
   if (p->mask < DATTN_MASK_CAUSAL || p->mask > DATTN_MASK_INDEX_LIST) c.fail(DATTN_EINVAL, "unknown mask");
+  // K/V rows (one kv head, one token) are addressed with 32-bit row indices
+  const long long kMaxPoolRows = 0xFFFFFFFFll;
   if (p->layout == DATTN_KV_PAGED_HND) {
     if (p->page_size < 1) c.fail(DATTN_EINVAL, "paged layout needs page_size >= 1");
     if (p->num_pages < 1) c.fail(DATTN_EINVAL, "paged layout needs num_pages >= 1");
+    if (p->page_size >= 1 && p->num_pages >= 1 && p->H_kv >= 1 &&
+        static_cast<long long>(p->num_pages) * p->H_kv * p->page_size >= kMaxPoolRows)
+      c.fail(DATTN_EUNSUPPORTED, "num_pages * H_kv * page_size must be below 2^32 - 1 rows");
   } else if (p->layout == DATTN_KV_CONTIG_NHD) {
     if (p->fmt != DATTN_FMT_BF16) c.fail(DATTN_EUNSUPPORTED, "quantized formats need the paged layout");
     if (p->T_cap < 1) c.fail(DATTN_EINVAL, "contiguous layout needs T_cap >= 1");
     if (p->B_cache < 1) c.fail(DATTN_EINVAL, "contiguous layout needs B_cache >= 1");
+    if (p->T_cap >= 1 && p->B_cache >= 1 && p->H_kv >= 1 &&
+        static_cast<long long>(p->B_cache) * p->T_cap * p->H_kv >= kMaxPoolRows)
+      c.fail(DATTN_EUNSUPPORTED, "B_cache * T_cap * H_kv must be below 2^32 - 1 rows");
   }
   if (p->fmt == DATTN_FMT_INT8_TOKEN && p->page_size >= 1 && (p->page_size % 4 || p->page_size > 256))
     c.fail(DATTN_EUNSUPPORTED, "INT8 pages must hold a multiple of 4 rows, at most 256");
