@@ -737,6 +737,8 @@ template <int D, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) partial_kernel(const __grid_constant__ PartialParams p) {
   using C = Cfg<D, FMT>;
   extern __shared__ __align__(1024) uint8_t smem[];
+  // the merge kernel may be scheduled now; it waits for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // zero the ring so that slots never written hold finite values
   for (int i = threadIdx.x; i < C::kStagesN * C::kStage / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);

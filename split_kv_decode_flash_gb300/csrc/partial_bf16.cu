@@ -529,6 +529,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_constant__ PartialParams p) {
   using C = Bf<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
+  // the merge kernel may be scheduled now; it waits for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
   for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
