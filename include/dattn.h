@@ -111,7 +111,9 @@ typedef struct {
 /* Host-side inputs of the planner. */
 typedef struct {
   const int32_t* kv_len;        /* host [B]: stored rows T_b (>= 0)                       */
-  const int32_t* page_indptr;   /* host [B+1] or NULL: checked against ceil(T_b / P)      */
+  const int32_t* page_indptr;   /* host [B+1] or NULL: checked against ceil(T_b / P); when
+                                   given, runs take the page-list bounds from the plan, so
+                                   the device page_indptr must hold the same contents    */
   const int32_t* index_indptr;  /* host [B*H_kv+1], INDEX_LIST only: list of (b, h_kv) is
                                    index_list[index_indptr[b*H_kv+h] : ...[b*H_kv+h+1]]  */
   const int32_t* index_list;    /* host or NULL; when given, every list is checked to be

@@ -145,6 +145,7 @@ void bind_blob(const dattn_plan_t* plan, void* ws, PartialParams& k) {
   k.items = reinterpret_cast<const WorkItem*>(base + h->off_items);
   k.cta_indptr = reinterpret_cast<const int32_t*>(base + h->off_cta_indptr);
   k.cta_items = reinterpret_cast<const int32_t*>(base + h->off_cta_items);
+  k.cta_recs = reinterpret_cast<const ItemRec*>(base + h->off_cta_recs);
   k.ml = reinterpret_cast<float2*>(base + h->off_ml);
   k.u = reinterpret_cast<float*>(base + h->off_u);
   k.status = reinterpret_cast<int32_t*>(base + offsetof(BlobHeader, status));

@@ -33,16 +33,14 @@ enum StatusBits : int32_t {
   kStPipeline = 64,     // a consumer found a ring stage stamped with another stage number
 };
 
-// Consumer warps are arranged in row blocks; each warp keeps the softmax
-// state of its block's rows over its own share of an item's keys, so an item
-// produces kConsumerWarps / row_blocks partial states per row.  The bf16
-// tensor-core kernel uses blocks of 16 rows (one mma tile), the byte formats
-// blocks of 4 rows.
-inline int row_blocks(int rows, int fmt) {
-  if (fmt == DATTN_FMT_BF16) return rows <= 16 ? 1 : 2;
-  return rows <= 4 ? 1 : rows <= 8 ? 2 : rows <= 16 ? 4 : 8;
+// Partial states an item leaves per query row.  Consumer warps are arranged
+// in row blocks (16 rows, one mma tile, in the bf16 tensor-core kernel; 4 rows
+// in the byte-format kernel); every warp leaves the state of its block's rows
+// over its own share of the item's keys.
+inline int states_per_item(int rows, int fmt) {
+  if (fmt == DATTN_FMT_BF16) return kConsumerWarps / (rows <= 16 ? 1 : 2);
+  return kConsumerWarps / (rows <= 4 ? 1 : rows <= 8 ? 2 : rows <= 16 ? 4 : 8);
 }
-inline int states_per_item(int rows, int fmt) { return kConsumerWarps / row_blocks(rows, fmt); }
 
 // One unit of producer work: keys [a, e) of the visible stream of group (b, h).
 // Interval programs: stream index j maps to position j < x0 ? j : x1 + (j - x0).
@@ -56,14 +54,26 @@ struct MergeGroup {
   int32_t b, h, slot0, n;
 };
 
+// A work item with its request's page-list bounds, stored in CTA order so a
+// CTA reads its items with one dependent load.
+struct ItemRec {
+  WorkItem it;
+  int32_t lo, hi;      // paged layout: page list entries [lo, hi) of request it.b
+  int32_t crow, pad;   // contiguous layout: cache row, resolved by the kernel
+};
+static_assert(sizeof(ItemRec) == 48, "ItemRec layout");
+
+// Item lists per CTA (workers of one CTA that walk lists of their own).
+inline int workers_per_cta(int /*fmt*/) { return 1; }
+
 // Head of the plan blob, copied to the start of the workspace by every run.
 struct BlobHeader {
   uint32_t magic;
   int32_t status;        // device status word, zeroed by the copy
   int32_t n_items, n_ctas, n_merge, rows, n_slots, pad;
-  int64_t off_items, off_cta_indptr, off_cta_items, off_merge, off_ml, off_u;
+  int64_t off_items, off_cta_indptr, off_cta_items, off_merge, off_ml, off_u, off_cta_recs, reserved;
 };
-static_assert(sizeof(BlobHeader) == 80, "BlobHeader layout");
+static_assert(sizeof(BlobHeader) == 96, "BlobHeader layout");
 
 // Arguments of the partial kernel (passed by value as a grid constant).
 struct PartialParams {
@@ -82,8 +92,9 @@ struct PartialParams {
   void* o;
   float* lse;
   const WorkItem* items;
-  const int32_t* cta_indptr;
+  const int32_t* cta_indptr;   // [n_ctas * workers_per_cta + 1]: item range of every worker
   const int32_t* cta_items;
+  const ItemRec* cta_recs;   // the items of cta_items as records, same order
   float2* ml;            // [n_slots * rows] (m in log2 units, l)
   float* u;              // [n_slots * rows * d]
   int32_t* status;

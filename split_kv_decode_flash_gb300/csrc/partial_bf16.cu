@@ -47,21 +47,25 @@ constexpr int kBfConsumerRegs = 200;
 static_assert(128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs <= kThreads * 168, "register split");
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;
 
-// A work item as the kernel walks it, with its cache coordinates.
-struct ItemRec {
-  WorkItem it;      // keys dropped (e = a) when an index list disagrees with the plan
-  int lo, hi;       // paged: the request's page list [lo, hi)
-  int crow, pad;    // contiguous: cache row (-1: outside the cache)
-};
-static_assert(sizeof(ItemRec) == 48, "ItemRec layout");
-
-__device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int idx, bool report) {
-  ItemRec r;
-  r.it = read_item(p, idx, report);
-  r.lo = r.hi = r.crow = r.pad = 0;
+// Item record "ii" of the CTA lists, completed with what only the device
+// knows: the page-list bounds when the plan was made without the host page
+// list, the cache row (contiguous layout), and the index-list consistency
+// check (keys dropped, e = a, when the list offsets disagree with the plan).
+__device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int ii, bool report) {
+  ItemRec r = p.cta_recs[ii];
+  if (p.mask == DATTN_MASK_INDEX_LIST) {
+    const int g = r.it.b * p.H_kv + r.it.h;
+    const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
+    if (lo != r.it.x0 || r.it.e > n) {
+      if (report) atomicOr(p.status, kStListRange);
+      r.it.e = r.it.a;
+    }
+  }
   if (p.layout == DATTN_KV_PAGED_HND) {
-    r.lo = p.page_indptr[r.it.b];
-    r.hi = p.page_indptr[r.it.b + 1];
+    if (r.lo < 0) {
+      r.lo = p.page_indptr[r.it.b];
+      r.hi = p.page_indptr[r.it.b + 1];
+    }
   } else {
     r.crow = cache_row(p.cache_batch_idx, r.it.b, p.B_cache, report ? p.status : nullptr);
   }
@@ -75,7 +79,7 @@ struct Walk {
   const ItemRec* cache;
   int begin, end;
   __device__ __forceinline__ ItemRec rec(int ii) const {
-    return ii - begin < kItemCache ? cache[ii - begin] : load_rec(p, p.cta_items[ii], false);
+    return ii - begin < kItemCache ? cache[ii - begin] : load_rec(p, ii, false);
   }
 };
 
@@ -96,7 +100,7 @@ struct Bf {
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
   static constexpr int kAbort = kEmptyBar + kStagesN * 8;
   static constexpr int kItems = align16(kAbort + 16);   // ItemRec [kItemCache]
-  static constexpr int kTotal = kItems + kItemCache * 48;
+  static constexpr int kTotal = kItems + kItemCache * static_cast<int>(sizeof(ItemRec));
   static_assert(kTotal <= 232448, "shared memory of one CTA");
 };
 
@@ -284,10 +288,11 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
   PCur c2 = c1;
   pc_advance(w, c2, kProducerWarps);
   const SlotKeys k0 = slot_keys(w, c0, lane);
-  SlotRows r0 = slot_rows(w, c0, k0, slot_pages(w, c0, k0), lane);
   SlotKeys k1 = slot_keys(w, c1, lane);
+  const SlotPages g0 = slot_pages(w, c0, k0);     // both stages' page lookups in flight together
   SlotPages g1 = slot_pages(w, c1, k1);
   SlotKeys k2 = slot_keys(w, c2, lane);
+  SlotRows r0 = slot_rows(w, c0, k0, g0, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
@@ -534,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
   for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
-    cache[i] = load_rec(p, p.cta_items[it_begin + i], true);
+    cache[i] = load_rec(p, it_begin + i, true);
   if (threadIdx.x == 0) {
     const int warps_per_stage = p.rows <= 16 ? kConsumerWarps / 2 : kConsumerWarps;
     for (int s = 0; s < C::kStagesN; ++s) {

@@ -224,8 +224,10 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   const int cps = in->ctas_per_sm > 0 ? in->ctas_per_sm : kDefaultCtasPerSm;
   const long long cta_target = static_cast<long long>(in->num_sms) * cps;
   long long L = in->chunk_tokens;
-  if (L <= 0) {
-    const long long per = (W + 4 * cta_target - 1) / (4 * cta_target);
+  const int wpc = workers_per_cta(p.fmt);
+  if (L <= 0) {   // about four chunks per worker
+    const long long parts = 4 * wpc * cta_target;
+    const long long per = (W + parts - 1) / parts;
     L = std::max<long long>(kTK, (per + kTK - 1) / kTK * kTK);
   }
   std::vector<int> group_first(n_groups + 1, 0);
@@ -288,6 +290,22 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
     heap.push({load + cost(i), cta});
   }
 
+  // 4b. inside every CTA, the same assignment over its workers (pipelines)
+  std::vector<std::vector<int>> per_worker(static_cast<size_t>(n_ctas) * wpc);
+  for (int cta = 0; cta < n_ctas; ++cta) {
+    std::vector<int> mine = per_cta[cta];
+    std::stable_sort(mine.begin(), mine.end(), [&](int x, int y) { return cost(x) > cost(y); });
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> wheap;
+    for (int w = 0; w < wpc; ++w) wheap.push({0, w});
+    for (int i : mine) {
+      auto [load, w] = wheap.top();
+      wheap.pop();
+      per_worker[static_cast<size_t>(cta) * wpc + w].push_back(i);
+      wheap.push({load + cost(i), w});
+    }
+  }
+  const int n_workers = n_ctas * wpc;
+
   // 5. blob and workspace
   BlobHeader hdr{};
   hdr.magic = kBlobMagic;
@@ -300,11 +318,13 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   hdr.off_items = off;
   off = align_up(off + sizeof(WorkItem) * n_items, 16);
   hdr.off_cta_indptr = off;
-  off = align_up(off + sizeof(int32_t) * (n_ctas + 1), 16);
+  off = align_up(off + sizeof(int32_t) * (n_workers + 1), 16);
   hdr.off_cta_items = off;
   off = align_up(off + sizeof(int32_t) * n_items, 16);
   hdr.off_merge = off;
-  off = align_up(off + sizeof(MergeGroup) * merges.size(), kWsAlign);
+  off = align_up(off + sizeof(MergeGroup) * merges.size(), 16);
+  hdr.off_cta_recs = off;
+  off = align_up(off + sizeof(ItemRec) * n_items, kWsAlign);
   const size_t blob_bytes = off;
   hdr.off_ml = off;
   off = align_up(off + sizeof(float) * 2 * static_cast<size_t>(n_slots) * rows, kWsAlign);
@@ -318,12 +338,23 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   std::memcpy(base + hdr.off_items, items.data(), sizeof(WorkItem) * n_items);
   auto* cta_indptr = reinterpret_cast<int32_t*>(base + hdr.off_cta_indptr);
   auto* cta_items = reinterpret_cast<int32_t*>(base + hdr.off_cta_items);
+  auto* cta_recs = reinterpret_cast<ItemRec*>(base + hdr.off_cta_recs);
   int pos = 0;
-  for (int cta = 0; cta < n_ctas; ++cta) {
-    cta_indptr[cta] = pos;
-    for (int i : per_cta[cta]) cta_items[pos++] = i;
+  for (int wk = 0; wk < n_workers; ++wk) {
+    cta_indptr[wk] = pos;
+    for (int i : per_worker[wk]) {
+      ItemRec r{};
+      r.it = items[i];
+      r.lo = r.hi = -1;      // resolved by the kernel when the host page list is unknown
+      if (p.layout == DATTN_KV_PAGED_HND && in->page_indptr) {
+        r.lo = in->page_indptr[items[i].b];
+        r.hi = in->page_indptr[items[i].b + 1];
+      }
+      cta_recs[pos] = r;
+      cta_items[pos++] = i;
+    }
   }
-  cta_indptr[n_ctas] = pos;
+  cta_indptr[n_workers] = pos;
   if (!merges.empty()) std::memcpy(base + hdr.off_merge, merges.data(), sizeof(MergeGroup) * merges.size());
 
   dattn_plan_info& info = plan->info;
