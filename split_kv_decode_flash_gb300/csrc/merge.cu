@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   __shared__ float sm_u[kMergeWarps][D];
   __shared__ float sm_ml[kMergeWarps][2];
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the partial kernel's states are complete
+  // a programmatically launched successor may be scheduled; it waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = blockIdx.x / p.rows, row = blockIdx.x % p.rows;
   const MergeGroup grp = p.groups[gi];

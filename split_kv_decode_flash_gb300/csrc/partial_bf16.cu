@@ -47,12 +47,12 @@ constexpr int kBfConsumerRegs = 200;
 static_assert(128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs <= kThreads * 168, "register split");
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;
 
-// Item record "ii" of the CTA lists, completed with what only the device
-// knows: the page-list bounds when the plan was made without the host page
-// list, the cache row (contiguous layout), and the index-list consistency
-// check (keys dropped, e = a, when the list offsets disagree with the plan).
-__device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int ii, bool report) {
-  ItemRec r = p.cta_recs[ii];
+// Completes item record r with what only the device knows: the page-list
+// bounds when the plan was made without the host page list, the cache row
+// (contiguous layout), and the index-list consistency check (keys dropped,
+// e = a, when the list offsets disagree with the plan).  Reads device inputs,
+// so only after griddepcontrol.wait.
+__device__ __forceinline__ ItemRec complete_rec(const PartialParams& p, ItemRec r, bool report) {
   if (p.mask == DATTN_MASK_INDEX_LIST) {
     const int g = r.it.b * p.H_kv + r.it.h;
     const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
@@ -70,6 +70,16 @@ __device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int ii, bool
     r.crow = cache_row(p.cache_batch_idx, r.it.b, p.B_cache, report ? p.status : nullptr);
   }
   return r;
+}
+
+// True when complete_rec changes nothing for this problem (paged layout with
+// the page-list bounds in the plan, interval masks).
+__device__ __forceinline__ bool rec_complete_as_planned(const PartialParams& p, const ItemRec& r) {
+  return p.mask != DATTN_MASK_INDEX_LIST && p.layout == DATTN_KV_PAGED_HND && r.lo >= 0;
+}
+
+__device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int ii, bool report) {
+  return complete_rec(p, p.cta_recs[ii], report);
 }
 
 // The CTA's item list: the first kItemCache records come from shared memory
@@ -538,8 +548,13 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
+  // The plan's records may be read while the preceding kernel of the stream
+  // still runs (programmatic launch); device inputs only after the wait.
   for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
-    cache[i] = load_rec(p, it_begin + i, true);
+    cache[i] = p.cta_recs[it_begin + i];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
+    if (!rec_complete_as_planned(p, cache[i])) cache[i] = complete_rec(p, cache[i], true);
   if (threadIdx.x == 0) {
     const int warps_per_stage = p.rows <= 16 ? kConsumerWarps / 2 : kConsumerWarps;
     for (int s = 0; s < C::kStagesN; ++s) {
@@ -574,8 +589,19 @@ int launch_bf16(const PartialParams& p, int n_ctas, void* stream) {
   err = cudaFuncSetAttribute(partial_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  partial_bf16_kernel<D><<<n_ctas, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
-  return cudaGetLastError();
+  // programmatic launch: the prologue overlaps the tail of the preceding kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr_pdl[1];
+  attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr_pdl;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, partial_bf16_kernel<D>, p);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace
