@@ -220,18 +220,30 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
       W += gn[k];
     }
 
-  // 2. chunks
+  // 2. chunks.  Three modes:
+  //  - fixed_splits > 0: balanced quotient/remainder bounds per group (§0x03B);
+  //  - chunk_tokens > 0: chunks of that width, assigned in step 4 longest-first
+  //    to the least-loaded CTA (the FlashInfer paper planner, §0x09E);
+  //  - default: the concatenation of all groups' visible streams is cut into
+  //    equal key segments, one per CTA, and a group is chunked where segment
+  //    boundaries fall into it (every CTA streams the same number of keys).
   const int cps = in->ctas_per_sm > 0 ? in->ctas_per_sm : kDefaultCtasPerSm;
   const long long cta_target = static_cast<long long>(in->num_sms) * cps;
-  long long L = in->chunk_tokens;
+  const long long L = in->chunk_tokens;
   const int wpc = workers_per_cta(p.fmt);
-  if (L <= 0) {   // about four chunks per worker
-    const long long parts = 4 * wpc * cta_target;
-    const long long per = (W + parts - 1) / parts;
-    L = std::max<long long>(kTK, (per + kTK - 1) / kTK * kTK);
+  const bool segmented = p.fixed_splits <= 0 && L <= 0;
+  long long seg = 1;
+  int n_seg = 1;
+  if (segmented && W > 0) {
+    const long long want = std::max<long long>(1, std::min<long long>(cta_target, (W + kTK - 1) / kTK));
+    seg = (W + want - 1) / want;
+    seg = (seg + 15) / 16 * 16;                      // whole 16-key tiles
+    n_seg = static_cast<int>((W + seg - 1) / seg);
   }
   std::vector<int> group_first(n_groups + 1, 0);
+  std::vector<int> seg_cta;                          // segmented mode: the CTA of every item
   auto& items = plan->items;
+  long long g_off = 0;                               // offset of the group in the concatenation
   for (int k = 0; k < n_groups; ++k) {
     group_first[k] = static_cast<int>(items.size());
     const int b = k / H, h = k % H, n = gn[k];
@@ -244,11 +256,24 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
         const int a = s * q + std::min(s, r);
         add(a, a + q + (s < r ? 1 : 0));
       }
+    } else if (segmented) {
+      if (n == 0) {
+        add(0, 0);
+        seg_cta.push_back(static_cast<int>(std::min<long long>(n_seg - 1, g_off / seg)));
+      }
+      for (long long a = 0; a < n;) {
+        const long long c = (g_off + a) / seg;
+        const long long e = std::min<long long>(n, (c + 1) * seg - g_off);
+        add(static_cast<int>(a), static_cast<int>(e));
+        seg_cta.push_back(static_cast<int>(c));
+        a = e;
+      }
     } else if (n == 0) {
       add(0, 0);
     } else {
       for (long long a = 0; a < n; a += L) add(static_cast<int>(a), static_cast<int>(std::min<long long>(n, a + L)));
     }
+    g_off += n;
   }
   group_first[n_groups] = static_cast<int>(items.size());
 
@@ -268,26 +293,35 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
     }
   }
 
-  // 4. longest-first, least-loaded CTA assignment (deterministic ties)
+  // 4. CTA assignment: the segment owner (default mode), else longest-first
+  //    to the least-loaded CTA (deterministic ties)
   const int n_items = static_cast<int>(items.size());
-  const int n_ctas = static_cast<int>(std::min<long long>(cta_target, n_items));
-  std::vector<int> order(n_items);
-  for (int i = 0; i < n_items; ++i) order[i] = i;
+  const int n_ctas = segmented ? n_seg : static_cast<int>(std::min<long long>(cta_target, n_items));
   auto cost = [&](int i) { return static_cast<long long>(items[i].e - items[i].a) + 16; };
-  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost(x) > cost(y); });
   using Slot = std::pair<long long, int>;
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int cta = 0; cta < n_ctas; ++cta) heap.push({0, cta});
   std::vector<std::vector<int>> per_cta(n_ctas);
   std::vector<long long> keys_of(n_ctas, 0);
   plan->item_cta.assign(n_items, 0);
-  for (int i : order) {
-    auto [load, cta] = heap.top();
-    heap.pop();
-    per_cta[cta].push_back(i);
-    plan->item_cta[i] = cta;
-    keys_of[cta] += items[i].e - items[i].a;
-    heap.push({load + cost(i), cta});
+  if (segmented) {
+    for (int i = 0; i < n_items; ++i) {
+      per_cta[seg_cta[i]].push_back(i);
+      plan->item_cta[i] = seg_cta[i];
+      keys_of[seg_cta[i]] += items[i].e - items[i].a;
+    }
+  } else {
+    std::vector<int> order(n_items);
+    for (int i = 0; i < n_items; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost(x) > cost(y); });
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int cta = 0; cta < n_ctas; ++cta) heap.push({0, cta});
+    for (int i : order) {
+      auto [load, cta] = heap.top();
+      heap.pop();
+      per_cta[cta].push_back(i);
+      plan->item_cta[i] = cta;
+      keys_of[cta] += items[i].e - items[i].a;
+      heap.push({load + cost(i), cta});
+    }
   }
 
   // 4b. inside every CTA, the same assignment over its workers (pipelines)
