@@ -63,9 +63,6 @@ struct ItemRec {
 };
 static_assert(sizeof(ItemRec) == 48, "ItemRec layout");
 
-// Item lists per CTA (workers of one CTA that walk lists of their own).
-inline int workers_per_cta(int /*fmt*/) { return 1; }
-
 // Head of the plan blob, copied to the start of the workspace by every run.
 struct BlobHeader {
   uint32_t magic;
@@ -92,7 +89,7 @@ struct PartialParams {
   void* o;
   float* lse;
   const WorkItem* items;
-  const int32_t* cta_indptr;   // [n_ctas * workers_per_cta + 1]: item range of every worker
+  const int32_t* cta_indptr;   // [n_ctas + 1]: item range of every CTA
   const int32_t* cta_items;
   const ItemRec* cta_recs;   // the items of cta_items as records, same order
   float2* ml;            // [n_slots * rows] (m in log2 units, l)

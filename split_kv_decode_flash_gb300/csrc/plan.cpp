@@ -230,7 +230,6 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   const int cps = in->ctas_per_sm > 0 ? in->ctas_per_sm : kDefaultCtasPerSm;
   const long long cta_target = static_cast<long long>(in->num_sms) * cps;
   const long long L = in->chunk_tokens;
-  const int wpc = workers_per_cta(p.fmt);
   const bool segmented = p.fixed_splits <= 0 && L <= 0;
   long long seg = 1;
   int n_seg = 1;
@@ -243,6 +242,9 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   std::vector<int> group_first(n_groups + 1, 0);
   std::vector<int> seg_cta;                          // segmented mode: the CTA of every item
   auto& items = plan->items;
+  items.reserve(static_cast<size_t>(n_groups) + (segmented ? n_seg : 0) +
+                (p.fixed_splits > 0 ? static_cast<size_t>(n_groups) * p.fixed_splits : 0));
+  seg_cta.reserve(items.capacity());
   long long g_off = 0;                               // offset of the group in the concatenation
   for (int k = 0; k < n_groups; ++k) {
     group_first[k] = static_cast<int>(items.size());
@@ -293,52 +295,43 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
     }
   }
 
-  // 4. CTA assignment: the segment owner (default mode), else longest-first
-  //    to the least-loaded CTA (deterministic ties)
+  // 4. CTA assignment: the segment owner (default mode; items are generated
+  //    in segment order already), else longest-first to the least-loaded CTA
+  //    (deterministic ties).  cta_start / cta_order: counting-sort layout of
+  //    the per-CTA item lists.
   const int n_items = static_cast<int>(items.size());
   const int n_ctas = segmented ? n_seg : static_cast<int>(std::min<long long>(cta_target, n_items));
   auto cost = [&](int i) { return static_cast<long long>(items[i].e - items[i].a) + 16; };
-  using Slot = std::pair<long long, int>;
-  std::vector<std::vector<int>> per_cta(n_ctas);
   std::vector<long long> keys_of(n_ctas, 0);
+  std::vector<int> cta_start(n_ctas + 1, 0), cta_order(n_items);
   plan->item_cta.assign(n_items, 0);
+  std::vector<int> order(n_items);          // order in which items are listed per CTA
+  for (int i = 0; i < n_items; ++i) order[i] = i;
   if (segmented) {
-    for (int i = 0; i < n_items; ++i) {
-      per_cta[seg_cta[i]].push_back(i);
-      plan->item_cta[i] = seg_cta[i];
-      keys_of[seg_cta[i]] += items[i].e - items[i].a;
-    }
+    for (int i = 0; i < n_items; ++i) plan->item_cta[i] = seg_cta[i];
   } else {
-    std::vector<int> order(n_items);
-    for (int i = 0; i < n_items; ++i) order[i] = i;
+    using Slot = std::pair<long long, int>;
     std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost(x) > cost(y); });
-    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    std::vector<Slot> heap_store;
+    heap_store.reserve(n_ctas);
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap(std::greater<Slot>(), std::move(heap_store));
     for (int cta = 0; cta < n_ctas; ++cta) heap.push({0, cta});
     for (int i : order) {
       auto [load, cta] = heap.top();
       heap.pop();
-      per_cta[cta].push_back(i);
       plan->item_cta[i] = cta;
-      keys_of[cta] += items[i].e - items[i].a;
       heap.push({load + cost(i), cta});
     }
   }
-
-  // 4b. inside every CTA, the same assignment over its workers (pipelines)
-  std::vector<std::vector<int>> per_worker(static_cast<size_t>(n_ctas) * wpc);
-  for (int cta = 0; cta < n_ctas; ++cta) {
-    std::vector<int> mine = per_cta[cta];
-    std::stable_sort(mine.begin(), mine.end(), [&](int x, int y) { return cost(x) > cost(y); });
-    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> wheap;
-    for (int w = 0; w < wpc; ++w) wheap.push({0, w});
-    for (int i : mine) {
-      auto [load, w] = wheap.top();
-      wheap.pop();
-      per_worker[static_cast<size_t>(cta) * wpc + w].push_back(i);
-      wheap.push({load + cost(i), w});
-    }
+  for (int i = 0; i < n_items; ++i) {
+    ++cta_start[plan->item_cta[i] + 1];
+    keys_of[plan->item_cta[i]] += items[i].e - items[i].a;
   }
-  const int n_workers = n_ctas * wpc;
+  for (int c = 0; c < n_ctas; ++c) cta_start[c + 1] += cta_start[c];
+  {
+    std::vector<int> fill(cta_start.begin(), cta_start.end() - 1);
+    for (int i : order) cta_order[fill[plan->item_cta[i]]++] = i;
+  }
 
   // 5. blob and workspace
   BlobHeader hdr{};
@@ -352,7 +345,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   hdr.off_items = off;
   off = align_up(off + sizeof(WorkItem) * n_items, 16);
   hdr.off_cta_indptr = off;
-  off = align_up(off + sizeof(int32_t) * (n_workers + 1), 16);
+  off = align_up(off + sizeof(int32_t) * (n_ctas + 1), 16);
   hdr.off_cta_items = off;
   off = align_up(off + sizeof(int32_t) * n_items, 16);
   hdr.off_merge = off;
@@ -374,9 +367,10 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   auto* cta_items = reinterpret_cast<int32_t*>(base + hdr.off_cta_items);
   auto* cta_recs = reinterpret_cast<ItemRec*>(base + hdr.off_cta_recs);
   int pos = 0;
-  for (int wk = 0; wk < n_workers; ++wk) {
-    cta_indptr[wk] = pos;
-    for (int i : per_worker[wk]) {
+  for (int cta = 0; cta < n_ctas; ++cta) {
+    cta_indptr[cta] = pos;
+    for (int k = cta_start[cta]; k < cta_start[cta + 1]; ++k) {
+      const int i = cta_order[k];
       ItemRec r{};
       r.it = items[i];
       r.lo = r.hi = -1;      // resolved by the kernel when the host page list is unknown
@@ -388,7 +382,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
       cta_items[pos++] = i;
     }
   }
-  cta_indptr[n_workers] = pos;
+  cta_indptr[n_ctas] = pos;
   if (!merges.empty()) std::memcpy(base + hdr.off_merge, merges.data(), sizeof(MergeGroup) * merges.size());
 
   dattn_plan_info& info = plan->info;
