@@ -88,6 +88,7 @@ struct Walk {
   const PartialParams& p;
   const ItemRec* cache;
   int begin, end;
+  uint64_t keep;      // L2 evict-last policy for the page-table reads
   __device__ __forceinline__ ItemRec rec(int ii) const {
     return ii - begin < kItemCache ? cache[ii - begin] : load_rec(p, ii, false);
   }
@@ -122,9 +123,42 @@ __device__ __forceinline__ uint32_t tile_off(int s, int c) {
 
 // ---- PTX wrappers -----------------------------------------------------------------------
 
+// L2 eviction policies: K/V rows are streamed once (evict first); the page
+// table and the plan's records are read by every launch and stay resident
+// (evict last) while the K/V stream passes through L2.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ int ld_keep(const int* p, uint64_t pol) {
+  int v;
+  asm volatile("ld.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+  return v;
+}
+
+__device__ __forceinline__ ItemRec ld_rec_keep(const ItemRec* p, uint64_t pol) {
+  ItemRec r;
+  int4* d = reinterpret_cast<int4*>(&r);
+  const int4* s = reinterpret_cast<const int4*>(p);
+#pragma unroll
+  for (int i = 0; i < 3; ++i)
+    asm volatile("ld.global.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(d[i].x), "=r"(d[i].y), "=r"(d[i].z), "=r"(d[i].w)
+                 : "l"(s + i), "l"(pol));
+  return r;
+}
+
 // 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(pol)
                : "memory");
 }
 
@@ -233,7 +267,7 @@ __device__ __forceinline__ SlotPages slot_pages(const Walk& w, const PCur& c, co
     const int t = k.t[h];
     if (t >= 0 && t < r.it.T) {
       const int blk = blk_of(w.p, t);
-      if (blk < r.hi - r.lo) g.pi[h] = w.p.page_indices[r.lo + blk];
+      if (blk < r.hi - r.lo) g.pi[h] = ld_keep(w.p.page_indices + r.lo + blk, w.keep);
     }
   }
   return g;
@@ -288,6 +322,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
   const char* kbase = static_cast<const char*>(p.k);
   const char* vbase = static_cast<const char*>(p.v);
   const int sub = lane / C::kChunks, ch = lane % C::kChunks;
+  const uint64_t stream_pol = policy_evict_first();
 
   // this warp's stages: pw, pw + 4, pw + 8, ... of the CTA's stage sequence
   PCur c0{w.begin, 0, 0};
@@ -323,8 +358,8 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
       const bool ok = row != kNoRow;
       const size_t off = static_cast<size_t>(ok ? row : 0u) * C::kRowB + ch * 16;
       const uint32_t dst = tile_off<D>(s, ch);
-      cp_async16(kt + dst, kbase + off, ok ? 16u : 0u);
-      cp_async16(vt + dst, vbase + off, ok ? 16u : 0u);
+      cp_async16(kt + dst, kbase + off, ok ? 16u : 0u, stream_pol);
+      cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
     }
     const uint32_t fb = full0 + 8 * st;
     cp_async_mbar_arrive(fb);
@@ -551,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   // The plan's records may be read while the preceding kernel of the stream
   // still runs (programmatic launch); device inputs only after the wait.
   for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
-    cache[i] = p.cta_recs[it_begin + i];
+    cache[i] = ld_rec_keep(p.cta_recs + it_begin + i, policy_evict_last());
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
     if (!rec_complete_as_planned(p, cache[i])) cache[i] = complete_rec(p, cache[i], true);
@@ -565,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
     fence_barrier_init();
   }
   __syncthreads();
-  const Walk w{p, cache, it_begin, it_end};
+  const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBfProducerRegs));
