@@ -15,18 +15,15 @@
 // folds combine in shared memory.  The kernel is launched as a programmatic
 // dependent of the partial kernel: it is resident before the partial kernel
 // ends and waits (griddepcontrol.wait) for its states to be complete.
-#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include "internal.h"
+#include "merge.cuh"
 
 namespace dattn {
 
 namespace {
 
-constexpr unsigned kAll = 0xffffffffu;
 constexpr int kMergeWarps = 4;
-constexpr int kBatch = 16;     // u loads in flight per lane
 
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_constant__ MergeParams p) {
@@ -39,90 +36,37 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = blockIdx.x / p.rows, row = blockIdx.x % p.rows;
   const MergeGroup grp = p.groups[gi];
-  const long long stride = static_cast<long long>(kMergeWarps) * p.rows * D;   // between a warp's states
 
-  float M = -INFINITY, Lsum = 0.f, U[C];
-#pragma unroll
-  for (int c = 0; c < C; ++c) U[c] = 0.f;
-  // this warp's states: w + kMergeWarps * i, i = 0, 1, ...; 32 at a time
+  // warp w folds states w, w + kMergeWarps, ...
+  RowFold<D> f;
+  fold_init(f);
   const int n_mine = grp.n > w ? (grp.n - w + kMergeWarps - 1) / kMergeWarps : 0;
-  for (int i0 = 0; i0 < n_mine; i0 += 32) {
-    const int n = min(32, n_mine - i0);
-    const int s_first = grp.slot0 + w + kMergeWarps * i0;
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (lane < n) ml = __ldcg(p.ml + static_cast<long long>(s_first + kMergeWarps * lane) * p.rows + row);
-    const bool valid = ml.y > 0.f;                         // empty state: identity
-    float mc = valid ? ml.x : -INFINITY;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kAll, mc, o));
-    if (mc == -INFINITY) continue;
-    const float m_new = fmaxf(M, mc);
-    const float scale_old = M == -INFINITY ? 0.f : exp2f(M - m_new);
-    const float wt = valid ? exp2f(ml.x - m_new) : 0.f;
-    float lw = wt * ml.y;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(kAll, lw, o);
-    Lsum = Lsum * scale_old + lw;
-#pragma unroll
-    for (int c = 0; c < C; ++c) U[c] *= scale_old;
-    M = m_new;
-    const unsigned live = __ballot_sync(kAll, valid);
-    const float* u0 = p.u + (static_cast<long long>(s_first) * p.rows + row) * D + lane * C;
-    for (int q0 = 0; q0 < n; q0 += kBatch) {
-      float v[kBatch][C];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const bool use = q0 + q < n && ((live >> (q0 + q)) & 1u);
-        const float* src = u0 + (q0 + q) * stride;
-        if constexpr (C == 4) {
-          const float4 x = use ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[q][0] = x.x; v[q][1] = x.y; v[q][2] = x.z; v[q][3] = x.w;
-        } else {
-          const float2 x = use ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
-          v[q][0] = x.x; v[q][1] = x.y;
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const float wq = __shfl_sync(kAll, wt, (q0 + q) & 31);
-#pragma unroll
-        for (int c = 0; c < C; ++c) U[c] = fmaf(wq, v[q][c], U[c]);
-      }
-    }
-  }
+  fold_states<D>(p.ml, p.u, p.rows, row, grp.slot0 + w, n_mine, kMergeWarps, lane, f);
   // combine the warps' folds
 #pragma unroll
-  for (int c = 0; c < C; ++c) sm_u[w][lane * C + c] = U[c];
+  for (int c = 0; c < C; ++c) sm_u[w][lane * C + c] = f.U[c];
   if (lane == 0) {
-    sm_ml[w][0] = M;
-    sm_ml[w][1] = Lsum;
+    sm_ml[w][0] = f.M;
+    sm_ml[w][1] = f.L;
   }
   __syncthreads();
   if (w != 0) return;
-  float Mt = -INFINITY;
+  RowFold<D> t;
+  fold_init(t);
 #pragma unroll
-  for (int k = 0; k < kMergeWarps; ++k) Mt = fmaxf(Mt, sm_ml[k][1] > 0.f ? sm_ml[k][0] : -INFINITY);
-  float Lt = 0.f, Ut[C];
-#pragma unroll
-  for (int c = 0; c < C; ++c) Ut[c] = 0.f;
-  if (Mt != -INFINITY) {
+  for (int k = 0; k < kMergeWarps; ++k) t.M = fmaxf(t.M, sm_ml[k][1] > 0.f ? sm_ml[k][0] : -INFINITY);
+  if (t.M != -INFINITY) {
 #pragma unroll
     for (int k = 0; k < kMergeWarps; ++k) {
       if (!(sm_ml[k][1] > 0.f)) continue;
-      const float a = exp2f(sm_ml[k][0] - Mt);
-      Lt += a * sm_ml[k][1];
+      const float a = exp2f(sm_ml[k][0] - t.M);
+      t.L += a * sm_ml[k][1];
 #pragma unroll
-      for (int c = 0; c < C; ++c) Ut[c] = fmaf(a, sm_u[k][lane * C + c], Ut[c]);
+      for (int c = 0; c < C; ++c) t.U[c] = fmaf(a, sm_u[k][lane * C + c], t.U[c]);
     }
   }
   const int i = row / p.g, hq = grp.h * p.g + row % p.g;
-  const long long orow = (static_cast<long long>(grp.b) * p.S_q + i) * p.H_q + hq;
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o) + orow * D + lane * C;
-  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
-#pragma unroll
-  for (int c = 0; c < C; c += 2)
-    *reinterpret_cast<__nv_bfloat162*>(o + c) = __floats2bfloat162_rn(Ut[c] * inv, Ut[c + 1] * inv);
-  if (lane == 0 && p.lse) p.lse[orow] = Lt > 0.f ? (Mt + __log2f(Lt)) * 0.69314718055994531f : -INFINITY;
+  write_folded_row<D>(p.o, p.lse, (static_cast<long long>(grp.b) * p.S_q + i) * p.H_q + hq, t, lane);
 }
 
 template <int D>
