@@ -38,7 +38,7 @@ enum StatusBits : int32_t {
 // in the byte-format kernel); every warp leaves the state of its block's rows
 // over its own share of the item's keys.
 inline int states_per_item(int rows, int fmt) {
-  if (fmt == DATTN_FMT_BF16) return kConsumerWarps / (rows <= 16 ? 1 : 2);
+  if (fmt != DATTN_FMT_INT4_KIVI) return kConsumerWarps / (rows <= 16 ? 1 : 2);
   return kConsumerWarps / (rows <= 4 ? 1 : rows <= 8 ? 2 : rows <= 16 ? 4 : 8);
 }
 
@@ -115,6 +115,7 @@ struct MergeParams {
 // Kernel launchers (partial.cu, merge.cu); return cudaError_t as int.
 int launch_partial(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_partial_bf16(const PartialParams& p, int d, int n_ctas, void* stream);
+int launch_partial_q8(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_merge(const MergeParams& p, int d, void* stream);
 
 }  // namespace dattn

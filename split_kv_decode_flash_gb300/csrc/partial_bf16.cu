@@ -32,67 +32,17 @@
 // O / LSE when it is the group's only state.
 #include <cuda_runtime.h>
 
-#include "stream.cuh"
+#include "tc_common.cuh"
 
 namespace dattn {
 
 namespace {
 
-constexpr unsigned kAll = 0xffffffffu;
-constexpr int kItemCache = 256;       // work items of a CTA kept in shared memory
 // setmaxnreg split of the launch's 384 x 168 registers: the producer
 // warpgroup's description pipeline needs more than the byte-format kernel's.
 constexpr int kBfProducerRegs = 96;
 constexpr int kBfConsumerRegs = 200;
 static_assert(128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs <= kThreads * 168, "register split");
-constexpr uint32_t kNoRow = 0xFFFFFFFFu;
-
-// Completes item record r with what only the device knows: the page-list
-// bounds when the plan was made without the host page list, the cache row
-// (contiguous layout), and the index-list consistency check (keys dropped,
-// e = a, when the list offsets disagree with the plan).  Reads device inputs,
-// so only after griddepcontrol.wait.
-__device__ __forceinline__ ItemRec complete_rec(const PartialParams& p, ItemRec r, bool report) {
-  if (p.mask == DATTN_MASK_INDEX_LIST) {
-    const int g = r.it.b * p.H_kv + r.it.h;
-    const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
-    if (lo != r.it.x0 || r.it.e > n) {
-      if (report) atomicOr(p.status, kStListRange);
-      r.it.e = r.it.a;
-    }
-  }
-  if (p.layout == DATTN_KV_PAGED_HND) {
-    if (r.lo < 0) {
-      r.lo = p.page_indptr[r.it.b];
-      r.hi = p.page_indptr[r.it.b + 1];
-    }
-  } else {
-    r.crow = cache_row(p.cache_batch_idx, r.it.b, p.B_cache, report ? p.status : nullptr);
-  }
-  return r;
-}
-
-// True when complete_rec changes nothing for this problem (paged layout with
-// the page-list bounds in the plan, interval masks).
-__device__ __forceinline__ bool rec_complete_as_planned(const PartialParams& p, const ItemRec& r) {
-  return p.mask != DATTN_MASK_INDEX_LIST && p.layout == DATTN_KV_PAGED_HND && r.lo >= 0;
-}
-
-__device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int ii, bool report) {
-  return complete_rec(p, p.cta_recs[ii], report);
-}
-
-// The CTA's item list: the first kItemCache records come from shared memory
-// (filled once at kernel start), later ones from global memory.
-struct Walk {
-  const PartialParams& p;
-  const ItemRec* cache;
-  int begin, end;
-  uint64_t keep;      // L2 evict-last policy for the page-table reads
-  __device__ __forceinline__ ItemRec rec(int ii) const {
-    return ii - begin < kItemCache ? cache[ii - begin] : load_rec(p, ii, false);
-  }
-};
 
 template <int D>
 struct Bf {
@@ -115,201 +65,6 @@ struct Bf {
   static_assert(kTotal <= 232448, "shared memory of one CTA");
 };
 
-// Byte offset of 16-byte chunk c of key slot s inside a stage tile.
-template <int D>
-__device__ __forceinline__ uint32_t tile_off(int s, int c) {
-  return static_cast<uint32_t>(s * (D * 2) + ((c ^ (s & 7)) << 4));
-}
-
-// ---- PTX wrappers -----------------------------------------------------------------------
-
-// L2 eviction policies: K/V rows are streamed once (evict first); the page
-// table and the plan's records are read by every launch and stay resident
-// (evict last) while the K/V stream passes through L2.
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-__device__ __forceinline__ int ld_keep(const int* p, uint64_t pol) {
-  int v;
-  asm volatile("ld.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
-  return v;
-}
-
-__device__ __forceinline__ ItemRec ld_rec_keep(const ItemRec* p, uint64_t pol) {
-  ItemRec r;
-  int4* d = reinterpret_cast<int4*>(&r);
-  const int4* s = reinterpret_cast<const int4*>(p);
-#pragma unroll
-  for (int i = 0; i < 3; ++i)
-    asm volatile("ld.global.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(d[i].x), "=r"(d[i].y), "=r"(d[i].z), "=r"(d[i].w)
-                 : "l"(s + i), "l"(pol));
-  return r;
-}
-
-// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t pol) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
-               "r"(src_bytes), "l"(pol)
-               : "memory");
-}
-
-// Arrive on "bar" once every earlier cp.async of this thread has landed (the
-// pending count is raised first, so the barrier's expected count is unchanged).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                              uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-
-// c += a (16x16, row-major bf16) * b (16x8, column-major bf16), fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// ---- producer ---------------------------------------------------------------------------
-
-// A producer warp's position: stream keys [j0, j1) of item ii (ii == end: none).
-struct PCur {
-  int ii, j0, j1;
-};
-
-__device__ __forceinline__ void pc_seek(const Walk& w, PCur& c) {
-  for (; c.ii < w.end; ++c.ii) {
-    const WorkItem it = w.rec(c.ii).it;
-    if (it.e > it.a) {
-      c.j0 = it.a;
-      c.j1 = min(it.a + kTK, it.e);
-      return;
-    }
-  }
-}
-
-__device__ __forceinline__ void pc_advance(const Walk& w, PCur& c, int n) {
-  for (int i = 0; i < n && c.ii < w.end; ++i) {
-    const int e = w.rec(c.ii).it.e;
-    if (c.j1 < e) {
-      c.j0 = c.j1;
-      c.j1 = min(c.j0 + kTK, e);
-    } else {
-      ++c.ii;
-      pc_seek(w, c);
-    }
-  }
-}
-
-// The description of a stage is built in three steps, each issued one stage
-// of this warp ahead of the next, so no load result is awaited right after
-// it was issued: logical keys (index-list entries are loads), page ids of the
-// keys' blocks (page-list loads, M4.5 §0x04D), and finally the checked K/V
-// row of every slot.
-struct SlotKeys {
-  int t[2];      // logical key of slots lane and lane + 32 (-1: none)
-};
-struct SlotPages {
-  int pi[2];     // page id of the key's block (-2: block outside the page list)
-};
-struct SlotRows {
-  int t[2];           // logical key, -1 when the slot is empty or invalid
-  uint32_t row[2];    // K/V row in the cache in rows of d elements (kNoRow: none)
-  bool full;          // FULL stage class
-};
-
-__device__ __forceinline__ SlotKeys slot_keys(const Walk& w, const PCur& c, int lane) {
-  SlotKeys k;
-  k.t[0] = k.t[1] = -1;
-  if (c.ii >= w.end) return k;
-  const WorkItem it = w.rec(c.ii).it;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int j = c.j0 + lane + 32 * h;
-    if (j < c.j1) k.t[h] = stream_key(it, w.p.mask, w.p.index_list, j);
-  }
-  return k;
-}
-
-__device__ __forceinline__ SlotPages slot_pages(const Walk& w, const PCur& c, const SlotKeys& k) {
-  SlotPages g;
-  g.pi[0] = g.pi[1] = -2;
-  if (c.ii >= w.end || w.p.layout != DATTN_KV_PAGED_HND) return g;
-  const ItemRec r = w.rec(c.ii);
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int t = k.t[h];
-    if (t >= 0 && t < r.it.T) {
-      const int blk = blk_of(w.p, t);
-      if (blk < r.hi - r.lo) g.pi[h] = ld_keep(w.p.page_indices + r.lo + blk, w.keep);
-    }
-  }
-  return g;
-}
-
-__device__ __forceinline__ SlotRows slot_rows(const Walk& w, const PCur& c, const SlotKeys& k, const SlotPages& g,
-                                              int lane) {
-  const PartialParams& p = w.p;
-  SlotRows d;
-  d.t[0] = d.t[1] = -1;
-  d.row[0] = d.row[1] = kNoRow;
-  d.full = false;
-  if (c.ii >= w.end) return d;
-  const ItemRec r = w.rec(c.ii);
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    int t = k.t[h];
-    uint32_t row = kNoRow;
-    if (p.mask == DATTN_MASK_INDEX_LIST && c.j0 + lane + 32 * h < c.j1 &&
-        (t < 0 || t >= r.it.T)) {
-      atomicOr(p.status, kStListRange);
-      t = -1;
-    }
-    if (t >= 0) {
-      if (p.layout == DATTN_KV_PAGED_HND) {
-        const int pi = g.pi[h];
-        if (pi == -2) atomicOr(p.status, kStBlockRange);
-        else if (pi < 0 || pi >= p.num_pages) atomicOr(p.status, kStPageRange);
-        else row = (static_cast<uint32_t>(pi) * p.H_kv + r.it.h) * p.P + row_of(p, t);
-      } else if (r.crow >= 0 && t < p.T_cap) {
-        row = (static_cast<uint32_t>(r.crow) * p.T_cap + t) * p.H_kv + r.it.h;
-      } else {
-        atomicOr(p.status, kStRowRange);
-      }
-      if (row == kNoRow) t = -1;
-    }
-    d.t[h] = t;
-    d.row[h] = row;
-  }
-  d.full = stage_is_full(p, r.it, c.j0, c.j1, d.t[0], d.t[1]);
-  return d;
-}
 
 template <int D>
 __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
@@ -326,18 +81,18 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
 
   // this warp's stages: pw, pw + 4, pw + 8, ... of the CTA's stage sequence
   PCur c0{w.begin, 0, 0};
-  pc_seek(w, c0);
-  pc_advance(w, c0, pw);
+  pc_seek<kTK>(w, c0);
+  pc_advance<kTK>(w, c0, pw);
   PCur c1 = c0;
-  pc_advance(w, c1, kProducerWarps);
+  pc_advance<kTK>(w, c1, kProducerWarps);
   PCur c2 = c1;
-  pc_advance(w, c2, kProducerWarps);
-  const SlotKeys k0 = slot_keys(w, c0, lane);
-  SlotKeys k1 = slot_keys(w, c1, lane);
-  const SlotPages g0 = slot_pages(w, c0, k0);     // both stages' page lookups in flight together
-  SlotPages g1 = slot_pages(w, c1, k1);
-  SlotKeys k2 = slot_keys(w, c2, lane);
-  SlotRows r0 = slot_rows(w, c0, k0, g0, lane);
+  pc_advance<kTK>(w, c2, kProducerWarps);
+  const SlotKeys<2> k0 = slot_keys<2>(w, c0, lane);
+  SlotKeys<2> k1 = slot_keys<2>(w, c1, lane);
+  const SlotPages<2> g0 = slot_pages<2>(w, c0, k0);     // both stages' page lookups in flight together
+  SlotPages<2> g1 = slot_pages<2>(w, c1, k1);
+  SlotKeys<2> k2 = slot_keys<2>(w, c2, lane);
+  SlotRows<2> r0 = slot_rows<2>(w, c0, k0, g0, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
@@ -357,7 +112,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
       const uint32_t row = __shfl_sync(kAll, s0 < 32 ? r0.row[0] : r0.row[1], s & 31);
       const bool ok = row != kNoRow;
       const size_t off = static_cast<size_t>(ok ? row : 0u) * C::kRowB + ch * 16;
-      const uint32_t dst = tile_off<D>(s, ch);
+      const uint32_t dst = tile_off<2 * D>(s, ch);
       cp_async16(kt + dst, kbase + off, ok ? 16u : 0u, stream_pol);
       cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
     }
@@ -367,13 +122,13 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
     if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
 
     // move the description pipeline one stage of this warp forward
-    r0 = slot_rows(w, c1, k1, g1, lane);
+    r0 = slot_rows<2>(w, c1, k1, g1, lane);
     c0 = c1;
-    g1 = slot_pages(w, c2, k2);
+    g1 = slot_pages<2>(w, c2, k2);
     k1 = k2;
     c1 = c2;
-    pc_advance(w, c2, kProducerWarps);
-    k2 = slot_keys(w, c2, lane);
+    pc_advance<kTK>(w, c2, kProducerWarps);
+    k2 = slot_keys<2>(w, c2, lane);
   }
   asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
 }
@@ -499,7 +254,7 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane) {
 #pragma unroll
         for (int m = 0; m < KS / 2; ++m) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kt + tile_off<D>(base + nt * 8 + lrow, 4 * m + lmat), b0, b1, b2, b3);
+          ldsm_x4(kt + tile_off<2 * D>(base + nt * 8 + lrow, 4 * m + lmat), b0, b1, b2, b3);
           mma_bf16(s[nt], qa[2 * m], b0, b1);
           mma_bf16(s[nt], qa[2 * m + 1], b2, b3);
         }
@@ -554,7 +309,7 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane) {
 #pragma unroll
       for (int n2 = 0; n2 < NT / 2; ++n2) {
         uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(vt + tile_off<D>(base + (lmat & 1) * 8 + lrow, 2 * n2 + (lmat >> 1)), v0, v1, v2, v3);
+        ldsm_x4_trans(vt + tile_off<2 * D>(base + (lmat & 1) * 8 + lrow, 2 * n2 + (lmat >> 1)), v0, v1, v2, v3);
         mma_bf16(o[2 * n2], pa, v0, v1);
         mma_bf16(o[2 * n2 + 1], pa, v2, v3);
       }

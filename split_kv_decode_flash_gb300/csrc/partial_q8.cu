@@ -1,0 +1,494 @@
+// Partial kernel of split-KV decode attention for INT8 per-token K/V
+// ("M8.6 Live-Data Quantization", §0x05B format), on the tensor cores.
+//
+// Same persistent producer / consumer structure as the bf16 kernel (item
+// records in shared memory, four producer warps with a three-step slot
+// description, per-warp partial states); stages hold 128 keys so that a
+// stage carries as many bytes as a bf16 one.
+//
+// Producer.  Every key row's codes are copied with 16-byte cp.async into
+// XOR-swizzled tiles, and its (s, z) fp16 pairs with 4-byte copies; empty
+// slots are zero-filled.
+//
+// Consumers (two stage groups of four warps, 32 keys per warp and stage,
+// in blocks of 16).  Scales stay where M8.6 §0x03 puts them:
+//   K: q.k_hat = s_t (q . code_t) + z_t (q . 1).  K codes are read with
+//      ldmatrix (byte pairs as 16-bit elements) and turned into f16 by one
+//      prmt per pair (1024 + code, exact); q . (1024 + code) comes from
+//      mma.sync.m16n8k16 f16 with the query rows converted to f16 (exact for
+//      bf16 values in f16's range; rows whose largest |q| is beyond 2^14 are
+//      scaled by a power of two first), fp32 accumulate, and the 1024 bias is
+//      folded into the offset: s = s_t S' + (z_t - 1024 s_t) (q . 1).
+//   V: sum_t p_t (s_t code_t + z_t) = sum_t (p_t s_t) code_t + sum_t p_t z_t.
+//      P' = p s_t is the f16 A operand of the P V mma; V codes come from
+//      ldmatrix.trans, so a lane holds the codes of two keys at two channels
+//      and one prmt makes each B register.  The bias adds 1024 sum_t P'_t to
+//      every channel, removed at the end together with adding
+//      sum_t p_t z_t.  Output tile 2 C + e holds channels 16 C + 2 n + e.
+// The online softmax is the same as in the bf16 kernel (log2 units, -inf
+// for masked cells, row maxima over the lane quad).
+#include <cuda_runtime.h>
+
+#include "tc_common.cuh"
+
+namespace dattn {
+
+namespace {
+
+constexpr int kQK = 128;              // keys per stage
+constexpr int kQS = kQK / 32;         // slots per producer lane
+constexpr int kQ8ProducerRegs = 88;
+constexpr int kQ8ConsumerRegs = 208;
+static_assert(128 * kQ8ProducerRegs + 32 * kConsumerWarps * kQ8ConsumerRegs <= kThreads * 168, "register split");
+
+template <int D>
+struct Q8 {
+  // Even depth: with two consumer stage groups taking alternate stages, every
+  // ring slot always belongs to the same group (no mbarrier parity alias).
+  static constexpr int kStagesN = D == 128 ? 6 : 10;
+  static_assert(kStagesN % 2 == 0, "ring depth must be even");
+  static constexpr int kRowB = D;                  // code bytes of one key row
+  static constexpr int kChunks = kRowB / 16;
+  static constexpr int kTile = kQK * kRowB;        // one tensor's codes
+  static constexpr int kQp = kQK * 4;              // one tensor's (s, z) pairs
+  static constexpr int kStage = 2 * kTile + 2 * kQp;
+  static constexpr int kPos = kStagesN * kStage;   // int32 [stages][kQK]
+  static constexpr int kFlags = kPos + kStagesN * kQK * 4;
+  static constexpr int kSeq = kFlags + kStagesN * 4;
+  static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
+  static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
+  static constexpr int kAbort = kEmptyBar + kStagesN * 8;
+  static constexpr int kItems = align16(kAbort + 16);
+  static constexpr int kTotal = kItems + kItemCache * static_cast<int>(sizeof(ItemRec));
+  static_assert(kTotal <= 232448, "shared memory of one CTA");
+};
+
+// Two bytes of w as an f16 pair (1024 + byte each): sel picks them, e.g.
+// 0x4140 bytes 0 and 1, 0x4342 bytes 2 and 3, 0x4240 bytes 0 and 2.
+__device__ __forceinline__ uint32_t biased_f16x2(uint32_t w, uint32_t sel) {
+  return __byte_perm(w, 0x64646464u, sel);
+}
+
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// ---- producer ---------------------------------------------------------------------------
+
+template <int D>
+__device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw) {
+  using C = Q8<D>;
+  const PartialParams& p = w.p;
+  constexpr int kSlotsPerPass = 32 / C::kChunks;   // key rows per warp instruction
+  const uint32_t full0 = smem_u32(smem + C::kFullBar);
+  const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
+  const char* kbase = static_cast<const char*>(p.k);
+  const char* vbase = static_cast<const char*>(p.v);
+  const char* kqbase = static_cast<const char*>(p.kqp);
+  const char* vqbase = static_cast<const char*>(p.vqp);
+  const int sub = lane / C::kChunks, ch = lane % C::kChunks;
+  const uint64_t stream_pol = policy_evict_first();
+
+  PCur c0{w.begin, 0, 0};
+  pc_seek<kQK>(w, c0);
+  pc_advance<kQK>(w, c0, pw);
+  PCur c1 = c0;
+  pc_advance<kQK>(w, c1, kProducerWarps);
+  PCur c2 = c1;
+  pc_advance<kQK>(w, c2, kProducerWarps);
+  const SlotKeys<kQS> k0 = slot_keys<kQS>(w, c0, lane);
+  SlotKeys<kQS> k1 = slot_keys<kQS>(w, c1, lane);
+  const SlotPages<kQS> g0 = slot_pages<kQS>(w, c0, k0);
+  SlotPages<kQS> g1 = slot_pages<kQS>(w, c1, k1);
+  SlotKeys<kQS> k2 = slot_keys<kQS>(w, c2, lane);
+  SlotRows<kQS> r0 = slot_rows<kQS>(w, c0, k0, g0, lane);
+
+  for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
+    const int st = k % C::kStagesN;
+    const uint32_t use = k / C::kStagesN;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kQK;
+#pragma unroll
+    for (int h = 0; h < kQS; ++h) pos[lane + 32 * h] = r0.t[h];
+    if (lane == 0) {
+      reinterpret_cast<int*>(smem + C::kFlags)[st] = r0.full ? kFlagFull : 0;
+      reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
+    }
+    const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
+    const uint32_t kq = vt + C::kTile, vq = kq + C::kQp;
+#pragma unroll
+    for (int s0 = 0; s0 < kQK; s0 += kSlotsPerPass) {
+      const int s = s0 + sub;
+      const uint32_t row = __shfl_sync(kAll, r0.row[s0 / 32], s & 31);
+      const bool ok = row != kNoRow;
+      const size_t off = static_cast<size_t>(ok ? row : 0u) * C::kRowB + ch * 16;
+      const uint32_t dst = tile_off<D>(s, ch);
+      cp_async16(kt + dst, kbase + off, ok ? 16u : 0u, stream_pol);
+      cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
+    }
+#pragma unroll
+    for (int h = 0; h < kQS; ++h) {
+      const uint32_t row = r0.row[h];
+      const bool ok = row != kNoRow;
+      const size_t off = static_cast<size_t>(ok ? row : 0u) * 4;
+      cp_async4(kq + 4 * (lane + 32 * h), kqbase + off, ok ? 4u : 0u);
+      cp_async4(vq + 4 * (lane + 32 * h), vqbase + off, ok ? 4u : 0u);
+    }
+    const uint32_t fb = full0 + 8 * st;
+    cp_async_mbar_arrive(fb);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
+
+    r0 = slot_rows<kQS>(w, c1, k1, g1, lane);
+    c0 = c1;
+    g1 = slot_pages<kQS>(w, c2, k2);
+    k1 = k2;
+    c1 = c2;
+    pc_advance<kQK>(w, c2, kProducerWarps);
+    k2 = slot_keys<kQS>(w, c2, lane);
+  }
+  asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
+}
+
+// ---- consumers --------------------------------------------------------------------------
+
+// Query rows r0, r1 of item "it" as f16 A fragments in the channel order the
+// K fragments use (k-step kk, lane quad t4: channels 16 kk + 4 t4 + 0..3),
+// their channel sums, and the power-of-two factor each row was divided by to
+// fit f16 (1 unless its largest |q| exceeds 2^14).
+template <int D>
+struct QRows {
+  uint32_t a[D / 16][4];
+  float qsum0, qsum1, fac0, fac1;
+};
+
+template <int D>
+__device__ __forceinline__ void load_q8(const PartialParams& p, const WorkItem& it, int r0, int r1, int t4,
+                                        QRows<D>& q) {
+  constexpr int KS = D / 16;
+  const bool ok0 = r0 < p.rows, ok1 = r1 < p.rows;
+  const __nv_bfloat16* q0 = static_cast<const __nv_bfloat16*>(p.q) +
+                            ((static_cast<long long>(it.b) * p.S_q + r0 / p.g) * p.H_q + it.h * p.g + r0 % p.g) * D;
+  const __nv_bfloat16* q1 = static_cast<const __nv_bfloat16*>(p.q) +
+                            ((static_cast<long long>(it.b) * p.S_q + r1 / p.g) * p.H_q + it.h * p.g + r1 % p.g) * D;
+  float v0[KS][4], v1[KS][4];
+  float mx0 = 0.f, mx1 = 0.f, s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    uint2 w0 = make_uint2(0u, 0u), w1 = make_uint2(0u, 0u);
+    if (ok0) w0 = *reinterpret_cast<const uint2*>(q0 + 16 * kk + 4 * t4);
+    if (ok1) w1 = *reinterpret_cast<const uint2*>(q1 + 16 * kk + 4 * t4);
+    const float2 a = bf16x2_to_float2(w0.x), b = bf16x2_to_float2(w0.y);
+    const float2 c = bf16x2_to_float2(w1.x), d = bf16x2_to_float2(w1.y);
+    v0[kk][0] = a.x; v0[kk][1] = a.y; v0[kk][2] = b.x; v0[kk][3] = b.y;
+    v1[kk][0] = c.x; v1[kk][1] = c.y; v1[kk][2] = d.x; v1[kk][3] = d.y;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mx0 = fmaxf(mx0, fabsf(v0[kk][e]));
+      mx1 = fmaxf(mx1, fabsf(v1[kk][e]));
+      s0 += v0[kk][e];
+      s1 += v1[kk][e];
+    }
+  }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, o));
+    s0 += __shfl_xor_sync(kAll, s0, o);
+    s1 += __shfl_xor_sync(kAll, s1, o);
+  }
+  // power-of-two scale that brings the row below 2^14 (exact in f16)
+  q.fac0 = mx0 > 16384.f ? exp2f(ceilf(log2f(mx0 / 16384.f))) : 1.f;
+  q.fac1 = mx1 > 16384.f ? exp2f(ceilf(log2f(mx1 / 16384.f))) : 1.f;
+  const float i0 = 1.f / q.fac0, i1 = 1.f / q.fac1;
+  q.qsum0 = s0;
+  q.qsum1 = s1;
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    q.a[kk][0] = pack_f16(v0[kk][0] * i0, v0[kk][1] * i0);
+    q.a[kk][1] = pack_f16(v1[kk][0] * i1, v1[kk][1] * i1);
+    q.a[kk][2] = pack_f16(v0[kk][2] * i0, v0[kk][3] * i0);
+    q.a[kk][3] = pack_f16(v1[kk][2] * i1, v1[kk][3] * i1);
+  }
+}
+
+// Writes one accumulator row: O / LSE when the item is its group's only
+// chunk, else the row's partial state.  Output tile 2 C + e holds, in
+// columns 2 t4 and 2 t4 + 1, channels 16 C + 4 t4 + e and 16 C + 4 t4 + 2 + e;
+// "bias" (1024 sum P') is removed and z (sum p z) added on every channel.
+template <int D>
+__device__ __forceinline__ void emit_row_q8(const PartialParams& p, const WorkItem& it, int my_state, int row, float m,
+                                            float l, float z, float bias, const float (&o)[D / 8][4], int half,
+                                            int t4) {
+  const int i = row / p.g, hq = it.h * p.g + row % p.g;
+  const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
+  const float add = z - bias;
+  if (it.slot < 0) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      const float* a0 = o[2 * c], *a1 = o[2 * c + 1];
+      __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + 16 * c + 4 * t4);
+      dst[0] = __floats2bfloat162_rn((a0[2 * half] + add) * inv, (a1[2 * half] + add) * inv);
+      dst[1] = __floats2bfloat162_rn((a0[2 * half + 1] + add) * inv, (a1[2 * half + 1] + add) * inv);
+    }
+    if (t4 == 0 && p.lse) p.lse[orow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+  } else {
+    const long long srow = static_cast<long long>(it.slot + my_state) * p.rows + row;
+    float* u = p.u + srow * D;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      const float* a0 = o[2 * c], *a1 = o[2 * c + 1];
+      *reinterpret_cast<float4*>(u + 16 * c + 4 * t4) =
+          make_float4(a0[2 * half] + add, a1[2 * half] + add, a0[2 * half + 1] + add, a1[2 * half + 1] + add);
+    }
+    if (t4 == 0) p.ml[srow] = make_float2(l > 0.f ? m : -INFINITY, l);
+  }
+}
+
+template <int D>
+__device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
+  using C = Q8<D>;
+  constexpr int KS = D / 16;   // k-steps of q.k
+  constexpr int NT = D / 8;    // 8-channel output tiles
+  const PartialParams& p = w.p;
+  const uint32_t full0 = smem_u32(smem + C::kFullBar);
+  const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
+
+  const int nrb = p.rows <= 16 ? 1 : 2;
+  const int ng = nrb == 1 ? 2 : 1;
+  const int wps = kConsumerWarps / ng;
+  const int sgrp = cw / wps, wi = cw % wps;
+  const int rb = wi % nrb, ts = wi / nrb;
+  const int my_state = (cw - rb) / nrb;
+  const int keys_per_warp = kQK / (wps / nrb);     // 32
+  const int g4 = lane >> 2, t4 = lane & 3;
+  const int r0 = rb * 16 + g4, r1 = r0 + 8;
+  const bool ok0 = r0 < p.rows, ok1 = r1 < p.rows;
+  const int qi0 = r0 / p.g, qi1 = r1 / p.g;
+  const int lrow = lane & 7, lmat = lane >> 3;   // ldmatrix address roles
+  const float sc = p.scale_log2;
+
+  uint32_t k = 0;
+  bool dead = false;
+  QRows<D> qn;
+  if (w.begin < w.end) load_q8<D>(p, w.rec(w.begin).it, r0, r1, t4, qn);
+  for (int ii = w.begin; ii < w.end; ++ii) {
+    const WorkItem it = w.rec(ii).it;
+    const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+    const QRows<D> q = qn;
+    if (ii + 1 < w.end) load_q8<D>(p, w.rec(ii + 1).it, r0, r1, t4, qn);
+    float o[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f, b0 = 0.f, b1 = 0.f;
+
+    for (int j0 = it.a; j0 < it.e; ++k) {
+      const int j1 = min(j0 + kQK, it.e);
+      if (static_cast<int>(k % ng) != sgrp) {
+        j0 = j1;
+        continue;
+      }
+      const int st = k % C::kStagesN;
+      const uint32_t use = k / C::kStagesN;
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+        dead = true;
+        break;
+      }
+      if (reinterpret_cast<const volatile int*>(smem + C::kSeq)[st] != static_cast<int>(k)) {
+        if (lane == 0) atomicOr(p.status, kStPipeline);
+        *abort_flag = 1;
+        dead = true;
+        break;
+      }
+      const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kQK;
+      const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
+      const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
+      const uint32_t* kqp = reinterpret_cast<const uint32_t*>(smem + st * C::kStage + 2 * C::kTile);
+      const uint32_t* vqp = kqp + kQK;
+
+      for (int blk = 0; blk < keys_per_warp / 16; ++blk) {
+        const int base = ts * keys_per_warp + blk * 16;
+        // q . (1024 + code) over 16 keys (two 8-key tiles); one ldmatrix.x4
+        // gives a lane 4 codes of its key for each of 4 k-steps
+        float s[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+          for (int m = 0; m < KS / 4; ++m) {
+            uint32_t r[4];
+            ldsm_x4(kt + tile_off<D>(base + nt * 8 + lrow, 4 * m + lmat), r[0], r[1], r[2], r[3]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              mma_f16(s[nt], q.a[4 * m + i], biased_f16x2(r[i], 0x4140u), biased_f16x2(r[i], 0x4342u));
+          }
+        }
+        // per-token K scale outside the dot, log2 units, -inf where masked
+        float vs[2][2], vz[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int slot = base + nt * 8 + 2 * t4 + e;
+            const int t = pos[slot];
+            const float2 ks = half2_bits_to_float2(kqp[slot]);
+            const float2 vq = half2_bits_to_float2(vqp[slot]);
+            vs[nt][e] = vq.x;
+            vz[nt][e] = vq.y;
+            const float off = fmaf(-1024.f, ks.x, ks.y);
+            const bool v0 = t >= 0 && ok0 && (full || key_visible(mc, qi0, t));
+            const bool v1 = t >= 0 && ok1 && (full || key_visible(mc, qi1, t));
+            s[nt][e] = v0 ? sc * fmaf(ks.x * q.fac0, s[nt][e], off * q.qsum0) : -INFINITY;
+            s[nt][2 + e] = v1 ? sc * fmaf(ks.x * q.fac1, s[nt][2 + e], off * q.qsum1) : -INFINITY;
+          }
+        }
+        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+        float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 2));
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+        const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+        const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+        float pr[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          pr[nt][0] = exp2f(s[nt][0] - u0);
+          pr[nt][1] = exp2f(s[nt][1] - u0);
+          pr[nt][2] = exp2f(s[nt][2] - u1);
+          pr[nt][3] = exp2f(s[nt][3] - u1);
+        }
+        // per-token V scale folded into the probabilities (the f16 A operand)
+        const uint32_t pa[4] = {pack_f16(pr[0][0] * vs[0][0], pr[0][1] * vs[0][1]),
+                                pack_f16(pr[0][2] * vs[0][0], pr[0][3] * vs[0][1]),
+                                pack_f16(pr[1][0] * vs[1][0], pr[1][1] * vs[1][1]),
+                                pack_f16(pr[1][2] * vs[1][0], pr[1][3] * vs[1][1])};
+        // sums of the f16 P' values the mma uses (rows r0: pa 0, 2; r1: pa 1, 3)
+        const float2 q0a = half2_bits_to_float2(pa[0]), q0b = half2_bits_to_float2(pa[2]);
+        const float2 q1a = half2_bits_to_float2(pa[1]), q1b = half2_bits_to_float2(pa[3]);
+        l0 = l0 * a0 + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
+        l1 = l1 * a1 + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+        z0 = z0 * a0 + ((pr[0][0] * vz[0][0] + pr[0][1] * vz[0][1]) + (pr[1][0] * vz[1][0] + pr[1][1] * vz[1][1]));
+        z1 = z1 * a1 + ((pr[0][2] * vz[0][0] + pr[0][3] * vz[0][1]) + (pr[1][2] * vz[1][0] + pr[1][3] * vz[1][1]));
+        b0 = b0 * a0 + ((q0a.x + q0a.y) + (q0b.x + q0b.y));
+        b1 = b1 * a1 + ((q1a.x + q1a.y) + (q1b.x + q1b.y));
+        m0 = n0;
+        m1 = n1;
+        if (__any_sync(kAll, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            o[n][0] *= a0;
+            o[n][1] *= a0;
+            o[n][2] *= a1;
+            o[n][3] *= a1;
+          }
+        }
+        // V codes by ldmatrix.trans: matrices (keys 0-7 | 8-15) x chunks (2 c2, 2 c2 + 1);
+        // a lane gets keys (2 t4, 2 t4 + 1) at channels 16 C + 2 g4 + {0, 1}
+#pragma unroll
+        for (int c2 = 0; c2 < D / 32; ++c2) {
+          uint32_t v[4];
+          ldsm_x4_trans(vt + tile_off<D>(base + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1], v[2], v[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {          // chunk 2 c2 + h: v[2 h] keys 0-7, v[2 h + 1] keys 8-15
+            const int C = 2 * c2 + h;
+            mma_f16(o[2 * C], pa, biased_f16x2(v[2 * h], 0x4240u), biased_f16x2(v[2 * h + 1], 0x4240u));
+            mma_f16(o[2 * C + 1], pa, biased_f16x2(v[2 * h], 0x4341u), biased_f16x2(v[2 * h + 1], 0x4341u));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      j0 = j1;
+    }
+
+    // end of item: row sums and value offsets over the quad; leave the rows
+#pragma unroll
+    for (int x = 1; x <= 2; x <<= 1) {
+      l0 += __shfl_xor_sync(kAll, l0, x);
+      l1 += __shfl_xor_sync(kAll, l1, x);
+      z0 += __shfl_xor_sync(kAll, z0, x);
+      z1 += __shfl_xor_sync(kAll, z1, x);
+      b0 += __shfl_xor_sync(kAll, b0, x);
+      b1 += __shfl_xor_sync(kAll, b1, x);
+    }
+    if (!dead) {
+      if (ok0) emit_row_q8<D>(p, it, my_state, r0, m0, l0, z0, 1024.f * b0, o, 0, t4);
+      if (ok1) emit_row_q8<D>(p, it, my_state, r1, m1, l1, z1, 1024.f * b1, o, 1, t4);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_constant__ PartialParams p) {
+  using C = Q8<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // the merge kernel may be scheduled now; it waits for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
+  ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
+  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
+    cache[i] = ld_rec_keep(p.cta_recs + it_begin + i, policy_evict_last());
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
+    if (!rec_complete_as_planned(p, cache[i])) cache[i] = complete_rec(p, cache[i], true);
+  if (threadIdx.x == 0) {
+    const int warps_per_stage = p.rows <= 16 ? kConsumerWarps / 2 : kConsumerWarps;
+    for (int s = 0; s < C::kStagesN; ++s) {
+      mbar_init(smem_u32(smem + C::kFullBar + 8 * s), 1);
+      mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), warps_per_stage);
+    }
+    *reinterpret_cast<int*>(smem + C::kAbort) = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= kConsumerWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ8ProducerRegs));
+    produce_q8<D>(w, smem, lane, warp - kConsumerWarps);
+    return;
+  }
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ8ConsumerRegs));
+  consume_q8<D>(w, smem, warp, lane);
+}
+
+template <int D>
+int launch_q8(const PartialParams& p, int n_ctas, void* stream) {
+  const size_t smem = Q8<D>::kTotal;
+  cudaFuncAttributes attr;
+  cudaError_t err = cudaFuncGetAttributes(&attr, partial_q8_kernel<D>);
+  if (err != cudaSuccess) return err;
+  // the consumers' setmaxnreg.inc waits for registers the producer warpgroup
+  // releases; it can only complete if the launch holds them
+  if (attr.numRegs * kThreads < 128 * kQ8ProducerRegs + 32 * kConsumerWarps * kQ8ConsumerRegs)
+    return cudaErrorInvalidConfiguration;
+  err = cudaFuncSetAttribute(partial_q8_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr_pdl[1];
+  attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr_pdl;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, partial_q8_kernel<D>, p);
+  return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_partial_q8(const PartialParams& p, int d, int n_ctas, void* stream) {
+  return d == 64 ? launch_q8<64>(p, n_ctas, stream) : launch_q8<128>(p, n_ctas, stream);
+}
+
+}  // namespace dattn

@@ -1,0 +1,302 @@
+// Pieces shared by the tensor-core partial kernels (bf16 and INT8 K/V): the
+// CTA's item records, the producer's stage cursor and three-step slot
+// description (logical key, page id, checked K/V row), L2 cache policies and
+// the PTX wrappers (cp.async, ldmatrix, mma.sync).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "stream.cuh"
+
+namespace dattn {
+
+namespace {
+
+constexpr unsigned kAll = 0xffffffffu;
+constexpr int kItemCache = 256;       // work items of a CTA kept in shared memory
+constexpr uint32_t kNoRow = 0xFFFFFFFFu;
+
+// Completes item record r with what only the device knows: the page-list
+// bounds when the plan was made without the host page list, the cache row
+// (contiguous layout), and the index-list consistency check (keys dropped,
+// e = a, when the list offsets disagree with the plan).  Reads device inputs,
+// so only after griddepcontrol.wait.
+__device__ __forceinline__ ItemRec complete_rec(const PartialParams& p, ItemRec r, bool report) {
+  if (p.mask == DATTN_MASK_INDEX_LIST) {
+    const int g = r.it.b * p.H_kv + r.it.h;
+    const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
+    if (lo != r.it.x0 || r.it.e > n) {
+      if (report) atomicOr(p.status, kStListRange);
+      r.it.e = r.it.a;
+    }
+  }
+  if (p.layout == DATTN_KV_PAGED_HND) {
+    if (r.lo < 0) {
+      r.lo = p.page_indptr[r.it.b];
+      r.hi = p.page_indptr[r.it.b + 1];
+    }
+  } else {
+    r.crow = cache_row(p.cache_batch_idx, r.it.b, p.B_cache, report ? p.status : nullptr);
+  }
+  return r;
+}
+
+// True when complete_rec changes nothing for this problem (paged layout with
+// the page-list bounds in the plan, interval masks).
+__device__ __forceinline__ bool rec_complete_as_planned(const PartialParams& p, const ItemRec& r) {
+  return p.mask != DATTN_MASK_INDEX_LIST && p.layout == DATTN_KV_PAGED_HND && r.lo >= 0;
+}
+
+__device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int ii, bool report) {
+  return complete_rec(p, p.cta_recs[ii], report);
+}
+
+// The CTA's item list: the first kItemCache records come from shared memory
+// (filled once at kernel start), later ones from global memory.
+struct Walk {
+  const PartialParams& p;
+  const ItemRec* cache;
+  int begin, end;
+  uint64_t keep;      // L2 evict-last policy for the page-table reads
+  __device__ __forceinline__ ItemRec rec(int ii) const {
+    return ii - begin < kItemCache ? cache[ii - begin] : load_rec(p, ii, false);
+  }
+};
+
+// ---- PTX wrappers -----------------------------------------------------------------------
+
+// L2 eviction policies: K/V rows are streamed once (evict first); the page
+// table and the plan's records are read by every launch and stay resident
+// (evict last) while the K/V stream passes through L2.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ int ld_keep(const int* p, uint64_t pol) {
+  int v;
+  asm volatile("ld.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+  return v;
+}
+
+__device__ __forceinline__ ItemRec ld_rec_keep(const ItemRec* p, uint64_t pol) {
+  ItemRec r;
+  int4* d = reinterpret_cast<int4*>(&r);
+  const int4* s = reinterpret_cast<const int4*>(p);
+#pragma unroll
+  for (int i = 0; i < 3; ++i)
+    asm volatile("ld.global.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(d[i].x), "=r"(d[i].y), "=r"(d[i].z), "=r"(d[i].w)
+                 : "l"(s + i), "l"(pol));
+  return r;
+}
+
+// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(pol)
+               : "memory");
+}
+
+// Arrive on "bar" once every earlier cp.async of this thread has landed (the
+// pending count is raised first, so the barrier's expected count is unchanged).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+// c += a (16x16, row-major bf16) * b (16x8, column-major bf16), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// c += a (16x16, row-major f16) * b (16x8, column-major f16), fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 4-byte global -> shared copy (cache-all path); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Byte offset of 16-byte chunk c of key slot s inside a stage tile whose rows
+// hold ROWB bytes; chunks are XOR-swizzled by the slot's low bits so the
+// rows read together by a warp fall in distinct bank groups.
+template <int ROWB>
+__device__ __forceinline__ uint32_t tile_off(int s, int c) {
+  constexpr int kMask = ROWB / 16 >= 8 ? 7 : ROWB / 16 - 1;
+  return static_cast<uint32_t>(s * ROWB + ((c ^ (s & kMask)) << 4));
+}
+
+// ---- producer ---------------------------------------------------------------------------
+
+// A producer warp's position: stream keys [j0, j1) of item ii (ii == end:
+// none), in stages of KS keys.
+struct PCur {
+  int ii, j0, j1;
+};
+
+template <int KS>
+__device__ __forceinline__ void pc_seek(const Walk& w, PCur& c) {
+  for (; c.ii < w.end; ++c.ii) {
+    const WorkItem it = w.rec(c.ii).it;
+    if (it.e > it.a) {
+      c.j0 = it.a;
+      c.j1 = min(it.a + KS, it.e);
+      return;
+    }
+  }
+}
+
+template <int KS>
+__device__ __forceinline__ void pc_advance(const Walk& w, PCur& c, int n) {
+  for (int i = 0; i < n && c.ii < w.end; ++i) {
+    const int e = w.rec(c.ii).it.e;
+    if (c.j1 < e) {
+      c.j0 = c.j1;
+      c.j1 = min(c.j0 + KS, e);
+    } else {
+      ++c.ii;
+      pc_seek<KS>(w, c);
+    }
+  }
+}
+
+// The description of a stage of 32 S slots is built in three steps, each
+// issued one stage of the warp ahead of the next, so no load result is
+// awaited right after it was issued: logical keys (index-list entries are
+// loads), page ids of the keys' blocks (page-list loads, M4.5 §0x04D), and
+// finally the checked K/V row of every slot.  Lane l describes slots
+// l, l + 32, ..., l + 32 (S - 1).
+template <int S>
+struct SlotKeys {
+  int t[S];      // logical key (-1: none)
+};
+template <int S>
+struct SlotPages {
+  int pi[S];     // page id of the key's block (-2: block outside the page list)
+};
+template <int S>
+struct SlotRows {
+  int t[S];           // logical key, -1 when the slot is empty or invalid
+  uint32_t row[S];    // K/V row in the cache in rows of d elements (kNoRow: none)
+  bool full;          // FULL stage class
+};
+
+template <int S>
+__device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, int lane) {
+  SlotKeys<S> k;
+#pragma unroll
+  for (int h = 0; h < S; ++h) k.t[h] = -1;
+  if (c.ii >= w.end) return k;
+  const WorkItem it = w.rec(c.ii).it;
+#pragma unroll
+  for (int h = 0; h < S; ++h) {
+    const int j = c.j0 + lane + 32 * h;
+    if (j < c.j1) k.t[h] = stream_key(it, w.p.mask, w.p.index_list, j);
+  }
+  return k;
+}
+
+template <int S>
+__device__ __forceinline__ SlotPages<S> slot_pages(const Walk& w, const PCur& c, const SlotKeys<S>& k) {
+  SlotPages<S> g;
+#pragma unroll
+  for (int h = 0; h < S; ++h) g.pi[h] = -2;
+  if (c.ii >= w.end || w.p.layout != DATTN_KV_PAGED_HND) return g;
+  const ItemRec r = w.rec(c.ii);
+#pragma unroll
+  for (int h = 0; h < S; ++h) {
+    const int t = k.t[h];
+    if (t >= 0 && t < r.it.T) {
+      const int blk = blk_of(w.p, t);
+      if (blk < r.hi - r.lo) g.pi[h] = ld_keep(w.p.page_indices + r.lo + blk, w.keep);
+    }
+  }
+  return g;
+}
+
+template <int S>
+__device__ __forceinline__ SlotRows<S> slot_rows(const Walk& w, const PCur& c, const SlotKeys<S>& k,
+                                                 const SlotPages<S>& g, int lane) {
+  const PartialParams& p = w.p;
+  SlotRows<S> d;
+#pragma unroll
+  for (int h = 0; h < S; ++h) {
+    d.t[h] = -1;
+    d.row[h] = kNoRow;
+  }
+  d.full = false;
+  if (c.ii >= w.end) return d;
+  const ItemRec r = w.rec(c.ii);
+  int tmax = -1;
+#pragma unroll
+  for (int h = 0; h < S; ++h) {
+    int t = k.t[h];
+    uint32_t row = kNoRow;
+    if (p.mask == DATTN_MASK_INDEX_LIST && c.j0 + lane + 32 * h < c.j1 && (t < 0 || t >= r.it.T)) {
+      atomicOr(p.status, kStListRange);
+      t = -1;
+    }
+    if (t >= 0) {
+      if (p.layout == DATTN_KV_PAGED_HND) {
+        const int pi = g.pi[h];
+        if (pi == -2) atomicOr(p.status, kStBlockRange);
+        else if (pi < 0 || pi >= p.num_pages) atomicOr(p.status, kStPageRange);
+        else row = (static_cast<uint32_t>(pi) * p.H_kv + r.it.h) * p.P + row_of(p, t);
+      } else if (r.crow >= 0 && t < p.T_cap) {
+        row = (static_cast<uint32_t>(r.crow) * p.T_cap + t) * p.H_kv + r.it.h;
+      } else {
+        atomicOr(p.status, kStRowRange);
+      }
+      if (row == kNoRow) t = -1;
+    }
+    d.t[h] = t;
+    d.row[h] = row;
+    tmax = max(tmax, t);
+  }
+  d.full = stage_is_full(p, r.it, c.j0, c.j1, tmax, -1);
+  return d;
+}
+
+}  // namespace
+
+}  // namespace dattn
