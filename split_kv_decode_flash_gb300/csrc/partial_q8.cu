@@ -425,6 +425,254 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
   }
 }
 
+// ---- consumers, at most 8 query rows: keys on the M side of the mma ----------------
+//
+// S^T (16 keys x 8 rows) = codes (A, keys x d) . Q^T (B): one mma per k-step
+// for 16 keys.  A lane's accumulators hold keys g4, g4 + 8 for rows 2 t4,
+// 2 t4 + 1; row maxima and sums reduce over the 8 lanes that share t4.  The
+// probabilities (times the V scale) are packed to f16 and transposed with
+// movmatrix into the B operand of O^T (16 channels x 8 rows) = V^T codes (A,
+// from ldmatrix.trans) . P'^T: one mma per 16 channels for 16 keys.  Output
+// tile C holds channels 16 C + 2 g4 (rows: columns) and 16 C + 2 g4 + 1.
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// Query row g4 as f16 B fragments (k-step kk: channels 16 kk + 4 t4 + 0..3),
+// with the row's channel sum and power-of-two f16 scale, both handed to the
+// lanes that own rows 2 t4 and 2 t4 + 1 of the accumulators.
+template <int D>
+struct QCols {
+  uint32_t b[D / 16][2];
+  float qsum0, qsum1, fac0, fac1;   // rows 2 t4, 2 t4 + 1
+};
+
+template <int D>
+__device__ __forceinline__ void load_q8_cols(const PartialParams& p, const WorkItem& it, int g4, int t4, QCols<D>& q) {
+  constexpr int KS = D / 16;
+  const bool ok = g4 < p.rows;
+  const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(p.q) +
+                            ((static_cast<long long>(it.b) * p.S_q + g4 / p.g) * p.H_q + it.h * p.g + g4 % p.g) * D;
+  float v[KS][4];
+  float mx = 0.f, sum = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    uint2 w = make_uint2(0u, 0u);
+    if (ok) w = *reinterpret_cast<const uint2*>(qr + 16 * kk + 4 * t4);
+    const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
+    v[kk][0] = a.x; v[kk][1] = a.y; v[kk][2] = b.x; v[kk][3] = b.y;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mx = fmaxf(mx, fabsf(v[kk][e]));
+      sum += v[kk][e];
+    }
+  }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, o));
+    sum += __shfl_xor_sync(kAll, sum, o);
+  }
+  const float fac = mx > 16384.f ? exp2f(ceilf(log2f(mx / 16384.f))) : 1.f;
+  const float inv = 1.f / fac;
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    q.b[kk][0] = pack_f16(v[kk][0] * inv, v[kk][1] * inv);
+    q.b[kk][1] = pack_f16(v[kk][2] * inv, v[kk][3] * inv);
+  }
+  // row r's values live in the quad g4 = r (lanes 4 r .. 4 r + 3)
+  q.qsum0 = __shfl_sync(kAll, sum, 8 * t4);
+  q.qsum1 = __shfl_sync(kAll, sum, 8 * t4 + 4);
+  q.fac0 = __shfl_sync(kAll, fac, 8 * t4);
+  q.fac1 = __shfl_sync(kAll, fac, 8 * t4 + 4);
+}
+
+template <int D>
+__device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) {
+  using C = Q8<D>;
+  constexpr int KS = D / 16;   // k-steps of q.k
+  constexpr int NC = D / 16;   // 16-channel output tiles
+  const PartialParams& p = w.p;
+  const uint32_t full0 = smem_u32(smem + C::kFullBar);
+  const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
+
+  constexpr int ng = 2;                         // stage groups of four warps
+  const int wps = kConsumerWarps / ng;
+  const int sgrp = cw / wps, ts = cw % wps;
+  const int my_state = cw;
+  const int keys_per_warp = kQK / wps;          // 32
+  const int g4 = lane >> 2, t4 = lane & 3;
+  const int ra = 2 * t4, rb = 2 * t4 + 1;       // the lane's accumulator rows
+  const bool oka = ra < p.rows, okb = rb < p.rows;
+  const int qia = ra / p.g, qib = rb / p.g;
+  const int lrow = lane & 7, lmat = lane >> 3;
+  const float sc = p.scale_log2;
+
+  uint32_t k = 0;
+  bool dead = false;
+  QCols<D> qn;
+  if (w.begin < w.end) load_q8_cols<D>(p, w.rec(w.begin).it, g4, t4, qn);
+  for (int ii = w.begin; ii < w.end; ++ii) {
+    const WorkItem it = w.rec(ii).it;
+    const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+    const QCols<D> q = qn;
+    if (ii + 1 < w.end) load_q8_cols<D>(p, w.rec(ii + 1).it, g4, t4, qn);
+    float o[NC][4];
+#pragma unroll
+    for (int n = 0; n < NC; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    // per lane, rows ra / rb: running max, and partial sums over the lane's keys of
+    // p, p z_v and the f16 P' the mma used
+    float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f, za = 0.f, zb = 0.f, ba = 0.f, bb = 0.f;
+
+    for (int j0 = it.a; j0 < it.e; ++k) {
+      const int j1 = min(j0 + kQK, it.e);
+      if (static_cast<int>(k % ng) != sgrp) {
+        j0 = j1;
+        continue;
+      }
+      const int st = k % C::kStagesN;
+      const uint32_t use = k / C::kStagesN;
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+        dead = true;
+        break;
+      }
+      if (reinterpret_cast<const volatile int*>(smem + C::kSeq)[st] != static_cast<int>(k)) {
+        if (lane == 0) atomicOr(p.status, kStPipeline);
+        *abort_flag = 1;
+        dead = true;
+        break;
+      }
+      const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kQK;
+      const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
+      const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
+      const uint32_t* kqp = reinterpret_cast<const uint32_t*>(smem + st * C::kStage + 2 * C::kTile);
+      const uint32_t* vqp = kqp + kQK;
+
+      for (int blk = 0; blk < keys_per_warp / 16; ++blk) {
+        const int base = ts * keys_per_warp + blk * 16;
+        // S'^T = (1024 + codes) . Q^T: ldmatrix.x4 gives keys g4 and g4 + 8 at
+        // two k-steps; one prmt per f16 pair
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c2 = 0; c2 < KS / 2; ++c2) {
+          uint32_t v[4];
+          ldsm_x4(kt + tile_off<D>(base + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1], v[2], v[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t a[4] = {biased_f16x2(v[2 * h], 0x4140u), biased_f16x2(v[2 * h + 1], 0x4140u),
+                                   biased_f16x2(v[2 * h], 0x4342u), biased_f16x2(v[2 * h + 1], 0x4342u)};
+            mma_f16(s, a, q.b[2 * c2 + h][0], q.b[2 * c2 + h][1]);
+          }
+        }
+        // keys g4 (s0, s1) and g4 + 8 (s2, s3); rows ra (s0, s2), rb (s1, s3)
+        const int kx = base + g4, ky = base + g4 + 8;
+        const int tx = pos[kx], ty = pos[ky];
+        const float2 ksx = half2_bits_to_float2(kqp[kx]), ksy = half2_bits_to_float2(kqp[ky]);
+        const float2 vqx = half2_bits_to_float2(vqp[kx]), vqy = half2_bits_to_float2(vqp[ky]);
+        const float offx = fmaf(-1024.f, ksx.x, ksx.y), offy = fmaf(-1024.f, ksy.x, ksy.y);
+        const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
+        const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
+        const bool vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
+        const bool vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
+        s[0] = vxa ? sc * fmaf(ksx.x * q.fac0, s[0], offx * q.qsum0) : -INFINITY;
+        s[1] = vxb ? sc * fmaf(ksx.x * q.fac1, s[1], offx * q.qsum1) : -INFINITY;
+        s[2] = vya ? sc * fmaf(ksy.x * q.fac0, s[2], offy * q.qsum0) : -INFINITY;
+        s[3] = vyb ? sc * fmaf(ksy.x * q.fac1, s[3], offy * q.qsum1) : -INFINITY;
+        // row maxima over the 8 lanes sharing t4
+        float mxa = fmaxf(s[0], s[2]), mxb = fmaxf(s[1], s[3]);
+#pragma unroll
+        for (int x = 4; x <= 16; x <<= 1) {
+          mxa = fmaxf(mxa, __shfl_xor_sync(kAll, mxa, x));
+          mxb = fmaxf(mxb, __shfl_xor_sync(kAll, mxb, x));
+        }
+        const float na = fmaxf(ma, mxa), nb = fmaxf(mb, mxb);
+        const float aa = na == -INFINITY ? 1.f : exp2f(ma - na);
+        const float ab = nb == -INFINITY ? 1.f : exp2f(mb - nb);
+        const float ua = na == -INFINITY ? 0.f : na, ub = nb == -INFINITY ? 0.f : nb;
+        const float p0 = exp2f(s[0] - ua), p1 = exp2f(s[1] - ub), p2 = exp2f(s[2] - ua), p3 = exp2f(s[3] - ub);
+        // P'^T (keys x rows), V scale folded in, f16; transposed into B fragments
+        const uint32_t px = pack_f16(p0 * vqx.x, p1 * vqx.x), py = pack_f16(p2 * vqy.x, p3 * vqy.x);
+        const float2 fx = half2_bits_to_float2(px), fy = half2_bits_to_float2(py);
+        la = la * aa + (p0 + p2);
+        lb = lb * ab + (p1 + p3);
+        za = za * aa + (p0 * vqx.y + p2 * vqy.y);
+        zb = zb * ab + (p1 * vqx.y + p3 * vqy.y);
+        ba = ba * aa + (fx.x + fy.x);
+        bb = bb * ab + (fx.y + fy.y);
+        ma = na;
+        mb = nb;
+        if (__any_sync(kAll, aa != 1.f || ab != 1.f)) {
+#pragma unroll
+          for (int n = 0; n < NC; ++n) {
+            o[n][0] *= aa;
+            o[n][1] *= ab;
+            o[n][2] *= aa;
+            o[n][3] *= ab;
+          }
+        }
+        const uint32_t pb0 = movmatrix_trans(px), pb1 = movmatrix_trans(py);
+        // O'^T += V^T codes . P'^T: ldmatrix.trans gives keys (2 t4, 2 t4 + 1) of
+        // keys 0-7 / 8-15 at channel pair g4 of two chunks
+#pragma unroll
+        for (int c2 = 0; c2 < NC / 2; ++c2) {
+          uint32_t v[4];
+          ldsm_x4_trans(vt + tile_off<D>(base + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1], v[2], v[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t a[4] = {biased_f16x2(v[2 * h], 0x4240u), biased_f16x2(v[2 * h], 0x4341u),
+                                   biased_f16x2(v[2 * h + 1], 0x4240u), biased_f16x2(v[2 * h + 1], 0x4341u)};
+            mma_f16(o[2 * c2 + h], a, pb0, pb1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      j0 = j1;
+    }
+
+    // end of item: complete the sums over the 8 lanes sharing t4
+#pragma unroll
+    for (int x = 4; x <= 16; x <<= 1) {
+      la += __shfl_xor_sync(kAll, la, x);
+      lb += __shfl_xor_sync(kAll, lb, x);
+      za += __shfl_xor_sync(kAll, za, x);
+      zb += __shfl_xor_sync(kAll, zb, x);
+      ba += __shfl_xor_sync(kAll, ba, x);
+      bb += __shfl_xor_sync(kAll, bb, x);
+    }
+    if (!dead) {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int row = rr ? rb : ra;
+        if (!(rr ? okb : oka)) continue;
+        const float m = rr ? mb : ma, l = rr ? lb : la;
+        const float add = (rr ? zb : za) - 1024.f * (rr ? bb : ba);
+        const int i = row / p.g, hq = it.h * p.g + row % p.g;
+        const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
+        if (it.slot < 0) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            *reinterpret_cast<__nv_bfloat162*>(out + 16 * c + 2 * g4) =
+                __floats2bfloat162_rn((o[c][rr] + add) * inv, (o[c][2 + rr] + add) * inv);
+          if (g4 == 0 && p.lse) p.lse[orow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        } else {
+          const long long srow = static_cast<long long>(it.slot + my_state) * p.rows + row;
+          float* u = p.u + srow * D;
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            *reinterpret_cast<float2*>(u + 16 * c + 2 * g4) = make_float2(o[c][rr] + add, o[c][2 + rr] + add);
+          if (g4 == 0) p.ml[srow] = make_float2(l > 0.f ? m : -INFINITY, l);
+        }
+      }
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_constant__ PartialParams p) {
   using C = Q8<D>;
@@ -456,7 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_co
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ8ConsumerRegs));
-  consume_q8<D>(w, smem, warp, lane);
+  if (p.rows <= 8) consume_q8_swap<D>(w, smem, warp, lane);
+  else consume_q8<D>(w, smem, warp, lane);
 }
 
 template <int D>

@@ -121,3 +121,15 @@ def test_int8_decode_page_sizes(P):
     p, cache = append_history(w, "int8", [[64, 200], [], []])
     O, L, info = _run(w, "int8", p, cache, chunk_tokens=128, num_sms=3)
     _compare(O, L, w, p, _oracle_cache(w, "int8"), H.all_rows(p))
+
+
+@pytest.mark.parametrize("S_q,H_q,H_kv,d", [(3, 16, 4, 128), (4, 16, 2, 128), (4, 16, 2, 64)])
+def test_int8_decode_more_than_eight_rows(S_q, H_q, H_kv, d):
+    """12 and 32 query rows per kv head (row tiles of 16 on the mma M side), causal verify rows."""
+    lens = [420, 37, 3]
+    w = W.quantized_history("q8r", B=3, S_q=S_q, H_q=H_q, H_kv=H_kv, d=d, lens=lens, P=16, seed=25,
+                            device="cuda", fmt="int8", pool_pages=sum(-(-t // 16) for t in lens) + 3)
+    p, cache = append_history(w, "int8", [[200], [], []])
+    O, L, info = _run(w, "int8", p, cache, chunk_tokens=128, num_sms=3)
+    assert info["rows"] == S_q * H_q // H_kv
+    _compare(O, L, w, p, _oracle_cache(w, "int8"), H.all_rows(p))
