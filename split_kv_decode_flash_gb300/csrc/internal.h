@@ -33,12 +33,22 @@ enum StatusBits : int32_t {
   kStPipeline = 64,     // a consumer found a ring stage stamped with another stage number
 };
 
+// KIVI INT4 problems with d = 128, at most 8 rows, Gv = 32, an interval
+// visibility program and power-of-two page size P and residual length R run
+// on the tensor-core kernel (partial_q4.cu); other KIVI problems on the
+// byte-format kernel (partial.cu).
+inline bool kivi_on_tensor_cores(int d, int rows, int Gv, int mask, int P, int R) {
+  return d == 128 && rows <= 8 && Gv == 32 && mask != DATTN_MASK_INDEX_LIST && P > 0 && (P & (P - 1)) == 0 &&
+         R > 0 && (R & (R - 1)) == 0;
+}
+
 // Partial states an item leaves per query row.  Consumer warps are arranged
-// in row blocks (16 rows, one mma tile, in the bf16 tensor-core kernel; 4 rows
-// in the byte-format kernel); every warp leaves the state of its block's rows
-// over its own share of the item's keys.
-inline int states_per_item(int rows, int fmt) {
-  if (fmt != DATTN_FMT_INT4_KIVI) return kConsumerWarps / (rows <= 16 ? 1 : 2);
+// in row blocks (16 rows, one mma tile, in the bf16 and INT8 tensor-core
+// kernels, 8 rows in the KIVI one; 4 rows in the byte-format kernel); every
+// warp leaves the state of its block's rows over its own share of the item's
+// keys.
+inline int states_per_item(int rows, int fmt, bool kivi_tc) {
+  if (fmt != DATTN_FMT_INT4_KIVI || kivi_tc) return kConsumerWarps / (rows <= 16 ? 1 : 2);
   return kConsumerWarps / (rows <= 4 ? 1 : rows <= 8 ? 2 : rows <= 16 ? 4 : 8);
 }
 
@@ -112,10 +122,11 @@ struct MergeParams {
   int32_t n_groups, rows, g, S_q, H_q;
 };
 
-// Kernel launchers (partial.cu, merge.cu); return cudaError_t as int.
+// Kernel launchers (partial*.cu, merge.cu); return cudaError_t as int.
 int launch_partial(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_partial_bf16(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_partial_q8(const PartialParams& p, int d, int n_ctas, void* stream);
+int launch_partial_q4(const PartialParams& p, int n_ctas, void* stream);
 int launch_merge(const MergeParams& p, int d, void* stream);
 
 }  // namespace dattn

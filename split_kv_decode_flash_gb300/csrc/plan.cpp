@@ -263,9 +263,12 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
         add(0, 0);
         seg_cta.push_back(static_cast<int>(std::min<long long>(n_seg - 1, g_off / seg)));
       }
+      // KIVI: cuts rounded up onto the 32-key grid, so that the consumers' 32-key
+      // steps never straddle a K group (a CTA streams at most 31 keys more)
+      const long long grid = p.fmt == DATTN_FMT_INT4_KIVI ? 32 : 1;
       for (long long a = 0; a < n;) {
         const long long c = (g_off + a) / seg;
-        const long long e = std::min<long long>(n, (c + 1) * seg - g_off);
+        const long long e = std::min<long long>(n, ((c + 1) * seg - g_off + grid - 1) / grid * grid);
         add(static_cast<int>(a), static_cast<int>(e));
         seg_cta.push_back(static_cast<int>(c));
         a = e;
@@ -283,7 +286,8 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   //    an item leaves its own state, so an item owns states_per_item slots; a
   //    group that is one item with one state per row writes O directly.
   std::vector<MergeGroup> merges;
-  const int spi = states_per_item(rows, p.fmt);
+  const bool kivi_tc = kivi_on_tensor_cores(p.d_h, rows, p.kivi_v_group, p.mask, p.page_size, p.kivi_residual);
+  const int spi = states_per_item(rows, p.fmt, kivi_tc);
   int n_slots = 0, max_splits = 0;
   for (int k = 0; k < n_groups; ++k) {
     const int n = group_first[k + 1] - group_first[k];

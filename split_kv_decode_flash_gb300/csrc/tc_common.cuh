@@ -52,6 +52,10 @@ __device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int ii, bool
   return complete_rec(p, p.cta_recs[ii], report);
 }
 
+// Out of line: reached only by CTAs with more than kItemCache items, and
+// inlining it at every record read would multiply the kernels' code size.
+__device__ __noinline__ ItemRec load_rec_uncached(const PartialParams& p, int ii) { return load_rec(p, ii, false); }
+
 // The CTA's item list: the first kItemCache records come from shared memory
 // (filled once at kernel start), later ones from global memory.
 struct Walk {
@@ -60,7 +64,7 @@ struct Walk {
   int begin, end;
   uint64_t keep;      // L2 evict-last policy for the page-table reads
   __device__ __forceinline__ ItemRec rec(int ii) const {
-    return ii - begin < kItemCache ? cache[ii - begin] : load_rec(p, ii, false);
+    return ii - begin < kItemCache ? cache[ii - begin] : load_rec_uncached(p, ii);
   }
 };
 

@@ -113,6 +113,26 @@ def test_quantized_full_size_sampled(fmt):
     _compare(O, L, w, p, _oracle_cache(w, fmt, reqs), rows)
 
 
+@pytest.mark.parametrize("S_q,H_q,H_kv,mask,chunk,num_sms", [
+    (1, 64, 8, "causal", 0, 152),         # 8 rows per kv head
+    (2, 8, 2, "sink_window", 0, 152),     # 8 rows, two-run stages, causal verify rows
+    (2, 8, 2, "sink_window", 50, 4),      # chunks that start inside K groups
+    (1, 16, 8, "sink_window", 64, 3),     # 2 rows
+])
+def test_int4_kivi_tensor_core_rows_and_windows(S_q, H_q, H_kv, mask, chunk, num_sms):
+    """d = 128, Gv = 32, at most 8 rows: K groups that straddle 16-key blocks
+    (window starts off the group grid), stages of two runs touching up to ten
+    groups, residual-only and just-closed-group requests."""
+    lens = [2000, 1999, 1777, 300, 129, 7]
+    w = W.quantized_history("q4t", B=len(lens), S_q=S_q, H_q=H_q, H_kv=H_kv, d=128, lens=lens, P=16, seed=26,
+                            device="cuda", fmt="int4_kivi", pool_pages=sum(-(-t // 16) for t in lens) + 3)
+    w.problem = dict(w.problem, mask=mask, n_sink=34, window=1000)
+    p, cache = append_history(w, "int4_kivi", [[900, 1500], [], [1000], [160], [], []])
+    O, L, info = _run(w, "int4_kivi", p, cache, chunk_tokens=chunk, num_sms=num_sms)
+    assert info["rows"] == S_q * H_q // H_kv
+    _compare(O, L, w, p, _oracle_cache(w, "int4_kivi"), H.all_rows(p))
+
+
 @pytest.mark.parametrize("P", [4, 64])
 def test_int8_decode_page_sizes(P):
     lens = [300, 70, 5]
