@@ -63,8 +63,9 @@ struct Q4 {
   static constexpr int kOffVQ = kOffGT + kGT;
   static constexpr int kStage = (kOffVQ + kVQ + 127) / 128 * 128;
   static_assert(kStage >= 2 * kRKeys * kD * 2, "a residual stage fits in a stage slot");
-  static constexpr int kPos = kStagesN * kStage;   // int32 [stages][kQKeys]
-  static constexpr int kFlags = kPos + kStagesN * kQKeys * 4;
+  static constexpr int kPos = kStagesN * kStage;   // int32 [stages][kQKeys]: logical key per slot
+  static constexpr int kRows = kPos + kStagesN * kQKeys * 4;   // uint32 [stages][kQKeys]: source row per slot
+  static constexpr int kFlags = kRows + kStagesN * kQKeys * 4;
   static constexpr int kSeq = kFlags + kStagesN * 4;
   static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
@@ -310,8 +311,13 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw) {
     const uint32_t use = k / C::kStagesN;
     if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kQKeys;
+    uint32_t* rows = reinterpret_cast<uint32_t*>(smem + C::kRows) + st * kQKeys;
 #pragma unroll
-    for (int h = 0; h < kQSlots; ++h) pos[lane + 32 * h] = r0.t[h];
+    for (int h = 0; h < kQSlots; ++h) {
+      pos[lane + 32 * h] = r0.t[h];
+      rows[lane + 32 * h] = r0.row[h];
+    }
+    __syncwarp();
     if (lane == 0) {
       reinterpret_cast<int*>(smem + C::kFlags)[st] = (r0.full ? kFlagFull : 0) | (r0.resid ? kFlagResidual : 0);
       reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
@@ -321,43 +327,39 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw) {
       // bf16 rows of the residual ring: 64 slots, 16 chunks per row, two rows per instruction
       const uint32_t rkt = kt, rvt = kt + kRKeys * kD * 2;
       const int sub = lane >> 4, ch = lane & 15;
-#pragma unroll
-      for (int h = 0; h < kRKeys / 32; ++h) {
 #pragma unroll 1
-        for (int s0 = 32 * h; s0 < 32 * h + 32; s0 += 2) {
-          const int s = s0 + sub;
-          const uint32_t row = __shfl_sync(kAll, r0.row[h], s & 31);
-          const bool ok = row != kNoRow;
-          const size_t off = static_cast<size_t>(ok ? row : 0u) * (kD * 2) + ch * 16;
-          const uint32_t dst = tile_off<kD * 2>(s, ch);
-          cp_async16(rkt + dst, kres + off, ok ? 16u : 0u, stream_pol);
-          cp_async16(rvt + dst, vres + off, ok ? 16u : 0u, stream_pol);
-        }
+      for (int s0 = 0; s0 < kRKeys; s0 += 2) {
+        const int s = s0 + sub;
+        const uint32_t row = rows[s];
+        const bool ok = row != kNoRow;
+        const size_t off = static_cast<size_t>(ok ? row : 0u) * (kD * 2) + ch * 16;
+        const uint32_t dst = tile_off<kD * 2>(s, ch);
+        cp_async16(rkt + dst, kres + off, ok ? 16u : 0u, stream_pol);
+        cp_async16(rvt + dst, vres + off, ok ? 16u : 0u, stream_pol);
       }
     } else {
       // codes: 256 slots, 4 chunks per row, eight rows per instruction
+      // (the swizzle of slot s0 + sub only depends on sub, as s0 steps by 8)
       const int sub = lane >> 2, ch = lane & 3;
-#pragma unroll
-      for (int h = 0; h < kQSlots; ++h) {
-#pragma unroll 1
-        for (int s0 = 32 * h; s0 < 32 * h + 32; s0 += 8) {
-          const int s = s0 + sub;
-          const uint32_t row = __shfl_sync(kAll, r0.row[h], s & 31);
-          const bool ok = row != kNoRow;
-          const size_t off = static_cast<size_t>(ok ? row : 0u) * C::kCodeRow + ch * 16;
-          const uint32_t dst = code_off(s, ch);
-          cp_async16(kt + dst, kbase + off, ok ? 16u : 0u, stream_pol);
-          cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
-        }
+      const uint32_t dst0 = code_off(sub, ch);
+      const char* kb = kbase + ch * 16;
+      const char* vb = vbase + ch * 16;
+#pragma unroll 4
+      for (int s0 = 0; s0 < kQKeys; s0 += 8) {
+        const uint32_t row = rows[s0 + sub];
+        const bool ok = row != kNoRow;
+        const size_t off = static_cast<size_t>(ok ? row : 0u) * C::kCodeRow;
+        const uint32_t dst = dst0 + s0 * C::kCodeRow;
+        cp_async16(kt + dst, kb + off, ok ? 16u : 0u, stream_pol);
+        cp_async16(vt + dst, vb + off, ok ? 16u : 0u, stream_pol);
       }
       // per-key V qparams
       const uint32_t vq = kt + C::kOffVQ;
-#pragma unroll
-      for (int h = 0; h < kQSlots; ++h) {
-        const uint32_t row = r0.row[h];
+#pragma unroll 1
+      for (int s = lane; s < kQKeys; s += 32) {
+        const uint32_t row = rows[s];
         const bool ok = row != kNoRow;
-        cp_async16(vq + 16 * (lane + 32 * h), vqbase + static_cast<size_t>(ok ? row : 0u) * 16, ok ? 16u : 0u,
-                   stream_pol);
+        cp_async16(vq + 16 * s, vqbase + static_cast<size_t>(ok ? row : 0u) * 16, ok ? 16u : 0u, stream_pol);
       }
       // K-group qparams table: group k (lane k's description) -> 32 chunks of 16 bytes
       const uint32_t gt = kt + C::kOffGT;
@@ -387,6 +389,12 @@ __device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+
+// a * (low half of b, in both halves), rounded to nearest.
+__device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2_rn(*reinterpret_cast<const __half2*>(&a), __low2half2(*reinterpret_cast<const __half2*>(&b)));
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // a * b - c with one rounding: the exact low part of a split f16 product.
@@ -688,9 +696,13 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
           const int sel1 = qsel_of(sg, it, min(j0 + base0 + 16 * NS - 1, j1 - 1), gsh);
           int selx[NS], sely[NS];
 #pragma unroll
-          for (int u = 0; u < NS; ++u) {
-            selx[u] = qsel_of(sg, it, min(j0 + base0 + 16 * u + g4, j1 - 1), gsh);
-            sely[u] = qsel_of(sg, it, min(j0 + base0 + 16 * u + g4 + 8, j1 - 1), gsh);
+          for (int u = 0; u < NS; ++u) selx[u] = sely[u] = sel0;
+          if (sel1 != sel0) {
+#pragma unroll
+            for (int u = 0; u < NS; ++u) {
+              selx[u] = qsel_of(sg, it, min(j0 + base0 + 16 * u + g4, j1 - 1), gsh);
+              sely[u] = qsel_of(sg, it, min(j0 + base0 + 16 * u + g4 + 8, j1 - 1), gsh);
+            }
           }
           for (int sel = sel0; sel <= sel1; ++sel) {
             if (sg.gid(sel) != cur_gid) {
@@ -728,23 +740,35 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
             for (int e = 0; e < 4; ++e) s[0][e] += __shfl_xor_sync(kAll, s[0][e], 2);
           }
         }
-        // visibility: the slot's key, the row, the mask program
+        // visibility: the slot's key, the row, the mask program.  A step of a
+        // FULL stage whose slots all hold keys needs none of it (rows past
+        // p.rows have a zero query, stay finite and are never written).
         float mxa = -INFINITY, mxb = -INFINITY;
+        if (full && !resid && j0 + base0 + 16 * NS <= j1) {
 #pragma unroll
-        for (int u = 0; u < NS; ++u) {
-          const bool live = !resid || u == 0;
-          const int kx = base0 + 16 * u + g4, ky = kx + 8;
-          const int tx = live ? pos[kx] : -1, ty = live ? pos[ky] : -1;
-          const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
-          const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
-          const bool vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
-          const bool vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
-          s[u][0] = vxa ? s[u][0] * sc : -INFINITY;
-          s[u][1] = vxb ? s[u][1] * sc : -INFINITY;
-          s[u][2] = vya ? s[u][2] * sc : -INFINITY;
-          s[u][3] = vyb ? s[u][3] * sc : -INFINITY;
-          mxa = fmaxf(mxa, fmaxf(s[u][0], s[u][2]));
-          mxb = fmaxf(mxb, fmaxf(s[u][1], s[u][3]));
+          for (int u = 0; u < NS; ++u) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[u][e] *= sc;
+            mxa = fmaxf(mxa, fmaxf(s[u][0], s[u][2]));
+            mxb = fmaxf(mxb, fmaxf(s[u][1], s[u][3]));
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < NS; ++u) {
+            const bool live = !resid || u == 0;
+            const int kx = base0 + 16 * u + g4, ky = kx + 8;
+            const int tx = live ? pos[kx] : -1, ty = live ? pos[ky] : -1;
+            const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
+            const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
+            const bool vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
+            const bool vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
+            s[u][0] = vxa ? s[u][0] * sc : -INFINITY;
+            s[u][1] = vxb ? s[u][1] * sc : -INFINITY;
+            s[u][2] = vya ? s[u][2] * sc : -INFINITY;
+            s[u][3] = vyb ? s[u][3] * sc : -INFINITY;
+            mxa = fmaxf(mxa, fmaxf(s[u][0], s[u][2]));
+            mxb = fmaxf(mxb, fmaxf(s[u][1], s[u][3]));
+          }
         }
 #pragma unroll
         for (int x = 4; x <= 16; x <<= 1) {
@@ -800,8 +824,8 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
             uint32_t pb[kCg][2];
 #pragma unroll
             for (int x = 0; x < kCg; ++x) {
-              pb[x][0] = movmatrix_t(hmul2_rn(px, __byte_perm(sx[x], 0u, 0x1010u)));
-              pb[x][1] = movmatrix_t(hmul2_rn(py, __byte_perm(sy[x], 0u, 0x1010u)));
+              pb[x][0] = movmatrix_t(hmul2_lo(px, sx[x]));
+              pb[x][1] = movmatrix_t(hmul2_lo(py, sy[x]));
               za[x] = fma_q_zhi<0>(px, sx[x], fma_q_zhi<0>(py, sy[x], za[x]));
               zb[x] = fma_q_zhi<1>(px, sx[x], fma_q_zhi<1>(py, sy[x], zb[x]));
             }
