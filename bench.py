@@ -37,6 +37,9 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
+OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "int8", "int4-kivi")
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -46,6 +49,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunk", type=int, default=0, help="planner chunk width (0 = default)")
+    ap.add_argument("--workload", choices=("paged",) + OTHER_WORKLOADS, default="paged",
+                    help="paged: the benchmark line; the others print one timing line for a decode step "
+                         "of that workload")
     ap.add_argument("--cpu-child", nargs="*", help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -81,7 +87,7 @@ def algorithmic_bytes(w, info, items):
 def kernel_hash():
     """Hash of the partial kernel's sources: DRAM counters taken on other sources are stale."""
     h = hashlib.sha256()
-    for f in ("device.cuh", "internal.h", "stream.cuh", "partial_bf16.cu"):
+    for f in ("device.cuh", "internal.h", "stream.cuh", "tc_common.cuh", "partial_bf16.cu"):
         with open(os.path.join(ROOT, "split_kv_decode_flash_gb300", "csrc", f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -454,6 +460,103 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---- the other workloads: one timing line each ------------------------------------------
+
+def _quantized_cache(dattn, w, fmt, dev):
+    """The workload's packed bf16 history written into a fresh cache by one kv_append call."""
+    import torch
+
+    p = dict(w.problem, fmt=fmt)
+    H, P, d, B, n = p["H_kv"], p["P"], p["d"], p["B"], p["num_pages"]
+    G, Gv, R = p["kivi_group"], p["kivi_v_group"], p["kivi_residual"]
+    c = {}
+    if fmt == "int8":
+        c["k"] = torch.zeros((n, H, P, d), dtype=torch.uint8, device=dev)
+        c["k_qparams"] = torch.zeros((n, H, P, 2), dtype=torch.float16, device=dev)
+        c["v_qparams"] = torch.zeros_like(c["k_qparams"])
+    else:
+        c["k"] = torch.zeros((n, H, P, d // 2), dtype=torch.uint8, device=dev)
+        c["k_qparams"] = torch.zeros((n, H, max(1, P // G), d, 2), dtype=torch.float16, device=dev)
+        c["v_qparams"] = torch.zeros((n, H, P, d // Gv, 2), dtype=torch.float16, device=dev)
+        c["k_residual"] = torch.zeros((B, R, H, d), dtype=torch.bfloat16, device=dev)
+        c["v_residual"] = torch.zeros_like(c["k_residual"])
+    c["v"] = torch.zeros_like(c["k"])
+    c["page_indptr"] = w.page_indptr.to(dev)
+    c["page_indices"] = w.page_indices.to(dev)
+    ws = torch.empty(dattn.kv_append_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    dattn.kv_append(p, dattn.tensors_from(**c), w.k_rows.to(dev), w.v_rows.to(dev), [0] * B,
+                    w.rows_indptr.tolist(), w.page_indptr, ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0, "kv_append device check fired"
+    return p, c
+
+
+def _stream_bytes(p, info, lens):
+    """K/V bytes of the visible streams (what the step must read)."""
+    d = p["d"]
+    fmt = p.get("fmt", "bf16")
+    if fmt == "bf16":
+        return info["stream_keys"] * 4 * d
+    if fmt == "int8":
+        return info["stream_keys"] * (2 * d + 8)
+    G, Gv, R = p["kivi_group"], p["kivi_v_group"], p["kivi_residual"]
+    total = 0
+    for T in lens:      # causal, S_q = 1: the stream is the whole history
+        nq = G * -(-max(0, T - R) // G)
+        total += nq * (d + 4 * d // Gv) + (nq // G) * 4 * d + (T - nq) * 4 * d
+    return total * p["H_kv"]
+
+
+def run_other(args):
+    import torch
+
+    import split_kv_decode_flash_gb300 as dattn
+    import workloads as W
+
+    assert torch.cuda.is_available(), "bench.py --workload needs a GPU"
+    dattn.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    name = args.workload
+    if name in ("int8", "int4-kivi"):
+        fmt = "int8" if name == "int8" else "int4_kivi"
+        w = W.quantized(dev, fmt=fmt)
+        p, cache = _quantized_cache(dattn, w, fmt, dev)
+    else:
+        w = {"long-s1": lambda: W.long_context(dev, 1), "long-s4": lambda: W.long_context(dev, 4),
+             "sink-window": lambda: W.retention(dev, "sink_window"),
+             "index-list": lambda: W.retention(dev, "index_list")}[name]()
+        p = w.problem
+        cache = dict(k=w.k, v=w.v, page_indptr=w.page_indptr.to(dev), page_indices=w.page_indices.to(dev))
+        if w.index_list is not None:
+            cache.update(index_indptr=w.index_indptr.to(dev), index_list=w.index_list.to(dev))
+    props = torch.cuda.get_device_properties(dev)
+    plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, index_indptr=w.index_indptr,
+                            index_list=w.index_list, num_sms=props.multi_processor_count, chunk_tokens=args.chunk)
+    o = torch.empty((p["B"], p["S_q"], p["H_q"], p["d"]), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p["B"], p["S_q"], p["H_q"]), dtype=torch.float32, device=dev)
+    t = dattn.tensors_from(q=w.q.to(dev), o=o, lse=lse, **cache)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    dattn.dattn_plan_upload(plan, ws, stream)
+    for _ in range(max(3, args.warmup)):
+        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, stream=stream)
+    torch.cuda.synchronize()
+    assert dattn.dattn_device_status(ws, stream) == 0, "device bounds check fired"
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    us = start.elapsed_time(end) / args.steps * 1e3
+    nb = _stream_bytes(p, plan.info, w.kv_len.tolist())
+    peak, peak_src = measured_peak()
+    print(json.dumps({"workload": w.name, "us_per_step": us, "kv_bytes_per_step": nb, "GBps": nb / us / 1e3,
+                      "frac": nb / us / 1e3 / peak, "peak": peak, "peak_source": peak_src,
+                      "rows": plan.info["rows"], "n_items": plan.info["n_items"], "steps": args.steps,
+                      "timing": "CUDA events around K back-to-back decode steps (partial + merge)"}), flush=True)
+
+
 def main():
     args = parse()
     if args.cpu_child is not None:
@@ -461,6 +564,8 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "paged":
+        run_other(args)
     else:
         run_ours(args)
 
