@@ -67,7 +67,7 @@ struct Bf {
 
 
 template <int D>
-__device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
+__device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
   using C = Bf<D>;
   const PartialParams& p = w.p;
   constexpr int kSlotsPerPass = 32 / C::kChunks;   // key rows per warp instruction
@@ -89,9 +89,11 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw) {
   pc_advance<kTK>(w, c2, kProducerWarps);
   const SlotKeys<2> k0 = slot_keys<2>(w, c0, lane);
   SlotKeys<2> k1 = slot_keys<2>(w, c1, lane);
+  SlotKeys<2> k2 = slot_keys<2>(w, c2, lane);
+  // Up to here only the plan was read; the page table is a device input.
+  dependency_wait(dep_wait);
   const SlotPages<2> g0 = slot_pages<2>(w, c0, k0);     // both stages' page lookups in flight together
   SlotPages<2> g1 = slot_pages<2>(w, c1, k1);
-  SlotKeys<2> k2 = slot_keys<2>(w, c2, lane);
   SlotRows<2> r0 = slot_rows<2>(w, c0, k0, g0, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
@@ -180,8 +182,9 @@ __device__ __forceinline__ void load_q(const PartialParams& p, const WorkItem& i
 }
 
 template <int D>
-__device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane) {
+__device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, bool dep_wait) {
   using C = Bf<D>;
+  dependency_wait(dep_wait);   // before Q and the state writes
   const PartialParams& p = w.p;
   constexpr int KS = D / 16;   // k-steps of q.k
   constexpr int NT = D / 8;    // 8-channel tiles of the output
@@ -338,13 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
-  // The plan's records may be read while the preceding kernel of the stream
-  // still runs (programmatic launch); device inputs only after the wait.
-  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
-    cache[i] = ld_rec_keep(p.cta_recs + it_begin + i, policy_evict_last());
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
-    if (!rec_complete_as_planned(p, cache[i])) cache[i] = complete_rec(p, cache[i], true);
+  const int incomplete = fill_item_cache(p, cache, it_begin, it_end);
   if (threadIdx.x == 0) {
     const int warps_per_stage = p.rows <= 16 ? kConsumerWarps / 2 : kConsumerWarps;
     for (int s = 0; s < C::kStagesN; ++s) {
@@ -354,16 +351,20 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
     fence_barrier_init();
   }
-  __syncthreads();
+  // Records that need device inputs are completed by the whole CTA after the
+  // wait.  Otherwise each warp waits on its own, just before its first device
+  // read, and the producers set up their first stages' keys in the meantime.
+  const bool complete_now = __syncthreads_or(incomplete);
+  if (complete_now) complete_item_cache(p, cache, it_begin, it_end);
   const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBfProducerRegs));
-    produce_bf16<D>(w, smem, lane, warp - kConsumerWarps);
+    produce_bf16<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));
-  consume_bf16<D>(w, smem, warp, lane);
+  consume_bf16<D>(w, smem, warp, lane, !complete_now);
 }
 
 template <int D>

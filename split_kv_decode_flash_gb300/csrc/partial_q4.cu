@@ -271,7 +271,7 @@ __device__ __forceinline__ Q4Desc q4_rows(const Walk& w, const QCur& c, const in
   return d;
 }
 
-__device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw) {
+__device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
   using C = Q4;
   const PartialParams& p = w.p;
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
@@ -297,6 +297,7 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw) {
   int t0[kQSlots], t1[kQSlots], pi0[kQSlots], g0i;
   q4_keys(w, c0, lane, t0);
   q4_keys(w, c1, lane, t1);
+  dependency_wait(dep_wait);   // the page table is a device input
   q4_pages(w, c0, t0, lane, sh, pi0, g0i);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
@@ -938,11 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4_kernel(const __grid_co
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
-  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
-    cache[i] = ld_rec_keep(p.cta_recs + it_begin + i, policy_evict_last());
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
-    if (!rec_complete_as_planned(p, cache[i])) cache[i] = complete_rec(p, cache[i], true);
+  const int incomplete = fill_item_cache(p, cache, it_begin, it_end);
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStagesN; ++s) {
       mbar_init(smem_u32(smem + C::kFullBar + 8 * s), 1);
@@ -951,15 +948,18 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4_kernel(const __grid_co
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
     fence_barrier_init();
   }
-  __syncthreads();
+  // without records to complete, each warp waits just before its first device read
+  const bool complete_now = __syncthreads_or(incomplete);
+  if (complete_now) complete_item_cache(p, cache, it_begin, it_end);
   const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ4ProducerRegs));
-    produce_q4(w, smem, lane, warp - kConsumerWarps);
+    produce_q4(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ4ConsumerRegs));
+  dependency_wait(!complete_now);   // before Q and the state writes
   if (p.rows <= 4) consume_q4<true>(w, smem, warp, lane);
   else consume_q4<false>(w, smem, warp, lane);
 }

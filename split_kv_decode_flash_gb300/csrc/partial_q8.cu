@@ -76,7 +76,7 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
 // ---- producer ---------------------------------------------------------------------------
 
 template <int D>
-__device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw) {
+__device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
   using C = Q8<D>;
   const PartialParams& p = w.p;
   constexpr int kSlotsPerPass = 32 / C::kChunks;   // key rows per warp instruction
@@ -99,6 +99,7 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw) {
   pc_advance<kQK>(w, c2, kProducerWarps);
   const SlotKeys<kQS> k0 = slot_keys<kQS>(w, c0, lane);
   SlotKeys<kQS> k1 = slot_keys<kQS>(w, c1, lane);
+  dependency_wait(dep_wait);   // the page table is a device input
   const SlotPages<kQS> g0 = slot_pages<kQS>(w, c0, k0);
   SlotPages<kQS> g1 = slot_pages<kQS>(w, c1, k1);
   SlotKeys<kQS> k2 = slot_keys<kQS>(w, c2, lane);
@@ -681,11 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_co
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
-  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
-    cache[i] = ld_rec_keep(p.cta_recs + it_begin + i, policy_evict_last());
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
-    if (!rec_complete_as_planned(p, cache[i])) cache[i] = complete_rec(p, cache[i], true);
+  const int incomplete = fill_item_cache(p, cache, it_begin, it_end);
   if (threadIdx.x == 0) {
     const int warps_per_stage = p.rows <= 16 ? kConsumerWarps / 2 : kConsumerWarps;
     for (int s = 0; s < C::kStagesN; ++s) {
@@ -695,15 +692,18 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_co
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
     fence_barrier_init();
   }
-  __syncthreads();
+  // without records to complete, each warp waits just before its first device read
+  const bool complete_now = __syncthreads_or(incomplete);
+  if (complete_now) complete_item_cache(p, cache, it_begin, it_end);
   const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ8ProducerRegs));
-    produce_q8<D>(w, smem, lane, warp - kConsumerWarps);
+    produce_q8<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ8ConsumerRegs));
+  dependency_wait(!complete_now);   // before Q and the state writes
   if (p.rows <= 8) consume_q8_swap<D>(w, smem, warp, lane);
   else consume_q8<D>(w, smem, warp, lane);
 }

@@ -170,6 +170,39 @@ __device__ __forceinline__ uint32_t tile_off(int s, int c) {
   return static_cast<uint32_t>(s * ROWB + ((c ^ (s & kMask)) << 4));
 }
 
+// ---- kernel prologue ----------------------------------------------------------------------
+//
+// The kernels are launched as programmatic dependents: the plan's records may
+// be read while the preceding kernel of the stream still runs, device inputs
+// (Q, K/V, page tables, lists) and the workspace only after griddepcontrol.wait.
+
+// Copies the CTA's records into shared memory; nonzero when some record
+// needs device inputs to complete (index lists, cache rows, page bounds the
+// plan lacks) or the CTA has more records than the cache holds.
+__device__ __forceinline__ int fill_item_cache(const PartialParams& p, ItemRec* cache, int it_begin, int it_end) {
+  int incomplete = it_end - it_begin > kItemCache;
+  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x) {
+    cache[i] = ld_rec_keep(p.cta_recs + it_begin + i, policy_evict_last());
+    incomplete |= !rec_complete_as_planned(p, cache[i]);
+  }
+  return incomplete;
+}
+
+// The whole CTA waits for the preceding grid and completes the records.
+__device__ __forceinline__ void complete_item_cache(const PartialParams& p, ItemRec* cache, int it_begin,
+                                                    int it_end) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int i = threadIdx.x; i < min(it_end - it_begin, kItemCache); i += blockDim.x)
+    if (!rec_complete_as_planned(p, cache[i])) cache[i] = complete_rec(p, cache[i], true);
+  __syncthreads();
+}
+
+// A warp's own wait, just before its first device read, when the CTA did not
+// wait as a whole.
+__device__ __forceinline__ void dependency_wait(bool needed) {
+  if (needed) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- producer ---------------------------------------------------------------------------
 
 // A producer warp's position: stream keys [j0, j1) of item ii (ii == end:
