@@ -15,6 +15,8 @@ Layouts (element order, outermost first):
   j lives in page indices[indptr[b] + j]                               (§0x04D)
 * paged INT8:            codes [N_pages, H_kv, P, d] uint8;
                          qparams [N_pages, H_kv, P, 2] fp16 (s, z)
+* paged FP8 E4M3:        codes [N_pages, H_kv, P, d] uint8; per-head scales
+                         k_qp, v_qp [H_kv] fp32 (1 when not calibrated)
 * paged INT4 KIVI:       codes [N_pages, H_kv, P, d/2] uint8 (packed);
                          K qparams [N_pages, H_kv, max(1, P/G), d, 2] fp16 held
                          by the page of the group's first token;
@@ -35,7 +37,7 @@ from . import address, quant
 @dataclass
 class Cache:
     layout: str            # "contig" | "paged"
-    fmt: str               # "bf16" | "int8" | "int4_kivi"
+    fmt: str               # "bf16" | "int8" | "fp8_e4m3" | "int4_kivi"
     H_kv: int
     d: int
     P: int = 0
@@ -91,6 +93,9 @@ def read_rows(cache: Cache, b: int, h_kv: int, positions) -> tuple[np.ndarray, n
         v = cache.v[pages, h_kv, rows, :].astype(np.float64) * vq[:, 0:1].astype(np.float64) \
             + vq[:, 1:2].astype(np.float64)
         return k, v
+    if cache.fmt == "fp8_e4m3":
+        return (quant.fp8_head_decode(cache.k[pages, h_kv, rows, :], cache.k_qp[h_kv]),
+                quant.fp8_head_decode(cache.v[pages, h_kv, rows, :], cache.v_qp[h_kv]))
     if cache.fmt == "int4_kivi":
         n_q = quant.kivi_quantized_prefix(int(cache.kv_len[b]), cache.G, cache.R)
         k = np.zeros((pos.size, cache.d))
@@ -123,8 +128,8 @@ def read_rows(cache: Cache, b: int, h_kv: int, positions) -> tuple[np.ndarray, n
 # ---- writers: the oracle's own construction of a paged cache ------------------
 
 def empty_paged(fmt: str, n_pages: int, H_kv: int, P: int, d: int, B: int,
-                G: int = 32, Gv: int = 32, R: int = 128) -> Cache:
-    """Zero-filled pools of the documented shapes."""
+                G: int = 32, Gv: int = 32, R: int = 128, k_scale=None, v_scale=None) -> Cache:
+    """Zero-filled pools of the documented shapes (FP8: with its per-head scales, 1 when None)."""
     c = Cache("paged", fmt, H_kv, d, P=P, G=G, Gv=Gv, R=R)
     if fmt == "bf16":
         c.k = np.zeros((n_pages, H_kv, P, d), np.uint16)
@@ -134,6 +139,11 @@ def empty_paged(fmt: str, n_pages: int, H_kv: int, P: int, d: int, B: int,
         c.v = np.zeros_like(c.k)
         c.k_qp = np.zeros((n_pages, H_kv, P, 2), np.float16)
         c.v_qp = np.zeros_like(c.k_qp)
+    elif fmt == "fp8_e4m3":
+        c.k = np.zeros((n_pages, H_kv, P, d), np.uint8)
+        c.v = np.zeros_like(c.k)
+        c.k_qp = np.ones(H_kv, np.float32) if k_scale is None else np.asarray(k_scale, np.float32)
+        c.v_qp = np.ones(H_kv, np.float32) if v_scale is None else np.asarray(v_scale, np.float32)
     elif fmt == "int4_kivi":
         c.k = np.zeros((n_pages, H_kv, P, d // 2), np.uint8)
         c.v = np.zeros_like(c.k)
@@ -151,7 +161,8 @@ def write_history(cache: Cache, page_indptr, page_indices, rows_indptr, k_bits, 
 
     ``k_bits`` / ``v_bits`` are packed ragged bf16 rows [sum T_b, H_kv, d]
     (rows of request b are rows_indptr[b]:rows_indptr[b+1], §0x04C).
-    INT8 rows are quantised one (token, head) at a time (M8.6 §0x05B); KIVI
+    INT8 rows are quantised one (token, head) at a time (M8.6 §0x05B), FP8 rows
+    with their head's scale (§0x0AA); KIVI
     closes K groups per channel and V rows per token for the first n_q(T_b)
     tokens and keeps the rest as bf16 residual (M8.6 §0x06B).
     """
@@ -180,6 +191,10 @@ def write_history(cache: Cache, page_indptr, page_indices, rows_indptr, k_bits, 
                     codes_pool[pages, h, rows] = codes[:, h]
                     qp_pool[pages, h, rows, 0] = s[:, h]
                     qp_pool[pages, h, rows, 1] = z[:, h]
+        elif cache.fmt == "fp8_e4m3":
+            for h in range(cache.H_kv):
+                cache.k[pages, h, rows] = quant.fp8_head_quantize(quant.bf16_bits_to_f32(kb[:, h]), cache.k_qp[h])
+                cache.v[pages, h, rows] = quant.fp8_head_quantize(quant.bf16_bits_to_f32(vb[:, h]), cache.v_qp[h])
         elif cache.fmt == "int4_kivi":
             G, Gv = cache.G, cache.Gv
             n_q = quant.kivi_quantized_prefix(T, G, cache.R)

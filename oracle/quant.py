@@ -27,6 +27,10 @@ Formats (the reading of the pages that the library documents):
 * INT4 KIVI: the same quantizer with 15 levels.  K: one (s, z) per
   (G-token group, channel).  V: one (s, z) per (token, Gv-channel group).
   Two codes per byte along d, the even channel in the low nibble.
+* FP8 E4M3 with a per-head scale (§0x0A-0x0AA: one scale per K/V head; no
+  calibration means scale 1): code = e4m3(x / s_h), the quotient in fp32
+  (one correctly rounded divide), rounded to the nearest E4M3 value with
+  ties to the even code and saturated to +-448; x_hat = e4m3_value(code) s_h.
 """
 
 from __future__ import annotations
@@ -139,6 +143,58 @@ def unpack_int4(packed) -> np.ndarray:
     out[..., 0::2] = p & 0xF
     out[..., 1::2] = p >> 4
     return out
+
+
+# ---- FP8 E4M3 with a per-head scale (M8.6 §0x0A-0x0AA) -----------------------
+#
+# E4M3 as KV caches use it: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+# bits, no infinities.  Exponent field 0 holds the subnormals m 2^-9; exponent
+# e in 1..15 holds (1 + m/8) 2^(e-7), except exponent 15 with mantissa 7, which
+# is NaN.  The largest finite magnitude is 1.75 2^8 = 448.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Exact float64 value of E4M3 codes (NaN for 0x7F / 0xFF)."""
+    c = np.asarray(codes).astype(np.int64)
+    sign = (c >> 7) & 1
+    e = (c >> 3) & 15
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (c & 7 == 7), np.nan, mag)
+    return np.where(sign == 1, -mag, mag)
+
+
+_E4M3_POS = e4m3_decode(np.arange(127))     # codes 0..126: the finite non-negative values, ascending
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 code of each value, ties to the even code, saturated to +-448; the sign
+    of x is kept (a negative value that rounds to zero gives 0x80).  NaN gives 0x7F."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 126)   # first value >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - a
+    code = np.where(d_lo < d_hi, lo, hi)
+    tie = d_lo == d_hi
+    code = np.where(tie, np.where(lo % 2 == 0, lo, hi), code)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def fp8_head_quantize(x_f32, scale_f32) -> np.ndarray:
+    """Rows [..., d] of one kv head -> E4M3 codes of x / s (the quotient rounded in fp32)."""
+    q = np.asarray(x_f32, dtype=np.float32) / np.float32(scale_f32)
+    return e4m3_encode(q.astype(np.float32))
+
+
+def fp8_head_decode(codes, scale_f32) -> np.ndarray:
+    """x_hat = e4m3_value(code) * s in float64."""
+    return e4m3_decode(codes) * np.float64(np.float32(scale_f32))
 
 
 # ---- byte ledger, M8.6 §0x04A-B ---------------------------------------------

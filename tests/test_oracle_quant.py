@@ -117,3 +117,111 @@ def test_quantized_cache_round_trip():
         O0, L0 = attention.decode_rows(problem, ref, q)
         O1, L1 = attention.decode_rows(problem, c, q)
         assert np.max(np.abs(O1 - O0)) < (0.05 if fmt == "int8" else 0.5)
+
+
+# ---- FP8 E4M3 with a per-head scale (M8.6 §0x0A-0x0AA) -----------------------
+
+def _torch_e4m3():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    return torch
+
+
+def test_e4m3_decode_matches_an_independent_implementation_on_all_codes():
+    """PyTorch's float8_e4m3fn is an implementation of the same format written by others."""
+    torch = _torch_e4m3()
+    codes = np.arange(256)
+    ours = quant.e4m3_decode(codes)
+    theirs = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(theirs))
+    assert np.array_equal(np.nan_to_num(ours), np.nan_to_num(theirs))
+    assert np.array_equal(np.signbit(ours[~np.isnan(ours)]), np.signbit(theirs[~np.isnan(theirs)]))
+
+
+def test_e4m3_decode_closed_forms():
+    dec = quant.e4m3_decode
+    assert dec(0x7E) == 448.0 and dec(0xFE) == -448.0          # 1.75 * 2^8, the largest finite value
+    assert dec(0x01) == 2.0 ** -9 and dec(0x07) == 7 * 2.0 ** -9   # subnormals m 2^-9
+    assert dec(0x08) == 2.0 ** -6                               # smallest normal
+    assert dec(0x38) == 1.0 and dec(0x39) == 1.125               # exponent field 7 is 2^0
+    assert np.isnan(dec(0x7F)) and np.isnan(dec(0xFF))           # no infinities, one NaN pattern
+    assert dec(0x80) == 0.0 and np.signbit(dec(0x80))
+    assert dec(0x77) == 240.0 and dec(0x78) == 256.0             # (1 + 7/8) 2^7, 2^8
+
+
+def test_e4m3_encode_rounds_to_nearest_with_ties_to_even():
+    enc = quant.e4m3_encode
+    u = 2.0 ** -9
+    assert enc(0.5 * u) == 0x00 and enc(1.5 * u) == 0x02 and enc(2.5 * u) == 0x02 and enc(3.5 * u) == 0x04
+    assert enc(0.49 * u) == 0x00 and enc(0.51 * u) == 0x01
+    assert enc(1.0625) == 0x38 and enc(1.1875) == 0x3A          # midpoints of [1, 1.125] and [1.125, 1.25]
+    assert enc(-1.0625) == 0xB8
+    assert enc(-1e-30) == 0x80                                  # the sign survives rounding to zero
+    assert enc(float("nan")) == 0x7F
+
+
+def test_e4m3_encode_saturates_and_agrees_with_torch_below_its_overflow():
+    """Saturation to +-448 (the KV-cache convention); PyTorch instead gives NaN from 464
+    up, so the two are compared on |x| < 464, with every midpoint included."""
+    torch = _torch_e4m3()
+    enc = quant.e4m3_encode
+    assert enc(448.0) == 0x7E and enc(463.9) == 0x7E and enc(1000.0) == 0x7E and enc(-1e9) == 0xFE
+    pos = quant.e4m3_decode(np.arange(127))
+    mids = (pos[:-1] + pos[1:]) / 2
+    rng = np.random.default_rng(30)
+    x = np.concatenate([rng.uniform(-463.9, 463.9, 50000), rng.normal(0, 1, 50000),
+                        rng.normal(0, 1e-3, 20000), mids, -mids, pos, -pos]).astype(np.float32)
+    theirs = torch.tensor(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(enc(x), theirs)
+
+
+def test_e4m3_round_trip_on_every_finite_code():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    assert np.array_equal(quant.e4m3_encode(quant.e4m3_decode(codes)), codes)
+
+
+def test_fp8_head_quantize_divides_in_fp32_then_rounds():
+    torch = _torch_e4m3()
+    rng = np.random.default_rng(31)
+    x = _f32(_bf16(rng, (64, 128)))
+    for s in (1.0, 0.0137, 3.0, 1.7e-3):
+        ours = quant.fp8_head_quantize(x, np.float32(s))
+        q = torch.tensor(x) / torch.tensor(np.float32(s))        # fp32 quotient
+        theirs = q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        inside = np.abs(q.numpy()) < 464.0                       # PyTorch gives NaN beyond
+        assert np.array_equal(ours[inside], theirs[inside])
+        assert np.all(ours[~inside] & 0x7F == 0x7E)               # saturated to +-448
+        err = np.abs(quant.fp8_head_decode(ours, np.float32(s)) - x)
+        ok = np.abs(x) <= 448.0 * np.float32(s)
+        assert np.all(err[ok] <= np.abs(x[ok]) * 2.0 ** -4 + np.float32(s) * 2.0 ** -10)   # half an ulp of 3 bits
+
+
+def test_fp8_cache_round_trip_and_decode_close_to_bf16():
+    rng = np.random.default_rng(32)
+    lens = [300, 129, 40]
+    H, d, P = 2, 64, 16
+    n_pages = [-(-T // P) for T in lens]
+    pool = sum(n_pages) + 2
+    indices = rng.permutation(pool)[:sum(n_pages)]
+    indptr = np.concatenate([[0], np.cumsum(n_pages)])
+    ri = np.concatenate([[0], np.cumsum(lens)])
+    k = _bf16(rng, (ri[-1], H, d))
+    v = _bf16(rng, (ri[-1], H, d))
+    ref = cm.empty_paged("bf16", pool, H, P, d, 3)
+    cm.write_history(ref, indptr, indices, ri, k, v)
+    ks = np.array([0.02, 1.0], np.float32)
+    vs = np.array([1.0, 0.011], np.float32)
+    c = cm.empty_paged("fp8_e4m3", pool, H, P, d, 3, k_scale=ks, v_scale=vs)
+    cm.write_history(c, indptr, indices, ri, k, v)
+    for b, T in enumerate(lens):
+        for h in range(H):
+            K0, V0 = cm.read_rows(ref, b, h, np.arange(T))
+            K1, V1 = cm.read_rows(c, b, h, np.arange(T))
+            assert np.all(np.abs(K1 - K0) <= np.abs(K0) / 16 + ks[h] * 2.0 ** -10)
+            assert np.all(np.abs(V1 - V0) <= np.abs(V0) / 16 + vs[h] * 2.0 ** -10)
+    problem = dict(B=3, S_q=1, H_q=4, H_kv=H, d=d)
+    q = _bf16(rng, (3, 1, 4, d))
+    O0, L0 = attention.decode_rows(problem, ref, q)
+    O1, L1 = attention.decode_rows(problem, c, q)
+    assert np.max(np.abs(O1 - O0)) < 0.05
