@@ -55,7 +55,8 @@ typedef enum {
  *      page_indices[page_indptr[b] + j] at page row t mod P (CSR page list). */
 typedef enum { DATTN_KV_CONTIG_NHD = 0, DATTN_KV_PAGED_HND = 1 } dattn_layout;
 
-/* K/V element formats (M8.6 §0x05B, §0x06A-B).  Paged layout only for INT8/INT4.
+/* K/V element formats (M8.6 §0x05B, §0x06A-B, §0x0A-0x0AA).  Paged layout only for
+ * the quantized formats.
  *  DATTN_FMT_BF16:       K, V bf16.
  *  DATTN_FMT_INT8_TOKEN: K, V uint8 codes [num_pages, H_kv, P, d];
  *      k_qparams, v_qparams fp16 pairs (s, z) [num_pages, H_kv, P, 2], one per
@@ -69,8 +70,17 @@ typedef enum { DATTN_KV_CONTIG_NHD = 0, DATTN_KV_PAGED_HND = 1 } dattn_layout;
  *      k_residual, v_residual bf16 [B, R, H_kv, d]: token t >= n_q(T_b) of
  *      request b sits in slot t mod R, where n_q(T) = G * ceil(max(0, T - R) / G)
  *      (the residual holds at most R rows; its oldest G rows close into a
- *      group while it holds more than R, M8.6 §0x06B). */
-typedef enum { DATTN_FMT_BF16 = 0, DATTN_FMT_INT8_TOKEN = 1, DATTN_FMT_INT4_KIVI = 2 } dattn_format;
+ *      group while it holds more than R, M8.6 §0x06B).
+ *  DATTN_FMT_FP8_E4M3:   K, V uint8 E4M3 codes [num_pages, H_kv, P, d] (sign,
+ *      4 exponent bits with bias 7, 3 mantissa bits; no infinities, 0x7F / 0xFF
+ *      NaN, largest magnitude 448).  k_qparams, v_qparams fp32 [H_kv]: one scale
+ *      per kv head, NULL for 1 (no calibration); x_hat = value(code) * s_h. */
+typedef enum {
+  DATTN_FMT_BF16 = 0,
+  DATTN_FMT_INT8_TOKEN = 1,
+  DATTN_FMT_INT4_KIVI = 2,
+  DATTN_FMT_FP8_E4M3 = 3
+} dattn_format;
 
 /* Visibility programs.  Query row i of request b sits at position
  * p_i = T_b - S_q + i and has frontier F_i = max(0, min(T_b, p_i + 1))
@@ -130,7 +140,7 @@ typedef struct {
   const void* q;                 /* device bf16 [B, S_q, H_q, d]                          */
   const void* k;                 /* device K cache (layout / format above)                */
   const void* v;                 /* device V cache                                        */
-  const void* k_qparams;         /* device, INT8 / INT4 KIVI                              */
+  const void* k_qparams;         /* device, INT8 / INT4 KIVI / FP8 (scales, may be NULL)  */
   const void* v_qparams;
   const void* k_residual;        /* device, INT4 KIVI                                     */
   const void* v_residual;
@@ -292,6 +302,8 @@ size_t kv_append_workspace_bytes(const dattn_problem* prob);
  *    with 15 levels, its V rows per-token (s, z) per Gv channels; rows that
  *    stay inside the residual are written to the residual ring.  The ring must
  *    hold the request's previous residual rows (as this function leaves them).
+ *  - FP8 E4M3: code = nearest E4M3 value to x / s_h (the quotient rounded in
+ *    fp32), ties to the even code, saturated to +-448; the scales are inputs.
  * Capacity (page list long enough for the new length) and arguments are
  * checked on the host before any write.  The caller advances its lengths
  * after the stream reaches this point.  "workspace" (device,

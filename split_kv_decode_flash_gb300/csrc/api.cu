@@ -31,10 +31,13 @@ void check_tensors(const dattn_problem& p, const dattn_tensors* t, bool need_q_o
     c.fail(DATTN_EINVAL, "paged layout needs page_indptr and page_indices");
   if (p.mask == DATTN_MASK_INDEX_LIST && (!t->index_indptr || !t->index_list))
     c.fail(DATTN_EINVAL, "index_list mask needs index_indptr and index_list");
-  if (p.fmt != DATTN_FMT_BF16) {
+  if (p.fmt == DATTN_FMT_INT8_TOKEN || p.fmt == DATTN_FMT_INT4_KIVI) {
     if (!t->k_qparams || !t->v_qparams || !aligned16(t->k_qparams) || !aligned16(t->v_qparams))
-      c.fail(DATTN_EINVAL, "quantized formats need 16-byte aligned k_qparams and v_qparams");
+      c.fail(DATTN_EINVAL, "INT8 and INT4 KIVI need 16-byte aligned k_qparams and v_qparams");
   }
+  if (p.fmt == DATTN_FMT_FP8_E4M3 && ((reinterpret_cast<uintptr_t>(t->k_qparams) % 4) ||
+                                      (reinterpret_cast<uintptr_t>(t->v_qparams) % 4)))
+    c.fail(DATTN_EINVAL, "FP8 scales (k_qparams, v_qparams) must be 4-byte aligned fp32 arrays or NULL");
   if (p.fmt == DATTN_FMT_INT4_KIVI) {
     if (!t->k_residual || !t->v_residual || !aligned16(t->k_residual) || !aligned16(t->v_residual))
       c.fail(DATTN_EINVAL, "INT4 KIVI needs 16-byte aligned k_residual and v_residual");

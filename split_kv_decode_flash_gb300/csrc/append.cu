@@ -15,6 +15,7 @@
 // host before any launch (the append transaction of M4.5 §0x08C).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -98,7 +99,9 @@ __device__ __forceinline__ void load_channels(const __nv_bfloat16* row, int lane
   }
 }
 
-// One warp per (new row, kv head): bf16 copy or INT8 per-token quantisation.
+// One warp per (new row, kv head): bf16 copy, INT8 per-token quantisation, or
+// FP8 E4M3 codes of x / s_h (correctly rounded fp32 quotient, then the
+// hardware's round-to-nearest-even conversion with saturation to +-448).
 template <int D, int FMT>
 __global__ void append_rows_kernel(AppendParams p, int total_rows) {
   constexpr int C = D / 32;
@@ -126,6 +129,21 @@ __global__ void append_rows_kernel(AppendParams p, int total_rows) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(kv ? p.v : p.k) + dst_row;
       if constexpr (C == 4) reinterpret_cast<uint2*>(out)[lane] = reinterpret_cast<const uint2*>(in)[lane];
       else reinterpret_cast<uint32_t*>(out)[lane] = reinterpret_cast<const uint32_t*>(in)[lane];
+    } else if constexpr (FMT == DATTN_FMT_FP8_E4M3) {
+      float x[C];
+      load_channels<C>(in, lane, x);
+      const float* scales = static_cast<const float*>(kv ? p.vqp : p.kqp);
+      const float sh = scales ? scales[h] : 1.f;
+      uint32_t packed = 0;
+#pragma unroll
+      for (int c = 0; c < C; c += 2) {
+        const __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(x[c], sh), __fdiv_rn(x[c + 1], sh)), __NV_SATFINITE, __NV_E4M3);
+        packed |= static_cast<uint32_t>(two) << (8 * c);
+      }
+      uint8_t* codes = static_cast<uint8_t*>(kv ? p.v : p.k) + dst_row;
+      if constexpr (C == 4) reinterpret_cast<uint32_t*>(codes)[lane] = packed;
+      else reinterpret_cast<uint16_t*>(codes)[lane] = static_cast<uint16_t>(packed);
     } else {
       float x[C];
       load_channels<C>(in, lane, x);
@@ -298,8 +316,8 @@ extern "C" dattn_status kv_append(const dattn_problem* prob, const dattn_append_
   const bool paged = p.layout == DATTN_KV_PAGED_HND;
   if (paged && (!in->page_indptr || !cache->page_indptr || !cache->page_indices))
     c.fail(DATTN_EINVAL, "paged cache needs host and device page_indptr and device page_indices");
-  if (p.fmt != DATTN_FMT_BF16 && (!cache->k_qparams || !cache->v_qparams))
-    c.fail(DATTN_EINVAL, "quantized formats need k_qparams and v_qparams");
+  if ((p.fmt == DATTN_FMT_INT8_TOKEN || p.fmt == DATTN_FMT_INT4_KIVI) && (!cache->k_qparams || !cache->v_qparams))
+    c.fail(DATTN_EINVAL, "INT8 and INT4 KIVI need k_qparams and v_qparams");
   if (p.fmt == DATTN_FMT_INT4_KIVI && (!cache->k_residual || !cache->v_residual))
     c.fail(DATTN_EINVAL, "INT4 KIVI needs k_residual and v_residual");
   const size_t need = kv_append_workspace_bytes(prob);
@@ -390,6 +408,9 @@ extern "C" dattn_status kv_append(const dattn_problem* prob, const dattn_append_
   } else if (p.fmt == DATTN_FMT_INT8_TOKEN) {
     err = d128 ? launch_warps(append_rows_kernel<128, DATTN_FMT_INT8_TOKEN>, new_indptr[B] * H, s, a, new_indptr[B])
                : launch_warps(append_rows_kernel<64, DATTN_FMT_INT8_TOKEN>, new_indptr[B] * H, s, a, new_indptr[B]);
+  } else if (p.fmt == DATTN_FMT_FP8_E4M3) {
+    err = d128 ? launch_warps(append_rows_kernel<128, DATTN_FMT_FP8_E4M3>, new_indptr[B] * H, s, a, new_indptr[B])
+               : launch_warps(append_rows_kernel<64, DATTN_FMT_FP8_E4M3>, new_indptr[B] * H, s, a, new_indptr[B]);
   } else {
     const int groups = work_indptr[B], rows = res_indptr[B];
     err = d128 ? launch_warps(kivi_close_kernel<128>, groups * H, s, a, groups)

@@ -1,5 +1,8 @@
-// Partial kernel of split-KV decode attention for INT8 per-token K/V
-// ("M8.6 Live-Data Quantization", §0x05B format), on the tensor cores.
+// Partial kernel of split-KV decode attention for byte-code K/V on the tensor
+// cores: INT8 per-token ("M8.6 Live-Data Quantization", §0x05B format) and
+// FP8 E4M3 with a per-head scale (§0x0A-0x0AA).  FP8 codes become exact f16
+// values with one cvt per pair and have no offset, so their (s, z) are the
+// head's scale and zero, and the 1024 bias below is zero.
 //
 // Same persistent producer / consumer structure as the bf16 kernel (item
 // records in shared memory, four producer warps with a three-step slot
@@ -63,11 +66,32 @@ struct Q8 {
   static_assert(kTotal <= 232448, "shared memory of one CTA");
 };
 
-// Two bytes of w as an f16 pair (1024 + byte each): sel picks them, e.g.
-// 0x4140 bytes 0 and 1, 0x4342 bytes 2 and 3, 0x4240 bytes 0 and 2.
-__device__ __forceinline__ uint32_t biased_f16x2(uint32_t w, uint32_t sel) {
-  return __byte_perm(w, 0x64646464u, sel);
-}
+// Two code bytes of w as an f16 pair; sel names them like a prmt selector:
+// 0x4140 bytes 0 and 1, 0x4342 bytes 2 and 3, 0x4240 bytes 0 and 2, 0x4341
+// bytes 1 and 3.  INT8: 1024 + byte each (exact), with kBias = 1024 to
+// remove.  FP8 E4M3: the byte's value, exact in f16 (cvt.rn.f16x2.e4m3x2).
+template <int FMT>
+struct Codes;
+
+template <>
+struct Codes<DATTN_FMT_INT8_TOKEN> {
+  static constexpr float kBias = 1024.f;
+  static __device__ __forceinline__ uint32_t pair(uint32_t w, uint32_t sel) {
+    return __byte_perm(w, 0x64646464u, sel);
+  }
+};
+
+template <>
+struct Codes<DATTN_FMT_FP8_E4M3> {
+  static constexpr float kBias = 0.f;
+  static __device__ __forceinline__ uint32_t pair(uint32_t w, uint32_t sel) {
+    // the two bytes as the low half of a word: byte A (sel nibble 0) low, byte B (nibble 2) high
+    const uint32_t b = sel == 0x4140u ? w : sel == 0x4342u ? w >> 16 : __byte_perm(w, 0u, (sel & 0xFu) | ((sel >> 4) & 0xF0u));
+    uint32_t d;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %1; cvt.rn.f16x2.e4m3x2 %0, lo; }" : "=r"(d) : "r"(b));
+    return d;
+  }
+};
 
 __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
@@ -75,7 +99,7 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
 
 // ---- producer ---------------------------------------------------------------------------
 
-template <int D>
+template <int D, int FMT>
 __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
   using C = Q8<D>;
   const PartialParams& p = w.p;
@@ -128,13 +152,15 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool 
       cp_async16(kt + dst, kbase + off, ok ? 16u : 0u, stream_pol);
       cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
     }
+    if constexpr (FMT == DATTN_FMT_INT8_TOKEN) {   // per-token (s, z); FP8 has per-head scales
 #pragma unroll
-    for (int h = 0; h < kQS; ++h) {
-      const uint32_t row = r0.row[h];
-      const bool ok = row != kNoRow;
-      const size_t off = static_cast<size_t>(ok ? row : 0u) * 4;
-      cp_async4(kq + 4 * (lane + 32 * h), kqbase + off, ok ? 4u : 0u);
-      cp_async4(vq + 4 * (lane + 32 * h), vqbase + off, ok ? 4u : 0u);
+      for (int h = 0; h < kQS; ++h) {
+        const uint32_t row = r0.row[h];
+        const bool ok = row != kNoRow;
+        const size_t off = static_cast<size_t>(ok ? row : 0u) * 4;
+        cp_async4(kq + 4 * (lane + 32 * h), kqbase + off, ok ? 4u : 0u);
+        cp_async4(vq + 4 * (lane + 32 * h), vqbase + off, ok ? 4u : 0u);
+      }
     }
     const uint32_t fb = full0 + 8 * st;
     cp_async_mbar_arrive(fb);
@@ -249,7 +275,7 @@ __device__ __forceinline__ void emit_row_q8(const PartialParams& p, const WorkIt
   }
 }
 
-template <int D>
+template <int D, int FMT>
 __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
   using C = Q8<D>;
   constexpr int KS = D / 16;   // k-steps of q.k
@@ -282,6 +308,11 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
     const QRows<D> q = qn;
     if (ii + 1 < w.end) load_q8<D>(p, w.rec(ii + 1).it, r0, r1, t4, qn);
+    float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given)
+    if constexpr (FMT == DATTN_FMT_FP8_E4M3) {
+      if (p.kqp) hk = static_cast<const float*>(p.kqp)[it.h];
+      if (p.vqp) hv = static_cast<const float*>(p.vqp)[it.h];
+    }
     float o[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -325,7 +356,7 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
             ldsm_x4(kt + tile_off<D>(base + nt * 8 + lrow, 4 * m + lmat), r[0], r[1], r[2], r[3]);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              mma_f16(s[nt], q.a[4 * m + i], biased_f16x2(r[i], 0x4140u), biased_f16x2(r[i], 0x4342u));
+              mma_f16(s[nt], q.a[4 * m + i], Codes<FMT>::pair(r[i], 0x4140u), Codes<FMT>::pair(r[i], 0x4342u));
           }
         }
         // per-token K scale outside the dot, log2 units, -inf where masked
@@ -336,11 +367,11 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
           for (int e = 0; e < 2; ++e) {
             const int slot = base + nt * 8 + 2 * t4 + e;
             const int t = pos[slot];
-            const float2 ks = half2_bits_to_float2(kqp[slot]);
-            const float2 vq = half2_bits_to_float2(vqp[slot]);
+            const float2 ks = FMT == DATTN_FMT_INT8_TOKEN ? half2_bits_to_float2(kqp[slot]) : make_float2(hk, 0.f);
+            const float2 vq = FMT == DATTN_FMT_INT8_TOKEN ? half2_bits_to_float2(vqp[slot]) : make_float2(hv, 0.f);
             vs[nt][e] = vq.x;
             vz[nt][e] = vq.y;
-            const float off = fmaf(-1024.f, ks.x, ks.y);
+            const float off = fmaf(-Codes<FMT>::kBias, ks.x, ks.y);
             const bool v0 = t >= 0 && ok0 && (full || key_visible(mc, qi0, t));
             const bool v1 = t >= 0 && ok1 && (full || key_visible(mc, qi1, t));
             s[nt][e] = v0 ? sc * fmaf(ks.x * q.fac0, s[nt][e], off * q.qsum0) : -INFINITY;
@@ -399,8 +430,8 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {          // chunk 2 c2 + h: v[2 h] keys 0-7, v[2 h + 1] keys 8-15
             const int C = 2 * c2 + h;
-            mma_f16(o[2 * C], pa, biased_f16x2(v[2 * h], 0x4240u), biased_f16x2(v[2 * h + 1], 0x4240u));
-            mma_f16(o[2 * C + 1], pa, biased_f16x2(v[2 * h], 0x4341u), biased_f16x2(v[2 * h + 1], 0x4341u));
+            mma_f16(o[2 * C], pa, Codes<FMT>::pair(v[2 * h], 0x4240u), Codes<FMT>::pair(v[2 * h + 1], 0x4240u));
+            mma_f16(o[2 * C + 1], pa, Codes<FMT>::pair(v[2 * h], 0x4341u), Codes<FMT>::pair(v[2 * h + 1], 0x4341u));
           }
         }
       }
@@ -420,8 +451,8 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
       b1 += __shfl_xor_sync(kAll, b1, x);
     }
     if (!dead) {
-      if (ok0) emit_row_q8<D>(p, it, my_state, r0, m0, l0, z0, 1024.f * b0, o, 0, t4);
-      if (ok1) emit_row_q8<D>(p, it, my_state, r1, m1, l1, z1, 1024.f * b1, o, 1, t4);
+      if (ok0) emit_row_q8<D>(p, it, my_state, r0, m0, l0, z0, Codes<FMT>::kBias * b0, o, 0, t4);
+      if (ok1) emit_row_q8<D>(p, it, my_state, r1, m1, l1, z1, Codes<FMT>::kBias * b1, o, 1, t4);
     }
   }
 }
@@ -490,7 +521,7 @@ __device__ __forceinline__ void load_q8_cols(const PartialParams& p, const WorkI
   q.fac1 = __shfl_sync(kAll, fac, 8 * t4 + 4);
 }
 
-template <int D>
+template <int D, int FMT>
 __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) {
   using C = Q8<D>;
   constexpr int KS = D / 16;   // k-steps of q.k
@@ -521,6 +552,11 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
     const QCols<D> q = qn;
     if (ii + 1 < w.end) load_q8_cols<D>(p, w.rec(ii + 1).it, g4, t4, qn);
+    float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given)
+    if constexpr (FMT == DATTN_FMT_FP8_E4M3) {
+      if (p.kqp) hk = static_cast<const float*>(p.kqp)[it.h];
+      if (p.vqp) hv = static_cast<const float*>(p.vqp)[it.h];
+    }
     float o[NC][4];
 #pragma unroll
     for (int n = 0; n < NC; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -563,17 +599,20 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
           ldsm_x4(kt + tile_off<D>(base + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1], v[2], v[3]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint32_t a[4] = {biased_f16x2(v[2 * h], 0x4140u), biased_f16x2(v[2 * h + 1], 0x4140u),
-                                   biased_f16x2(v[2 * h], 0x4342u), biased_f16x2(v[2 * h + 1], 0x4342u)};
+            const uint32_t a[4] = {Codes<FMT>::pair(v[2 * h], 0x4140u), Codes<FMT>::pair(v[2 * h + 1], 0x4140u),
+                                   Codes<FMT>::pair(v[2 * h], 0x4342u), Codes<FMT>::pair(v[2 * h + 1], 0x4342u)};
             mma_f16(s, a, q.b[2 * c2 + h][0], q.b[2 * c2 + h][1]);
           }
         }
         // keys g4 (s0, s1) and g4 + 8 (s2, s3); rows ra (s0, s2), rb (s1, s3)
         const int kx = base + g4, ky = base + g4 + 8;
         const int tx = pos[kx], ty = pos[ky];
-        const float2 ksx = half2_bits_to_float2(kqp[kx]), ksy = half2_bits_to_float2(kqp[ky]);
-        const float2 vqx = half2_bits_to_float2(vqp[kx]), vqy = half2_bits_to_float2(vqp[ky]);
-        const float offx = fmaf(-1024.f, ksx.x, ksx.y), offy = fmaf(-1024.f, ksy.x, ksy.y);
+        constexpr bool kI8 = FMT == DATTN_FMT_INT8_TOKEN;
+        const float2 ksx = kI8 ? half2_bits_to_float2(kqp[kx]) : make_float2(hk, 0.f);
+        const float2 ksy = kI8 ? half2_bits_to_float2(kqp[ky]) : make_float2(hk, 0.f);
+        const float2 vqx = kI8 ? half2_bits_to_float2(vqp[kx]) : make_float2(hv, 0.f);
+        const float2 vqy = kI8 ? half2_bits_to_float2(vqp[ky]) : make_float2(hv, 0.f);
+        const float offx = fmaf(-Codes<FMT>::kBias, ksx.x, ksx.y), offy = fmaf(-Codes<FMT>::kBias, ksy.x, ksy.y);
         const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
         const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
         const bool vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
@@ -623,8 +662,8 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
           ldsm_x4_trans(vt + tile_off<D>(base + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1], v[2], v[3]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint32_t a[4] = {biased_f16x2(v[2 * h], 0x4240u), biased_f16x2(v[2 * h], 0x4341u),
-                                   biased_f16x2(v[2 * h + 1], 0x4240u), biased_f16x2(v[2 * h + 1], 0x4341u)};
+            const uint32_t a[4] = {Codes<FMT>::pair(v[2 * h], 0x4240u), Codes<FMT>::pair(v[2 * h], 0x4341u),
+                                   Codes<FMT>::pair(v[2 * h + 1], 0x4240u), Codes<FMT>::pair(v[2 * h + 1], 0x4341u)};
             mma_f16(o[2 * c2 + h], a, pb0, pb1);
           }
         }
@@ -650,7 +689,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
         const int row = rr ? rb : ra;
         if (!(rr ? okb : oka)) continue;
         const float m = rr ? mb : ma, l = rr ? lb : la;
-        const float add = (rr ? zb : za) - 1024.f * (rr ? bb : ba);
+        const float add = (rr ? zb : za) - Codes<FMT>::kBias * (rr ? bb : ba);
         const int i = row / p.g, hq = it.h * p.g + row % p.g;
         const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
         if (it.slot < 0) {
@@ -674,7 +713,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
   }
 }
 
-template <int D>
+template <int D, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_constant__ PartialParams p) {
   using C = Q8<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -699,26 +738,26 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ8ProducerRegs));
-    produce_q8<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    produce_q8<D, FMT>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ8ConsumerRegs));
   dependency_wait(!complete_now);   // before Q and the state writes
-  if (p.rows <= 8) consume_q8_swap<D>(w, smem, warp, lane);
-  else consume_q8<D>(w, smem, warp, lane);
+  if (p.rows <= 8) consume_q8_swap<D, FMT>(w, smem, warp, lane);
+  else consume_q8<D, FMT>(w, smem, warp, lane);
 }
 
-template <int D>
+template <int D, int FMT>
 int launch_q8(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Q8<D>::kTotal;
   cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, partial_q8_kernel<D>);
+  cudaError_t err = cudaFuncGetAttributes(&attr, partial_q8_kernel<D, FMT>);
   if (err != cudaSuccess) return err;
   // the consumers' setmaxnreg.inc waits for registers the producer warpgroup
   // releases; it can only complete if the launch holds them
   if (attr.numRegs * kThreads < 128 * kQ8ProducerRegs + 32 * kConsumerWarps * kQ8ConsumerRegs)
     return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(partial_q8_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  err = cudaFuncSetAttribute(partial_q8_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
@@ -730,14 +769,18 @@ int launch_q8(const PartialParams& p, int n_ctas, void* stream) {
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, partial_q8_kernel<D>, p);
+  err = cudaLaunchKernelEx(&cfg, partial_q8_kernel<D, FMT>, p);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace
 
 int launch_partial_q8(const PartialParams& p, int d, int n_ctas, void* stream) {
-  return d == 64 ? launch_q8<64>(p, n_ctas, stream) : launch_q8<128>(p, n_ctas, stream);
+  if (p.fmt == DATTN_FMT_FP8_E4M3)
+    return d == 64 ? launch_q8<64, DATTN_FMT_FP8_E4M3>(p, n_ctas, stream)
+                   : launch_q8<128, DATTN_FMT_FP8_E4M3>(p, n_ctas, stream);
+  return d == 64 ? launch_q8<64, DATTN_FMT_INT8_TOKEN>(p, n_ctas, stream)
+                 : launch_q8<128, DATTN_FMT_INT8_TOKEN>(p, n_ctas, stream);
 }
 
 }  // namespace dattn

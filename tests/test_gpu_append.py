@@ -27,7 +27,7 @@ def _cuda():
     dattn.load()
 
 
-def _alloc(fmt, p, n_pages, B, dev="cuda"):
+def _alloc(fmt, p, n_pages, B, dev="cuda", scales=None):
     H, P, d = p["H_kv"], p["P"], p["d"]
     G, Gv, R = p["kivi_group"], p["kivi_v_group"], p["kivi_residual"]
     out = {}
@@ -39,6 +39,12 @@ def _alloc(fmt, p, n_pages, B, dev="cuda"):
         out["v"] = torch.zeros_like(out["k"])
         out["k_qparams"] = torch.zeros((n_pages, H, P, 2), dtype=torch.float16, device=dev)
         out["v_qparams"] = torch.zeros_like(out["k_qparams"])
+    elif fmt == "fp8_e4m3":
+        out["k"] = torch.zeros((n_pages, H, P, d), dtype=torch.uint8, device=dev)
+        out["v"] = torch.zeros_like(out["k"])
+        if scales is not None:
+            out["k_qparams"] = scales[0].to(dev, torch.float32).contiguous()
+            out["v_qparams"] = scales[1].to(dev, torch.float32).contiguous()
     else:
         out["k"] = torch.zeros((n_pages, H, P, d // 2), dtype=torch.uint8, device=dev)
         out["v"] = torch.zeros_like(out["k"])
@@ -53,7 +59,8 @@ def append_history(w, fmt, cuts_per_request):
     """kv_append the workload's packed history in pieces; returns the device cache dict."""
     p = dict(w.problem, fmt=fmt)
     B = p["B"]
-    cache = _alloc(fmt, p, p["num_pages"], B)
+    scales = (w.meta["k_scale"], w.meta["v_scale"]) if fmt == "fp8_e4m3" and "k_scale" in w.meta else None
+    cache = _alloc(fmt, p, p["num_pages"], B, scales=scales)
     cache["page_indptr"] = w.page_indptr.cuda()
     cache["page_indices"] = w.page_indices.cuda()
     ws = torch.empty(dattn.kv_append_workspace_bytes(p), dtype=torch.uint8, device="cuda")
@@ -83,10 +90,18 @@ def append_history(w, fmt, cuts_per_request):
     return p, cache
 
 
+def fp8_scales(w):
+    """The FP8 per-head scales the workload's cache uses (None: 1, no calibration)."""
+    if "k_scale" not in w.meta:
+        return None, None
+    return w.meta["k_scale"].numpy(), w.meta["v_scale"].numpy()
+
+
 def oracle_written(w, fmt):
     p = w.problem
+    ks, vs = fp8_scales(w)
     c = ocache.empty_paged(fmt, p["num_pages"], p["H_kv"], p["P"], p["d"], p["B"], G=p["kivi_group"],
-                           Gv=p["kivi_v_group"], R=p["kivi_residual"])
+                           Gv=p["kivi_v_group"], R=p["kivi_residual"], k_scale=ks, v_scale=vs)
     ocache.write_history(c, w.page_indptr.numpy(), w.page_indices.numpy(), w.rows_indptr.numpy(),
                          bits(w.k_rows), bits(w.v_rows))
     return c
@@ -136,6 +151,29 @@ def test_int8_append_codes_and_qparams_bit_exact(d):
         assert np.array_equal(vq[pg, :, r], ref.v_qp[pg, :, r])
         assert np.array_equal(kc[pg, :, r], ref.k[pg, :, r])
         assert np.array_equal(vc[pg, :, r], ref.v[pg, :, r])
+
+
+@pytest.mark.parametrize("d,scales", [(128, "calibrated"), (64, "calibrated"), (128, "none"), (128, "tight")])
+def test_fp8_append_codes_bit_exact(d, scales):
+    """E4M3 codes of x / s_h: calibrated scales, no scales (1), and scales a quarter of the
+    calibrated ones, so that a quarter of the range saturates to +-448."""
+    w = W.quantized_history("fp8", B=3, S_q=1, H_q=8, H_kv=2, d=d, lens=[333, 1, 96], P=16, seed=15,
+                            device="cuda", fmt="fp8_e4m3", pool_pages=40)
+    if scales == "none":
+        del w.meta["k_scale"], w.meta["v_scale"]
+    elif scales == "tight":
+        w.meta["k_scale"] = w.meta["k_scale"] / 4
+        w.meta["v_scale"] = w.meta["v_scale"] / 4
+    p, cache = append_history(w, "fp8_e4m3", _cuts(w.kv_len.tolist(), np.random.default_rng(3)))
+    ref = oracle_written(w, "fp8_e4m3")
+    kc, vc = cache["k"].cpu().numpy(), cache["v"].cpu().numpy()
+    n_sat = 0
+    for b, t, pg, r in _visible_rows(w):
+        assert np.array_equal(kc[pg, :, r], ref.k[pg, :, r])
+        assert np.array_equal(vc[pg, :, r], ref.v[pg, :, r])
+        n_sat += int(np.sum((kc[pg, :, r] & 0x7F) == 0x7E))
+    # calibrated: only each head's largest |x| meets 448; tight: a quarter of the range saturates
+    assert n_sat >= 100 if scales == "tight" else n_sat < 20
 
 
 @pytest.mark.parametrize("d,P", [(128, 16), (64, 16), (128, 64)])

@@ -174,9 +174,14 @@ def quantized_history(name, *, B, S_q, H_q, H_kv, d, lens, P, seed, device, fmt,
     problem = dict(B=B, S_q=S_q, H_q=H_q, H_kv=H_kv, d=d, layout="paged", fmt=fmt, P=P,
                    num_pages=pool_pages, mask="causal", kivi_group=32, kivi_v_group=32,
                    kivi_residual=128)
+    meta_out = {"outlier_channels": och, "seed": seed}
+    if fmt == "fp8_e4m3":
+        # per-head scales from a calibration pass over the history: max |x| / 448 (fp32)
+        meta_out["k_scale"] = (k_rows.float().abs().amax(dim=(0, 2)) / 448.0).cpu()
+        meta_out["v_scale"] = (v_rows.float().abs().amax(dim=(0, 2)) / 448.0).cpu()
     return Workload(name, problem, q, torch.tensor(lens, dtype=torch.int32),
                     page_indptr=indptr, page_indices=indices, rows_indptr=rows_indptr,
-                    k_rows=k_rows, v_rows=v_rows, meta={"outlier_channels": och, "seed": seed})
+                    k_rows=k_rows, v_rows=v_rows, meta=meta_out)
 
 
 def h2o_index_lists(lens, H_kv, budget, n_sink, n_recent, meta):
