@@ -15,7 +15,7 @@ Layouts (element order, outermost first):
   j lives in page indices[indptr[b] + j]                               (§0x04D)
 * paged INT8:            codes [N_pages, H_kv, P, d] uint8;
                          qparams [N_pages, H_kv, P, 2] fp16 (s, z)
-* paged FP8 E4M3:        codes [N_pages, H_kv, P, d] uint8; per-head scales
+* paged FP8 E4M3 / E5M2: codes [N_pages, H_kv, P, d] uint8; per-head scales
                          k_qp, v_qp [H_kv] fp32 (1 when not calibrated)
 * paged INT4 KIVI:       codes [N_pages, H_kv, P, d/2] uint8 (packed);
                          K qparams [N_pages, H_kv, max(1, P/G), d, 2] fp16 held
@@ -37,7 +37,7 @@ from . import address, quant
 @dataclass
 class Cache:
     layout: str            # "contig" | "paged"
-    fmt: str               # "bf16" | "int8" | "fp8_e4m3" | "int4_kivi"
+    fmt: str               # "bf16" | "int8" | "fp8_e4m3" | "fp8_e5m2" | "int4_kivi"
     H_kv: int
     d: int
     P: int = 0
@@ -93,9 +93,9 @@ def read_rows(cache: Cache, b: int, h_kv: int, positions) -> tuple[np.ndarray, n
         v = cache.v[pages, h_kv, rows, :].astype(np.float64) * vq[:, 0:1].astype(np.float64) \
             + vq[:, 1:2].astype(np.float64)
         return k, v
-    if cache.fmt == "fp8_e4m3":
-        return (quant.fp8_head_decode(cache.k[pages, h_kv, rows, :], cache.k_qp[h_kv]),
-                quant.fp8_head_decode(cache.v[pages, h_kv, rows, :], cache.v_qp[h_kv]))
+    if cache.fmt in quant.FP8_FORMATS:
+        return (quant.fp8_head_decode(cache.k[pages, h_kv, rows, :], cache.k_qp[h_kv], cache.fmt),
+                quant.fp8_head_decode(cache.v[pages, h_kv, rows, :], cache.v_qp[h_kv], cache.fmt))
     if cache.fmt == "int4_kivi":
         n_q = quant.kivi_quantized_prefix(int(cache.kv_len[b]), cache.G, cache.R)
         k = np.zeros((pos.size, cache.d))
@@ -139,7 +139,7 @@ def empty_paged(fmt: str, n_pages: int, H_kv: int, P: int, d: int, B: int,
         c.v = np.zeros_like(c.k)
         c.k_qp = np.zeros((n_pages, H_kv, P, 2), np.float16)
         c.v_qp = np.zeros_like(c.k_qp)
-    elif fmt == "fp8_e4m3":
+    elif fmt in quant.FP8_FORMATS:
         c.k = np.zeros((n_pages, H_kv, P, d), np.uint8)
         c.v = np.zeros_like(c.k)
         c.k_qp = np.ones(H_kv, np.float32) if k_scale is None else np.asarray(k_scale, np.float32)
@@ -191,10 +191,12 @@ def write_history(cache: Cache, page_indptr, page_indices, rows_indptr, k_bits, 
                     codes_pool[pages, h, rows] = codes[:, h]
                     qp_pool[pages, h, rows, 0] = s[:, h]
                     qp_pool[pages, h, rows, 1] = z[:, h]
-        elif cache.fmt == "fp8_e4m3":
+        elif cache.fmt in quant.FP8_FORMATS:
             for h in range(cache.H_kv):
-                cache.k[pages, h, rows] = quant.fp8_head_quantize(quant.bf16_bits_to_f32(kb[:, h]), cache.k_qp[h])
-                cache.v[pages, h, rows] = quant.fp8_head_quantize(quant.bf16_bits_to_f32(vb[:, h]), cache.v_qp[h])
+                cache.k[pages, h, rows] = quant.fp8_head_quantize(quant.bf16_bits_to_f32(kb[:, h]),
+                                                                  cache.k_qp[h], cache.fmt)
+                cache.v[pages, h, rows] = quant.fp8_head_quantize(quant.bf16_bits_to_f32(vb[:, h]),
+                                                                  cache.v_qp[h], cache.fmt)
         elif cache.fmt == "int4_kivi":
             G, Gv = cache.G, cache.Gv
             n_q = quant.kivi_quantized_prefix(T, G, cache.R)

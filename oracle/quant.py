@@ -31,6 +31,7 @@ Formats (the reading of the pages that the library documents):
   calibration means scale 1): code = e4m3(x / s_h), the quotient in fp32
   (one correctly rounded divide), rounded to the nearest E4M3 value with
   ties to the even code and saturated to +-448; x_hat = e4m3_value(code) s_h.
+  FP8 E5M2 the same way, saturated to +-57344.
 """
 
 from __future__ import annotations
@@ -186,15 +187,62 @@ def e4m3_encode(x) -> np.ndarray:
     return code.astype(np.uint8)
 
 
-def fp8_head_quantize(x_f32, scale_f32) -> np.ndarray:
-    """Rows [..., d] of one kv head -> E4M3 codes of x / s (the quotient rounded in fp32)."""
+# E5M2: 1 sign bit, 5 exponent bits with bias 15, 2 mantissa bits (the upper
+# byte of an IEEE half).  Exponent field 0 holds the subnormals m 2^-16; 31 holds
+# infinity (mantissa 0) and NaN.  The largest finite magnitude is 1.75 2^15.
+
+E5M2_MAX = 57344.0
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    """Exact float64 value of E5M2 codes (+-inf for 0x7C / 0xFC, NaN for the rest of exponent 31)."""
+    c = np.asarray(codes).astype(np.int64)
+    sign = (c >> 7) & 1
+    e = (c >> 2) & 31
+    m = (c & 3).astype(np.float64)
+    mag = np.where(e == 0, m * 2.0 ** -16, (1.0 + m / 4.0) * np.exp2(e.astype(np.float64) - 15.0))
+    mag = np.where(e == 31, np.where(c & 3 == 0, np.inf, np.nan), mag)
+    return np.where(sign == 1, -mag, mag)
+
+
+_E5M2_POS = e5m2_decode(np.arange(124))     # codes 0..123: the finite non-negative values, ascending
+
+
+def _nearest_code(x, table, top: float, nan_code: int) -> np.ndarray:
+    """Nearest code of |x| in an ascending table of finite values, ties to the even code,
+    saturated to the table's top value; sign bit from x; NaN to nan_code."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), top)
+    last = len(table) - 1
+    hi = np.clip(np.searchsorted(table, a, side="left"), 0, last)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - table[lo]
+    d_hi = table[hi] - a
+    code = np.where(d_lo < d_hi, lo, hi)
+    code = np.where(d_lo == d_hi, np.where(lo % 2 == 0, lo, hi), code)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    code = np.where(np.isnan(x), nan_code, code)
+    return code.astype(np.uint8)
+
+
+def e5m2_encode(x) -> np.ndarray:
+    """Nearest E5M2 code, ties to the even code, saturated to +-57344 (infinities included);
+    the sign of x is kept.  NaN gives 0x7F."""
+    return _nearest_code(x, _E5M2_POS, E5M2_MAX, 0x7F)
+
+
+FP8_FORMATS = {"fp8_e4m3": (e4m3_encode, e4m3_decode), "fp8_e5m2": (e5m2_encode, e5m2_decode)}
+
+
+def fp8_head_quantize(x_f32, scale_f32, fmt: str = "fp8_e4m3") -> np.ndarray:
+    """Rows [..., d] of one kv head -> FP8 codes of x / s (the quotient rounded in fp32)."""
     q = np.asarray(x_f32, dtype=np.float32) / np.float32(scale_f32)
-    return e4m3_encode(q.astype(np.float32))
+    return FP8_FORMATS[fmt][0](q.astype(np.float32))
 
 
-def fp8_head_decode(codes, scale_f32) -> np.ndarray:
-    """x_hat = e4m3_value(code) * s in float64."""
-    return e4m3_decode(codes) * np.float64(np.float32(scale_f32))
+def fp8_head_decode(codes, scale_f32, fmt: str = "fp8_e4m3") -> np.ndarray:
+    """x_hat = value(code) * s in float64."""
+    return FP8_FORMATS[fmt][1](codes) * np.float64(np.float32(scale_f32))
 
 
 # ---- byte ledger, M8.6 §0x04A-B ---------------------------------------------

@@ -225,3 +225,76 @@ def test_fp8_cache_round_trip_and_decode_close_to_bf16():
     O0, L0 = attention.decode_rows(problem, ref, q)
     O1, L1 = attention.decode_rows(problem, c, q)
     assert np.max(np.abs(O1 - O0)) < 0.05
+
+
+def _torch_e5m2():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e5m2"):
+        pytest.skip("torch without float8_e5m2")
+    return torch
+
+
+def test_e5m2_decode_matches_an_independent_implementation_on_all_codes():
+    torch = _torch_e5m2()
+    codes = np.arange(256)
+    ours = quant.e5m2_decode(codes)
+    theirs = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e5m2).double().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(theirs))
+    fin = ~np.isnan(ours)
+    assert np.array_equal(ours[fin], theirs[fin])
+    assert np.array_equal(np.signbit(ours[fin]), np.signbit(theirs[fin]))
+
+
+def test_e5m2_decode_closed_forms():
+    dec = quant.e5m2_decode
+    assert dec(0x7B) == 57344.0 and dec(0xFB) == -57344.0        # 1.75 * 2^15
+    assert dec(0x7C) == np.inf and dec(0xFC) == -np.inf
+    assert np.isnan(dec(0x7D)) and np.isnan(dec(0x7F))
+    assert dec(0x01) == 2.0 ** -16 and dec(0x03) == 3 * 2.0 ** -16   # subnormals m 2^-16
+    assert dec(0x04) == 2.0 ** -14 and dec(0x3C) == 1.0 and dec(0x3D) == 1.25
+    # an E5M2 code is the upper byte of the IEEE half with the same value
+    fin = [c for c in range(256) if (c >> 2) & 31 != 31]
+    halves = (np.array(fin, np.uint16) << 8).view(np.float16).astype(np.float64)
+    assert np.array_equal(dec(np.array(fin)), halves)
+
+
+def test_e5m2_encode_ties_saturation_and_agreement_below_overflow():
+    torch = _torch_e5m2()
+    enc = quant.e5m2_encode
+    u = 2.0 ** -16
+    assert enc(0.5 * u) == 0x00 and enc(1.5 * u) == 0x02 and enc(2.5 * u) == 0x02
+    assert enc(1.125) == 0x3C and enc(1.375) == 0x3E           # ties to the even code
+    assert enc(57344.0) == 0x7B and enc(1e6) == 0x7B and enc(np.inf) == 0x7B and enc(-np.inf) == 0xFB
+    pos = quant.e5m2_decode(np.arange(124))
+    mids = (pos[:-1] + pos[1:]) / 2
+    rng = np.random.default_rng(33)
+    x = np.concatenate([rng.uniform(-61000, 61000, 50000), rng.normal(0, 1, 50000),
+                        rng.normal(0, 1e-4, 20000), mids, -mids, pos, -pos]).astype(np.float32)
+    theirs = torch.tensor(x).to(torch.float8_e5m2).view(torch.uint8).numpy()   # overflows to inf past 61440
+    assert np.array_equal(enc(x), theirs)
+    codes = np.array([c for c in range(256) if (c >> 2) & 31 != 31], np.uint8)
+    assert np.array_equal(enc(quant.e5m2_decode(codes)), codes)
+
+
+def test_fp8_e5m2_cache_decode_close_to_bf16():
+    rng = np.random.default_rng(34)
+    lens = [200, 33]
+    H, d, P = 2, 64, 16
+    n_pages = [-(-T // P) for T in lens]
+    pool = sum(n_pages) + 1
+    indices = rng.permutation(pool)[:sum(n_pages)]
+    indptr = np.concatenate([[0], np.cumsum(n_pages)])
+    ri = np.concatenate([[0], np.cumsum(lens)])
+    k = _bf16(rng, (ri[-1], H, d))
+    v = _bf16(rng, (ri[-1], H, d))
+    ref = cm.empty_paged("bf16", pool, H, P, d, 2)
+    cm.write_history(ref, indptr, indices, ri, k, v)
+    c = cm.empty_paged("fp8_e5m2", pool, H, P, d, 2, k_scale=np.array([1e-4, 1.0], np.float32))
+    cm.write_history(c, indptr, indices, ri, k, v)
+    for b, T in enumerate(lens):
+        for h in range(H):
+            K0, V0 = cm.read_rows(ref, b, h, np.arange(T))
+            K1, V1 = cm.read_rows(c, b, h, np.arange(T))
+            s = c.k_qp[h]
+            assert np.all(np.abs(K1 - K0) <= np.abs(K0) / 8 + s * 2.0 ** -17)
+            assert np.all(np.abs(V1 - V0) <= np.abs(V0) / 8 + 2.0 ** -17)
