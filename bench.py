@@ -37,7 +37,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "int8", "fp8", "int4-kivi")
+OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "int8", "fp8", "fp8-e5m2", "int4-kivi")
 
 
 def parse():
@@ -474,7 +474,7 @@ def _quantized_cache(dattn, w, fmt, dev):
         c["k"] = torch.zeros((n, H, P, d), dtype=torch.uint8, device=dev)
         c["k_qparams"] = torch.zeros((n, H, P, 2), dtype=torch.float16, device=dev)
         c["v_qparams"] = torch.zeros_like(c["k_qparams"])
-    elif fmt == "fp8_e4m3":
+    elif fmt in ("fp8_e4m3", "fp8_e5m2"):
         c["k"] = torch.zeros((n, H, P, d), dtype=torch.uint8, device=dev)
         c["k_qparams"] = w.meta["k_scale"].to(dev, torch.float32)     # per-head scales
         c["v_qparams"] = w.meta["v_scale"].to(dev, torch.float32)
@@ -503,7 +503,7 @@ def _stream_bytes(p, info, lens):
         return info["stream_keys"] * 4 * d
     if fmt == "int8":
         return info["stream_keys"] * (2 * d + 8)
-    if fmt == "fp8_e4m3":
+    if fmt in ("fp8_e4m3", "fp8_e5m2"):
         return info["stream_keys"] * 2 * d
     G, Gv, R = p["kivi_group"], p["kivi_v_group"], p["kivi_residual"]
     total = 0
@@ -523,8 +523,8 @@ def run_other(args):
     dattn.load()
     dev = torch.device("cuda", torch.cuda.current_device())
     name = args.workload
-    if name in ("int8", "fp8", "int4-kivi"):
-        fmt = {"int8": "int8", "fp8": "fp8_e4m3", "int4-kivi": "int4_kivi"}[name]
+    if name in ("int8", "fp8", "fp8-e5m2", "int4-kivi"):
+        fmt = {"int8": "int8", "fp8": "fp8_e4m3", "fp8-e5m2": "fp8_e5m2", "int4-kivi": "int4_kivi"}[name]
         w = W.quantized(dev, fmt=fmt)
         p, cache = _quantized_cache(dattn, w, fmt, dev)
     else:

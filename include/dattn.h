@@ -74,12 +74,16 @@ typedef enum { DATTN_KV_CONTIG_NHD = 0, DATTN_KV_PAGED_HND = 1 } dattn_layout;
  *  DATTN_FMT_FP8_E4M3:   K, V uint8 E4M3 codes [num_pages, H_kv, P, d] (sign,
  *      4 exponent bits with bias 7, 3 mantissa bits; no infinities, 0x7F / 0xFF
  *      NaN, largest magnitude 448).  k_qparams, v_qparams fp32 [H_kv]: one scale
- *      per kv head, NULL for 1 (no calibration); x_hat = value(code) * s_h. */
+ *      per kv head, NULL for 1 (no calibration); x_hat = value(code) * s_h.
+ *  DATTN_FMT_FP8_E5M2:   the same with E5M2 codes (5 exponent bits with bias 15,
+ *      2 mantissa bits, the upper byte of the IEEE half of the same value;
+ *      largest finite magnitude 57344). */
 typedef enum {
   DATTN_FMT_BF16 = 0,
   DATTN_FMT_INT8_TOKEN = 1,
   DATTN_FMT_INT4_KIVI = 2,
-  DATTN_FMT_FP8_E4M3 = 3
+  DATTN_FMT_FP8_E4M3 = 3,
+  DATTN_FMT_FP8_E5M2 = 4
 } dattn_format;
 
 /* Visibility programs.  Query row i of request b sits at position
@@ -304,6 +308,7 @@ size_t kv_append_workspace_bytes(const dattn_problem* prob);
  *    hold the request's previous residual rows (as this function leaves them).
  *  - FP8 E4M3: code = nearest E4M3 value to x / s_h (the quotient rounded in
  *    fp32), ties to the even code, saturated to +-448; the scales are inputs.
+ *  - FP8 E5M2: the same, saturated to +-57344.
  * Capacity (page list long enough for the new length) and arguments are
  * checked on the host before any write.  The caller advances its lengths
  * after the stream reaches this point.  "workspace" (device,

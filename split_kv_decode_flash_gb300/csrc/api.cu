@@ -35,8 +35,8 @@ void check_tensors(const dattn_problem& p, const dattn_tensors* t, bool need_q_o
     if (!t->k_qparams || !t->v_qparams || !aligned16(t->k_qparams) || !aligned16(t->v_qparams))
       c.fail(DATTN_EINVAL, "INT8 and INT4 KIVI need 16-byte aligned k_qparams and v_qparams");
   }
-  if (p.fmt == DATTN_FMT_FP8_E4M3 && ((reinterpret_cast<uintptr_t>(t->k_qparams) % 4) ||
-                                      (reinterpret_cast<uintptr_t>(t->v_qparams) % 4)))
+  if ((p.fmt == DATTN_FMT_FP8_E4M3 || p.fmt == DATTN_FMT_FP8_E5M2) &&
+      ((reinterpret_cast<uintptr_t>(t->k_qparams) % 4) || (reinterpret_cast<uintptr_t>(t->v_qparams) % 4)))
     c.fail(DATTN_EINVAL, "FP8 scales (k_qparams, v_qparams) must be 4-byte aligned fp32 arrays or NULL");
   if (p.fmt == DATTN_FMT_INT4_KIVI) {
     if (!t->k_residual || !t->v_residual || !aligned16(t->k_residual) || !aligned16(t->v_residual))

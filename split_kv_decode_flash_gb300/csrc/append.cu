@@ -100,8 +100,9 @@ __device__ __forceinline__ void load_channels(const __nv_bfloat16* row, int lane
 }
 
 // One warp per (new row, kv head): bf16 copy, INT8 per-token quantisation, or
-// FP8 E4M3 codes of x / s_h (correctly rounded fp32 quotient, then the
-// hardware's round-to-nearest-even conversion with saturation to +-448).
+// FP8 E4M3 / E5M2 codes of x / s_h (correctly rounded fp32 quotient, then the
+// hardware's round-to-nearest-even conversion with saturation to the largest
+// finite value).
 template <int D, int FMT>
 __global__ void append_rows_kernel(AppendParams p, int total_rows) {
   constexpr int C = D / 32;
@@ -129,7 +130,7 @@ __global__ void append_rows_kernel(AppendParams p, int total_rows) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(kv ? p.v : p.k) + dst_row;
       if constexpr (C == 4) reinterpret_cast<uint2*>(out)[lane] = reinterpret_cast<const uint2*>(in)[lane];
       else reinterpret_cast<uint32_t*>(out)[lane] = reinterpret_cast<const uint32_t*>(in)[lane];
-    } else if constexpr (FMT == DATTN_FMT_FP8_E4M3) {
+    } else if constexpr (FMT == DATTN_FMT_FP8_E4M3 || FMT == DATTN_FMT_FP8_E5M2) {
       float x[C];
       load_channels<C>(in, lane, x);
       const float* scales = static_cast<const float*>(kv ? p.vqp : p.kqp);
@@ -138,7 +139,8 @@ __global__ void append_rows_kernel(AppendParams p, int total_rows) {
 #pragma unroll
       for (int c = 0; c < C; c += 2) {
         const __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(x[c], sh), __fdiv_rn(x[c + 1], sh)), __NV_SATFINITE, __NV_E4M3);
+            make_float2(__fdiv_rn(x[c], sh), __fdiv_rn(x[c + 1], sh)), __NV_SATFINITE,
+            FMT == DATTN_FMT_FP8_E4M3 ? __NV_E4M3 : __NV_E5M2);
         packed |= static_cast<uint32_t>(two) << (8 * c);
       }
       uint8_t* codes = static_cast<uint8_t*>(kv ? p.v : p.k) + dst_row;
@@ -411,6 +413,9 @@ extern "C" dattn_status kv_append(const dattn_problem* prob, const dattn_append_
   } else if (p.fmt == DATTN_FMT_FP8_E4M3) {
     err = d128 ? launch_warps(append_rows_kernel<128, DATTN_FMT_FP8_E4M3>, new_indptr[B] * H, s, a, new_indptr[B])
                : launch_warps(append_rows_kernel<64, DATTN_FMT_FP8_E4M3>, new_indptr[B] * H, s, a, new_indptr[B]);
+  } else if (p.fmt == DATTN_FMT_FP8_E5M2) {
+    err = d128 ? launch_warps(append_rows_kernel<128, DATTN_FMT_FP8_E5M2>, new_indptr[B] * H, s, a, new_indptr[B])
+               : launch_warps(append_rows_kernel<64, DATTN_FMT_FP8_E5M2>, new_indptr[B] * H, s, a, new_indptr[B]);
   } else {
     const int groups = work_indptr[B], rows = res_indptr[B];
     err = d128 ? launch_warps(kivi_close_kernel<128>, groups * H, s, a, groups)

@@ -1,8 +1,9 @@
 // Partial kernel of split-KV decode attention for byte-code K/V on the tensor
 // cores: INT8 per-token ("M8.6 Live-Data Quantization", §0x05B format) and
-// FP8 E4M3 with a per-head scale (§0x0A-0x0AA).  FP8 codes become exact f16
-// values with one cvt per pair and have no offset, so their (s, z) are the
-// head's scale and zero, and the 1024 bias below is zero.
+// FP8 E4M3 / E5M2 with a per-head scale (§0x0A-0x0AA).  FP8 codes become exact
+// f16 values (one cvt per E4M3 pair; an E5M2 byte is the upper byte of its f16)
+// and have no offset, so their (s, z) are the head's scale and zero, and the
+// 1024 bias below is zero.
 //
 // Same persistent producer / consumer structure as the bf16 kernel (item
 // records in shared memory, four producer warps with a three-step slot
@@ -78,6 +79,15 @@ struct Codes<DATTN_FMT_INT8_TOKEN> {
   static constexpr float kBias = 1024.f;
   static __device__ __forceinline__ uint32_t pair(uint32_t w, uint32_t sel) {
     return __byte_perm(w, 0x64646464u, sel);
+  }
+};
+
+template <>
+struct Codes<DATTN_FMT_FP8_E5M2> {
+  static constexpr float kBias = 0.f;
+  static __device__ __forceinline__ uint32_t pair(uint32_t w, uint32_t sel) {
+    // byte A (sel nibble 0) to byte 1, byte B (nibble 2) to byte 3, zero low bytes
+    return __byte_perm(w, 0u, 0x0404u | ((sel & 0xFu) << 4) | (((sel >> 8) & 0xFu) << 12));
   }
 };
 
@@ -243,16 +253,18 @@ __device__ __forceinline__ void load_q8(const PartialParams& p, const WorkItem& 
 // Writes one accumulator row: O / LSE when the item is its group's only
 // chunk, else the row's partial state.  Output tile 2 C + e holds, in
 // columns 2 t4 and 2 t4 + 1, channels 16 C + 4 t4 + e and 16 C + 4 t4 + 2 + e;
-// "bias" (1024 sum P') is removed and z (sum p z) added on every channel.
+// "bias" (1024 sum P') is removed and z (sum p z) added on every channel, and
+// the result multiplied by vsc (FP8: the head's V scale, kept out of the f16
+// probabilities so that they stay in f16's normal range).
 template <int D>
 __device__ __forceinline__ void emit_row_q8(const PartialParams& p, const WorkItem& it, int my_state, int row, float m,
-                                            float l, float z, float bias, const float (&o)[D / 8][4], int half,
-                                            int t4) {
+                                            float l, float z, float bias, float vsc, const float (&o)[D / 8][4],
+                                            int half, int t4) {
   const int i = row / p.g, hq = it.h * p.g + row % p.g;
   const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
   const float add = z - bias;
   if (it.slot < 0) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? vsc / l : 0.f;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
 #pragma unroll
     for (int c = 0; c < D / 16; ++c) {
@@ -269,7 +281,8 @@ __device__ __forceinline__ void emit_row_q8(const PartialParams& p, const WorkIt
     for (int c = 0; c < D / 16; ++c) {
       const float* a0 = o[2 * c], *a1 = o[2 * c + 1];
       *reinterpret_cast<float4*>(u + 16 * c + 4 * t4) =
-          make_float4(a0[2 * half] + add, a1[2 * half] + add, a0[2 * half + 1] + add, a1[2 * half + 1] + add);
+          make_float4((a0[2 * half] + add) * vsc, (a1[2 * half] + add) * vsc, (a0[2 * half + 1] + add) * vsc,
+                      (a1[2 * half + 1] + add) * vsc);
     }
     if (t4 == 0) p.ml[srow] = make_float2(l > 0.f ? m : -INFINITY, l);
   }
@@ -308,8 +321,8 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
     const QRows<D> q = qn;
     if (ii + 1 < w.end) load_q8<D>(p, w.rec(ii + 1).it, r0, r1, t4, qn);
-    float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given)
-    if constexpr (FMT == DATTN_FMT_FP8_E4M3) {
+    float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given); INT8: 1
+    if constexpr (FMT != DATTN_FMT_INT8_TOKEN) {
       if (p.kqp) hk = static_cast<const float*>(p.kqp)[it.h];
       if (p.vqp) hv = static_cast<const float*>(p.vqp)[it.h];
     }
@@ -368,7 +381,7 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
             const int slot = base + nt * 8 + 2 * t4 + e;
             const int t = pos[slot];
             const float2 ks = FMT == DATTN_FMT_INT8_TOKEN ? half2_bits_to_float2(kqp[slot]) : make_float2(hk, 0.f);
-            const float2 vq = FMT == DATTN_FMT_INT8_TOKEN ? half2_bits_to_float2(vqp[slot]) : make_float2(hv, 0.f);
+            const float2 vq = FMT == DATTN_FMT_INT8_TOKEN ? half2_bits_to_float2(vqp[slot]) : make_float2(1.f, 0.f);
             vs[nt][e] = vq.x;
             vz[nt][e] = vq.y;
             const float off = fmaf(-Codes<FMT>::kBias, ks.x, ks.y);
@@ -451,8 +464,8 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
       b1 += __shfl_xor_sync(kAll, b1, x);
     }
     if (!dead) {
-      if (ok0) emit_row_q8<D>(p, it, my_state, r0, m0, l0, z0, Codes<FMT>::kBias * b0, o, 0, t4);
-      if (ok1) emit_row_q8<D>(p, it, my_state, r1, m1, l1, z1, Codes<FMT>::kBias * b1, o, 1, t4);
+      if (ok0) emit_row_q8<D>(p, it, my_state, r0, m0, l0, z0, Codes<FMT>::kBias * b0, hv, o, 0, t4);
+      if (ok1) emit_row_q8<D>(p, it, my_state, r1, m1, l1, z1, Codes<FMT>::kBias * b1, hv, o, 1, t4);
     }
   }
 }
@@ -552,8 +565,8 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
     const QCols<D> q = qn;
     if (ii + 1 < w.end) load_q8_cols<D>(p, w.rec(ii + 1).it, g4, t4, qn);
-    float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given)
-    if constexpr (FMT == DATTN_FMT_FP8_E4M3) {
+    float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given); INT8: 1
+    if constexpr (FMT != DATTN_FMT_INT8_TOKEN) {
       if (p.kqp) hk = static_cast<const float*>(p.kqp)[it.h];
       if (p.vqp) hv = static_cast<const float*>(p.vqp)[it.h];
     }
@@ -610,8 +623,8 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
         constexpr bool kI8 = FMT == DATTN_FMT_INT8_TOKEN;
         const float2 ksx = kI8 ? half2_bits_to_float2(kqp[kx]) : make_float2(hk, 0.f);
         const float2 ksy = kI8 ? half2_bits_to_float2(kqp[ky]) : make_float2(hk, 0.f);
-        const float2 vqx = kI8 ? half2_bits_to_float2(vqp[kx]) : make_float2(hv, 0.f);
-        const float2 vqy = kI8 ? half2_bits_to_float2(vqp[ky]) : make_float2(hv, 0.f);
+        const float2 vqx = kI8 ? half2_bits_to_float2(vqp[kx]) : make_float2(1.f, 0.f);
+        const float2 vqy = kI8 ? half2_bits_to_float2(vqp[ky]) : make_float2(1.f, 0.f);
         const float offx = fmaf(-Codes<FMT>::kBias, ksx.x, ksx.y), offy = fmaf(-Codes<FMT>::kBias, ksy.x, ksy.y);
         const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
         const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
@@ -693,7 +706,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
         const int i = row / p.g, hq = it.h * p.g + row % p.g;
         const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
         if (it.slot < 0) {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
+          const float inv = l > 0.f ? hv / l : 0.f;
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
 #pragma unroll
           for (int c = 0; c < NC; ++c)
@@ -705,7 +718,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
           float* u = p.u + srow * D;
 #pragma unroll
           for (int c = 0; c < NC; ++c)
-            *reinterpret_cast<float2*>(u + 16 * c + 2 * g4) = make_float2(o[c][rr] + add, o[c][2 + rr] + add);
+            *reinterpret_cast<float2*>(u + 16 * c + 2 * g4) = make_float2((o[c][rr] + add) * hv, (o[c][2 + rr] + add) * hv);
           if (g4 == 0) p.ml[srow] = make_float2(l > 0.f ? m : -INFINITY, l);
         }
       }
@@ -779,6 +792,9 @@ int launch_partial_q8(const PartialParams& p, int d, int n_ctas, void* stream) {
   if (p.fmt == DATTN_FMT_FP8_E4M3)
     return d == 64 ? launch_q8<64, DATTN_FMT_FP8_E4M3>(p, n_ctas, stream)
                    : launch_q8<128, DATTN_FMT_FP8_E4M3>(p, n_ctas, stream);
+  if (p.fmt == DATTN_FMT_FP8_E5M2)
+    return d == 64 ? launch_q8<64, DATTN_FMT_FP8_E5M2>(p, n_ctas, stream)
+                   : launch_q8<128, DATTN_FMT_FP8_E5M2>(p, n_ctas, stream);
   return d == 64 ? launch_q8<64, DATTN_FMT_INT8_TOKEN>(p, n_ctas, stream)
                  : launch_q8<128, DATTN_FMT_INT8_TOKEN>(p, n_ctas, stream);
 }

@@ -39,7 +39,7 @@ def _alloc(fmt, p, n_pages, B, dev="cuda", scales=None):
         out["v"] = torch.zeros_like(out["k"])
         out["k_qparams"] = torch.zeros((n_pages, H, P, 2), dtype=torch.float16, device=dev)
         out["v_qparams"] = torch.zeros_like(out["k_qparams"])
-    elif fmt == "fp8_e4m3":
+    elif fmt in ("fp8_e4m3", "fp8_e5m2"):
         out["k"] = torch.zeros((n_pages, H, P, d), dtype=torch.uint8, device=dev)
         out["v"] = torch.zeros_like(out["k"])
         if scales is not None:
@@ -59,7 +59,7 @@ def append_history(w, fmt, cuts_per_request):
     """kv_append the workload's packed history in pieces; returns the device cache dict."""
     p = dict(w.problem, fmt=fmt)
     B = p["B"]
-    scales = (w.meta["k_scale"], w.meta["v_scale"]) if fmt == "fp8_e4m3" and "k_scale" in w.meta else None
+    scales = (w.meta["k_scale"], w.meta["v_scale"]) if fmt.startswith("fp8") and "k_scale" in w.meta else None
     cache = _alloc(fmt, p, p["num_pages"], B, scales=scales)
     cache["page_indptr"] = w.page_indptr.cuda()
     cache["page_indices"] = w.page_indices.cuda()
@@ -153,25 +153,27 @@ def test_int8_append_codes_and_qparams_bit_exact(d):
         assert np.array_equal(vc[pg, :, r], ref.v[pg, :, r])
 
 
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "fp8_e5m2"])
 @pytest.mark.parametrize("d,scales", [(128, "calibrated"), (64, "calibrated"), (128, "none"), (128, "tight")])
-def test_fp8_append_codes_bit_exact(d, scales):
-    """E4M3 codes of x / s_h: calibrated scales, no scales (1), and scales a quarter of the
-    calibrated ones, so that a quarter of the range saturates to +-448."""
+def test_fp8_append_codes_bit_exact(fmt, d, scales):
+    """FP8 codes of x / s_h: calibrated scales, no scales (1), and scales a quarter of the
+    calibrated ones, so that a quarter of the range saturates to the largest finite value."""
     w = W.quantized_history("fp8", B=3, S_q=1, H_q=8, H_kv=2, d=d, lens=[333, 1, 96], P=16, seed=15,
-                            device="cuda", fmt="fp8_e4m3", pool_pages=40)
+                            device="cuda", fmt=fmt, pool_pages=40)
     if scales == "none":
         del w.meta["k_scale"], w.meta["v_scale"]
     elif scales == "tight":
         w.meta["k_scale"] = w.meta["k_scale"] / 4
         w.meta["v_scale"] = w.meta["v_scale"] / 4
-    p, cache = append_history(w, "fp8_e4m3", _cuts(w.kv_len.tolist(), np.random.default_rng(3)))
-    ref = oracle_written(w, "fp8_e4m3")
+    p, cache = append_history(w, fmt, _cuts(w.kv_len.tolist(), np.random.default_rng(3)))
+    ref = oracle_written(w, fmt)
+    top = 0x7E if fmt == "fp8_e4m3" else 0x7B
     kc, vc = cache["k"].cpu().numpy(), cache["v"].cpu().numpy()
     n_sat = 0
     for b, t, pg, r in _visible_rows(w):
         assert np.array_equal(kc[pg, :, r], ref.k[pg, :, r])
         assert np.array_equal(vc[pg, :, r], ref.v[pg, :, r])
-        n_sat += int(np.sum((kc[pg, :, r] & 0x7F) == 0x7E))
+        n_sat += int(np.sum((kc[pg, :, r] & 0x7F) == top))
     # calibrated: only each head's largest |x| meets 448; tight: a quarter of the range saturates
     assert n_sat >= 100 if scales == "tight" else n_sat < 20
 

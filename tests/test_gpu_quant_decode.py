@@ -68,7 +68,7 @@ def _compare(O, L, w, p, cache_ref, rows):
     return H.compare(O, L, w2, rows, cache=cache_ref)
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4_kivi", "fp8_e4m3"])
+@pytest.mark.parametrize("fmt", ["int8", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
 @pytest.mark.parametrize("chunk,num_sms", [(0, 152), (64, 5)])
 def test_quantized_decode_small_all_rows(fmt, chunk, num_sms):
     lens = [700, 129, 128, 161, 40, 1]
@@ -80,7 +80,7 @@ def test_quantized_decode_small_all_rows(fmt, chunk, num_sms):
     _compare(O, L, w, p, ref, H.all_rows(p))
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4_kivi", "fp8_e4m3"])
+@pytest.mark.parametrize("fmt", ["int8", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
 def test_quantized_decode_d64_multi_row_sink_window(fmt):
     lens = [500, 90]
     w = W.quantized_history("q64", B=2, S_q=2, H_q=8, H_kv=2, d=64, lens=lens, P=16, seed=22, device="cuda",
@@ -101,7 +101,7 @@ def test_int4_kivi_verify_rows_cross_the_residual_boundary():
     _compare(O, L, w, p, _oracle_cache(w, "int4_kivi"), H.all_rows(p))
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4_kivi", "fp8_e4m3"])
+@pytest.mark.parametrize("fmt", ["int8", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
 def test_quantized_full_size_sampled(fmt):
     """B=32, T ~ U[2048, 32768], K outlier channels: the full quantized workload."""
     w = W.quantized("cuda", fmt=fmt)
@@ -144,7 +144,7 @@ def test_int8_decode_page_sizes(P):
     _compare(O, L, w, p, _oracle_cache(w, "int8"), H.all_rows(p))
 
 
-@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3"])
+@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "fp8_e5m2"])
 @pytest.mark.parametrize("S_q,H_q,H_kv,d", [(3, 16, 4, 128), (4, 16, 2, 128), (4, 16, 2, 64)])
 def test_byte_codes_decode_more_than_eight_rows(fmt, S_q, H_q, H_kv, d):
     """12 and 32 query rows per kv head (row tiles of 16 on the mma M side), causal verify rows."""
@@ -157,17 +157,18 @@ def test_byte_codes_decode_more_than_eight_rows(fmt, S_q, H_q, H_kv, d):
     _compare(O, L, w, p, _oracle_cache(w, fmt), H.all_rows(p))
 
 
-def test_fp8_decode_without_scales_and_with_saturation():
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "fp8_e5m2"])
+def test_fp8_decode_without_scales_and_with_saturation(fmt):
     """FP8 with no scales (1) and with scales that saturate part of the range."""
     lens = [300, 65, 8]
     for mode in ("none", "tight"):
         w = W.quantized_history("f8s", B=3, S_q=1, H_q=16, H_kv=4, d=128, lens=lens, P=16, seed=26,
-                                device="cuda", fmt="fp8_e4m3", pool_pages=sum(-(-t // 16) for t in lens) + 2)
+                                device="cuda", fmt=fmt, pool_pages=sum(-(-t // 16) for t in lens) + 2)
         if mode == "none":
             del w.meta["k_scale"], w.meta["v_scale"]
         else:
             w.meta["k_scale"] = w.meta["k_scale"] / 8
             w.meta["v_scale"] = w.meta["v_scale"] / 8
-        p, cache = append_history(w, "fp8_e4m3", [[] for _ in lens])
-        O, L, info = _run(w, "fp8_e4m3", p, cache, chunk_tokens=64, num_sms=4)
-        _compare(O, L, w, p, _oracle_cache(w, "fp8_e4m3"), H.all_rows(p))
+        p, cache = append_history(w, fmt, [[] for _ in lens])
+        O, L, info = _run(w, fmt, p, cache, chunk_tokens=64, num_sms=4)
+        _compare(O, L, w, p, _oracle_cache(w, fmt), H.all_rows(p))

@@ -175,10 +175,11 @@ def quantized_history(name, *, B, S_q, H_q, H_kv, d, lens, P, seed, device, fmt,
                    num_pages=pool_pages, mask="causal", kivi_group=32, kivi_v_group=32,
                    kivi_residual=128)
     meta_out = {"outlier_channels": och, "seed": seed}
-    if fmt == "fp8_e4m3":
-        # per-head scales from a calibration pass over the history: max |x| / 448 (fp32)
-        meta_out["k_scale"] = (k_rows.float().abs().amax(dim=(0, 2)) / 448.0).cpu()
-        meta_out["v_scale"] = (v_rows.float().abs().amax(dim=(0, 2)) / 448.0).cpu()
+    if fmt in ("fp8_e4m3", "fp8_e5m2"):
+        # per-head scales from a calibration pass over the history: max |x| / largest finite (fp32)
+        top = 448.0 if fmt == "fp8_e4m3" else 57344.0
+        meta_out["k_scale"] = (k_rows.float().abs().amax(dim=(0, 2)) / top).cpu()
+        meta_out["v_scale"] = (v_rows.float().abs().amax(dim=(0, 2)) / top).cpu()
     return Workload(name, problem, q, torch.tensor(lens, dtype=torch.int32),
                     page_indptr=indptr, page_indices=indices, rows_indptr=rows_indptr,
                     k_rows=k_rows, v_rows=v_rows, meta=meta_out)
