@@ -445,7 +445,7 @@ def run_ours(args):
                 "includes": "pinned H2D of q and page tables, host planning, work-list H2D, both kernels, "
                             "D2H of O and LSE, stream sync"},
         "clocks": ck,
-        "gpu_launches": K * (1 + (1 if info["n_merge_groups"] else 0)),
+        "gpu_launches": K * (1 + (1 if info["n_merge_groups"] and not info["fused_merge"] else 0)),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:

@@ -135,6 +135,11 @@ typedef struct {
   int32_t num_sms;              /* SMs to plan for (>= 1)                                 */
   int32_t ctas_per_sm;          /* resident CTAs per SM to plan for; 0 = library default  */
   int32_t chunk_tokens;         /* chunk width in keys; 0 = planner default               */
+  int32_t fused_merge;          /* 1: bf16 groups of several chunks are merged inside the
+                                   partial kernel by the last CTA to finish them (one
+                                   launch); 0: by the LSE-merge kernel.  Off by default: on
+                                   GB300 the merge then sits on the partial kernel's tail,
+                                   and the step is slower (see the design notes)          */
 } dattn_plan_inputs;
 
 typedef struct dattn_plan_s dattn_plan_t;
@@ -169,6 +174,9 @@ typedef struct {
   int32_t rows;             /* query rows per group, g * S_q                           */
   int64_t stream_keys;      /* keys read by all groups (sum of visible streams)        */
   int64_t max_cta_keys;     /* keys of the most loaded CTA                             */
+  int32_t fused_merge;      /* 1: the last CTA to finish a group's chunks merges it     */
+                            /*    inside the partial kernel (no merge launch)          */
+  int32_t reserved;
 } dattn_plan_info;
 
 /* One work item as planned: keys [a, e) of the visible stream of (b, h_kv).
@@ -204,10 +212,14 @@ dattn_status dattn_plan_get_items(const dattn_plan_t* plan, dattn_work_item* ite
 
 /* Runs one decode step: copies the plan's work list into the head of
  * "workspace" (device, >= info.workspace_bytes, 256-byte aligned), launches
- * the partial kernel (one producer warp streaming K/V pages through shared
- * memory with bulk copies, consumer warps updating exact (m, l, u) states)
- * and, when some group has several chunks, the LSE-merge kernel
- * (M4.5 §0x03I two-launch schedule).  "prob" must equal the planned problem
+ * the partial kernel (producer warps streaming K/V rows through a shared
+ * memory ring, consumer warps updating exact (m, l, u) states) and, when some
+ * group has several chunks, merges their states (M4.5 §0x03I) with a second,
+ * LSE-merge kernel, or, for a bf16 plan made with fused_merge, inside the
+ * partial kernel (the last CTA to finish a group's chunks merges it;
+ * info.fused_merge = 1).  A fused run that ended with a device error leaves
+ * the merge counters undefined: upload the plan again (a run without
+ * DATTN_RUN_REUSE_UPLOAD) afterwards.  "prob" must equal the planned problem
  * (else ESTALE_PLAN).  Device-side bounds checks (page id < num_pages, block
  * inside the request's page list, list entry inside [0, T_b), cache row <
  * B_cache) skip the offending rows and raise a flag that dattn_device_status

@@ -152,6 +152,9 @@ void bind_blob(const dattn_plan_t* plan, void* ws, PartialParams& k) {
   k.ml = reinterpret_cast<float2*>(base + h->off_ml);
   k.u = reinterpret_cast<float*>(base + h->off_u);
   k.status = reinterpret_cast<int32_t*>(base + offsetof(BlobHeader, status));
+  k.groups = reinterpret_cast<const MergeGroup*>(base + h->off_merge);
+  k.group_count = reinterpret_cast<int32_t*>(base + h->off_count);
+  k.fused = h->fused;
 }
 
 dattn_status upload_blob(const dattn_plan_t* plan, void* ws, cudaStream_t s, PartialParams& k) {
@@ -217,7 +220,7 @@ dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const
     if (err != cudaSuccess) return cuda_fail("dattn_run partial kernel", err);
   }
   if ((st = record(events, 1, s)) != DATTN_OK) return st;
-  if (plan->info.n_merge_groups > 0) {
+  if (plan->info.n_merge_groups > 0 && !plan->info.fused_merge) {
     const BlobHeader* h = reinterpret_cast<const BlobHeader*>(plan->blob.data());
     MergeParams m{};
     m.groups = reinterpret_cast<const MergeGroup*>(static_cast<uint8_t*>(workspace) + h->off_merge);

@@ -69,7 +69,8 @@ struct MergeGroup {
 struct ItemRec {
   WorkItem it;
   int32_t lo, hi;      // paged layout: page list entries [lo, hi) of request it.b
-  int32_t crow, pad;   // contiguous layout: cache row, resolved by the kernel
+  int32_t crow;        // contiguous layout: cache row, resolved by the kernel
+  int32_t merge;       // index of the item's merge group, -1 when it writes O directly
 };
 static_assert(sizeof(ItemRec) == 48, "ItemRec layout");
 
@@ -77,8 +78,10 @@ static_assert(sizeof(ItemRec) == 48, "ItemRec layout");
 struct BlobHeader {
   uint32_t magic;
   int32_t status;        // device status word, zeroed by the copy
-  int32_t n_items, n_ctas, n_merge, rows, n_slots, pad;
-  int64_t off_items, off_cta_indptr, off_cta_items, off_merge, off_ml, off_u, off_cta_recs, reserved;
+  int32_t n_items, n_ctas, n_merge, rows, n_slots;
+  int32_t fused;         // merge groups merged inside the partial kernel
+  int64_t off_items, off_cta_indptr, off_cta_items, off_merge, off_ml, off_u, off_cta_recs;
+  int64_t off_count;     // int32 [n_merge]: finished items per merge group (fused merge)
 };
 static_assert(sizeof(BlobHeader) == 96, "BlobHeader layout");
 
@@ -105,6 +108,9 @@ struct PartialParams {
   float2* ml;            // [n_slots * rows] (m in log2 units, l)
   float* u;              // [n_slots * rows * d]
   int32_t* status;
+  const MergeGroup* groups;   // [n_merge]
+  int32_t* group_count;       // [n_merge], fused merge: zero between runs
+  int32_t fused;              // 1: the last CTA to finish a group merges it
   int32_t B, S_q, H_q, H_kv, g, rows;
   int32_t layout, fmt, mask, P, num_pages, T_cap, B_cache;
   int32_t n_sink, window, kivi_G, kivi_Gv, kivi_R;

@@ -32,6 +32,7 @@
 // O / LSE when it is the group's only state.
 #include <cuda_runtime.h>
 
+#include "merge.cuh"
 #include "tc_common.cuh"
 
 namespace dattn {
@@ -333,6 +334,88 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
   }
 }
 
+// Fused LSE merge (M4.5 §0x02B-§0x02C, as in the merge kernel): after the
+// consumers have written their states, the CTA counts its finished items per
+// merge group; the CTA that completes a group's count merges that group.  The
+// states were written before a gpu-scope fence and the count (release); the
+// merging CTA fences after reading the final count (acquire) and reads the
+// states through L2.  Warps take (row, share of the states) tasks and combine
+// a row's shares in shared memory (the drained ring).  The merging CTA resets
+// the group's count for the next run.
+template <int D>
+__device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
+  constexpr int C = D / 32;
+  const PartialParams& p = w.p;
+  constexpr int kCW = kConsumerWarps;
+  int* list = reinterpret_cast<int*>(smem);                       // [0]: n, then merge group ids
+  float* sm_u = reinterpret_cast<float*>(smem + 1024);            // [kCW][D]
+  float* sm_ml = sm_u + kCW * D;                                  // [kCW][2]
+  __threadfence();                                                // this thread's state writes
+  named_barrier(1, 32 * kCW);
+  if (cw == 0 && lane == 0) {
+    const int spi = kConsumerWarps / (p.rows <= 16 ? 1 : 2);       // states per item
+    int n = 0;
+    for (int ii = w.begin; ii < w.end; ++ii) {
+      const int g = w.rec(ii).merge;
+      if (g < 0) continue;
+      const int total = p.groups[g].n / spi;
+      if (atomicAdd(p.group_count + g, 1) + 1 == total) list[1 + n++] = g;
+    }
+    list[0] = n;
+    __threadfence();
+  }
+  named_barrier(1, 32 * kCW);
+  const int n = list[0];
+  if (n == 0) return;
+  __threadfence();
+  const int R = p.rows;
+  const int W = R >= kCW ? 1 : kCW / R;      // warps per row
+  for (int k = 0; k < n; ++k) {
+    const int gi = list[1 + k];
+    const MergeGroup grp = p.groups[gi];
+    for (int r0 = 0; r0 < R; r0 += kCW / W) {
+      const int row = r0 + cw / W, share = cw % W;
+      const bool active = cw / W < kCW / W && row < R;
+      RowFold<D> f;
+      fold_init(f);
+      if (active) {
+        const int n_mine = grp.n > share ? (grp.n - share + W - 1) / W : 0;
+        fold_states<D>(p.ml, p.u, R, row, grp.slot0 + share, n_mine, W, lane, f);
+      }
+      if (W > 1) {
+#pragma unroll
+        for (int c = 0; c < C; ++c) sm_u[cw * D + lane * C + c] = f.U[c];
+        if (lane == 0) {
+          sm_ml[2 * cw] = f.M;
+          sm_ml[2 * cw + 1] = f.L;
+        }
+        named_barrier(1, 32 * kCW);
+        if (active && share == 0) {
+          RowFold<D> t;
+          fold_init(t);
+          for (int j = cw; j < cw + W; ++j) t.M = fmaxf(t.M, sm_ml[2 * j + 1] > 0.f ? sm_ml[2 * j] : -INFINITY);
+          if (t.M != -INFINITY) {
+            for (int j = cw; j < cw + W; ++j) {
+              if (!(sm_ml[2 * j + 1] > 0.f)) continue;
+              const float a = exp2f(sm_ml[2 * j] - t.M);
+              t.L += a * sm_ml[2 * j + 1];
+#pragma unroll
+              for (int c = 0; c < C; ++c) t.U[c] = fmaf(a, sm_u[j * D + lane * C + c], t.U[c]);
+            }
+          }
+          f = t;
+        }
+        named_barrier(1, 32 * kCW);
+      }
+      if (active && share == 0) {
+        const int i = row / p.g, hq = grp.h * p.g + row % p.g;
+        write_folded_row<D>(p.o, p.lse, (static_cast<long long>(grp.b) * p.S_q + i) * p.H_q + hq, f, lane);
+      }
+    }
+    if (cw == 0 && lane == 0) p.group_count[gi] = 0;    // ready for the next run
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_constant__ PartialParams p) {
   using C = Bf<D>;
@@ -365,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));
   consume_bf16<D>(w, smem, warp, lane, !complete_now);
+  if (p.fused) fused_merge<D>(w, smem, warp, lane);
 }
 
 template <int D>

@@ -286,6 +286,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   //    an item leaves its own state, so an item owns states_per_item slots; a
   //    group that is one item with one state per row writes O directly.
   std::vector<MergeGroup> merges;
+  std::vector<int> merge_of_group(n_groups, -1);
   const bool kivi_tc = kivi_on_tensor_cores(p.d_h, rows, p.kivi_v_group, p.mask, p.page_size, p.kivi_residual);
   const int spi = states_per_item(rows, p.fmt, kivi_tc);
   int n_slots = 0, max_splits = 0;
@@ -293,6 +294,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
     const int n = group_first[k + 1] - group_first[k];
     max_splits = std::max(max_splits, n);
     if (n * spi > 1) {
+      merge_of_group[k] = static_cast<int>(merges.size());
       merges.push_back(MergeGroup{k / H, k % H, n_slots, n * spi});
       for (int i = 0; i < n; ++i) items[group_first[k] + i].slot = n_slots + i * spi;
       n_slots += n * spi;
@@ -345,6 +347,8 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   hdr.n_merge = static_cast<int>(merges.size());
   hdr.rows = rows;
   hdr.n_slots = n_slots;
+  // on request, bf16 groups are merged inside the partial kernel by the last CTA to finish them
+  hdr.fused = in->fused_merge != 0 && p.fmt == DATTN_FMT_BF16 && !merges.empty();
   size_t off = align_up(sizeof(BlobHeader), 16);
   hdr.off_items = off;
   off = align_up(off + sizeof(WorkItem) * n_items, 16);
@@ -355,7 +359,9 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   hdr.off_merge = off;
   off = align_up(off + sizeof(MergeGroup) * merges.size(), 16);
   hdr.off_cta_recs = off;
-  off = align_up(off + sizeof(ItemRec) * n_items, kWsAlign);
+  off = align_up(off + sizeof(ItemRec) * n_items, 16);
+  hdr.off_count = off;
+  off = align_up(off + sizeof(int32_t) * merges.size(), kWsAlign);
   const size_t blob_bytes = off;
   hdr.off_ml = off;
   off = align_up(off + sizeof(float) * 2 * static_cast<size_t>(n_slots) * rows, kWsAlign);
@@ -377,6 +383,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
       const int i = cta_order[k];
       ItemRec r{};
       r.it = items[i];
+      r.merge = merge_of_group[static_cast<size_t>(items[i].b) * H + items[i].h];
       r.lo = r.hi = -1;      // resolved by the kernel when the host page list is unknown
       if (p.layout == DATTN_KV_PAGED_HND && in->page_indptr) {
         r.lo = in->page_indptr[items[i].b];
@@ -396,6 +403,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   info.n_ctas = n_ctas;
   info.n_slots = n_slots;
   info.n_merge_groups = static_cast<int>(merges.size());
+  info.fused_merge = hdr.fused;
   info.max_splits = max_splits;
   info.rows = rows;
   info.stream_keys = W;

@@ -253,3 +253,26 @@ def test_device_bounds_check_flags_out_of_pool_page_without_reading_it():
     assert flags & 1               # kStPageRange
     # request 1 is untouched by the bad entry and still matches the oracle
     H.compare(O, L, w, [(1, 0, h) for h in range(8)])
+
+
+@pytest.mark.parametrize("chunk,num_sms,S_q", [(0, 152, 1), (64, 7, 1), (0, 152, 4), (64, 7, 2)])
+def test_fused_merge_matches_and_counters_reset_for_reused_uploads(chunk, num_sms, S_q):
+    """With fused_merge, bf16 groups are merged inside the partial kernel by the CTA that
+    completes them (4 to 32 rows); the per-group counters must come back to zero, so runs
+    that reuse the uploaded work list give bit-identical outputs."""
+    w = W.paged_ragged_gqa("cuda", B=6, lo=1, hi=900, pool_pages=500)
+    if S_q > 1:
+        w = W.paged_bf16("fused", B=5, S_q=S_q, H_q=32, H_kv=4, d=128, lens=[700, 5, 300, 64, 1], P=16,
+                         seed=31, device="cuda")
+    keep = {}
+    O, L, info, flags = H.run_gpu(w, chunk_tokens=chunk, num_sms=num_sms, keep=keep, fused_merge=True)
+    assert flags == 0 and info["n_merge_groups"] > 0 and info["fused_merge"] == 1
+    H.compare(O, L, w)
+    t = dattn.tensors_from(**keep["kw"])
+    for _ in range(3):
+        keep["kw"]["o"].fill_(float("nan"))
+        dattn.dattn_run_ex(keep["plan"], w.problem, t, keep["ws"], reuse_upload=True)
+        torch.cuda.synchronize()
+        assert dattn.dattn_device_status(keep["ws"]) == 0
+        assert torch.equal(keep["kw"]["o"].float().cpu(), O)
+        assert torch.equal(keep["kw"]["lse"].cpu(), L)
