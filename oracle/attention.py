@@ -37,10 +37,14 @@ def attend(q, K, V, scale: float):
     return (w @ V) / l, m + math.log(l)
 
 
-def visible_for(problem: dict, T_b: int, i: int, index_list=None):
+def visible_for(problem: dict, T_b: int, i: int, index_list=None, b: int = 0):
+    intervals = None
+    if problem.get("mask") == masks.MASK_FLASHMASK:      # packed ragged [sum T_b, 4], fm_indptr [B+1]
+        ip = problem["fm_indptr"]
+        intervals = np.asarray(problem["fm_intervals"]).reshape(-1, 4)[ip[b]:ip[b + 1]]
     return masks.visible_positions(problem.get("mask", masks.MASK_CAUSAL), T_b, problem["S_q"], i,
                                    n_sink=problem.get("n_sink", 0), window=problem.get("window", 0),
-                                   index_list=index_list)
+                                   index_list=index_list, intervals=intervals)
 
 
 def index_list_of(problem: dict, b: int, h_kv: int):
@@ -69,7 +73,7 @@ def decode_rows(problem: dict, cache, q_bits, rows=None):
         h_kv = address.kv_head(h_q, H_q, H_kv)
         key = (b, i, h_kv)
         if key not in cached:
-            vis = visible_for(problem, int(cache.kv_len[b]), i, index_list_of(problem, b, h_kv))
+            vis = visible_for(problem, int(cache.kv_len[b]), i, index_list_of(problem, b, h_kv), b)
             cached = {key: cache_mod.read_rows(cache, b, h_kv, vis)}
         K, V = cached[key]
         O[n], LSE[n] = attend(q[b, i, h_q], K, V, scale)
@@ -89,7 +93,7 @@ def decode_rows_split(problem: dict, cache, q_bits, rows, n_splits: int, order=N
     LSE = np.zeros(len(rows))
     for n, (b, i, h_q) in enumerate(rows):
         h_kv = address.kv_head(h_q, H_q, H_kv)
-        vis = visible_for(problem, int(cache.kv_len[b]), i, index_list_of(problem, b, h_kv))
+        vis = visible_for(problem, int(cache.kv_len[b]), i, index_list_of(problem, b, h_kv), b)
         K, V = cache_mod.read_rows(cache, b, h_kv, vis)
         s = (K @ q[b, i, h_q]) * scale
         states = []
