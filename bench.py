@@ -37,7 +37,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "int8", "fp8", "fp8-e5m2", "int4-kivi")
+OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "tree-verify", "int8", "fp8", "fp8-e5m2",
+                   "int4-kivi")
 
 
 def parse():
@@ -530,11 +531,14 @@ def run_other(args):
     else:
         w = {"long-s1": lambda: W.long_context(dev, 1), "long-s4": lambda: W.long_context(dev, 4),
              "sink-window": lambda: W.retention(dev, "sink_window"),
-             "index-list": lambda: W.retention(dev, "index_list")}[name]()
+             "index-list": lambda: W.retention(dev, "index_list"),
+             "tree-verify": lambda: W.tree_verify(dev)}[name]()
         p = w.problem
         cache = dict(k=w.k, v=w.v, page_indptr=w.page_indptr.to(dev), page_indices=w.page_indices.to(dev))
         if w.index_list is not None:
             cache.update(index_indptr=w.index_indptr.to(dev), index_list=w.index_list.to(dev))
+        if w.fm_intervals is not None:
+            cache.update(fm_intervals=w.fm_intervals.to(dev).contiguous())
     props = torch.cuda.get_device_properties(dev)
     plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, index_indptr=w.index_indptr,
                             index_list=w.index_list, num_sms=props.multi_processor_count, chunk_tokens=args.chunk)

@@ -93,8 +93,20 @@ typedef enum {
  *  DATTN_MASK_SINK_WINDOW: keys [0, min(n_sink, F_i)) U [max(0, F_i - window), F_i)
  *                          (M5.4 §0x05 union, never double counted).
  *  DATTN_MASK_INDEX_LIST:  keys of the sorted list of (b, h_kv) that are < F_i
- *                          (per-kv-head retained sets, M5.4 §0x06E shape). */
-typedef enum { DATTN_MASK_CAUSAL = 0, DATTN_MASK_SINK_WINDOW = 1, DATTN_MASK_INDEX_LIST = 2 } dattn_mask_kind;
+ *                          (per-kv-head retained sets, M5.4 §0x06E shape).
+ *  DATTN_MASK_FLASHMASK:   two masked query-row intervals per key column (M4.5
+ *                          §0x06A): key j in [0, T_b) is hidden from query row i of
+ *                          the call (0 <= i < S_q) when UTS_j <= i < UTE_j or
+ *                          LTS_j <= i < LTE_j, with (UTS, UTE, LTS, LTE)_j =
+ *                          fm_intervals[off_b + j], off_b = T_0 + ... + T_{b-1}
+ *                          (device int32 [sum T_b, 4], one set per request, shared
+ *                          by its heads).  No causal limit applies.  bf16 K/V. */
+typedef enum {
+  DATTN_MASK_CAUSAL = 0,
+  DATTN_MASK_SINK_WINDOW = 1,
+  DATTN_MASK_INDEX_LIST = 2,
+  DATTN_MASK_FLASHMASK = 3
+} dattn_mask_kind;
 
 /* Tile classes of M4.5 §0x05C. */
 typedef enum { DATTN_TILE_SKIP = 0, DATTN_TILE_FULL = 1, DATTN_TILE_PARTIAL = 2 } dattn_tile_class;
@@ -160,6 +172,7 @@ typedef struct {
   const int32_t* index_list;     /* device, INDEX_LIST                                     */
   void* o;                       /* device bf16 [B, S_q, H_q, d] (output)                  */
   float* lse;                    /* device fp32 [B, S_q, H_q] (output) or NULL             */
+  const int32_t* fm_intervals;   /* device int32 [sum T_b, 4], FLASHMASK, 16-byte aligned  */
 } dattn_tensors;
 
 /* Summary of a plan, for reporting (split counts of M4.5 §0x0AC). */

@@ -30,7 +30,7 @@ STATUS = {0: "DATTN_OK", 1: "DATTN_EINVAL", 2: "DATTN_EUNSUPPORTED", 3: "DATTN_E
           4: "DATTN_ESTALE_PLAN", 5: "DATTN_ECUDA", 6: "DATTN_EDEVICE_CHECK"}
 LAYOUTS = {"contig": 0, "paged": 1}
 FORMATS = {"bf16": 0, "int8": 1, "int4_kivi": 2, "fp8_e4m3": 3, "fp8_e5m2": 4}
-MASKS = {"causal": 0, "sink_window": 1, "index_list": 2}
+MASKS = {"causal": 0, "sink_window": 1, "index_list": 2, "flashmask": 3}
 TILE_CLASSES = {0: "SKIP", 1: "FULL", 2: "PARTIAL"}
 
 
@@ -57,7 +57,7 @@ class PlanInputs(ctypes.Structure):
 class Tensors(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "q", "k", "v", "k_qparams", "v_qparams", "k_residual", "v_residual", "page_indptr",
-        "page_indices", "cache_batch_idx", "index_indptr", "index_list", "o", "lse")]
+        "page_indices", "cache_batch_idx", "index_indptr", "index_list", "o", "lse", "fm_intervals")]
 
 
 class PlanInfo(ctypes.Structure):

@@ -31,6 +31,8 @@ void check_tensors(const dattn_problem& p, const dattn_tensors* t, bool need_q_o
     c.fail(DATTN_EINVAL, "paged layout needs page_indptr and page_indices");
   if (p.mask == DATTN_MASK_INDEX_LIST && (!t->index_indptr || !t->index_list))
     c.fail(DATTN_EINVAL, "index_list mask needs index_indptr and index_list");
+  if (p.mask == DATTN_MASK_FLASHMASK && (!t->fm_intervals || !aligned16(t->fm_intervals)))
+    c.fail(DATTN_EINVAL, "flashmask needs 16-byte aligned fm_intervals");
   if (p.fmt == DATTN_FMT_INT8_TOKEN || p.fmt == DATTN_FMT_INT4_KIVI) {
     if (!t->k_qparams || !t->v_qparams || !aligned16(t->k_qparams) || !aligned16(t->v_qparams))
       c.fail(DATTN_EINVAL, "INT8 and INT4 KIVI need 16-byte aligned k_qparams and v_qparams");
@@ -58,6 +60,7 @@ void fill_common(const dattn_problem& p, const dattn_tensors& t, PartialParams& 
   k.cache_batch_idx = t.cache_batch_idx;
   k.index_indptr = t.index_indptr;
   k.index_list = t.index_list;
+  k.fm_intervals = t.fm_intervals;
   k.o = t.o;
   k.lse = t.lse;
   k.B = p.B;
@@ -305,6 +308,8 @@ extern "C" dattn_status dattn_debug_classify(const dattn_problem* prob, const da
   if (!kv_len || (n > 0 && (!tiles || !out))) c.fail(DATTN_EINVAL, "kv_len, tiles and out are required");
   if (c.status == DATTN_OK && prob->mask == DATTN_MASK_INDEX_LIST && (!t || !t->index_indptr || !t->index_list))
     c.fail(DATTN_EINVAL, "index_list mask needs index_indptr and index_list");
+  if (c.status == DATTN_OK && prob->mask == DATTN_MASK_FLASHMASK)
+    c.fail(DATTN_EUNSUPPORTED, "the tile classifier covers interval programs and index lists");
   if (n < 0) c.fail(DATTN_EINVAL, "n must be >= 0");
   if (c.status != DATTN_OK) return c.finish("dattn_debug_classify");
   if (n == 0) return DATTN_OK;
@@ -333,6 +338,7 @@ extern "C" dattn_status dattn_debug_gather(const dattn_plan_t* plan, const dattn
   if (!count || (capacity > 0 && !out) || b < 0 || b >= prob->B || h_kv < 0 || h_kv >= prob->H_kv)
     c.fail(DATTN_EINVAL, "bad group or output");
   if (prob->mask == DATTN_MASK_INDEX_LIST && (!t || !t->index_list)) c.fail(DATTN_EINVAL, "index_list is required");
+  if (prob->mask == DATTN_MASK_FLASHMASK) c.fail(DATTN_EUNSUPPORTED, "the gather covers interval programs and index lists");
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) ||
       workspace_bytes < static_cast<size_t>(plan->info.workspace_bytes)) {
     c.fail(DATTN_EWORKSPACE, "workspace too small or misaligned");

@@ -55,6 +55,7 @@ inline int states_per_item(int rows, int fmt, bool kivi_tc) {
 // One unit of producer work: keys [a, e) of the visible stream of group (b, h).
 // Interval programs: stream index j maps to position j < x0 ? j : x1 + (j - x0).
 // Index lists: x0 is the list offset of the group, position = index_list[x0 + j].
+// FlashMask: position = j (x0 = T), x1 = the request's row offset in fm_intervals.
 struct WorkItem {
   int32_t b, h, a, e, slot, T, x0, x1;
 };
@@ -99,6 +100,7 @@ struct PartialParams {
   const int32_t* cache_batch_idx;
   const int32_t* index_indptr;
   const int32_t* index_list;
+  const int32_t* fm_intervals;   // FLASHMASK: [sum T_b, 4]
   void* o;
   float* lse;
   const WorkItem* items;

@@ -56,7 +56,8 @@ struct Bf {
   static constexpr int kTile = kTK * kRowB;        // one tensor's stage tile
   static constexpr int kStage = 2 * kTile;
   static constexpr int kPos = kStagesN * kStage;   // int32 [stages][kTK]: logical key or -1
-  static constexpr int kFlags = kPos + kStagesN * kTK * 4;
+  static constexpr int kVis = kPos + kStagesN * kTK * 4;   // uint32 [stages][kTK]: FlashMask row bits
+  static constexpr int kFlags = kVis + kStagesN * kTK * 4;
   static constexpr int kSeq = kFlags + kStagesN * 4;   // int32 [stages]: stage number
   static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
@@ -67,7 +68,7 @@ struct Bf {
 };
 
 
-template <int D>
+template <int D, bool FM>
 __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
   using C = Bf<D>;
   const PartialParams& p = w.p;
@@ -93,9 +94,9 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   SlotKeys<2> k2 = slot_keys<2>(w, c2, lane);
   // Up to here only the plan was read; the page table is a device input.
   dependency_wait(dep_wait);
-  const SlotPages<2> g0 = slot_pages<2>(w, c0, k0);     // both stages' page lookups in flight together
-  SlotPages<2> g1 = slot_pages<2>(w, c1, k1);
-  SlotRows<2> r0 = slot_rows<2>(w, c0, k0, g0, lane);
+  const SlotPages<2, FM> g0 = slot_pages<2, FM>(w, c0, k0);     // both stages' page lookups in flight together
+  SlotPages<2, FM> g1 = slot_pages<2, FM>(w, c1, k1);
+  SlotRows<2, FM> r0 = slot_rows<2, FM>(w, c0, k0, g0, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
@@ -104,6 +105,11 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
     pos[lane] = r0.t[0];
     pos[lane + 32] = r0.t[1];
+    if constexpr (FM) {
+      uint32_t* vis = reinterpret_cast<uint32_t*>(smem + C::kVis) + st * kTK;
+      vis[lane] = r0.vis[0];
+      vis[lane + 32] = r0.vis[1];
+    }
     if (lane == 0) {
       reinterpret_cast<int*>(smem + C::kFlags)[st] = r0.full ? kFlagFull : 0;
       reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
@@ -125,9 +131,9 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
     if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
 
     // move the description pipeline one stage of this warp forward
-    r0 = slot_rows<2>(w, c1, k1, g1, lane);
+    r0 = slot_rows<2, FM>(w, c1, k1, g1, lane);
     c0 = c1;
-    g1 = slot_pages<2>(w, c2, k2);
+    g1 = slot_pages<2, FM>(w, c2, k2);
     k1 = k2;
     c1 = c2;
     pc_advance<kTK>(w, c2, kProducerWarps);
@@ -207,6 +213,7 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
   const int qi0 = r0 / p.g, qi1 = r1 / p.g;
   const int lrow = lane & 7, lmat = lane >> 3;   // ldmatrix address roles
   const float sc = p.scale_log2;
+  const bool fm = p.mask == DATTN_MASK_FLASHMASK;
 
   uint32_t k = 0;
   bool dead = false;   // a bounded wait gave up: stop consuming, write nothing
@@ -246,6 +253,7 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
         break;
       }
       const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kTK;
+      const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kTK;
       const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
       const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
       const int base = ts * 16;
@@ -268,9 +276,17 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
       for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int t = pos[base + nt * 8 + 2 * t4 + e];
-          const bool v0 = t >= 0 && ok0 && (full || key_visible(mc, qi0, t));
-          const bool v1 = t >= 0 && ok1 && (full || key_visible(mc, qi1, t));
+          const int slot = base + nt * 8 + 2 * t4 + e;
+          const int t = pos[slot];
+          bool v0, v1;
+          if (fm) {   // FlashMask: the producer's row bits of the column
+            const uint32_t bits = vis[slot];
+            v0 = t >= 0 && ok0 && (full || ((bits >> qi0) & 1u));
+            v1 = t >= 0 && ok1 && (full || ((bits >> qi1) & 1u));
+          } else {
+            v0 = t >= 0 && ok0 && (full || key_visible(mc, qi0, t));
+            v1 = t >= 0 && ok1 && (full || key_visible(mc, qi1, t));
+          }
           s[nt][e] = v0 ? s[nt][e] * sc : -INFINITY;
           s[nt][2 + e] = v1 ? s[nt][2 + e] * sc : -INFINITY;
         }
@@ -443,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBfProducerRegs));
-    produce_bf16<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    if (p.mask == DATTN_MASK_FLASHMASK) produce_bf16<D, true>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    else produce_bf16<D, false>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));

@@ -58,7 +58,9 @@ void check_problem(const dattn_problem* p, Checker& c) {
   if (p->layout != DATTN_KV_CONTIG_NHD && p->layout != DATTN_KV_PAGED_HND)
     c.fail(DATTN_EINVAL, "unknown layout");
   if (p->fmt < DATTN_FMT_BF16 || p->fmt > DATTN_FMT_FP8_E5M2) c.fail(DATTN_EINVAL, "unknown format");
-  if (p->mask < DATTN_MASK_CAUSAL || p->mask > DATTN_MASK_INDEX_LIST) c.fail(DATTN_EINVAL, "unknown mask");
+  if (p->mask < DATTN_MASK_CAUSAL || p->mask > DATTN_MASK_FLASHMASK) c.fail(DATTN_EINVAL, "unknown mask");
+  if (p->mask == DATTN_MASK_FLASHMASK && p->fmt != DATTN_FMT_BF16)
+    c.fail(DATTN_EUNSUPPORTED, "flashmask runs on bf16 K/V");
   // K/V rows (one kv head, one token) are addressed with 32-bit row indices
   const long long kMaxPoolRows = 0xFFFFFFFFll;
   if (p->layout == DATTN_KV_PAGED_HND) {
@@ -197,6 +199,11 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   }
   if (p.mask == DATTN_MASK_INDEX_LIST && in->index_indptr[0] != 0)
     c.fail(DATTN_EINVAL, "index_indptr[0] must be 0");
+  if (p.mask == DATTN_MASK_FLASHMASK) {
+    long long keys = 0;
+    for (int b = 0; b < B; ++b) keys += std::max(0, in->kv_len[b]);
+    if (keys > INT32_MAX / 4) c.fail(DATTN_EUNSUPPORTED, "flashmask intervals of more than 2^29 keys");
+  }
   if (c.status != DATTN_OK) return c.finish("dattn_plan");
 
   auto* plan = new dattn_plan_s();
@@ -207,8 +214,8 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
 
   // 1. visible key stream of every group
   std::vector<int> gn(n_groups), gx0(n_groups), gx1(n_groups);
-  long long W = 0;
-  for (int b = 0; b < B; ++b)
+  long long W = 0, fm_off = 0;
+  for (int b = 0; b < B; ++b) {
     for (int h = 0; h < H; ++h) {
       const int k = b * H + h;
       int len = 0, off = 0;
@@ -217,8 +224,13 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
         len = in->index_indptr[k + 1] - off;
       }
       stream_of(p, in->kv_len[b], len, off, gn[k], gx0[k], gx1[k]);
+      // FlashMask: every stored key is in the stream; x1 locates the request's intervals
+      if (p.mask == DATTN_MASK_FLASHMASK) gx1[k] = static_cast<int>(fm_off);
       W += gn[k];
     }
+    fm_off += in->kv_len[b];
+  }
+
 
   // 2. chunks.  Three modes:
   //  - fixed_splits > 0: balanced quotient/remainder bounds per group (§0x03B);

@@ -247,16 +247,24 @@ template <int S>
 struct SlotKeys {
   int t[S];      // logical key (-1: none)
 };
-template <int S>
+template <int S, bool FM = false>
 struct SlotPages {
   int pi[S];     // page id of the key's block (-2: block outside the page list)
+  int4 iv[FM ? S : 1];   // FlashMask: the key column's (UTS, UTE, LTS, LTE)
 };
-template <int S>
+template <int S, bool FM = false>
 struct SlotRows {
   int t[S];           // logical key, -1 when the slot is empty or invalid
   uint32_t row[S];    // K/V row in the cache in rows of d elements (kNoRow: none)
+  uint32_t vis[FM ? S : 1];   // FlashMask: bit i set when query row i sees the key
   bool full;          // FULL stage class
 };
+
+// Bits [a, b) of a 32-bit row mask (clipped to [0, 32)).
+__device__ __forceinline__ uint32_t row_bits(int a, int b) {
+  auto below = [](int x) { return x <= 0 ? 0u : x >= 32 ? 0xFFFFFFFFu : (1u << x) - 1u; };
+  return b > a ? below(b) & ~below(a) : 0u;
+}
 
 template <int S>
 __device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, int lane) {
@@ -273,13 +281,25 @@ __device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, i
   return k;
 }
 
-template <int S>
-__device__ __forceinline__ SlotPages<S> slot_pages(const Walk& w, const PCur& c, const SlotKeys<S>& k) {
-  SlotPages<S> g;
+template <int S, bool FM = false>
+__device__ __forceinline__ SlotPages<S, FM> slot_pages(const Walk& w, const PCur& c, const SlotKeys<S>& k) {
+  SlotPages<S, FM> g;
 #pragma unroll
   for (int h = 0; h < S; ++h) g.pi[h] = -2;
-  if (c.ii >= w.end || w.p.layout != DATTN_KV_PAGED_HND) return g;
+  if constexpr (FM) {
+#pragma unroll
+    for (int h = 0; h < S; ++h) g.iv[h] = make_int4(0, 0, 0, 0);
+  }
+  if (c.ii >= w.end) return g;
   const ItemRec r = w.rec(c.ii);
+  if constexpr (FM) {   // the column intervals travel with the page ids
+#pragma unroll
+    for (int h = 0; h < S; ++h) {
+      const int t = k.t[h];
+      if (t >= 0 && t < r.it.T) g.iv[h] = *reinterpret_cast<const int4*>(w.p.fm_intervals + 4ll * (r.it.x1 + t));
+    }
+  }
+  if (w.p.layout != DATTN_KV_PAGED_HND) return g;
 #pragma unroll
   for (int h = 0; h < S; ++h) {
     const int t = k.t[h];
@@ -291,15 +311,16 @@ __device__ __forceinline__ SlotPages<S> slot_pages(const Walk& w, const PCur& c,
   return g;
 }
 
-template <int S>
-__device__ __forceinline__ SlotRows<S> slot_rows(const Walk& w, const PCur& c, const SlotKeys<S>& k,
-                                                 const SlotPages<S>& g, int lane) {
+template <int S, bool FM = false>
+__device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& c, const SlotKeys<S>& k,
+                                                     const SlotPages<S, FM>& g, int lane) {
   const PartialParams& p = w.p;
-  SlotRows<S> d;
+  SlotRows<S, FM> d;
 #pragma unroll
   for (int h = 0; h < S; ++h) {
     d.t[h] = -1;
     d.row[h] = kNoRow;
+    if constexpr (FM) d.vis[h] = 0u;
   }
   d.full = false;
   if (c.ii >= w.end) return d;
@@ -312,6 +333,11 @@ __device__ __forceinline__ SlotRows<S> slot_rows(const Walk& w, const PCur& c, c
     if (p.mask == DATTN_MASK_INDEX_LIST && c.j0 + lane + 32 * h < c.j1 && (t < 0 || t >= r.it.T)) {
       atomicOr(p.status, kStListRange);
       t = -1;
+    }
+    if constexpr (FM) {   // a column hidden from every query row is never loaded
+      const uint32_t rows = row_bits(0, p.S_q);
+      d.vis[h] = t >= 0 ? rows & ~(row_bits(g.iv[h].x, g.iv[h].y) | row_bits(g.iv[h].z, g.iv[h].w)) : 0u;
+      if (d.vis[h] == 0u) t = -1;
     }
     if (t >= 0) {
       if (p.layout == DATTN_KV_PAGED_HND) {
@@ -330,7 +356,15 @@ __device__ __forceinline__ SlotRows<S> slot_rows(const Walk& w, const PCur& c, c
     d.row[h] = row;
     tmax = max(tmax, t);
   }
-  d.full = stage_is_full(p, r.it, c.j0, c.j1, tmax, -1);
+  if constexpr (FM) {   // FULL: every slot of the stage holds a key that every row sees
+    bool all = true;
+#pragma unroll
+    for (int h = 0; h < S; ++h)
+      if (c.j0 + lane + 32 * h < c.j1) all = all && d.vis[h] == row_bits(0, p.S_q);
+    d.full = __all_sync(kAll, all);
+  } else {
+    d.full = stage_is_full(p, r.it, c.j0, c.j1, tmax, -1);
+  }
   return d;
 }
 

@@ -45,6 +45,9 @@ def oracle_problem(w) -> dict:
     if w.index_list is not None:
         p["index_indptr"] = w.index_indptr.numpy()
         p["index_list"] = w.index_list.numpy()
+    if w.fm_intervals is not None:
+        p["fm_intervals"] = w.fm_intervals.numpy()
+        p["fm_indptr"] = np.concatenate([[0], np.cumsum(w.kv_len.numpy().astype(np.int64))])
     return p
 
 
@@ -58,6 +61,8 @@ def device_tensors(w, o, lse, dev="cuda"):
     if w.index_list is not None:
         kw["index_indptr"] = w.index_indptr.to(dev)
         kw["index_list"] = w.index_list.to(dev)
+    if w.fm_intervals is not None:
+        kw["fm_intervals"] = w.fm_intervals.to(dev).contiguous()
     return kw
 
 

@@ -276,3 +276,75 @@ def test_fused_merge_matches_and_counters_reset_for_reused_uploads(chunk, num_sm
         assert dattn.dattn_device_status(keep["ws"]) == 0
         assert torch.equal(keep["kw"]["o"].float().cpu(), O)
         assert torch.equal(keep["kw"]["lse"].cpu(), L)
+
+
+# ---- FlashMask two-interval columns (M4.5 §0x06A-§0x06D) ---------------------------------
+
+@pytest.mark.parametrize("chunk,num_sms", [(0, 152), (64, 5)])
+def test_flashmask_speculation_tree_all_rows(chunk, num_sms):
+    """8 draft rows of a DFS-ordered tree (32 query rows per kv head) over short prefixes."""
+    w = W.tree_verify("cuda", B=4, S_q=8, lo=1, hi=300, seed=7)
+    O, L, info, flags = H.run_gpu(w, chunk_tokens=chunk, num_sms=num_sms)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+def _random_fm_intervals(rng, lens, S_q):
+    out = []
+    for T in lens:
+        a = np.sort(rng.integers(0, S_q + 1, size=(T, 2)), axis=1)
+        b = np.sort(rng.integers(0, S_q + 1, size=(T, 2)), axis=1)
+        iv = np.concatenate([a, b], axis=1)
+        iv[rng.random(T) < 0.2] = [0, S_q, 0, 0]          # columns hidden from every row
+        iv[rng.random(T) < 0.3] = [0, 0, 0, 0]            # columns every row sees
+        out.append(iv)
+    return np.concatenate(out) if out else np.zeros((0, 4), np.int64)
+
+
+@pytest.mark.parametrize("S_q,H_q,H_kv", [(4, 16, 2), (1, 8, 2), (32, 32, 32), (3, 16, 4)])
+def test_flashmask_random_intervals_with_hidden_columns_and_rows(S_q, H_q, H_kv):
+    lens = [300, 65, 1, 0, 130]
+    w = W.paged_bf16("fm", B=len(lens), S_q=S_q, H_q=H_q, H_kv=H_kv, d=128, lens=lens, P=16, seed=32,
+                     device="cuda")
+    rng = np.random.default_rng(33 + S_q)
+    iv = _random_fm_intervals(rng, lens, S_q)
+    iv[sum(lens[:2])] = [0, S_q, 0, 0]                     # request 2: its only key hidden from all rows
+    w.problem = dict(w.problem, mask="flashmask")
+    w.fm_intervals = torch.tensor(iv, dtype=torch.int32)
+    O, L, info, flags = H.run_gpu(w, chunk_tokens=64, num_sms=7)
+    assert flags == 0
+    assert torch.isinf(L[2]).all() and (L[2] < 0).all()
+    H.compare(O, L, w)
+
+
+def test_flashmask_causal_rewrite_agrees_with_causal():
+    lens = [257, 40, 4]
+    S_q = 4
+    w = W.paged_bf16("fmc", B=3, S_q=S_q, H_q=16, H_kv=4, d=128, lens=lens, P=16, seed=34, device="cuda")
+    O0, L0, _, _ = H.run_gpu(w, chunk_tokens=64, num_sms=5)
+    H.compare(O0, L0, w)
+    iv = []
+    for T in lens:
+        iv += [(0, max(0, min(S_q, j - (T - S_q))), 0, 0) for j in range(T)]
+    w.problem = dict(w.problem, mask="flashmask")
+    w.fm_intervals = torch.tensor(iv, dtype=torch.int32)
+    O1, L1, _, flags = H.run_gpu(w, chunk_tokens=64, num_sms=5)
+    assert flags == 0
+    H.compare(O1, L1, w)
+    assert torch.allclose(O0, O1, atol=1e-2, rtol=1e-2) and torch.allclose(L0, L1, atol=1e-4, rtol=1e-5)
+
+
+def test_flashmask_tree_verify_full_size_sampled():
+    """The tree-verification workload: B=16, prefixes U[1024, 8192], 8 draft rows."""
+    w = W.tree_verify("cuda")
+    O, L, info, flags = H.run_gpu(w)
+    assert flags == 0
+    H.finite_or_masked(O, L)
+    rows = H.sample_rows(w.problem, 96, seed=2, must=[(0, 0, 0), (15, 7, 31)])
+    H.compare(O, L, w, rows)
+
+
+def test_flashmask_rejected_for_byte_formats():
+    p = dict(B=1, S_q=1, H_q=8, H_kv=2, d=128, layout="paged", fmt="int8", P=16, num_pages=4, mask="flashmask")
+    with pytest.raises(dattn.DattnError, match="flashmask runs on bf16"):
+        dattn.dattn_plan(p, [10], page_indptr=np.array([0, 1], np.int32), num_sms=4)

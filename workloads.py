@@ -57,6 +57,7 @@ class Workload:
     cache_batch_idx: torch.Tensor = None
     index_indptr: torch.Tensor = None         # int32 [B*H_kv+1] CPU
     index_list: torch.Tensor = None           # int32 CPU
+    fm_intervals: torch.Tensor = None         # int32 [sum T_b, 4] CPU, FlashMask (UTS, UTE, LTS, LTE)
     rows_indptr: torch.Tensor = None          # packed ragged history (quantized workloads)
     k_rows: torch.Tensor = None
     v_rows: torch.Tensor = None
@@ -248,3 +249,40 @@ def quantized(device="cpu", fmt="int8", B=32, lo=2048, hi=32768):
     lens = torch.randint(lo, hi + 1, (B,), generator=meta).tolist()
     return quantized_history(f"quantized KV ({fmt}) B={B} T~U[{lo},{hi}]", B=B, S_q=1, H_q=32,
                              H_kv=8, d=128, lens=lens, P=16, seed=4, device=device, fmt=fmt)
+
+
+def _dfs_tree_intervals(S_q: int, gen) -> list:
+    """A random speculation tree of S_q draft tokens in DFS order: the rows that see draft
+    r form its subtree [r, e_r), so its column hides U = [0, r) and L = [e_r, S_q)."""
+    parent = [-1] + [int(torch.randint(0, j, (1,), generator=gen)) for j in range(1, S_q)]
+    children = [[] for _ in range(S_q)]
+    for j in range(1, S_q):
+        children[parent[j]].append(j)
+    order, span = [], {}
+
+    def visit(u):
+        start = len(order)
+        order.append(u)
+        for c in children[u]:
+            visit(c)
+        span[u] = (start, len(order))
+    visit(0)
+    return [(0, span[u][0], span[u][1], S_q) for u in order]
+
+
+def tree_verify(device="cpu", B=16, S_q=8, lo=1024, hi=8192, seed=5):
+    """Speculative-tree verification: each request's stored keys are a prefix of lo..hi
+    tokens followed by S_q draft tokens in DFS order; query row r is draft r and sees the
+    whole prefix and its ancestors' drafts (FlashMask intervals, one set per request)."""
+    meta = torch.Generator().manual_seed(seed)
+    prefix = torch.randint(lo, hi + 1, (B,), generator=meta).tolist()
+    lens = [t + S_q for t in prefix]
+    w = paged_bf16(f"speculative tree verify B={B} S_q={S_q} H_q=32 H_kv=8 d=128 P=16 prefix~U[{lo},{hi}]",
+                   B=B, S_q=S_q, H_q=32, H_kv=8, d=128, lens=lens, P=16, seed=seed, device=device)
+    iv = []
+    for b in range(B):
+        iv += [(0, 0, 0, 0)] * prefix[b]
+        iv += _dfs_tree_intervals(S_q, meta)
+    w.problem = dict(w.problem, mask="flashmask")
+    w.fm_intervals = torch.tensor(iv, dtype=torch.int32)
+    return w
