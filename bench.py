@@ -37,8 +37,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "tree-verify", "int8", "fp8", "fp8-e5m2",
-                   "int4-kivi")
+OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "tree-verify", "mixed", "int8", "fp8",
+                   "fp8-e5m2", "int4-kivi")
 
 
 def parse():
@@ -532,7 +532,7 @@ def run_other(args):
         w = {"long-s1": lambda: W.long_context(dev, 1), "long-s4": lambda: W.long_context(dev, 4),
              "sink-window": lambda: W.retention(dev, "sink_window"),
              "index-list": lambda: W.retention(dev, "index_list"),
-             "tree-verify": lambda: W.tree_verify(dev)}[name]()
+             "tree-verify": lambda: W.tree_verify(dev), "mixed": lambda: W.mixed_batch(dev)}[name]()
         p = w.problem
         cache = dict(k=w.k, v=w.v, page_indptr=w.page_indptr.to(dev), page_indices=w.page_indices.to(dev))
         if w.index_list is not None:
@@ -541,9 +541,11 @@ def run_other(args):
             cache.update(fm_intervals=w.fm_intervals.to(dev).contiguous())
     props = torch.cuda.get_device_properties(dev)
     plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, index_indptr=w.index_indptr,
-                            index_list=w.index_list, num_sms=props.multi_processor_count, chunk_tokens=args.chunk)
-    o = torch.empty((p["B"], p["S_q"], p["H_q"], p["d"]), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((p["B"], p["S_q"], p["H_q"]), dtype=torch.float32, device=dev)
+                            index_list=w.index_list, num_sms=props.multi_processor_count, chunk_tokens=args.chunk,
+                            qo_indptr=w.qo_indptr)
+    n_rows = p["B"] * p["S_q"] if w.qo_indptr is None else int(w.qo_indptr[-1])   # packed query rows
+    o = torch.empty((n_rows, p["H_q"], p["d"]), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((n_rows, p["H_q"]), dtype=torch.float32, device=dev)
     t = dattn.tensors_from(q=w.q.to(dev), o=o, lse=lse, **cache)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()

@@ -152,6 +152,12 @@ typedef struct {
                                    launch); 0: by the LSE-merge kernel.  Off by default: on
                                    GB300 the merge then sits on the partial kernel's tail,
                                    and the step is slower (see the design notes)          */
+  const int32_t* qo_indptr;     /* host [B+1] or NULL: a mixed batch (M4.5 §0x08F).  Request
+                                   b has C_b = qo_indptr[b+1] - qo_indptr[b] query rows
+                                   (0 <= C_b <= S_q), packed rows qo_indptr[b] .. of q, o
+                                   and lse ([qo_indptr[B], H_q, d] and [qo_indptr[B], H_q]),
+                                   at positions T_b - C_b + i (bottom-right).  NULL: C_b =
+                                   S_q for every request.  Non-uniform C_b: bf16 K/V only */
 } dattn_plan_inputs;
 
 typedef struct dattn_plan_s dattn_plan_t;

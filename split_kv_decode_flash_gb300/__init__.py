@@ -51,7 +51,8 @@ class PlanInputs(ctypes.Structure):
     _fields_ = [("kv_len", ctypes.c_void_p), ("page_indptr", ctypes.c_void_p),
                 ("index_indptr", ctypes.c_void_p), ("index_list", ctypes.c_void_p),
                 ("num_sms", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
-                ("chunk_tokens", ctypes.c_int32), ("fused_merge", ctypes.c_int32)]
+                ("chunk_tokens", ctypes.c_int32), ("fused_merge", ctypes.c_int32),
+                ("qo_indptr", ctypes.c_void_p)]
 
 
 class Tensors(ctypes.Structure):
@@ -211,16 +212,17 @@ class Plan:
 
 
 def dattn_plan(problem, kv_len, *, page_indptr=None, index_indptr=None, index_list=None, num_sms=None,
-               ctas_per_sm=0, chunk_tokens=0, fused_merge=False) -> Plan:
+               ctas_per_sm=0, chunk_tokens=0, fused_merge=False, qo_indptr=None) -> Plan:
     """Host-only planning (see dattn_plan in dattn.h).  Arrays are host int32."""
     lib = load()
     prob = problem if isinstance(problem, Problem) else make_problem(problem)
     if num_sms is None:
         import torch
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    keep = [_i32_host(kv_len), _i32_host(page_indptr), _i32_host(index_indptr), _i32_host(index_list)]
+    keep = [_i32_host(kv_len), _i32_host(page_indptr), _i32_host(index_indptr), _i32_host(index_list),
+            _i32_host(qo_indptr)]
     inp = PlanInputs(_ptr(keep[0]), _ptr(keep[1]), _ptr(keep[2]), _ptr(keep[3]), int(num_sms),
-                     int(ctas_per_sm), int(chunk_tokens), int(bool(fused_merge)))
+                     int(ctas_per_sm), int(chunk_tokens), int(bool(fused_merge)), _ptr(keep[4]))
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     _check(lib.dattn_plan(ctypes.byref(prob), ctypes.byref(inp), ctypes.byref(handle), ctypes.byref(ws)),

@@ -63,7 +63,10 @@ static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 
 struct MergeGroup {
   int32_t b, h, slot0, n;
+  int32_t qo, nq;      // request b's first packed query row and its query rows C_b
+  int32_t pad0, pad1;
 };
+static_assert(sizeof(MergeGroup) == 32, "MergeGroup layout");
 
 // A work item with its request's page-list bounds, stored in CTA order so a
 // CTA reads its items with one dependent load.
@@ -72,8 +75,10 @@ struct ItemRec {
   int32_t lo, hi;      // paged layout: page list entries [lo, hi) of request it.b
   int32_t crow;        // contiguous layout: cache row, resolved by the kernel
   int32_t merge;       // index of the item's merge group, -1 when it writes O directly
+  int32_t qo, nq;      // request it.b's first packed query row and its query rows C_b
+  int32_t pad0, pad1;
 };
-static_assert(sizeof(ItemRec) == 48, "ItemRec layout");
+static_assert(sizeof(ItemRec) == 64, "ItemRec layout");
 
 // Head of the plan blob, copied to the start of the workspace by every run.
 struct BlobHeader {

@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = blockIdx.x / p.rows, row = blockIdx.x % p.rows;
   const MergeGroup grp = p.groups[gi];
+  if (row >= p.g * grp.nq) return;   // the request has fewer query rows than the widest one
 
   // warp w folds states w, w + kMergeWarps, ...
   RowFold<D> f;
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
     }
   }
   const int i = row / p.g, hq = grp.h * p.g + row % p.g;
-  write_folded_row<D>(p.o, p.lse, (static_cast<long long>(grp.b) * p.S_q + i) * p.H_q + hq, t, lane);
+  write_folded_row<D>(p.o, p.lse, (static_cast<long long>(grp.qo) + i) * p.H_q + hq, t, lane);
 }
 
 template <int D>

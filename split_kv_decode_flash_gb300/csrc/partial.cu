@@ -347,7 +347,7 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
 
     // stage class
     int flags = resid ? kFlagResidual : 0;
-    const bool full = stage_is_full(p, cur.it, cur.j0, cur.j1, t0, t1);
+    const bool full = stage_is_full(p, cur.it, p.S_q, cur.j0, cur.j1, t0, t1);
     if (full) flags |= kFlagFull;
     if (lane == 0) {
       reinterpret_cast<int*>(smem + C::kFlags)[st] = flags;

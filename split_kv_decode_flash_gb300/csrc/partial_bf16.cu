@@ -146,11 +146,12 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
 
 // Writes one query row of a warp's result: O / LSE when the item is its
 // group's only state, else the row's partial state (m in log2 units, l, u).
+// qo: the request's first packed query row.
 template <int D>
-__device__ __forceinline__ void emit_row(const PartialParams& p, const WorkItem& it, int my_state, int row, float m,
-                                         float l, const float (&o)[D / 8][4], int half, int t4) {
+__device__ __forceinline__ void emit_row(const PartialParams& p, const WorkItem& it, int qo, int my_state, int row,
+                                         float m, float l, const float (&o)[D / 8][4], int half, int t4) {
   const int i = row / p.g, hq = it.h * p.g + row % p.g;
-  const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
+  const long long orow = (static_cast<long long>(qo) + i) * p.H_q + hq;
   if (it.slot < 0) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
@@ -169,16 +170,16 @@ __device__ __forceinline__ void emit_row(const PartialParams& p, const WorkItem&
   }
 }
 
-// The two accumulator rows r0, r1 of a lane, for item "it", as mma A
-// fragments (rows past the group are zero).
+// The two accumulator rows r0, r1 of a lane, for item record "r", as mma A
+// fragments (rows past the request's g C_b rows are zero).
 template <int D>
-__device__ __forceinline__ void load_q(const PartialParams& p, const WorkItem& it, int r0, int r1, int t4,
+__device__ __forceinline__ void load_q(const PartialParams& p, const ItemRec& r, int r0, int r1, int t4,
                                        uint32_t (&qa)[D / 16][4]) {
-  const bool ok0 = r0 < p.rows, ok1 = r1 < p.rows;
+  const bool ok0 = r0 < p.g * r.nq, ok1 = r1 < p.g * r.nq;
   const uint32_t* q0 = static_cast<const uint32_t*>(p.q) +
-                       ((static_cast<long long>(it.b) * p.S_q + r0 / p.g) * p.H_q + it.h * p.g + r0 % p.g) * (D / 2);
+                       ((static_cast<long long>(r.qo) + r0 / p.g) * p.H_q + r.it.h * p.g + r0 % p.g) * (D / 2);
   const uint32_t* q1 = static_cast<const uint32_t*>(p.q) +
-                       ((static_cast<long long>(it.b) * p.S_q + r1 / p.g) * p.H_q + it.h * p.g + r1 % p.g) * (D / 2);
+                       ((static_cast<long long>(r.qo) + r1 / p.g) * p.H_q + r.it.h * p.g + r1 % p.g) * (D / 2);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     qa[kk][0] = ok0 ? q0[8 * kk + t4] : 0u;
@@ -209,7 +210,6 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
   const int my_state = (cw - rb) / nrb;
   const int g4 = lane >> 2, t4 = lane & 3;
   const int r0 = rb * 16 + g4, r1 = r0 + 8;   // the lane's two accumulator rows
-  const bool ok0 = r0 < p.rows, ok1 = r1 < p.rows;
   const int qi0 = r0 / p.g, qi1 = r1 / p.g;
   const int lrow = lane & 7, lmat = lane >> 3;   // ldmatrix address roles
   const float sc = p.scale_log2;
@@ -219,16 +219,18 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
   bool dead = false;   // a bounded wait gave up: stop consuming, write nothing
   // the next item's query fragments are loaded while the current item runs
   uint32_t qn[KS][4];
-  if (w.begin < w.end) load_q<D>(p, w.rec(w.begin).it, r0, r1, t4, qn);
+  if (w.begin < w.end) load_q<D>(p, w.rec(w.begin), r0, r1, t4, qn);
   for (int ii = w.begin; ii < w.end; ++ii) {
-    const WorkItem it = w.rec(ii).it;
-    const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+    const ItemRec rec = w.rec(ii);
+    const WorkItem it = rec.it;
+    const MaskCtx mc{p.mask, rec.nq, it.T, p.n_sink, p.window};
+    const bool ok0 = r0 < p.g * rec.nq, ok1 = r1 < p.g * rec.nq;   // rows of the request
     uint32_t qa[KS][4];
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
       for (int x = 0; x < 4; ++x) qa[kk][x] = qn[kk][x];
-    if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1).it, r0, r1, t4, qn);
+    if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1), r0, r1, t4, qn);
     float o[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -344,8 +346,8 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
     l0 += __shfl_xor_sync(kAll, l0, 2);
     l1 += __shfl_xor_sync(kAll, l1, 2);
     if (!dead) {
-      if (ok0) emit_row<D>(p, it, my_state, r0, m0, l0, o, 0, t4);
-      if (ok1) emit_row<D>(p, it, my_state, r1, m1, l1, o, 1, t4);
+      if (ok0) emit_row<D>(p, it, rec.qo, my_state, r0, m0, l0, o, 0, t4);
+      if (ok1) emit_row<D>(p, it, rec.qo, my_state, r1, m1, l1, o, 1, t4);
     }
   }
 }
@@ -391,7 +393,7 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
     const MergeGroup grp = p.groups[gi];
     for (int r0 = 0; r0 < R; r0 += kCW / W) {
       const int row = r0 + cw / W, share = cw % W;
-      const bool active = cw / W < kCW / W && row < R;
+      const bool active = cw / W < kCW / W && row < p.g * grp.nq;
       RowFold<D> f;
       fold_init(f);
       if (active) {
@@ -425,7 +427,7 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
       }
       if (active && share == 0) {
         const int i = row / p.g, hq = grp.h * p.g + row % p.g;
-        write_folded_row<D>(p.o, p.lse, (static_cast<long long>(grp.b) * p.S_q + i) * p.H_q + hq, f, lane);
+        write_folded_row<D>(p.o, p.lse, (static_cast<long long>(grp.qo) + i) * p.H_q + hq, f, lane);
       }
     }
     if (cw == 0 && lane == 0) p.group_count[gi] = 0;    // ready for the next run

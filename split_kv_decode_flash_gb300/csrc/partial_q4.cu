@@ -267,7 +267,7 @@ __device__ __forceinline__ Q4Desc q4_rows(const Walk& w, const QCur& c, const in
     }
   }
   if (err) atomicOr(p.status, err);
-  d.full = stage_is_full(p, r.it, c.j0, c.j1, tmax, -1);
+  d.full = stage_is_full(p, r.it, r.nq, c.j0, c.j1, tmax, -1);
   return d;
 }
 

@@ -102,8 +102,12 @@ bool same_problem(const dattn_problem& a, const dattn_problem& b) {
 }
 
 // Visible key stream of one group: length and the two-interval map.
-static void stream_of(const dattn_problem& p, int T, int list_len, int list_off, int& n, int& x0,
+static void stream_of(const dattn_problem& p, int T, int C, int list_len, int list_off, int& n, int& x0,
                       int& x1) {
+  if (C == 0) {   // a request without query rows reads nothing
+    n = x0 = x1 = 0;
+    return;
+  }
   if (p.mask == DATTN_MASK_INDEX_LIST) {
     n = list_len;
     x0 = list_off;
@@ -112,9 +116,9 @@ static void stream_of(const dattn_problem& p, int T, int list_len, int list_off,
   }
   if (p.mask == DATTN_MASK_SINK_WINDOW) {
     // Union over rows of [0, min(n_sink, F_i)) U [max(0, F_i - W), F_i)
-    // with F_i = max(0, min(T, T - S_q + i + 1)); F_i grows with i.
+    // with F_i = max(0, min(T, T - C + i + 1)); F_i grows with i.
     const int f_max = std::max(0, T);
-    const int f_min = std::max(0, std::min(T, T - p.S_q + 1));
+    const int f_min = std::max(0, std::min(T, T - C + 1));
     const int sink_end = std::min(p.n_sink, f_max);
     const int win_start = std::max(0, f_min - p.window);
     if (win_start <= sink_end) {
@@ -199,6 +203,19 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   }
   if (p.mask == DATTN_MASK_INDEX_LIST && in->index_indptr[0] != 0)
     c.fail(DATTN_EINVAL, "index_indptr[0] must be 0");
+  if (in->qo_indptr) {
+    if (in->qo_indptr[0] != 0) c.fail(DATTN_EINVAL, "qo_indptr[0] must be 0");
+    bool mixed = false;
+    for (int b = 0; b < B; ++b) {
+      const int cb = in->qo_indptr[b + 1] - in->qo_indptr[b];
+      if (cb < 0 || cb > p.S_q)
+        c.fail(DATTN_EINVAL, "request " + std::to_string(b) + " has " + std::to_string(cb) +
+                                 " query rows; 0 <= C_b <= S_q");
+      mixed = mixed || cb != p.S_q;
+    }
+    if (mixed && p.fmt != DATTN_FMT_BF16)
+      c.fail(DATTN_EUNSUPPORTED, "mixed query-row counts run on bf16 K/V");
+  }
   if (p.mask == DATTN_MASK_FLASHMASK) {
     long long keys = 0;
     for (int b = 0; b < B; ++b) keys += std::max(0, in->kv_len[b]);
@@ -213,6 +230,9 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   const int n_groups = B * H;
 
   // 1. visible key stream of every group
+  // request b's packed query rows: qo_indptr[b] .. + C_b (uniform S_q without qo_indptr)
+  auto query_start = [&](int b) { return in->qo_indptr ? in->qo_indptr[b] : b * p.S_q; };
+  auto query_rows = [&](int b) { return in->qo_indptr ? in->qo_indptr[b + 1] - in->qo_indptr[b] : p.S_q; };
   std::vector<int> gn(n_groups), gx0(n_groups), gx1(n_groups);
   long long W = 0, fm_off = 0;
   for (int b = 0; b < B; ++b) {
@@ -223,7 +243,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
         off = in->index_indptr[k];
         len = in->index_indptr[k + 1] - off;
       }
-      stream_of(p, in->kv_len[b], len, off, gn[k], gx0[k], gx1[k]);
+      stream_of(p, in->kv_len[b], query_rows(b), len, off, gn[k], gx0[k], gx1[k]);
       // FlashMask: every stored key is in the stream; x1 locates the request's intervals
       if (p.mask == DATTN_MASK_FLASHMASK) gx1[k] = static_cast<int>(fm_off);
       W += gn[k];
@@ -307,7 +327,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
     max_splits = std::max(max_splits, n);
     if (n * spi > 1) {
       merge_of_group[k] = static_cast<int>(merges.size());
-      merges.push_back(MergeGroup{k / H, k % H, n_slots, n * spi});
+      merges.push_back(MergeGroup{k / H, k % H, n_slots, n * spi, query_start(k / H), query_rows(k / H), 0, 0});
       for (int i = 0; i < n; ++i) items[group_first[k] + i].slot = n_slots + i * spi;
       n_slots += n * spi;
     }
@@ -396,6 +416,8 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
       ItemRec r{};
       r.it = items[i];
       r.merge = merge_of_group[static_cast<size_t>(items[i].b) * H + items[i].h];
+      r.qo = query_start(items[i].b);
+      r.nq = query_rows(items[i].b);
       r.lo = r.hi = -1;      // resolved by the kernel when the host page list is unknown
       if (p.layout == DATTN_KV_PAGED_HND && in->page_indptr) {
         r.lo = in->page_indptr[items[i].b];

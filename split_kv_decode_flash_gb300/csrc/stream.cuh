@@ -118,14 +118,14 @@ __device__ __forceinline__ void advance(const PartialParams& p, Cursor& c, int i
   seek(p, c, it_end, lane);
 }
 
-// FULL when every query row sees every key of stream [j0, j1) of item "it"
-// (M4.5 §0x05C); the consumers then skip the per-element predicate.  For
-// index lists the keys are the lane's two slot keys t0, t1 (-1 when empty):
-// the stage is FULL when the largest listed key is visible to the first (most
-// restricted) row.  Called by all 32 lanes of a warp.
-__device__ __forceinline__ bool stage_is_full(const PartialParams& p, const WorkItem& it, int j0, int j1, int t0,
-                                              int t1) {
-  const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+// FULL when every one of the request's S_q query rows sees every key of stream
+// [j0, j1) of item "it" (M4.5 §0x05C); the consumers then skip the per-element
+// predicate.  For index lists the keys are the lane's two slot keys t0, t1 (-1
+// when empty): the stage is FULL when the largest listed key is visible to the
+// first (most restricted) row.  Called by all 32 lanes of a warp.
+__device__ __forceinline__ bool stage_is_full(const PartialParams& p, const WorkItem& it, int S_q, int j0, int j1,
+                                              int t0, int t1) {
+  const MaskCtx mc{p.mask, S_q, it.T, p.n_sink, p.window};
   if (p.mask == DATTN_MASK_INDEX_LIST) {
     int mx = max(t0, t1);
 #pragma unroll
@@ -135,7 +135,7 @@ __device__ __forceinline__ bool stage_is_full(const PartialParams& p, const Work
   Run r0, r1;
   const int nr = item_runs(it, j0, j1, r0, r1);
   bool full = true;
-  for (int i = 0; i < p.S_q && full; ++i) {
+  for (int i = 0; i < S_q && full; ++i) {
     if (nr > 0 && visible_in_run(mc, i, r0.p0, r0.p1) != r0.p1 - r0.p0) full = false;
     if (nr > 1 && visible_in_run(mc, i, r1.p0, r1.p1) != r1.p1 - r1.p0) full = false;
   }

@@ -95,7 +95,7 @@ __device__ __forceinline__ ItemRec ld_rec_keep(const ItemRec* p, uint64_t pol) {
   int4* d = reinterpret_cast<int4*>(&r);
   const int4* s = reinterpret_cast<const int4*>(p);
 #pragma unroll
-  for (int i = 0; i < 3; ++i)
+  for (int i = 0; i < static_cast<int>(sizeof(ItemRec) / 16); ++i)
     asm volatile("ld.global.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
                  : "=r"(d[i].x), "=r"(d[i].y), "=r"(d[i].z), "=r"(d[i].w)
                  : "l"(s + i), "l"(pol));
@@ -335,7 +335,7 @@ __device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& 
       t = -1;
     }
     if constexpr (FM) {   // a column hidden from every query row is never loaded
-      const uint32_t rows = row_bits(0, p.S_q);
+      const uint32_t rows = row_bits(0, r.nq);
       d.vis[h] = t >= 0 ? rows & ~(row_bits(g.iv[h].x, g.iv[h].y) | row_bits(g.iv[h].z, g.iv[h].w)) : 0u;
       if (d.vis[h] == 0u) t = -1;
     }
@@ -360,10 +360,10 @@ __device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& 
     bool all = true;
 #pragma unroll
     for (int h = 0; h < S; ++h)
-      if (c.j0 + lane + 32 * h < c.j1) all = all && d.vis[h] == row_bits(0, p.S_q);
+      if (c.j0 + lane + 32 * h < c.j1) all = all && d.vis[h] == row_bits(0, r.nq);
     d.full = __all_sync(kAll, all);
   } else {
-    d.full = stage_is_full(p, r.it, c.j0, c.j1, tmax, -1);
+    d.full = stage_is_full(p, r.it, r.nq, c.j0, c.j1, tmax, -1);
   }
   return d;
 }

@@ -48,7 +48,17 @@ def oracle_problem(w) -> dict:
     if w.fm_intervals is not None:
         p["fm_intervals"] = w.fm_intervals.numpy()
         p["fm_indptr"] = np.concatenate([[0], np.cumsum(w.kv_len.numpy().astype(np.int64))])
+    if w.qo_indptr is not None:
+        p["qo_indptr"] = w.qo_indptr.numpy().astype(np.int64)
     return p
+
+
+def query_rows(w, b):
+    """(first packed query row, C_b) of request b."""
+    if w.qo_indptr is None:
+        return b * w.problem["S_q"], w.problem["S_q"]
+    a, e = int(w.qo_indptr[b]), int(w.qo_indptr[b + 1])
+    return a, e - a
 
 
 def device_tensors(w, o, lse, dev="cuda"):
@@ -72,9 +82,10 @@ def run_gpu(w, *, num_sms=None, ctas_per_sm=0, chunk_tokens=0, problem=None, kee
     B, S_q, H_q, d = p["B"], p["S_q"], p["H_q"], p["d"]
     plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, index_indptr=w.index_indptr,
                             index_list=w.index_list, num_sms=num_sms, ctas_per_sm=ctas_per_sm,
-                            chunk_tokens=chunk_tokens, fused_merge=fused_merge)
-    o = torch.full((B, S_q, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lse = torch.full((B, S_q, H_q), float("nan"), dtype=torch.float32, device="cuda")
+                            chunk_tokens=chunk_tokens, fused_merge=fused_merge, qo_indptr=w.qo_indptr)
+    n_rows = B * S_q if w.qo_indptr is None else int(w.qo_indptr[-1])
+    o = torch.full((n_rows, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((n_rows, H_q), float("nan"), dtype=torch.float32, device="cuda")
     ws = torch.empty(max(256, plan.workspace_bytes), dtype=torch.uint8, device="cuda")
     kw = device_tensors(w, o, lse)
     dattn.dattn_run(plan, p, dattn.tensors_from(**kw), ws)
@@ -82,11 +93,23 @@ def run_gpu(w, *, num_sms=None, ctas_per_sm=0, chunk_tokens=0, problem=None, kee
     flags = dattn.dattn_device_status(ws)
     if keep is not None:
         keep.update(plan=plan, ws=ws, kw=kw)
+    if w.qo_indptr is None:
+        o, lse = o.view(B, S_q, H_q, d), lse.view(B, S_q, H_q)
     return o.float().cpu(), lse.cpu(), plan.info, flags
 
 
 def all_rows(p):
-    return [(b, i, h) for b in range(p["B"]) for i in range(p["S_q"]) for h in range(p["H_q"])]
+    """Every (b, i, h_q) query row; i < C_b for a mixed batch."""
+    qo = p.get("qo_indptr")
+    return [(b, i, h) for b in range(p["B"])
+            for i in range(p["S_q"] if qo is None else int(qo[b + 1] - qo[b])) for h in range(p["H_q"])]
+
+
+def gpu_row(O, w, b, i, h):
+    """Row (b, i, h_q) of a GPU result in [B, S_q, H_q, ...] or packed [sum C_b, H_q, ...] form."""
+    if w.qo_indptr is None:
+        return O[b, i, h]
+    return O[int(w.qo_indptr[b]) + i, h]
 
 
 def compare(O, LSE, w, rows=None, cache=None):
@@ -95,8 +118,8 @@ def compare(O, LSE, w, rows=None, cache=None):
     rows = rows or all_rows(p)
     cache = cache or oracle_cache(w)
     Oref, Lref = attention.decode_rows(p, cache, bits(w.q), rows)
-    og = np.stack([O[b, i, h].numpy() for b, i, h in rows]).astype(np.float64)
-    lg = np.array([LSE[b, i, h].item() for b, i, h in rows], dtype=np.float64)
+    og = np.stack([gpu_row(O, w, b, i, h).numpy() for b, i, h in rows]).astype(np.float64)
+    lg = np.array([gpu_row(LSE, w, b, i, h).item() for b, i, h in rows], dtype=np.float64)
     masked = np.isneginf(Lref)
     assert np.array_equal(np.isneginf(lg), masked), "all-masked rows differ"
     assert not og[masked].any(), "masked rows must give exactly zero output"

@@ -274,8 +274,8 @@ def test_fused_merge_matches_and_counters_reset_for_reused_uploads(chunk, num_sm
         dattn.dattn_run_ex(keep["plan"], w.problem, t, keep["ws"], reuse_upload=True)
         torch.cuda.synchronize()
         assert dattn.dattn_device_status(keep["ws"]) == 0
-        assert torch.equal(keep["kw"]["o"].float().cpu(), O)
-        assert torch.equal(keep["kw"]["lse"].cpu(), L)
+        assert torch.equal(keep["kw"]["o"].float().cpu().reshape(O.shape), O)
+        assert torch.equal(keep["kw"]["lse"].cpu().reshape(L.shape), L)
 
 
 # ---- FlashMask two-interval columns (M4.5 §0x06A-§0x06D) ---------------------------------
@@ -348,3 +348,94 @@ def test_flashmask_rejected_for_byte_formats():
     p = dict(B=1, S_q=1, H_q=8, H_kv=2, d=128, layout="paged", fmt="int8", P=16, num_pages=4, mask="flashmask")
     with pytest.raises(dattn.DattnError, match="flashmask runs on bf16"):
         dattn.dattn_plan(p, [10], page_indptr=np.array([0, 1], np.int32), num_sms=4)
+
+
+# ---- mixed prefill / append / decode batches (per-request query rows) -------------------
+
+
+@pytest.mark.parametrize("chunk,num_sms", [(0, 152), (4, 3)])
+def test_mixed_batch_phase_fixture_all_rows(chunk, num_sms):
+    """The three-request mix of the phase fixture: prefill (0,4), append (6,2), decode (9,1)."""
+    w = W.mixed_batch("cuda", TC=[(0, 4), (6, 2), (9, 1)], seed=40)
+    assert w.qo_indptr.tolist() == [0, 4, 6, 7]
+    O, L, info, flags = H.run_gpu(w, chunk_tokens=chunk, num_sms=num_sms)
+    assert flags == 0
+    assert O.shape == (7, 32, 128)
+    H.compare(O, L, w)
+
+
+@pytest.mark.parametrize("chunk,num_sms,fused", [(0, 152, False), (64, 7, False), (64, 7, True),
+                                                 (100000, 152, False)])
+def test_mixed_batch_small_all_rows(chunk, num_sms, fused):
+    """Every phase plus an idle request, histories spanning several stages and a ragged tail."""
+    TC = [(0, 8), (130, 1), (0, 1), (65, 3), (7, 0), (300, 8), (1, 2), (64, 5), (0, 0), (200, 1)]
+    w = W.mixed_batch("cuda", TC=TC, seed=41)
+    O, L, info, flags = H.run_gpu(w, chunk_tokens=chunk, num_sms=num_sms, fused_merge=fused)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+def test_mixed_batch_sink_window():
+    TC = [(0, 8), (300, 1), (90, 4), (5, 2), (0, 3)]
+    w = W.mixed_batch("cuda", TC=TC, seed=42, mask="sink_window", n_sink=4, window=64)
+    O, L, info, flags = H.run_gpu(w, chunk_tokens=64, num_sms=5)
+    assert flags == 0
+    H.compare(O, L, w)
+
+
+def test_mixed_batch_no_query_rows_at_all():
+    """Every request idle: the launch writes nothing (the one-row buffers stay NaN) and raises no flag."""
+    w = W.mixed_batch("cuda", TC=[(5, 0), (0, 0), (70, 0)], seed=43)
+    p = w.problem
+    plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, qo_indptr=w.qo_indptr, num_sms=8)
+    assert plan.info["stream_keys"] == 0
+    o = torch.full((1, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((1, 32), float("nan"), dtype=torch.float32, device="cuda")
+    q = torch.zeros((1, 32, 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(256, plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+    kw = H.device_tensors(w, o, lse)
+    kw["q"] = q
+    dattn.dattn_run(plan, p, dattn.tensors_from(**kw), ws)
+    torch.cuda.synchronize()
+    assert dattn.dattn_device_status(ws) == 0
+    assert o.isnan().all() and lse.isnan().all()
+
+
+def test_mixed_batch_uniform_indptr_equals_plain_batch():
+    """qo_indptr = [0, S_q, 2 S_q, ...] is the plain batch: identical bits."""
+    w = W.paged_bf16("u", B=3, S_q=4, H_q=16, H_kv=4, d=128, lens=[200, 17, 90], P=16, seed=44, device="cuda")
+    O0, L0, _, _ = H.run_gpu(w, chunk_tokens=64, num_sms=5)
+    w.qo_indptr = torch.arange(0, 13, 4, dtype=torch.int32)
+    w.q = w.q.reshape(12, 16, 128)
+    O1, L1, _, flags = H.run_gpu(w, chunk_tokens=64, num_sms=5)
+    assert flags == 0
+    assert torch.equal(O0.reshape(12, 16, 128), O1) and torch.equal(L0.reshape(12, 16), L1)
+
+
+def test_mixed_batch_full_size_sampled():
+    """B=16: ten decode rows, three appends, two 8-row prefills and one idle request."""
+    w = W.mixed_batch("cuda")
+    O, L, info, flags = H.run_gpu(w)
+    assert flags == 0
+    H.finite_or_masked(O, L)
+    p = H.oracle_problem(w)
+    rows = H.sample_rows(p, 128, seed=3)
+    H.compare(O, L, w, rows)
+
+
+def test_mixed_batch_flashmask_trees_of_different_sizes():
+    """Speculation trees of 1..8 drafts per request: FlashMask intervals in each request's C_b rows."""
+    TC = [(40, 8), (7, 3), (130, 1), (0, 5), (66, 0)]
+    w = W.mixed_batch("cuda", TC=TC, seed=45)
+    iv = []
+    gen = torch.Generator().manual_seed(46)
+    for T, C in TC:
+        iv += [(0, 0, 0, 0)] * T
+        if C:
+            iv += W._dfs_tree_intervals(C, gen)
+    w.problem = dict(w.problem, mask="flashmask")
+    w.fm_intervals = torch.tensor(iv, dtype=torch.int32)
+    assert w.fm_intervals.shape[0] == sum(T + C for T, C in TC)
+    O, L, info, flags = H.run_gpu(w, chunk_tokens=64, num_sms=5)
+    assert flags == 0
+    H.compare(O, L, w)

@@ -229,3 +229,38 @@ def test_run_rejects_stale_plan_and_small_workspace_without_a_gpu():
     with pytest.raises(dattn.DattnError) as e:
         dattn.dattn_run(plan, _problem(), t, Fake(plan.workspace_bytes - 256), stream=0)
     assert dattn.STATUS[e.value.status] == "DATTN_EWORKSPACE"
+
+
+def test_mixed_batch_streams_follow_each_requests_query_rows():
+    """§0x08F: request b's stream is the union of its own C_b rows' visible sets; C_b = 0 reads nothing."""
+    TC = [(0, 4), (6, 2), (9, 1), (30, 0), (100, 3)]
+    T = [t + c for t, c in TC]
+    qo = np.concatenate([[0], np.cumsum([c for _, c in TC])]).astype(np.int32)
+    for mask, extra in (("causal", {}), ("sink_window", dict(n_sink=2, window=5))):
+        prob = _problem(B=len(TC), S_q=4, H_q=4, H_kv=2, mask=mask, **extra)
+        plan = dattn.dattn_plan(prob, T, qo_indptr=qo, num_sms=3, chunk_tokens=64)
+
+        def want(g):
+            C = TC[g[0]][1]
+            vis = [masks.visible_positions(mask, T[g[0]], C, i, **extra) for i in range(C)]
+            return len(np.unique(np.concatenate(vis))) if C else 0
+        _coverage(plan.items(), [(b, h) for b in range(len(TC)) for h in range(2)], want)
+
+
+def test_mixed_batch_validation():
+    prob = _problem(B=3, S_q=4)
+    T = [5, 6, 7]
+    with pytest.raises(dattn.DattnError, match=r"qo_indptr\[0\]"):
+        dattn.dattn_plan(prob, T, qo_indptr=np.array([1, 2, 3, 4], np.int32), num_sms=4)
+    with pytest.raises(dattn.DattnError, match="C_b <= S_q"):
+        dattn.dattn_plan(prob, T, qo_indptr=np.array([0, 5, 6, 7], np.int32), num_sms=4)
+    with pytest.raises(dattn.DattnError, match="0 <= C_b"):
+        dattn.dattn_plan(prob, T, qo_indptr=np.array([0, 2, 1, 3], np.int32), num_sms=4)
+    q8 = _problem(B=3, S_q=4, fmt="int8")
+    with pytest.raises(dattn.DattnError) as e:
+        dattn.dattn_plan(q8, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
+                         qo_indptr=np.array([0, 1, 2, 4], np.int32), num_sms=4)
+    assert dattn.STATUS[e.value.status] == "DATTN_EUNSUPPORTED"
+    # a uniform qo_indptr is the plain batch, for every format
+    dattn.dattn_plan(q8, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
+                     qo_indptr=np.array([0, 4, 8, 12], np.int32), num_sms=4)

@@ -164,3 +164,53 @@ def test_symbolic_gather_through_index_lists():
     assert lst[pr["packed_row"]] == pr["position"]
     assert kpool[pages, pr["h_kv"], rows][pr["packed_row"]].tolist() == pr["K"]
     assert vpool[pages, pr["h_kv"], rows][pr["packed_row"]].tolist() == pr["V"]
+
+
+def test_mixed_batch_rows_follow_their_own_request():
+    """§0x08F mixed batch: packed query rows, C_b per request, bottom-right positions.
+
+    The phase fixture's three requests (prefill (0,4), append (6,2), decode (9,1))
+    after their rows are staged: T_b + C_b stored rows, qo_indptr [0, 4, 6, 7].
+    Each packed row is checked against a dense softmax over keys [0, T_b + i + 1)
+    written out here, and the visible cells against the fixture's total.
+    """
+    g = golden("phase_fixture.json")["mixed"]
+    TC = g["TC"]
+    lens = [T + C for T, C in TC]
+    qo = np.array(g["qo_indptr"])
+    rng = np.random.default_rng(16)
+    B, H_q, H_kv, d, P = len(TC), 4, 2, 16, 4
+    c, k, v, ri = _paged_case(rng, lens, H_kv, d, P)
+    S_q = max(C for _, C in TC)
+    q = _bf16(rng, (int(qo[-1]), H_q, d))
+    problem = dict(B=B, S_q=S_q, H_q=H_q, H_kv=H_kv, d=d, qo_indptr=qo)
+    cells = sum(len(attention.visible_for(problem, lens[b], i, None, b)) for b in range(B)
+                for i in range(TC[b][1]))
+    assert cells == g["visible"]
+    O, LSE = attention.decode_rows(problem, c, q)
+    assert len(O) == qo[-1] * H_q
+    n = 0
+    for b, (T, C) in enumerate(TC):
+        for i in range(C):
+            for h in range(H_q):
+                hk = h // (H_q // H_kv)
+                K = quant.bf16_bits_to_f64(k[ri[b]:ri[b] + T + i + 1, hk])
+                V = quant.bf16_bits_to_f64(v[ri[b]:ri[b] + T + i + 1, hk])
+                s = K @ quant.bf16_bits_to_f64(q[qo[b] + i, h]) / math.sqrt(d)
+                lse = logsumexp(s)
+                np.testing.assert_allclose(O[n], np.exp(s - lse) @ V, rtol=1e-12, atol=1e-13)
+                assert LSE[n] == pytest.approx(lse, rel=1e-13)
+                n += 1
+    # a request alone, as a uniform batch of S_q = C_b rows, gives the same rows
+    n = 0
+    for b, (T, C) in enumerate(TC):
+        one = cm.empty_paged("bf16", c.k.shape[0], H_kv, P, d, 1)
+        one.k, one.v = c.k, c.v
+        one.page_indptr = np.array([0, c.page_indptr[b + 1] - c.page_indptr[b]])
+        one.page_indices = c.page_indices[c.page_indptr[b]:c.page_indptr[b + 1]]
+        one.kv_len = np.array([lens[b]])
+        O1, L1 = attention.decode_rows(dict(B=1, S_q=C, H_q=H_q, H_kv=H_kv, d=d), one,
+                                       q[qo[b]:qo[b + 1]].reshape(1, C, H_q, d))
+        np.testing.assert_array_equal(O1, O[n:n + C * H_q])
+        np.testing.assert_array_equal(L1, LSE[n:n + C * H_q])
+        n += C * H_q

@@ -58,6 +58,7 @@ class Workload:
     index_indptr: torch.Tensor = None         # int32 [B*H_kv+1] CPU
     index_list: torch.Tensor = None           # int32 CPU
     fm_intervals: torch.Tensor = None         # int32 [sum T_b, 4] CPU, FlashMask (UTS, UTE, LTS, LTE)
+    qo_indptr: torch.Tensor = None            # int32 [B+1] CPU, mixed batch: q is [qo_indptr[B], H_q, d]
     rows_indptr: torch.Tensor = None          # packed ragged history (quantized workloads)
     k_rows: torch.Tensor = None
     v_rows: torch.Tensor = None
@@ -285,4 +286,44 @@ def tree_verify(device="cpu", B=16, S_q=8, lo=1024, hi=8192, seed=5):
         iv += _dfs_tree_intervals(S_q, meta)
     w.problem = dict(w.problem, mask="flashmask")
     w.fm_intervals = torch.tensor(iv, dtype=torch.int32)
+    return w
+
+
+def mixed_batch(device="cpu", TC=None, B=16, lo=1024, hi=8192, S_q=8, seed=6, **mask_args):
+    """One launch over requests in different phases: request b has T_b committed rows and
+    C_b new query rows (prefill T_b = 0, append C_b > 1, decode C_b = 1, C_b = 0 idle),
+    its C_b rows already staged in the cache (T_b + C_b stored rows) and its query rows
+    packed at qo_indptr[b] .. qo_indptr[b+1] of a [qo_indptr[B], H_q, d] query.
+
+    Default mix: 10 decode rows, 3 appends of 2..S_q rows, 2 prefills of S_q rows and one
+    idle request, T_b ~ U[lo, hi] for the ones with history."""
+    meta = torch.Generator().manual_seed(seed)
+    if TC is None:
+        T = torch.randint(lo, hi + 1, (B,), generator=meta).tolist()
+        kinds = ["decode"] * (B - 6) + ["append"] * 3 + ["prefill"] * 2 + ["idle"]
+        order = torch.randperm(B, generator=meta).tolist()
+        TC = []
+        for b in range(B):
+            k = kinds[order[b]]
+            if k == "decode":
+                TC.append((T[b], 1))
+            elif k == "append":
+                TC.append((T[b], int(torch.randint(2, S_q + 1, (1,), generator=meta))))
+            elif k == "prefill":
+                TC.append((0, S_q))
+            else:
+                TC.append((T[b], 0))
+    B = len(TC)
+    S_q = max(max(C for _, C in TC), 1)
+    lens = [t + c for t, c in TC]
+    w = paged_bf16(f"mixed prefill/append/decode batch B={B} C_b<={S_q} H_q=32 H_kv=8 d=128 P=16",
+                   B=B, S_q=S_q, H_q=32, H_kv=8, d=128, lens=lens, P=16, seed=seed, device=device,
+                   **mask_args)
+    qo = [0]
+    for _, c in TC:
+        qo.append(qo[-1] + c)
+    w.qo_indptr = torch.tensor(qo, dtype=torch.int32)
+    gen = torch.Generator(device=device).manual_seed(seed + 2000)
+    w.q = _normal_bf16((qo[-1], 32, 128), gen, device)
+    w.meta["TC"] = TC
     return w
