@@ -17,6 +17,9 @@ Layouts (element order, outermost first):
                          qparams [N_pages, H_kv, P, 2] fp16 (s, z)
 * paged FP8 E4M3 / E5M2: codes [N_pages, H_kv, P, d] uint8; per-head scales
                          k_qp, v_qp [H_kv] fp32 (1 when not calibrated)
+* paged INT4 per head:   codes [N_pages, H_kv, P, d/2] uint8 (packed);
+                         qparams [N_pages, H_kv, P, 2] fp16 (s, o), one per
+                         (token, kv head); x_hat = (code - o) * s
 * paged INT4 KIVI:       codes [N_pages, H_kv, P, d/2] uint8 (packed);
                          K qparams [N_pages, H_kv, max(1, P/G), d, 2] fp16 held
                          by the page of the group's first token;
@@ -37,7 +40,7 @@ from . import address, quant
 @dataclass
 class Cache:
     layout: str            # "contig" | "paged"
-    fmt: str               # "bf16" | "int8" | "fp8_e4m3" | "fp8_e5m2" | "int4_kivi"
+    fmt: str               # "bf16" | "int8" | "fp8_e4m3" | "fp8_e5m2" | "int4_head" | "int4_kivi"
     H_kv: int
     d: int
     P: int = 0
@@ -93,6 +96,11 @@ def read_rows(cache: Cache, b: int, h_kv: int, positions) -> tuple[np.ndarray, n
         v = cache.v[pages, h_kv, rows, :].astype(np.float64) * vq[:, 0:1].astype(np.float64) \
             + vq[:, 1:2].astype(np.float64)
         return k, v
+    if cache.fmt == "int4_head":
+        kq = cache.k_qp[pages, h_kv, rows]          # [n, 2] fp16 (s, o)
+        vq = cache.v_qp[pages, h_kv, rows]
+        return (quant.int4_head_decode(quant.unpack_int4(cache.k[pages, h_kv, rows, :]), kq[:, 0], kq[:, 1]),
+                quant.int4_head_decode(quant.unpack_int4(cache.v[pages, h_kv, rows, :]), vq[:, 0], vq[:, 1]))
     if cache.fmt in quant.FP8_FORMATS:
         return (quant.fp8_head_decode(cache.k[pages, h_kv, rows, :], cache.k_qp[h_kv], cache.fmt),
                 quant.fp8_head_decode(cache.v[pages, h_kv, rows, :], cache.v_qp[h_kv], cache.fmt))
@@ -139,6 +147,11 @@ def empty_paged(fmt: str, n_pages: int, H_kv: int, P: int, d: int, B: int,
         c.v = np.zeros_like(c.k)
         c.k_qp = np.zeros((n_pages, H_kv, P, 2), np.float16)
         c.v_qp = np.zeros_like(c.k_qp)
+    elif fmt == "int4_head":
+        c.k = np.zeros((n_pages, H_kv, P, d // 2), np.uint8)
+        c.v = np.zeros_like(c.k)
+        c.k_qp = np.zeros((n_pages, H_kv, P, 2), np.float16)
+        c.v_qp = np.zeros_like(c.k_qp)
     elif fmt in quant.FP8_FORMATS:
         c.k = np.zeros((n_pages, H_kv, P, d), np.uint8)
         c.v = np.zeros_like(c.k)
@@ -161,7 +174,8 @@ def write_history(cache: Cache, page_indptr, page_indices, rows_indptr, k_bits, 
 
     ``k_bits`` / ``v_bits`` are packed ragged bf16 rows [sum T_b, H_kv, d]
     (rows of request b are rows_indptr[b]:rows_indptr[b+1], §0x04C).
-    INT8 rows are quantised one (token, head) at a time (M8.6 §0x05B), FP8 rows
+    INT8 and per-head INT4 rows are quantised one (token, head) at a time (M8.6
+    §0x05B, §0x09C), FP8 rows
     with their head's scale (§0x0AA); KIVI
     closes K groups per channel and V rows per token for the first n_q(T_b)
     tokens and keeps the rest as bf16 residual (M8.6 §0x06B).
@@ -191,6 +205,13 @@ def write_history(cache: Cache, page_indptr, page_indices, rows_indptr, k_bits, 
                     codes_pool[pages, h, rows] = codes[:, h]
                     qp_pool[pages, h, rows, 0] = s[:, h]
                     qp_pool[pages, h, rows, 1] = z[:, h]
+        elif cache.fmt == "int4_head":
+            for src, codes_pool, qp_pool in ((kb, cache.k, cache.k_qp), (vb, cache.v, cache.v_qp)):
+                codes, s, o = quant.int4_head_quantize(quant.bf16_bits_to_f32(src))  # [T, H, d]
+                for h in range(cache.H_kv):
+                    codes_pool[pages, h, rows] = quant.pack_int4(codes[:, h])
+                    qp_pool[pages, h, rows, 0] = s[:, h]
+                    qp_pool[pages, h, rows, 1] = o[:, h]
         elif cache.fmt in quant.FP8_FORMATS:
             for h in range(cache.H_kv):
                 cache.k[pages, h, rows] = quant.fp8_head_quantize(quant.bf16_bits_to_f32(kb[:, h]),

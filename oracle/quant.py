@@ -14,7 +14,8 @@ Follows "M8.6 Live-Data Quantization: Activations and KV Cache":
           full-precision residual whose oldest G rows close while it holds
           more than R rows; §0x06E  G = 32, R = 128;
 * §0x09C  the asymmetric floating-offset ABI (an offset stored as a value,
-          not clamped to the code range).
+          not clamped to the code range), used by the INT8 zero point and by
+          the per-head asymmetric KV4 format.
 
 Formats (the reading of the pages that the library documents):
 
@@ -32,6 +33,9 @@ Formats (the reading of the pages that the library documents):
   (one correctly rounded divide), rounded to the nearest E4M3 value with
   ties to the even code and saturated to +-448; x_hat = e4m3_value(code) s_h.
   FP8 E5M2 the same way, saturated to +-57344.
+* INT4 per head (QServe-style KV4, §0x09C): one fp16 (s, o) per (token, kv
+  head) with s = (max - min) / 15 and a floating offset o = -min / s that is
+  not clamped; code = clip(rint_even(x / s + o), 0, 15); x_hat = (code - o) s.
 """
 
 from __future__ import annotations
@@ -243,6 +247,73 @@ def fp8_head_quantize(x_f32, scale_f32, fmt: str = "fp8_e4m3") -> np.ndarray:
 def fp8_head_decode(codes, scale_f32, fmt: str = "fp8_e4m3") -> np.ndarray:
     """x_hat = value(code) * s in float64."""
     return FP8_FORMATS[fmt][1](codes) * np.float64(np.float32(scale_f32))
+
+
+# ---- per-head asymmetric KV4 with a floating offset (M8.6 §0x09C) -----------
+#
+# One (scale, offset) pair per (token, kv head), separately for K and V, over
+# the head's d channels.  Before storage rounding the page's parameters are
+# s* = (max - min) / 15 and o* = -min / s*; both are stored as fp16 and the
+# offset is a floating value that is NOT clamped to the code range (a range
+# [1, 2] has o* = -15).  Codes are clip(rint(x / s + o), 0, 15) with the
+# re-read stored s and o, the rounding done after the offset is added;
+# x_hat = (code - o) * s.  Two codes per byte along d, the even channel in the
+# low nibble (the same packing as the KIVI format).
+#
+# The page leaves the degenerate heads to the implementation and rejects them
+# in its model; the readings taken here keep every stored value finite:
+#  * a constant head (max == min) stores the sentinel s = 1 (M8.6 §0x02A) and
+#    o = fp16(-min), so it decodes to fp16(min);
+#  * a stored scale below 2^-14 (zero or subnormal fp16) is raised to 2^-14,
+#    and the offset is then computed with that scale;
+#  * fp16 conversions round to nearest even and saturate to +-65504.
+# Arithmetic is fp32 (min / max exact, each divide and add correctly rounded).
+
+def f16_saturated(x_f32) -> np.ndarray:
+    """fp32 -> fp16, round to nearest even, saturated to the largest finite magnitude."""
+    x = np.asarray(x_f32, dtype=np.float32)
+    return np.clip(x, np.float32(-65504.0), np.float32(65504.0)).astype(np.float16)
+
+
+def int4_head_qparams(x_f32):
+    """Stored (s, o) fp16 of each (token, head) row along the last axis  (M8.6 §0x09C)."""
+    x = np.asarray(x_f32, dtype=np.float32)
+    mn = x.min(axis=-1)
+    mx = x.max(axis=-1)
+    width = (mx - mn).astype(np.float32)
+    flat = width == 0
+    with np.errstate(over="ignore"):
+        base = np.where(flat, np.float32(1.0), width / np.float32(15.0)).astype(np.float32)
+    s = f16_saturated(base)
+    tiny = (s < F16_MIN_NORMAL) & ~flat
+    s = np.where(tiny, F16_MIN_NORMAL, s).astype(np.float16)
+    base = np.where(tiny, np.float32(F16_MIN_NORMAL), base).astype(np.float32)
+    with np.errstate(over="ignore"):
+        o = f16_saturated((-mn).astype(np.float32) / base)
+    return s, o
+
+
+def int4_head_encode(x_f32, s16, o16) -> np.ndarray:
+    """codes = clip(rint_even(x / s + o), 0, 15), each fp32 operation rounded once."""
+    x = np.asarray(x_f32, dtype=np.float32)
+    s = np.asarray(s16, dtype=np.float16).astype(np.float32)[..., None]
+    o = np.asarray(o16, dtype=np.float16).astype(np.float32)[..., None]
+    with np.errstate(over="ignore"):
+        u = (x / s).astype(np.float32) + o
+    return np.clip(np.rint(u), 0, 15).astype(np.uint8)
+
+
+def int4_head_quantize(x_f32):
+    """(token, head) rows [..., d] -> codes uint8 [..., d] (unpacked), s, o fp16 [...]."""
+    s, o = int4_head_qparams(x_f32)
+    return int4_head_encode(x_f32, s, o), s, o
+
+
+def int4_head_decode(codes, s16, o16) -> np.ndarray:
+    """x_hat = (code - o) * s in float64 (s, o broadcast over the row)."""
+    s = np.asarray(s16, dtype=np.float16).astype(np.float64)[..., None]
+    o = np.asarray(o16, dtype=np.float16).astype(np.float64)[..., None]
+    return (np.asarray(codes, dtype=np.float64) - o) * s
 
 
 # ---- byte ledger, M8.6 §0x04A-B ---------------------------------------------

@@ -298,3 +298,115 @@ def test_fp8_e5m2_cache_decode_close_to_bf16():
             s = c.k_qp[h]
             assert np.all(np.abs(K1 - K0) <= np.abs(K0) / 8 + s * 2.0 ** -17)
             assert np.all(np.abs(V1 - V0) <= np.abs(V0) / 8 + 2.0 ** -17)
+
+
+# ---- per-head asymmetric KV4 with a floating offset (M8.6 §0x09C) ------------
+
+def test_int4_head_positive_range_keeps_the_unclamped_offset():
+    """§0x09C: a head whose values lie in [1, 2] has the ideal offset -15, outside the code
+    range; clamping it to zero would bring both endpoints back near one."""
+    row = np.array([[1.0, 2.0, 1.5, 1.25, 1.75, 1.0625, 1.9375, 1.5]], np.float32)
+    codes, s, o = quant.int4_head_quantize(row)
+    assert s[0] == np.float16(1.0 / 15.0)
+    assert o[0] == -15.0
+    assert codes[0, 0] == 0 and codes[0, 1] == 15
+    xh = quant.int4_head_decode(codes, s, o)
+    assert np.all(np.abs(xh - row) <= 0.5 * float(s[0]))
+    clamped = quant.int4_head_decode(quant.int4_head_encode(row, s, np.float16([0.0])), s, np.float16([0.0]))
+    assert abs(clamped[0, 0] - 1.0) < 0.01 and abs(clamped[0, 1] - 1.0) < 0.01   # 2 comes back near 1
+
+
+def test_int4_head_round_trip_bound_and_endpoints():
+    rng = np.random.default_rng(40)
+    x = _f32(_bf16(rng, (600, 128)))
+    x[:, 9] *= 8
+    x[:300] = x[:300] * np.float32(0.125) + np.float32(6.0)   # positive rows: offsets below -15
+    codes, s, o = quant.int4_head_quantize(x)
+    xh = quant.int4_head_decode(codes, s, o)
+    s64 = s.astype(np.float64)[:, None]
+    assert np.all(np.abs(xh - x) <= 0.5 * s64 * (1 + 1e-5) + 1e-7)
+    rows = np.arange(600)
+    assert np.all(codes[rows, x.argmin(axis=1)] == 0)
+    assert np.all(codes[rows, x.argmax(axis=1)] == 15)
+    width = (x.max(1) - x.min(1)).astype(np.float64)
+    np.testing.assert_allclose(s.astype(np.float64), width / 15, rtol=2 ** -11)
+    np.testing.assert_allclose(o.astype(np.float64), -x.min(1) / (width / 15), rtol=2 ** -10)
+    assert np.any(o[:300] < -15)                       # the offset is not clamped to [0, 15]
+
+
+def test_int4_head_rounds_after_adding_the_offset_with_ties_to_even():
+    row = np.array([[0, 15, 2.5, 3.5, 4.5, 0.5, 1.5, 14.5]], np.float32)   # s = 1, o = -0
+    codes, s, o = quant.int4_head_quantize(row)
+    assert s[0] == 1.0 and o[0] == 0.0
+    assert codes[0].tolist() == [0, 15, 2, 4, 4, 0, 2, 14]
+    shifted = row - np.float32(0.25)                   # o = 0.25: x / s + o lands on the same ties
+    codes2, s2, o2 = quant.int4_head_quantize(shifted)
+    assert s2[0] == 1.0 and o2[0] == 0.25
+    assert codes2[0].tolist() == [0, 15, 2, 4, 4, 0, 2, 14]
+
+
+def test_int4_head_degenerate_heads():
+    # constant head: sentinel scale 1, decodes to fp16(min)
+    for val in (0.75, 3.14159, -2.0):
+        codes, s, o = quant.int4_head_quantize(np.full((1, 16), val, np.float32))
+        assert s[0] == 1.0 and o[0] == np.float16(-val) and not codes.any()
+        assert quant.int4_head_decode(codes, s, o)[0, 0] == float(np.float16(val))
+    # range / 15 below the smallest normal fp16: scale 2^-14, offset computed with it
+    codes, s, o = quant.int4_head_quantize(np.array([[1.0, 1.0 + 2 ** -12]], np.float32))
+    assert s[0] == np.float16(2 ** -14) and o[0] == -16384.0
+    assert codes[0].tolist() == [0, 4]
+    assert np.array_equal(quant.int4_head_decode(codes, s, o)[0], [1.0, 1.0 + 2 ** -12])
+    # stored values saturate to the largest finite fp16
+    codes, s, o = quant.int4_head_quantize(np.array([[0.0, 1.0e6]], np.float32))
+    assert s[0] == 65504.0 and codes[0].tolist() == [0, 15]
+    codes, s, o = quant.int4_head_quantize(np.array([[1.0e5, 1.0e5 + 1.0]], np.float32))
+    assert o[0] == -65504.0 and np.all(np.isfinite(quant.int4_head_decode(codes, s, o)))
+
+
+def test_int4_head_fp32_encoding_agrees_with_fp64_away_from_ties():
+    """The page's arithmetic model rounds x / s + o in float64; away from a tie fp32 gives the
+    same code."""
+    rng = np.random.default_rng(41)
+    x = _f32(_bf16(rng, (400, 64)))
+    codes, s, o = quant.int4_head_quantize(x)
+    u64 = x.astype(np.float64) / s.astype(np.float64)[:, None] + o.astype(np.float64)[:, None]
+    c64 = np.clip(np.rint(u64), 0, 15)
+    near_tie = np.abs(u64 - np.floor(u64) - 0.5) < 2.0 ** -16
+    assert np.array_equal(codes[~near_tie], c64[~near_tie])
+
+
+def test_int4_head_cache_round_trip_and_decode_close_to_bf16():
+    rng = np.random.default_rng(42)
+    lens = [300, 129, 40]
+    H, d, P = 2, 64, 16
+    n_pages = [-(-T // P) for T in lens]
+    pool = sum(n_pages) + 2
+    indices = rng.permutation(pool)[:sum(n_pages)]
+    indptr = np.concatenate([[0], np.cumsum(n_pages)])
+    ri = np.concatenate([[0], np.cumsum(lens)])
+    k = _bf16(rng, (ri[-1], H, d))
+    v = _bf16(rng, (ri[-1], H, d))
+    ref = cm.empty_paged("bf16", pool, H, P, d, 3)
+    cm.write_history(ref, indptr, indices, ri, k, v)
+    c = cm.empty_paged("int4_head", pool, H, P, d, 3)
+    cm.write_history(c, indptr, indices, ri, k, v)
+    assert c.k.shape == (pool, H, P, d // 2) and c.k_qp.shape == (pool, H, P, 2)
+    for b, T in enumerate(lens):
+        t = np.arange(T)
+        pages = indices[indptr[b] + t // P]
+        for h in range(H):
+            K0, V0 = cm.read_rows(ref, b, h, t)
+            K1, V1 = cm.read_rows(c, b, h, t)
+            ks = c.k_qp[pages, h, t % P, 0].astype(np.float64)[:, None]
+            vs = c.v_qp[pages, h, t % P, 0].astype(np.float64)[:, None]
+            assert np.all(np.abs(K1 - K0) <= 0.5 * ks * (1 + 1e-5) + 1e-7)
+            assert np.all(np.abs(V1 - V0) <= 0.5 * vs * (1 + 1e-5) + 1e-7)
+            # the byte layout: even channel in the low nibble of byte c / 2
+            kc = c.k[pages, h, t % P]
+            assert np.array_equal(kc[:, 3] & 0xF, quant.int4_head_quantize(quant.bf16_bits_to_f32(
+                k[ri[b]:ri[b + 1], h]))[0][:, 6])
+    problem = dict(B=3, S_q=1, H_q=4, H_kv=H, d=d)
+    q = _bf16(rng, (3, 1, 4, d))
+    O0, L0 = attention.decode_rows(problem, ref, q)
+    O1, L1 = attention.decode_rows(problem, c, q)
+    assert np.max(np.abs(O1 - O0)) < 0.5
