@@ -38,7 +38,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "tree-verify", "mixed", "int8", "fp8",
-                   "fp8-e5m2", "int4-kivi")
+                   "fp8-e5m2", "int4-head", "int4-kivi")
 
 
 def parse():
@@ -471,8 +471,8 @@ def _quantized_cache(dattn, w, fmt, dev):
     H, P, d, B, n = p["H_kv"], p["P"], p["d"], p["B"], p["num_pages"]
     G, Gv, R = p["kivi_group"], p["kivi_v_group"], p["kivi_residual"]
     c = {}
-    if fmt == "int8":
-        c["k"] = torch.zeros((n, H, P, d), dtype=torch.uint8, device=dev)
+    if fmt in ("int8", "int4_head"):
+        c["k"] = torch.zeros((n, H, P, d if fmt == "int8" else d // 2), dtype=torch.uint8, device=dev)
         c["k_qparams"] = torch.zeros((n, H, P, 2), dtype=torch.float16, device=dev)
         c["v_qparams"] = torch.zeros_like(c["k_qparams"])
     elif fmt in ("fp8_e4m3", "fp8_e5m2"):
@@ -506,6 +506,8 @@ def _stream_bytes(p, info, lens):
         return info["stream_keys"] * (2 * d + 8)
     if fmt in ("fp8_e4m3", "fp8_e5m2"):
         return info["stream_keys"] * 2 * d
+    if fmt == "int4_head":
+        return info["stream_keys"] * (d + 8)
     G, Gv, R = p["kivi_group"], p["kivi_v_group"], p["kivi_residual"]
     total = 0
     for T in lens:      # causal, S_q = 1: the stream is the whole history
@@ -524,8 +526,9 @@ def run_other(args):
     dattn.load()
     dev = torch.device("cuda", torch.cuda.current_device())
     name = args.workload
-    if name in ("int8", "fp8", "fp8-e5m2", "int4-kivi"):
-        fmt = {"int8": "int8", "fp8": "fp8_e4m3", "fp8-e5m2": "fp8_e5m2", "int4-kivi": "int4_kivi"}[name]
+    if name in ("int8", "fp8", "fp8-e5m2", "int4-head", "int4-kivi"):
+        fmt = {"int8": "int8", "fp8": "fp8_e4m3", "fp8-e5m2": "fp8_e5m2", "int4-head": "int4_head",
+               "int4-kivi": "int4_kivi"}[name]
         w = W.quantized(dev, fmt=fmt)
         p, cache = _quantized_cache(dattn, w, fmt, dev)
     else:

@@ -55,7 +55,7 @@ typedef enum {
  *      page_indices[page_indptr[b] + j] at page row t mod P (CSR page list). */
 typedef enum { DATTN_KV_CONTIG_NHD = 0, DATTN_KV_PAGED_HND = 1 } dattn_layout;
 
-/* K/V element formats (M8.6 §0x05B, §0x06A-B, §0x0A-0x0AA).  Paged layout only for
+/* K/V element formats (M8.6 §0x05B, §0x06A-B, §0x09C, §0x0A-0x0AA).  Paged layout only for
  * the quantized formats.
  *  DATTN_FMT_BF16:       K, V bf16.
  *  DATTN_FMT_INT8_TOKEN: K, V uint8 codes [num_pages, H_kv, P, d];
@@ -77,13 +77,23 @@ typedef enum { DATTN_KV_CONTIG_NHD = 0, DATTN_KV_PAGED_HND = 1 } dattn_layout;
  *      per kv head, NULL for 1 (no calibration); x_hat = value(code) * s_h.
  *  DATTN_FMT_FP8_E5M2:   the same with E5M2 codes (5 exponent bits with bias 15,
  *      2 mantissa bits, the upper byte of the IEEE half of the same value;
- *      largest finite magnitude 57344). */
+ *      largest finite magnitude 57344).
+ *  DATTN_FMT_INT4_HEAD:  per-head asymmetric KV4 (M8.6 §0x09C): K, V uint8
+ *      [num_pages, H_kv, P, d/2], two 4-bit codes per byte, the even channel in
+ *      the low nibble; k_qparams, v_qparams fp16 pairs (s, o) [num_pages, H_kv, P, 2],
+ *      one per (token, kv head), with the floating offset o not clamped to the
+ *      code range; x_hat = (code - o) * s.  kv_append writes s = fp16((max - min) / 15),
+ *      o = fp16(-min / ((max - min) / 15)) (fp32 arithmetic, fp16 saturated to
+ *      +-65504; a constant head stores s = 1, o = fp16(-min); a scale below 2^-14
+ *      is raised to 2^-14 and the offset computed with it) and codes
+ *      clip(rint(x / s + o), 0, 15) with the stored s, o.  K/V rows must be finite. */
 typedef enum {
   DATTN_FMT_BF16 = 0,
   DATTN_FMT_INT8_TOKEN = 1,
   DATTN_FMT_INT4_KIVI = 2,
   DATTN_FMT_FP8_E4M3 = 3,
-  DATTN_FMT_FP8_E5M2 = 4
+  DATTN_FMT_FP8_E5M2 = 4,
+  DATTN_FMT_INT4_HEAD = 5
 } dattn_format;
 
 /* Visibility programs.  Query row i of request b sits at position

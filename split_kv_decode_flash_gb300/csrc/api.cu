@@ -33,9 +33,9 @@ void check_tensors(const dattn_problem& p, const dattn_tensors* t, bool need_q_o
     c.fail(DATTN_EINVAL, "index_list mask needs index_indptr and index_list");
   if (p.mask == DATTN_MASK_FLASHMASK && (!t->fm_intervals || !aligned16(t->fm_intervals)))
     c.fail(DATTN_EINVAL, "flashmask needs 16-byte aligned fm_intervals");
-  if (p.fmt == DATTN_FMT_INT8_TOKEN || p.fmt == DATTN_FMT_INT4_KIVI) {
+  if (p.fmt == DATTN_FMT_INT8_TOKEN || p.fmt == DATTN_FMT_INT4_KIVI || p.fmt == DATTN_FMT_INT4_HEAD) {
     if (!t->k_qparams || !t->v_qparams || !aligned16(t->k_qparams) || !aligned16(t->v_qparams))
-      c.fail(DATTN_EINVAL, "INT8 and INT4 KIVI need 16-byte aligned k_qparams and v_qparams");
+      c.fail(DATTN_EINVAL, "INT8 and INT4 formats need 16-byte aligned k_qparams and v_qparams");
   }
   if ((p.fmt == DATTN_FMT_FP8_E4M3 || p.fmt == DATTN_FMT_FP8_E5M2) &&
       ((reinterpret_cast<uintptr_t>(t->k_qparams) % 4) || (reinterpret_cast<uintptr_t>(t->v_qparams) % 4)))

@@ -10,7 +10,9 @@
 //    per Gv channels; rows stay bf16 in a residual ring until their group
 //    closes (the oldest G rows close while the residual holds more than R).
 //  - §0x09C the zero point is a floating value offset stored as fp16
-//    (x_hat = code * s + z), not an integer clamped to the code range.
+//    (x_hat = code * s + z), not an integer clamped to the code range; the
+//    per-head asymmetric INT4 format stores one (s, o) per token and kv head
+//    and encodes rint(x / s + o) with x_hat = (code - o) * s.
 // All arguments, and the page capacity of every request, are validated on the
 // host before any launch (the append transaction of M4.5 §0x08C).
 #include <cuda_bf16.h>
@@ -74,6 +76,29 @@ __device__ __forceinline__ void qparams(float mn, float mx, float qmax, __half& 
 __device__ __forceinline__ uint32_t encode(float x, float s, float z, float qmax) {
   const float r = rintf(__fdiv_rn(x - z, s));
   return static_cast<uint32_t>(fminf(fmaxf(r, 0.f), qmax));
+}
+
+// Per-head asymmetric INT4 (§0x09C): s = fp16((mx - mn) / 15), floating offset
+// o = fp16(-mn / ((mx - mn) / 15)), both saturated to the finite fp16 range; a
+// constant head stores s = 1, o = fp16(-mn); a scale below 2^-14 is raised to
+// 2^-14 and the offset taken with it.
+__device__ __forceinline__ __half f16_sat(float x) { return __float2half_rn(fminf(fmaxf(x, -65504.f), 65504.f)); }
+
+__device__ __forceinline__ void head_qparams(float mn, float mx, __half& s, __half& o) {
+  const float width = mx - mn;
+  float base = width == 0.f ? 1.f : __fdiv_rn(width, 15.f);
+  s = f16_sat(base);
+  if (width != 0.f && __half2float(s) < 6.103515625e-05f) {
+    s = __float2half_rn(6.103515625e-05f);
+    base = 6.103515625e-05f;
+  }
+  o = f16_sat(__fdiv_rn(-mn, base));
+}
+
+// code = clip(rint(x / s + o), 0, 15): the offset is added before rounding.
+__device__ __forceinline__ uint32_t encode_offset(float x, float s, float o) {
+  const float r = rintf(__fadd_rn(__fdiv_rn(x, s), o));
+  return static_cast<uint32_t>(fminf(fmaxf(r, 0.f), 15.f));
 }
 
 __device__ __forceinline__ float warp_min(float x, int width) {
@@ -146,6 +171,27 @@ __global__ void append_rows_kernel(AppendParams p, int total_rows) {
       uint8_t* codes = static_cast<uint8_t*>(kv ? p.v : p.k) + dst_row;
       if constexpr (C == 4) reinterpret_cast<uint32_t*>(codes)[lane] = packed;
       else reinterpret_cast<uint16_t*>(codes)[lane] = static_cast<uint16_t>(packed);
+    } else if constexpr (FMT == DATTN_FMT_INT4_HEAD) {
+      float x[C];
+      load_channels<C>(in, lane, x);
+      float mn = x[0], mx = x[0];
+#pragma unroll
+      for (int c = 1; c < C; ++c) { mn = fminf(mn, x[c]); mx = fmaxf(mx, x[c]); }
+      mn = warp_min(mn, 32);
+      mx = warp_max(mx, 32);
+      __half s, o;
+      head_qparams(mn, mx, s, o);
+      const float sf = __half2float(s), of = __half2float(o);
+      uint32_t packed = 0;
+#pragma unroll
+      for (int c = 0; c < C; ++c) packed |= encode_offset(x[c], sf, of) << (4 * c);
+      uint8_t* codes = static_cast<uint8_t*>(kv ? p.v : p.k) + dst_row / 2;
+      if constexpr (C == 4) reinterpret_cast<uint16_t*>(codes)[lane] = static_cast<uint16_t>(packed);
+      else codes[lane] = static_cast<uint8_t>(packed);
+      if (lane == 0) {
+        __half2* qp = static_cast<__half2*>(kv ? p.vqp : p.kqp);
+        qp[dst_row / D] = __halves2half2(s, o);   // [page][h][row] matches the code row
+      }
     } else {
       float x[C];
       load_channels<C>(in, lane, x);
@@ -318,8 +364,9 @@ extern "C" dattn_status kv_append(const dattn_problem* prob, const dattn_append_
   const bool paged = p.layout == DATTN_KV_PAGED_HND;
   if (paged && (!in->page_indptr || !cache->page_indptr || !cache->page_indices))
     c.fail(DATTN_EINVAL, "paged cache needs host and device page_indptr and device page_indices");
-  if ((p.fmt == DATTN_FMT_INT8_TOKEN || p.fmt == DATTN_FMT_INT4_KIVI) && (!cache->k_qparams || !cache->v_qparams))
-    c.fail(DATTN_EINVAL, "INT8 and INT4 KIVI need k_qparams and v_qparams");
+  if ((p.fmt == DATTN_FMT_INT8_TOKEN || p.fmt == DATTN_FMT_INT4_KIVI || p.fmt == DATTN_FMT_INT4_HEAD) &&
+      (!cache->k_qparams || !cache->v_qparams))
+    c.fail(DATTN_EINVAL, "INT8 and INT4 formats need k_qparams and v_qparams");
   if (p.fmt == DATTN_FMT_INT4_KIVI && (!cache->k_residual || !cache->v_residual))
     c.fail(DATTN_EINVAL, "INT4 KIVI needs k_residual and v_residual");
   const size_t need = kv_append_workspace_bytes(prob);
@@ -410,6 +457,9 @@ extern "C" dattn_status kv_append(const dattn_problem* prob, const dattn_append_
   } else if (p.fmt == DATTN_FMT_INT8_TOKEN) {
     err = d128 ? launch_warps(append_rows_kernel<128, DATTN_FMT_INT8_TOKEN>, new_indptr[B] * H, s, a, new_indptr[B])
                : launch_warps(append_rows_kernel<64, DATTN_FMT_INT8_TOKEN>, new_indptr[B] * H, s, a, new_indptr[B]);
+  } else if (p.fmt == DATTN_FMT_INT4_HEAD) {
+    err = d128 ? launch_warps(append_rows_kernel<128, DATTN_FMT_INT4_HEAD>, new_indptr[B] * H, s, a, new_indptr[B])
+               : launch_warps(append_rows_kernel<64, DATTN_FMT_INT4_HEAD>, new_indptr[B] * H, s, a, new_indptr[B]);
   } else if (p.fmt == DATTN_FMT_FP8_E4M3) {
     err = d128 ? launch_warps(append_rows_kernel<128, DATTN_FMT_FP8_E4M3>, new_indptr[B] * H, s, a, new_indptr[B])
                : launch_warps(append_rows_kernel<64, DATTN_FMT_FP8_E4M3>, new_indptr[B] * H, s, a, new_indptr[B]);

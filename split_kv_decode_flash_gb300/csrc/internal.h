@@ -44,10 +44,12 @@ inline bool kivi_on_tensor_cores(int d, int rows, int Gv, int mask, int P, int R
 
 // Partial states an item leaves per query row.  Consumer warps are arranged
 // in row blocks (16 rows, one mma tile, in the bf16 and INT8 tensor-core
-// kernels, 8 rows in the KIVI one; 4 rows in the byte-format kernel); every
+// kernels, 8 rows in the KIVI and per-head INT4 ones; 4 rows in the
+// byte-format kernel); every
 // warp leaves the state of its block's rows over its own share of the item's
 // keys.
 inline int states_per_item(int rows, int fmt, bool kivi_tc) {
+  if (fmt == DATTN_FMT_INT4_HEAD) return kConsumerWarps / (rows <= 8 ? 1 : rows <= 16 ? 2 : 4);
   if (fmt != DATTN_FMT_INT4_KIVI || kivi_tc) return kConsumerWarps / (rows <= 16 ? 1 : 2);
   return kConsumerWarps / (rows <= 4 ? 1 : rows <= 8 ? 2 : rows <= 16 ? 4 : 8);
 }
@@ -140,6 +142,7 @@ int launch_partial(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_partial_bf16(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_partial_q8(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_partial_q4(const PartialParams& p, int n_ctas, void* stream);
+int launch_partial_q4h(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_merge(const MergeParams& p, int d, void* stream);
 
 }  // namespace dattn

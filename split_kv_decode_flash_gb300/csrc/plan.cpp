@@ -57,7 +57,7 @@ void check_problem(const dattn_problem* p, Checker& c) {
   if (p->d_h != 64 && p->d_h != 128) c.fail(DATTN_EUNSUPPORTED, "d_h must be 64 or 128");
   if (p->layout != DATTN_KV_CONTIG_NHD && p->layout != DATTN_KV_PAGED_HND)
     c.fail(DATTN_EINVAL, "unknown layout");
-  if (p->fmt < DATTN_FMT_BF16 || p->fmt > DATTN_FMT_FP8_E5M2) c.fail(DATTN_EINVAL, "unknown format");
+  if (p->fmt < DATTN_FMT_BF16 || p->fmt > DATTN_FMT_INT4_HEAD) c.fail(DATTN_EINVAL, "unknown format");
   if (p->mask < DATTN_MASK_CAUSAL || p->mask > DATTN_MASK_FLASHMASK) c.fail(DATTN_EINVAL, "unknown mask");
   if (p->mask == DATTN_MASK_FLASHMASK && p->fmt != DATTN_FMT_BF16)
     c.fail(DATTN_EUNSUPPORTED, "flashmask runs on bf16 K/V");

@@ -34,8 +34,9 @@ def _alloc(fmt, p, n_pages, B, dev="cuda", scales=None):
     if fmt == "bf16":
         out["k"] = torch.zeros((n_pages, H, P, d), dtype=torch.bfloat16, device=dev)
         out["v"] = torch.zeros_like(out["k"])
-    elif fmt == "int8":
-        out["k"] = torch.zeros((n_pages, H, P, d), dtype=torch.uint8, device=dev)
+    elif fmt in ("int8", "int4_head"):
+        row = d if fmt == "int8" else d // 2
+        out["k"] = torch.zeros((n_pages, H, P, row), dtype=torch.uint8, device=dev)
         out["v"] = torch.zeros_like(out["k"])
         out["k_qparams"] = torch.zeros((n_pages, H, P, 2), dtype=torch.float16, device=dev)
         out["v_qparams"] = torch.zeros_like(out["k_qparams"])
@@ -153,6 +154,29 @@ def test_int8_append_codes_and_qparams_bit_exact(d):
         assert np.array_equal(vc[pg, :, r], ref.v[pg, :, r])
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_int4_head_append_codes_and_qparams_bit_exact(d):
+    """Per-head INT4 (M8.6 §0x09C): (s, o) and packed codes bit for bit, with heads that
+    are constant, positive-only (offset below -15) and of tiny range mixed in."""
+    w = W.quantized_history("int4h", B=3, S_q=1, H_q=8, H_kv=2, d=d, lens=[333, 1, 96], P=16, seed=16,
+                            device="cuda", fmt="int4_head", pool_pages=40)
+    k = w.k_rows.clone()
+    k[5] = 0.75                                    # constant rows
+    k[6] = (k[6].float().abs() * 0.05 + 3.0).to(torch.bfloat16)   # positive-only rows: offset below -15
+    k[7] = (1.0 + k[7].float() * 2.0 ** -12).to(torch.bfloat16)   # range below 15 * 2^-14
+    w.k_rows = k.contiguous()
+    p, cache = append_history(w, "int4_head", _cuts(w.kv_len.tolist(), np.random.default_rng(4)))
+    ref = oracle_written(w, "int4_head")
+    kc, vc = cache["k"].cpu().numpy(), cache["v"].cpu().numpy()
+    kq, vq = cache["k_qparams"].cpu().numpy(), cache["v_qparams"].cpu().numpy()
+    for b, t, pg, r in _visible_rows(w):
+        assert np.array_equal(kq[pg, :, r].view(np.uint16), ref.k_qp[pg, :, r].view(np.uint16))
+        assert np.array_equal(vq[pg, :, r].view(np.uint16), ref.v_qp[pg, :, r].view(np.uint16))
+        assert np.array_equal(kc[pg, :, r], ref.k[pg, :, r])
+        assert np.array_equal(vc[pg, :, r], ref.v[pg, :, r])
+    assert np.any(ref.k_qp[..., 1].astype(np.float32) < -15)
+
+
 @pytest.mark.parametrize("fmt", ["fp8_e4m3", "fp8_e5m2"])
 @pytest.mark.parametrize("d,scales", [(128, "calibrated"), (64, "calibrated"), (128, "none"), (128, "tight")])
 def test_fp8_append_codes_bit_exact(fmt, d, scales):
@@ -222,7 +246,7 @@ def test_append_rejects_capacity_overflow_before_writing():
     assert not cache["k"].float().abs().sum().item(), "rejected append must not write"
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4_kivi"])
+@pytest.mark.parametrize("fmt", ["int8", "int4_head", "int4_kivi"])
 def test_full_size_quantized_append_sampled(fmt):
     """The quantized workload (B=32, T ~ U[2048, 32768]) written in one call; sampled rows checked."""
     w = W.quantized("cuda", fmt=fmt)
@@ -234,12 +258,14 @@ def test_full_size_quantized_append_sampled(fmt):
     for b in rng.choice(p["B"], size=6, replace=False):
         T = int(w.kv_len[b])
         row0 = int(w.rows_indptr[b])
-        if fmt == "int8":
+        if fmt in ("int8", "int4_head"):
             ts = rng.choice(T, size=64, replace=False)
             x = quant.bf16_bits_to_f32(bits(w.k_rows[row0 + torch.as_tensor(ts)]))
-            codes, s, z = quant.int8_token_quantize(x)
+            codes, s, z = quant.int8_token_quantize(x) if fmt == "int8" else quant.int4_head_quantize(x)
             pg = ind[ptr[b] + ts // P]
             got = kc[torch.as_tensor(pg), :, torch.as_tensor(ts % P)].cpu().numpy()
+            if fmt == "int4_head":
+                got = quant.unpack_int4(got)
             gq = cache["k_qparams"][torch.as_tensor(pg), :, torch.as_tensor(ts % P)].cpu().numpy()
             assert np.array_equal(got, codes)
             assert np.array_equal(gq[..., 0], s) and np.array_equal(gq[..., 1], z)

@@ -1,4 +1,5 @@
-"""GPU parity of decode over INT8 and KIVI-INT4 caches (M8.6 §0x03, §0x05B, §0x06B-C).
+"""GPU parity of decode over INT8, per-head INT4, FP8 and KIVI-INT4 caches (M8.6 §0x03, §0x05B,
+§0x06B-C, §0x09C, §0x0A).
 
 The GPU cache is written by kv_append; the oracle writes its own cache from
 the same bf16 history with its own quantiser and dequantises it in float64.
@@ -68,7 +69,7 @@ def _compare(O, L, w, p, cache_ref, rows):
     return H.compare(O, L, w2, rows, cache=cache_ref)
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("fmt", ["int8", "int4_head", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
 @pytest.mark.parametrize("chunk,num_sms", [(0, 152), (64, 5)])
 def test_quantized_decode_small_all_rows(fmt, chunk, num_sms):
     lens = [700, 129, 128, 161, 40, 1]
@@ -80,7 +81,7 @@ def test_quantized_decode_small_all_rows(fmt, chunk, num_sms):
     _compare(O, L, w, p, ref, H.all_rows(p))
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("fmt", ["int8", "int4_head", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
 def test_quantized_decode_d64_multi_row_sink_window(fmt):
     lens = [500, 90]
     w = W.quantized_history("q64", B=2, S_q=2, H_q=8, H_kv=2, d=64, lens=lens, P=16, seed=22, device="cuda",
@@ -101,7 +102,7 @@ def test_int4_kivi_verify_rows_cross_the_residual_boundary():
     _compare(O, L, w, p, _oracle_cache(w, "int4_kivi"), H.all_rows(p))
 
 
-@pytest.mark.parametrize("fmt", ["int8", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("fmt", ["int8", "int4_head", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
 def test_quantized_full_size_sampled(fmt):
     """B=32, T ~ U[2048, 32768], K outlier channels: the full quantized workload."""
     w = W.quantized("cuda", fmt=fmt)
@@ -144,7 +145,7 @@ def test_int8_decode_page_sizes(P):
     _compare(O, L, w, p, _oracle_cache(w, "int8"), H.all_rows(p))
 
 
-@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("fmt", ["int8", "int4_head", "fp8_e4m3", "fp8_e5m2"])
 @pytest.mark.parametrize("S_q,H_q,H_kv,d", [(3, 16, 4, 128), (4, 16, 2, 128), (4, 16, 2, 64)])
 def test_byte_codes_decode_more_than_eight_rows(fmt, S_q, H_q, H_kv, d):
     """12 and 32 query rows per kv head (row tiles of 16 on the mma M side), causal verify rows."""
@@ -172,3 +173,34 @@ def test_fp8_decode_without_scales_and_with_saturation(fmt):
         p, cache = append_history(w, fmt, [[] for _ in lens])
         O, L, info = _run(w, fmt, p, cache, chunk_tokens=64, num_sms=4)
         _compare(O, L, w, p, _oracle_cache(w, fmt), H.all_rows(p))
+
+
+@pytest.mark.parametrize("S_q,H_q,H_kv,d,mask", [
+    (1, 32, 8, 128, "index_list"),   # 4 rows: one row block
+    (2, 32, 8, 64, "causal"),        # 8 rows
+    (5, 12, 4, 128, "sink_window"),  # 15 rows: two row blocks, the last one short
+    (3, 64, 8, 128, "causal"),       # 24 rows: four row blocks
+])
+def test_int4_head_rows_masks_and_widths(S_q, H_q, H_kv, d, mask):
+    """Per-head INT4: 8-row blocks on the mma N side (1, 2 and 4 blocks), every visibility
+    program, partial stages and requests shorter than their query rows."""
+    lens = [1300, 257, 256, 17, 2]
+    w = W.quantized_history("q4h", B=len(lens), S_q=S_q, H_q=H_q, H_kv=H_kv, d=d, lens=lens, P=16, seed=27,
+                            device="cuda", fmt="int4_head", pool_pages=sum(-(-t // 16) for t in lens) + 3)
+    if mask == "sink_window":
+        w.problem = dict(w.problem, mask=mask, n_sink=5, window=300)
+    elif mask == "index_list":
+        gen = torch.Generator().manual_seed(3)
+        lists = [sorted(torch.randperm(T, generator=gen)[:max(1, T // 3)].tolist()) for T in lens for _ in range(H_kv)]
+        w.index_indptr = torch.tensor(np.concatenate([[0], np.cumsum([len(x) for x in lists])]), dtype=torch.int32)
+        w.index_list = torch.tensor(np.concatenate(lists), dtype=torch.int32)
+        w.problem = dict(w.problem, mask=mask)
+    p, cache = append_history(w, "int4_head", [[600], [], [100], [], []])
+    plan_kw = dict(chunk_tokens=128, num_sms=5)
+    if mask == "index_list":
+        cache.update(index_indptr=w.index_indptr.cuda(), index_list=w.index_list.cuda())
+        plan_kw.update(index_indptr=w.index_indptr, index_list=w.index_list)
+    O, L, info = _run(w, "int4_head", p, cache, **plan_kw)
+    assert info["rows"] == S_q * H_q // H_kv
+    w2 = W.Workload(w.name, p, w.q, w.kv_len, index_indptr=w.index_indptr, index_list=w.index_list)
+    H.compare(O, L, w2, H.all_rows(p), cache=_oracle_cache(w, "int4_head"))
