@@ -230,9 +230,10 @@ __device__ __forceinline__ void load_q4h(const PartialParams& p, const WorkItem&
 // S'^T (16 keys x 8 rows) = codes (A, keys x d) . Q^T (B): two mma per
 // 32-channel chunk for 16 keys.  A lane's accumulators hold keys g4, g4 + 8
 // for the block's rows 2 t4, 2 t4 + 1; row maxima and sums reduce over the 8
-// lanes that share t4.  Row blocks of 8 split a stage's keys among the four
-// warps of a stage group: 1 block, 64 keys a warp; 2 blocks, 128; 4 blocks,
-// 256, so that an item leaves 8, 4 or 2 states per row.
+// lanes that share t4.  A warp steps over 32 keys, two 16-key blocks that
+// share the row maxima and the rescale.  Row blocks of 8 split a stage's keys
+// among the four warps of a stage group: 1 block, 64 keys a warp; 2 blocks,
+// 128; 4 blocks, 256, so that an item leaves 8, 4 or 2 states per row.
 template <int D>
 __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
   using C = Q4H<D>;
@@ -266,6 +267,8 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
     const QH<D> q = qn;
     if (ii + 1 < w.end) load_q4h<D>(p, w.rec(ii + 1).it, 8 * rb + g4, t4, qn);
+    // log2-unit score = s_t (sc 2^24 / f) S' + z_t (sc sum q), per row
+    const float ku0 = sc * q.unit0, ku1 = sc * q.unit1, kz0 = sc * q.qsum0, kz1 = sc * q.qsum1;
     float o[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -297,57 +300,84 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
       const uint32_t* kqp = reinterpret_cast<const uint32_t*>(smem + st * C::kStage + 2 * C::kTile);
       const uint32_t* vqp = kqp + kHK;
 
-      for (int blk = 0; blk < keys_per_warp / 16; ++blk) {
-        const int base = ts * keys_per_warp + blk * 16;
+      // steps of 32 keys: two 16-key blocks share the row maxima and the rescale
+      for (int stp = 0; stp < keys_per_warp / 32; ++stp) {
+        const int base = ts * keys_per_warp + stp * 32;
         if (base >= j1 - j0) break;     // the rest of the warp's slots are empty
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        float s[2][4];
 #pragma unroll
-        for (int c2 = 0; c2 < NCH / 2; ++c2) {
-          uint32_t v[4];
-          ldsm_x4(kt + code_off<C::kRowB>(base + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1], v[2], v[3]);
+        for (int bb = 0; bb < 2; ++bb) {
+          s[bb][0] = s[bb][1] = s[bb][2] = s[bb][3] = 0.f;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t x = v[2 * h], y = v[2 * h + 1];     // keys g4, g4 + 8
-            const uint32_t x8 = x >> 8, y8 = y >> 8;
-            const uint32_t a0[4] = {x & kNibLo, y & kNibLo, x & kNibHi, y & kNibHi};
-            mma_f16(s, a0, q.b[2 * c2 + h][0][0], q.b[2 * c2 + h][0][1]);
-            const uint32_t a1[4] = {x8 & kNibLo, y8 & kNibLo, x8 & kNibHi, y8 & kNibHi};
-            mma_f16(s, a1, q.b[2 * c2 + h][1][0], q.b[2 * c2 + h][1][1]);
+          for (int c2 = 0; c2 < NCH / 2; ++c2) {
+            uint32_t v[4];
+            ldsm_x4(kt + code_off<C::kRowB>(base + 16 * bb + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1],
+                    v[2], v[3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t x = v[2 * h], y = v[2 * h + 1];     // keys g4, g4 + 8
+              const uint32_t x8 = x >> 8, y8 = y >> 8;
+              const uint32_t a0[4] = {x & kNibLo, y & kNibLo, x & kNibHi, y & kNibHi};
+              mma_f16(s[bb], a0, q.b[2 * c2 + h][0][0], q.b[2 * c2 + h][0][1]);
+              const uint32_t a1[4] = {x8 & kNibLo, y8 & kNibLo, x8 & kNibHi, y8 & kNibHi};
+              mma_f16(s[bb], a1, q.b[2 * c2 + h][1][0], q.b[2 * c2 + h][1][1]);
+            }
           }
         }
-        // keys g4 (s0, s1) and g4 + 8 (s2, s3); rows ra (s0, s2), rb1 (s1, s3).
+        // block bb: keys base + 16 bb + g4 (s0, s1) and + 8 (s2, s3); rows ra (s0, s2), rb1 (s1, s3).
         // q . k_hat = s_t 2^24 S' - o_t s_t sum(q), in log2 units; -inf where masked
-        const int kx = base + g4, ky = base + g4 + 8;
-        const int tx = pos[kx], ty = pos[ky];
-        const float2 ksx = h2_to_f2(kqp[kx]), ksy = h2_to_f2(kqp[ky]);
-        const float2 vqx = h2_to_f2(vqp[kx]), vqy = h2_to_f2(vqp[ky]);
-        const float zx = -ksx.y * ksx.x, zy = -ksy.y * ksy.x;   // exact: fp16 x fp16
-        const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
-        const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
-        const bool vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
-        const bool vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
-        s[0] = vxa ? sc * fmaf(ksx.x * q.unit0, s[0], zx * q.qsum0) : -INFINITY;
-        s[1] = vxb ? sc * fmaf(ksx.x * q.unit1, s[1], zx * q.qsum1) : -INFINITY;
-        s[2] = vya ? sc * fmaf(ksy.x * q.unit0, s[2], zy * q.qsum0) : -INFINITY;
-        s[3] = vyb ? sc * fmaf(ksy.x * q.unit1, s[3], zy * q.qsum1) : -INFINITY;
-        float mxa = fmaxf(s[0], s[2]), mxb = fmaxf(s[1], s[3]);
+        float vsx[2], vsy[2], vox[2], voy[2];
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const int kx = base + 16 * bb + g4, ky = kx + 8;
+          const int tx = pos[kx], ty = pos[ky];
+          const float2 ksx = h2_to_f2(kqp[kx]), ksy = h2_to_f2(kqp[ky]);
+          const float2 vqx = h2_to_f2(vqp[kx]), vqy = h2_to_f2(vqp[ky]);
+          vsx[bb] = vqx.x;
+          vox[bb] = vqx.y;
+          vsy[bb] = vqy.x;
+          voy[bb] = vqy.y;
+          const float zx = -ksx.y * ksx.x, zy = -ksy.y * ksy.x;   // exact: fp16 x fp16
+          const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
+          const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
+          const bool vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
+          const bool vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
+          s[bb][0] = vxa ? fmaf(ksx.x * ku0, s[bb][0], zx * kz0) : -INFINITY;
+          s[bb][1] = vxb ? fmaf(ksx.x * ku1, s[bb][1], zx * kz1) : -INFINITY;
+          s[bb][2] = vya ? fmaf(ksy.x * ku0, s[bb][2], zy * kz0) : -INFINITY;
+          s[bb][3] = vyb ? fmaf(ksy.x * ku1, s[bb][3], zy * kz1) : -INFINITY;
+        }
+        float mxa = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
+        float mxb = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
 #pragma unroll
         for (int x = 4; x <= 16; x <<= 1) {
           mxa = fmaxf(mxa, __shfl_xor_sync(kAll, mxa, x));
           mxb = fmaxf(mxb, __shfl_xor_sync(kAll, mxb, x));
         }
         const float na = fmaxf(ma, mxa), nb = fmaxf(mb, mxb);
-        const float aa = na == -INFINITY ? 1.f : exp2f(ma - na);
-        const float ab = nb == -INFINITY ? 1.f : exp2f(mb - nb);
+        const float aa = na == -INFINITY ? 1.f : ex2_approx(ma - na);
+        const float ab = nb == -INFINITY ? 1.f : ex2_approx(mb - nb);
         const float ua = na == -INFINITY ? 0.f : na, ub = nb == -INFINITY ? 0.f : nb;
-        const float p0 = exp2f(s[0] - ua), p1 = exp2f(s[1] - ub), p2 = exp2f(s[2] - ua), p3 = exp2f(s[3] - ub);
         // P'^T (keys x rows) = p s_v in f16, transposed into B fragments
-        const uint32_t px = pack_f16(p0 * vqx.x, p1 * vqx.x), py = pack_f16(p2 * vqy.x, p3 * vqy.x);
-        const float2 fx = h2_to_f2(px), fy = h2_to_f2(py);
-        la = la * aa + (p0 + p2);
-        lb = lb * ab + (p1 + p3);
-        za = za * aa + (fx.x * vqx.y + fy.x * vqy.y);
-        zb = zb * ab + (fx.y * vqx.y + fy.y * vqy.y);
+        uint32_t pb[2][2];
+        float sla = 0.f, slb = 0.f, sza = 0.f, szb = 0.f;
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const float p0 = ex2_approx(s[bb][0] - ua), p1 = ex2_approx(s[bb][1] - ub);
+          const float p2 = ex2_approx(s[bb][2] - ua), p3 = ex2_approx(s[bb][3] - ub);
+          const uint32_t px = pack_f16(p0 * vsx[bb], p1 * vsx[bb]), py = pack_f16(p2 * vsy[bb], p3 * vsy[bb]);
+          const float2 fx = h2_to_f2(px), fy = h2_to_f2(py);
+          sla += p0 + p2;
+          slb += p1 + p3;
+          sza += fx.x * vox[bb] + fy.x * voy[bb];
+          szb += fx.y * vox[bb] + fy.y * voy[bb];
+          pb[bb][0] = movmatrix_tr(px);
+          pb[bb][1] = movmatrix_tr(py);
+        }
+        la = la * aa + sla;
+        lb = lb * ab + slb;
+        za = za * aa + sza;
+        zb = zb * ab + szb;
         ma = na;
         mb = nb;
         if (__any_sync(kAll, aa != 1.f || ab != 1.f)) {
@@ -359,24 +389,26 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
             o[n][3] *= ab;
           }
         }
-        const uint32_t pb0 = movmatrix_tr(px), pb1 = movmatrix_tr(py);
         // O'^T += V^T codes . P'^T: ldmatrix.trans gives a lane keys (2 t4,
         // 2 t4 + 1) of keys 0-7 / 8-15 at channels 4 g4 .. 4 g4 + 3 of two chunks
 #pragma unroll
-        for (int c2 = 0; c2 < NCH / 2; ++c2) {
-          uint32_t v[4];
-          ldsm_x4_trans(vt + code_off<C::kRowB>(base + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1], v[2],
-                        v[3]);
-          // v[0] keys 0-7 / chunk 2 c2, v[1] keys 8-15 / chunk 2 c2, v[2], v[3] chunk 2 c2 + 1
-          const uint32_t w0 = v[0] >> 8, w1 = v[1] >> 8, w2 = v[2] >> 8, w3 = v[3] >> 8;
-          const uint32_t a0[4] = {v[0] & kNibLo, v[2] & kNibLo, v[1] & kNibLo, v[3] & kNibLo};
-          mma_f16(o[4 * c2 + 0], a0, pb0, pb1);
-          const uint32_t a1[4] = {v[0] & kNibHi, v[2] & kNibHi, v[1] & kNibHi, v[3] & kNibHi};
-          mma_f16(o[4 * c2 + 1], a1, pb0, pb1);
-          const uint32_t a2[4] = {w0 & kNibLo, w2 & kNibLo, w1 & kNibLo, w3 & kNibLo};
-          mma_f16(o[4 * c2 + 2], a2, pb0, pb1);
-          const uint32_t a3[4] = {w0 & kNibHi, w2 & kNibHi, w1 & kNibHi, w3 & kNibHi};
-          mma_f16(o[4 * c2 + 3], a3, pb0, pb1);
+        for (int bb = 0; bb < 2; ++bb) {
+#pragma unroll
+          for (int c2 = 0; c2 < NCH / 2; ++c2) {
+            uint32_t v[4];
+            ldsm_x4_trans(vt + code_off<C::kRowB>(base + 16 * bb + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0],
+                          v[1], v[2], v[3]);
+            // v[0] keys 0-7 / chunk 2 c2, v[1] keys 8-15 / chunk 2 c2, v[2], v[3] chunk 2 c2 + 1
+            const uint32_t w0 = v[0] >> 8, w1 = v[1] >> 8, w2 = v[2] >> 8, w3 = v[3] >> 8;
+            const uint32_t a0[4] = {v[0] & kNibLo, v[2] & kNibLo, v[1] & kNibLo, v[3] & kNibLo};
+            mma_f16(o[4 * c2 + 0], a0, pb[bb][0], pb[bb][1]);
+            const uint32_t a1[4] = {v[0] & kNibHi, v[2] & kNibHi, v[1] & kNibHi, v[3] & kNibHi};
+            mma_f16(o[4 * c2 + 1], a1, pb[bb][0], pb[bb][1]);
+            const uint32_t a2[4] = {w0 & kNibLo, w2 & kNibLo, w1 & kNibLo, w3 & kNibLo};
+            mma_f16(o[4 * c2 + 2], a2, pb[bb][0], pb[bb][1]);
+            const uint32_t a3[4] = {w0 & kNibHi, w2 & kNibHi, w1 & kNibHi, w3 & kNibHi};
+            mma_f16(o[4 * c2 + 3], a3, pb[bb][0], pb[bb][1]);
+          }
         }
       }
       __syncwarp();
