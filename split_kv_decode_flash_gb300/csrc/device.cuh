@@ -104,6 +104,16 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 
 // ---- visibility programs (M4.5 §0x05A, §0x08B; M5.4 §0x04-§0x05) --------------------
 
+// 2^x with the hardware's approximate exponential (PTX ex2.approx.ftz.f32:
+// relative error about 2^-22, -inf gives +0, results below 2^-126 flush to
+// zero).  The softmax weights it produces are summed in fp32 and cast to
+// f16 / bf16 for the P.V product, far coarser than its error.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 struct MaskCtx {
   int mask, S_q, T, n_sink, window;
 };

@@ -600,10 +600,10 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
         mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 16));
         const float m_new = fmaxf(m_run, mx);
-        const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+        const float alpha = m_new == -INFINITY ? 1.f : ex2_approx(m_run - m_new);
         float pk[4];
 #pragma unroll
-        for (int pp = 0; pp < 4; ++pp) pk[pp] = sv[pp] == -INFINITY ? 0.f : exp2f(sv[pp] - m_new);
+        for (int pp = 0; pp < 4; ++pp) pk[pp] = sv[pp] == -INFINITY ? 0.f : ex2_approx(sv[pp] - m_new);
         l_run = l_run * alpha + ((pk[0] + pk[1]) + (pk[2] + pk[3]));
         m_run = m_new;
         if (__any_sync(kAll, alpha != 1.f)) {

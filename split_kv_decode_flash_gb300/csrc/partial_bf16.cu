@@ -301,16 +301,16 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
       mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 2));
       mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 2));
       const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
-      const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+      const float a0 = n0 == -INFINITY ? 1.f : ex2_approx(m0 - n0);
+      const float a1 = n1 == -INFINITY ? 1.f : ex2_approx(m1 - n1);
       const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
       float pr[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        pr[nt][0] = exp2f(s[nt][0] - u0);
-        pr[nt][1] = exp2f(s[nt][1] - u0);
-        pr[nt][2] = exp2f(s[nt][2] - u1);
-        pr[nt][3] = exp2f(s[nt][3] - u1);
+        pr[nt][0] = ex2_approx(s[nt][0] - u0);
+        pr[nt][1] = ex2_approx(s[nt][1] - u0);
+        pr[nt][2] = ex2_approx(s[nt][2] - u1);
+        pr[nt][3] = ex2_approx(s[nt][3] - u1);
       }
       l0 = l0 * a0 + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
       l1 = l1 * a1 + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));

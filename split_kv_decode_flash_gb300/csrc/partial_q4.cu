@@ -777,16 +777,16 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
           mxb = fmaxf(mxb, __shfl_xor_sync(kAll, mxb, x));
         }
         const float na = fmaxf(ma, mxa), nb = fmaxf(mb, mxb);
-        const float aa = na == -INFINITY ? 1.f : exp2f(ma - na);
-        const float ab = nb == -INFINITY ? 1.f : exp2f(mb - nb);
+        const float aa = na == -INFINITY ? 1.f : ex2_approx(ma - na);
+        const float ab = nb == -INFINITY ? 1.f : ex2_approx(mb - nb);
         const float ua = na == -INFINITY ? 0.f : na, ub = nb == -INFINITY ? 0.f : nb;
         float pr[NS][4];
 #pragma unroll
         for (int u = 0; u < NS; ++u) {
-          pr[u][0] = exp2f(s[u][0] - ua);
-          pr[u][1] = exp2f(s[u][1] - ub);
-          pr[u][2] = exp2f(s[u][2] - ua);
-          pr[u][3] = exp2f(s[u][3] - ub);
+          pr[u][0] = ex2_approx(s[u][0] - ua);
+          pr[u][1] = ex2_approx(s[u][1] - ub);
+          pr[u][2] = ex2_approx(s[u][2] - ua);
+          pr[u][3] = ex2_approx(s[u][3] - ub);
         }
         float sa = 0.f, sb = 0.f;
 #pragma unroll

@@ -398,16 +398,16 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 2));
         const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
-        const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+        const float a0 = n0 == -INFINITY ? 1.f : ex2_approx(m0 - n0);
+        const float a1 = n1 == -INFINITY ? 1.f : ex2_approx(m1 - n1);
         const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
         float pr[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          pr[nt][0] = exp2f(s[nt][0] - u0);
-          pr[nt][1] = exp2f(s[nt][1] - u0);
-          pr[nt][2] = exp2f(s[nt][2] - u1);
-          pr[nt][3] = exp2f(s[nt][3] - u1);
+          pr[nt][0] = ex2_approx(s[nt][0] - u0);
+          pr[nt][1] = ex2_approx(s[nt][1] - u0);
+          pr[nt][2] = ex2_approx(s[nt][2] - u1);
+          pr[nt][3] = ex2_approx(s[nt][3] - u1);
         }
         // per-token V scale folded into the probabilities (the f16 A operand)
         const uint32_t pa[4] = {pack_f16(pr[0][0] * vs[0][0], pr[0][1] * vs[0][1]),
@@ -642,10 +642,10 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
           mxb = fmaxf(mxb, __shfl_xor_sync(kAll, mxb, x));
         }
         const float na = fmaxf(ma, mxa), nb = fmaxf(mb, mxb);
-        const float aa = na == -INFINITY ? 1.f : exp2f(ma - na);
-        const float ab = nb == -INFINITY ? 1.f : exp2f(mb - nb);
+        const float aa = na == -INFINITY ? 1.f : ex2_approx(ma - na);
+        const float ab = nb == -INFINITY ? 1.f : ex2_approx(mb - nb);
         const float ua = na == -INFINITY ? 0.f : na, ub = nb == -INFINITY ? 0.f : nb;
-        const float p0 = exp2f(s[0] - ua), p1 = exp2f(s[1] - ub), p2 = exp2f(s[2] - ua), p3 = exp2f(s[3] - ub);
+        const float p0 = ex2_approx(s[0] - ua), p1 = ex2_approx(s[1] - ub), p2 = ex2_approx(s[2] - ua), p3 = ex2_approx(s[3] - ub);
         // P'^T (keys x rows), V scale folded in, f16; transposed into B fragments
         const uint32_t px = pack_f16(p0 * vqx.x, p1 * vqx.x), py = pack_f16(p2 * vqy.x, p3 * vqy.x);
         const float2 fx = half2_bits_to_float2(px), fy = half2_bits_to_float2(py);

@@ -151,16 +151,6 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// 2^x with the hardware's approximate exponential (PTX ex2.approx.ftz.f32:
-// relative error about 2^-22, -inf gives +0, results below 2^-126 flush to
-// zero).  The softmax weights it produces are summed in fp32 and cast to
-// f16 / bf16 for the P.V product, far coarser than its error.
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
