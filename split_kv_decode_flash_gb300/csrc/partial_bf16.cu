@@ -189,7 +189,7 @@ __device__ __forceinline__ void load_q(const PartialParams& p, const ItemRec& r,
   }
 }
 
-template <int D>
+template <int D, int KW>
 __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, bool dep_wait) {
   using C = Bf<D>;
   dependency_wait(dep_wait);   // before Q and the state writes
@@ -200,10 +200,15 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
   const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
 
-  // Row blocks of 16 query rows; with one block, two stage groups of four
-  // warps take alternate stages.  Each warp owns 16 keys of its stages.
-  const int nrb = p.rows <= 16 ? 1 : 2;
-  const int ng = nrb == 1 ? 2 : 1;
+  // Two stage groups of four warps take alternate stages.  KW = 16: one row
+  // block of 16 query rows, each warp owns 16 keys of its stages.  KW = 32:
+  // two row blocks (17 to 32 rows) times two key halves, each warp owns 32
+  // keys, so that its S accumulation runs as four independent mma chains and
+  // one softmax update covers 32 keys.
+  static_assert(KW == 16 || KW == 32, "keys per warp");
+  constexpr int NTK = KW / 8;  // 8-key tiles of a warp's keys
+  constexpr int nrb = KW == 16 ? 1 : 2;
+  constexpr int ng = 2;
   const int wps = kConsumerWarps / ng;
   const int sgrp = cw / wps, wi = cw % wps;
   const int rb = wi % nrb, ts = wi / nrb;
@@ -217,20 +222,27 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
 
   uint32_t k = 0;
   bool dead = false;   // a bounded wait gave up: stop consuming, write nothing
-  // the next item's query fragments are loaded while the current item runs
-  uint32_t qn[KS][4];
-  if (w.begin < w.end) load_q<D>(p, w.rec(w.begin), r0, r1, t4, qn);
+  // KW = 16: the next item's query fragments are loaded while the current
+  // item runs (KW = 32 keeps the registers for its wider score tiles)
+  uint32_t qn[KW == 16 ? KS : 1][4];
+  if constexpr (KW == 16) {
+    if (w.begin < w.end) load_q<D>(p, w.rec(w.begin), r0, r1, t4, qn);
+  }
   for (int ii = w.begin; ii < w.end; ++ii) {
     const ItemRec rec = w.rec(ii);
     const WorkItem it = rec.it;
     const MaskCtx mc{p.mask, rec.nq, it.T, p.n_sink, p.window};
     const bool ok0 = r0 < p.g * rec.nq, ok1 = r1 < p.g * rec.nq;   // rows of the request
     uint32_t qa[KS][4];
+    if constexpr (KW == 16) {
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk)
+      for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
-      for (int x = 0; x < 4; ++x) qa[kk][x] = qn[kk][x];
-    if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1), r0, r1, t4, qn);
+        for (int x = 0; x < 4; ++x) qa[kk][x] = qn[kk][x];
+      if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1), r0, r1, t4, qn);
+    } else {
+      load_q<D>(p, rec, r0, r1, t4, qa);
+    }
     float o[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -258,12 +270,12 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
       const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kTK;
       const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
       const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
-      const int base = ts * 16;
+      const int base = ts * KW;
 
-      // S = Q K^T over the warp's 16 keys (two 8-key tiles)
-      float s[2][4];
+      // S = Q K^T over the warp's KW keys (8-key tiles)
+      float s[NTK][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < NTK; ++nt) {
         s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
         for (int m = 0; m < KS / 2; ++m) {
@@ -275,7 +287,7 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
       }
       // scale to log2 units, -inf where the key is absent or masked for the row
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < NTK; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int slot = base + nt * 8 + 2 * t4 + e;
@@ -296,6 +308,11 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
       // online softmax: row maxima over the lane quad
       float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
       float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+#pragma unroll
+      for (int nt = 2; nt < NTK; ++nt) {
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+      }
       mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 1));
       mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 2));
@@ -304,16 +321,19 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
       const float a0 = n0 == -INFINITY ? 1.f : ex2_approx(m0 - n0);
       const float a1 = n1 == -INFINITY ? 1.f : ex2_approx(m1 - n1);
       const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
-      float pr[2][4];
+      float (&pr)[NTK][4] = s;   // the probabilities replace the scores
+      float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < NTK; ++nt) {
         pr[nt][0] = ex2_approx(s[nt][0] - u0);
         pr[nt][1] = ex2_approx(s[nt][1] - u0);
         pr[nt][2] = ex2_approx(s[nt][2] - u1);
         pr[nt][3] = ex2_approx(s[nt][3] - u1);
+        ps0 += pr[nt][0] + pr[nt][1];
+        ps1 += pr[nt][2] + pr[nt][3];
       }
-      l0 = l0 * a0 + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
-      l1 = l1 * a1 + ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
+      l0 = l0 * a0 + ps0;
+      l1 = l1 * a1 + ps1;
       m0 = n0;
       m1 = n1;
       if (__any_sync(kAll, a0 != 1.f || a1 != 1.f)) {
@@ -325,15 +345,21 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
           o[n][3] *= a1;
         }
       }
-      // O += P V: the S fragments re-packed as the A operand (keys are the k index)
-      const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
-                              pack_bf16(pr[1][0], pr[1][1]), pack_bf16(pr[1][2], pr[1][3])};
+      // O += P V: the S fragments re-packed as the A operand (keys are the k index),
+      // one k-step per 16 keys
 #pragma unroll
-      for (int n2 = 0; n2 < NT / 2; ++n2) {
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_trans(vt + tile_off<2 * D>(base + (lmat & 1) * 8 + lrow, 2 * n2 + (lmat >> 1)), v0, v1, v2, v3);
-        mma_bf16(o[2 * n2], pa, v0, v1);
-        mma_bf16(o[2 * n2 + 1], pa, v2, v3);
+      for (int kb = 0; kb < KW / 16; ++kb) {
+        const uint32_t pa[4] = {pack_bf16(pr[2 * kb][0], pr[2 * kb][1]), pack_bf16(pr[2 * kb][2], pr[2 * kb][3]),
+                                pack_bf16(pr[2 * kb + 1][0], pr[2 * kb + 1][1]),
+                                pack_bf16(pr[2 * kb + 1][2], pr[2 * kb + 1][3])};
+#pragma unroll
+        for (int n2 = 0; n2 < NT / 2; ++n2) {
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_trans(vt + tile_off<2 * D>(base + 16 * kb + (lmat & 1) * 8 + lrow, 2 * n2 + (lmat >> 1)), v0, v1,
+                        v2, v3);
+          mma_bf16(o[2 * n2], pa, v0, v1);
+          mma_bf16(o[2 * n2 + 1], pa, v2, v3);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * st);
@@ -444,10 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
   const int incomplete = fill_item_cache(p, cache, it_begin, it_end);
   if (threadIdx.x == 0) {
-    const int warps_per_stage = p.rows <= 16 ? kConsumerWarps / 2 : kConsumerWarps;
-    for (int s = 0; s < C::kStagesN; ++s) {
+    for (int s = 0; s < C::kStagesN; ++s) {   // four consumer warps take each stage
       mbar_init(smem_u32(smem + C::kFullBar + 8 * s), 1);
-      mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), warps_per_stage);
+      mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), kConsumerWarps / 2);
     }
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
     fence_barrier_init();
@@ -466,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));
-  consume_bf16<D>(w, smem, warp, lane, !complete_now);
+  if (p.rows <= 16) consume_bf16<D, 16>(w, smem, warp, lane, !complete_now);
+  else consume_bf16<D, 32>(w, smem, warp, lane, !complete_now);
   if (p.fused) fused_merge<D>(w, smem, warp, lane);
 }
 
