@@ -168,6 +168,11 @@ typedef struct {
                                    and lse ([qo_indptr[B], H_q, d] and [qo_indptr[B], H_q]),
                                    at positions T_b - C_b + i (bottom-right).  NULL: C_b =
                                    S_q for every request.  Non-uniform C_b: bf16 K/V only */
+  int32_t item_cost_keys;       /* default (equal-segment) mode: the fixed cost of a work
+                                   item, in keys, charged when the concatenated streams are
+                                   cut into one segment per CTA, so that a CTA holding many
+                                   short items (tiny requests) gets fewer keys.  0 = library
+                                   default (about 48 KB of K/V per item); < 0 = none     */
 } dattn_plan_inputs;
 
 typedef struct dattn_plan_s dattn_plan_t;

@@ -52,7 +52,7 @@ class PlanInputs(ctypes.Structure):
                 ("index_indptr", ctypes.c_void_p), ("index_list", ctypes.c_void_p),
                 ("num_sms", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("chunk_tokens", ctypes.c_int32), ("fused_merge", ctypes.c_int32),
-                ("qo_indptr", ctypes.c_void_p)]
+                ("qo_indptr", ctypes.c_void_p), ("item_cost_keys", ctypes.c_int32)]
 
 
 class Tensors(ctypes.Structure):
@@ -212,7 +212,7 @@ class Plan:
 
 
 def dattn_plan(problem, kv_len, *, page_indptr=None, index_indptr=None, index_list=None, num_sms=None,
-               ctas_per_sm=0, chunk_tokens=0, fused_merge=False, qo_indptr=None) -> Plan:
+               ctas_per_sm=0, chunk_tokens=0, fused_merge=False, qo_indptr=None, item_cost_keys=0) -> Plan:
     """Host-only planning (see dattn_plan in dattn.h).  Arrays are host int32."""
     lib = load()
     prob = problem if isinstance(problem, Problem) else make_problem(problem)
@@ -222,7 +222,8 @@ def dattn_plan(problem, kv_len, *, page_indptr=None, index_indptr=None, index_li
     keep = [_i32_host(kv_len), _i32_host(page_indptr), _i32_host(index_indptr), _i32_host(index_list),
             _i32_host(qo_indptr)]
     inp = PlanInputs(_ptr(keep[0]), _ptr(keep[1]), _ptr(keep[2]), _ptr(keep[3]), int(num_sms),
-                     int(ctas_per_sm), int(chunk_tokens), int(bool(fused_merge)), _ptr(keep[4]))
+                     int(ctas_per_sm), int(chunk_tokens), int(bool(fused_merge)), _ptr(keep[4]),
+                     int(item_cost_keys))
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     _check(lib.dattn_plan(ctypes.byref(prob), ctypes.byref(inp), ctypes.byref(handle), ctypes.byref(ws)),

@@ -189,191 +189,226 @@ __device__ __forceinline__ void load_q(const PartialParams& p, const ItemRec& r,
   }
 }
 
+// A consumer warp's part of an item.  Two stage groups of four warps take
+// alternate stages.  KW = 16: one row block of 16 query rows, each warp owns
+// 16 keys of its stages (8 states per row).  KW = 32: two row blocks (17 to
+// 32 rows) times two key halves, each warp owns 32 keys, so that its S
+// accumulation runs as four independent mma chains and one softmax update
+// covers 32 keys (4 states per row).
+template <int KW>
+struct WarpRole {
+  static_assert(KW == 16 || KW == 32, "keys per warp");
+  static constexpr int nrb = KW == 16 ? 1 : 2;
+  int sgrp, rb, ts, my_state, r0, r1;
+  __device__ __forceinline__ WarpRole(int cw, int lane) {
+    constexpr int wps = kConsumerWarps / 2;
+    sgrp = cw / wps;
+    const int wi = cw % wps;
+    rb = wi % nrb;
+    ts = wi / nrb;
+    my_state = (cw - rb) / nrb;
+    r0 = rb * 16 + (lane >> 2);   // the lane's two accumulator rows
+    r1 = r0 + 8;
+  }
+};
+
+// One item: its stages (k counts the CTA's stages across items), then its rows.
 template <int D, int KW>
-__device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, bool dep_wait) {
+__device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const ItemRec& rec,
+                                             const uint32_t (&qa)[D / 16][4], int cw, int lane, uint32_t& k,
+                                             bool& dead) {
   using C = Bf<D>;
-  dependency_wait(dep_wait);   // before Q and the state writes
   const PartialParams& p = w.p;
   constexpr int KS = D / 16;   // k-steps of q.k
   constexpr int NT = D / 8;    // 8-channel tiles of the output
+  constexpr int NTK = KW / 8;  // 8-key tiles of a warp's keys
+  constexpr int ng = 2;
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
   const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
-
-  // Two stage groups of four warps take alternate stages.  KW = 16: one row
-  // block of 16 query rows, each warp owns 16 keys of its stages.  KW = 32:
-  // two row blocks (17 to 32 rows) times two key halves, each warp owns 32
-  // keys, so that its S accumulation runs as four independent mma chains and
-  // one softmax update covers 32 keys.
-  static_assert(KW == 16 || KW == 32, "keys per warp");
-  constexpr int NTK = KW / 8;  // 8-key tiles of a warp's keys
-  constexpr int nrb = KW == 16 ? 1 : 2;
-  constexpr int ng = 2;
-  const int wps = kConsumerWarps / ng;
-  const int sgrp = cw / wps, wi = cw % wps;
-  const int rb = wi % nrb, ts = wi / nrb;
-  const int my_state = (cw - rb) / nrb;
+  const WarpRole<KW> role(cw, lane);
+  const int sgrp = role.sgrp, ts = role.ts, my_state = role.my_state, r0 = role.r0, r1 = role.r1;
   const int g4 = lane >> 2, t4 = lane & 3;
-  const int r0 = rb * 16 + g4, r1 = r0 + 8;   // the lane's two accumulator rows
   const int qi0 = r0 / p.g, qi1 = r1 / p.g;
   const int lrow = lane & 7, lmat = lane >> 3;   // ldmatrix address roles
   const float sc = p.scale_log2;
   const bool fm = p.mask == DATTN_MASK_FLASHMASK;
+  const WorkItem it = rec.it;
+  const MaskCtx mc{p.mask, rec.nq, it.T, p.n_sink, p.window};
+  const bool ok0 = r0 < p.g * rec.nq, ok1 = r1 < p.g * rec.nq;   // rows of the request
+  (void)g4;
+  float o[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
+  for (int j0 = it.a; j0 < it.e; ++k) {
+    const int j1 = min(j0 + kTK, it.e);
+    if (static_cast<int>(k % ng) != sgrp) {     // the other stage group's turn
+      j0 = j1;
+      continue;
+    }
+    const int st = k % C::kStagesN;
+    const uint32_t use = k / C::kStagesN;
+    if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+      dead = true;
+      break;
+    }
+    if (reinterpret_cast<const volatile int*>(smem + C::kSeq)[st] != static_cast<int>(k)) {
+      if (lane == 0) atomicOr(p.status, kStPipeline);   // wrong phase: stop, never consume stale data
+      *abort_flag = 1;
+      dead = true;
+      break;
+    }
+    const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kTK;
+    const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kTK;
+    const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
+    const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
+    const int base = ts * KW;
+
+    // S = Q K^T over the warp's KW keys (8-key tiles)
+    float s[NTK][4];
+#pragma unroll
+    for (int nt = 0; nt < NTK; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int m = 0; m < KS / 2; ++m) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kt + tile_off<2 * D>(base + nt * 8 + lrow, 4 * m + lmat), b0, b1, b2, b3);
+        mma_bf16(s[nt], qa[2 * m], b0, b1);
+        mma_bf16(s[nt], qa[2 * m + 1], b2, b3);
+      }
+    }
+    // scale to log2 units, -inf where the key is absent or masked for the row
+#pragma unroll
+    for (int nt = 0; nt < NTK; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int slot = base + nt * 8 + 2 * t4 + e;
+        const int t = pos[slot];
+        bool v0, v1;
+        if (fm) {   // FlashMask: the producer's row bits of the column
+          const uint32_t bits = vis[slot];
+          v0 = t >= 0 && ok0 && (full || ((bits >> qi0) & 1u));
+          v1 = t >= 0 && ok1 && (full || ((bits >> qi1) & 1u));
+        } else {
+          v0 = t >= 0 && ok0 && (full || key_visible(mc, qi0, t));
+          v1 = t >= 0 && ok1 && (full || key_visible(mc, qi1, t));
+        }
+        s[nt][e] = v0 ? s[nt][e] * sc : -INFINITY;
+        s[nt][2 + e] = v1 ? s[nt][2 + e] * sc : -INFINITY;
+      }
+    }
+    // online softmax: row maxima over the lane quad
+    float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+#pragma unroll
+    for (int nt = 2; nt < NTK; ++nt) {
+      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 2));
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+    const float a0 = n0 == -INFINITY ? 1.f : ex2_approx(m0 - n0);
+    const float a1 = n1 == -INFINITY ? 1.f : ex2_approx(m1 - n1);
+    const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+    float (&pr)[NTK][4] = s;   // the probabilities replace the scores
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NTK; ++nt) {
+      pr[nt][0] = ex2_approx(s[nt][0] - u0);
+      pr[nt][1] = ex2_approx(s[nt][1] - u0);
+      pr[nt][2] = ex2_approx(s[nt][2] - u1);
+      pr[nt][3] = ex2_approx(s[nt][3] - u1);
+      ps0 += pr[nt][0] + pr[nt][1];
+      ps1 += pr[nt][2] + pr[nt][3];
+    }
+    l0 = l0 * a0 + ps0;
+    l1 = l1 * a1 + ps1;
+    m0 = n0;
+    m1 = n1;
+    if (__any_sync(kAll, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] *= a0;
+        o[n][1] *= a0;
+        o[n][2] *= a1;
+        o[n][3] *= a1;
+      }
+    }
+    // O += P V: the S fragments re-packed as the A operand (keys are the k index),
+    // one k-step per 16 keys
+#pragma unroll
+    for (int kb = 0; kb < KW / 16; ++kb) {
+      const uint32_t pa[4] = {pack_bf16(pr[2 * kb][0], pr[2 * kb][1]), pack_bf16(pr[2 * kb][2], pr[2 * kb][3]),
+                              pack_bf16(pr[2 * kb + 1][0], pr[2 * kb + 1][1]),
+                              pack_bf16(pr[2 * kb + 1][2], pr[2 * kb + 1][3])};
+#pragma unroll
+      for (int n2 = 0; n2 < NT / 2; ++n2) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(vt + tile_off<2 * D>(base + 16 * kb + (lmat & 1) * 8 + lrow, 2 * n2 + (lmat >> 1)), v0, v1,
+                      v2, v3);
+        mma_bf16(o[2 * n2], pa, v0, v1);
+        mma_bf16(o[2 * n2 + 1], pa, v2, v3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    j0 = j1;
+  }
+
+  // end of item: complete the row sums over the quad and leave the rows
+  l0 += __shfl_xor_sync(kAll, l0, 1);
+  l1 += __shfl_xor_sync(kAll, l1, 1);
+  l0 += __shfl_xor_sync(kAll, l0, 2);
+  l1 += __shfl_xor_sync(kAll, l1, 2);
+  if (!dead) {
+    if (ok0) emit_row<D>(p, it, rec.qo, my_state, r0, m0, l0, o, 0, t4);
+    if (ok1) emit_row<D>(p, it, rec.qo, my_state, r1, m1, l1, o, 1, t4);
+  }
+}
+
+// Items of a call with at most 16 rows run the one-tile layout, with the next
+// item's query fragments loaded while the current one runs.  In a call with
+// more rows (a mixed batch's widest request, or a uniform batch of 17 to 32
+// rows) each item takes the layout of its own request's g C_b rows.
+template <int D>
+__device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, bool dep_wait) {
+  dependency_wait(dep_wait);   // before Q and the state writes
+  const PartialParams& p = w.p;
+  constexpr int KS = D / 16;
+  const int t4 = lane & 3;
   uint32_t k = 0;
   bool dead = false;   // a bounded wait gave up: stop consuming, write nothing
-  // KW = 16: the next item's query fragments are loaded while the current
-  // item runs (KW = 32 keeps the registers for its wider score tiles)
-  uint32_t qn[KW == 16 ? KS : 1][4];
-  if constexpr (KW == 16) {
-    if (w.begin < w.end) load_q<D>(p, w.rec(w.begin), r0, r1, t4, qn);
-  }
-  for (int ii = w.begin; ii < w.end; ++ii) {
-    const ItemRec rec = w.rec(ii);
-    const WorkItem it = rec.it;
-    const MaskCtx mc{p.mask, rec.nq, it.T, p.n_sink, p.window};
-    const bool ok0 = r0 < p.g * rec.nq, ok1 = r1 < p.g * rec.nq;   // rows of the request
-    uint32_t qa[KS][4];
-    if constexpr (KW == 16) {
+  if (p.rows <= 16) {
+    const WarpRole<16> role(cw, lane);
+    uint32_t qn[KS][4];
+    if (w.begin < w.end) load_q<D>(p, w.rec(w.begin), role.r0, role.r1, t4, qn);
+    for (int ii = w.begin; ii < w.end; ++ii) {
+      uint32_t qa[KS][4];
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk)
 #pragma unroll
         for (int x = 0; x < 4; ++x) qa[kk][x] = qn[kk][x];
-      if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1), r0, r1, t4, qn);
-    } else {
-      load_q<D>(p, rec, r0, r1, t4, qa);
+      if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1), role.r0, role.r1, t4, qn);
+      consume_item<D, 16>(w, smem, w.rec(ii), qa, cw, lane, k, dead);
     }
-    float o[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-    for (int j0 = it.a; j0 < it.e; ++k) {
-      const int j1 = min(j0 + kTK, it.e);
-      if (static_cast<int>(k % ng) != sgrp) {     // the other stage group's turn
-        j0 = j1;
-        continue;
+  } else {
+    for (int ii = w.begin; ii < w.end; ++ii) {
+      const ItemRec rec = w.rec(ii);
+      uint32_t qa[KS][4];
+      if (p.g * rec.nq <= 16) {
+        const WarpRole<16> role(cw, lane);
+        load_q<D>(p, rec, role.r0, role.r1, t4, qa);
+        consume_item<D, 16>(w, smem, rec, qa, cw, lane, k, dead);
+      } else {
+        const WarpRole<32> role(cw, lane);
+        load_q<D>(p, rec, role.r0, role.r1, t4, qa);
+        consume_item<D, 32>(w, smem, rec, qa, cw, lane, k, dead);
       }
-      const int st = k % C::kStagesN;
-      const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
-        dead = true;
-        break;
-      }
-      if (reinterpret_cast<const volatile int*>(smem + C::kSeq)[st] != static_cast<int>(k)) {
-        if (lane == 0) atomicOr(p.status, kStPipeline);   // wrong phase: stop, never consume stale data
-        *abort_flag = 1;
-        dead = true;
-        break;
-      }
-      const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kTK;
-      const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kTK;
-      const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
-      const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
-      const int base = ts * KW;
-
-      // S = Q K^T over the warp's KW keys (8-key tiles)
-      float s[NTK][4];
-#pragma unroll
-      for (int nt = 0; nt < NTK; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-        for (int m = 0; m < KS / 2; ++m) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kt + tile_off<2 * D>(base + nt * 8 + lrow, 4 * m + lmat), b0, b1, b2, b3);
-          mma_bf16(s[nt], qa[2 * m], b0, b1);
-          mma_bf16(s[nt], qa[2 * m + 1], b2, b3);
-        }
-      }
-      // scale to log2 units, -inf where the key is absent or masked for the row
-#pragma unroll
-      for (int nt = 0; nt < NTK; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int slot = base + nt * 8 + 2 * t4 + e;
-          const int t = pos[slot];
-          bool v0, v1;
-          if (fm) {   // FlashMask: the producer's row bits of the column
-            const uint32_t bits = vis[slot];
-            v0 = t >= 0 && ok0 && (full || ((bits >> qi0) & 1u));
-            v1 = t >= 0 && ok1 && (full || ((bits >> qi1) & 1u));
-          } else {
-            v0 = t >= 0 && ok0 && (full || key_visible(mc, qi0, t));
-            v1 = t >= 0 && ok1 && (full || key_visible(mc, qi1, t));
-          }
-          s[nt][e] = v0 ? s[nt][e] * sc : -INFINITY;
-          s[nt][2 + e] = v1 ? s[nt][2 + e] * sc : -INFINITY;
-        }
-      }
-      // online softmax: row maxima over the lane quad
-      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-#pragma unroll
-      for (int nt = 2; nt < NTK; ++nt) {
-        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float a0 = n0 == -INFINITY ? 1.f : ex2_approx(m0 - n0);
-      const float a1 = n1 == -INFINITY ? 1.f : ex2_approx(m1 - n1);
-      const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
-      float (&pr)[NTK][4] = s;   // the probabilities replace the scores
-      float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < NTK; ++nt) {
-        pr[nt][0] = ex2_approx(s[nt][0] - u0);
-        pr[nt][1] = ex2_approx(s[nt][1] - u0);
-        pr[nt][2] = ex2_approx(s[nt][2] - u1);
-        pr[nt][3] = ex2_approx(s[nt][3] - u1);
-        ps0 += pr[nt][0] + pr[nt][1];
-        ps1 += pr[nt][2] + pr[nt][3];
-      }
-      l0 = l0 * a0 + ps0;
-      l1 = l1 * a1 + ps1;
-      m0 = n0;
-      m1 = n1;
-      if (__any_sync(kAll, a0 != 1.f || a1 != 1.f)) {
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          o[n][0] *= a0;
-          o[n][1] *= a0;
-          o[n][2] *= a1;
-          o[n][3] *= a1;
-        }
-      }
-      // O += P V: the S fragments re-packed as the A operand (keys are the k index),
-      // one k-step per 16 keys
-#pragma unroll
-      for (int kb = 0; kb < KW / 16; ++kb) {
-        const uint32_t pa[4] = {pack_bf16(pr[2 * kb][0], pr[2 * kb][1]), pack_bf16(pr[2 * kb][2], pr[2 * kb][3]),
-                                pack_bf16(pr[2 * kb + 1][0], pr[2 * kb + 1][1]),
-                                pack_bf16(pr[2 * kb + 1][2], pr[2 * kb + 1][3])};
-#pragma unroll
-        for (int n2 = 0; n2 < NT / 2; ++n2) {
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_trans(vt + tile_off<2 * D>(base + 16 * kb + (lmat & 1) * 8 + lrow, 2 * n2 + (lmat >> 1)), v0, v1,
-                        v2, v3);
-          mma_bf16(o[2 * n2], pa, v0, v1);
-          mma_bf16(o[2 * n2 + 1], pa, v2, v3);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * st);
-      j0 = j1;
-    }
-
-    // end of item: complete the row sums over the quad and leave the rows
-    l0 += __shfl_xor_sync(kAll, l0, 1);
-    l1 += __shfl_xor_sync(kAll, l1, 1);
-    l0 += __shfl_xor_sync(kAll, l0, 2);
-    l1 += __shfl_xor_sync(kAll, l1, 2);
-    if (!dead) {
-      if (ok0) emit_row<D>(p, it, rec.qo, my_state, r0, m0, l0, o, 0, t4);
-      if (ok1) emit_row<D>(p, it, rec.qo, my_state, r1, m1, l1, o, 1, t4);
     }
   }
 }
@@ -397,11 +432,12 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
   __threadfence();                                                // this thread's state writes
   named_barrier(1, 32 * kCW);
   if (cw == 0 && lane == 0) {
-    const int spi = kConsumerWarps / (p.rows <= 16 ? 1 : 2);       // states per item
     int n = 0;
     for (int ii = w.begin; ii < w.end; ++ii) {
       const int g = w.rec(ii).merge;
       if (g < 0) continue;
+      // states per item: 8 for requests of at most 16 rows, else 4
+      const int spi = p.rows <= 16 || p.g * p.groups[g].nq <= 16 ? kConsumerWarps : kConsumerWarps / 2;
       const int total = p.groups[g].n / spi;
       if (atomicAdd(p.group_count + g, 1) + 1 == total) list[1 + n++] = g;
     }
@@ -491,8 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));
-  if (p.rows <= 16) consume_bf16<D, 16>(w, smem, warp, lane, !complete_now);
-  else consume_bf16<D, 32>(w, smem, warp, lane, !complete_now);
+  consume_bf16<D>(w, smem, warp, lane, !complete_now);
   if (p.fused) fused_merge<D>(w, smem, warp, lane);
 }
 

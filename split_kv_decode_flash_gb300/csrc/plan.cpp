@@ -97,6 +97,25 @@ void check_problem(const dattn_problem* p, Checker& c) {
   if (p->fixed_splits < 0) c.fail(DATTN_EINVAL, "fixed_splits must be >= 0");
 }
 
+// Default cost of a work item in the equal-segment partition, in keys of the
+// format: about 48 KB of K/V of fixed pipeline time (a stage and a half of the
+// bf16 kernel) plus the partial states the item writes (rows x states per row
+// x (d + 2) fp32 values), which the merge reads back.
+static long long default_item_cost_keys(const dattn_problem& p, int item_rows, int states_per_row) {
+  const long long d = p.d_h;
+  long long kb;   // K and V bytes of one key
+  switch (p.fmt) {
+    case DATTN_FMT_INT8_TOKEN: kb = 2 * d + 8; break;
+    case DATTN_FMT_FP8_E4M3:
+    case DATTN_FMT_FP8_E5M2: kb = 2 * d; break;
+    case DATTN_FMT_INT4_HEAD:
+    case DATTN_FMT_INT4_KIVI: kb = d + 8; break;
+    default: kb = 4 * d;
+  }
+  const long long bytes = 49152 + static_cast<long long>(item_rows) * states_per_row * (d + 2) * 4;
+  return (bytes / kb + 15) / 16 * 16;
+}
+
 bool same_problem(const dattn_problem& a, const dattn_problem& b) {
   return std::memcmp(&a, &b, sizeof(dattn_problem)) == 0;
 }
@@ -263,13 +282,35 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   const long long cta_target = static_cast<long long>(in->num_sms) * cps;
   const long long L = in->chunk_tokens;
   const bool segmented = p.fixed_splits <= 0 && L <= 0;
+  // Every item also costs a fixed amount of pipeline time (its first stage's
+  // fill, its states), which the segments account for as "pad" keys charged
+  // at the start of each non-empty group: without it, a CTA that receives
+  // many tiny groups streams as many keys as the others plus their overheads,
+  // and finishes last.
+  const bool kivi_tc = kivi_on_tensor_cores(p.d_h, rows, p.kivi_v_group, p.mask, p.page_size, p.kivi_residual);
+  const int spi = states_per_item(rows, p.fmt, kivi_tc);
+  // states per row of request b's items: bf16 requests of at most 16 rows run
+  // the one-tile layout (8) even when the call's widest request has more
+  auto spi_of = [&](int b) {
+    return p.fmt == DATTN_FMT_BF16 && rows > 16 && (p.H_q / p.H_kv) * query_rows(b) <= 16
+               ? states_per_item(16, p.fmt, kivi_tc) : spi;
+  };
+  std::vector<long long> pad(n_groups, 0);
+  long long Wp = W;                                  // padded length of the concatenation
+  for (int k = 0; k < n_groups; ++k) {
+    if (!segmented || gn[k] == 0 || in->item_cost_keys < 0) continue;
+    const int b = k / H;
+    pad[k] = in->item_cost_keys > 0 ? in->item_cost_keys
+                                    : default_item_cost_keys(p, (p.H_q / p.H_kv) * query_rows(b), spi_of(b));
+    Wp += pad[k];
+  }
   long long seg = 1;
   int n_seg = 1;
-  if (segmented && W > 0) {
-    const long long want = std::max<long long>(1, std::min<long long>(cta_target, (W + kTK - 1) / kTK));
-    seg = (W + want - 1) / want;
+  if (segmented && Wp > 0) {
+    const long long want = std::max<long long>(1, std::min<long long>(cta_target, (Wp + kTK - 1) / kTK));
+    seg = (Wp + want - 1) / want;
     seg = (seg + 15) / 16 * 16;                      // whole 16-key tiles
-    n_seg = static_cast<int>((W + seg - 1) / seg);
+    n_seg = static_cast<int>((Wp + seg - 1) / seg);
   }
   std::vector<int> group_first(n_groups + 1, 0);
   std::vector<int> seg_cta;                          // segmented mode: the CTA of every item
@@ -298,9 +339,10 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
       // KIVI: cuts rounded up onto the 32-key grid, so that the consumers' 32-key
       // steps never straddle a K group (a CTA streams at most 31 keys more)
       const long long grid = p.fmt == DATTN_FMT_INT4_KIVI ? 32 : 1;
+      const long long k0 = g_off + pad[k];   // padded position of the group's first key
       for (long long a = 0; a < n;) {
-        const long long c = (g_off + a) / seg;
-        const long long e = std::min<long long>(n, ((c + 1) * seg - g_off + grid - 1) / grid * grid);
+        const long long c = std::min<long long>(n_seg - 1, (k0 + a) / seg);
+        const long long e = std::min<long long>(n, ((c + 1) * seg - k0 + grid - 1) / grid * grid);
         add(static_cast<int>(a), static_cast<int>(e));
         seg_cta.push_back(static_cast<int>(c));
         a = e;
@@ -310,7 +352,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
     } else {
       for (long long a = 0; a < n; a += L) add(static_cast<int>(a), static_cast<int>(std::min<long long>(n, a + L)));
     }
-    g_off += n;
+    g_off += n + pad[k];
   }
   group_first[n_groups] = static_cast<int>(items.size());
 
@@ -319,17 +361,16 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   //    group that is one item with one state per row writes O directly.
   std::vector<MergeGroup> merges;
   std::vector<int> merge_of_group(n_groups, -1);
-  const bool kivi_tc = kivi_on_tensor_cores(p.d_h, rows, p.kivi_v_group, p.mask, p.page_size, p.kivi_residual);
-  const int spi = states_per_item(rows, p.fmt, kivi_tc);
   int n_slots = 0, max_splits = 0;
   for (int k = 0; k < n_groups; ++k) {
     const int n = group_first[k + 1] - group_first[k];
     max_splits = std::max(max_splits, n);
-    if (n * spi > 1) {
+    const int spi_k = spi_of(k / H);
+    if (n * spi_k > 1) {
       merge_of_group[k] = static_cast<int>(merges.size());
-      merges.push_back(MergeGroup{k / H, k % H, n_slots, n * spi, query_start(k / H), query_rows(k / H), 0, 0});
-      for (int i = 0; i < n; ++i) items[group_first[k] + i].slot = n_slots + i * spi;
-      n_slots += n * spi;
+      merges.push_back(MergeGroup{k / H, k % H, n_slots, n * spi_k, query_start(k / H), query_rows(k / H), 0, 0});
+      for (int i = 0; i < n; ++i) items[group_first[k] + i].slot = n_slots + i * spi_k;
+      n_slots += n * spi_k;
     }
   }
 

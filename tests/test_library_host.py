@@ -145,6 +145,41 @@ def test_default_planner_covers_ragged_batch_and_balances():
     assert info["n_ctas"] <= 152
 
 
+def _cta_cost(items, pad_of):
+    """Per-CTA keys and items of a plan."""
+    keys, n = {}, {}
+    for it in items:
+        keys[it["cta"]] = keys.get(it["cta"], 0) + it["e"] - it["a"]
+        n[it["cta"]] = n.get(it["cta"], 0) + 1
+    return keys, n
+
+
+def test_item_cost_keeps_tiny_groups_from_piling_onto_one_cta():
+    """Two 8-key requests (16 tiny groups) inside a ragged batch: without an item cost they
+    land on one CTA that streams a full share of keys on top of their overheads; with the
+    default cost that CTA gets correspondingly fewer keys, and the cover stays exact."""
+    rng = np.random.default_rng(1)
+    T = rng.integers(1024, 8193, 16).tolist()
+    T = T[:12] + [8, 8] + T[12:]
+    groups = [(b, h) for b in range(18) for h in range(8)]
+    plain = dattn.dattn_plan(_problem(B=18, H_q=32, H_kv=8), T, num_sms=152, item_cost_keys=-1)
+    costed = dattn.dattn_plan(_problem(B=18, H_q=32, H_kv=8), T, num_sms=152)
+    for plan in (plain, costed):
+        _coverage(plan.items(), groups, lambda g: T[g[0]])
+    for plan, crowded_share in ((plain, 0.9), (costed, 0.8)):
+        keys, n = _cta_cost(plan.items(), None)
+        busiest = max(n, key=lambda c: n[c])
+        mean = plan.info["stream_keys"] / plan.info["n_ctas"]
+        if plan is plain:
+            assert n[busiest] >= 16 and keys[busiest] >= crowded_share * mean
+        else:
+            assert keys[busiest] <= crowded_share * mean
+    # a constant cost applies to every group; a negative one turns the cost off
+    const = dattn.dattn_plan(_problem(B=18, H_q=32, H_kv=8), T, num_sms=152, item_cost_keys=320)
+    _coverage(const.items(), groups, lambda g: T[g[0]])
+    assert [(i["a"], i["e"], i["cta"]) for i in plain.items()] != [(i["a"], i["e"], i["cta"]) for i in const.items()]
+
+
 def test_workspace_bytes_follow_the_mlu_ledger():
     """Partial area = n_slots * rows * (d * 4 + 2 * 4): the (m, l, u) ABI without a validity byte."""
     T = [4096, 3587]
