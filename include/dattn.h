@@ -22,7 +22,8 @@
  *    failing call on the calling thread (the rejection vector of M4.5 §0x07B).
  *  - Streams: "stream" is a cudaStream_t passed as void*.  Device work is
  *    enqueued on it and the library never synchronises the device, except in
- *    dattn_device_status, which reads back one word.
+ *    dattn_device_status / dattn_step_host_status, which read back one word,
+ *    and dattn_step_host, which returns its results in host memory.
  *  - Numbers: scores, maxima, sums and partial states are fp32; O is bf16
  *    rounded to nearest even; LSE is fp32 in natural-log units.  A query row
  *    with no visible key gets O = 0 and LSE = -inf (M4.5 §0x02C).
@@ -284,6 +285,57 @@ dattn_status dattn_plan_upload(const dattn_plan_t* plan, void* workspace, size_t
 dattn_status dattn_run_ex(const dattn_plan_t* plan, const dattn_problem* prob,
                           const dattn_tensors* t, void* workspace, size_t workspace_bytes,
                           void* stream, const dattn_run_options* options);
+
+/* ---- one step from host memory (the end-to-end path) --------------------------------
+ *
+ * The plan/run lifecycle of M4.5 §0x07F and §0x0AD in one call for a caller
+ * whose query and page table live in host memory: plan from the host lengths,
+ * one host->device transfer of the query, the page table and the work list,
+ * the partial and merge kernels, one device->host transfer of O and LSE, then
+ * the results are copied into the caller's host arrays.  Returns after the
+ * step has completed on "stream" (it synchronises the stream).  The cache
+ * (K, V and their qparams / residual) stays on the device: "cache" supplies
+ * only those pointers; its q, o, lse, page_indptr, page_indices fields are
+ * ignored.  Visibility programs that read device-side lists (INDEX_LIST,
+ * FLASHMASK) and mixed batches go through dattn_plan / dattn_run instead
+ * (EUNSUPPORTED here).  The step's device bounds-check word is read with
+ * dattn_step_host_status.
+ *
+ * Layouts (offsets from the start of each buffer, 256-byte aligned pieces):
+ *   workspace: [q | page_indptr | page_indices | plan workspace | O | LSE]
+ *   staging:   the same pieces in pinned host memory; the first four are sent
+ *              in one transfer, O and LSE come back in one transfer.
+ * The staging buffer should be page-locked (cudaHostAlloc / pinned) so that
+ * both transfers are asynchronous DMA; the library never allocates it. */
+typedef struct {
+  const void* q;                 /* host bf16 [B, S_q, H_q, d]                             */
+  const int32_t* kv_len;         /* host [B]: stored rows T_b                              */
+  const int32_t* page_indptr;    /* host [B+1] (paged layout; NULL for contiguous)         */
+  const int32_t* page_indices;   /* host [page_indptr[B]] (paged layout)                   */
+  void* o;                       /* host bf16 [B, S_q, H_q, d] (output)                    */
+  float* lse;                    /* host fp32 [B, S_q, H_q] (output) or NULL               */
+  int32_t num_sms;               /* SMs to plan for (>= 1)                                 */
+} dattn_host_step;
+
+/* Bytes of the device workspace and of the pinned staging buffer that
+ * dattn_step_host needs for this call (it plans once to find out). */
+dattn_status dattn_step_host_sizes(const dattn_problem* prob, const dattn_host_step* io,
+                                   size_t* workspace_bytes, size_t* staging_bytes);
+
+/* One decode step through host memory (see above).  The transfer of q and the
+ * page table is issued before the host plans, so that it overlaps planning;
+ * it writes only the workspace's input region.  Every other check (the plan's
+ * validation, the full workspace and staging sizes) runs before any kernel is
+ * launched; a failure returns its status (EWORKSPACE names the sizes needed)
+ * after the stream has at most received that one transfer. */
+dattn_status dattn_step_host(const dattn_problem* prob, const dattn_host_step* io, const dattn_tensors* cache,
+                             void* staging, size_t staging_bytes, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Device bounds-check word of the last dattn_step_host on this workspace (like
+ * dattn_device_status; synchronises "stream"). */
+dattn_status dattn_step_host_status(const dattn_problem* prob, const dattn_host_step* io, const void* workspace,
+                                    int32_t* flags, void* stream);
 
 /* Size of the library-owned scratch array that dattn_run_noalloc uses on each device. */
 #define DATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)  /* 16 MiB */

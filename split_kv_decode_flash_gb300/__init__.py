@@ -55,6 +55,12 @@ class PlanInputs(ctypes.Structure):
                 ("qo_indptr", ctypes.c_void_p), ("item_cost_keys", ctypes.c_int32)]
 
 
+class HostStep(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("kv_len", ctypes.c_void_p), ("page_indptr", ctypes.c_void_p),
+                ("page_indices", ctypes.c_void_p), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("num_sms", ctypes.c_int32)]
+
+
 class Tensors(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "q", "k", "v", "k_qparams", "v_qparams", "k_residual", "v_residual", "page_indptr",
@@ -121,6 +127,12 @@ def load():
         "dattn_debug_gather": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP,
                                      ctypes.c_size_t, ctypes.c_int32, ctypes.c_int32, _VP, ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_int32), _VP]),
+        "dattn_step_host_sizes": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(HostStep),
+                                        ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]),
+        "dattn_step_host": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(HostStep), ctypes.POINTER(Tensors),
+                                  _VP, ctypes.c_size_t, _VP, ctypes.c_size_t, _VP]),
+        "dattn_step_host_status": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(HostStep), _VP,
+                                         ctypes.POINTER(ctypes.c_int32), _VP]),
         "dattn_last_error": (ctypes.c_char_p, []),
         "dattn_version": (ctypes.c_int32, []),
     }
@@ -358,3 +370,46 @@ def decode(problem, plan: Plan, workspace, *, q, o, lse=None, stream=None, **cac
 
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+# ---- one step from host memory -------------------------------------------------------------
+
+def host_step(q, kv_len, o, *, page_indptr=None, page_indices=None, lse=None, num_sms=None) -> HostStep:
+    """dattn_host_step from host arrays (torch CPU tensors, pinned for asynchronous copies,
+    or numpy arrays).  The struct keeps references to the arrays it points to."""
+    if num_sms is None:
+        import torch
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    keep = [q, _i32_host(kv_len), _i32_host(page_indptr), _i32_host(page_indices), o, lse]
+    io = HostStep(_ptr(keep[0]), _ptr(keep[1]), _ptr(keep[2]), _ptr(keep[3]), _ptr(keep[4]), _ptr(keep[5]),
+                  int(num_sms))
+    io._keep = keep
+    return io
+
+
+def dattn_step_host_sizes(problem, io: HostStep):
+    """(workspace bytes, staging bytes) that dattn_step_host needs for this call."""
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    ws, sg = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().dattn_step_host_sizes(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(ws), ctypes.byref(sg)),
+           "dattn_step_host_sizes")
+    return ws.value, sg.value
+
+
+def dattn_step_host(problem, io: HostStep, cache: Tensors, staging, workspace, stream=None) -> None:
+    """One decode step from host memory: returns with O (and LSE) in the host arrays of io.
+    ``staging`` is a pinned host uint8 tensor, ``workspace`` a device uint8 tensor."""
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    _check(load().dattn_step_host(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache), staging.data_ptr(),
+                                  staging.numel(), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)),
+           "dattn_step_host")
+
+
+def dattn_step_host_status(problem, io: HostStep, workspace, stream=None) -> int:
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    flags = ctypes.c_int32()
+    st = load().dattn_step_host_status(ctypes.byref(prob), ctypes.byref(io), workspace.data_ptr(),
+                                       ctypes.byref(flags), _stream_ptr(stream))
+    if st not in (0, 6):
+        _check(st, "dattn_step_host_status")
+    return flags.value

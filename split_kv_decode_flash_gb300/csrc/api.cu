@@ -361,3 +361,167 @@ extern "C" dattn_status dattn_debug_gather(const dattn_plan_t* plan, const dattn
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? DATTN_OK : cuda_fail("dattn_debug_gather", err);
 }
+
+// ---- one step from host memory ---------------------------------------------------------
+
+namespace {
+
+struct StepLayout {
+  size_t q_bytes, pi_bytes, px_bytes, o_bytes, lse_bytes;
+  size_t pi_off, px_off, plan_off;      // device and staging (inputs, then the work list)
+  size_t o_off, lse_off, ws_total;      // device
+  size_t o_off_s, staging_total;        // staging: outputs after the work list
+};
+
+size_t align_ws(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+StepLayout step_layout(const dattn_problem& p, long long n_pidx, size_t plan_ws, size_t blob_bytes) {
+  StepLayout L{};
+  const bool paged = p.layout == DATTN_KV_PAGED_HND;
+  const size_t rows = static_cast<size_t>(p.B) * p.S_q * p.H_q;
+  L.q_bytes = rows * p.d_h * 2;
+  L.pi_bytes = paged ? static_cast<size_t>(p.B + 1) * 4 : 0;
+  L.px_bytes = paged ? static_cast<size_t>(n_pidx) * 4 : 0;
+  L.o_bytes = rows * p.d_h * 2;
+  L.lse_bytes = rows * 4;
+  L.pi_off = align_ws(L.q_bytes);
+  L.px_off = L.pi_off + align_ws(L.pi_bytes);
+  L.plan_off = L.px_off + align_ws(L.px_bytes);
+  L.o_off = L.plan_off + align_ws(plan_ws);
+  L.lse_off = L.o_off + align_ws(L.o_bytes);
+  L.ws_total = L.lse_off + align_ws(L.lse_bytes);
+  L.o_off_s = L.plan_off + align_ws(blob_bytes);
+  L.staging_total = L.o_off_s + align_ws(L.o_bytes) + align_ws(L.lse_bytes);
+  return L;
+}
+
+dattn_status check_step(const dattn_problem* prob, const dattn_host_step* io, bool need_io_arrays,
+                        const char* where) {
+  Checker c;
+  check_problem(prob, c);
+  if (!io) c.fail(DATTN_EINVAL, "io is NULL");
+  if (c.status != DATTN_OK) return c.finish(where);
+  if (prob->mask != DATTN_MASK_CAUSAL && prob->mask != DATTN_MASK_SINK_WINDOW)
+    c.fail(DATTN_EUNSUPPORTED, "index-list and flashmask programs read device lists: use dattn_run");
+  if (!io->kv_len) c.fail(DATTN_EINVAL, "kv_len is required");
+  if (io->num_sms < 1) c.fail(DATTN_EINVAL, "num_sms must be >= 1");
+  if (prob->layout == DATTN_KV_PAGED_HND && (!io->page_indptr || !io->page_indices))
+    c.fail(DATTN_EINVAL, "paged layout needs host page_indptr and page_indices");
+  if (need_io_arrays && (!io->q || !io->o)) c.fail(DATTN_EINVAL, "host q and o are required");
+  return c.finish(where);
+}
+
+// Plans the step; on success *plan is owned by the caller.
+dattn_status plan_step(const dattn_problem* prob, const dattn_host_step* io, dattn_plan_t** plan, size_t* plan_ws) {
+  dattn_plan_inputs in{};
+  in.kv_len = io->kv_len;
+  in.page_indptr = prob->layout == DATTN_KV_PAGED_HND ? io->page_indptr : nullptr;
+  in.num_sms = io->num_sms;
+  return dattn_plan(prob, &in, plan, plan_ws);
+}
+
+long long page_entries(const dattn_problem* prob, const dattn_host_step* io) {
+  return prob->layout == DATTN_KV_PAGED_HND ? io->page_indptr[prob->B] : 0;
+}
+
+}  // namespace
+
+extern "C" dattn_status dattn_step_host_sizes(const dattn_problem* prob, const dattn_host_step* io,
+                                              size_t* workspace_bytes, size_t* staging_bytes) {
+  dattn_status st = check_step(prob, io, false, "dattn_step_host_sizes");
+  if (st != DATTN_OK) return st;
+  if (!workspace_bytes || !staging_bytes) {
+    set_error("dattn_step_host_sizes: NULL output");
+    return DATTN_EINVAL;
+  }
+  dattn_plan_t* plan = nullptr;
+  size_t plan_ws = 0;
+  if ((st = plan_step(prob, io, &plan, &plan_ws)) != DATTN_OK) return st;
+  const StepLayout L = step_layout(*prob, page_entries(prob, io), plan_ws, plan->blob.size());
+  dattn_plan_destroy(plan);
+  *workspace_bytes = L.ws_total;
+  *staging_bytes = L.staging_total;
+  return DATTN_OK;
+}
+
+extern "C" dattn_status dattn_step_host(const dattn_problem* prob, const dattn_host_step* io,
+                                        const dattn_tensors* cache, void* staging, size_t staging_bytes,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  const char* where = "dattn_step_host";
+  dattn_status st = check_step(prob, io, true, where);
+  if (st != DATTN_OK) return st;
+  if (!cache || !staging) {
+    set_error("dattn_step_host: cache and staging are required");
+    return DATTN_EINVAL;
+  }
+  // The input region (q, page table) does not depend on the plan: its transfer
+  // is issued first and runs while the host plans.  Only the workspace's input
+  // region is written before the plan's checks.
+  const StepLayout L0 = step_layout(*prob, page_entries(prob, io), 0, 0);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) || workspace_bytes < L0.plan_off ||
+      (reinterpret_cast<uintptr_t>(staging) % 16) || staging_bytes < L0.plan_off) {
+    set_error("dattn_step_host: workspace (256-byte aligned) and staging (16-byte aligned) must hold at least " +
+              std::to_string(L0.plan_off) + " bytes; dattn_step_host_sizes gives the full sizes");
+    return DATTN_EWORKSPACE;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* sg = static_cast<uint8_t*>(staging);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::memcpy(sg, io->q, L0.q_bytes);
+  if (L0.pi_bytes) std::memcpy(sg + L0.pi_off, io->page_indptr, L0.pi_bytes);
+  if (L0.px_bytes) std::memcpy(sg + L0.px_off, io->page_indices, L0.px_bytes);
+  cudaError_t err = cudaMemcpyAsync(ws, sg, L0.plan_off, cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return cuda_fail("dattn_step_host input transfer", err);
+
+  dattn_plan_t* plan = nullptr;
+  size_t plan_ws = 0;
+  if ((st = plan_step(prob, io, &plan, &plan_ws)) != DATTN_OK) return st;
+  const StepLayout L = step_layout(*prob, page_entries(prob, io), plan_ws, plan->blob.size());
+  if (workspace_bytes < L.ws_total || staging_bytes < L.staging_total) {
+    set_error("dattn_step_host: workspace needs " + std::to_string(L.ws_total) + " bytes and staging " +
+              std::to_string(L.staging_total) + " bytes");
+    dattn_plan_destroy(plan);
+    return DATTN_EWORKSPACE;
+  }
+  // the cache pointers from "cache"; the step's inputs and outputs in the workspace
+  dattn_tensors t = *cache;
+  t.q = ws;
+  t.o = ws + L.o_off;
+  t.lse = reinterpret_cast<float*>(ws + L.lse_off);
+  if (prob->layout == DATTN_KV_PAGED_HND) {
+    t.page_indptr = reinterpret_cast<const int32_t*>(ws + L.pi_off);
+    t.page_indices = reinterpret_cast<const int32_t*>(ws + L.px_off);
+  }
+  if ((st = check_run_args(plan, prob, &t, ws + L.plan_off, plan_ws, true, where)) != DATTN_OK) {
+    dattn_plan_destroy(plan);
+    return st;
+  }
+  // the work list (the staging copy of the inputs may still be in flight: it is
+  // not touched again before the stream is synchronised)
+  std::memcpy(sg + L.plan_off, plan->blob.data(), plan->blob.size());
+  err = cudaMemcpyAsync(ws + L.plan_off, sg + L.plan_off, plan->blob.size(), cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) {
+    dattn_plan_destroy(plan);
+    return cuda_fail("dattn_step_host work-list transfer", err);
+  }
+  dattn_run_options opt{};
+  opt.flags = DATTN_RUN_REUSE_UPLOAD;
+  st = run_impl(plan, prob, &t, ws + L.plan_off, plan_ws, stream, &opt, where);
+  dattn_plan_destroy(plan);
+  if (st != DATTN_OK) return st;
+  // outputs: one device->host transfer, then into the caller's arrays
+  err = cudaMemcpyAsync(sg + L.o_off_s, ws + L.o_off, align_ws(L.o_bytes) + L.lse_bytes, cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return cuda_fail("dattn_step_host output transfer", err);
+  std::memcpy(io->o, sg + L.o_off_s, L.o_bytes);
+  if (io->lse) std::memcpy(io->lse, sg + L.o_off_s + align_ws(L.o_bytes), L.lse_bytes);
+  return DATTN_OK;
+}
+
+extern "C" dattn_status dattn_step_host_status(const dattn_problem* prob, const dattn_host_step* io,
+                                               const void* workspace, int32_t* flags, void* stream) {
+  dattn_status st = check_step(prob, io, false, "dattn_step_host_status");
+  if (st != DATTN_OK) return st;
+  const StepLayout L = step_layout(*prob, page_entries(prob, io), 0, 0);
+  return dattn_device_status(static_cast<const uint8_t*>(workspace) + L.plan_off, flags, stream);
+}

@@ -30,6 +30,7 @@
 // its own fp32 partial state (or O / LSE when it is the group's only state).
 #include <cuda_runtime.h>
 
+#include "launch.cuh"
 #include "stream.cuh"
 
 namespace dattn {
@@ -767,15 +768,9 @@ __global__ void __launch_bounds__(kThreads, 1) partial_kernel(const __grid_const
 template <int D, int FMT>
 int launch_one(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Cfg<D, FMT>::kTotal;
-  // The consumers' setmaxnreg.inc waits for registers released by the producer
-  // warpgroup; it can only complete if the launch holds enough of them.
-  cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, partial_kernel<D, FMT>);
-  if (err != cudaSuccess) return err;
-  if (attr.numRegs * kThreads < 128 * kProducerRegs + 32 * kConsumerWarps * kConsumerRegs)
-    return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(partial_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+  // the register budget check and the shared-memory opt-in, once per device
+  static std::atomic<unsigned long long> ready{0};
+  cudaError_t err = prepare_kernel_once(partial_kernel<D, FMT>, smem, 128 * kProducerRegs + 32 * kConsumerWarps * kConsumerRegs, ready);
   if (err != cudaSuccess) return err;
   partial_kernel<D, FMT><<<n_ctas, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError();

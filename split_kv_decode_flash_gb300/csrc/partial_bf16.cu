@@ -32,6 +32,7 @@
 // O / LSE when it is the group's only state.
 #include <cuda_runtime.h>
 
+#include "launch.cuh"
 #include "merge.cuh"
 #include "tc_common.cuh"
 
@@ -534,15 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
 template <int D>
 int launch_bf16(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Bf<D>::kTotal;
-  // The consumers' setmaxnreg.inc waits for registers released by the producer
-  // warpgroup; it can only complete if the launch holds enough of them.
-  cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, partial_bf16_kernel<D>);
-  if (err != cudaSuccess) return err;
-  if (attr.numRegs * kThreads < 128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs)
-    return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(partial_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+  // the register budget check and the shared-memory opt-in, once per device
+  static std::atomic<unsigned long long> ready{0};
+  cudaError_t err = prepare_kernel_once(partial_bf16_kernel<D>, smem, 128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs, ready);
   if (err != cudaSuccess) return err;
   // programmatic launch: the prologue overlaps the tail of the preceding kernel
   cudaLaunchConfig_t cfg = {};

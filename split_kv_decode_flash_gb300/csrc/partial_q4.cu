@@ -38,6 +38,7 @@
 //   probabilities times 2^-24, so they share the accumulators' units.
 #include <cuda_runtime.h>
 
+#include "launch.cuh"
 #include "tc_common.cuh"
 
 namespace dattn {
@@ -968,14 +969,9 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4_kernel(const __grid_co
 
 int launch_partial_q4(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Q4::kTotal;
-  cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, partial_q4_kernel);
-  if (err != cudaSuccess) return err;
-  // the consumers' setmaxnreg.inc waits for registers the producer warpgroup
-  // releases; it can only complete if the launch holds them
-  if (attr.numRegs * kThreads < 128 * kQ4ProducerRegs + 32 * kConsumerWarps * kQ4ConsumerRegs)
-    return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(partial_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  // the register budget check and the shared-memory opt-in, once per device
+  static std::atomic<unsigned long long> ready{0};
+  cudaError_t err = prepare_kernel_once(partial_q4_kernel, smem, 128 * kQ4ProducerRegs + 32 * kConsumerWarps * kQ4ConsumerRegs, ready);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);

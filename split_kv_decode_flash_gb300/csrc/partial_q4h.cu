@@ -31,6 +31,7 @@
 // cells, row maxima over the 8 lanes that share a query-row pair).
 #include <cuda_runtime.h>
 
+#include "launch.cuh"
 #include "tc_common.cuh"
 
 namespace dattn {
@@ -503,14 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4h_kernel(const __grid_c
 template <int D>
 int launch_q4h(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Q4H<D>::kTotal;
-  cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, partial_q4h_kernel<D>);
-  if (err != cudaSuccess) return err;
-  // the consumers' setmaxnreg.inc waits for registers the producer warpgroup
-  // releases; it can only complete if the launch holds them
-  if (attr.numRegs * kThreads < 128 * kHProducerRegs + 32 * kConsumerWarps * kHConsumerRegs)
-    return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(partial_q4h_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  // the register budget check and the shared-memory opt-in, once per device
+  static std::atomic<unsigned long long> ready{0};
+  cudaError_t err = prepare_kernel_once(partial_q4h_kernel<D>, smem, 128 * kHProducerRegs + 32 * kConsumerWarps * kHConsumerRegs, ready);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);

@@ -33,6 +33,7 @@
 // for masked cells, row maxima over the lane quad).
 #include <cuda_runtime.h>
 
+#include "launch.cuh"
 #include "tc_common.cuh"
 
 namespace dattn {
@@ -763,14 +764,9 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_co
 template <int D, int FMT>
 int launch_q8(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Q8<D>::kTotal;
-  cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, partial_q8_kernel<D, FMT>);
-  if (err != cudaSuccess) return err;
-  // the consumers' setmaxnreg.inc waits for registers the producer warpgroup
-  // releases; it can only complete if the launch holds them
-  if (attr.numRegs * kThreads < 128 * kQ8ProducerRegs + 32 * kConsumerWarps * kQ8ConsumerRegs)
-    return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(partial_q8_kernel<D, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  // the register budget check and the shared-memory opt-in, once per device
+  static std::atomic<unsigned long long> ready{0};
+  cudaError_t err = prepare_kernel_once(partial_q8_kernel<D, FMT>, smem, 128 * kQ8ProducerRegs + 32 * kConsumerWarps * kQ8ConsumerRegs, ready);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);

@@ -439,3 +439,73 @@ def test_mixed_batch_flashmask_trees_of_different_sizes():
     O, L, info, flags = H.run_gpu(w, chunk_tokens=64, num_sms=5)
     assert flags == 0
     H.compare(O, L, w)
+
+
+def _step_host(w, mask_args=None, num_sms=152):
+    """One dattn_step_host over workload w (host q and page table in, host O and LSE out)."""
+    p = dict(w.problem, **(mask_args or {}))
+    B, S_q, H_q, d = p["B"], p["S_q"], p["H_q"], p["d"]
+    q_host = w.q.cpu().pin_memory()
+    o_host = torch.full((B, S_q, H_q, d), float("nan"), dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.full((B, S_q, H_q), float("nan"), dtype=torch.float32).pin_memory()
+    paged = p["layout"] == "paged"
+    io = dattn.host_step(q_host, w.kv_len, o_host, lse=lse_host, num_sms=num_sms,
+                         page_indptr=w.page_indptr if paged else None, page_indices=w.page_indices if paged else None)
+    ws_bytes, sg_bytes = dattn.dattn_step_host_sizes(p, io)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    staging = torch.empty(sg_bytes, dtype=torch.uint8).pin_memory()
+    cache = dattn.tensors_from(k=w.k, v=w.v, cache_batch_idx=None if w.cache_batch_idx is None else
+                               w.cache_batch_idx.cuda())
+    dattn.dattn_step_host(p, io, cache, staging, ws)
+    assert dattn.dattn_step_host_status(p, io, ws) == 0
+    return p, o_host.float(), lse_host
+
+
+@pytest.mark.parametrize("case", ["paged", "contig", "sink_window_verify"])
+def test_step_host_matches_oracle_and_dattn_run(case):
+    """The host-memory step gives the oracle's result, and the same bits as dattn_run on
+    device copies of the same inputs (same plan, same kernels)."""
+    if case == "contig":
+        w = W.tiny_contiguous("cuda")
+        mask_args = None
+    else:
+        w = W.paged_ragged_gqa("cuda", B=6, lo=1, hi=900, pool_pages=500)
+        mask_args = None
+        if case == "sink_window_verify":
+            w = W.paged_bf16("swv", B=4, S_q=3, H_q=8, H_kv=2, d=128, lens=[700, 3, 64, 1],
+                             P=16, seed=9, device="cuda", pool_pages=80)
+            mask_args = dict(mask="sink_window", n_sink=5, window=100)
+    p, O, L = _step_host(w, mask_args)
+    w.problem = p
+    H.compare(O, L, w)
+    O2, L2, info, flags = H.run_gpu(w, num_sms=152)
+    assert flags == 0
+    assert torch.equal(O, O2) and torch.equal(L, L2)
+
+
+def test_step_host_full_size_sampled_and_repeated():
+    """The benchmark's workload through the host-memory step, twice in a row on one workspace."""
+    w = W.paged_ragged_gqa("cuda")
+    for _ in range(2):
+        p, O, L = _step_host(w)
+        H.finite_or_masked(O, L)
+        H.compare(O, L, w, H.sample_rows(p, 48, seed=4))
+
+
+def test_step_host_rejects_short_buffers_after_planning():
+    """A workspace or staging buffer that holds the inputs but not the plan and outputs is
+    rejected after planning, before any kernel: the outputs stay untouched."""
+    w = W.paged_ragged_gqa("cuda", B=3, lo=1, hi=300, pool_pages=64)
+    p = w.problem
+    q_host = w.q.cpu().pin_memory()
+    o_host = torch.full((3, 1, 32, 128), 7.0, dtype=torch.bfloat16)
+    io = dattn.host_step(q_host, w.kv_len, o_host, page_indptr=w.page_indptr, page_indices=w.page_indices)
+    ws_bytes, sg_bytes = dattn.dattn_step_host_sizes(p, io)
+    cache = dattn.tensors_from(k=w.k, v=w.v)
+    for ws_n, sg_n in ((ws_bytes - 256, sg_bytes), (ws_bytes, sg_bytes - 256)):
+        ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
+        staging = torch.empty(sg_n, dtype=torch.uint8).pin_memory()
+        with pytest.raises(dattn.DattnError, match="DATTN_EWORKSPACE"):
+            dattn.dattn_step_host(p, io, cache, staging, ws)
+    torch.cuda.synchronize()
+    assert bool((o_host.float() == 7.0).all())

@@ -299,3 +299,37 @@ def test_mixed_batch_validation():
     # a uniform qo_indptr is the plain batch, for every format
     dattn.dattn_plan(q8, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
                      qo_indptr=np.array([0, 4, 8, 12], np.int32), num_sms=4)
+
+
+def test_step_host_sizes_and_rejections_without_a_gpu():
+    """dattn_step_host: the sizes query plans on the host; a workspace without room for the
+    inputs, an index-list program and missing host arrays are rejected before any transfer."""
+    rng = np.random.default_rng(3)
+    T = rng.integers(1, 300, 3).tolist()
+    pages = [-(-t // 16) for t in T]
+    indptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    indices = rng.permutation(64)[:indptr[-1]].astype(np.int32)
+    p = _problem(B=3, S_q=2, H_q=8, H_kv=2, num_pages=64)
+    q = np.zeros((3, 2, 8, 128), np.uint16)
+    o = np.zeros_like(q)
+    io = dattn.host_step(q, T, o, page_indptr=indptr, page_indices=indices, num_sms=8)
+    ws, sg = dattn.dattn_step_host_sizes(p, io)
+    plan = dattn.dattn_plan(p, T, page_indptr=indptr, num_sms=8)
+    rows = 3 * 2 * 8
+    al = lambda x: -(-x // 256) * 256
+    in_bytes = al(rows * 128 * 2) + al(4 * 4) + al(4 * int(indptr[-1]))
+    assert ws == in_bytes + al(plan.workspace_bytes) + al(rows * 128 * 2) + al(rows * 4)
+    assert sg == in_bytes + al(plan.info["blob_bytes"]) + al(rows * 128 * 2) + al(rows * 4)
+    lib = dattn.load()
+    prob = dattn.make_problem(p)
+    cache = dattn.Tensors()
+    fake = 1 << 20          # never dereferenced: a workspace without room for the inputs fails first
+    st = lib.dattn_step_host(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache), fake, sg, fake * 4,
+                             in_bytes - 256, None)
+    assert st == 3 and "workspace" in dattn.dattn_last_error()
+    bad = dattn.make_problem(dict(p, mask="index_list"))
+    assert lib.dattn_step_host_sizes(ctypes.byref(bad), ctypes.byref(io), ctypes.byref(ctypes.c_size_t()),
+                                     ctypes.byref(ctypes.c_size_t())) == 2
+    io2 = dattn.host_step(q, T, o, num_sms=8)       # paged without host page tables
+    assert lib.dattn_step_host_sizes(ctypes.byref(prob), ctypes.byref(io2), ctypes.byref(ctypes.c_size_t()),
+                                     ctypes.byref(ctypes.c_size_t())) == 1
