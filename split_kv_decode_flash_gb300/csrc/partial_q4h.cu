@@ -167,82 +167,6 @@ __device__ void produce_q4h(const Walk& w, uint8_t* smem, int lane, int pw, bool
   asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
 }
 
-// Page-run producer (interval visibility programs on a paged cache whose P is
-// a power of two, at least 16).  A stage's positions are at most two runs of
-// consecutive keys, so instead of describing 256 keys one by one (key, page
-// id, row per slot) the producer loads one page id per lane (the pages the
-// runs touch, at most 20) a stage ahead and derives each slot's key and row
-// from its position and a shuffle of its page's id.
-struct RunStage {
-  int ii;              // item of the stage (w.end: none)
-  int p0, n1, q0, n2;  // slots [0, n1) hold keys p0 + s; slots [n1, n1 + n2) keys q0 + s - n1
-  int b1, np1, b2;     // first logical block of each run; run 1's pages are lanes [0, np1)
-  bool full;
-};
-
-__device__ __forceinline__ RunStage run_stage(const Walk& w, const PCur& c) {
-  RunStage r{};
-  r.ii = c.ii;
-  if (c.ii >= w.end) return r;
-  const ItemRec rec = w.rec(c.ii);
-  Run a, b;
-  const int n = item_runs(rec.it, c.j0, c.j1, a, b);
-  const int ps = w.p.P_shift;
-  r.p0 = a.p0;
-  r.n1 = n > 0 ? a.p1 - a.p0 : 0;
-  r.q0 = b.p0;
-  r.n2 = n > 1 ? b.p1 - b.p0 : 0;
-  r.b1 = r.p0 >> ps;
-  r.np1 = r.n1 ? ((r.p0 + r.n1 - 1) >> ps) - r.b1 + 1 : 0;
-  r.b2 = r.q0 >> ps;
-  r.full = stage_is_full(w.p, rec.it, rec.nq, c.j0, c.j1, -1, -1);
-  return r;
-}
-
-// The lane's page id for stage r (-1: the lane holds none; -2: invalid, reported).
-__device__ __forceinline__ int run_stage_page(const Walk& w, const RunStage& r, int lane) {
-  if (r.ii >= w.end) return -1;
-  const PartialParams& p = w.p;
-  const ItemRec rec = w.rec(r.ii);
-  const int np2 = r.n2 ? ((r.q0 + r.n2 - 1) >> p.P_shift) - r.b2 + 1 : 0;
-  int blk;
-  if (lane < r.np1) blk = r.b1 + lane;
-  else if (lane < r.np1 + np2) blk = r.b2 + (lane - r.np1);
-  else return -1;
-  if (blk >= rec.hi - rec.lo) {
-    atomicOr(p.status, kStBlockRange);
-    return -2;
-  }
-  const int pid = ld_keep(p.page_indices + rec.lo + blk, w.keep);
-  if (pid < 0 || pid >= p.num_pages) {
-    atomicOr(p.status, kStPageRange);
-    return -2;
-  }
-  return pid;
-}
-
-// Key (-1: none) and K/V row (kNoRow: none) of slot s of stage r; every lane
-// of the warp calls it (the page id comes by shuffle from its lane).
-__device__ __forceinline__ void run_slot(const PartialParams& p, const RunStage& r, int T, int h, int pid_lane,
-                                         int s, int& t, uint32_t& row) {
-  int pl = 0;
-  t = -1;
-  if (s < r.n1) {
-    t = r.p0 + s;
-    pl = (t >> p.P_shift) - r.b1;
-  } else if (s < r.n1 + r.n2) {
-    t = r.q0 + (s - r.n1);
-    pl = r.np1 + (t >> p.P_shift) - r.b2;
-  }
-  const int pid = __shfl_sync(kAll, pid_lane, pl & 31);
-  if (t < 0 || t >= T || pid < 0) {
-    t = -1;
-    row = kNoRow;
-    return;
-  }
-  row = (static_cast<uint32_t>(pid) * p.H_kv + h) * p.P + (t & (p.P - 1));
-}
-
 template <int D>
 __device__ void produce_q4h_runs(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
   using C = Q4H<D>;
@@ -647,9 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4h_kernel(const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kHProducerRegs));
-    const bool runs = p.layout == DATTN_KV_PAGED_HND && p.P_shift >= 4 &&
-                      (p.mask == DATTN_MASK_CAUSAL || p.mask == DATTN_MASK_SINK_WINDOW);
-    if (runs) produce_q4h_runs<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    if (runs_apply<kHK>(p)) produce_q4h_runs<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     else produce_q4h<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
