@@ -143,6 +143,76 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
 }
 
+// The same producer for interval programs on power-of-two pages (not
+// FlashMask): one page id per lane and stage instead of a key, a page-table
+// load and a row per slot (RunStage in tc_common.cuh).
+template <int D>
+__device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
+  using C = Bf<D>;
+  const PartialParams& p = w.p;
+  constexpr int kSlotsPerPass = 32 / C::kChunks;   // key rows per warp instruction
+  const uint32_t full0 = smem_u32(smem + C::kFullBar);
+  const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbort);
+  const char* kbase = static_cast<const char*>(p.k);
+  const char* vbase = static_cast<const char*>(p.v);
+  const int sub = lane / C::kChunks, ch = lane % C::kChunks;
+  const uint64_t stream_pol = policy_evict_first();
+
+  PCur c0{w.begin, 0, 0};
+  pc_seek<kTK>(w, c0);
+  pc_advance<kTK>(w, c0, pw);
+  PCur c1 = c0;
+  pc_advance<kTK>(w, c1, kProducerWarps);
+  RunStage s0 = run_stage(w, c0);
+  RunStage s1 = run_stage(w, c1);
+  dependency_wait(dep_wait);   // the page table is a device input
+  int pid0 = run_stage_page(w, s0, lane);
+  int pid1 = run_stage_page(w, s1, lane);
+
+  for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
+    const int st = k % C::kStagesN;
+    const uint32_t use = k / C::kStagesN;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    const ItemRec rec = w.rec(c0.ii);
+    uint32_t rows[2];
+    int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int t;
+      run_slot(p, s0, rec.it.T, rec.it.h, pid0, lane + 32 * h, t, rows[h]);
+      pos[lane + 32 * h] = t;
+    }
+    if (lane == 0) {
+      reinterpret_cast<int*>(smem + C::kFlags)[st] = s0.full ? kFlagFull : 0;
+      reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
+    }
+    const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
+#pragma unroll
+    for (int s0i = 0; s0i < kTK; s0i += kSlotsPerPass) {
+      const int s = s0i + sub;
+      const uint32_t row = __shfl_sync(kAll, s0i < 32 ? rows[0] : rows[1], s & 31);
+      const bool ok = row != kNoRow;
+      const size_t off = static_cast<size_t>(ok ? row : 0u) * C::kRowB + ch * 16;
+      const uint32_t dst = tile_off<2 * D>(s, ch);
+      cp_async16(kt + dst, kbase + off, ok ? 16u : 0u, stream_pol);
+      cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
+    }
+    const uint32_t fb = full0 + 8 * st;
+    cp_async_mbar_arrive(fb);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
+
+    c0 = c1;
+    s0 = s1;
+    pid0 = pid1;
+    pc_advance<kTK>(w, c1, kProducerWarps);
+    s1 = run_stage(w, c1);
+    pid1 = run_stage_page(w, s1, lane);
+  }
+  asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
+}
+
 // ---- consumers --------------------------------------------------------------------------
 
 // Writes one query row of a warp's result: O / LSE when the item is its
@@ -524,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBfProducerRegs));
     if (p.mask == DATTN_MASK_FLASHMASK) produce_bf16<D, true>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    else if (runs_apply<kTK>(p)) produce_bf16_runs<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     else produce_bf16<D, false>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
