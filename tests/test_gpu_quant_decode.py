@@ -204,3 +204,24 @@ def test_int4_head_rows_masks_and_widths(S_q, H_q, H_kv, d, mask):
     assert info["rows"] == S_q * H_q // H_kv
     w2 = W.Workload(w.name, p, w.q, w.kv_len, index_indptr=w.index_indptr, index_list=w.index_list)
     H.compare(O, L, w2, H.all_rows(p), cache=_oracle_cache(w, "int4_head"))
+
+
+@pytest.mark.parametrize("fmt", ["int8", "int4_head"])
+def test_quantized_bounds_check_flags_out_of_pool_page(fmt):
+    """A page id past the pool in the run's page list is caught before any address is formed;
+    the other request still matches the oracle."""
+    lens = [300, 200]
+    w = W.quantized_history("oob", B=2, S_q=1, H_q=8, H_kv=2, d=128, lens=lens, P=16, seed=28, device="cuda",
+                            fmt=fmt, pool_pages=sum(-(-t // 16) for t in lens) + 1)
+    p, cache = append_history(w, fmt, [[] for _ in lens])
+    bad = cache["page_indices"].clone()
+    bad[3] = p["num_pages"]                 # request 0, logical block 3
+    cache["page_indices"] = bad
+    plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, num_sms=4)
+    o = torch.zeros((2, 1, 8, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((2, 1, 8), dtype=torch.float32, device="cuda")
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    dattn.dattn_run(plan, p, dattn.tensors_from(q=w.q.cuda(), o=o, lse=lse, **cache), ws)
+    torch.cuda.synchronize()
+    assert dattn.dattn_device_status(ws) & 1            # kStPageRange
+    _compare(o.float().cpu(), lse.cpu(), w, p, _oracle_cache(w, fmt), [(1, 0, h) for h in range(8)])
