@@ -237,6 +237,7 @@ dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const
     m.g = k.g;
     m.S_q = k.S_q;
     m.H_q = k.H_q;
+    m.mean_states = plan->info.n_slots / plan->info.n_merge_groups;
     const int err = launch_merge(m, prob->d_h, stream);
     if (err != cudaSuccess) return cuda_fail("dattn_run merge kernel", err);
   }

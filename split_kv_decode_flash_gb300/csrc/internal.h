@@ -135,6 +135,7 @@ struct MergeParams {
   float* lse;
   int32_t* status;
   int32_t n_groups, rows, g, S_q, H_q;
+  int32_t mean_states;   // partial states per merge group, on average (chooses the warps per row)
 };
 
 // Kernel launchers (partial*.cu, merge.cu); return cudaError_t as int.

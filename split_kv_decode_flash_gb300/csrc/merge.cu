@@ -8,11 +8,12 @@
 // rounded to bf16 and LSE = m + ln l, all-masked rows giving O = 0 and
 // LSE = -inf.
 //
-// One block of four warps per (group, query row).  Warp w takes states
-// w, w + 4, ...: its lanes fetch (m, l) of up to 32 states at once, the warp
-// agrees on the frame, and the u vectors of all of them are then read with
-// every load in flight (each lane owns d / 32 channels).  The four warps'
-// folds combine in shared memory.  The kernel is launched as a programmatic
+// Groups of fewer than 8 rows: one block of four warps per (group, query
+// row); warp w takes states w, w + 4, ..., and the four warps' folds combine
+// in shared memory.  Groups of 8 rows or more: one warp per (group, row).  A
+// warp's lanes fetch (m, l) of up to 32 states at once, the warp agrees on
+// the frame, and the u vectors are then read with the loads in flight (each
+// lane owns d / 32 channels).  The kernel is launched as a programmatic
 // dependent of the partial kernel: it is resident before the partial kernel
 // ends and waits (griddepcontrol.wait) for its states to be complete.
 #include <cuda_runtime.h>
@@ -25,55 +26,79 @@ namespace {
 
 constexpr int kMergeWarps = 4;
 
-template <int D>
+// WPR = 4: one block of four warps per (group, row); warp w folds states w,
+// w + 4, ... and the four folds combine in shared memory (few rows, many
+// states).  WPR = 1: one warp per (group, row), four rows per block, each
+// warp folding all of its row's states (many rows, few states each: the
+// combine and its barrier would cost more than the fold).
+template <int D, int WPR>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_constant__ MergeParams p) {
   constexpr int C = D / 32;
-  __shared__ float sm_u[kMergeWarps][D];
-  __shared__ float sm_ml[kMergeWarps][2];
+  constexpr int kRowsPerBlock = kMergeWarps / WPR;
+  __shared__ float sm_u[WPR > 1 ? kMergeWarps : 1][D];
+  __shared__ float sm_ml[WPR > 1 ? kMergeWarps : 1][2];
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the partial kernel's states are complete
   // a programmatically launched successor may be scheduled; it waits for this grid
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gi = blockIdx.x / p.rows, row = blockIdx.x % p.rows;
+  const int blocks_per_group = (p.rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  const int gi = blockIdx.x / blocks_per_group;
+  const int row = (blockIdx.x % blocks_per_group) * kRowsPerBlock + (WPR > 1 ? 0 : w);
   const MergeGroup grp = p.groups[gi];
-  if (row >= p.g * grp.nq) return;   // the request has fewer query rows than the widest one
-
-  // warp w folds states w, w + kMergeWarps, ...
-  RowFold<D> f;
-  fold_init(f);
-  const int n_mine = grp.n > w ? (grp.n - w + kMergeWarps - 1) / kMergeWarps : 0;
-  fold_states<D>(p.ml, p.u, p.rows, row, grp.slot0 + w, n_mine, kMergeWarps, lane, f);
-  // combine the warps' folds
-#pragma unroll
-  for (int c = 0; c < C; ++c) sm_u[w][lane * C + c] = f.U[c];
-  if (lane == 0) {
-    sm_ml[w][0] = f.M;
-    sm_ml[w][1] = f.L;
-  }
-  __syncthreads();
-  if (w != 0) return;
-  RowFold<D> t;
-  fold_init(t);
-#pragma unroll
-  for (int k = 0; k < kMergeWarps; ++k) t.M = fmaxf(t.M, sm_ml[k][1] > 0.f ? sm_ml[k][0] : -INFINITY);
-  if (t.M != -INFINITY) {
-#pragma unroll
-    for (int k = 0; k < kMergeWarps; ++k) {
-      if (!(sm_ml[k][1] > 0.f)) continue;
-      const float a = exp2f(sm_ml[k][0] - t.M);
-      t.L += a * sm_ml[k][1];
-#pragma unroll
-      for (int c = 0; c < C; ++c) t.U[c] = fmaf(a, sm_u[k][lane * C + c], t.U[c]);
-    }
-  }
   const int i = row / p.g, hq = grp.h * p.g + row % p.g;
-  write_folded_row<D>(p.o, p.lse, (static_cast<long long>(grp.qo) + i) * p.H_q + hq, t, lane);
+  const long long orow = (static_cast<long long>(grp.qo) + i) * p.H_q + hq;
+  if constexpr (WPR == 1) {
+    if (row >= p.g * grp.nq) return;   // the request has fewer query rows than the widest one
+    RowFold<D> f;
+    fold_init(f);
+    fold_states<D>(p.ml, p.u, p.rows, row, grp.slot0, grp.n, 1, lane, f);
+    write_folded_row<D>(p.o, p.lse, orow, f, lane);
+    return;
+  } else {
+    if (row >= p.g * grp.nq) return;
+    // warp w folds states w, w + kMergeWarps, ...
+    RowFold<D> f;
+    fold_init(f);
+    const int n_mine = grp.n > w ? (grp.n - w + kMergeWarps - 1) / kMergeWarps : 0;
+    fold_states<D>(p.ml, p.u, p.rows, row, grp.slot0 + w, n_mine, kMergeWarps, lane, f);
+    // combine the warps' folds
+#pragma unroll
+    for (int c = 0; c < C; ++c) sm_u[w][lane * C + c] = f.U[c];
+    if (lane == 0) {
+      sm_ml[w][0] = f.M;
+      sm_ml[w][1] = f.L;
+    }
+    __syncthreads();
+    if (w != 0) return;
+    RowFold<D> t;
+    fold_init(t);
+#pragma unroll
+    for (int k = 0; k < kMergeWarps; ++k) t.M = fmaxf(t.M, sm_ml[k][1] > 0.f ? sm_ml[k][0] : -INFINITY);
+    if (t.M != -INFINITY) {
+#pragma unroll
+      for (int k = 0; k < kMergeWarps; ++k) {
+        if (!(sm_ml[k][1] > 0.f)) continue;
+        const float a = exp2f(sm_ml[k][0] - t.M);
+        t.L += a * sm_ml[k][1];
+#pragma unroll
+        for (int c = 0; c < C; ++c) t.U[c] = fmaf(a, sm_u[k][lane * C + c], t.U[c]);
+      }
+    }
+    write_folded_row<D>(p.o, p.lse, orow, t, lane);
+  }
 }
 
-template <int D>
-cudaError_t launch_d(const MergeParams& p, int blocks, void* stream) {
+// One warp merges a row alone when the groups have at least 8 rows and at
+// most 20 states on average (then the four-warp blocks, one per row, and
+// their shared-memory combine cost more than they save; with more states one
+// warp's sequential batches lengthen the merge's critical path).
+constexpr int kOneWarpRows = 8, kOneWarpStates = 20;
+
+template <int D, int WPR>
+cudaError_t launch_d(const MergeParams& p, void* stream) {
+  constexpr int kRowsPerBlock = kMergeWarps / WPR;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(blocks);
+  cfg.gridDim = dim3(p.n_groups * ((p.rows + kRowsPerBlock - 1) / kRowsPerBlock));
   cfg.blockDim = dim3(32 * kMergeWarps);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
@@ -82,15 +107,16 @@ cudaError_t launch_d(const MergeParams& p, int blocks, void* stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<D>, p);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D, WPR>, p);
 }
 
 }  // namespace
 
 int launch_merge(const MergeParams& p, int d, void* stream) {
-  const int blocks = p.n_groups * p.rows;       // one block per (group, row)
-  if (blocks == 0) return cudaSuccess;
-  const cudaError_t err = d == 64 ? launch_d<64>(p, blocks, stream) : launch_d<128>(p, blocks, stream);
+  if (p.n_groups * p.rows == 0) return cudaSuccess;
+  cudaError_t err;
+  if (p.rows >= kOneWarpRows && p.mean_states <= kOneWarpStates) err = d == 64 ? launch_d<64, 1>(p, stream) : launch_d<128, 1>(p, stream);
+  else err = d == 64 ? launch_d<64, 4>(p, stream) : launch_d<128, 4>(p, stream);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 

@@ -31,13 +31,13 @@ __device__ __forceinline__ void fold_init(RowFold<D>& f) {
 
 // Folds states s_first + s_stride * i, i in [0, n), of row "row" into f.
 // Lanes fetch (m, l) of 32 states at a time; the u vectors of the live ones
-// are then read kBatch at a time with all loads in flight.
-template <int D>
+// are then read kBatch at a time with all loads in flight (a batch is
+// unrolled: its unused slots still cost their predicated instructions).
+template <int D, int kBatch = 8>
 __device__ __forceinline__ void fold_states(const float2* ml, const float* u, int rows, int row, int s_first,
                                             int n_states, int s_stride, int lane, RowFold<D>& f) {
   constexpr unsigned kAll = 0xffffffffu;
   constexpr int C = D / 32;
-  constexpr int kBatch = 16;
   const long long stride = static_cast<long long>(s_stride) * rows * D;   // between consecutive states
   for (int i0 = 0; i0 < n_states; i0 += 32) {
     const int n = min(32, n_states - i0);
