@@ -17,6 +17,10 @@ Layouts (element order, outermost first):
                          qparams [N_pages, H_kv, P, 2] fp16 (s, z)
 * paged FP8 E4M3 / E5M2: codes [N_pages, H_kv, P, d] uint8; per-head scales
                          k_qp, v_qp [H_kv] fp32 (1 when not calibrated)
+* packed rows (bf16):    K, V [R_total, d]; the retained rows of slice s = b H_kv + h
+                         are rows row_offsets[s] .. row_offsets[s+1]-1, row r holding
+                         the source row at original position position_map[r]
+                         (M5.4 §0x04C ragged packed view: a gather, not a re-encoding)
 * paged INT4 per head:   codes [N_pages, H_kv, P, d/2] uint8 (packed);
                          qparams [N_pages, H_kv, P, 2] fp16 (s, o), one per
                          (token, kv head); x_hat = (code - o) * s
@@ -39,7 +43,7 @@ from . import address, quant
 
 @dataclass
 class Cache:
-    layout: str            # "contig" | "paged"
+    layout: str            # "contig" | "paged" | "packed"
     fmt: str               # "bf16" | "int8" | "fp8_e4m3" | "fp8_e5m2" | "int4_head" | "int4_kivi"
     H_kv: int
     d: int
@@ -77,6 +81,9 @@ def _pages_and_rows(cache: Cache, b: int, positions: np.ndarray):
 def read_rows(cache: Cache, b: int, h_kv: int, positions) -> tuple[np.ndarray, np.ndarray]:
     """Dequantised K_hat, V_hat [n, d] (float64) of request b, kv head h_kv, at ``positions``."""
     pos = np.asarray(positions, dtype=np.int64)
+    if cache.layout == "packed":
+        r = packed_rows(cache, b, h_kv, pos)
+        return quant.bf16_bits_to_f64(cache.k[r]), quant.bf16_bits_to_f64(cache.v[r])
     if cache.layout == "contig":
         c = b if cache.cache_batch_idx is None else int(cache.cache_batch_idx[b])
         if pos.size and (pos.min() < 0 or pos.max() >= cache.kv_len[b]):
@@ -131,6 +138,45 @@ def read_rows(cache: Cache, b: int, h_kv: int, positions) -> tuple[np.ndarray, n
             v[new] = quant.bf16_bits_to_f64(cache.v_res[b, slot, h_kv, :])
         return k, v
     raise ValueError(cache.fmt)
+
+
+# ---- ragged packed view (M5.4 §0x04C) -----------------------------------------
+
+def pack_view(k_slices, v_slices, position_sets):
+    """Packs the rows of each slice at its ordered position set: packed row r of slice s is
+    the source row at position_map[r] (M5.4 §0x04C).  k_slices[s] / v_slices[s] are the
+    slice's source rows [T_s, d] (any dtype, copied as is); position_sets[s] its positions.
+
+    Returns packed K [R_total, d], packed V, position_map [R_total], row_offsets [S + 1]
+    (independent global offsets: monotonic, the last one R_total)."""
+    offsets = [0]
+    pmap, ks, vs = [], [], []
+    for ksrc, vsrc, pos in zip(k_slices, v_slices, position_sets):
+        pos = np.asarray(pos, dtype=np.int64)
+        if pos.size and (np.any(np.diff(pos) <= 0) or pos[0] < 0 or pos[-1] >= len(ksrc)):
+            raise ValueError("a position set must be strictly increasing and inside its source")
+        ks.append(np.asarray(ksrc)[pos])
+        vs.append(np.asarray(vsrc)[pos])
+        pmap.append(pos)
+        offsets.append(offsets[-1] + len(pos))
+    d = np.asarray(k_slices[0]).shape[-1]
+    dt = np.asarray(k_slices[0]).dtype
+    K = np.concatenate(ks) if ks else np.zeros((0, d), dt)
+    V = np.concatenate(vs) if vs else np.zeros((0, d), dt)
+    return K, V, np.concatenate(pmap).astype(np.int64), np.asarray(offsets, np.int64)
+
+
+def packed_rows(cache: Cache, b: int, h_kv: int, positions) -> np.ndarray:
+    """Packed rows of slice (b, h_kv) holding the given original positions (each must be one
+    of the slice's retained positions; the packed row is a storage coordinate only)."""
+    s = b * cache.H_kv + h_kv
+    lo, hi = int(cache.extra["row_offsets"][s]), int(cache.extra["row_offsets"][s + 1])
+    pm = np.asarray(cache.extra["position_map"][lo:hi], dtype=np.int64)
+    pos = np.asarray(positions, dtype=np.int64)
+    idx = np.searchsorted(pm, pos)
+    if pos.size and (np.any(idx >= len(pm)) or np.any(pm[np.minimum(idx, len(pm) - 1)] != pos)):
+        raise IndexError("position not retained in the packed slice")
+    return lo + idx
 
 
 # ---- writers: the oracle's own construction of a paged cache ------------------
