@@ -37,7 +37,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "tree-verify", "mixed", "int8", "fp8",
+OTHER_WORKLOADS = ("long-s1", "long-s4", "sink-window", "index-list", "packed", "tree-verify", "mixed", "int8", "fp8",
                    "fp8-e5m2", "int4-head", "int4-kivi")
 
 
@@ -531,9 +531,12 @@ def run_other(args):
         w = {"long-s1": lambda: W.long_context(dev, 1), "long-s4": lambda: W.long_context(dev, 4),
              "sink-window": lambda: W.retention(dev, "sink_window"),
              "index-list": lambda: W.retention(dev, "index_list"),
+             "packed": lambda: W.packed_view(W.retention(dev, "index_list")),
              "tree-verify": lambda: W.tree_verify(dev), "mixed": lambda: W.mixed_batch(dev)}[name]()
         p = w.problem
-        cache = dict(k=w.k, v=w.v, page_indptr=w.page_indptr.to(dev), page_indices=w.page_indices.to(dev))
+        cache = dict(k=w.k, v=w.v)
+        if w.page_indptr is not None:
+            cache.update(page_indptr=w.page_indptr.to(dev), page_indices=w.page_indices.to(dev))
         if w.index_list is not None:
             cache.update(index_indptr=w.index_indptr.to(dev), index_list=w.index_list.to(dev))
         if w.fm_intervals is not None:

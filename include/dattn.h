@@ -48,13 +48,20 @@ typedef enum {
   DATTN_EDEVICE_CHECK = 6    /* a device-side bounds check fired (dattn_device_status)   */
 } dattn_status;
 
-/* K/V storage (M4.5 §0x04B, §0x04D).
+/* K/V storage (M4.5 §0x04B, §0x04D; M5.4 §0x04C).
  *  DATTN_KV_CONTIG_NHD: K, V bf16 [B_cache, T_cap, H_kv, d]; request b uses
  *      cache row cache_batch_idx[b] (b when the pointer is NULL).
  *  DATTN_KV_PAGED_HND:  pools [num_pages, H_kv, P, d] (format-dependent element,
  *      see dattn_format); request b's logical block j = t / P lives in page
- *      page_indices[page_indptr[b] + j] at page row t mod P (CSR page list). */
-typedef enum { DATTN_KV_CONTIG_NHD = 0, DATTN_KV_PAGED_HND = 1 } dattn_layout;
+ *      page_indices[page_indptr[b] + j] at page row t mod P (CSR page list).
+ *  DATTN_KV_PACKED_ROWS: the ragged packed view of retained rows (M5.4 §0x04C):
+ *      K, V bf16 [R_total, d].  Slice s = b * H_kv + h_kv holds rows
+ *      index_indptr[s] .. index_indptr[s+1]-1, row r being the (b, h_kv) source
+ *      row at original position index_list[r] (the position map: strictly
+ *      increasing within a slice, each < T_b).  Requires DATTN_MASK_INDEX_LIST,
+ *      whose visibility applies to the original positions; the packed row is a
+ *      storage coordinate only.  bf16 only; kv_append does not write it. */
+typedef enum { DATTN_KV_CONTIG_NHD = 0, DATTN_KV_PAGED_HND = 1, DATTN_KV_PACKED_ROWS = 2 } dattn_layout;
 
 /* K/V element formats (M8.6 §0x05B, §0x06A-B, §0x09C, §0x0A-0x0AA).  Paged layout only for
  * the quantized formats.

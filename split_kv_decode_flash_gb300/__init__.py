@@ -28,7 +28,7 @@ __all__ = [
 
 STATUS = {0: "DATTN_OK", 1: "DATTN_EINVAL", 2: "DATTN_EUNSUPPORTED", 3: "DATTN_EWORKSPACE",
           4: "DATTN_ESTALE_PLAN", 5: "DATTN_ECUDA", 6: "DATTN_EDEVICE_CHECK"}
-LAYOUTS = {"contig": 0, "paged": 1}
+LAYOUTS = {"contig": 0, "paged": 1, "packed": 2}
 FORMATS = {"bf16": 0, "int8": 1, "int4_kivi": 2, "fp8_e4m3": 3, "fp8_e5m2": 4, "int4_head": 5}
 MASKS = {"causal": 0, "sink_window": 1, "index_list": 2, "flashmask": 3}
 TILE_CLASSES = {0: "SKIP", 1: "FULL", 2: "PARTIAL"}

@@ -108,6 +108,15 @@ __global__ void translate_kernel(PartialParams p, int d, const int32_t* kv_len, 
     if (p.layout == DATTN_KV_PAGED_HND) {
       const int pi = page_of(p.page_indptr, p.page_indices, b, t / p.P, p.num_pages, nullptr);
       if (pi >= 0) off = paged_hnd_offset(pi, t % p.P, h, x, p.P, p.H_kv, d);
+    } else if (p.layout == DATTN_KV_PACKED_ROWS) {
+      // the packed row that holds original position t of slice (b, h), if retained
+      const int s = b * p.H_kv + h;
+      int lo = p.index_indptr[s], hi = p.index_indptr[s + 1];
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (p.index_list[mid] < t) lo = mid + 1; else hi = mid;
+      }
+      if (lo < p.index_indptr[s + 1] && p.index_list[lo] == t) off = static_cast<long long>(lo) * d + x;
     } else {
       const int c = cache_row(p.cache_batch_idx, b, p.B_cache, nullptr);
       if (c >= 0 && t < p.T_cap) off = contig_nhd_offset(c, t, h, x, p.T_cap, p.H_kv, d);

@@ -359,6 +359,8 @@ extern "C" dattn_status kv_append(const dattn_problem* prob, const dattn_append_
   check_problem(prob, c);
   if (!in || !in->kv_len_old || !in->new_indptr) c.fail(DATTN_EINVAL, "kv_len_old and new_indptr are required");
   if (!cache || !cache->k || !cache->v) c.fail(DATTN_EINVAL, "cache k and v are required");
+  if (prob->layout == DATTN_KV_PACKED_ROWS)
+    c.fail(DATTN_EUNSUPPORTED, "kv_append writes paged or contiguous caches, not a packed view");
   if (c.status != DATTN_OK) return c.finish("kv_append");
   const dattn_problem& p = *prob;
   const bool paged = p.layout == DATTN_KV_PAGED_HND;

@@ -55,8 +55,13 @@ void check_problem(const dattn_problem* p, Checker& c) {
   else if (p->S_q >= 1 && group_rows(*p) > kMaxRows)
     c.fail(DATTN_EUNSUPPORTED, "g * S_q query rows per kv head must be <= 32");
   if (p->d_h != 64 && p->d_h != 128) c.fail(DATTN_EUNSUPPORTED, "d_h must be 64 or 128");
-  if (p->layout != DATTN_KV_CONTIG_NHD && p->layout != DATTN_KV_PAGED_HND)
+  if (p->layout != DATTN_KV_CONTIG_NHD && p->layout != DATTN_KV_PAGED_HND && p->layout != DATTN_KV_PACKED_ROWS)
     c.fail(DATTN_EINVAL, "unknown layout");
+  if (p->layout == DATTN_KV_PACKED_ROWS) {
+    if (p->fmt != DATTN_FMT_BF16) c.fail(DATTN_EUNSUPPORTED, "the packed-row layout holds bf16 rows");
+    if (p->mask != DATTN_MASK_INDEX_LIST)
+      c.fail(DATTN_EINVAL, "the packed-row layout needs the index-list program (its position map)");
+  }
   if (p->fmt < DATTN_FMT_BF16 || p->fmt > DATTN_FMT_INT4_HEAD) c.fail(DATTN_EINVAL, "unknown format");
   if (p->mask < DATTN_MASK_CAUSAL || p->mask > DATTN_MASK_FLASHMASK) c.fail(DATTN_EINVAL, "unknown mask");
   if (p->mask == DATTN_MASK_FLASHMASK && p->fmt != DATTN_FMT_BF16)

@@ -36,7 +36,7 @@ __device__ __forceinline__ ItemRec complete_rec(const PartialParams& p, ItemRec 
       r.lo = p.page_indptr[r.it.b];
       r.hi = p.page_indptr[r.it.b + 1];
     }
-  } else {
+  } else if (p.layout == DATTN_KV_CONTIG_NHD) {
     r.crow = cache_row(p.cache_batch_idx, r.it.b, p.B_cache, report ? p.status : nullptr);
   }
   return r;
@@ -345,6 +345,9 @@ __device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& 
         if (pi == -2) atomicOr(p.status, kStBlockRange);
         else if (pi < 0 || pi >= p.num_pages) atomicOr(p.status, kStPageRange);
         else row = (static_cast<uint32_t>(pi) * p.H_kv + r.it.h) * p.P + row_of(p, t);
+      } else if (p.layout == DATTN_KV_PACKED_ROWS) {
+        // packed view: list entry x0 + j is packed row x0 + j (its position t only masks)
+        row = static_cast<uint32_t>(r.it.x0 + c.j0 + lane + 32 * h);
       } else if (r.crow >= 0 && t < p.T_cap) {
         row = (static_cast<uint32_t>(r.crow) * p.T_cap + t) * p.H_kv + r.it.h;
       } else {

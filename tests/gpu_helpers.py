@@ -28,6 +28,11 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 def oracle_cache(w) -> ocache.Cache:
     p = w.problem
+    if p["layout"] == "packed":
+        return ocache.Cache("packed", "bf16", p["H_kv"], p["d"], k=bits(w.k), v=bits(w.v),
+                            kv_len=w.kv_len.numpy().astype(np.int64),
+                            extra={"row_offsets": w.index_indptr.numpy().astype(np.int64),
+                                   "position_map": w.index_list.numpy().astype(np.int64)})
     if p["layout"] == "contig":
         c = ocache.Cache("contig", "bf16", p["H_kv"], p["d"], T_c=p["T_cap"], k=bits(w.k), v=bits(w.v),
                          kv_len=w.kv_len.numpy().astype(np.int64))

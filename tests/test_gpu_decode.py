@@ -12,6 +12,7 @@ import torch
 import split_kv_decode_flash_gb300 as dattn
 import workloads as W
 from oracle import address, masks
+from oracle import cache as ocache
 from tests import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
@@ -509,3 +510,52 @@ def test_step_host_rejects_short_buffers_after_planning():
             dattn.dattn_step_host(p, io, cache, staging, ws)
     torch.cuda.synchronize()
     assert bool((o_host.float() == 7.0).all())
+
+
+# ---- the ragged packed view of retained rows (M5.4 §0x04C) ----------------------------------
+
+@pytest.mark.parametrize("S_q,chunk,num_sms", [(1, 128, 5), (1, 0, 152), (3, 64, 7)])
+def test_packed_view_matches_oracle_and_the_index_list_gather(S_q, chunk, num_sms):
+    """Decode over the compacted rows equals decode over the paged cache with the same lists,
+    bit for bit (the same keys in the same order), and both match the oracle."""
+    w = W.retention("cuda", "index_list", B=3, T=3000)
+    if S_q > 1:
+        w.problem = dict(w.problem, S_q=S_q)
+        w.q = torch.randn((3, S_q, 32, 128), device="cuda").to(torch.bfloat16)
+    wp = W.packed_view(w)
+    O1, L1, info1, f1 = H.run_gpu(w, num_sms=num_sms, chunk_tokens=chunk)
+    O2, L2, info2, f2 = H.run_gpu(wp, num_sms=num_sms, chunk_tokens=chunk)
+    assert f1 == 0 and f2 == 0
+    assert info1["stream_keys"] == info2["stream_keys"]
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+    H.compare(O2, L2, wp)
+
+
+def test_packed_view_full_size_sampled():
+    wp = W.packed_view(W.retention("cuda", "index_list"))
+    O, L, info, flags = H.run_gpu(wp)
+    assert flags == 0 and info["stream_keys"] == 8 * 8 * 2048
+    assert wp.k.shape == (8 * 8 * 2048, 128)
+    H.finite_or_masked(O, L)
+    H.compare(O, L, wp, H.sample_rows(wp.problem, 32, seed=5))
+
+
+def test_debug_translate_packed_view_matches_oracle_rows():
+    w = W.packed_view(W.retention("cuda", "index_list", B=2, T=500))
+    p = w.problem
+    rng = np.random.default_rng(9)
+    coords = []
+    for _ in range(300):
+        coords.append((int(rng.integers(0, 2)), int(rng.integers(0, 500)), int(rng.integers(0, 32)),
+                       int(rng.integers(0, 128))))
+    c = H.oracle_cache(w)
+    want = []
+    for b, t, hq, x in coords:
+        try:
+            want.append(int(ocache.packed_rows(c, b, hq // 4, [t])[0]) * 128 + x)
+        except IndexError:
+            want.append(-1)
+    c_dev = torch.tensor(coords, dtype=torch.int32, device="cuda")
+    out = torch.empty(len(coords), dtype=torch.int64, device="cuda")
+    dattn.dattn_debug_translate(p, dattn.tensors_from(**H.device_tensors(w, None, None)), w.kv_len.cuda(), c_dev, out)
+    assert out.cpu().tolist() == want and (np.asarray(want) >= 0).sum() > 30

@@ -333,3 +333,24 @@ def test_step_host_sizes_and_rejections_without_a_gpu():
     io2 = dattn.host_step(q, T, o, num_sms=8)       # paged without host page tables
     assert lib.dattn_step_host_sizes(ctypes.byref(prob), ctypes.byref(io2), ctypes.byref(ctypes.c_size_t()),
                                      ctypes.byref(ctypes.c_size_t())) == 1
+
+
+def test_packed_view_layout_validation():
+    """The packed-row layout takes the index-list program (its position map) and bf16 rows only;
+    kv_append does not write it."""
+    base = _problem(B=2, H_q=8, H_kv=2, layout="packed", mask="index_list")
+    T = [40, 30]
+    lists = [np.arange(0, 40, 3), np.arange(1, 40, 5), np.arange(0, 30, 2), np.arange(3, 30, 7)]
+    indptr = np.concatenate([[0], np.cumsum([len(x) for x in lists])]).astype(np.int32)
+    lst = np.concatenate(lists).astype(np.int32)
+    plan = dattn.dattn_plan(base, T, index_indptr=indptr, index_list=lst, num_sms=4)
+    assert plan.info["stream_keys"] == len(lst)
+    with pytest.raises(dattn.DattnError, match="index-list program"):
+        dattn.dattn_plan(dict(base, mask="causal"), T, num_sms=4)
+    with pytest.raises(dattn.DattnError, match="bf16 rows"):
+        dattn.dattn_plan(dict(base, fmt="int8"), T, index_indptr=indptr, index_list=lst, num_sms=4)
+    lib = dattn.load()
+    prob = dattn.make_problem(base)
+    st = lib.kv_append(ctypes.byref(prob), ctypes.byref(dattn.AppendInputs()), ctypes.byref(dattn.Tensors()),
+                       None, None, None, 0, None)
+    assert st != 0 and "packed view" in dattn.dattn_last_error()

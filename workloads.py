@@ -245,6 +245,27 @@ def retention(device="cpu", program="sink_window", B=8, T=32768):
     return w
 
 
+def packed_view(w: Workload) -> Workload:
+    """The retained rows of an index-list workload compacted into the ragged packed view
+    (M5.4 §0x04C): slice b H_kv + h holds the (b, h) rows at its list positions, in list
+    order, so the list doubles as the position map.  A gather of stored rows, nothing more."""
+    p = w.problem
+    P, H = p["P"], p["H_kv"]
+    ind = w.index_indptr.long()
+    pos = w.index_list.long()
+    s = torch.repeat_interleave(torch.arange(len(ind) - 1), ind[1:] - ind[:-1])
+    b, h = s // H, s % H
+    pages = w.page_indices.long()[w.page_indptr.long()[b] + pos // P]
+    dev = w.k.device
+    idx = (pages.to(dev), h.to(dev), (pos % P).to(dev))
+    k = w.k[idx].contiguous()
+    v = w.v[idx].contiguous()
+    problem = dict(p, layout="packed")
+    problem.pop("num_pages", None)
+    return Workload(w.name + " (packed view)", problem, w.q, w.kv_len, k=k, v=v,
+                    index_indptr=w.index_indptr, index_list=w.index_list, meta=dict(w.meta))
+
+
 def quantized(device="cpu", fmt="int8", B=32, lo=2048, hi=32768):
     meta = torch.Generator().manual_seed(4)
     lens = torch.randint(lo, hi + 1, (B,), generator=meta).tolist()
