@@ -136,6 +136,37 @@ def naive_average(outs) -> np.ndarray:
 
 # ---- split bounds, §0x03B ---------------------------------------------------
 
+# ---- shared-shift partials with a range guard (M4.5 §0x09C) --------------------
+
+FALLBACK = None
+
+
+def shared_shift_partial(scores, values, allowed, phi: float, lower: float, upper: float):
+    """One partition's numerator and denominator in the common frame phi:
+    n = sum e^{s - phi} v, l = sum e^{s - phi} over the allowed keys, or FALLBACK when
+    some allowed key has s - phi <= lower or >= upper (the range guard)."""
+    s = np.asarray(scores, dtype=np.float64)
+    a = np.asarray(allowed, dtype=bool)
+    delta = s[a] - phi
+    if np.any(delta <= lower) or np.any(delta >= upper):
+        return FALLBACK
+    w = np.exp(delta)
+    return w @ np.asarray(values, dtype=np.float64)[a], float(w.sum())
+
+
+def shared_shift_attention(scores, values, allowed, bounds, phi: float, lower: float, upper: float):
+    """Partitions [a, e) of one row with a shared shift; no cross-partition rescaling.  If any
+    partition's guard fails the row is recomputed with synchronized partial softmax states
+    (summarize + merge).  Returns (O, used_fallback)."""
+    parts = [shared_shift_partial(scores[a:e], values[a:e], allowed[a:e], phi, lower, upper) for a, e in bounds]
+    if any(x is FALLBACK for x in parts):
+        st = merge_all([summarize(scores[a:e], values[a:e], allowed[a:e]) for a, e in bounds])
+        return finalize(st)[0], True
+    n = sum(x[0] for x in parts)
+    l = sum(x[1] for x in parts)
+    return (n / l if l > 0 else np.zeros(np.asarray(values).shape[-1])), False
+
+
 def balanced_split_bounds(T: int, S: int):
     """Half-open [start, end) of each of S splits of [0, T)  (§0x03B).
 

@@ -158,3 +158,42 @@ def test_fp16_order_sensitivity_and_fp64_exactness():
     # the float64 oracle returns the exact output for equal scores
     st = ss.summarize(np.zeros(n), np.array(vals, float)[:, None], np.ones(n, bool))
     assert ss.finalize(st)[0][0] == g["exact_output"]
+
+
+# ---- shared-shift partials with a range guard (M4.5 §0x09C) --------------------
+
+def test_shared_shift_gives_the_exact_softmax_for_any_frame():
+    """A common shift phi leaves the softmax ratio unchanged; partitions need no rescaling."""
+    rng = np.random.default_rng(60)
+    s = rng.normal(size=200) * 2.0
+    v = rng.normal(size=(200, 8))
+    allowed = rng.random(200) < 0.8
+    exact = np.exp(s[allowed] - s[allowed].max()) @ v[allowed] / np.exp(s[allowed] - s[allowed].max()).sum()
+    bounds = ss.balanced_split_bounds(200, 7)
+    for phi in (0.0, 2.5, s[allowed].max(), -1.0):
+        o, fell_back = ss.shared_shift_attention(s, v, allowed, bounds, phi, -40.0, 40.0)
+        assert not fell_back
+        np.testing.assert_allclose(o, exact, rtol=1e-12, atol=1e-12)
+
+
+def test_shared_shift_guard_boundaries_and_fallback():
+    s = np.array([0.0, 1.0, 2.9, -2.9])
+    v = np.eye(4)
+    allowed = np.ones(4, bool)
+    n, l = ss.shared_shift_partial(s, v, allowed, 0.0, -3.0, 3.0)
+    assert l == pytest.approx(1 + math.e + math.exp(2.9) + math.exp(-2.9))
+    # the guard is exclusive at both ends (the pages' delta <= lower / delta >= upper)
+    assert ss.shared_shift_partial(np.array([3.0]), v[:1], allowed[:1], 0.0, -3.0, 3.0) is ss.FALLBACK
+    assert ss.shared_shift_partial(np.array([-3.0]), v[:1], allowed[:1], 0.0, -3.0, 3.0) is ss.FALLBACK
+    # a masked key outside the range does not trip the guard
+    assert ss.shared_shift_partial(np.array([0.0, 9.0]), v[:2], np.array([True, False]), 0.0, -3.0, 3.0) \
+        is not ss.FALLBACK
+    # one failing partition sends the whole row to synchronized partial softmax: still exact
+    s2 = np.array([0.0, 0.5, 6.0, 1.0])
+    o, fell_back = ss.shared_shift_attention(s2, v, allowed, [(0, 2), (2, 4)], 0.0, -3.0, 3.0)
+    assert fell_back
+    w = np.exp(s2 - s2.max())
+    np.testing.assert_allclose(o, w / w.sum(), rtol=1e-12)
+    # an all-masked row has no partial to guard and gives zeros
+    o, fell_back = ss.shared_shift_attention(s2, v, np.zeros(4, bool), [(0, 4)], 0.0, -3.0, 3.0)
+    assert not fell_back and not o.any()
