@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunk", type=int, default=0, help="planner chunk width (0 = default)")
+    ap.add_argument("--shared-shift", default=None, metavar="PHI,LO,HI",
+                    help="bf16 partials in the common frame PHI with the guard LO < s - PHI < HI")
     ap.add_argument("--workload", choices=("paged",) + OTHER_WORKLOADS, default="paged",
                     help="paged: the benchmark line; the others print one timing line for a decode step "
                          "of that workload")
@@ -368,11 +370,12 @@ def run_ours(args):
     # per-kernel events are taken in a second pass of K steps right after.
     start.record(stream)
     for k in range(K):
-        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, stream=stream)
+        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, shared_shift=_shift(args), stream=stream)
     end.record(stream)
     torch.cuda.synchronize()
     for k in range(K):
-        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, events=evs[k], stream=stream)
+        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, events=evs[k], shared_shift=_shift(args),
+                           stream=stream)
     torch.cuda.synchronize()
     barrier(world)
     ck = clocks.stop()
@@ -424,6 +427,7 @@ def run_ours(args):
                    "lengths": "uniform integers in [1024, 8192], seed 1",
                    "l2": "no flush: K/V read per step (%.0f MB) is larger than the 129 MB L2" % (ab["kv"] / 1e6),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "shared_shift": _shift(args),
                    "plan": {k: info[k] for k in ("n_items", "n_ctas", "n_slots", "n_merge_groups", "max_splits",
                                                  "stream_keys", "max_cta_keys", "workspace_bytes")}},
         "kv_bytes_per_step": ab["kv"],
@@ -492,6 +496,11 @@ def _quantized_cache(dattn, w, fmt, dev):
     return p, c
 
 
+def _shift(args):
+    """(phi, lo, hi) of --shared-shift, or None."""
+    return None if args.shared_shift is None else tuple(float(x) for x in args.shared_shift.split(","))
+
+
 def _stream_bytes(p, info, lens):
     """K/V bytes of the visible streams (what the step must read)."""
     d = p["d"]
@@ -553,21 +562,23 @@ def run_other(args):
     stream = torch.cuda.current_stream()
     dattn.dattn_plan_upload(plan, ws, stream)
     for _ in range(max(3, args.warmup)):
-        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, stream=stream)
+        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, shared_shift=_shift(args), stream=stream)
     torch.cuda.synchronize()
     assert dattn.dattn_device_status(ws, stream) == 0, "device bounds check fired"
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for _ in range(args.steps):
-        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, stream=stream)
+        dattn.dattn_run_ex(plan, p, t, ws, reuse_upload=True, shared_shift=_shift(args), stream=stream)
     end.record(stream)
     torch.cuda.synchronize()
     us = start.elapsed_time(end) / args.steps * 1e3
+    fallbacks = dattn.dattn_shift_fallbacks(ws, stream) if args.shared_shift else None
     nb = _stream_bytes(p, plan.info, w.kv_len.tolist())
     peak, peak_src = measured_peak()
     print(json.dumps({"workload": w.name, "us_per_step": us, "kv_bytes_per_step": nb, "GBps": nb / us / 1e3,
                       "frac": nb / us / 1e3 / peak, "peak": peak, "peak_source": peak_src,
                       "rows": plan.info["rows"], "n_items": plan.info["n_items"], "steps": args.steps,
+                      "shared_shift": _shift(args), "shift_fallbacks": fallbacks,
                       "timing": "CUDA events around K back-to-back decode steps (partial + merge)"}), flush=True)
 
 

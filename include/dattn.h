@@ -275,11 +275,27 @@ dattn_status dattn_run(const dattn_plan_t* plan, const dattn_problem* prob,
                                       (dattn_plan_upload or an earlier run with this plan and
                                       workspace); skip the host->device copy. The caller
                                       guarantees that nothing overwrote the workspace since. */
+#define DATTN_RUN_SHARED_SHIFT 2u  /* shared-shift partials (M4.5 §0x09C, bf16 K/V only): the
+                                      partial states accumulate e^(s - phi) v and e^(s - phi)
+                                      in the common frame "shift_phi" (natural-log score
+                                      units, s = q.k * sm_scale) with no running maximum, as
+                                      long as every visible score of a consumer warp's keys
+                                      satisfies shift_lo < s - phi < shift_hi (the range
+                                      guard); a warp whose guard fails continues in the
+                                      synchronized running-max frame from that point (the
+                                      fallback), so the result is the softmax either way.
+                                      Requires -80 <= shift_lo < shift_hi <= 40 and a finite
+                                      shift_phi.  dattn_shift_fallbacks counts the fallbacks */
 typedef struct {
   uint32_t flags;     /* DATTN_RUN_* bits                                                  */
   void* events[3];    /* cudaEvent_t (as void*) recorded on "stream" before the partial
                          kernel, after it and after the merge kernel; NULL entries skipped */
+  float shift_phi, shift_lo, shift_hi;   /* DATTN_RUN_SHARED_SHIFT frame and guard      */
 } dattn_run_options;
+
+/* Number of consumer warps that left the shared-shift frame (guard failed) since the work
+ * list was last uploaded to "workspace" (synchronises "stream"). */
+dattn_status dattn_shift_fallbacks(const void* workspace, int32_t* count, void* stream);
 
 /* Copies the plan's work list into the head of "workspace" (stream-ordered).
  * A plan is typically built once per decode step and then run by every layer

@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "DattnError", "Problem", "load", "make_problem", "dattn_plan", "dattn_plan_get_info",
-    "dattn_plan_get_items", "dattn_run", "dattn_run_ex", "dattn_plan_upload", "dattn_device_status", "kv_append",
+    "dattn_plan_get_items", "dattn_run", "dattn_run_ex", "dattn_plan_upload", "dattn_device_status", "dattn_shift_fallbacks", "kv_append",
     "kv_append_workspace_bytes", "dattn_debug_translate", "dattn_debug_classify",
     "dattn_debug_gather", "dattn_last_error", "dattn_version", "tensors_from", "decode",
     "LAYOUTS", "FORMATS", "MASKS", "TILE_CLASSES", "STATUS",
@@ -80,10 +80,12 @@ class WorkItem(ctypes.Structure):
 
 
 class RunOptions(ctypes.Structure):
-    _fields_ = [("flags", ctypes.c_uint32), ("events", ctypes.c_void_p * 3)]
+    _fields_ = [("flags", ctypes.c_uint32), ("events", ctypes.c_void_p * 3),
+                ("shift_phi", ctypes.c_float), ("shift_lo", ctypes.c_float), ("shift_hi", ctypes.c_float)]
 
 
 RUN_REUSE_UPLOAD = 1
+RUN_SHARED_SHIFT = 2
 NOALLOC_SCRATCH_BYTES = 16 << 20  # DATTN_NOALLOC_SCRATCH_BYTES
 
 
@@ -117,6 +119,7 @@ def load():
         "dattn_plan_upload": (_ST, [_VP, _VP, ctypes.c_size_t, _VP]),
         "dattn_run_noalloc": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP]),
         "dattn_device_status": (_ST, [_VP, ctypes.POINTER(ctypes.c_int32), _VP]),
+        "dattn_shift_fallbacks": (_ST, [_VP, ctypes.POINTER(ctypes.c_int32), _VP]),
         "kv_append_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Problem)]),
         "kv_append": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(AppendInputs), ctypes.POINTER(Tensors),
                             _VP, _VP, _VP, ctypes.c_size_t, _VP]),
@@ -300,12 +303,16 @@ def dattn_plan_upload(plan: Plan, workspace, stream=None) -> None:
 
 
 def dattn_run_ex(plan: Plan, problem, tensors: Tensors, workspace, *, reuse_upload=False, events=None,
-                 stream=None) -> None:
+                 shared_shift=None, stream=None) -> None:
     """dattn_run with options: reuse an uploaded work list, record three torch.cuda.Events
-    (before the partial kernel, after it, after the merge kernel)."""
+    (before the partial kernel, after it, after the merge kernel), and ``shared_shift =
+    (phi, lo, hi)``: partials in the fixed frame phi, guarded by lo < s - phi < hi."""
     prob = problem if isinstance(problem, Problem) else make_problem(problem)
     opt = RunOptions()
     opt.flags = RUN_REUSE_UPLOAD if reuse_upload else 0
+    if shared_shift is not None:
+        opt.flags |= RUN_SHARED_SHIFT
+        opt.shift_phi, opt.shift_lo, opt.shift_hi = (float(x) for x in shared_shift)
     for i, e in enumerate(events or ()):
         opt.events[i] = None if e is None else e.cuda_event
     _check(load().dattn_run_ex(plan.handle, ctypes.byref(prob), ctypes.byref(tensors), workspace.data_ptr(),
@@ -319,6 +326,14 @@ def dattn_device_status(workspace, stream=None) -> int:
     if st not in (0, 6):
         _check(st, "dattn_device_status")
     return flags.value
+
+
+def dattn_shift_fallbacks(workspace, stream=None) -> int:
+    """Groups of the last shared-shift run whose scores left the guard and took the online-max path."""
+    count = ctypes.c_int32()
+    _check(load().dattn_shift_fallbacks(workspace.data_ptr(), ctypes.byref(count), _stream_ptr(stream)),
+           "dattn_shift_fallbacks")
+    return count.value
 
 
 def kv_append_workspace_bytes(problem) -> int:

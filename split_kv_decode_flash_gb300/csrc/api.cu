@@ -214,12 +214,30 @@ dattn_status record(void* const* events, int i, cudaStream_t s) {
 
 dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const dattn_tensors* t, void* workspace,
                       size_t workspace_bytes, void* stream, const dattn_run_options* opt, const char* where) {
+  const bool shift = opt && (opt->flags & DATTN_RUN_SHARED_SHIFT);
+  if (shift) {
+    Checker c;
+    if (prob && prob->fmt != DATTN_FMT_BF16) c.fail(DATTN_EUNSUPPORTED, "shared-shift partials run on bf16 K/V");
+    if (!std::isfinite(opt->shift_phi)) c.fail(DATTN_EINVAL, "shift_phi must be finite");
+    if (!(opt->shift_lo >= -80.f && opt->shift_lo < opt->shift_hi && opt->shift_hi <= 40.f))
+      c.fail(DATTN_EINVAL, "the guard needs -80 <= shift_lo < shift_hi <= 40");
+    if (c.status != DATTN_OK) return c.finish(where);
+  }
   dattn_status st = check_run_args(plan, prob, t, workspace, workspace_bytes, true, where);
   if (st != DATTN_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* const* events = opt ? opt->events : nullptr;
   PartialParams k;
   fill_common(*prob, *t, k);
+  if (shift) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    k.shift_on = 1;
+    k.shift_phi2 = opt->shift_phi * kLog2e;
+    k.shift_lo2 = opt->shift_lo * kLog2e;
+    k.shift_hi2 = opt->shift_hi * kLog2e;
+    k.shift_fallbacks = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                                   offsetof(BlobHeader, shift_fallbacks));
+  }
   if (opt && (opt->flags & DATTN_RUN_REUSE_UPLOAD)) {
     bind_blob(plan, workspace, k);
   } else {
@@ -276,6 +294,18 @@ extern "C" dattn_status dattn_plan_upload(const dattn_plan_t* plan, void* worksp
   PartialParams k;
   std::memset(&k, 0, sizeof(k));
   return upload_blob(plan, workspace, static_cast<cudaStream_t>(stream), k);
+}
+
+extern "C" dattn_status dattn_shift_fallbacks(const void* workspace, int32_t* count, void* stream) {
+  if (!workspace || !count) {
+    set_error("dattn_shift_fallbacks: NULL argument");
+    return DATTN_EINVAL;
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemcpyAsync(count, static_cast<const uint8_t*>(workspace) + offsetof(BlobHeader, shift_fallbacks),
+                                    sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  return err == cudaSuccess ? DATTN_OK : cuda_fail("dattn_shift_fallbacks", err);
 }
 
 extern "C" dattn_status dattn_device_status(const void* workspace, int32_t* flags, void* stream) {

@@ -88,10 +88,12 @@ struct BlobHeader {
   int32_t status;        // device status word, zeroed by the copy
   int32_t n_items, n_ctas, n_merge, rows, n_slots;
   int32_t fused;         // merge groups merged inside the partial kernel
+  int32_t shift_fallbacks;   // warps that left the shared-shift frame, zeroed by the upload
+  int32_t pad0;
   int64_t off_items, off_cta_indptr, off_cta_items, off_merge, off_ml, off_u, off_cta_recs;
   int64_t off_count;     // int32 [n_merge]: finished items per merge group (fused merge)
 };
-static_assert(sizeof(BlobHeader) == 96, "BlobHeader layout");
+static_assert(sizeof(BlobHeader) == 104, "BlobHeader layout");
 
 // Arguments of the partial kernel (passed by value as a grid constant).
 struct PartialParams {
@@ -125,6 +127,9 @@ struct PartialParams {
   int32_t n_sink, window, kivi_G, kivi_Gv, kivi_R;
   int32_t P_shift;       // log2(P) when P is a power of two, else -1
   float scale_log2;      // sm_scale * log2(e)
+  int32_t shift_on;       // shared-shift partials (bf16 kernel)
+  float shift_phi2, shift_lo2, shift_hi2;   // frame and guard, log2 units
+  int32_t* shift_fallbacks;
 };
 
 struct MergeParams {

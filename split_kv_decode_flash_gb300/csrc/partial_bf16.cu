@@ -284,7 +284,7 @@ struct WarpRole {
 };
 
 // One item: its stages (k counts the CTA's stages across items), then its rows.
-template <int D, int KW>
+template <int D, int KW, bool SHIFT>
 __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const ItemRec& rec,
                                              const uint32_t (&qa)[D / 16][4], int cw, int lane, uint32_t& k,
                                              bool& dead) {
@@ -311,7 +311,14 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
   float o[NT][4];
 #pragma unroll
   for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // Shared-shift partials (M4.5 §0x09C): the states live in the common frame phi
+  // (log2 units) with no running maximum while the warp's guard holds.  A failed
+  // guard moves the accumulated keys to their own maximum (tracked per lane,
+  // reduced only then) and continues with the running-max softmax, so the
+  // result is that of the synchronized states.
+  bool shared = SHIFT;
+  float m0 = shared ? p.shift_phi2 : -INFINITY, m1 = m0, l0 = 0.f, l1 = 0.f;
+  float sx0 = -INFINITY, sx1 = -INFINITY;   // this lane's largest accepted score per row
 
   for (int j0 = it.a; j0 < it.e; ++k) {
     const int j1 = min(j0 + kTK, it.e);
@@ -370,44 +377,91 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
         s[nt][2 + e] = v1 ? s[nt][2 + e] * sc : -INFINITY;
       }
     }
-    // online softmax: row maxima over the lane quad
-    float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-    float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+    if (shared) {   // the range guard of the common frame
+      bool bad = false;
 #pragma unroll
-    for (int nt = 2; nt < NTK; ++nt) {
-      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+      for (int nt = 0; nt < NTK; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float dl = s[nt][e] - p.shift_phi2;
+          bad = bad || (s[nt][e] != -INFINITY && !(dl > p.shift_lo2 && dl < p.shift_hi2));
+        }
+      if (__any_sync(kAll, bad)) {
+        shared = false;
+        if (lane == 0) atomicAdd(p.shift_fallbacks, 1);
+        sx0 = fmaxf(sx0, __shfl_xor_sync(kAll, sx0, 1));
+        sx1 = fmaxf(sx1, __shfl_xor_sync(kAll, sx1, 1));
+        sx0 = fmaxf(sx0, __shfl_xor_sync(kAll, sx0, 2));
+        sx1 = fmaxf(sx1, __shfl_xor_sync(kAll, sx1, 2));
+        // accepted scores lie in (phi + lo, phi + hi): the factor stays inside fp32
+        const float a0 = sx0 == -INFINITY ? 0.f : ex2_approx(m0 - sx0);
+        const float a1 = sx1 == -INFINITY ? 0.f : ex2_approx(m1 - sx1);
+        m0 = sx0;
+        m1 = sx1;
+        l0 *= a0;
+        l1 *= a1;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          o[n][0] *= a0;
+          o[n][1] *= a0;
+          o[n][2] *= a1;
+          o[n][3] *= a1;
+        }
+      }
     }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 2));
-    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    const float a0 = n0 == -INFINITY ? 1.f : ex2_approx(m0 - n0);
-    const float a1 = n1 == -INFINITY ? 1.f : ex2_approx(m1 - n1);
-    const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
     float (&pr)[NTK][4] = s;   // the probabilities replace the scores
-    float ps0 = 0.f, ps1 = 0.f;
+    if (shared) {   // e^(s - phi): no maximum, no rescale
+      float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NTK; ++nt) {
-      pr[nt][0] = ex2_approx(s[nt][0] - u0);
-      pr[nt][1] = ex2_approx(s[nt][1] - u0);
-      pr[nt][2] = ex2_approx(s[nt][2] - u1);
-      pr[nt][3] = ex2_approx(s[nt][3] - u1);
-      ps0 += pr[nt][0] + pr[nt][1];
-      ps1 += pr[nt][2] + pr[nt][3];
-    }
-    l0 = l0 * a0 + ps0;
-    l1 = l1 * a1 + ps1;
-    m0 = n0;
-    m1 = n1;
-    if (__any_sync(kAll, a0 != 1.f || a1 != 1.f)) {
+      for (int nt = 0; nt < NTK; ++nt) {
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        o[n][0] *= a0;
-        o[n][1] *= a0;
-        o[n][2] *= a1;
-        o[n][3] *= a1;
+        for (int e = 0; e < 4; ++e) pr[nt][e] = ex2_approx(s[nt][e] - p.shift_phi2);
+        sx0 = fmaxf(sx0, fmaxf(s[nt][0], s[nt][1]));
+        sx1 = fmaxf(sx1, fmaxf(s[nt][2], s[nt][3]));
+        ps0 += pr[nt][0] + pr[nt][1];
+        ps1 += pr[nt][2] + pr[nt][3];
+      }
+      l0 += ps0;
+      l1 += ps1;
+    } else {
+      // online softmax: row maxima over the lane quad
+      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+#pragma unroll
+      for (int nt = 2; nt < NTK; ++nt) {
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kAll, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kAll, mx1, 2));
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float a0 = n0 == -INFINITY ? 1.f : ex2_approx(m0 - n0);
+      const float a1 = n1 == -INFINITY ? 1.f : ex2_approx(m1 - n1);
+      const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NTK; ++nt) {
+        pr[nt][0] = ex2_approx(s[nt][0] - u0);
+        pr[nt][1] = ex2_approx(s[nt][1] - u0);
+        pr[nt][2] = ex2_approx(s[nt][2] - u1);
+        pr[nt][3] = ex2_approx(s[nt][3] - u1);
+        ps0 += pr[nt][0] + pr[nt][1];
+        ps1 += pr[nt][2] + pr[nt][3];
+      }
+      l0 = l0 * a0 + ps0;
+      l1 = l1 * a1 + ps1;
+      m0 = n0;
+      m1 = n1;
+      if (__any_sync(kAll, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          o[n][0] *= a0;
+          o[n][1] *= a0;
+          o[n][2] *= a1;
+          o[n][3] *= a1;
+        }
       }
     }
     // O += P V: the S fragments re-packed as the A operand (keys are the k index),
@@ -446,7 +500,8 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
 // item's query fragments loaded while the current one runs.  In a call with
 // more rows (a mixed batch's widest request, or a uniform batch of 17 to 32
 // rows) each item takes the layout of its own request's g C_b rows.
-template <int D>
+// SHIFT: shared-shift partials; the synchronized path is compiled without them.
+template <int D, bool SHIFT>
 __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, bool dep_wait) {
   dependency_wait(dep_wait);   // before Q and the state writes
   const PartialParams& p = w.p;
@@ -465,7 +520,7 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
 #pragma unroll
         for (int x = 0; x < 4; ++x) qa[kk][x] = qn[kk][x];
       if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1), role.r0, role.r1, t4, qn);
-      consume_item<D, 16>(w, smem, w.rec(ii), qa, cw, lane, k, dead);
+      consume_item<D, 16, SHIFT>(w, smem, w.rec(ii), qa, cw, lane, k, dead);
     }
   } else {
     for (int ii = w.begin; ii < w.end; ++ii) {
@@ -474,11 +529,11 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
       if (p.g * rec.nq <= 16) {
         const WarpRole<16> role(cw, lane);
         load_q<D>(p, rec, role.r0, role.r1, t4, qa);
-        consume_item<D, 16>(w, smem, rec, qa, cw, lane, k, dead);
+        consume_item<D, 16, SHIFT>(w, smem, rec, qa, cw, lane, k, dead);
       } else {
         const WarpRole<32> role(cw, lane);
         load_q<D>(p, rec, role.r0, role.r1, t4, qa);
-        consume_item<D, 32>(w, smem, rec, qa, cw, lane, k, dead);
+        consume_item<D, 32, SHIFT>(w, smem, rec, qa, cw, lane, k, dead);
       }
     }
   }
@@ -599,7 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));
-  consume_bf16<D>(w, smem, warp, lane, !complete_now);
+  if (p.shift_on) consume_bf16<D, true>(w, smem, warp, lane, !complete_now);
+  else consume_bf16<D, false>(w, smem, warp, lane, !complete_now);
   if (p.fused) fused_merge<D>(w, smem, warp, lane);
 }
 
