@@ -80,7 +80,10 @@ void fill_common(const dattn_problem& p, const dattn_tensors& t, PartialParams& 
   }
   k.num_pages = p.num_pages;
   k.T_cap = p.T_cap;
-  k.B_cache = p.B_cache;
+  // the packed-row layout has no cache rows: the kernels' row lookup (identity
+  // over the B requests) then passes and is not used
+  k.B_cache = p.layout == DATTN_KV_PACKED_ROWS ? p.B : p.B_cache;
+  if (p.layout == DATTN_KV_PACKED_ROWS) k.cache_batch_idx = nullptr;
   k.n_sink = p.n_sink;
   k.window = p.window;
   k.kivi_G = p.kivi_group;

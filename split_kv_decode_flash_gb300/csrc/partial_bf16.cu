@@ -97,7 +97,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   dependency_wait(dep_wait);
   const SlotPages<2, FM> g0 = slot_pages<2, FM>(w, c0, k0);     // both stages' page lookups in flight together
   SlotPages<2, FM> g1 = slot_pages<2, FM>(w, c1, k1);
-  SlotRows<2, FM> r0 = slot_rows<2, FM>(w, c0, k0, g0, lane);
+  SlotRows<2, FM> r0 = slot_rows<2, FM, true>(w, c0, k0, g0, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
@@ -132,7 +132,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
     if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
 
     // move the description pipeline one stage of this warp forward
-    r0 = slot_rows<2, FM>(w, c1, k1, g1, lane);
+    r0 = slot_rows<2, FM, true>(w, c1, k1, g1, lane);
     c0 = c1;
     g1 = slot_pages<2, FM>(w, c2, k2);
     k1 = k2;

@@ -36,7 +36,7 @@ __device__ __forceinline__ ItemRec complete_rec(const PartialParams& p, ItemRec 
       r.lo = p.page_indptr[r.it.b];
       r.hi = p.page_indptr[r.it.b + 1];
     }
-  } else if (p.layout == DATTN_KV_CONTIG_NHD) {
+  } else {
     r.crow = cache_row(p.cache_batch_idx, r.it.b, p.B_cache, report ? p.status : nullptr);
   }
   return r;
@@ -311,7 +311,9 @@ __device__ __forceinline__ SlotPages<S, FM> slot_pages(const Walk& w, const PCur
   return g;
 }
 
-template <int S, bool FM = false>
+// PACKED: the kernel may see the packed-row layout (bf16 only; the planner
+// rejects it for the other formats, whose producers are compiled without it).
+template <int S, bool FM = false, bool PACKED = false>
 __device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& c, const SlotKeys<S>& k,
                                                      const SlotPages<S, FM>& g, int lane) {
   const PartialParams& p = w.p;
@@ -345,7 +347,7 @@ __device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& 
         if (pi == -2) atomicOr(p.status, kStBlockRange);
         else if (pi < 0 || pi >= p.num_pages) atomicOr(p.status, kStPageRange);
         else row = (static_cast<uint32_t>(pi) * p.H_kv + r.it.h) * p.P + row_of(p, t);
-      } else if (p.layout == DATTN_KV_PACKED_ROWS) {
+      } else if (PACKED && p.layout == DATTN_KV_PACKED_ROWS) {
         // packed view: list entry x0 + j is packed row x0 + j (its position t only masks)
         row = static_cast<uint32_t>(r.it.x0 + c.j0 + lane + 32 * h);
       } else if (r.crow >= 0 && t < p.T_cap) {
