@@ -354,3 +354,46 @@ def test_packed_view_layout_validation():
     st = lib.kv_append(ctypes.byref(prob), ctypes.byref(dattn.AppendInputs()), ctypes.byref(dattn.Tensors()),
                        None, None, None, 0, None)
     assert st != 0 and "packed view" in dattn.dattn_last_error()
+
+
+@pytest.mark.parametrize("shift,status", [((float("nan"), -1.0, 1.0), "EINVAL"), ((0.0, 1.0, 1.0), "EINVAL"),
+                                          ((0.0, -90.0, 1.0), "EINVAL"), ((0.0, -1.0, 50.0), "EINVAL"),
+                                          ((float("inf"), -1.0, 1.0), "EINVAL")])
+def test_shared_shift_guard_checked_before_any_device_work(shift, status):
+    """The frame and guard fields of dattn_run_options reach the library (ctypes layout = C layout)
+    and are checked before the workspace or the tensors are touched."""
+    plan = dattn.dattn_plan(_problem(), [10, 20], num_sms=4)
+
+    class Never:   # a workspace that would fault if it were ever used
+        def data_ptr(self):
+            return 16
+
+        def numel(self):
+            return plan.workspace_bytes
+
+        def element_size(self):
+            return 1
+
+    with pytest.raises(dattn.DattnError, match=status):
+        dattn.dattn_run_ex(plan, _problem(), dattn.Tensors(), Never(), shared_shift=shift, stream=0)
+
+
+def test_shared_shift_needs_bf16_and_options_layout():
+    plan = dattn.dattn_plan(_problem(), [10, 20], num_sms=4)
+    ws = (ctypes.c_uint8 * 16)()
+
+    class W:
+        def data_ptr(self):
+            return ctypes.addressof(ws)
+
+        def numel(self):
+            return plan.workspace_bytes
+
+        def element_size(self):
+            return 1
+
+    with pytest.raises(dattn.DattnError, match="EUNSUPPORTED"):
+        dattn.dattn_run_ex(plan, _problem(fmt="int8"), dattn.Tensors(), W(), shared_shift=(0.0, -1.0, 1.0), stream=0)
+    # C layout: uint32 flags, void* events[3], float phi, lo, hi
+    assert dattn.RunOptions.shift_phi.offset == 32 and dattn.RunOptions.shift_hi.offset == 40
+    assert ctypes.sizeof(dattn.RunOptions) == 48
