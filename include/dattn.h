@@ -286,11 +286,22 @@ dattn_status dattn_run(const dattn_plan_t* plan, const dattn_problem* prob,
                                       fallback), so the result is the softmax either way.
                                       Requires -80 <= shift_lo < shift_hi <= 40 and a finite
                                       shift_phi.  dattn_shift_fallbacks counts the fallbacks */
+#define DATTN_RUN_TEST_SKIP_ARRIVAL 4u  /* test hook of the fail-closed path (M4.5 §0x07B),
+                                      bf16 K/V only: the producers of CTA 0 withhold the
+                                      completion of its first ring stage, so its consumers'
+                                      bounded wait runs out after wait_limit_us (required,
+                                      1 .. 100000).  Nothing faults or hangs: the CTA stops,
+                                      the status word gets the timeout bit (16) and no output
+                                      row is written from the states it left unwritten */
 typedef struct {
   uint32_t flags;     /* DATTN_RUN_* bits                                                  */
   void* events[3];    /* cudaEvent_t (as void*) recorded on "stream" before the partial
                          kernel, after it and after the merge kernel; NULL entries skipped */
   float shift_phi, shift_lo, shift_hi;   /* DATTN_RUN_SHARED_SHIFT frame and guard      */
+  uint32_t wait_limit_us;   /* limit of each bounded wait on a ring stage in microseconds
+                               (0: 2 s).  A wait that runs out stops its CTA, sets the
+                               timeout bit (16) of the device status word, and the merge
+                               then writes no output row (fail closed)                     */
 } dattn_run_options;
 
 /* Number of consumer warps that left the shared-shift frame (guard failed) since the work
@@ -326,8 +337,10 @@ dattn_status dattn_run_ex(const dattn_plan_t* plan, const dattn_problem* prob,
  *
  * Layouts (offsets from the start of each buffer, 256-byte aligned pieces):
  *   workspace: [q | page_indptr | page_indices | plan workspace | O | LSE]
- *   staging:   the same pieces in pinned host memory; the first four are sent
- *              in one transfer, O and LSE come back in one transfer.
+ *   staging:   [q | page_indptr | page_indices | work list | ... | O | LSE] in
+ *              pinned host memory; the first four are sent in one transfer, O
+ *              and LSE come back in one transfer into the buffer's last
+ *              round_up(O, 256) + round_up(LSE, 256) bytes (16-byte aligned).
  * The staging buffer should be page-locked (cudaHostAlloc / pinned) so that
  * both transfers are asynchronous DMA; the library never allocates it. */
 typedef struct {
@@ -355,6 +368,22 @@ dattn_status dattn_step_host(const dattn_problem* prob, const dattn_host_step* i
                              void* staging, size_t staging_bytes, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* The same step split in two, so that the host work of the next step (its
+ * staging copies and planning) overlaps this step on the device.
+ * dattn_step_host_submit does everything dattn_step_host does up to the
+ * enqueue of the output transfer, records "done_event" (a cudaEvent_t as
+ * void*, required) on "stream" after it and returns without waiting.
+ * dattn_step_host_finish waits for "done_event" and copies O and LSE from the
+ * staging buffer into io->o / io->lse.  Between the two calls the staging
+ * buffer belongs to the step: a pipelined caller alternates two staging
+ * buffers (and two events); steps on one stream may share a workspace.
+ * Errors as for dattn_step_host; a failed submit records no event. */
+dattn_status dattn_step_host_submit(const dattn_problem* prob, const dattn_host_step* io,
+                                    const dattn_tensors* cache, void* staging, size_t staging_bytes,
+                                    void* workspace, size_t workspace_bytes, void* stream, void* done_event);
+dattn_status dattn_step_host_finish(const dattn_problem* prob, const dattn_host_step* io, const void* staging,
+                                    size_t staging_bytes, void* done_event);
+
 /* Device bounds-check word of the last dattn_step_host on this workspace (like
  * dattn_device_status; synchronises "stream"). */
 dattn_status dattn_step_host_status(const dattn_problem* prob, const dattn_host_step* io, const void* workspace,
@@ -379,8 +408,19 @@ dattn_status dattn_step_host_status(const dattn_problem* prob, const dattn_host_
  *
  * First call on a device:
  *  - It looks up the array's address with cudaGetSymbolAddress on the current
- *    device and keeps it for later calls.
+ *    device and keeps it, per device ordinal, for later calls.
  *  - Make that call before any stream capture on that device.
+ *  - The kept address belongs to the device's primary context as it was at
+ *    that call: after cudaDeviceReset, or from a thread bound to another
+ *    driver context of the same device, it no longer names the array, so
+ *    neither case is supported once a call has been made.
+ *
+ * Copies:
+ *  - Each call copies the plan's work list from the plan's host memory into
+ *    the array, on "stream".  That host memory is ordinary (pageable), so
+ *    CUDA may complete this copy synchronously with respect to the host
+ *    before the call returns; a caller that needs the call to return at once
+ *    uses dattn_plan_upload / dattn_run_ex with its own workspace instead.
  *
  * Sharing and races:
  *  - All calls on a device share the one array, which keeps the last call's
@@ -395,10 +435,17 @@ dattn_status dattn_step_host_status(const dattn_problem* prob, const dattn_host_
  *    gets DATTN_EWORKSPACE and a message; use dattn_run for it.
  *  - Any other argument error is reported as dattn_run reports it.
  *
- * dattn_device_status cannot read this call's status word, because the caller
- * holds no pointer to the array. */
+ * The device bounds checks of this call (page id outside the pool, block
+ * outside the request's page list, ...) and a bounded wait that gave up are
+ * reported in the array's status word: read it with dattn_noalloc_status. */
 dattn_status dattn_run_noalloc(const dattn_plan_t* plan, const dattn_problem* prob,
                                const dattn_tensors* t, void* stream);
+
+/* Device status word of the last dattn_run_noalloc on the current device, read
+ * from the library's scratch array (like dattn_device_status: synchronises
+ * "stream", *flags = 0 when no device check fired, DATTN_EDEVICE_CHECK when
+ * one did).  Allocates nothing; the pages have no counterpart. */
+dattn_status dattn_noalloc_status(int32_t* flags, void* stream);
 
 /* Reads the device status word of the last run that used "workspace"
  * (synchronises "stream").  *flags = 0 when no device check fired. */

@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "DattnError", "Problem", "load", "make_problem", "dattn_plan", "dattn_plan_get_info",
-    "dattn_plan_get_items", "dattn_run", "dattn_run_ex", "dattn_plan_upload", "dattn_device_status", "dattn_shift_fallbacks", "kv_append",
+    "dattn_plan_get_items", "dattn_run", "dattn_run_ex", "dattn_run_noalloc", "dattn_noalloc_status", "dattn_plan_upload", "dattn_device_status", "dattn_shift_fallbacks", "kv_append",
     "kv_append_workspace_bytes", "dattn_debug_translate", "dattn_debug_classify",
     "dattn_debug_gather", "dattn_last_error", "dattn_version", "tensors_from", "decode",
     "LAYOUTS", "FORMATS", "MASKS", "TILE_CLASSES", "STATUS",
@@ -81,11 +81,13 @@ class WorkItem(ctypes.Structure):
 
 class RunOptions(ctypes.Structure):
     _fields_ = [("flags", ctypes.c_uint32), ("events", ctypes.c_void_p * 3),
-                ("shift_phi", ctypes.c_float), ("shift_lo", ctypes.c_float), ("shift_hi", ctypes.c_float)]
+                ("shift_phi", ctypes.c_float), ("shift_lo", ctypes.c_float), ("shift_hi", ctypes.c_float),
+                ("wait_limit_us", ctypes.c_uint32)]
 
 
 RUN_REUSE_UPLOAD = 1
 RUN_SHARED_SHIFT = 2
+RUN_TEST_SKIP_ARRIVAL = 4
 NOALLOC_SCRATCH_BYTES = 16 << 20  # DATTN_NOALLOC_SCRATCH_BYTES
 
 
@@ -118,6 +120,7 @@ def load():
                                ctypes.c_size_t, _VP, ctypes.POINTER(RunOptions)]),
         "dattn_plan_upload": (_ST, [_VP, _VP, ctypes.c_size_t, _VP]),
         "dattn_run_noalloc": (_ST, [_VP, ctypes.POINTER(Problem), ctypes.POINTER(Tensors), _VP]),
+        "dattn_noalloc_status": (_ST, [ctypes.POINTER(ctypes.c_int32), _VP]),
         "dattn_device_status": (_ST, [_VP, ctypes.POINTER(ctypes.c_int32), _VP]),
         "dattn_shift_fallbacks": (_ST, [_VP, ctypes.POINTER(ctypes.c_int32), _VP]),
         "kv_append_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Problem)]),
@@ -136,6 +139,10 @@ def load():
                                   _VP, ctypes.c_size_t, _VP, ctypes.c_size_t, _VP]),
         "dattn_step_host_status": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(HostStep), _VP,
                                          ctypes.POINTER(ctypes.c_int32), _VP]),
+        "dattn_step_host_submit": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(HostStep), ctypes.POINTER(Tensors),
+                                         _VP, ctypes.c_size_t, _VP, ctypes.c_size_t, _VP, _VP]),
+        "dattn_step_host_finish": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(HostStep), _VP, ctypes.c_size_t,
+                                         _VP]),
         "dattn_last_error": (ctypes.c_char_p, []),
         "dattn_version": (ctypes.c_int32, []),
     }
@@ -296,6 +303,15 @@ def dattn_run_noalloc(plan: Plan, problem, tensors: Tensors, stream=None) -> Non
            "dattn_run_noalloc")
 
 
+def dattn_noalloc_status(stream=None) -> int:
+    """Device status word of the last dattn_run_noalloc on the current device (0: no check fired)."""
+    flags = ctypes.c_int32()
+    st = load().dattn_noalloc_status(ctypes.byref(flags), _stream_ptr(stream))
+    if st not in (0, 6):
+        _check(st, "dattn_noalloc_status")
+    return flags.value
+
+
 def dattn_plan_upload(plan: Plan, workspace, stream=None) -> None:
     """Copy the plan's work list into ``workspace`` (see dattn_plan_upload in dattn.h)."""
     _check(load().dattn_plan_upload(plan.handle, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
@@ -303,13 +319,16 @@ def dattn_plan_upload(plan: Plan, workspace, stream=None) -> None:
 
 
 def dattn_run_ex(plan: Plan, problem, tensors: Tensors, workspace, *, reuse_upload=False, events=None,
-                 shared_shift=None, stream=None) -> None:
+                 shared_shift=None, wait_limit_us=0, test_skip_arrival=False, stream=None) -> None:
     """dattn_run with options: reuse an uploaded work list, record three torch.cuda.Events
-    (before the partial kernel, after it, after the merge kernel), and ``shared_shift =
-    (phi, lo, hi)``: partials in the fixed frame phi, guarded by lo < s - phi < hi."""
+    (before the partial kernel, after it, after the merge kernel), ``shared_shift =
+    (phi, lo, hi)``: partials in the fixed frame phi, guarded by lo < s - phi < hi,
+    ``wait_limit_us``: the bounded waits' limit, and ``test_skip_arrival``: the hook that
+    makes one wait run out (DATTN_RUN_TEST_SKIP_ARRIVAL)."""
     prob = problem if isinstance(problem, Problem) else make_problem(problem)
     opt = RunOptions()
-    opt.flags = RUN_REUSE_UPLOAD if reuse_upload else 0
+    opt.flags = (RUN_REUSE_UPLOAD if reuse_upload else 0) | (RUN_TEST_SKIP_ARRIVAL if test_skip_arrival else 0)
+    opt.wait_limit_us = int(wait_limit_us)
     if shared_shift is not None:
         opt.flags |= RUN_SHARED_SHIFT
         opt.shift_phi, opt.shift_lo, opt.shift_hi = (float(x) for x in shared_shift)
@@ -418,6 +437,24 @@ def dattn_step_host(problem, io: HostStep, cache: Tensors, staging, workspace, s
     _check(load().dattn_step_host(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache), staging.data_ptr(),
                                   staging.numel(), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)),
            "dattn_step_host")
+
+
+def dattn_step_host_submit(problem, io: HostStep, cache: Tensors, staging, workspace, done_event,
+                           stream=None) -> None:
+    """Enqueue one decode step from host memory and return at once; ``done_event`` (a
+    torch.cuda.Event) is recorded after its output transfer (see dattn.h)."""
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    _check(load().dattn_step_host_submit(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache),
+                                         staging.data_ptr(), staging.numel(), workspace.data_ptr(),
+                                         workspace.numel(), _stream_ptr(stream), done_event.cuda_event),
+           "dattn_step_host_submit")
+
+
+def dattn_step_host_finish(problem, io: HostStep, staging, done_event) -> None:
+    """Wait for a submitted step and copy its O (and LSE) into the host arrays of io."""
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    _check(load().dattn_step_host_finish(ctypes.byref(prob), ctypes.byref(io), staging.data_ptr(), staging.numel(),
+                                         done_event.cuda_event), "dattn_step_host_finish")
 
 
 def dattn_step_host_status(problem, io: HostStep, workspace, stream=None) -> int:

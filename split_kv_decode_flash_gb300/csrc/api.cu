@@ -91,6 +91,7 @@ void fill_common(const dattn_problem& p, const dattn_tensors& t, PartialParams& 
   k.kivi_R = p.kivi_residual;
   const float scale = p.sm_scale > 0.f ? p.sm_scale : 1.f / std::sqrt(static_cast<float>(p.d_h));
   k.scale_log2 = scale * 1.4426950408889634f;
+  k.wait_ns = kDefaultWaitNs;
 }
 
 dattn_status cuda_fail(const char* where, int err) {
@@ -218,12 +219,20 @@ dattn_status record(void* const* events, int i, cudaStream_t s) {
 dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const dattn_tensors* t, void* workspace,
                       size_t workspace_bytes, void* stream, const dattn_run_options* opt, const char* where) {
   const bool shift = opt && (opt->flags & DATTN_RUN_SHARED_SHIFT);
+  const bool skip_arrival = opt && (opt->flags & DATTN_RUN_TEST_SKIP_ARRIVAL);
   if (shift) {
     Checker c;
     if (prob && prob->fmt != DATTN_FMT_BF16) c.fail(DATTN_EUNSUPPORTED, "shared-shift partials run on bf16 K/V");
     if (!std::isfinite(opt->shift_phi)) c.fail(DATTN_EINVAL, "shift_phi must be finite");
     if (!(opt->shift_lo >= -80.f && opt->shift_lo < opt->shift_hi && opt->shift_hi <= 40.f))
       c.fail(DATTN_EINVAL, "the guard needs -80 <= shift_lo < shift_hi <= 40");
+    if (c.status != DATTN_OK) return c.finish(where);
+  }
+  if (skip_arrival) {
+    Checker c;
+    if (prob && prob->fmt != DATTN_FMT_BF16) c.fail(DATTN_EUNSUPPORTED, "the skipped-arrival hook runs on bf16 K/V");
+    if (opt->wait_limit_us == 0 || opt->wait_limit_us > 100000u)
+      c.fail(DATTN_EINVAL, "the skipped-arrival hook needs a wait limit of 1 .. 100000 us");
     if (c.status != DATTN_OK) return c.finish(where);
   }
   dattn_status st = check_run_args(plan, prob, t, workspace, workspace_bytes, true, where);
@@ -241,6 +250,8 @@ dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const
     k.shift_fallbacks = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
                                                    offsetof(BlobHeader, shift_fallbacks));
   }
+  if (opt && opt->wait_limit_us) k.wait_ns = static_cast<uint64_t>(opt->wait_limit_us) * 1000ull;
+  k.skip_arrival = skip_arrival ? 1 : 0;
   if (opt && (opt->flags & DATTN_RUN_REUSE_UPLOAD)) {
     bind_blob(plan, workspace, k);
   } else {
@@ -413,7 +424,7 @@ struct StepLayout {
   size_t q_bytes, pi_bytes, px_bytes, o_bytes, lse_bytes;
   size_t pi_off, px_off, plan_off;      // device and staging (inputs, then the work list)
   size_t o_off, lse_off, ws_total;      // device
-  size_t o_off_s, staging_total;        // staging: outputs after the work list
+  size_t o_off_s, staging_total;        // staging: the work list's end, and the size with the outputs
 };
 
 size_t align_ws(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
@@ -487,24 +498,35 @@ extern "C" dattn_status dattn_step_host_sizes(const dattn_problem* prob, const d
   return DATTN_OK;
 }
 
-extern "C" dattn_status dattn_step_host(const dattn_problem* prob, const dattn_host_step* io,
-                                        const dattn_tensors* cache, void* staging, size_t staging_bytes,
-                                        void* workspace, size_t workspace_bytes, void* stream) {
-  const char* where = "dattn_step_host";
+namespace {
+
+// Where O and LSE come back in the staging buffer: its last
+// align_ws(o) + align_ws(lse) bytes (a fixed place, so that the step's finish
+// finds them without the plan).
+size_t staging_out_off(const StepLayout& L, size_t staging_bytes) {
+  const size_t out = align_ws(L.o_bytes) + align_ws(L.lse_bytes);
+  return staging_bytes >= out ? (staging_bytes - out) / 16 * 16 : 0;
+}
+
+dattn_status step_submit(const dattn_problem* prob, const dattn_host_step* io, const dattn_tensors* cache,
+                         void* staging, size_t staging_bytes, void* workspace, size_t workspace_bytes,
+                         void* stream, void* done_event, const char* where) {
   dattn_status st = check_step(prob, io, true, where);
   if (st != DATTN_OK) return st;
   if (!cache || !staging) {
-    set_error("dattn_step_host: cache and staging are required");
+    set_error(std::string(where) + ": cache and staging are required");
     return DATTN_EINVAL;
   }
   // The input region (q, page table) does not depend on the plan: its transfer
   // is issued first and runs while the host plans.  Only the workspace's input
   // region is written before the plan's checks.
   const StepLayout L0 = step_layout(*prob, page_entries(prob, io), 0, 0);
+  const size_t out0 = staging_out_off(L0, staging_bytes);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) || workspace_bytes < L0.plan_off ||
-      (reinterpret_cast<uintptr_t>(staging) % 16) || staging_bytes < L0.plan_off) {
-    set_error("dattn_step_host: workspace (256-byte aligned) and staging (16-byte aligned) must hold at least " +
-              std::to_string(L0.plan_off) + " bytes; dattn_step_host_sizes gives the full sizes");
+      (reinterpret_cast<uintptr_t>(staging) % 16) || staging_bytes < L0.plan_off || out0 < L0.plan_off) {
+    set_error(std::string(where) + ": workspace (256-byte aligned) and staging (16-byte aligned) must hold at "
+              "least " + std::to_string(L0.plan_off) + " bytes of inputs; dattn_step_host_sizes gives the full "
+              "sizes");
     return DATTN_EWORKSPACE;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -514,14 +536,14 @@ extern "C" dattn_status dattn_step_host(const dattn_problem* prob, const dattn_h
   if (L0.pi_bytes) std::memcpy(sg + L0.pi_off, io->page_indptr, L0.pi_bytes);
   if (L0.px_bytes) std::memcpy(sg + L0.px_off, io->page_indices, L0.px_bytes);
   cudaError_t err = cudaMemcpyAsync(ws, sg, L0.plan_off, cudaMemcpyHostToDevice, s);
-  if (err != cudaSuccess) return cuda_fail("dattn_step_host input transfer", err);
+  if (err != cudaSuccess) return cuda_fail("host step input transfer", err);
 
   dattn_plan_t* plan = nullptr;
   size_t plan_ws = 0;
   if ((st = plan_step(prob, io, &plan, &plan_ws)) != DATTN_OK) return st;
   const StepLayout L = step_layout(*prob, page_entries(prob, io), plan_ws, plan->blob.size());
   if (workspace_bytes < L.ws_total || staging_bytes < L.staging_total) {
-    set_error("dattn_step_host: workspace needs " + std::to_string(L.ws_total) + " bytes and staging " +
+    set_error(std::string(where) + ": workspace needs " + std::to_string(L.ws_total) + " bytes and staging " +
               std::to_string(L.staging_total) + " bytes");
     dattn_plan_destroy(plan);
     return DATTN_EWORKSPACE;
@@ -539,25 +561,70 @@ extern "C" dattn_status dattn_step_host(const dattn_problem* prob, const dattn_h
     dattn_plan_destroy(plan);
     return st;
   }
-  // the work list (the staging copy of the inputs may still be in flight: it is
-  // not touched again before the stream is synchronised)
+  // the work list (the staging copy of the inputs may still be in flight: that
+  // part of the staging buffer is not touched again before the step is done)
   std::memcpy(sg + L.plan_off, plan->blob.data(), plan->blob.size());
   err = cudaMemcpyAsync(ws + L.plan_off, sg + L.plan_off, plan->blob.size(), cudaMemcpyHostToDevice, s);
   if (err != cudaSuccess) {
     dattn_plan_destroy(plan);
-    return cuda_fail("dattn_step_host work-list transfer", err);
+    return cuda_fail("host step work-list transfer", err);
   }
   dattn_run_options opt{};
   opt.flags = DATTN_RUN_REUSE_UPLOAD;
   st = run_impl(plan, prob, &t, ws + L.plan_off, plan_ws, stream, &opt, where);
   dattn_plan_destroy(plan);
   if (st != DATTN_OK) return st;
-  // outputs: one device->host transfer, then into the caller's arrays
-  err = cudaMemcpyAsync(sg + L.o_off_s, ws + L.o_off, align_ws(L.o_bytes) + L.lse_bytes, cudaMemcpyDeviceToHost, s);
-  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
-  if (err != cudaSuccess) return cuda_fail("dattn_step_host output transfer", err);
-  std::memcpy(io->o, sg + L.o_off_s, L.o_bytes);
-  if (io->lse) std::memcpy(io->lse, sg + L.o_off_s + align_ws(L.o_bytes), L.lse_bytes);
+  // outputs: one device->host transfer into the end of the staging buffer
+  err = cudaMemcpyAsync(sg + staging_out_off(L, staging_bytes), ws + L.o_off, align_ws(L.o_bytes) + L.lse_bytes,
+                        cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess && done_event) err = cudaEventRecord(static_cast<cudaEvent_t>(done_event), s);
+  if (err != cudaSuccess) return cuda_fail("host step output transfer", err);
+  return DATTN_OK;
+}
+
+// Copies a finished step's O and LSE from the staging buffer into the caller's arrays.
+void step_copy_out(const dattn_problem* prob, const dattn_host_step* io, const void* staging, size_t staging_bytes) {
+  const StepLayout L = step_layout(*prob, page_entries(prob, io), 0, 0);
+  const uint8_t* out = static_cast<const uint8_t*>(staging) + staging_out_off(L, staging_bytes);
+  std::memcpy(io->o, out, L.o_bytes);
+  if (io->lse) std::memcpy(io->lse, out + align_ws(L.o_bytes), L.lse_bytes);
+}
+
+}  // namespace
+
+extern "C" dattn_status dattn_step_host(const dattn_problem* prob, const dattn_host_step* io,
+                                        const dattn_tensors* cache, void* staging, size_t staging_bytes,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  dattn_status st = step_submit(prob, io, cache, staging, staging_bytes, workspace, workspace_bytes, stream,
+                                nullptr, "dattn_step_host");
+  if (st != DATTN_OK) return st;
+  const cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail("dattn_step_host", err);
+  step_copy_out(prob, io, staging, staging_bytes);
+  return DATTN_OK;
+}
+
+extern "C" dattn_status dattn_step_host_submit(const dattn_problem* prob, const dattn_host_step* io,
+                                               const dattn_tensors* cache, void* staging, size_t staging_bytes,
+                                               void* workspace, size_t workspace_bytes, void* stream,
+                                               void* done_event) {
+  if (!done_event) {
+    set_error("dattn_step_host_submit: done_event is required");
+    return DATTN_EINVAL;
+  }
+  return step_submit(prob, io, cache, staging, staging_bytes, workspace, workspace_bytes, stream, done_event,
+                     "dattn_step_host_submit");
+}
+
+extern "C" dattn_status dattn_step_host_finish(const dattn_problem* prob, const dattn_host_step* io,
+                                               const void* staging, size_t staging_bytes, void* done_event) {
+  Checker c;
+  check_problem(prob, c);
+  if (!io || !io->o || !staging || !done_event) c.fail(DATTN_EINVAL, "io, io->o, staging and done_event are required");
+  if (c.status != DATTN_OK) return c.finish("dattn_step_host_finish");
+  const cudaError_t err = cudaEventSynchronize(static_cast<cudaEvent_t>(done_event));
+  if (err != cudaSuccess) return cuda_fail("dattn_step_host_finish", err);
+  step_copy_out(prob, io, staging, staging_bytes);
   return DATTN_OK;
 }
 

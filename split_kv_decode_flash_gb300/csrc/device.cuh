@@ -70,17 +70,18 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Bounded wait.  The thread sleeps inside try_wait (hardware suspend, woken
 // by the phase completing) instead of spinning, so waiting warps leave the
-// issue slots to working ones.  After 2 s of wall time it raises the abort
-// flag and the timeout status bit, so that every warp of the CTA stops.
+// issue slots to working ones.  After limit_ns of wall time (2 s unless the
+// caller set another limit) it raises the abort flag and the timeout status
+// bit, so that every warp of the CTA stops.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((it & 7u) == 7u) {
       if (*abort_flag) return false;
-      if (global_ns() - t0 > 2000000000ull) {
+      if (global_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, kStTimeout);
         return false;

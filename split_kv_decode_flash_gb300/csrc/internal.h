@@ -34,12 +34,12 @@ enum StatusBits : int32_t {
 };
 
 // KIVI INT4 problems with d = 128, at most 8 rows, Gv = 32, an interval
-// visibility program and power-of-two page size P and residual length R run
-// on the tensor-core kernel (partial_q4.cu); other KIVI problems on the
-// byte-format kernel (partial.cu).
+// visibility program and a power-of-two page size P run on the tensor-core
+// kernel (partial_q4.cu); other KIVI problems on the byte-format kernel
+// (partial.cu).  The residual length R is any positive multiple of G on both.
 inline bool kivi_on_tensor_cores(int d, int rows, int Gv, int mask, int P, int R) {
   return d == 128 && rows <= 8 && Gv == 32 && mask != DATTN_MASK_INDEX_LIST && P > 0 && (P & (P - 1)) == 0 &&
-         R > 0 && (R & (R - 1)) == 0;
+         R > 0;
 }
 
 // Partial states an item leaves per query row.  Consumer warps are arranged
@@ -130,7 +130,11 @@ struct PartialParams {
   int32_t shift_on;       // shared-shift partials (bf16 kernel)
   float shift_phi2, shift_lo2, shift_hi2;   // frame and guard, log2 units
   int32_t* shift_fallbacks;
+  uint64_t wait_ns;       // limit of every bounded mbarrier wait
+  int32_t skip_arrival;   // test hook (bf16 kernel): CTA 0 never completes its first stage
 };
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
 
 struct MergeParams {
   const MergeGroup* groups;

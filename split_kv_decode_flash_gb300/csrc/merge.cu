@@ -45,6 +45,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   const int gi = blockIdx.x / blocks_per_group;
   const int row = (blockIdx.x % blocks_per_group) * kRowsPerBlock + (WPR > 1 ? 0 : w);
   const MergeGroup grp = p.groups[gi];
+  // A partial kernel whose bounded wait gave up (or met a mis-stamped stage)
+  // left states unwritten: then no row is written from them.  The word is
+  // read with the group and tested only before the write.
+  const int32_t partial_status = __ldcg(p.status);
+  const bool fail_closed = partial_status & (kStTimeout | kStPipeline);
   const int i = row / p.g, hq = grp.h * p.g + row % p.g;
   const long long orow = (static_cast<long long>(grp.qo) + i) * p.H_q + hq;
   if constexpr (WPR == 1) {
@@ -52,7 +57,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
     RowFold<D> f;
     fold_init(f);
     fold_states<D>(p.ml, p.u, p.rows, row, grp.slot0, grp.n, 1, lane, f);
-    write_folded_row<D>(p.o, p.lse, orow, f, lane);
+    if (!fail_closed) write_folded_row<D>(p.o, p.lse, orow, f, lane);
     return;
   } else {
     if (row >= p.g * grp.nq) return;
@@ -84,7 +89,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
         for (int c = 0; c < C; ++c) t.U[c] = fmaf(a, sm_u[k][lane * C + c], t.U[c]);
       }
     }
-    write_folded_row<D>(p.o, p.lse, orow, t, lane);
+    if (!fail_closed) write_folded_row<D>(p.o, p.lse, orow, t, lane);
   }
 }
 

@@ -74,9 +74,22 @@ extern "C" dattn_status dattn_run_noalloc(const dattn_plan_t* plan, const dattn_
   void* scratch = nullptr;
   const dattn_status st = scratch_of_current_device(&scratch);
   if (st != DATTN_OK) return st;
-  // The work list (whose header holds the zeroed status word) is copied into
-  // the scratch by dattn_run on "stream"; every partial-state slot the merge
-  // reads is written by the partial kernel first, so no other part of the
-  // previous call's contents needs clearing.
+  // The work list is copied into the scratch by dattn_run on "stream"; it
+  // carries the zeroed status word and, for a fused-merge plan, the zeroed
+  // per-group completion counters.  Every partial-state slot the merge reads
+  // is written by the partial kernel first, so no other part of the previous
+  // call's contents needs clearing.
   return dattn_run(plan, prob, t, scratch, kScratchBytes, stream);
+}
+
+extern "C" dattn_status dattn_noalloc_status(int32_t* flags, void* stream) {
+  if (!flags) {
+    dattn::set_error("dattn_noalloc_status: flags is NULL");
+    return DATTN_EINVAL;
+  }
+  void* scratch = nullptr;
+  const dattn_status st = scratch_of_current_device(&scratch);
+  if (st != DATTN_OK) return st;
+  // the status word sits in the work-list header at the start of the array
+  return dattn_device_status(scratch, flags, stream);
 }

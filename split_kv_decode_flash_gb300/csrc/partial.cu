@@ -208,7 +208,7 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
 
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) return;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) return;
     uint8_t* stage = smem + st * C::kStage;
     uint8_t* kt = stage;
     uint8_t* vt = stage + C::kTile;
@@ -497,7 +497,7 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
         dead = true;
         break;
       }

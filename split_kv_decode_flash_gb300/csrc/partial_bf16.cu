@@ -102,7 +102,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
     pos[lane] = r0.t[0];
     pos[lane + 32] = r0.t[1];
@@ -127,9 +127,11 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
       cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
     }
     const uint32_t fb = full0 + 8 * st;
-    cp_async_mbar_arrive(fb);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
+    if (!(p.skip_arrival && blockIdx.x == 0 && k == 0)) {   // the test hook withholds stage 0 of CTA 0
+      cp_async_mbar_arrive(fb);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fb);   // publishes pos / flags / stamp; the copies complete the phase
+    }
 
     // move the description pipeline one stage of this warp forward
     r0 = slot_rows<2, FM, true>(w, c1, k1, g1, lane);
@@ -173,7 +175,7 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
     const ItemRec rec = w.rec(c0.ii);
     uint32_t rows[2];
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
@@ -199,9 +201,11 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
       cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
     }
     const uint32_t fb = full0 + 8 * st;
-    cp_async_mbar_arrive(fb);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
+    if (!(p.skip_arrival && blockIdx.x == 0 && k == 0)) {   // the test hook withholds stage 0 of CTA 0
+      cp_async_mbar_arrive(fb);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fb);   // publishes pos / flags / stamp; the copies complete the phase
+    }
 
     c0 = c1;
     s0 = s1;
@@ -328,7 +332,7 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
     }
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+    if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
       dead = true;
       break;
     }
@@ -557,6 +561,9 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
   float* sm_ml = sm_u + kCW * D;                                  // [kCW][2]
   __threadfence();                                                // this thread's state writes
   named_barrier(1, 32 * kCW);
+  // A CTA whose wait gave up left some states unwritten: it counts none of its
+  // items, so their groups are never merged (no row from stale states).
+  if (*reinterpret_cast<volatile int*>(smem + Bf<D>::kAbort)) return;
   if (cw == 0 && lane == 0) {
     int n = 0;
     for (int ii = w.begin; ii < w.end; ++ii) {

@@ -173,10 +173,10 @@ struct Q4Desc {
   bool full, resid;
 };
 
-// The producer's index arithmetic: P, G and R are powers of two on this
-// kernel (shifts psh, gsh; ring mask rmask).
+// The producer's index arithmetic: P and G are powers of two on this kernel
+// (shifts psh, gsh); R, the residual ring's length, is any multiple of G.
 struct Q4Shapes {
-  int psh, gsh, rmask;
+  int psh, gsh, R;
 };
 
 __device__ __forceinline__ void q4_keys(const Walk& w, const QCur& c, int lane, int (&t)[kQSlots]) {
@@ -231,14 +231,14 @@ __device__ __forceinline__ Q4Desc q4_rows(const Walk& w, const QCur& c, const in
   d.resid = c.j0 >= c.jq;
   int tmax = -1, err = 0;
   // residual ring row of token t: (b R + (t mod R)) H + h; page row: (pi H + h) P + (t mod P)
-  const uint32_t ring0 = static_cast<uint32_t>(r.it.b) * (sh.rmask + 1);
+  const uint32_t ring0 = static_cast<uint32_t>(r.it.b) * sh.R;
 #pragma unroll
   for (int h = 0; h < kQSlots; ++h) {
     const int tk = t[h];
     uint32_t row = kNoRow;
     if (tk >= 0) {
       if (d.resid) {
-        row = (ring0 + (tk & sh.rmask)) * p.H_kv + r.it.h;
+        row = (ring0 + static_cast<uint32_t>(tk % sh.R)) * p.H_kv + r.it.h;
       } else if (pi[h] == -2) {
         err |= kStBlockRange;
       } else if (pi[h] < 0 || pi[h] >= p.num_pages) {
@@ -285,7 +285,7 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool 
   const char* kqbase = static_cast<const char*>(p.kqp);
   const char* vqbase = static_cast<const char*>(p.vqp);
   const uint64_t stream_pol = policy_evict_first();
-  const Q4Shapes sh{p.P_shift, p.kivi_G == 32 ? 5 : 6, p.kivi_R - 1};
+  const Q4Shapes sh{p.P_shift, p.kivi_G == 32 ? 5 : 6, p.kivi_R};
 
   // Stages are described in three steps a stage apart (keys two stages ahead,
   // page ids one stage ahead, rows for the stage at hand), so the page-table
@@ -311,7 +311,7 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool 
     q4_keys(w, c2, lane, t1);
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kQKeys;
     uint32_t* rows = reinterpret_cast<uint32_t*>(smem + C::kRows) + st * kQKeys;
 #pragma unroll
@@ -660,7 +660,7 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
         dead = true;
         break;
       }

@@ -123,7 +123,7 @@ __device__ void produce_q4h(const Walk& w, uint8_t* smem, int lane, int pw, bool
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kHK;
 #pragma unroll
     for (int h = 0; h < kHS; ++h) pos[lane + 32 * h] = r0.t[h];
@@ -196,7 +196,7 @@ __device__ void produce_q4h_runs(const Walk& w, uint8_t* smem, int lane, int pw,
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
     const ItemRec rec = w.rec(c0.ii);
     uint32_t rows[kHS];
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kHK;
@@ -363,7 +363,7 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
         dead = true;
         break;
       }

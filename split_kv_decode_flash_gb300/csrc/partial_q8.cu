@@ -143,7 +143,7 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kQK;
 #pragma unroll
     for (int h = 0; h < kQS; ++h) pos[lane + 32 * h] = r0.t[h];
@@ -221,7 +221,7 @@ __device__ void produce_q8_runs(const Walk& w, uint8_t* smem, int lane, int pw, 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
     const ItemRec rec = w.rec(c0.ii);
     uint32_t rows[kQS];
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kQK;
@@ -423,7 +423,7 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
         dead = true;
         break;
       }
@@ -669,7 +669,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
         dead = true;
         break;
       }

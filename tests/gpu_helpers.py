@@ -117,12 +117,29 @@ def gpu_row(O, w, b, i, h):
     return O[int(w.qo_indptr[b]) + i, h]
 
 
-def compare(O, LSE, w, rows=None, cache=None):
-    """Element-by-element comparison of the GPU rows against the oracle; returns max errors."""
+def cache_arrays(w):
+    """(spec, arrays) of a bf16 workload's cache for ``oracle_pool.decode_rows_parallel``."""
+    p = w.problem
+    spec = dict(kind="cache", layout=p["layout"], H_kv=p["H_kv"], d=p["d"], P=p.get("P", 0), T_cap=p.get("T_cap", 0))
+    i64 = lambda t: None if t is None else t.numpy().astype(np.int64)
+    arrays = dict(k=bits(w.k), v=bits(w.v), kv_len=i64(w.kv_len), page_indptr=i64(w.page_indptr),
+                  page_indices=i64(w.page_indices), cache_batch_idx=i64(w.cache_batch_idx))
+    if p["layout"] == "packed":
+        arrays.update(row_offsets=i64(w.index_indptr), position_map=i64(w.index_list))
+    return spec, arrays
+
+
+def compare(O, LSE, w, rows=None, cache=None, ref=None):
+    """Element-by-element comparison of the GPU rows against the oracle; returns max errors.
+
+    ``ref`` = (O_ref, LSE_ref) of ``rows`` computed beforehand (e.g. in parallel)."""
     p = oracle_problem(w)
     rows = rows or all_rows(p)
-    cache = cache or oracle_cache(w)
-    Oref, Lref = attention.decode_rows(p, cache, bits(w.q), rows)
+    if ref is None:
+        cache = cache or oracle_cache(w)
+        Oref, Lref = attention.decode_rows(p, cache, bits(w.q), rows)
+    else:
+        Oref, Lref = ref
     og = np.stack([gpu_row(O, w, b, i, h).numpy() for b, i, h in rows]).astype(np.float64)
     lg = np.array([gpu_row(LSE, w, b, i, h).item() for b, i, h in rows], dtype=np.float64)
     masked = np.isneginf(Lref)
@@ -138,6 +155,17 @@ def compare(O, LSE, w, rows=None, cache=None):
     assert (lerr <= LSE_RTOL * np.maximum(1.0, np.abs(Lref[fin]))).all(), f"LSE error {lerr.max():.3g}"
     return {"max_abs_O": float(err.max()), "max_abs_LSE": float(lerr.max()) if lerr.size else 0.0,
             "rows": len(rows)}
+
+
+def compare_all_rows(O, LSE, w):
+    """Every query row of a bf16 workload against the oracle, the oracle run over worker
+    processes (full-size workloads)."""
+    from tests import oracle_pool
+    p = oracle_problem(w)
+    rows = all_rows(p)
+    spec, arrays = cache_arrays(w)
+    ref = oracle_pool.decode_rows_parallel(p, spec, arrays, bits(w.q), rows)
+    return compare(O, LSE, w, rows, ref=ref)
 
 
 def sample_rows(p, n, seed=0, must=()):

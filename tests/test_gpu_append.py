@@ -270,7 +270,7 @@ def test_full_size_quantized_append_sampled(fmt):
             assert np.array_equal(got, codes)
             assert np.array_equal(gq[..., 0], s) and np.array_equal(gq[..., 1], z)
         else:
-            n_q = quant.kivi_quantized_prefix(T, G, 128)
+            n_q = quant.kivi_quantized_prefix(T, G, p["kivi_residual"])
             for g0 in rng.choice(np.arange(0, n_q, G), size=4, replace=False):
                 x = quant.bf16_bits_to_f32(bits(w.k_rows[row0 + g0: row0 + g0 + G]))   # [G, H, d]
                 codes, s, z = quant.kivi_k_group_quantize(x.transpose(1, 0, 2))

@@ -103,32 +103,45 @@ def test_int4_kivi_verify_rows_cross_the_residual_boundary():
 
 
 @pytest.mark.parametrize("fmt", ["int8", "int4_head", "int4_kivi", "fp8_e4m3", "fp8_e5m2"])
-def test_quantized_full_size_sampled(fmt):
-    """B=32, T ~ U[2048, 32768], K outlier channels: the full quantized workload."""
+def test_quantized_full_size_all_rows(fmt):
+    """B=32, T ~ U[2048, 32768], K outlier channels: the full quantized workload, every
+    query row against the oracle's own cache (written by the oracle's quantiser in worker
+    processes, see ``tests.oracle_pool``)."""
+    from tests import oracle_pool
     w = W.quantized("cuda", fmt=fmt)
     p, cache = append_history(w, fmt, [[] for _ in range(w.problem["B"])])
+    if fmt == "int4_kivi":      # the 128 most recent tokens of every request stay bf16
+        assert p["kivi_residual"] == 160
     O, L, info = _run(w, fmt, p, cache)
-    H.finite_or_masked(O, L)
-    rng = np.random.default_rng(7)
-    reqs = sorted(rng.choice(p["B"], size=4, replace=False).tolist())
-    rows = [(b, 0, h) for b in reqs for h in rng.choice(p["H_q"], size=6, replace=False).tolist()]
-    _compare(O, L, w, p, _oracle_cache(w, fmt, reqs), rows)
+    rows = H.all_rows(p)
+    ks, vs = fp8_scales(w)
+    spec = dict(kind="history", fmt=fmt, H_kv=p["H_kv"], d=p["d"], P=p["P"], G=p["kivi_group"],
+                Gv=p["kivi_v_group"], R=p["kivi_residual"], k_scale=ks, v_scale=vs)
+    i64 = lambda t: t.numpy().astype(np.int64)
+    arrays = dict(k_rows=H.bits(w.k_rows), v_rows=H.bits(w.v_rows), rows_indptr=i64(w.rows_indptr),
+                  page_indptr=i64(w.page_indptr), page_indices=i64(w.page_indices), kv_len=i64(w.kv_len))
+    ref = oracle_pool.decode_rows_parallel(dict(p), spec, arrays, H.bits(w.q), rows)
+    w2 = W.Workload(w.name, p, w.q, w.kv_len)
+    assert H.compare(O, L, w2, rows, ref=ref)["rows"] == 32 * 32
 
 
-@pytest.mark.parametrize("S_q,H_q,H_kv,mask,chunk,num_sms", [
-    (1, 64, 8, "causal", 0, 152),         # 8 rows per kv head
-    (2, 8, 2, "sink_window", 0, 152),     # 8 rows, two-run stages, causal verify rows
-    (2, 8, 2, "sink_window", 50, 4),      # chunks that start inside K groups
-    (1, 16, 8, "sink_window", 64, 3),     # 2 rows
+@pytest.mark.parametrize("S_q,H_q,H_kv,mask,chunk,num_sms,R", [
+    (1, 64, 8, "causal", 0, 152, 160),         # 8 rows per kv head
+    (2, 8, 2, "sink_window", 0, 152, 160),     # 8 rows, two-run stages, causal verify rows
+    (2, 8, 2, "sink_window", 50, 4, 160),      # chunks that start inside K groups
+    (1, 16, 8, "sink_window", 64, 3, 160),     # 2 rows
+    (1, 64, 8, "causal", 64, 7, 64),           # a power-of-two residual ring
+    (2, 8, 2, "sink_window", 0, 152, 96),      # a residual ring of three groups
 ])
-def test_int4_kivi_tensor_core_rows_and_windows(S_q, H_q, H_kv, mask, chunk, num_sms):
+def test_int4_kivi_tensor_core_rows_and_windows(S_q, H_q, H_kv, mask, chunk, num_sms, R):
     """d = 128, Gv = 32, at most 8 rows: K groups that straddle 16-key blocks
     (window starts off the group grid), stages of two runs touching up to ten
-    groups, residual-only and just-closed-group requests."""
+    groups, residual-only and just-closed-group requests, residual rings of
+    several lengths R."""
     lens = [2000, 1999, 1777, 300, 129, 7]
     w = W.quantized_history("q4t", B=len(lens), S_q=S_q, H_q=H_q, H_kv=H_kv, d=128, lens=lens, P=16, seed=26,
                             device="cuda", fmt="int4_kivi", pool_pages=sum(-(-t // 16) for t in lens) + 3)
-    w.problem = dict(w.problem, mask=mask, n_sink=34, window=1000)
+    w.problem = dict(w.problem, mask=mask, n_sink=34, window=1000, kivi_residual=R)
     p, cache = append_history(w, "int4_kivi", [[900, 1500], [], [1000], [160], [], []])
     O, L, info = _run(w, "int4_kivi", p, cache, chunk_tokens=chunk, num_sms=num_sms)
     assert info["rows"] == S_q * H_q // H_kv

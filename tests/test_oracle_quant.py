@@ -87,6 +87,27 @@ def test_kivi_frontier_replay():
             assert R - G < T - n_q <= R
 
 
+def test_kivi_frontier_keeps_the_newest_128_rows_bf16_at_the_workload_residual():
+    """The quantized workload keeps "the most recent 128 tokens" in bf16: with G = 32
+    and R = 160 the closing loop never quantizes one of the newest 128 rows and never
+    holds more than R residual rows (the ring); past R appends the residual stays in
+    (128, 160], one group of G above the 128 rows it must keep."""
+    import workloads as W
+    G, R = 32, W.KIVI_RESIDUAL
+    assert R == 160
+    for T in range(0, 1200):
+        n_q = quant.kivi_quantized_prefix(T, G, R)
+        resid = T - n_q
+        assert n_q % G == 0 and 0 <= n_q <= T
+        assert resid >= min(T, 128)                      # rows T-128 .. T-1 stay bf16
+        assert resid <= R                                # the ring of R rows holds them
+        if T > R:
+            assert 128 < resid <= 128 + G                # at most one group above the 128 kept rows
+    w = W.quantized_history("kivi", B=2, S_q=1, H_q=4, H_kv=1, d=64, lens=[200, 33], P=16, seed=0,
+                            device="cpu", fmt="int4_kivi")
+    assert w.problem["kivi_residual"] == R
+
+
 def test_quantized_cache_round_trip():
     rng = np.random.default_rng(23)
     lens = [300, 129, 40]

@@ -26,6 +26,9 @@ Recipe (shapes and distributions of the five workloads):
    uniform in [2048, 32768]; K, V ~ N(0,1) bf16 with 4 K outlier channels
    per kv head scaled by 8; 16-token pages; the history is handed over as
    packed ragged bf16 rows for the cache writer (kv_append) to encode.
+   KIVI INT4: K groups of 32 tokens, V groups of 32 channels; the residual
+   length R = 160 = 128 + G of the group-closing loop keeps the residual in
+   (128, 160] rows, so the 128 most recent tokens always stay bf16.
 
 Everywhere: Q ~ N(0,1) bf16 of shape [B, S_q, H_q, d]; metadata (lengths,
 permutations, outlier channels, index lists) is drawn on the CPU from
@@ -42,6 +45,11 @@ from dataclasses import dataclass, field
 import torch
 
 NAN_BF16 = float("nan")
+
+# KIVI residual length R of the quantized workload: the group-closing loop
+# (close the oldest 32 rows while more than R are in bf16) then never leaves
+# fewer than 129 bf16 rows, so the 128 most recent tokens are never quantized.
+KIVI_RESIDUAL = 160
 
 
 @dataclass
@@ -175,7 +183,7 @@ def quantized_history(name, *, B, S_q, H_q, H_kv, d, lens, P, seed, device, fmt,
     rows_indptr[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
     problem = dict(B=B, S_q=S_q, H_q=H_q, H_kv=H_kv, d=d, layout="paged", fmt=fmt, P=P,
                    num_pages=pool_pages, mask="causal", kivi_group=32, kivi_v_group=32,
-                   kivi_residual=128)
+                   kivi_residual=KIVI_RESIDUAL)
     meta_out = {"outlier_channels": och, "seed": seed}
     if fmt in ("fp8_e4m3", "fp8_e5m2"):
         # per-head scales from a calibration pass over the history: max |x| / largest finite (fp32)
