@@ -444,6 +444,8 @@ def dattn_step_host_submit(problem, io: HostStep, cache: Tensors, staging, works
     """Enqueue one decode step from host memory and return at once; ``done_event`` (a
     torch.cuda.Event) is recorded after its output transfer (see dattn.h)."""
     prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    if not done_event.cuda_event:      # torch creates the CUDA event at its first record
+        done_event.record(stream if stream is not None else None)
     _check(load().dattn_step_host_submit(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache),
                                          staging.data_ptr(), staging.numel(), workspace.data_ptr(),
                                          workspace.numel(), _stream_ptr(stream), done_event.cuda_event),

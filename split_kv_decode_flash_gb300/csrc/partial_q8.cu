@@ -58,7 +58,8 @@ struct Q8 {
   static constexpr int kQp = kQK * 4;              // one tensor's (s, z) pairs
   static constexpr int kStage = 2 * kTile + 2 * kQp;
   static constexpr int kPos = kStagesN * kStage;   // int32 [stages][kQK]
-  static constexpr int kFlags = kPos + kStagesN * kQK * 4;
+  static constexpr int kVis = kPos + kStagesN * kQK * 4;   // uint32 [stages][kQK]: FlashMask row bits
+  static constexpr int kFlags = kVis + kStagesN * kQK * 4;
   static constexpr int kSeq = kFlags + kStagesN * 4;
   static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
@@ -110,7 +111,7 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
 
 // ---- producer ---------------------------------------------------------------------------
 
-template <int D, int FMT>
+template <int D, int FMT, bool FM>
 __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
   using C = Q8<D>;
   const PartialParams& p = w.p;
@@ -135,10 +136,10 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool 
   const SlotKeys<kQS> k0 = slot_keys<kQS>(w, c0, lane);
   SlotKeys<kQS> k1 = slot_keys<kQS>(w, c1, lane);
   dependency_wait(dep_wait);   // the page table is a device input
-  const SlotPages<kQS> g0 = slot_pages<kQS>(w, c0, k0);
-  SlotPages<kQS> g1 = slot_pages<kQS>(w, c1, k1);
+  const SlotPages<kQS, FM> g0 = slot_pages<kQS, FM>(w, c0, k0);
+  SlotPages<kQS, FM> g1 = slot_pages<kQS, FM>(w, c1, k1);
   SlotKeys<kQS> k2 = slot_keys<kQS>(w, c2, lane);
-  SlotRows<kQS> r0 = slot_rows<kQS>(w, c0, k0, g0, lane);
+  SlotRows<kQS, FM> r0 = slot_rows<kQS, FM>(w, c0, k0, g0, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
@@ -147,6 +148,11 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool 
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kQK;
 #pragma unroll
     for (int h = 0; h < kQS; ++h) pos[lane + 32 * h] = r0.t[h];
+    if constexpr (FM) {
+      uint32_t* vis = reinterpret_cast<uint32_t*>(smem + C::kVis) + st * kQK;
+#pragma unroll
+      for (int h = 0; h < kQS; ++h) vis[lane + 32 * h] = r0.vis[h];
+    }
     if (lane == 0) {
       reinterpret_cast<int*>(smem + C::kFlags)[st] = r0.full ? kFlagFull : 0;
       reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
@@ -178,9 +184,9 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool 
     __syncwarp();
     if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
 
-    r0 = slot_rows<kQS>(w, c1, k1, g1, lane);
+    r0 = slot_rows<kQS, FM>(w, c1, k1, g1, lane);
     c0 = c1;
-    g1 = slot_pages<kQS>(w, c2, k2);
+    g1 = slot_pages<kQS, FM>(w, c2, k2);
     k1 = k2;
     c1 = c2;
     pc_advance<kQK>(w, c2, kProducerWarps);
@@ -284,15 +290,18 @@ struct QRows {
   float qsum0, qsum1, fac0, fac1;
 };
 
+// rec: the item's record; its request's query rows are packed rows rec.qo ..
+// rec.qo + rec.nq - 1 (a mixed batch, M4.5 §0x08F), and rows past g rec.nq are zero.
 template <int D>
-__device__ __forceinline__ void load_q8(const PartialParams& p, const WorkItem& it, int r0, int r1, int t4,
+__device__ __forceinline__ void load_q8(const PartialParams& p, const ItemRec& rec, int r0, int r1, int t4,
                                         QRows<D>& q) {
   constexpr int KS = D / 16;
-  const bool ok0 = r0 < p.rows, ok1 = r1 < p.rows;
+  const WorkItem& it = rec.it;
+  const bool ok0 = r0 < p.g * rec.nq, ok1 = r1 < p.g * rec.nq;
   const __nv_bfloat16* q0 = static_cast<const __nv_bfloat16*>(p.q) +
-                            ((static_cast<long long>(it.b) * p.S_q + r0 / p.g) * p.H_q + it.h * p.g + r0 % p.g) * D;
+                            ((static_cast<long long>(rec.qo) + r0 / p.g) * p.H_q + it.h * p.g + r0 % p.g) * D;
   const __nv_bfloat16* q1 = static_cast<const __nv_bfloat16*>(p.q) +
-                            ((static_cast<long long>(it.b) * p.S_q + r1 / p.g) * p.H_q + it.h * p.g + r1 % p.g) * D;
+                            ((static_cast<long long>(rec.qo) + r1 / p.g) * p.H_q + it.h * p.g + r1 % p.g) * D;
   float v0[KS][4], v1[KS][4];
   float mx0 = 0.f, mx1 = 0.f, s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -341,11 +350,11 @@ __device__ __forceinline__ void load_q8(const PartialParams& p, const WorkItem& 
 // the result multiplied by vsc (FP8: the head's V scale, kept out of the f16
 // probabilities so that they stay in f16's normal range).
 template <int D>
-__device__ __forceinline__ void emit_row_q8(const PartialParams& p, const WorkItem& it, int my_state, int row, float m,
-                                            float l, float z, float bias, float vsc, const float (&o)[D / 8][4],
-                                            int half, int t4) {
+__device__ __forceinline__ void emit_row_q8(const PartialParams& p, const WorkItem& it, int qo, int my_state, int row,
+                                            float m, float l, float z, float bias, float vsc,
+                                            const float (&o)[D / 8][4], int half, int t4) {
   const int i = row / p.g, hq = it.h * p.g + row % p.g;
-  const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
+  const long long orow = (static_cast<long long>(qo) + i) * p.H_q + hq;
   const float add = z - bias;
   if (it.slot < 0) {
     const float inv = l > 0.f ? vsc / l : 0.f;
@@ -391,20 +400,22 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
   const int keys_per_warp = kQK / (wps / nrb);     // 32
   const int g4 = lane >> 2, t4 = lane & 3;
   const int r0 = rb * 16 + g4, r1 = r0 + 8;
-  const bool ok0 = r0 < p.rows, ok1 = r1 < p.rows;
   const int qi0 = r0 / p.g, qi1 = r1 / p.g;
   const int lrow = lane & 7, lmat = lane >> 3;   // ldmatrix address roles
   const float sc = p.scale_log2;
+  const bool fm = p.mask == DATTN_MASK_FLASHMASK;
 
   uint32_t k = 0;
   bool dead = false;
   QRows<D> qn;
-  if (w.begin < w.end) load_q8<D>(p, w.rec(w.begin).it, r0, r1, t4, qn);
+  if (w.begin < w.end) load_q8<D>(p, w.rec(w.begin), r0, r1, t4, qn);
   for (int ii = w.begin; ii < w.end; ++ii) {
-    const WorkItem it = w.rec(ii).it;
-    const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+    const ItemRec rec = w.rec(ii);
+    const WorkItem it = rec.it;
+    const MaskCtx mc{p.mask, rec.nq, it.T, p.n_sink, p.window};
+    const bool ok0 = r0 < p.g * rec.nq, ok1 = r1 < p.g * rec.nq;   // rows of the request
     const QRows<D> q = qn;
-    if (ii + 1 < w.end) load_q8<D>(p, w.rec(ii + 1).it, r0, r1, t4, qn);
+    if (ii + 1 < w.end) load_q8<D>(p, w.rec(ii + 1), r0, r1, t4, qn);
     float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given); INT8: 1
     if constexpr (FMT != DATTN_FMT_INT8_TOKEN) {
       if (p.kqp) hk = static_cast<const float*>(p.kqp)[it.h];
@@ -434,6 +445,7 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
         break;
       }
       const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kQK;
+      const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kQK;
       const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
       const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
       const uint32_t* kqp = reinterpret_cast<const uint32_t*>(smem + st * C::kStage + 2 * C::kTile);
@@ -469,8 +481,15 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
             vs[nt][e] = vq.x;
             vz[nt][e] = vq.y;
             const float off = fmaf(-Codes<FMT>::kBias, ks.x, ks.y);
-            const bool v0 = t >= 0 && ok0 && (full || key_visible(mc, qi0, t));
-            const bool v1 = t >= 0 && ok1 && (full || key_visible(mc, qi1, t));
+            bool v0, v1;
+            if (fm) {   // FlashMask: the producer's row bits of the column
+              const uint32_t bits = vis[slot];
+              v0 = t >= 0 && ok0 && (full || ((bits >> qi0) & 1u));
+              v1 = t >= 0 && ok1 && (full || ((bits >> qi1) & 1u));
+            } else {
+              v0 = t >= 0 && ok0 && (full || key_visible(mc, qi0, t));
+              v1 = t >= 0 && ok1 && (full || key_visible(mc, qi1, t));
+            }
             s[nt][e] = v0 ? sc * fmaf(ks.x * q.fac0, s[nt][e], off * q.qsum0) : -INFINITY;
             s[nt][2 + e] = v1 ? sc * fmaf(ks.x * q.fac1, s[nt][2 + e], off * q.qsum1) : -INFINITY;
           }
@@ -548,8 +567,8 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
       b1 += __shfl_xor_sync(kAll, b1, x);
     }
     if (!dead) {
-      if (ok0) emit_row_q8<D>(p, it, my_state, r0, m0, l0, z0, Codes<FMT>::kBias * b0, hv, o, 0, t4);
-      if (ok1) emit_row_q8<D>(p, it, my_state, r1, m1, l1, z1, Codes<FMT>::kBias * b1, hv, o, 1, t4);
+      if (ok0) emit_row_q8<D>(p, it, rec.qo, my_state, r0, m0, l0, z0, Codes<FMT>::kBias * b0, hv, o, 0, t4);
+      if (ok1) emit_row_q8<D>(p, it, rec.qo, my_state, r1, m1, l1, z1, Codes<FMT>::kBias * b1, hv, o, 1, t4);
     }
   }
 }
@@ -580,11 +599,13 @@ struct QCols {
 };
 
 template <int D>
-__device__ __forceinline__ void load_q8_cols(const PartialParams& p, const WorkItem& it, int g4, int t4, QCols<D>& q) {
+__device__ __forceinline__ void load_q8_cols(const PartialParams& p, const ItemRec& rec, int g4, int t4,
+                                             QCols<D>& q) {
   constexpr int KS = D / 16;
-  const bool ok = g4 < p.rows;
+  const WorkItem& it = rec.it;
+  const bool ok = g4 < p.g * rec.nq;
   const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(p.q) +
-                            ((static_cast<long long>(it.b) * p.S_q + g4 / p.g) * p.H_q + it.h * p.g + g4 % p.g) * D;
+                            ((static_cast<long long>(rec.qo) + g4 / p.g) * p.H_q + it.h * p.g + g4 % p.g) * D;
   float v[KS][4];
   float mx = 0.f, sum = 0.f;
 #pragma unroll
@@ -635,20 +656,22 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
   const int keys_per_warp = kQK / wps;          // 32
   const int g4 = lane >> 2, t4 = lane & 3;
   const int ra = 2 * t4, rb = 2 * t4 + 1;       // the lane's accumulator rows
-  const bool oka = ra < p.rows, okb = rb < p.rows;
   const int qia = ra / p.g, qib = rb / p.g;
   const int lrow = lane & 7, lmat = lane >> 3;
   const float sc = p.scale_log2;
+  const bool fm = p.mask == DATTN_MASK_FLASHMASK;
 
   uint32_t k = 0;
   bool dead = false;
   QCols<D> qn;
-  if (w.begin < w.end) load_q8_cols<D>(p, w.rec(w.begin).it, g4, t4, qn);
+  if (w.begin < w.end) load_q8_cols<D>(p, w.rec(w.begin), g4, t4, qn);
   for (int ii = w.begin; ii < w.end; ++ii) {
-    const WorkItem it = w.rec(ii).it;
-    const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+    const ItemRec rec = w.rec(ii);
+    const WorkItem it = rec.it;
+    const MaskCtx mc{p.mask, rec.nq, it.T, p.n_sink, p.window};
+    const bool oka = ra < p.g * rec.nq, okb = rb < p.g * rec.nq;   // rows of the request
     const QCols<D> q = qn;
-    if (ii + 1 < w.end) load_q8_cols<D>(p, w.rec(ii + 1).it, g4, t4, qn);
+    if (ii + 1 < w.end) load_q8_cols<D>(p, w.rec(ii + 1), g4, t4, qn);
     float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given); INT8: 1
     if constexpr (FMT != DATTN_FMT_INT8_TOKEN) {
       if (p.kqp) hk = static_cast<const float*>(p.kqp)[it.h];
@@ -680,6 +703,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
         break;
       }
       const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kQK;
+      const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kQK;
       const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
       const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
       const uint32_t* kqp = reinterpret_cast<const uint32_t*>(smem + st * C::kStage + 2 * C::kTile);
@@ -710,10 +734,19 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
         const float2 vqx = kI8 ? half2_bits_to_float2(vqp[kx]) : make_float2(1.f, 0.f);
         const float2 vqy = kI8 ? half2_bits_to_float2(vqp[ky]) : make_float2(1.f, 0.f);
         const float offx = fmaf(-Codes<FMT>::kBias, ksx.x, ksx.y), offy = fmaf(-Codes<FMT>::kBias, ksy.x, ksy.y);
-        const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
-        const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
-        const bool vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
-        const bool vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
+        bool vxa, vxb, vya, vyb;
+        if (fm) {   // FlashMask: the producer's row bits of the columns
+          const uint32_t bx = vis[kx], by = vis[ky];
+          vxa = tx >= 0 && oka && (full || ((bx >> qia) & 1u));
+          vxb = tx >= 0 && okb && (full || ((bx >> qib) & 1u));
+          vya = ty >= 0 && oka && (full || ((by >> qia) & 1u));
+          vyb = ty >= 0 && okb && (full || ((by >> qib) & 1u));
+        } else {
+          vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
+          vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
+          vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
+          vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
+        }
         s[0] = vxa ? sc * fmaf(ksx.x * q.fac0, s[0], offx * q.qsum0) : -INFINITY;
         s[1] = vxb ? sc * fmaf(ksx.x * q.fac1, s[1], offx * q.qsum1) : -INFINITY;
         s[2] = vya ? sc * fmaf(ksy.x * q.fac0, s[2], offy * q.qsum0) : -INFINITY;
@@ -788,7 +821,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
         const float m = rr ? mb : ma, l = rr ? lb : la;
         const float add = (rr ? zb : za) - Codes<FMT>::kBias * (rr ? bb : ba);
         const int i = row / p.g, hq = it.h * p.g + row % p.g;
-        const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
+        const long long orow = (static_cast<long long>(rec.qo) + i) * p.H_q + hq;
         if (it.slot < 0) {
           const float inv = l > 0.f ? hv / l : 0.f;
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
@@ -835,8 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ8ProducerRegs));
-    if (runs_apply<kQK>(p)) produce_q8_runs<D, FMT>(w, smem, lane, warp - kConsumerWarps, !complete_now);
-    else produce_q8<D, FMT>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    if (p.mask == DATTN_MASK_FLASHMASK) produce_q8<D, FMT, true>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    else if (runs_apply<kQK>(p)) produce_q8_runs<D, FMT>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    else produce_q8<D, FMT, false>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ8ConsumerRegs));

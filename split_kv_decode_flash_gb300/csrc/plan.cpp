@@ -64,8 +64,9 @@ void check_problem(const dattn_problem* p, Checker& c) {
   }
   if (p->fmt < DATTN_FMT_BF16 || p->fmt > DATTN_FMT_INT4_HEAD) c.fail(DATTN_EINVAL, "unknown format");
   if (p->mask < DATTN_MASK_CAUSAL || p->mask > DATTN_MASK_FLASHMASK) c.fail(DATTN_EINVAL, "unknown mask");
-  if (p->mask == DATTN_MASK_FLASHMASK && p->fmt != DATTN_FMT_BF16)
-    c.fail(DATTN_EUNSUPPORTED, "flashmask runs on bf16 K/V");
+  if (p->mask == DATTN_MASK_FLASHMASK && p->fmt != DATTN_FMT_BF16 && p->fmt != DATTN_FMT_INT8_TOKEN &&
+      p->fmt != DATTN_FMT_FP8_E4M3 && p->fmt != DATTN_FMT_FP8_E5M2)
+    c.fail(DATTN_EUNSUPPORTED, "flashmask runs on bf16, INT8 and FP8 K/V");
   // K/V rows (one kv head, one token) are addressed with 32-bit row indices
   const long long kMaxPoolRows = 0xFFFFFFFFll;
   if (p->layout == DATTN_KV_PAGED_HND) {
@@ -237,8 +238,9 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
                                  " query rows; 0 <= C_b <= S_q");
       mixed = mixed || cb != p.S_q;
     }
-    if (mixed && p.fmt != DATTN_FMT_BF16)
-      c.fail(DATTN_EUNSUPPORTED, "mixed query-row counts run on bf16 K/V");
+    if (mixed && p.fmt != DATTN_FMT_BF16 && p.fmt != DATTN_FMT_INT8_TOKEN && p.fmt != DATTN_FMT_FP8_E4M3 &&
+        p.fmt != DATTN_FMT_FP8_E5M2)
+      c.fail(DATTN_EUNSUPPORTED, "mixed query-row counts run on bf16, INT8 and FP8 K/V");
   }
   if (p.mask == DATTN_MASK_FLASHMASK) {
     long long keys = 0;

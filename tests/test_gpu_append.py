@@ -213,7 +213,8 @@ def test_kivi_append_groups_residual_bit_exact(d, P):
     ref = oracle_written(w, "int4_kivi")
     got = {n: cache[n].cpu() for n in ("k", "v", "k_qparams", "v_qparams")}
     kres, vres = bits(cache["k_residual"]), bits(cache["v_residual"])
-    G, R = 32, 128
+    G, R = p["kivi_group"], p["kivi_residual"]
+    assert R == 160
     for b, t, pg, r in _visible_rows(w):
         T = len(t)
         n_q = quant.kivi_quantized_prefix(T, G, R)

@@ -238,3 +238,86 @@ def test_quantized_bounds_check_flags_out_of_pool_page(fmt):
     torch.cuda.synchronize()
     assert dattn.dattn_device_status(ws) & 1            # kStPageRange
     _compare(o.float().cpu(), lse.cpu(), w, p, _oracle_cache(w, fmt), [(1, 0, h) for h in range(8)])
+
+
+# ---- mixed batches and FlashMask columns on INT8 / FP8 codes (M4.5 §0x08F, §0x06A-§0x06D) ----
+
+def _packed_run(w, fmt, p, cache, qo_indptr=None, **plan_kw):
+    """dattn_run with the query, O and LSE packed by qo_indptr (uniform when None)."""
+    H_q, d = p["H_q"], p["d"]
+    n_rows = p["B"] * p["S_q"] if qo_indptr is None else int(qo_indptr[-1])
+    plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, qo_indptr=qo_indptr, **plan_kw)
+    o = torch.full((n_rows, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((n_rows, H_q), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(256, plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+    dattn.dattn_run(plan, p, dattn.tensors_from(q=w.q.cuda().reshape(n_rows, H_q, d), o=o, lse=lse, **cache), ws)
+    torch.cuda.synchronize()
+    assert dattn.dattn_device_status(ws) == 0
+    if qo_indptr is None:
+        return o.float().cpu().reshape(p["B"], p["S_q"], H_q, d), lse.cpu().reshape(p["B"], p["S_q"], H_q)
+    return o.float().cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("H_q,H_kv,chunk,num_sms", [(32, 8, 64, 7), (32, 8, 0, 152), (8, 8, 64, 5)])
+def test_byte_codes_mixed_batch_all_rows(fmt, H_q, H_kv, chunk, num_sms):
+    """Prefill, append, decode and idle requests in one launch over INT8 / FP8 codes: 32 rows
+    per kv head for the widest request (two 16-row tiles) and 8 (keys on the mma M side)."""
+    TC = [(0, 8), (130, 1), (0, 1), (65, 3), (7, 0), (300, 8), (1, 2), (64, 5), (200, 1)]
+    lens = [t + c for t, c in TC]
+    w = W.quantized_history("mixq", B=len(TC), S_q=8, H_q=H_q, H_kv=H_kv, d=128, lens=lens, P=16, seed=51,
+                            device="cuda", fmt=fmt, pool_pages=sum(-(-t // 16) for t in lens) + 2)
+    qo = np.concatenate([[0], np.cumsum([c for _, c in TC])]).astype(np.int32)
+    gen = torch.Generator(device="cuda").manual_seed(52)
+    w.q = torch.randn((int(qo[-1]), H_q, 128), generator=gen, device="cuda").to(torch.bfloat16)
+    p, cache = append_history(w, fmt, [[] for _ in TC])
+    O, L = _packed_run(w, fmt, p, cache, qo_indptr=qo, chunk_tokens=chunk, num_sms=num_sms)
+    w2 = W.Workload(w.name, p, w.q, w.kv_len, qo_indptr=torch.tensor(qo))
+    assert H.compare(O, L, w2, cache=_oracle_cache(w, fmt))["rows"] == int(qo[-1]) * H_q
+
+
+@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("S_q,H_q,H_kv", [(4, 16, 2), (3, 16, 4), (8, 8, 8), (2, 8, 2)])
+def test_byte_codes_flashmask_random_intervals(fmt, S_q, H_q, H_kv):
+    """FlashMask two-interval columns over INT8 / FP8 codes: columns hidden from every row,
+    columns every row sees, and a request whose only key is hidden; 32, 12 and 8 rows."""
+    from tests.test_gpu_decode import _random_fm_intervals
+    lens = [300, 65, 1, 0, 130]
+    w = W.quantized_history("fmq", B=len(lens), S_q=S_q, H_q=H_q, H_kv=H_kv, d=128, lens=lens, P=16, seed=53,
+                            device="cuda", fmt=fmt, pool_pages=sum(-(-t // 16) for t in lens) + 2)
+    rng = np.random.default_rng(54 + S_q)
+    iv = _random_fm_intervals(rng, lens, S_q)
+    iv[sum(lens[:2])] = [0, S_q, 0, 0]                     # request 2: its only key hidden from all rows
+    w.problem = dict(w.problem, mask="flashmask")
+    fm = torch.tensor(iv, dtype=torch.int32)
+    p, cache = append_history(w, fmt, [[] for _ in lens])
+    cache["fm_intervals"] = fm.cuda().contiguous()
+    O, L = _packed_run(w, fmt, p, cache, chunk_tokens=64, num_sms=7)
+    assert torch.isinf(L[2]).all() and (L[2] < 0).all()
+    w2 = W.Workload(w.name, p, w.q, w.kv_len, fm_intervals=fm)
+    H.compare(O, L, w2, cache=_oracle_cache(w, fmt))
+
+
+@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3"])
+def test_byte_codes_tree_verify_full_size_all_rows(fmt):
+    """The speculative-tree verify workload (B=16, prefixes U[1024, 8192], 8 DFS-ordered draft
+    rows, FlashMask intervals) over INT8 / FP8 codes, every row."""
+    from tests import oracle_pool
+    t = W.tree_verify("cpu")
+    w = W.quantized_history("treeq", B=16, S_q=8, H_q=32, H_kv=8, d=128, lens=t.kv_len.tolist(), P=16, seed=55,
+                            device="cuda", fmt=fmt)
+    w.problem = dict(w.problem, mask="flashmask")
+    p, cache = append_history(w, fmt, [[] for _ in range(16)])
+    cache["fm_intervals"] = t.fm_intervals.cuda().contiguous()
+    O, L = _packed_run(w, fmt, p, cache)
+    w2 = W.Workload(w.name, p, w.q, w.kv_len, fm_intervals=t.fm_intervals)
+    prob = H.oracle_problem(w2)
+    rows = H.all_rows(prob)
+    ks, vs = fp8_scales(w)
+    spec = dict(kind="history", fmt=fmt, H_kv=p["H_kv"], d=p["d"], P=p["P"], G=p["kivi_group"],
+                Gv=p["kivi_v_group"], R=p["kivi_residual"], k_scale=ks, v_scale=vs)
+    i64 = lambda x: x.numpy().astype(np.int64)
+    arrays = dict(k_rows=H.bits(w.k_rows), v_rows=H.bits(w.v_rows), rows_indptr=i64(w.rows_indptr),
+                  page_indptr=i64(w.page_indptr), page_indices=i64(w.page_indices), kv_len=i64(w.kv_len))
+    ref = oracle_pool.decode_rows_parallel(prob, spec, arrays, H.bits(w.q), rows)
+    assert H.compare(O, L, w2, rows, ref=ref)["rows"] == 16 * 8 * 32

@@ -291,13 +291,17 @@ def test_mixed_batch_validation():
         dattn.dattn_plan(prob, T, qo_indptr=np.array([0, 5, 6, 7], np.int32), num_sms=4)
     with pytest.raises(dattn.DattnError, match="0 <= C_b"):
         dattn.dattn_plan(prob, T, qo_indptr=np.array([0, 2, 1, 3], np.int32), num_sms=4)
-    q8 = _problem(B=3, S_q=4, fmt="int8")
+    # non-uniform C_b: bf16, INT8 and FP8 codes; the INT4 formats take uniform batches only
+    for fmt in ("int8", "fp8_e4m3", "fp8_e5m2"):
+        dattn.dattn_plan(_problem(B=3, S_q=4, fmt=fmt), T, page_indptr=np.array([0, 1, 2, 3], np.int32),
+                         qo_indptr=np.array([0, 1, 2, 4], np.int32), num_sms=4)
+    q4 = _problem(B=3, S_q=4, fmt="int4_head")
     with pytest.raises(dattn.DattnError) as e:
-        dattn.dattn_plan(q8, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
+        dattn.dattn_plan(q4, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
                          qo_indptr=np.array([0, 1, 2, 4], np.int32), num_sms=4)
     assert dattn.STATUS[e.value.status] == "DATTN_EUNSUPPORTED"
     # a uniform qo_indptr is the plain batch, for every format
-    dattn.dattn_plan(q8, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
+    dattn.dattn_plan(q4, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
                      qo_indptr=np.array([0, 4, 8, 12], np.int32), num_sms=4)
 
 
