@@ -514,6 +514,50 @@ def kernel_pass(step, K):
     return statistics.mean(part), statistics.mean(merge)
 
 
+def timeline(step, n_steps=40, skip=10):
+    """Per-step phases from the kernels' %globaltimer trace (bf16 K/V; dattn_run_options.trace):
+    medians over steps of each phase in µs.  Steps run back to back as in the timed region."""
+    import numpy as np
+    import torch
+    if step.p.get("fmt", "bf16") != "bf16":
+        return None
+    info = step.info
+    n_ctas, words_m = info["n_ctas"], 2 * info["n_merge_groups"] * info["rows"]
+    words = 16 * n_ctas + words_m
+    buf = torch.zeros((n_steps, words), dtype=torch.int64, device=step.ws.device)
+    torch.cuda.synchronize()
+    for k in range(n_steps):
+        step.dattn.dattn_run_ex(step.plan, step.p, step.t, step.ws, reuse_upload=True, trace=buf[k],
+                                shared_shift=step.shift, stream=step.stream)
+    torch.cuda.synchronize()
+    tr = buf.cpu().numpy().astype(np.float64)
+    rows = []
+    prev_merge_end = None
+    for k in range(n_steps):
+        P = tr[k, :16 * n_ctas].reshape(n_ctas, 16)
+        M = tr[k, 16 * n_ctas:].reshape(-1, 2)
+        M = M[M[:, 0] > 0]
+        live = P[:, 2] > 0                                   # CTAs whose producer passed the wait
+        wait = P[live, 2]
+        end = P[:, 8:16].max(axis=1)
+        merge_start = M[:, 0].min() if len(M) else end.max()
+        merge_end = M[:, 1].max() if len(M) else end.max()
+        if prev_merge_end is not None and k >= skip:
+            rows.append({
+                "wait_after_prev_step_us": (np.median(wait) - prev_merge_end) / 1e3,
+                "first_copy_after_wait_us": np.median(P[live, 3] - wait) / 1e3,
+                "first_stage_after_wait_us": np.median(P[live & (P[:, 4] > 0), 4] - P[live & (P[:, 4] > 0), 2]) / 1e3,
+                "stream_median_cta_us": (np.median(end) - np.median(wait)) / 1e3,
+                "tail_last_cta_us": (end.max() - np.median(end)) / 1e3,
+                "cta_end_spread_p5_p95_us": (np.percentile(end, 95) - np.percentile(end, 5)) / 1e3,
+                "merge_wait_after_last_cta_us": (merge_start - end.max()) / 1e3,
+                "merge_us": (merge_end - merge_start) / 1e3,
+                "period_us": (merge_end - prev_merge_end) / 1e3,
+            })
+        prev_merge_end = merge_end
+    return {k: float(np.median([r[k] for r in rows])) for k in rows[0]} if rows else None
+
+
 # ---- the two arms ---------------------------------------------------------------------
 
 def run_reference(args):
@@ -602,6 +646,7 @@ def config_line(dattn, name, dev, num_sms, steps, cpu=True):
     assert step.status() == 0, f"device bounds check fired ({name})"
     samples, total_ms = timed_samples(step, steps, 20)
     part_us, merge_us = kernel_pass(step, min(200, steps))
+    tl = timeline(step)
     nb = stream_bytes(p, step.info, w.kv_len.tolist())
     peak, _ = measured_peak()
     s = summary(samples)
@@ -613,6 +658,8 @@ def config_line(dattn, name, dev, num_sms, steps, cpu=True):
            "merge_share": merge_us / (part_us + merge_us) if step.merges else 0.0,
            "kernel_event_pass_us": {"partial": part_us, "merge": merge_us},
            "gpu_launches_per_step": 1 + step.merges}
+    if tl:
+        out["timeline"] = tl
     if cpu:
         try:
             with tempfile.TemporaryDirectory() as td:
@@ -659,6 +706,7 @@ def run_ours(args):
     K = args.steps
     samples, total_ms = timed_samples(step, K, max(3, args.warmup), world)
     part_us, merge_us = kernel_pass(step, min(K, 500))
+    tl = timeline(step)
     ck = clocks.stop()
     ms_step = max_over_ranks(total_ms / K, world)
     s = summary(samples)
@@ -703,6 +751,8 @@ def run_ours(args):
                      "duration": "the median step of the headline region (an upper bound of the partial "
                                  "kernel's duration: the step also holds the merge's tail)",
                      "event_pass_frac": ab["partial"] / (part_us * 1e-6) / 1e9 / peak},
+        "timeline": dict(tl or {}, what="medians over steps of the kernels' %globaltimer trace in a pass of "
+                                         "back-to-back steps after the timed region (dattn_run_options.trace)"),
         "clocks": ck,
         "gpu_launches": K * (1 + step.merges),
     }
@@ -763,13 +813,14 @@ def run_other(args):
     samples, total_ms = timed_samples(step, max(MIN_SAMPLES, args.steps), max(3, args.warmup))
     s = summary(samples)
     fallbacks = dattn.dattn_shift_fallbacks(step.ws, step.stream) if args.shared_shift else None
+    tl = timeline(step)
     nb = stream_bytes(p, step.info, w.kv_len.tolist())
     peak, peak_src = measured_peak()
     print(json.dumps({"workload": w.name, "us_per_step": total_ms * 1e3 / max(MIN_SAMPLES, args.steps),
                       "us_per_step_samples": s, "kv_bytes_per_step": nb, "GBps": nb / s["median"] / 1e3,
                       "frac": nb / s["median"] / 1e3 / peak, "peak": peak, "peak_source": peak_src,
                       "rows": step.info["rows"], "n_items": step.info["n_items"], "steps": args.steps,
-                      "shared_shift": _shift(args), "shift_fallbacks": fallbacks,
+                      "shared_shift": _shift(args), "shift_fallbacks": fallbacks, "timeline": tl,
                       "timing": "CUDA events around K back-to-back decode steps (partial + merge); GBps and "
                                 "frac from the median per-step sample"}), flush=True)
 

@@ -304,6 +304,14 @@ typedef struct {
                                (0: 2 s).  A wait that runs out stops its CTA, sets the
                                timeout bit (16) of the device status word, and the merge
                                then writes no output row (fail closed)                     */
+  void* trace;        /* NULL, or (bf16 K/V) a device uint64 array of at least
+                         16 n_ctas + 2 n_merge_groups rows words (zeroed by the caller):
+                         %globaltimer stamps in ns.  Partial CTA c writes words
+                         16 c + {0: entry, 1: records read, 2: producer warp 0 past
+                         the wait for the preceding grid, 3: its first stage's copies
+                         issued, 4: the first stage landed for consumer warp 0,
+                         8 + w: consumer warp w done}; merge block j then writes
+                         16 n_ctas + 2 j (past its wait) and + 2 j + 1 (done)        */
 } dattn_run_options;
 
 /* Number of consumer warps that left the shared-shift frame (guard failed) since the work

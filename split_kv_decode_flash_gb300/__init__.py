@@ -82,7 +82,7 @@ class WorkItem(ctypes.Structure):
 class RunOptions(ctypes.Structure):
     _fields_ = [("flags", ctypes.c_uint32), ("events", ctypes.c_void_p * 3),
                 ("shift_phi", ctypes.c_float), ("shift_lo", ctypes.c_float), ("shift_hi", ctypes.c_float),
-                ("wait_limit_us", ctypes.c_uint32)]
+                ("wait_limit_us", ctypes.c_uint32), ("trace", ctypes.c_void_p)]
 
 
 RUN_REUSE_UPLOAD = 1
@@ -319,7 +319,7 @@ def dattn_plan_upload(plan: Plan, workspace, stream=None) -> None:
 
 
 def dattn_run_ex(plan: Plan, problem, tensors: Tensors, workspace, *, reuse_upload=False, events=None,
-                 shared_shift=None, wait_limit_us=0, test_skip_arrival=False, stream=None) -> None:
+                 shared_shift=None, wait_limit_us=0, test_skip_arrival=False, trace=None, stream=None) -> None:
     """dattn_run with options: reuse an uploaded work list, record three torch.cuda.Events
     (before the partial kernel, after it, after the merge kernel), ``shared_shift =
     (phi, lo, hi)``: partials in the fixed frame phi, guarded by lo < s - phi < hi,
@@ -329,6 +329,7 @@ def dattn_run_ex(plan: Plan, problem, tensors: Tensors, workspace, *, reuse_uplo
     opt = RunOptions()
     opt.flags = (RUN_REUSE_UPLOAD if reuse_upload else 0) | (RUN_TEST_SKIP_ARRIVAL if test_skip_arrival else 0)
     opt.wait_limit_us = int(wait_limit_us)
+    opt.trace = None if trace is None else trace.data_ptr()
     if shared_shift is not None:
         opt.flags |= RUN_SHARED_SHIFT
         opt.shift_phi, opt.shift_lo, opt.shift_hi = (float(x) for x in shared_shift)

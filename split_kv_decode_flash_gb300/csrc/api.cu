@@ -252,6 +252,8 @@ dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const
   }
   if (opt && opt->wait_limit_us) k.wait_ns = static_cast<uint64_t>(opt->wait_limit_us) * 1000ull;
   k.skip_arrival = skip_arrival ? 1 : 0;
+  uint64_t* trace = opt && prob->fmt == DATTN_FMT_BF16 ? static_cast<uint64_t*>(opt->trace) : nullptr;
+  k.trace = trace;
   if (opt && (opt->flags & DATTN_RUN_REUSE_UPLOAD)) {
     bind_blob(plan, workspace, k);
   } else {
@@ -279,6 +281,7 @@ dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const
     m.S_q = k.S_q;
     m.H_q = k.H_q;
     m.mean_states = plan->info.n_slots / plan->info.n_merge_groups;
+    m.trace = trace ? trace + static_cast<size_t>(plan->info.n_ctas) * kTraceSlots : nullptr;
     const int err = launch_merge(m, prob->d_h, stream);
     if (err != cudaSuccess) return cuda_fail("dattn_run merge kernel", err);
   }

@@ -132,7 +132,17 @@ struct PartialParams {
   int32_t* shift_fallbacks;
   uint64_t wait_ns;       // limit of every bounded mbarrier wait
   int32_t skip_arrival;   // test hook (bf16 kernel): CTA 0 never completes its first stage
+  uint64_t* trace;        // timeline trace (bf16 kernel): kTraceSlots %globaltimer stamps per CTA, or null
 };
+
+// Timeline trace of the bf16 partial kernel: per CTA, kTraceSlots words of
+// %globaltimer (ns): entry, records read, producer warp 0 past the wait for the
+// preceding grid, its first stage's copies issued, the first stage landed for
+// consumer warp 0, and the end of each consumer warp (slots 8 + warp).  The
+// merge kernel follows with two words per block: past its wait, and done.
+enum TraceSlot : int { kTrEntry = 0, kTrRecords = 1, kTrWaitDone = 2, kTrFirstCopy = 3, kTrFirstStage = 4,
+                       kTrConsumerEnd = 8 };
+constexpr int kTraceSlots = 16;
 
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
 
@@ -145,6 +155,7 @@ struct MergeParams {
   int32_t* status;
   int32_t n_groups, rows, g, S_q, H_q;
   int32_t mean_states;   // partial states per merge group, on average (chooses the warps per row)
+  uint64_t* trace;       // two stamps per block (past the wait, done), or null
 };
 
 // Kernel launchers (partial*.cu, merge.cu); return cudaError_t as int.

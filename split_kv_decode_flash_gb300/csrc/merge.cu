@@ -26,6 +26,18 @@ namespace {
 
 constexpr int kMergeWarps = 4;
 
+__device__ __forceinline__ unsigned long long merge_clock_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Timeline trace: the block's time past its wait, and (latest warp) done.
+__device__ __forceinline__ void merge_trace_done(const MergeParams& p, int lane) {
+  if (p.trace && lane == 0)
+    atomicMax(reinterpret_cast<unsigned long long*>(p.trace) + 2 * blockIdx.x + 1, merge_clock_ns());
+}
+
 // WPR = 4: one block of four warps per (group, row); warp w folds states w,
 // w + 4, ... and the four folds combine in shared memory (few rows, many
 // states).  WPR = 1: one warp per (group, row), four rows per block, each
@@ -41,6 +53,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   // a programmatically launched successor may be scheduled; it waits for this grid
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (p.trace && threadIdx.x == 0) p.trace[2 * blockIdx.x] = merge_clock_ns();
   const int blocks_per_group = (p.rows + kRowsPerBlock - 1) / kRowsPerBlock;
   const int gi = blockIdx.x / blocks_per_group;
   const int row = (blockIdx.x % blocks_per_group) * kRowsPerBlock + (WPR > 1 ? 0 : w);
@@ -53,14 +66,21 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   const int i = row / p.g, hq = grp.h * p.g + row % p.g;
   const long long orow = (static_cast<long long>(grp.qo) + i) * p.H_q + hq;
   if constexpr (WPR == 1) {
-    if (row >= p.g * grp.nq) return;   // the request has fewer query rows than the widest one
+    if (row >= p.g * grp.nq) {   // the request has fewer query rows than the widest one
+      merge_trace_done(p, lane);
+      return;
+    }
     RowFold<D> f;
     fold_init(f);
     fold_states<D>(p.ml, p.u, p.rows, row, grp.slot0, grp.n, 1, lane, f);
     if (!fail_closed) write_folded_row<D>(p.o, p.lse, orow, f, lane);
+    merge_trace_done(p, lane);
     return;
   } else {
-    if (row >= p.g * grp.nq) return;
+    if (row >= p.g * grp.nq) {
+      merge_trace_done(p, lane);
+      return;
+    }
     // warp w folds states w, w + kMergeWarps, ...
     RowFold<D> f;
     fold_init(f);
@@ -74,7 +94,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
       sm_ml[w][1] = f.L;
     }
     __syncthreads();
-    if (w != 0) return;
+    if (w != 0) {
+      merge_trace_done(p, lane);
+      return;
+    }
     RowFold<D> t;
     fold_init(t);
 #pragma unroll
@@ -90,6 +113,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
       }
     }
     if (!fail_closed) write_folded_row<D>(p.o, p.lse, orow, t, lane);
+    merge_trace_done(p, lane);
   }
 }
 

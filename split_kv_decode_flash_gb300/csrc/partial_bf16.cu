@@ -95,6 +95,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   SlotKeys<2> k2 = slot_keys<2>(w, c2, lane);
   // Up to here only the plan was read; the page table is a device input.
   dependency_wait(dep_wait);
+  if (pw == 0 && lane == 0) trace_stamp(p, kTrWaitDone);
   const SlotPages<2, FM> g0 = slot_pages<2, FM>(w, c0, k0);     // both stages' page lookups in flight together
   SlotPages<2, FM> g1 = slot_pages<2, FM>(w, c1, k1);
   SlotRows<2, FM> r0 = slot_rows<2, FM, true>(w, c0, k0, g0, lane);
@@ -132,6 +133,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
       __syncwarp();
       if (lane == 0) mbar_arrive(fb);   // publishes pos / flags / stamp; the copies complete the phase
     }
+    if (k == 0 && lane == 0) trace_stamp(p, kTrFirstCopy);
 
     // move the description pipeline one stage of this warp forward
     r0 = slot_rows<2, FM, true>(w, c1, k1, g1, lane);
@@ -169,6 +171,7 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
   RunStage s0 = run_stage(w, c0);
   RunStage s1 = run_stage(w, c1);
   dependency_wait(dep_wait);   // the page table is a device input
+  if (pw == 0 && lane == 0) trace_stamp(p, kTrWaitDone);
   int pid0 = run_stage_page(w, s0, lane);
   int pid1 = run_stage_page(w, s1, lane);
 
@@ -206,6 +209,7 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
       __syncwarp();
       if (lane == 0) mbar_arrive(fb);   // publishes pos / flags / stamp; the copies complete the phase
     }
+    if (k == 0 && lane == 0) trace_stamp(p, kTrFirstCopy);
 
     c0 = c1;
     s0 = s1;
@@ -342,6 +346,7 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
       dead = true;
       break;
     }
+    if (k == 0 && cw == 0 && lane == 0) trace_stamp(p, kTrFirstStage);
     const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kTK;
     const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kTK;
     const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
@@ -635,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may be scheduled now; it waits for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) trace_stamp(p, kTrEntry);
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
   const int incomplete = fill_item_cache(p, cache, it_begin, it_end);
@@ -650,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   // wait.  Otherwise each warp waits on its own, just before its first device
   // read, and the producers set up their first stages' keys in the meantime.
   const bool complete_now = __syncthreads_or(incomplete);
+  if (threadIdx.x == 0) trace_stamp(p, kTrRecords);
   if (complete_now) complete_item_cache(p, cache, it_begin, it_end);
   const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -663,6 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));
   if (p.shift_on) consume_bf16<D, true>(w, smem, warp, lane, !complete_now);
   else consume_bf16<D, false>(w, smem, warp, lane, !complete_now);
+  if (lane == 0) trace_stamp(p, kTrConsumerEnd + warp);
   if (p.fused) fused_merge<D>(w, smem, warp, lane);
 }
 

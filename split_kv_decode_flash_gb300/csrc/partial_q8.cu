@@ -381,7 +381,9 @@ __device__ __forceinline__ void emit_row_q8(const PartialParams& p, const WorkIt
   }
 }
 
-template <int D, int FMT>
+// FM: FlashMask columns (the row bits of each key column from the producer);
+// the other programs are compiled without them.
+template <int D, int FMT, bool FM>
 __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
   using C = Q8<D>;
   constexpr int KS = D / 16;   // k-steps of q.k
@@ -403,17 +405,16 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
   const int qi0 = r0 / p.g, qi1 = r1 / p.g;
   const int lrow = lane & 7, lmat = lane >> 3;   // ldmatrix address roles
   const float sc = p.scale_log2;
-  const bool fm = p.mask == DATTN_MASK_FLASHMASK;
 
   uint32_t k = 0;
   bool dead = false;
   QRows<D> qn;
   if (w.begin < w.end) load_q8<D>(p, w.rec(w.begin), r0, r1, t4, qn);
   for (int ii = w.begin; ii < w.end; ++ii) {
-    const ItemRec rec = w.rec(ii);
-    const WorkItem it = rec.it;
-    const MaskCtx mc{p.mask, rec.nq, it.T, p.n_sink, p.window};
-    const bool ok0 = r0 < p.g * rec.nq, ok1 = r1 < p.g * rec.nq;   // rows of the request
+    const WorkItem it = w.rec(ii).it;
+    const int nq = w.rec(ii).nq;                  // the request's query rows
+    const MaskCtx mc{p.mask, nq, it.T, p.n_sink, p.window};
+    const bool ok0 = r0 < p.g * nq, ok1 = r1 < p.g * nq;
     const QRows<D> q = qn;
     if (ii + 1 < w.end) load_q8<D>(p, w.rec(ii + 1), r0, r1, t4, qn);
     float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given); INT8: 1
@@ -482,7 +483,7 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
             vz[nt][e] = vq.y;
             const float off = fmaf(-Codes<FMT>::kBias, ks.x, ks.y);
             bool v0, v1;
-            if (fm) {   // FlashMask: the producer's row bits of the column
+            if constexpr (FM) {   // FlashMask: the producer's row bits of the column
               const uint32_t bits = vis[slot];
               v0 = t >= 0 && ok0 && (full || ((bits >> qi0) & 1u));
               v1 = t >= 0 && ok1 && (full || ((bits >> qi1) & 1u));
@@ -567,8 +568,9 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
       b1 += __shfl_xor_sync(kAll, b1, x);
     }
     if (!dead) {
-      if (ok0) emit_row_q8<D>(p, it, rec.qo, my_state, r0, m0, l0, z0, Codes<FMT>::kBias * b0, hv, o, 0, t4);
-      if (ok1) emit_row_q8<D>(p, it, rec.qo, my_state, r1, m1, l1, z1, Codes<FMT>::kBias * b1, hv, o, 1, t4);
+      const int qo = w.rec(ii).qo;
+      if (ok0) emit_row_q8<D>(p, it, qo, my_state, r0, m0, l0, z0, Codes<FMT>::kBias * b0, hv, o, 0, t4);
+      if (ok1) emit_row_q8<D>(p, it, qo, my_state, r1, m1, l1, z1, Codes<FMT>::kBias * b1, hv, o, 1, t4);
     }
   }
 }
@@ -639,7 +641,7 @@ __device__ __forceinline__ void load_q8_cols(const PartialParams& p, const ItemR
   q.fac1 = __shfl_sync(kAll, fac, 8 * t4 + 4);
 }
 
-template <int D, int FMT>
+template <int D, int FMT, bool FM>
 __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) {
   using C = Q8<D>;
   constexpr int KS = D / 16;   // k-steps of q.k
@@ -659,17 +661,16 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
   const int qia = ra / p.g, qib = rb / p.g;
   const int lrow = lane & 7, lmat = lane >> 3;
   const float sc = p.scale_log2;
-  const bool fm = p.mask == DATTN_MASK_FLASHMASK;
 
   uint32_t k = 0;
   bool dead = false;
   QCols<D> qn;
   if (w.begin < w.end) load_q8_cols<D>(p, w.rec(w.begin), g4, t4, qn);
   for (int ii = w.begin; ii < w.end; ++ii) {
-    const ItemRec rec = w.rec(ii);
-    const WorkItem it = rec.it;
-    const MaskCtx mc{p.mask, rec.nq, it.T, p.n_sink, p.window};
-    const bool oka = ra < p.g * rec.nq, okb = rb < p.g * rec.nq;   // rows of the request
+    const WorkItem it = w.rec(ii).it;
+    const int nq = w.rec(ii).nq;                  // the request's query rows
+    const MaskCtx mc{p.mask, nq, it.T, p.n_sink, p.window};
+    const bool oka = ra < p.g * nq, okb = rb < p.g * nq;
     const QCols<D> q = qn;
     if (ii + 1 < w.end) load_q8_cols<D>(p, w.rec(ii + 1), g4, t4, qn);
     float hk = 1.f, hv = 1.f;   // FP8: the kv head's scales (1 when not given); INT8: 1
@@ -735,7 +736,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
         const float2 vqy = kI8 ? half2_bits_to_float2(vqp[ky]) : make_float2(1.f, 0.f);
         const float offx = fmaf(-Codes<FMT>::kBias, ksx.x, ksx.y), offy = fmaf(-Codes<FMT>::kBias, ksy.x, ksy.y);
         bool vxa, vxb, vya, vyb;
-        if (fm) {   // FlashMask: the producer's row bits of the columns
+        if constexpr (FM) {   // FlashMask: the producer's row bits of the columns
           const uint32_t bx = vis[kx], by = vis[ky];
           vxa = tx >= 0 && oka && (full || ((bx >> qia) & 1u));
           vxb = tx >= 0 && okb && (full || ((bx >> qib) & 1u));
@@ -814,6 +815,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
       bb += __shfl_xor_sync(kAll, bb, x);
     }
     if (!dead) {
+      const int qo = w.rec(ii).qo;
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const int row = rr ? rb : ra;
@@ -821,7 +823,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
         const float m = rr ? mb : ma, l = rr ? lb : la;
         const float add = (rr ? zb : za) - Codes<FMT>::kBias * (rr ? bb : ba);
         const int i = row / p.g, hq = it.h * p.g + row % p.g;
-        const long long orow = (static_cast<long long>(rec.qo) + i) * p.H_q + hq;
+        const long long orow = (static_cast<long long>(qo) + i) * p.H_q + hq;
         if (it.slot < 0) {
           const float inv = l > 0.f ? hv / l : 0.f;
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
@@ -843,7 +845,9 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
   }
 }
 
-template <int D, int FMT>
+// FM: the FlashMask instance (producers carry each column's row bits), launched
+// only for that program; the other programs run the instance compiled without it.
+template <int D, int FMT, bool FM>
 __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_constant__ PartialParams p) {
   using C = Q8<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -868,23 +872,23 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ8ProducerRegs));
-    if (p.mask == DATTN_MASK_FLASHMASK) produce_q8<D, FMT, true>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    if constexpr (FM) produce_q8<D, FMT, true>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     else if (runs_apply<kQK>(p)) produce_q8_runs<D, FMT>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     else produce_q8<D, FMT, false>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ8ConsumerRegs));
   dependency_wait(!complete_now);   // before Q and the state writes
-  if (p.rows <= 8) consume_q8_swap<D, FMT>(w, smem, warp, lane);
-  else consume_q8<D, FMT>(w, smem, warp, lane);
+  if (p.rows <= 8) consume_q8_swap<D, FMT, FM>(w, smem, warp, lane);
+  else consume_q8<D, FMT, FM>(w, smem, warp, lane);
 }
 
-template <int D, int FMT>
-int launch_q8(const PartialParams& p, int n_ctas, void* stream) {
+template <int D, int FMT, bool FM>
+int launch_q8_inst(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Q8<D>::kTotal;
   // the register budget check and the shared-memory opt-in, once per device
   static std::atomic<unsigned long long> ready{0};
-  cudaError_t err = prepare_kernel_once(partial_q8_kernel<D, FMT>, smem, 128 * kQ8ProducerRegs + 32 * kConsumerWarps * kQ8ConsumerRegs, ready);
+  cudaError_t err = prepare_kernel_once(partial_q8_kernel<D, FMT, FM>, smem, 128 * kQ8ProducerRegs + 32 * kConsumerWarps * kQ8ConsumerRegs, ready);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
@@ -896,8 +900,14 @@ int launch_q8(const PartialParams& p, int n_ctas, void* stream) {
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, partial_q8_kernel<D, FMT>, p);
+  err = cudaLaunchKernelEx(&cfg, partial_q8_kernel<D, FMT, FM>, p);
   return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+template <int D, int FMT>
+int launch_q8(const PartialParams& p, int n_ctas, void* stream) {
+  return p.mask == DATTN_MASK_FLASHMASK ? launch_q8_inst<D, FMT, true>(p, n_ctas, stream)
+                                        : launch_q8_inst<D, FMT, false>(p, n_ctas, stream);
 }
 
 }  // namespace

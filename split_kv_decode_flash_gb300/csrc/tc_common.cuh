@@ -170,6 +170,12 @@ __device__ __forceinline__ uint32_t tile_off(int s, int c) {
   return static_cast<uint32_t>(s * ROWB + ((c ^ (s & kMask)) << 4));
 }
 
+// ---- timeline trace ----------------------------------------------------------------------
+
+__device__ __forceinline__ void trace_stamp(const PartialParams& p, int slot) {
+  if (p.trace) p.trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + slot] = global_ns();
+}
+
 // ---- kernel prologue ----------------------------------------------------------------------
 //
 // The kernels are launched as programmatic dependents: the plan's records may
@@ -250,7 +256,7 @@ struct SlotKeys {
 template <int S, bool FM = false>
 struct SlotPages {
   int pi[S];     // page id of the key's block (-2: block outside the page list)
-  int4 iv[FM ? S : 1];   // FlashMask: the key column's (UTS, UTE, LTS, LTE)
+  uint32_t vis[FM ? S : 1];   // FlashMask: bit i set when query row i sees the key column
 };
 template <int S, bool FM = false>
 struct SlotRows {
@@ -288,15 +294,19 @@ __device__ __forceinline__ SlotPages<S, FM> slot_pages(const Walk& w, const PCur
   for (int h = 0; h < S; ++h) g.pi[h] = -2;
   if constexpr (FM) {
 #pragma unroll
-    for (int h = 0; h < S; ++h) g.iv[h] = make_int4(0, 0, 0, 0);
+    for (int h = 0; h < S; ++h) g.vis[h] = 0u;
   }
   if (c.ii >= w.end) return g;
   const ItemRec r = w.rec(c.ii);
-  if constexpr (FM) {   // the column intervals travel with the page ids
+  if constexpr (FM) {   // the column intervals are loaded with the page ids, kept as the rows that see the key
+    const uint32_t rows = row_bits(0, r.nq);
 #pragma unroll
     for (int h = 0; h < S; ++h) {
       const int t = k.t[h];
-      if (t >= 0 && t < r.it.T) g.iv[h] = *reinterpret_cast<const int4*>(w.p.fm_intervals + 4ll * (r.it.x1 + t));
+      if (t >= 0 && t < r.it.T) {
+        const int4 iv = *reinterpret_cast<const int4*>(w.p.fm_intervals + 4ll * (r.it.x1 + t));
+        g.vis[h] = rows & ~(row_bits(iv.x, iv.y) | row_bits(iv.z, iv.w));
+      }
     }
   }
   if (w.p.layout != DATTN_KV_PAGED_HND) return g;
@@ -337,8 +347,7 @@ __device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& 
       t = -1;
     }
     if constexpr (FM) {   // a column hidden from every query row is never loaded
-      const uint32_t rows = row_bits(0, r.nq);
-      d.vis[h] = t >= 0 ? rows & ~(row_bits(g.iv[h].x, g.iv[h].y) | row_bits(g.iv[h].z, g.iv[h].w)) : 0u;
+      d.vis[h] = t >= 0 ? g.vis[h] : 0u;
       if (d.vis[h] == 0u) t = -1;
     }
     if (t >= 0) {

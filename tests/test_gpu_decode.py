@@ -177,6 +177,29 @@ def test_bounded_wait_gives_up_and_the_step_fails_closed(fused):
     H.compare(o.float().cpu(), lse.cpu(), w)
 
 
+def test_timeline_trace_is_ordered_and_leaves_the_outputs_unchanged():
+    """dattn_run_options.trace: per CTA the stamps come in pipeline order, every merge block
+    starts after the last partial CTA ended, and the traced step gives the same bits."""
+    w = W.paged_ragged_gqa("cuda", B=6, lo=200, hi=2000, pool_pages=800)
+    keep = {}
+    O, L, info, flags = H.run_gpu(w, num_sms=16, keep=keep)
+    assert flags == 0 and info["n_merge_groups"] > 0
+    n = info["n_ctas"]
+    buf = torch.zeros(16 * n + 2 * info["n_merge_groups"] * info["rows"], dtype=torch.int64, device="cuda")
+    keep["kw"]["o"].fill_(float("nan"))
+    dattn.dattn_run_ex(keep["plan"], w.problem, dattn.tensors_from(**keep["kw"]), keep["ws"], trace=buf)
+    torch.cuda.synchronize()
+    assert torch.equal(keep["kw"]["o"].float().cpu().reshape(O.shape), O)
+    t = buf.cpu().numpy()
+    P = t[:16 * n].reshape(n, 16)
+    assert (P[:, 0] > 0).all() and (P[:, 1] >= P[:, 0]).all()
+    assert (P[:, 2] >= P[:, 1]).all() and (P[:, 3] >= P[:, 2]).all() and (P[:, 4] >= P[:, 3]).all()
+    assert (P[:, 8:16] >= P[:, 4:5]).all()
+    M = t[16 * n:].reshape(-1, 2)
+    M = M[M[:, 0] > 0]
+    assert len(M) and (M[:, 0] >= P[:, 8:16].max()).all() and (M[:, 1] >= M[:, 0]).all()
+
+
 def test_wait_limit_options_are_checked():
     w = W.paged_ragged_gqa("cuda", B=2, lo=10, hi=40, pool_pages=10)
     p = w.problem

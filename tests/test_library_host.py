@@ -398,6 +398,7 @@ def test_shared_shift_needs_bf16_and_options_layout():
 
     with pytest.raises(dattn.DattnError, match="EUNSUPPORTED"):
         dattn.dattn_run_ex(plan, _problem(fmt="int8"), dattn.Tensors(), W(), shared_shift=(0.0, -1.0, 1.0), stream=0)
-    # C layout: uint32 flags, void* events[3], float phi, lo, hi
+    # C layout: uint32 flags, void* events[3], float phi, lo, hi, uint32 wait_limit_us, void* trace
     assert dattn.RunOptions.shift_phi.offset == 32 and dattn.RunOptions.shift_hi.offset == 40
-    assert ctypes.sizeof(dattn.RunOptions) == 48
+    assert dattn.RunOptions.wait_limit_us.offset == 44 and dattn.RunOptions.trace.offset == 48
+    assert ctypes.sizeof(dattn.RunOptions) == 56
