@@ -78,7 +78,8 @@ struct ItemRec {
   int32_t crow;        // contiguous layout: cache row, resolved by the kernel
   int32_t merge;       // index of the item's merge group, -1 when it writes O directly
   int32_t qo, nq;      // request it.b's first packed query row and its query rows C_b
-  int32_t pad0, pad1;
+  int32_t ring_off;    // INT4 KIVI: residual key t sits in ring slot t + ring_off, less R once >= R
+  int32_t pad1;
 };
 static_assert(sizeof(ItemRec) == 64, "ItemRec layout");
 

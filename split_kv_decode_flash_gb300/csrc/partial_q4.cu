@@ -230,15 +230,20 @@ __device__ __forceinline__ Q4Desc q4_rows(const Walk& w, const QCur& c, const in
   const ItemRec r = w.rec(c.ii);
   d.resid = c.j0 >= c.jq;
   int tmax = -1, err = 0;
-  // residual ring row of token t: (b R + (t mod R)) H + h; page row: (pi H + h) P + (t mod P)
+  // residual ring row of token t: (b R + (t mod R)) H + h; page row: (pi H + h) P + (t mod P).
+  // Residual keys lie in [n_q, T) with T - n_q <= R, so t mod R = (n_q mod R) + (t - n_q),
+  // less R once it reaches R; the planner stores (n_q mod R) - n_q in the item's record.
   const uint32_t ring0 = static_cast<uint32_t>(r.it.b) * sh.R;
+  const int roff = r.ring_off;   // ring slot of residual key t: t + roff, less R once it reaches R
 #pragma unroll
   for (int h = 0; h < kQSlots; ++h) {
     const int tk = t[h];
     uint32_t row = kNoRow;
     if (tk >= 0) {
       if (d.resid) {
-        row = (ring0 + static_cast<uint32_t>(tk % sh.R)) * p.H_kv + r.it.h;
+        int sl = tk + roff;
+        if (sl >= sh.R) sl -= sh.R;
+        row = (ring0 + static_cast<uint32_t>(sl)) * p.H_kv + r.it.h;
       } else if (pi[h] == -2) {
         err |= kStBlockRange;
       } else if (pi[h] < 0 || pi[h] >= p.num_pages) {

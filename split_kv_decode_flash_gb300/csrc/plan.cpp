@@ -466,6 +466,11 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
       r.merge = merge_of_group[static_cast<size_t>(items[i].b) * H + items[i].h];
       r.qo = query_start(items[i].b);
       r.nq = query_rows(items[i].b);
+      if (p.fmt == DATTN_FMT_INT4_KIVI) {   // residual keys lie in [n_q, T) with T - n_q <= R
+        const int T = items[i].T, G = p.kivi_group, R = p.kivi_residual;
+        const int nq = T > R ? (T - R + G - 1) / G * G : 0;
+        r.ring_off = nq % R - nq;
+      }
       r.lo = r.hi = -1;      // resolved by the kernel when the host page list is unknown
       if (p.layout == DATTN_KV_PAGED_HND && in->page_indptr) {
         r.lo = in->page_indptr[items[i].b];
