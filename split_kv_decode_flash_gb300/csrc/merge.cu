@@ -49,15 +49,17 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   constexpr int kRowsPerBlock = kMergeWarps / WPR;
   __shared__ float sm_u[WPR > 1 ? kMergeWarps : 1][D];
   __shared__ float sm_ml[WPR > 1 ? kMergeWarps : 1][2];
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the partial kernel's states are complete
-  // a programmatically launched successor may be scheduled; it waits for this grid
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (p.trace && threadIdx.x == 0) p.trace[2 * blockIdx.x] = merge_clock_ns();
   const int blocks_per_group = (p.rows + kRowsPerBlock - 1) / kRowsPerBlock;
   const int gi = blockIdx.x / blocks_per_group;
   const int row = (blockIdx.x % blocks_per_group) * kRowsPerBlock + (WPR > 1 ? 0 : w);
+  // the merge groups are part of the plan, copied before the partial kernel started:
+  // they may be read before the wait
   const MergeGroup grp = p.groups[gi];
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the partial kernel's states are complete
+  // a programmatically launched successor may be scheduled; it waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (p.trace && threadIdx.x == 0) p.trace[2 * blockIdx.x] = merge_clock_ns();
   // A partial kernel whose bounded wait gave up (or met a mis-stamped stage)
   // left states unwritten: then no row is written from them.  The word is
   // read with the group and tested only before the write.

@@ -170,6 +170,8 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
   pc_advance<kTK>(w, c1, kProducerWarps);
   RunStage s0 = run_stage(w, c0);
   RunStage s1 = run_stage(w, c1);
+  run_stage_page_prefetch(w, s0, lane);   // into L2 while the preceding grid finishes
+  run_stage_page_prefetch(w, s1, lane);
   dependency_wait(dep_wait);   // the page table is a device input
   if (pw == 0 && lane == 0) trace_stamp(p, kTrWaitDone);
   int pid0 = run_stage_page(w, s0, lane);
@@ -598,7 +600,7 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
       fold_init(f);
       if (active) {
         const int n_mine = grp.n > share ? (grp.n - share + W - 1) / W : 0;
-        fold_states<D>(p.ml, p.u, R, row, grp.slot0 + share, n_mine, W, lane, f);
+        fold_states<D, 8, false>(p.ml, p.u, R, row, grp.slot0 + share, n_mine, W, lane, f);
       }
       if (W > 1) {
 #pragma unroll
