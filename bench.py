@@ -533,8 +533,13 @@ def timeline(step, n_steps=40, skip=10):
     tr = buf.cpu().numpy().astype(np.float64)
     rows = []
     prev_merge_end = None
+    per_sm = {}
     for k in range(n_steps):
         P = tr[k, :16 * n_ctas].reshape(n_ctas, 16)
+        if k >= skip:      # each CTA's streaming time by the SM it ran on
+            for c in range(n_ctas):
+                if P[c, 2] > 0:
+                    per_sm.setdefault(int(P[c, 5]), []).append((P[c, 8:16].max() - P[c, 2]) / 1e3)
         M = tr[k, 16 * n_ctas:].reshape(-1, 2)
         M = M[M[:, 0] > 0]
         live = P[:, 2] > 0                                   # CTAs whose producer passed the wait
@@ -555,7 +560,16 @@ def timeline(step, n_steps=40, skip=10):
                 "period_us": (merge_end - prev_merge_end) / 1e3,
             })
         prev_merge_end = merge_end
-    return {k: float(np.median([r[k] for r in rows])) for k in rows[0]} if rows else None
+    if not rows:
+        return None
+    out = {k: float(np.median([r[k] for r in rows])) for k in rows[0]}
+    # how much of the CTAs' spread belongs to the SM (same SM slow in every step) rather than
+    # to the step: the variance of the per-SM means over the variance of all samples
+    allv = [x for v in per_sm.values() for x in v]
+    means = [np.mean(v) for v in per_sm.values() if len(v) > 1]
+    if len(allv) > 2 and np.var(allv) > 0 and len(means) > 2:
+        out["cta_time_share_of_variance_by_sm"] = float(np.var(means) / np.var(allv))
+    return out
 
 
 # ---- the two arms ---------------------------------------------------------------------

@@ -310,7 +310,8 @@ typedef struct {
                          16 c + {0: entry, 1: records read, 2: producer warp 0 past
                          the wait for the preceding grid, 3: its first stage's copies
                          issued, 4: the first stage landed for consumer warp 0,
-                         8 + w: consumer warp w done}; merge block j then writes
+                         5: the SM it ran on (%smid), 8 + w: consumer warp w done};
+                         merge block j then writes
                          16 n_ctas + 2 j (past its wait) and + 2 j + 1 (done)        */
 } dattn_run_options;
 

@@ -90,6 +90,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   pc_advance<kTK>(w, c1, kProducerWarps);
   PCur c2 = c1;
   pc_advance<kTK>(w, c2, kProducerWarps);
+  index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
   const SlotKeys<2> k0 = slot_keys<2>(w, c0, lane);
   SlotKeys<2> k1 = slot_keys<2>(w, c1, lane);
   SlotKeys<2> k2 = slot_keys<2>(w, c2, lane);
@@ -642,7 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may be scheduled now; it waits for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) trace_stamp(p, kTrEntry);
+  if (threadIdx.x == 0) {
+    trace_stamp(p, kTrEntry);
+    if (p.trace) {
+      uint32_t sm;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+      p.trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + kTrSm] = sm;
+    }
+  }
   const int it_begin = p.cta_indptr[blockIdx.x], it_end = p.cta_indptr[blockIdx.x + 1];
   ItemRec* cache = reinterpret_cast<ItemRec*>(smem + C::kItems);
   const int incomplete = fill_item_cache(p, cache, it_begin, it_end);

@@ -112,6 +112,7 @@ __device__ void produce_q4h(const Walk& w, uint8_t* smem, int lane, int pw, bool
   pc_advance<kHK>(w, c1, kProducerWarps);
   PCur c2 = c1;
   pc_advance<kHK>(w, c2, kProducerWarps);
+  index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
   const SlotKeys<kHS> k0 = slot_keys<kHS>(w, c0, lane);
   SlotKeys<kHS> k1 = slot_keys<kHS>(w, c1, lane);
   dependency_wait(dep_wait);   // the page table is a device input

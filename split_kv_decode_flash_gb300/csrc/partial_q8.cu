@@ -133,6 +133,7 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool 
   pc_advance<kQK>(w, c1, kProducerWarps);
   PCur c2 = c1;
   pc_advance<kQK>(w, c2, kProducerWarps);
+  index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
   const SlotKeys<kQS> k0 = slot_keys<kQS>(w, c0, lane);
   SlotKeys<kQS> k1 = slot_keys<kQS>(w, c1, lane);
   dependency_wait(dep_wait);   // the page table is a device input

@@ -18,19 +18,10 @@ constexpr int kItemCache = 256;       // work items of a CTA kept in shared memo
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;
 
 // Completes item record r with what only the device knows: the page-list
-// bounds when the plan was made without the host page list, the cache row
-// (contiguous layout), and the index-list consistency check (keys dropped,
-// e = a, when the list offsets disagree with the plan).  Reads device inputs,
-// so only after griddepcontrol.wait.
+// bounds when the plan was made without the host page list and the cache row
+// (contiguous layout).  Reads device inputs, so only after griddepcontrol.wait.
+// (The index-list consistency check runs where the list is read, slot_keys.)
 __device__ __forceinline__ ItemRec complete_rec(const PartialParams& p, ItemRec r, bool report) {
-  if (p.mask == DATTN_MASK_INDEX_LIST) {
-    const int g = r.it.b * p.H_kv + r.it.h;
-    const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
-    if (lo != r.it.x0 || r.it.e > n) {
-      if (report) atomicOr(p.status, kStListRange);
-      r.it.e = r.it.a;
-    }
-  }
   if (p.layout == DATTN_KV_PAGED_HND) {
     if (r.lo < 0) {
       r.lo = p.page_indptr[r.it.b];
@@ -43,9 +34,9 @@ __device__ __forceinline__ ItemRec complete_rec(const PartialParams& p, ItemRec 
 }
 
 // True when complete_rec changes nothing for this problem (paged layout with
-// the page-list bounds in the plan, interval masks).
+// the page-list bounds in the plan).
 __device__ __forceinline__ bool rec_complete_as_planned(const PartialParams& p, const ItemRec& r) {
-  return p.mask != DATTN_MASK_INDEX_LIST && p.layout == DATTN_KV_PAGED_HND && r.lo >= 0;
+  return p.layout == DATTN_KV_PAGED_HND && r.lo >= 0;
 }
 
 __device__ __forceinline__ ItemRec load_rec(const PartialParams& p, int ii, bool report) {
@@ -272,6 +263,10 @@ __device__ __forceinline__ uint32_t row_bits(int a, int b) {
   return b > a ? below(b) & ~below(a) : 0u;
 }
 
+// Index lists: the entries are read at the planned offsets, and the group's
+// device list bounds are checked beside them; when they disagree with the plan
+// every key of the stage is dropped (-1) and the status word says why, so the
+// consumers see only masked slots.
 template <int S>
 __device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, int lane) {
   SlotKeys<S> k;
@@ -284,7 +279,38 @@ __device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, i
     const int j = c.j0 + lane + 32 * h;
     if (j < c.j1) k.t[h] = stream_key(it, w.p.mask, w.p.index_list, j);
   }
+  if (w.p.mask == DATTN_MASK_INDEX_LIST) {
+    const int g = it.b * w.p.H_kv + it.h;
+    const int lo = w.p.index_indptr[g], n = w.p.index_indptr[g + 1] - lo;
+    if (lo != it.x0 || it.e > n) {
+      if (lane == 0) atomicOr(w.p.status, kStListRange);
+#pragma unroll
+      for (int h = 0; h < S; ++h) k.t[h] = -1;
+    }
+  }
   return k;
+}
+
+// Index lists: a producer warp's first keys are list entries, device inputs.
+// Their lines, the group's list bounds and the request's page-table lines are
+// prefetched into L2 (plan addresses only, nothing read), then the warp waits
+// for the preceding grid before slot_keys reads them.  No-op for the other
+// programs, whose keys are arithmetic.
+__device__ __forceinline__ void index_list_prologue(const Walk& w, const PCur& c0, int lane, bool dep_wait) {
+  const PartialParams& p = w.p;
+  if (p.mask != DATTN_MASK_INDEX_LIST) return;
+  if (c0.ii < w.end) {
+    const ItemRec r = w.rec(c0.ii);
+    const int j = c0.j0 + 32 * lane;                         // 32 entries (one line) per lane
+    if (j < r.it.e) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.index_list + r.it.x0 + j));
+    if (lane == 0)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.index_indptr + r.it.b * p.H_kv + r.it.h));
+    if (p.layout == DATTN_KV_PAGED_HND && r.lo >= 0) {
+      for (int e = r.lo + 32 * lane; e < r.hi && e < r.lo + 2048; e += 32 * 32)
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.page_indices + e));
+    }
+  }
+  dependency_wait(dep_wait);
 }
 
 template <int S, bool FM = false>

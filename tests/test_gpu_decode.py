@@ -129,6 +129,30 @@ def test_index_lists_small():
     H.compare(O, L, w)
 
 
+def test_index_list_bounds_that_disagree_with_the_plan_drop_the_group():
+    """A device index_indptr that disagrees with the planned one for group (0, 1): its keys
+    are dropped (every slot masked), the status word gets the list bit (4), its rows come out
+    all-masked (O = 0, LSE = -inf) and every other row still matches the oracle."""
+    w = W.retention("cuda", "index_list", B=3, T=3000)
+    p = w.problem
+    plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, index_indptr=w.index_indptr,
+                            index_list=w.index_list, num_sms=5, chunk_tokens=128)
+    o = torch.full((3, 1, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((3, 1, 32), float("nan"), dtype=torch.float32, device="cuda")
+    kw = H.device_tensors(w, o, lse)
+    bad = kw["index_indptr"].clone()
+    bad[1] += 1                                  # group 1 = (request 0, kv head 1) starts one entry late
+    kw["index_indptr"] = bad
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    dattn.dattn_run(plan, p, dattn.tensors_from(**kw), ws)
+    torch.cuda.synchronize()
+    assert dattn.dattn_device_status(ws) & 4
+    O, L = o.float().cpu(), lse.cpu()
+    assert torch.isinf(L[0, 0, 4:8]).all() and (L[0, 0, 4:8] < 0).all() and not O[0, 0, 4:8].any()
+    rows = [(b, 0, h) for b in range(3) for h in range(32) if not (b == 0 and 4 <= h < 8)]
+    H.compare(O, L, w, rows)
+
+
 def test_index_lists_full_size_all_rows():
     w = W.retention("cuda", "index_list")
     O, L, info, flags = H.run_gpu(w)
