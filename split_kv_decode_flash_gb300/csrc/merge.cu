@@ -8,12 +8,12 @@
 // rounded to bf16 and LSE = m + ln l, all-masked rows giving O = 0 and
 // LSE = -inf.
 //
-// Groups of fewer than 8 rows: one block of four warps per (group, query
-// row); warp w takes states w, w + 4, ..., and the four warps' folds combine
-// in shared memory.  Groups of 8 rows or more: one warp per (group, row).  A
-// warp's lanes fetch (m, l) of up to 32 states at once, the warp agrees on
-// the frame, and the u vectors are then read with the loads in flight (each
-// lane owns d / 32 channels).  The kernel is launched as a programmatic
+// Groups of at most 32 states on average: one warp per (group, row), four
+// rows per block; the warp reads all of the row's states in one round, (m, l)
+// one per lane and every u vector (each lane owns d / 32 channels) with the
+// loads in flight together, agrees on the frame and folds.  More states: one
+// block of four warps per (group, query row); warp w takes states w, w + 4,
+// ... in batches of 8, and the four warps' folds combine in shared memory.  The kernel is launched as a programmatic
 // dependent of the partial kernel: it is resident before the partial kernel
 // ends and waits (griddepcontrol.wait) for its states to be complete.
 #include <cuda_runtime.h>
@@ -43,7 +43,8 @@ __device__ __forceinline__ void merge_trace_done(const MergeParams& p, int lane)
 // states).  WPR = 1: one warp per (group, row), four rows per block, each
 // warp folding all of its row's states (many rows, few states each: the
 // combine and its barrier would cost more than the fold).
-template <int D, int WPR>
+// KB: u vectors read per batch (32: every state of a row of up to 32 states in one round).
+template <int D, int WPR, int KB>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_constant__ MergeParams p) {
   constexpr int C = D / 32;
   constexpr int kRowsPerBlock = kMergeWarps / WPR;
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
     }
     RowFold<D> f;
     fold_init(f);
-    fold_states<D>(p.ml, p.u, p.rows, row, grp.slot0, grp.n, 1, lane, f);
+    fold_states<D, KB>(p.ml, p.u, p.rows, row, grp.slot0, grp.n, 1, lane, f);
     if (!fail_closed) write_folded_row<D>(p.o, p.lse, orow, f, lane);
     merge_trace_done(p, lane);
     return;
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
     RowFold<D> f;
     fold_init(f);
     const int n_mine = grp.n > w ? (grp.n - w + kMergeWarps - 1) / kMergeWarps : 0;
-    fold_states<D>(p.ml, p.u, p.rows, row, grp.slot0 + w, n_mine, kMergeWarps, lane, f);
+    fold_states<D, KB>(p.ml, p.u, p.rows, row, grp.slot0 + w, n_mine, kMergeWarps, lane, f);
     // combine the warps' folds
 #pragma unroll
     for (int c = 0; c < C; ++c) sm_u[w][lane * C + c] = f.U[c];
@@ -119,13 +120,14 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   }
 }
 
-// One warp merges a row alone when the groups have at least 8 rows and at
-// most 20 states on average (then the four-warp blocks, one per row, and
-// their shared-memory combine cost more than they save; with more states one
-// warp's sequential batches lengthen the merge's critical path).
-constexpr int kOneWarpRows = 8, kOneWarpStates = 20;
+// Groups of at most 32 states on average: one warp per row reads all of the
+// row's states in one round (their (m, l) and u together), four rows per
+// block, no shared-memory combine.  More states: one block of four warps per
+// row, each folding every fourth state in batches of 8, combined in shared
+// memory (one warp's sequential rounds would lengthen the critical path).
+constexpr int kOneRoundStates = 32;
 
-template <int D, int WPR>
+template <int D, int WPR, int KB>
 cudaError_t launch_d(const MergeParams& p, void* stream) {
   constexpr int kRowsPerBlock = kMergeWarps / WPR;
   cudaLaunchConfig_t cfg = {};
@@ -138,7 +140,7 @@ cudaError_t launch_d(const MergeParams& p, void* stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<D, WPR>, p);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D, WPR, KB>, p);
 }
 
 }  // namespace
@@ -146,8 +148,10 @@ cudaError_t launch_d(const MergeParams& p, void* stream) {
 int launch_merge(const MergeParams& p, int d, void* stream) {
   if (p.n_groups * p.rows == 0) return cudaSuccess;
   cudaError_t err;
-  if (p.rows >= kOneWarpRows && p.mean_states <= kOneWarpStates) err = d == 64 ? launch_d<64, 1>(p, stream) : launch_d<128, 1>(p, stream);
-  else err = d == 64 ? launch_d<64, 4>(p, stream) : launch_d<128, 4>(p, stream);
+  if (p.mean_states <= kOneRoundStates)
+    err = d == 64 ? launch_d<64, 1, 32>(p, stream) : launch_d<128, 1, 32>(p, stream);
+  else
+    err = d == 64 ? launch_d<64, 4, 8>(p, stream) : launch_d<128, 4, 8>(p, stream);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 

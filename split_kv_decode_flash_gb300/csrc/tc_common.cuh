@@ -243,6 +243,7 @@ __device__ __forceinline__ void pc_advance(const Walk& w, PCur& c, int n) {
 template <int S>
 struct SlotKeys {
   int t[S];      // logical key (-1: none)
+  bool bad;      // index lists: the group's device list bounds disagree with the plan
 };
 template <int S, bool FM = false>
 struct SlotPages {
@@ -264,12 +265,14 @@ __device__ __forceinline__ uint32_t row_bits(int a, int b) {
 }
 
 // Index lists: the entries are read at the planned offsets, and the group's
-// device list bounds are checked beside them; when they disagree with the plan
-// every key of the stage is dropped (-1) and the status word says why, so the
+// device list bounds beside them, without waiting for either (so the next
+// stages' loads are issued at once); when the bounds disagree with the plan,
+// slot_rows drops every key of the stage and the status word says why, so the
 // consumers see only masked slots.
 template <int S>
 __device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, int lane) {
   SlotKeys<S> k;
+  k.bad = false;
 #pragma unroll
   for (int h = 0; h < S; ++h) k.t[h] = -1;
   if (c.ii >= w.end) return k;
@@ -282,11 +285,7 @@ __device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, i
   if (w.p.mask == DATTN_MASK_INDEX_LIST) {
     const int g = it.b * w.p.H_kv + it.h;
     const int lo = w.p.index_indptr[g], n = w.p.index_indptr[g + 1] - lo;
-    if (lo != it.x0 || it.e > n) {
-      if (lane == 0) atomicOr(w.p.status, kStListRange);
-#pragma unroll
-      for (int h = 0; h < S; ++h) k.t[h] = -1;
-    }
+    k.bad = lo != it.x0 || it.e > n;
   }
   return k;
 }
@@ -363,10 +362,11 @@ __device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& 
   d.full = false;
   if (c.ii >= w.end) return d;
   const ItemRec r = w.rec(c.ii);
+  if (k.bad && lane == 0) atomicOr(p.status, kStListRange);
   int tmax = -1;
 #pragma unroll
   for (int h = 0; h < S; ++h) {
-    int t = k.t[h];
+    int t = k.bad ? -1 : k.t[h];
     uint32_t row = kNoRow;
     if (p.mask == DATTN_MASK_INDEX_LIST && c.j0 + lane + 32 * h < c.j1 && (t < 0 || t >= r.it.T)) {
       atomicOr(p.status, kStListRange);
