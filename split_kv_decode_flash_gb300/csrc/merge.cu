@@ -8,12 +8,12 @@
 // rounded to bf16 and LSE = m + ln l, all-masked rows giving O = 0 and
 // LSE = -inf.
 //
-// Groups of at most 32 states on average: one warp per (group, row), four
-// rows per block; the warp reads all of the row's states in one round, (m, l)
-// one per lane and every u vector (each lane owns d / 32 channels) with the
-// loads in flight together, agrees on the frame and folds.  More states: one
-// block of four warps per (group, query row); warp w takes states w, w + 4,
-// ... in batches of 8, and the four warps' folds combine in shared memory.  The kernel is launched as a programmatic
+// Groups of fewer than 8 rows (or many states): one block of four warps per
+// (group, query row); warp w takes states w, w + 4, ..., and the four warps'
+// folds combine in shared memory.  Groups of 8 rows or more: one warp per
+// (group, row).  A warp's lanes fetch (m, l) of up to 32 states at once with
+// the first batch of u vectors (each lane owns d / 32 channels), agree on the
+// frame, and read the remaining u vectors a batch at a time.  The kernel is launched as a programmatic
 // dependent of the partial kernel: it is resident before the partial kernel
 // ends and waits (griddepcontrol.wait) for its states to be complete.
 #include <cuda_runtime.h>
@@ -120,12 +120,14 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   }
 }
 
-// Groups of at most 32 states on average: one warp per row reads all of the
-// row's states in one round (their (m, l) and u together), four rows per
-// block, no shared-memory combine.  More states: one block of four warps per
-// row, each folding every fourth state in batches of 8, combined in shared
-// memory (one warp's sequential rounds would lengthen the critical path).
-constexpr int kOneRoundStates = 32;
+// One warp merges a row alone when the groups have at least 8 rows and at
+// most 20 states on average (then the four-warp blocks, one per row, and
+// their shared-memory combine cost more than they save; with more states one
+// warp's sequential batches lengthen the merge's critical path).  A row's
+// whole fold in one round (every state's u read at once) was slower: the
+// unrolled batch of 32 predicated loads costs more than the round trips it
+// saves.
+constexpr int kOneWarpRows = 8, kOneWarpStates = 20;
 
 template <int D, int WPR, int KB>
 cudaError_t launch_d(const MergeParams& p, void* stream) {
@@ -148,8 +150,8 @@ cudaError_t launch_d(const MergeParams& p, void* stream) {
 int launch_merge(const MergeParams& p, int d, void* stream) {
   if (p.n_groups * p.rows == 0) return cudaSuccess;
   cudaError_t err;
-  if (p.mean_states <= kOneRoundStates)
-    err = d == 64 ? launch_d<64, 1, 32>(p, stream) : launch_d<128, 1, 32>(p, stream);
+  if (p.rows >= kOneWarpRows && p.mean_states <= kOneWarpStates)
+    err = d == 64 ? launch_d<64, 1, 8>(p, stream) : launch_d<128, 1, 8>(p, stream);
   else
     err = d == 64 ? launch_d<64, 4, 8>(p, stream) : launch_d<128, 4, 8>(p, stream);
   return err != cudaSuccess ? err : cudaGetLastError();
