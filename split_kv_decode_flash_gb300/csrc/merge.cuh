@@ -51,12 +51,12 @@ __device__ __forceinline__ void load_u_batch(float (&x)[kBatch][D / 32], const f
 
 // Folds states s_first + s_stride * i, i in [0, n), of row "row" into f.
 // Lanes fetch (m, l) of 32 states at a time; the u vectors are read kBatch
-// at a time with all loads in flight, the first batch together with (m, l)
-// when kEarly (its loads do not depend on them; the fused merge inside the
-// partial kernel, short of registers, reads it after).  Empty states (l = 0) are skipped by
+// at a time with all loads in flight; with kEarly the first batch goes out
+// together with (m, l) (its loads do not depend on them), which measured
+// slightly slower on GB300 and is off.  Empty states (l = 0) are skipped by
 // predicate, so whatever their u holds never enters the fold.  A batch is
 // unrolled: its unused slots still cost their predicated instructions.
-template <int D, int kBatch = 8, bool kEarly = true>
+template <int D, int kBatch = 8, bool kEarly = false>
 __device__ __forceinline__ void fold_states(const float2* ml, const float* u, int rows, int row, int s_first,
                                             int n_states, int s_stride, int lane, RowFold<D>& f) {
   constexpr unsigned kAll = 0xffffffffu;

@@ -248,14 +248,24 @@ struct SlotKeys {
 template <int S, bool FM = false>
 struct SlotPages {
   int pi[S];     // page id of the key's block (-2: block outside the page list)
-  uint32_t vis[FM ? S : 1];   // FlashMask: bit i set when query row i sees the key column
+  int4 iv[S];    // FlashMask: the key column's (UTS, UTE, LTS, LTE), used a stage later
+};
+template <int S>
+struct SlotPages<S, false> {
+  int pi[S];
 };
 template <int S, bool FM = false>
 struct SlotRows {
   int t[S];           // logical key, -1 when the slot is empty or invalid
   uint32_t row[S];    // K/V row in the cache in rows of d elements (kNoRow: none)
-  uint32_t vis[FM ? S : 1];   // FlashMask: bit i set when query row i sees the key
+  uint32_t vis[S];    // FlashMask: bit i set when query row i sees the key
   bool full;          // FULL stage class
+};
+template <int S>
+struct SlotRows<S, false> {
+  int t[S];
+  uint32_t row[S];
+  bool full;
 };
 
 // Bits [a, b) of a 32-bit row mask (clipped to [0, 32)).
@@ -319,19 +329,15 @@ __device__ __forceinline__ SlotPages<S, FM> slot_pages(const Walk& w, const PCur
   for (int h = 0; h < S; ++h) g.pi[h] = -2;
   if constexpr (FM) {
 #pragma unroll
-    for (int h = 0; h < S; ++h) g.vis[h] = 0u;
+    for (int h = 0; h < S; ++h) g.iv[h] = make_int4(0, 0, 0, 0);
   }
   if (c.ii >= w.end) return g;
   const ItemRec r = w.rec(c.ii);
-  if constexpr (FM) {   // the column intervals are loaded with the page ids, kept as the rows that see the key
-    const uint32_t rows = row_bits(0, r.nq);
+  if constexpr (FM) {   // the column intervals travel with the page ids (not awaited here)
 #pragma unroll
     for (int h = 0; h < S; ++h) {
       const int t = k.t[h];
-      if (t >= 0 && t < r.it.T) {
-        const int4 iv = *reinterpret_cast<const int4*>(w.p.fm_intervals + 4ll * (r.it.x1 + t));
-        g.vis[h] = rows & ~(row_bits(iv.x, iv.y) | row_bits(iv.z, iv.w));
-      }
+      if (t >= 0 && t < r.it.T) g.iv[h] = *reinterpret_cast<const int4*>(w.p.fm_intervals + 4ll * (r.it.x1 + t));
     }
   }
   if (w.p.layout != DATTN_KV_PAGED_HND) return g;
@@ -373,7 +379,8 @@ __device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& 
       t = -1;
     }
     if constexpr (FM) {   // a column hidden from every query row is never loaded
-      d.vis[h] = t >= 0 ? g.vis[h] : 0u;
+      const uint32_t rows = row_bits(0, r.nq);
+      d.vis[h] = t >= 0 ? rows & ~(row_bits(g.iv[h].x, g.iv[h].y) | row_bits(g.iv[h].z, g.iv[h].w)) : 0u;
       if (d.vis[h] == 0u) t = -1;
     }
     if (t >= 0) {
