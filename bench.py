@@ -497,6 +497,25 @@ def timed_samples(step, K, warmup, world=1):
     return samples, evs[0].elapsed_time(evs[-1])
 
 
+def timed_unbroken(step, K, warmup, world=1):
+    """K steps back to back after ``warmup`` steps between two events only (no event
+    inside the region can stop a kernel from launching under its predecessor's tail):
+    total ms."""
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(warmup):
+        step.run()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(step.stream)
+    for _ in range(K):
+        step.run()
+    end.record(step.stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end)
+
+
 def kernel_pass(step, K):
     """K steps with events around each kernel (this breaks the programmatic overlap of the
     two kernels, so it is a separate pass): mean partial and merge µs."""
@@ -658,7 +677,8 @@ def config_line(dattn, name, dev, num_sms, steps, cpu=True):
         step.run()
     torch.cuda.synchronize()
     assert step.status() == 0, f"device bounds check fired ({name})"
-    samples, total_ms = timed_samples(step, steps, 20)
+    total_ms = timed_unbroken(step, steps, 20)
+    samples, _ = timed_samples(step, steps, 3)
     part_us, merge_us = kernel_pass(step, min(200, steps))
     tl = timeline(step)
     nb = stream_bytes(p, step.info, w.kv_len.tolist())
@@ -718,7 +738,8 @@ def run_ours(args):
     # would stop the merge from launching programmatically under the partial
     # kernel's tail, so the per-kernel events are taken in a separate pass.
     K = args.steps
-    samples, total_ms = timed_samples(step, K, max(3, args.warmup), world)
+    total_ms = timed_unbroken(step, K, max(3, args.warmup), world)
+    samples, _ = timed_samples(step, K, 3, world)
     part_us, merge_us = kernel_pass(step, min(K, 500))
     tl = timeline(step)
     ck = clocks.stop()
@@ -749,7 +770,9 @@ def run_ours(args):
                                                  "stream_keys", "max_cta_keys", "workspace_bytes")}},
         "kv_bytes_per_step": ab["kv"],
         "us_per_step_samples": dict(s, what=f"{s['n']} samples, each the mean of {max(1, K // MIN_SAMPLES)} "
-                                             f"consecutive steps between two events of the timed region"),
+                                             f"consecutive steps between two events, in a second region of "
+                                             f"K steps right after the timed one (the events between batches "
+                                             f"cost a little: the timed region has none)"),
         "GBps_median": world * ab["kv"] / (med_us * 1e-6) / 1e9,
         "frac_of_nominal_8TBps": ab["kv"] / (med_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
         "frac_of_measured_hbm": ab["kv"] / (med_us * 1e-6) / 1e9 / peak,
@@ -824,7 +847,8 @@ def run_other(args):
         step.run()
     torch.cuda.synchronize()
     assert step.status() == 0, "device bounds check fired"
-    samples, total_ms = timed_samples(step, max(MIN_SAMPLES, args.steps), max(3, args.warmup))
+    total_ms = timed_unbroken(step, max(MIN_SAMPLES, args.steps), max(3, args.warmup))
+    samples, _ = timed_samples(step, max(MIN_SAMPLES, args.steps), 3)
     s = summary(samples)
     fallbacks = dattn.dattn_shift_fallbacks(step.ws, step.stream) if args.shared_shift else None
     tl = timeline(step)
@@ -835,8 +859,9 @@ def run_other(args):
                       "frac": nb / s["median"] / 1e3 / peak, "peak": peak, "peak_source": peak_src,
                       "rows": step.info["rows"], "n_items": step.info["n_items"], "steps": args.steps,
                       "shared_shift": _shift(args), "shift_fallbacks": fallbacks, "timeline": tl,
-                      "timing": "CUDA events around K back-to-back decode steps (partial + merge); GBps and "
-                                "frac from the median per-step sample"}), flush=True)
+                      "timing": "us_per_step: CUDA events around K back-to-back decode steps (partial + merge); "
+                                "samples: a second region of K steps with an event after every K/50; GBps and "
+                                "frac from the median sample"}), flush=True)
 
 
 def main():

@@ -70,17 +70,20 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Bounded wait.  The thread sleeps inside try_wait (hardware suspend, woken
 // by the phase completing) instead of spinning, so waiting warps leave the
-// issue slots to working ones.  After limit_ns of wall time (2 s unless the
-// caller set another limit) it raises the abort flag and the timeout status
-// bit, so that every warp of the CTA stops.
+// issue slots to working ones.  After the CTA's wait limit of wall time (2 s
+// unless the caller set another; a uint64 of ns kept 8 bytes after the abort
+// flag, read only on this slow path) it raises the abort flag and the timeout
+// status bit, so that every warp of the CTA stops.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status, uint64_t limit_ns) {
+                                          int32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((it & 7u) == 7u) {
       if (*abort_flag) return false;
+      const uint64_t limit_ns =
+          *reinterpret_cast<const volatile unsigned long long*>(reinterpret_cast<const volatile char*>(abort_flag) + 8);
       if (global_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, kStTimeout);

@@ -208,7 +208,7 @@ __device__ void produce(const PartialParams& p, uint8_t* smem, int it_begin, int
 
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) return;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) return;
     uint8_t* stage = smem + st * C::kStage;
     uint8_t* kt = stage;
     uint8_t* vt = stage + C::kTile;
@@ -497,7 +497,7 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
         dead = true;
         break;
       }
@@ -749,6 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_kernel(const __grid_const
       mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), kConsumerWarps / stage_groups(p.rows));
     }
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
+    *reinterpret_cast<uint64_t*>(smem + C::kAbort + 8) = p.wait_ns;   // read by the bounded waits
     fence_barrier_init();
   }
   fence_proxy_async_smem();

@@ -69,7 +69,9 @@ struct Bf {
 };
 
 
-template <int D, bool FM>
+// HK: the instance with the timeline stamps and the skipped-arrival test hook
+// (launched only when a run asks for either; the plain instance has neither).
+template <int D, bool FM, bool HK>
 __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
   using C = Bf<D>;
   const PartialParams& p = w.p;
@@ -96,7 +98,9 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   SlotKeys<2> k2 = slot_keys<2>(w, c2, lane);
   // Up to here only the plan was read; the page table is a device input.
   dependency_wait(dep_wait);
-  if (pw == 0 && lane == 0) trace_stamp(p, kTrWaitDone);
+  if constexpr (HK) {
+    if (pw == 0 && lane == 0) trace_stamp(p, kTrWaitDone);
+  }
   const SlotPages<2, FM> g0 = slot_pages<2, FM>(w, c0, k0);     // both stages' page lookups in flight together
   SlotPages<2, FM> g1 = slot_pages<2, FM>(w, c1, k1);
   SlotRows<2, FM> r0 = slot_rows<2, FM, true>(w, c0, k0, g0, lane);
@@ -104,7 +108,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
     pos[lane] = r0.t[0];
     pos[lane + 32] = r0.t[1];
@@ -129,12 +133,14 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
       cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
     }
     const uint32_t fb = full0 + 8 * st;
-    if (!(p.skip_arrival && blockIdx.x == 0 && k == 0)) {   // the test hook withholds stage 0 of CTA 0
+    if (!(HK && p.skip_arrival && blockIdx.x == 0 && k == 0)) {   // the test hook withholds stage 0 of CTA 0
       cp_async_mbar_arrive(fb);
       __syncwarp();
       if (lane == 0) mbar_arrive(fb);   // publishes pos / flags / stamp; the copies complete the phase
     }
-    if (k == 0 && lane == 0) trace_stamp(p, kTrFirstCopy);
+    if constexpr (HK) {
+      if (k == 0 && lane == 0) trace_stamp(p, kTrFirstCopy);
+    }
 
     // move the description pipeline one stage of this warp forward
     r0 = slot_rows<2, FM, true>(w, c1, k1, g1, lane);
@@ -151,7 +157,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
 // The same producer for interval programs on power-of-two pages (not
 // FlashMask): one page id per lane and stage instead of a key, a page-table
 // load and a row per slot (RunStage in tc_common.cuh).
-template <int D>
+template <int D, bool HK>
 __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
   using C = Bf<D>;
   const PartialParams& p = w.p;
@@ -171,17 +177,17 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
   pc_advance<kTK>(w, c1, kProducerWarps);
   RunStage s0 = run_stage(w, c0);
   RunStage s1 = run_stage(w, c1);
-  run_stage_page_prefetch(w, s0, lane);   // into L2 while the preceding grid finishes
-  run_stage_page_prefetch(w, s1, lane);
   dependency_wait(dep_wait);   // the page table is a device input
-  if (pw == 0 && lane == 0) trace_stamp(p, kTrWaitDone);
+  if constexpr (HK) {
+    if (pw == 0 && lane == 0) trace_stamp(p, kTrWaitDone);
+  }
   int pid0 = run_stage_page(w, s0, lane);
   int pid1 = run_stage_page(w, s1, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     const ItemRec rec = w.rec(c0.ii);
     uint32_t rows[2];
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
@@ -207,12 +213,14 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
       cp_async16(vt + dst, vbase + off, ok ? 16u : 0u, stream_pol);
     }
     const uint32_t fb = full0 + 8 * st;
-    if (!(p.skip_arrival && blockIdx.x == 0 && k == 0)) {   // the test hook withholds stage 0 of CTA 0
+    if (!(HK && p.skip_arrival && blockIdx.x == 0 && k == 0)) {   // the test hook withholds stage 0 of CTA 0
       cp_async_mbar_arrive(fb);
       __syncwarp();
       if (lane == 0) mbar_arrive(fb);   // publishes pos / flags / stamp; the copies complete the phase
     }
-    if (k == 0 && lane == 0) trace_stamp(p, kTrFirstCopy);
+    if constexpr (HK) {
+      if (k == 0 && lane == 0) trace_stamp(p, kTrFirstCopy);
+    }
 
     c0 = c1;
     s0 = s1;
@@ -295,7 +303,7 @@ struct WarpRole {
 };
 
 // One item: its stages (k counts the CTA's stages across items), then its rows.
-template <int D, int KW, bool SHIFT>
+template <int D, int KW, bool SHIFT, bool HK>
 __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const ItemRec& rec,
                                              const uint32_t (&qa)[D / 16][4], int cw, int lane, uint32_t& k,
                                              bool& dead) {
@@ -339,7 +347,7 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
     }
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
+    if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
       dead = true;
       break;
     }
@@ -349,7 +357,9 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
       dead = true;
       break;
     }
-    if (k == 0 && cw == 0 && lane == 0) trace_stamp(p, kTrFirstStage);
+    if constexpr (HK) {
+      if (k == 0 && cw == 0 && lane == 0) trace_stamp(p, kTrFirstStage);
+    }
     const int* pos = reinterpret_cast<const int*>(smem + C::kPos) + st * kTK;
     const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kTK;
     const bool full = reinterpret_cast<const int*>(smem + C::kFlags)[st] & kFlagFull;
@@ -513,7 +523,7 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
 // more rows (a mixed batch's widest request, or a uniform batch of 17 to 32
 // rows) each item takes the layout of its own request's g C_b rows.
 // SHIFT: shared-shift partials; the synchronized path is compiled without them.
-template <int D, bool SHIFT>
+template <int D, bool SHIFT, bool HK>
 __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, bool dep_wait) {
   dependency_wait(dep_wait);   // before Q and the state writes
   const PartialParams& p = w.p;
@@ -532,7 +542,7 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
 #pragma unroll
         for (int x = 0; x < 4; ++x) qa[kk][x] = qn[kk][x];
       if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1), role.r0, role.r1, t4, qn);
-      consume_item<D, 16, SHIFT>(w, smem, w.rec(ii), qa, cw, lane, k, dead);
+      consume_item<D, 16, SHIFT, HK>(w, smem, w.rec(ii), qa, cw, lane, k, dead);
     }
   } else {
     for (int ii = w.begin; ii < w.end; ++ii) {
@@ -541,11 +551,11 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
       if (p.g * rec.nq <= 16) {
         const WarpRole<16> role(cw, lane);
         load_q<D>(p, rec, role.r0, role.r1, t4, qa);
-        consume_item<D, 16, SHIFT>(w, smem, rec, qa, cw, lane, k, dead);
+        consume_item<D, 16, SHIFT, HK>(w, smem, rec, qa, cw, lane, k, dead);
       } else {
         const WarpRole<32> role(cw, lane);
         load_q<D>(p, rec, role.r0, role.r1, t4, qa);
-        consume_item<D, 32, SHIFT>(w, smem, rec, qa, cw, lane, k, dead);
+        consume_item<D, 32, SHIFT, HK>(w, smem, rec, qa, cw, lane, k, dead);
       }
     }
   }
@@ -637,13 +647,13 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
   }
 }
 
-template <int D>
+template <int D, bool HK>
 __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_constant__ PartialParams p) {
   using C = Bf<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may be scheduled now; it waits for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) {
+  if (HK && threadIdx.x == 0) {
     trace_stamp(p, kTrEntry);
     if (p.trace) {
       uint32_t sm;
@@ -660,36 +670,37 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
       mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), kConsumerWarps / 2);
     }
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
+    *reinterpret_cast<uint64_t*>(smem + C::kAbort + 8) = p.wait_ns;   // read by the bounded waits
     fence_barrier_init();
   }
   // Records that need device inputs are completed by the whole CTA after the
   // wait.  Otherwise each warp waits on its own, just before its first device
   // read, and the producers set up their first stages' keys in the meantime.
   const bool complete_now = __syncthreads_or(incomplete);
-  if (threadIdx.x == 0) trace_stamp(p, kTrRecords);
+  if (HK && threadIdx.x == 0) trace_stamp(p, kTrRecords);
   if (complete_now) complete_item_cache(p, cache, it_begin, it_end);
   const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBfProducerRegs));
-    if (p.mask == DATTN_MASK_FLASHMASK) produce_bf16<D, true>(w, smem, lane, warp - kConsumerWarps, !complete_now);
-    else if (runs_apply<kTK>(p)) produce_bf16_runs<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
-    else produce_bf16<D, false>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    if (p.mask == DATTN_MASK_FLASHMASK) produce_bf16<D, true, HK>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    else if (runs_apply<kTK>(p)) produce_bf16_runs<D, HK>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    else produce_bf16<D, false, HK>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));
-  if (p.shift_on) consume_bf16<D, true>(w, smem, warp, lane, !complete_now);
-  else consume_bf16<D, false>(w, smem, warp, lane, !complete_now);
-  if (lane == 0) trace_stamp(p, kTrConsumerEnd + warp);
+  if (p.shift_on) consume_bf16<D, true, HK>(w, smem, warp, lane, !complete_now);
+  else consume_bf16<D, false, HK>(w, smem, warp, lane, !complete_now);
+  if (HK && lane == 0) trace_stamp(p, kTrConsumerEnd + warp);
   if (p.fused) fused_merge<D>(w, smem, warp, lane);
 }
 
-template <int D>
-int launch_bf16(const PartialParams& p, int n_ctas, void* stream) {
+template <int D, bool HK>
+int launch_bf16_inst(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Bf<D>::kTotal;
   // the register budget check and the shared-memory opt-in, once per device
   static std::atomic<unsigned long long> ready{0};
-  cudaError_t err = prepare_kernel_once(partial_bf16_kernel<D>, smem, 128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs, ready);
+  cudaError_t err = prepare_kernel_once(partial_bf16_kernel<D, HK>, smem, 128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs, ready);
   if (err != cudaSuccess) return err;
   // programmatic launch: the prologue overlaps the tail of the preceding kernel
   cudaLaunchConfig_t cfg = {};
@@ -702,8 +713,14 @@ int launch_bf16(const PartialParams& p, int n_ctas, void* stream) {
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, partial_bf16_kernel<D>, p);
+  err = cudaLaunchKernelEx(&cfg, partial_bf16_kernel<D, HK>, p);
   return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+template <int D>
+int launch_bf16(const PartialParams& p, int n_ctas, void* stream) {
+  return p.trace || p.skip_arrival ? launch_bf16_inst<D, true>(p, n_ctas, stream)
+                                   : launch_bf16_inst<D, false>(p, n_ctas, stream);
 }
 
 }  // namespace

@@ -316,7 +316,7 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool 
     q4_keys(w, c2, lane, t1);
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kQKeys;
     uint32_t* rows = reinterpret_cast<uint32_t*>(smem + C::kRows) + st * kQKeys;
 #pragma unroll
@@ -665,7 +665,7 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
         dead = true;
         break;
       }
@@ -952,6 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4_kernel(const __grid_co
       mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), kConsumerWarps / 2);
     }
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
+    *reinterpret_cast<uint64_t*>(smem + C::kAbort + 8) = p.wait_ns;   // read by the bounded waits
     fence_barrier_init();
   }
   // without records to complete, each warp waits just before its first device read

@@ -124,7 +124,7 @@ __device__ void produce_q4h(const Walk& w, uint8_t* smem, int lane, int pw, bool
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kHK;
 #pragma unroll
     for (int h = 0; h < kHS; ++h) pos[lane + 32 * h] = r0.t[h];
@@ -197,7 +197,7 @@ __device__ void produce_q4h_runs(const Walk& w, uint8_t* smem, int lane, int pw,
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     const ItemRec rec = w.rec(c0.ii);
     uint32_t rows[kHS];
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kHK;
@@ -364,7 +364,7 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
         dead = true;
         break;
       }
@@ -563,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4h_kernel(const __grid_c
       mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), kConsumerWarps / 2);
     }
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
+    *reinterpret_cast<uint64_t*>(smem + C::kAbort + 8) = p.wait_ns;   // read by the bounded waits
     fence_barrier_init();
   }
   // without records to complete, each warp waits just before its first device read

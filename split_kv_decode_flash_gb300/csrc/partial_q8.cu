@@ -145,7 +145,7 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kQK;
 #pragma unroll
     for (int h = 0; h < kQS; ++h) pos[lane + 32 * h] = r0.t[h];
@@ -228,7 +228,7 @@ __device__ void produce_q8_runs(const Walk& w, uint8_t* smem, int lane, int pw, 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
-    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status, p.wait_ns)) break;
+    if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     const ItemRec rec = w.rec(c0.ii);
     uint32_t rows[kQS];
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kQK;
@@ -436,7 +436,7 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
         dead = true;
         break;
       }
@@ -694,7 +694,7 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
       }
       const int st = k % C::kStagesN;
       const uint32_t use = k / C::kStagesN;
-      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status, p.wait_ns)) {
+      if (dead || !mbar_wait(full0 + 8 * st, use & 1, abort_flag, p.status)) {
         dead = true;
         break;
       }
@@ -864,6 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_co
       mbar_init(smem_u32(smem + C::kEmptyBar + 8 * s), warps_per_stage);
     }
     *reinterpret_cast<int*>(smem + C::kAbort) = 0;
+    *reinterpret_cast<uint64_t*>(smem + C::kAbort + 8) = p.wait_ns;   // read by the bounded waits
     fence_barrier_init();
   }
   // without records to complete, each warp waits just before its first device read

@@ -469,22 +469,6 @@ __device__ __forceinline__ int run_stage_page(const Walk& w, const RunStage& r, 
   return pid;
 }
 
-// Warms L2 with the page-table line that run_stage_page will read for stage
-// r.  Only addresses from the plan are used and nothing is read, so it may run
-// before the wait for the preceding grid (which may still write the table).
-__device__ __forceinline__ void run_stage_page_prefetch(const Walk& w, const RunStage& r, int lane) {
-  if (r.ii >= w.end) return;
-  const ItemRec rec = w.rec(r.ii);
-  if (rec.lo < 0) return;
-  const int np2 = r.n2 ? ((r.q0 + r.n2 - 1) >> w.p.P_shift) - r.b2 + 1 : 0;
-  int blk;
-  if (lane < r.np1) blk = r.b1 + lane;
-  else if (lane < r.np1 + np2) blk = r.b2 + (lane - r.np1);
-  else return;
-  if (blk < rec.hi - rec.lo)
-    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(w.p.page_indices + rec.lo + blk));
-}
-
 // Key (-1: none) and K/V row (kNoRow: none) of slot s of stage r; every lane
 // of the warp calls it (the page id comes by shuffle from its lane).
 __device__ __forceinline__ void run_slot(const PartialParams& p, const RunStage& r, int T, int h, int pid_lane,

@@ -217,7 +217,8 @@ def test_timeline_trace_is_ordered_and_leaves_the_outputs_unchanged():
     t = buf.cpu().numpy()
     P = t[:16 * n].reshape(n, 16)
     assert (P[:, 0] > 0).all() and (P[:, 1] >= P[:, 0]).all()
-    assert (P[:, 2] >= P[:, 1]).all() and (P[:, 3] >= P[:, 2]).all() and (P[:, 4] >= P[:, 3]).all()
+    # (the first stage can land, L2-resident, before producer warp 0 stamps its own first copy)
+    assert (P[:, 2] >= P[:, 1]).all() and (P[:, 3] >= P[:, 2]).all() and (P[:, 4] >= P[:, 2]).all()
     assert (P[:, 8:16] >= P[:, 4:5]).all()
     M = t[16 * n:].reshape(-1, 2)
     M = M[M[:, 0] > 0]
