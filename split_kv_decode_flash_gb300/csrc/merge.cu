@@ -11,9 +11,10 @@
 // Groups of fewer than 8 rows (or many states): one block of four warps per
 // (group, query row); warp w takes states w, w + 4, ..., and the four warps'
 // folds combine in shared memory.  Groups of 8 rows or more: one warp per
-// (group, row).  A warp's lanes fetch (m, l) of up to 32 states at once with
-// the first batch of u vectors (each lane owns d / 32 channels), agree on the
-// frame, and read the remaining u vectors a batch at a time.  The kernel is launched as a programmatic
+// (group, row).  A warp's lanes fetch (m, l) of up to 32 states at once, the
+// warp agrees on the frame, and the u vectors of the live states are then
+// read a batch at a time with the loads in flight (each lane owns d / 32
+// channels).  The kernel is launched as a programmatic
 // dependent of the partial kernel: it is resident before the partial kernel
 // ends and waits (griddepcontrol.wait) for its states to be complete.
 #include <cuda_runtime.h>
@@ -43,7 +44,7 @@ __device__ __forceinline__ void merge_trace_done(const MergeParams& p, int lane)
 // states).  WPR = 1: one warp per (group, row), four rows per block, each
 // warp folding all of its row's states (many rows, few states each: the
 // combine and its barrier would cost more than the fold).
-// KB: u vectors read per batch (32: every state of a row of up to 32 states in one round).
+// KB: u vectors read per batch.
 template <int D, int WPR, int KB>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_constant__ MergeParams p) {
   constexpr int C = D / 32;

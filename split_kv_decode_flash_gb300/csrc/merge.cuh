@@ -29,34 +29,11 @@ __device__ __forceinline__ void fold_init(RowFold<D>& f) {
   for (int c = 0; c < D / 32; ++c) f.U[c] = 0.f;
 }
 
-// The lane's D / 32 channels of the u vectors of states q0 .. q0 + kBatch - 1
-// (those below n; the others read as zero).
-template <int D, int kBatch>
-__device__ __forceinline__ void load_u_batch(float (&x)[kBatch][D / 32], const float* u0, long long stride, int q0,
-                                             int n) {
-  constexpr int C = D / 32;
-#pragma unroll
-  for (int q = 0; q < kBatch; ++q) {
-    const bool use = q0 + q < n;
-    const float* src = u0 + (q0 + q) * stride;
-    if constexpr (C == 4) {
-      const float4 t = use ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      x[q][0] = t.x; x[q][1] = t.y; x[q][2] = t.z; x[q][3] = t.w;
-    } else {
-      const float2 t = use ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
-      x[q][0] = t.x; x[q][1] = t.y;
-    }
-  }
-}
-
 // Folds states s_first + s_stride * i, i in [0, n), of row "row" into f.
-// Lanes fetch (m, l) of 32 states at a time; the u vectors are read kBatch
-// at a time with all loads in flight; with kEarly the first batch goes out
-// together with (m, l) (its loads do not depend on them), which measured
-// slightly slower on GB300 and is off.  Empty states (l = 0) are skipped by
-// predicate, so whatever their u holds never enters the fold.  A batch is
-// unrolled: its unused slots still cost their predicated instructions.
-template <int D, int kBatch = 8, bool kEarly = false>
+// Lanes fetch (m, l) of 32 states at a time; the u vectors of the live ones
+// are then read kBatch at a time with all loads in flight (a batch is
+// unrolled: its unused slots still cost their predicated instructions).
+template <int D, int kBatch = 8>
 __device__ __forceinline__ void fold_states(const float2* ml, const float* u, int rows, int row, int s_first,
                                             int n_states, int s_stride, int lane, RowFold<D>& f) {
   constexpr unsigned kAll = 0xffffffffu;
@@ -65,9 +42,6 @@ __device__ __forceinline__ void fold_states(const float2* ml, const float* u, in
   for (int i0 = 0; i0 < n_states; i0 += 32) {
     const int n = min(32, n_states - i0);
     const int s0 = s_first + s_stride * i0;
-    const float* u0 = u + (static_cast<long long>(s0) * rows + row) * D + lane * C;
-    float x[kBatch][C];
-    if constexpr (kEarly) load_u_batch<D, kBatch>(x, u0, stride, 0, n);
     float2 v = make_float2(-INFINITY, 0.f);
     if (lane < n) v = __ldcg(ml + static_cast<long long>(s0 + s_stride * lane) * rows + row);
     const bool valid = v.y > 0.f;
@@ -86,14 +60,26 @@ __device__ __forceinline__ void fold_states(const float2* ml, const float* u, in
     for (int c = 0; c < C; ++c) f.U[c] *= scale_old;
     f.M = m_new;
     const unsigned live = __ballot_sync(kAll, valid);
+    const float* u0 = u + (static_cast<long long>(s0) * rows + row) * D + lane * C;
     for (int q0 = 0; q0 < n; q0 += kBatch) {
-      if (q0 > 0 || !kEarly) load_u_batch<D, kBatch>(x, u0, stride, q0, n);
+      float x[kBatch][C];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const bool use = q0 + q < n && ((live >> (q0 + q)) & 1u);
+        const float* src = u0 + (q0 + q) * stride;
+        if constexpr (C == 4) {
+          const float4 t = use ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[q][0] = t.x; x[q][1] = t.y; x[q][2] = t.z; x[q][3] = t.w;
+        } else {
+          const float2 t = use ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
+          x[q][0] = t.x; x[q][1] = t.y;
+        }
+      }
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         const float wq = __shfl_sync(kAll, wt, (q0 + q) & 31);
-        const bool use = q0 + q < n && ((live >> (q0 + q)) & 1u);
 #pragma unroll
-        for (int c = 0; c < C; ++c) f.U[c] = use ? fmaf(wq, x[q][c], f.U[c]) : f.U[c];
+        for (int c = 0; c < C; ++c) f.U[c] = fmaf(wq, x[q][c], f.U[c]);
       }
     }
   }

@@ -92,10 +92,10 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   pc_advance<kTK>(w, c1, kProducerWarps);
   PCur c2 = c1;
   pc_advance<kTK>(w, c2, kProducerWarps);
-  index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
-  const SlotKeys<2> k0 = slot_keys<2>(w, c0, lane);
-  SlotKeys<2> k1 = slot_keys<2>(w, c1, lane);
-  SlotKeys<2> k2 = slot_keys<2>(w, c2, lane);
+  if constexpr (!FM) index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
+  const SlotKeys<2> k0 = slot_keys<2, !FM>(w, c0, lane);
+  SlotKeys<2> k1 = slot_keys<2, !FM>(w, c1, lane);
+  SlotKeys<2> k2 = slot_keys<2, !FM>(w, c2, lane);
   // Up to here only the plan was read; the page table is a device input.
   dependency_wait(dep_wait);
   if constexpr (HK) {
@@ -149,7 +149,7 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
     k1 = k2;
     c1 = c2;
     pc_advance<kTK>(w, c2, kProducerWarps);
-    k2 = slot_keys<2>(w, c2, lane);
+    k2 = slot_keys<2, !FM>(w, c2, lane);
   }
   asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
 }
@@ -611,7 +611,7 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
       fold_init(f);
       if (active) {
         const int n_mine = grp.n > share ? (grp.n - share + W - 1) / W : 0;
-        fold_states<D, 8, false>(p.ml, p.u, R, row, grp.slot0 + share, n_mine, W, lane, f);
+        fold_states<D>(p.ml, p.u, R, row, grp.slot0 + share, n_mine, W, lane, f);
       }
       if (W > 1) {
 #pragma unroll

@@ -133,13 +133,13 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool 
   pc_advance<kQK>(w, c1, kProducerWarps);
   PCur c2 = c1;
   pc_advance<kQK>(w, c2, kProducerWarps);
-  index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
-  const SlotKeys<kQS> k0 = slot_keys<kQS>(w, c0, lane);
-  SlotKeys<kQS> k1 = slot_keys<kQS>(w, c1, lane);
+  if constexpr (!FM) index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
+  const SlotKeys<kQS> k0 = slot_keys<kQS, !FM>(w, c0, lane);
+  SlotKeys<kQS> k1 = slot_keys<kQS, !FM>(w, c1, lane);
   dependency_wait(dep_wait);   // the page table is a device input
   const SlotPages<kQS, FM> g0 = slot_pages<kQS, FM>(w, c0, k0);
   SlotPages<kQS, FM> g1 = slot_pages<kQS, FM>(w, c1, k1);
-  SlotKeys<kQS> k2 = slot_keys<kQS>(w, c2, lane);
+  SlotKeys<kQS> k2 = slot_keys<kQS, !FM>(w, c2, lane);
   SlotRows<kQS, FM> r0 = slot_rows<kQS, FM>(w, c0, k0, g0, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
@@ -191,7 +191,7 @@ __device__ void produce_q8(const Walk& w, uint8_t* smem, int lane, int pw, bool 
     k1 = k2;
     c1 = c2;
     pc_advance<kQK>(w, c2, kProducerWarps);
-    k2 = slot_keys<kQS>(w, c2, lane);
+    k2 = slot_keys<kQS, !FM>(w, c2, lane);
   }
   asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
 }

@@ -278,8 +278,9 @@ __device__ __forceinline__ uint32_t row_bits(int a, int b) {
 // device list bounds beside them, without waiting for either (so the next
 // stages' loads are issued at once); when the bounds disagree with the plan,
 // slot_rows drops every key of the stage and the status word says why, so the
-// consumers see only masked slots.
-template <int S>
+// consumers see only masked slots.  LIST = false: the caller never runs an
+// index-list program (FlashMask producers), and none of this is compiled.
+template <int S, bool LIST = true>
 __device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, int lane) {
   SlotKeys<S> k;
   k.bad = false;
@@ -292,7 +293,7 @@ __device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, i
     const int j = c.j0 + lane + 32 * h;
     if (j < c.j1) k.t[h] = stream_key(it, w.p.mask, w.p.index_list, j);
   }
-  if (w.p.mask == DATTN_MASK_INDEX_LIST) {
+  if (LIST && w.p.mask == DATTN_MASK_INDEX_LIST) {
     const int g = it.b * w.p.H_kv + it.h;
     const int lo = w.p.index_indptr[g], n = w.p.index_indptr[g + 1] - lo;
     k.bad = lo != it.x0 || it.e > n;
