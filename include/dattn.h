@@ -294,7 +294,8 @@ dattn_status dattn_run(const dattn_plan_t* plan, const dattn_problem* prob,
                                       bounded wait runs out after wait_limit_us (required,
                                       1 .. 100000).  Nothing faults or hangs: the CTA stops,
                                       the status word gets the timeout bit (16) and no output
-                                      row is written from the states it left unwritten */
+                                      row is written from the states it left unwritten (the
+                                      rows of the groups it worked on stay as they were) */
 typedef struct {
   uint32_t flags;     /* DATTN_RUN_* bits                                                  */
   void* events[3];    /* cudaEvent_t (as void*) recorded on "stream" before the partial
@@ -302,8 +303,9 @@ typedef struct {
   float shift_phi, shift_lo, shift_hi;   /* DATTN_RUN_SHARED_SHIFT frame and guard      */
   uint32_t wait_limit_us;   /* limit of each bounded wait on a ring stage in microseconds
                                (0: 2 s).  A wait that runs out stops its CTA, sets the
-                               timeout bit (16) of the device status word, and the merge
-                               then writes no output row (fail closed)                     */
+                               timeout bit (16) of the device status word, and its warps
+                               mark their partial states unwritten, so that no output row
+                               depending on them is written (fail closed, row by row)      */
   void* trace;        /* NULL, or (bf16 K/V) a device uint64 array of at least
                          16 n_ctas + 2 n_merge_groups rows words (zeroed by the caller):
                          %globaltimer stamps in ns.  Partial CTA c writes words

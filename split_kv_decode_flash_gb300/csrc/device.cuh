@@ -225,6 +225,13 @@ __device__ __forceinline__ int cache_row(const int32_t* cache_batch_idx, int b, 
   return c;
 }
 
+// Marks partial-state row "srow" as never written (m = l = NaN): a consumer
+// warp whose bounded wait gave up leaves this instead of a state, and the
+// merge writes none of the rows that depend on it (fail closed, row by row).
+__device__ __forceinline__ void mark_state_unwritten(float2* ml, long long srow) {
+  ml[srow] = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+}
+
 // ---- small numeric helpers ------------------------------------------------------------
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {

@@ -62,11 +62,6 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   // a programmatically launched successor may be scheduled; it waits for this grid
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (p.trace && threadIdx.x == 0) p.trace[2 * blockIdx.x] = merge_clock_ns();
-  // A partial kernel whose bounded wait gave up (or met a mis-stamped stage)
-  // left states unwritten: then no row is written from them.  The word is
-  // read with the group and tested only before the write.
-  const int32_t partial_status = __ldcg(p.status);
-  const bool fail_closed = partial_status & (kStTimeout | kStPipeline);
   const int i = row / p.g, hq = grp.h * p.g + row % p.g;
   const long long orow = (static_cast<long long>(grp.qo) + i) * p.H_q + hq;
   if constexpr (WPR == 1) {
@@ -77,7 +72,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
     RowFold<D> f;
     fold_init(f);
     fold_states<D, KB>(p.ml, p.u, p.rows, row, grp.slot0, grp.n, 1, lane, f);
-    if (!fail_closed) write_folded_row<D>(p.o, p.lse, orow, f, lane);
+    if (!f.bad) write_folded_row<D>(p.o, p.lse, orow, f, lane);   // rows with an unwritten state stay unwritten
     merge_trace_done(p, lane);
     return;
   } else {
@@ -95,7 +90,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
     for (int c = 0; c < C; ++c) sm_u[w][lane * C + c] = f.U[c];
     if (lane == 0) {
       sm_ml[w][0] = f.M;
-      sm_ml[w][1] = f.L;
+      sm_ml[w][1] = f.bad ? __int_as_float(0x7fc00000) : f.L;   // NaN carries the unwritten mark
     }
     __syncthreads();
     if (w != 0) {
@@ -105,7 +100,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
     RowFold<D> t;
     fold_init(t);
 #pragma unroll
-    for (int k = 0; k < kMergeWarps; ++k) t.M = fmaxf(t.M, sm_ml[k][1] > 0.f ? sm_ml[k][0] : -INFINITY);
+    for (int k = 0; k < kMergeWarps; ++k) {
+      t.M = fmaxf(t.M, sm_ml[k][1] > 0.f ? sm_ml[k][0] : -INFINITY);
+      t.bad = t.bad || sm_ml[k][1] != sm_ml[k][1];
+    }
     if (t.M != -INFINITY) {
 #pragma unroll
       for (int k = 0; k < kMergeWarps; ++k) {
@@ -116,7 +114,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
         for (int c = 0; c < C; ++c) t.U[c] = fmaf(a, sm_u[k][lane * C + c], t.U[c]);
       }
     }
-    if (!fail_closed) write_folded_row<D>(p.o, p.lse, orow, t, lane);
+    if (!t.bad) write_folded_row<D>(p.o, p.lse, orow, t, lane);
     merge_trace_done(p, lane);
   }
 }

@@ -10,19 +10,23 @@
 
 #include <cuda_bf16.h>
 
-#include "internal.h"
+#include "device.cuh"
 
 namespace dattn {
 
-// A warp's running fold of one row: frame M (log2 units), sum L, and the
-// lane's D / 32 channels of u.
+// A warp's running fold of one row: frame M (log2 units), sum L, the lane's
+// D / 32 channels of u, and whether some state was marked unwritten (l = NaN:
+// its partial-kernel warp gave up, see mark_state_unwritten) so that the row
+// must not be written.
 template <int D>
 struct RowFold {
   float M, L, U[D / 32];
+  bool bad;
 };
 
 template <int D>
 __device__ __forceinline__ void fold_init(RowFold<D>& f) {
+  f.bad = false;
   f.M = -INFINITY;
   f.L = 0.f;
 #pragma unroll
@@ -44,6 +48,7 @@ __device__ __forceinline__ void fold_states(const float2* ml, const float* u, in
     const int s0 = s_first + s_stride * i0;
     float2 v = make_float2(-INFINITY, 0.f);
     if (lane < n) v = __ldcg(ml + static_cast<long long>(s0 + s_stride * lane) * rows + row);
+    if (__any_sync(kAll, v.y != v.y)) f.bad = true;    // a state marked unwritten
     const bool valid = v.y > 0.f;
     float mc = valid ? v.x : -INFINITY;
 #pragma unroll

@@ -730,6 +730,8 @@ __device__ void consume(const PartialParams& p, uint8_t* smem, int it_begin, int
           *reinterpret_cast<float4*>(u + C::chan(j, x)) = make_float4(ov[x].x, ov[x].y, ov[x + 1].x, ov[x + 1].y);
         if (j == 0) p.ml[srow] = make_float2(l_mine > 0.f ? m_mine : -INFINITY, l_mine);
       }
+    } else if (row < p.rows && dead && it.slot >= 0 && j == 0) {   // the warp gave up: its state is marked
+      mark_state_unwritten(p.ml, static_cast<long long>(it.slot + my_state) * p.rows + row);
     }
   }
 }

@@ -515,6 +515,9 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
   if (!dead) {
     if (ok0) emit_row<D>(p, it, rec.qo, my_state, r0, m0, l0, o, 0, t4);
     if (ok1) emit_row<D>(p, it, rec.qo, my_state, r1, m1, l1, o, 1, t4);
+  } else if (it.slot >= 0 && t4 == 0) {   // the warp gave up: its states are marked, never guessed
+    if (ok0) mark_state_unwritten(p.ml, static_cast<long long>(it.slot + my_state) * p.rows + r0);
+    if (ok1) mark_state_unwritten(p.ml, static_cast<long long>(it.slot + my_state) * p.rows + r1);
   }
 }
 
@@ -618,13 +621,16 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
         for (int c = 0; c < C; ++c) sm_u[cw * D + lane * C + c] = f.U[c];
         if (lane == 0) {
           sm_ml[2 * cw] = f.M;
-          sm_ml[2 * cw + 1] = f.L;
+          sm_ml[2 * cw + 1] = f.bad ? __int_as_float(0x7fc00000) : f.L;   // NaN carries the unwritten mark
         }
         named_barrier(1, 32 * kCW);
         if (active && share == 0) {
           RowFold<D> t;
           fold_init(t);
-          for (int j = cw; j < cw + W; ++j) t.M = fmaxf(t.M, sm_ml[2 * j + 1] > 0.f ? sm_ml[2 * j] : -INFINITY);
+          for (int j = cw; j < cw + W; ++j) {
+            t.M = fmaxf(t.M, sm_ml[2 * j + 1] > 0.f ? sm_ml[2 * j] : -INFINITY);
+            t.bad = t.bad || sm_ml[2 * j + 1] != sm_ml[2 * j + 1];
+          }
           if (t.M != -INFINITY) {
             for (int j = cw; j < cw + W; ++j) {
               if (!(sm_ml[2 * j + 1] > 0.f)) continue;
@@ -640,7 +646,7 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
       }
       if (active && share == 0) {
         const int i = row / p.g, hq = grp.h * p.g + row % p.g;
-        write_folded_row<D>(p.o, p.lse, (static_cast<long long>(grp.qo) + i) * p.H_q + hq, f, lane);
+        if (!f.bad) write_folded_row<D>(p.o, p.lse, (static_cast<long long>(grp.qo) + i) * p.H_q + hq, f, lane);
       }
     }
     if (cw == 0 && lane == 0) p.group_count[gi] = 0;    // ready for the next run

@@ -544,6 +544,9 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
           if (g4 == 0) p.ml[srow] = make_float2(l > 0.f ? m : -INFINITY, l);
         }
       }
+    } else if (it.slot >= 0 && g4 == 0) {   // the warp gave up: its states are marked, never guessed
+      if (oka) mark_state_unwritten(p.ml, static_cast<long long>(it.slot + my_state) * p.rows + ra);
+      if (okb) mark_state_unwritten(p.ml, static_cast<long long>(it.slot + my_state) * p.rows + rb1);
     }
   }
 }

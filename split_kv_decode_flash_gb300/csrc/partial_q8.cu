@@ -572,6 +572,9 @@ __device__ void consume_q8(const Walk& w, uint8_t* smem, int cw, int lane) {
       const int qo = w.rec(ii).qo;
       if (ok0) emit_row_q8<D>(p, it, qo, my_state, r0, m0, l0, z0, Codes<FMT>::kBias * b0, hv, o, 0, t4);
       if (ok1) emit_row_q8<D>(p, it, qo, my_state, r1, m1, l1, z1, Codes<FMT>::kBias * b1, hv, o, 1, t4);
+    } else if (it.slot >= 0 && t4 == 0) {   // the warp gave up: its states are marked, never guessed
+      if (ok0) mark_state_unwritten(p.ml, static_cast<long long>(it.slot + my_state) * p.rows + r0);
+      if (ok1) mark_state_unwritten(p.ml, static_cast<long long>(it.slot + my_state) * p.rows + r1);
     }
   }
 }
@@ -842,6 +845,9 @@ __device__ void consume_q8_swap(const Walk& w, uint8_t* smem, int cw, int lane) 
           if (g4 == 0) p.ml[srow] = make_float2(l > 0.f ? m : -INFINITY, l);
         }
       }
+    } else if (it.slot >= 0 && g4 == 0) {   // the warp gave up: its states are marked, never guessed
+      if (oka) mark_state_unwritten(p.ml, static_cast<long long>(it.slot + my_state) * p.rows + ra);
+      if (okb) mark_state_unwritten(p.ml, static_cast<long long>(it.slot + my_state) * p.rows + rb);
     }
   }
 }

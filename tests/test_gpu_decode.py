@@ -166,10 +166,10 @@ def test_index_lists_full_size_all_rows():
 def test_bounded_wait_gives_up_and_the_step_fails_closed(fused):
     """The test hook withholds the completion of CTA 0's first ring stage: its consumers'
     wait runs out after 1 ms, the CTA stops and the status word gets the timeout bit (16).
-    No output row may come from the states it left unwritten: with the merge kernel no
-    row is written at all; with the fused merge the groups CTA 0 took part in stay
-    unwritten and every other row is exact.  The context stays usable: the next step on
-    the same workspace gives every row exactly."""
+    No output row may come from the states it left unwritten: its warps mark their state
+    slots unwritten (merge kernel) or count none of their items (fused merge), so the rows
+    of every group CTA 0 took part in stay unwritten, and every other row is exact.  The
+    context stays usable: the next step on the same workspace gives every row exactly."""
     w = W.paged_ragged_gqa("cuda", B=4, lo=300, hi=900, pool_pages=300)
     p = w.problem
     plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, num_sms=6, fused_merge=fused)
@@ -189,12 +189,9 @@ def test_bounded_wait_gives_up_and_the_step_fails_closed(fused):
     g = p["H_q"] // p["H_kv"]
     for b, h in cta0:          # groups that CTA 0 took part in: never written
         assert not written[b, 0, h * g:(h + 1) * g].any()
-    if not fused:
-        assert not written.any()
-    else:
-        rows = [(b, 0, h) for b in range(p["B"]) for h in range(p["H_q"]) if written[b, 0, h]]
-        assert rows
-        H.compare(O, L, w, rows)
+    rows = [(b, 0, h) for b in range(p["B"]) for h in range(p["H_q"]) if written[b, 0, h]]
+    assert rows
+    H.compare(O, L, w, rows)
     dattn.dattn_run(plan, p, t, ws)         # uploads the plan again (fresh counters and status)
     torch.cuda.synchronize()
     assert dattn.dattn_device_status(ws) == 0
