@@ -45,6 +45,15 @@ constexpr int kQS = kQK / 32;         // slots per producer lane
 constexpr int kQ8ProducerRegs = 88;
 constexpr int kQ8ConsumerRegs = 208;
 static_assert(128 * kQ8ProducerRegs + 32 * kConsumerWarps * kQ8ConsumerRegs <= kThreads * 168, "register split");
+// The FlashMask instance's producers carry four interval ends per slot a stage
+// ahead: they get more of the register file.
+constexpr int kQ8FmProducerRegs = 104;
+constexpr int kQ8FmConsumerRegs = 200;
+static_assert(128 * kQ8FmProducerRegs + 32 * kConsumerWarps * kQ8FmConsumerRegs <= kThreads * 168, "register split");
+template <bool FM>
+constexpr int q8_producer_regs() { return FM ? kQ8FmProducerRegs : kQ8ProducerRegs; }
+template <bool FM>
+constexpr int q8_consumer_regs() { return FM ? kQ8FmConsumerRegs : kQ8ConsumerRegs; }
 
 template <int D>
 struct Q8 {
@@ -879,13 +888,13 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q8_kernel(const __grid_co
   const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ8ProducerRegs));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(q8_producer_regs<FM>()));
     if constexpr (FM) produce_q8<D, FMT, true>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     else if (runs_apply<kQK>(p)) produce_q8_runs<D, FMT>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     else produce_q8<D, FMT, false>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ8ConsumerRegs));
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(q8_consumer_regs<FM>()));
   dependency_wait(!complete_now);   // before Q and the state writes
   if (p.rows <= 8) consume_q8_swap<D, FMT, FM>(w, smem, warp, lane);
   else consume_q8<D, FMT, FM>(w, smem, warp, lane);
@@ -896,7 +905,7 @@ int launch_q8_inst(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Q8<D>::kTotal;
   // the register budget check and the shared-memory opt-in, once per device
   static std::atomic<unsigned long long> ready{0};
-  cudaError_t err = prepare_kernel_once(partial_q8_kernel<D, FMT, FM>, smem, 128 * kQ8ProducerRegs + 32 * kConsumerWarps * kQ8ConsumerRegs, ready);
+  cudaError_t err = prepare_kernel_once(partial_q8_kernel<D, FMT, FM>, smem, 128 * q8_producer_regs<FM>() + 32 * kConsumerWarps * q8_consumer_regs<FM>(), ready);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);

@@ -18,10 +18,21 @@ constexpr int kItemCache = 256;       // work items of a CTA kept in shared memo
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;
 
 // Completes item record r with what only the device knows: the page-list
-// bounds when the plan was made without the host page list and the cache row
-// (contiguous layout).  Reads device inputs, so only after griddepcontrol.wait.
-// (The index-list consistency check runs where the list is read, slot_keys.)
+// bounds when the plan was made without the host page list, the cache row
+// (contiguous layout), and the index-list consistency check (keys dropped,
+// e = a, when the list offsets disagree with the plan).  Reads device inputs,
+// so only after griddepcontrol.wait.  Paged index-list records are complete as
+// planned (rec_complete_as_planned): slot_keys makes the same check where the
+// list is read, so that no CTA-wide wait precedes the first list load.
 __device__ __forceinline__ ItemRec complete_rec(const PartialParams& p, ItemRec r, bool report) {
+  if (p.mask == DATTN_MASK_INDEX_LIST) {
+    const int g = r.it.b * p.H_kv + r.it.h;
+    const int lo = p.index_indptr[g], n = p.index_indptr[g + 1] - lo;
+    if (lo != r.it.x0 || r.it.e > n) {
+      if (report) atomicOr(p.status, kStListRange);
+      r.it.e = r.it.a;
+    }
+  }
   if (p.layout == DATTN_KV_PAGED_HND) {
     if (r.lo < 0) {
       r.lo = p.page_indptr[r.it.b];
