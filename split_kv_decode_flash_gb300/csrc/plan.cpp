@@ -302,21 +302,31 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
     return p.fmt == DATTN_FMT_BF16 && rows > 16 && (p.H_q / p.H_kv) * query_rows(b) <= 16
                ? states_per_item(16, p.fmt, kivi_tc) : spi;
   };
+  // The segments are cut on an axis of sixteenths of a key: a group's keys
+  // weigh kKeyUnit each, those of a bf16 request with more than 16 rows (the
+  // 32-row tile, about a quarter slower per key on GB300 than one 16-row tile)
+  // kWideKeyUnit, and each non-empty group starts with its pad.
+  constexpr long long kKeyUnit = 16, kWideKeyUnit = 20;
+  auto weight_of = [&](int b) {
+    return p.fmt == DATTN_FMT_BF16 && (p.H_q / p.H_kv) * query_rows(b) > 16 ? kWideKeyUnit : kKeyUnit;
+  };
   std::vector<long long> pad(n_groups, 0);
-  long long Wp = W;                                  // padded length of the concatenation
+  long long Wp = 0;                                  // padded, weighted length of the concatenation
   for (int k = 0; k < n_groups; ++k) {
-    if (!segmented || gn[k] == 0 || in->item_cost_keys < 0) continue;
     const int b = k / H;
-    pad[k] = in->item_cost_keys > 0 ? in->item_cost_keys
-                                    : default_item_cost_keys(p, (p.H_q / p.H_kv) * query_rows(b), spi_of(b));
+    Wp += static_cast<long long>(gn[k]) * weight_of(b);
+    if (!segmented || gn[k] == 0 || in->item_cost_keys < 0) continue;
+    pad[k] = kKeyUnit * (in->item_cost_keys > 0 ? in->item_cost_keys
+                                                : default_item_cost_keys(p, (p.H_q / p.H_kv) * query_rows(b), spi_of(b)));
     Wp += pad[k];
   }
   long long seg = 1;
   int n_seg = 1;
   if (segmented && Wp > 0) {
-    const long long want = std::max<long long>(1, std::min<long long>(cta_target, (Wp + kTK - 1) / kTK));
+    const long long keys = (Wp + kKeyUnit - 1) / kKeyUnit;
+    const long long want = std::max<long long>(1, std::min<long long>(cta_target, (keys + kTK - 1) / kTK));
     seg = (Wp + want - 1) / want;
-    seg = (seg + 15) / 16 * 16;                      // whole 16-key tiles
+    seg = (seg + 16 * kKeyUnit - 1) / (16 * kKeyUnit) * (16 * kKeyUnit);   // whole 16-key tiles
     n_seg = static_cast<int>((Wp + seg - 1) / seg);
   }
   std::vector<int> group_first(n_groups + 1, 0);
@@ -347,9 +357,11 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
       // steps never straddle a K group (a CTA streams at most 31 keys more)
       const long long grid = p.fmt == DATTN_FMT_INT4_KIVI ? 32 : 1;
       const long long k0 = g_off + pad[k];   // padded position of the group's first key
+      const long long wk = weight_of(b);
       for (long long a = 0; a < n;) {
-        const long long c = std::min<long long>(n_seg - 1, (k0 + a) / seg);
-        const long long e = std::min<long long>(n, ((c + 1) * seg - k0 + grid - 1) / grid * grid);
+        const long long c = std::min<long long>(n_seg - 1, (k0 + a * wk) / seg);
+        const long long cut = ((c + 1) * seg - k0 + wk - 1) / wk;    // first key of the next segment
+        const long long e = std::min<long long>(n, std::max<long long>(a + 1, (cut + grid - 1) / grid * grid));
         add(static_cast<int>(a), static_cast<int>(e));
         seg_cta.push_back(static_cast<int>(c));
         a = e;
@@ -359,7 +371,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
     } else {
       for (long long a = 0; a < n; a += L) add(static_cast<int>(a), static_cast<int>(std::min<long long>(n, a + L)));
     }
-    g_off += n + pad[k];
+    g_off += static_cast<long long>(n) * (segmented ? weight_of(b) : 1) + pad[k];
   }
   group_first[n_groups] = static_cast<int>(items.size());
 

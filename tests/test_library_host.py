@@ -282,6 +282,39 @@ def test_mixed_batch_streams_follow_each_requests_query_rows():
         _coverage(plan.items(), [(b, h) for b in range(len(TC)) for h in range(2)], want)
 
 
+def test_equal_segments_weigh_the_keys_of_wide_bf16_requests():
+    """Keys of a bf16 request with more than 16 rows (the 32-row tile) weigh 1.25 in the
+    equal-segment partition: a CTA holding only such keys gets about 1/1.25 of the keys of
+    one holding only 4-row keys, and every CTA's weighted load is about the same."""
+    B, S_q = 6, 8
+    qo = np.array([0, 1, 2, 10, 11, 18, 19], np.int32)          # C_b: 1, 1, 8, 1, 7, 1
+    T = [6000, 5000, 7000, 6500, 7200, 5500]
+    prob = _problem(B=B, S_q=S_q, H_q=32, H_kv=8, num_pages=20000)
+    pages = [-(-t // 16) for t in T]
+    indptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    plan = dattn.dattn_plan(prob, T, page_indptr=indptr, qo_indptr=qo, num_sms=40, item_cost_keys=-1)
+    C = np.diff(qo)
+    wide = {b for b in range(B) if 4 * C[b] > 16}
+    assert wide == {2, 4}
+    load, keys_only = {}, {}
+    for it in plan.items():
+        n = it["e"] - it["a"]
+        load[it["cta"]] = load.get(it["cta"], 0) + n * (1.25 if it["b"] in wide else 1.0)
+        kind = "wide" if it["b"] in wide else "narrow"
+        keys_only.setdefault(it["cta"], set()).add(kind)
+    v = np.array([load[c] for c in sorted(load)])
+    assert v.max() - v[:-1].min() <= 16 * 1.25 + 2        # equal up to a tile and a cut (last CTA short)
+    pure = {c: ks for c, ks in keys_only.items() if len(ks) == 1}
+    per_kind = {}
+    for it in plan.items():
+        if it["cta"] in pure and it["cta"] != max(load):
+            per_kind.setdefault(next(iter(pure[it["cta"]])), {}).setdefault(it["cta"], 0)
+            per_kind[next(iter(pure[it["cta"]]))][it["cta"]] += it["e"] - it["a"]
+    nw = np.median(list(per_kind["wide"].values()))
+    nn = np.median(list(per_kind["narrow"].values()))
+    assert abs(nn / nw - 1.25) < 0.05
+
+
 def test_mixed_batch_validation():
     prob = _problem(B=3, S_q=4)
     T = [5, 6, 7]
