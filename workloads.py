@@ -274,10 +274,11 @@ def packed_view(w: Workload) -> Workload:
                     index_indptr=w.index_indptr, index_list=w.index_list, meta=dict(w.meta))
 
 
-def quantized(device="cpu", fmt="int8", B=32, lo=2048, hi=32768):
+def quantized(device="cpu", fmt="int8", B=32, lo=2048, hi=32768, S_q=1):
     meta = torch.Generator().manual_seed(4)
     lens = torch.randint(lo, hi + 1, (B,), generator=meta).tolist()
-    return quantized_history(f"quantized KV ({fmt}) B={B} T~U[{lo},{hi}]", B=B, S_q=1, H_q=32,
+    rows = f" S_q={S_q}" if S_q != 1 else ""
+    return quantized_history(f"quantized KV ({fmt}) B={B} T~U[{lo},{hi}]{rows}", B=B, S_q=S_q, H_q=32,
                              H_kv=8, d=128, lens=lens, P=16, seed=4, device=device, fmt=fmt)
 
 
