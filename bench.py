@@ -49,12 +49,13 @@ MIN_SAMPLES = 50
 # extra workloads --workload can time alone.
 CONFIGS = ("tiny", "long-s1", "long-s4", "sink-window", "index-list", "int8", "int4-kivi")
 OTHER_WORKLOADS = ("tiny", "long-s1", "long-s4", "sink-window", "index-list", "packed", "tree-verify", "mixed",
-                   "int8", "fp8", "fp8-e5m2", "int4-head", "int4-kivi", "int4-kivi-s4")
+                   "int8", "fp8", "fp8-e5m2", "int4-head", "int4-kivi", "int4-kivi-s4", "int4-kivi-d64", "int4-kivi-p96")
 CONFIG_LABEL = {"tiny": "1 tiny contiguous", "long-s1": "3 long context S_q=1", "long-s4": "3 long context S_q=4",
                 "sink-window": "4a sink + window", "index-list": "4b index lists", "int8": "5a INT8",
                 "int4-kivi": "5b KIVI INT4"}
 QUANT = {"int8": "int8", "fp8": "fp8_e4m3", "fp8-e5m2": "fp8_e5m2", "int4-head": "int4_head",
-         "int4-kivi": "int4_kivi", "int4-kivi-s4": "int4_kivi"}
+         "int4-kivi": "int4_kivi", "int4-kivi-s4": "int4_kivi", "int4-kivi-d64": "int4_kivi",
+         "int4-kivi-p96": "int4_kivi"}
 
 
 def parse():
@@ -420,8 +421,10 @@ def build_workload(dattn, name, dev):
     import workloads as W
     if name in QUANT:
         # int4-kivi-s4: the quantized workload with 4 verify rows per request (16 rows per kv
-        # head), a KIVI shape that runs on the CUDA-core byte-format kernel
-        w = W.quantized(dev, fmt=QUANT[name], S_q=4 if name.endswith("-s4") else 1)
+        # head); int4-kivi-d64: 64-channel heads (V channel groups of 16); int4-kivi-p96:
+        # 96-token pages, the KIVI shape that runs on the CUDA-core byte-format kernel
+        w = W.quantized(dev, fmt=QUANT[name], S_q=4 if name.endswith("-s4") else 1,
+                        d=64 if name.endswith("-d64") else 128, P=96 if name.endswith("-p96") else 16)
         p, cache = quantized_cache(dattn, w, QUANT[name], dev)
         w.k_rows = w.v_rows = None          # the bf16 history is no longer needed
         return w, p, cache

@@ -33,13 +33,14 @@ enum StatusBits : int32_t {
   kStPipeline = 64,     // a consumer found a ring stage stamped with another stage number
 };
 
-// KIVI INT4 problems with d = 128, at most 8 rows, Gv = 32, an interval
-// visibility program and a power-of-two page size P run on the tensor-core
-// kernel (partial_q4.cu); other KIVI problems on the byte-format kernel
-// (partial.cu).  The residual length R is any positive multiple of G on both.
+// KIVI INT4 problems with d = 128 (Gv = 16 or 32) or d = 64 (Gv = 16), at most
+// 32 rows, an interval visibility program and a power-of-two page size P run
+// on the tensor-core kernel (partial_q4.cu); other KIVI problems on the
+// byte-format kernel (partial.cu).  The residual length R is any positive
+// multiple of G on both.
 inline bool kivi_on_tensor_cores(int d, int rows, int Gv, int mask, int P, int R) {
-  return d == 128 && rows <= 8 && Gv == 32 && mask != DATTN_MASK_INDEX_LIST && P > 0 && (P & (P - 1)) == 0 &&
-         R > 0;
+  return ((d == 128 && (Gv == 16 || Gv == 32)) || (d == 64 && Gv == 16)) && rows <= 32 &&
+         mask != DATTN_MASK_INDEX_LIST && P > 0 && (P & (P - 1)) == 0 && R > 0;
 }
 
 // Partial states an item leaves per query row.  Consumer warps are arranged
@@ -49,8 +50,9 @@ inline bool kivi_on_tensor_cores(int d, int rows, int Gv, int mask, int P, int R
 // warp leaves the state of its block's rows over its own share of the item's
 // keys.
 inline int states_per_item(int rows, int fmt, bool kivi_tc) {
-  if (fmt == DATTN_FMT_INT4_HEAD) return kConsumerWarps / (rows <= 8 ? 1 : rows <= 16 ? 2 : 4);
-  if (fmt != DATTN_FMT_INT4_KIVI || kivi_tc) return kConsumerWarps / (rows <= 16 ? 1 : 2);
+  if (fmt == DATTN_FMT_INT4_HEAD || (fmt == DATTN_FMT_INT4_KIVI && kivi_tc))
+    return kConsumerWarps / (rows <= 8 ? 1 : rows <= 16 ? 2 : 4);
+  if (fmt != DATTN_FMT_INT4_KIVI) return kConsumerWarps / (rows <= 16 ? 1 : 2);
   return kConsumerWarps / (rows <= 4 ? 1 : rows <= 8 ? 2 : rows <= 16 ? 4 : 8);
 }
 
@@ -164,7 +166,7 @@ struct MergeParams {
 int launch_partial(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_partial_bf16(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_partial_q8(const PartialParams& p, int d, int n_ctas, void* stream);
-int launch_partial_q4(const PartialParams& p, int n_ctas, void* stream);
+int launch_partial_q4(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_partial_q4h(const PartialParams& p, int d, int n_ctas, void* stream);
 int launch_merge(const MergeParams& p, int d, void* stream);
 

@@ -786,7 +786,7 @@ int launch_partial(const PartialParams& p, int d, int n_ctas, void* stream) {
   if (p.fmt == DATTN_FMT_INT8_TOKEN || p.fmt == DATTN_FMT_FP8_E4M3 || p.fmt == DATTN_FMT_FP8_E5M2)
     return launch_partial_q8(p, d, n_ctas, stream);
   if (p.fmt == DATTN_FMT_INT4_HEAD) return launch_partial_q4h(p, d, n_ctas, stream);
-  if (kivi_on_tensor_cores(d, p.rows, p.kivi_Gv, p.mask, p.P, p.kivi_R)) return launch_partial_q4(p, n_ctas, stream);
+  if (kivi_on_tensor_cores(d, p.rows, p.kivi_Gv, p.mask, p.P, p.kivi_R)) return launch_partial_q4(p, d, n_ctas, stream);
   return d == 64 ? launch_one<64, DATTN_FMT_INT4_KIVI>(p, n_ctas, stream)
                  : launch_one<128, DATTN_FMT_INT4_KIVI>(p, n_ctas, stream);
 }

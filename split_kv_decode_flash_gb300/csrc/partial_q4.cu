@@ -1,10 +1,10 @@
 // Partial kernel of split-KV decode attention for KIVI INT4 K/V ("M8.6 Live-
-// Data Quantization", §0x06A-B format) on the tensor cores, for d_h = 128,
-// at most 8 query rows per kv head and V channel groups Gv >= 32 (other KIVI
+// Data Quantization", §0x06A-B format) on the tensor cores, for d_h = 64 and
+// 128, at most 32 query rows per kv head and V channel groups Gv = 32 (other KIVI
 // shapes, and index-list visibility programs, run on the byte-format kernel).
 //
 // Same persistent producer / consumer structure as the bf16 and INT8
-// kernels.  Quantized keys move in stages of 256 (32 KB of codes); the
+// kernels.  Quantized keys move in stages of 256 (32 KB of codes at d = 128); the
 // residual keys (bf16 rows of the per-request ring) in stages of 64.
 //
 // Producer.  Per quantized stage: the codes of every key row (16-byte
@@ -16,7 +16,8 @@
 // alongside the keys' pages.
 //
 // Consumers (two stage groups of four warps; keys on the M side of the mma,
-// as in the INT8 kernel):
+// as in the INT8 kernel; a warp scores one block of 8 query rows, and 2 or 4
+// blocks share a stage's keys between fewer warps each):
 //   Codes enter the mma as f16 subnormals: a nibble masked in place into the
 //   mantissa of an f16 is the exact value code * 2^-24 (bits 0-3) or
 //   code * 2^-20 (bits 4-7), so a word of eight codes becomes four f16 pairs
@@ -45,7 +46,6 @@ namespace dattn {
 
 namespace {
 
-constexpr int kD = 128;
 constexpr int kQKeys = 256;           // keys of a quantized stage
 constexpr int kRKeys = 64;            // keys of a residual stage
 constexpr int kQSlots = kQKeys / 32;  // slots per producer lane
@@ -54,16 +54,19 @@ constexpr int kQ4ProducerRegs = 104;
 constexpr int kQ4ConsumerRegs = 200;
 static_assert(128 * kQ4ProducerRegs + 32 * kConsumerWarps * kQ4ConsumerRegs <= kThreads * 168, "register split");
 
+template <int D, int GV>
 struct Q4 {
   static constexpr int kStagesN = 4;               // even: stage groups alternate
-  static constexpr int kCodeRow = kD / 2;          // bytes of a key's codes
-  static constexpr int kTile = kQKeys * kCodeRow;  // 16 KB of codes per tensor
-  static constexpr int kGT = kMaxGroups * kD * 4;  // K-group (s, z) table
-  static constexpr int kVQ = kQKeys * 16;          // per-key V (s, z) pairs, Gv = 32
+  static constexpr int kCodeRow = D / 2;           // bytes of a key's codes
+  static constexpr int kTile = kQKeys * kCodeRow;  // 16 KB (d = 128) of codes per tensor
+  static constexpr int kGT = kMaxGroups * D * 4;   // K-group (s, z) table
+  static constexpr int kVQB = D / GV * 4;          // bytes of a key's V (s, z) pairs: 16 or 32
+  static_assert(kVQB == 16 || kVQB == 32, "V qparams of a key: one or two 16-byte chunks");
+  static constexpr int kVQ = kQKeys * kVQB;
   static constexpr int kOffGT = 2 * kTile;
   static constexpr int kOffVQ = kOffGT + kGT;
   static constexpr int kStage = (kOffVQ + kVQ + 127) / 128 * 128;
-  static_assert(kStage >= 2 * kRKeys * kD * 2, "a residual stage fits in a stage slot");
+  static_assert(kStage >= 2 * kRKeys * D * 2, "a residual stage fits in a stage slot");
   static constexpr int kPos = kStagesN * kStage;   // int32 [stages][kQKeys]: logical key per slot
   static constexpr int kRows = kPos + kStagesN * kQKeys * 4;   // uint32 [stages][kQKeys]: source row per slot
   static constexpr int kFlags = kRows + kStagesN * kQKeys * 4;
@@ -76,10 +79,13 @@ struct Q4 {
   static_assert(kTotal <= 232448, "shared memory of one CTA");
 };
 
-// 64-byte code rows: 16-byte chunk c of slot s, swizzled so that the eight
-// rows an ldmatrix reads fall in distinct bank groups.
+// Code rows of ROWB = 64 (d = 128) or 32 (d = 64) bytes: 16-byte chunk c of
+// slot s, swizzled so that the eight rows an ldmatrix reads fall in distinct
+// bank groups.
+template <int ROWB>
 __device__ __forceinline__ uint32_t code_off(int s, int c) {
-  return static_cast<uint32_t>(s * 64 + ((c ^ ((s >> 1) & 3)) << 4));
+  if constexpr (ROWB == 64) return static_cast<uint32_t>(s * 64 + ((c ^ ((s >> 1) & 3)) << 4));
+  else return static_cast<uint32_t>(s * 32 + ((c ^ ((s >> 2) & 1)) << 4));
 }
 
 // Masks of the low and the high nibble of bytes 0 and 2 of a code word; the
@@ -101,6 +107,16 @@ __device__ __forceinline__ uint32_t times16_bf16x2(uint32_t w) {
 }
 
 __device__ __forceinline__ float2 h2f2(uint32_t w) { return __half22float2(*reinterpret_cast<const __half2*>(&w)); }
+
+// A key's V (s, z) pairs, one word per channel group (4 or 8 groups).
+template <int NG>
+__device__ __forceinline__ void load_vq(const uint8_t* src, uint32_t (&w)[NG]) {
+#pragma unroll
+  for (int i = 0; i < NG / 4; ++i) {
+    const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+    w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+  }
+}
 
 // ---- stages -------------------------------------------------------------------------
 
@@ -277,8 +293,9 @@ __device__ __forceinline__ Q4Desc q4_rows(const Walk& w, const QCur& c, const in
   return d;
 }
 
+template <int D, int GV>
 __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
-  using C = Q4;
+  using C = Q4<D, GV>;
   const PartialParams& p = w.p;
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
   const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
@@ -331,28 +348,30 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool 
     }
     const uint32_t kt = smem_u32(smem + st * C::kStage), vt = kt + C::kTile;
     if (r0.resid) {
-      // bf16 rows of the residual ring: 64 slots, 16 chunks per row, two rows per instruction
-      const uint32_t rkt = kt, rvt = kt + kRKeys * kD * 2;
-      const int sub = lane >> 4, ch = lane & 15;
+      // bf16 rows of the residual ring: 64 slots, RC chunks per row, 32 / RC rows per instruction
+      constexpr int RC = D * 2 / 16;
+      const uint32_t rkt = kt, rvt = kt + kRKeys * D * 2;
+      const int sub = lane / RC, ch = lane % RC;
 #pragma unroll 1
-      for (int s0 = 0; s0 < kRKeys; s0 += 2) {
+      for (int s0 = 0; s0 < kRKeys; s0 += 32 / RC) {
         const int s = s0 + sub;
         const uint32_t row = rows[s];
         const bool ok = row != kNoRow;
-        const size_t off = static_cast<size_t>(ok ? row : 0u) * (kD * 2) + ch * 16;
-        const uint32_t dst = tile_off<kD * 2>(s, ch);
+        const size_t off = static_cast<size_t>(ok ? row : 0u) * (D * 2) + ch * 16;
+        const uint32_t dst = tile_off<D * 2>(s, ch);
         cp_async16(rkt + dst, kres + off, ok ? 16u : 0u, stream_pol);
         cp_async16(rvt + dst, vres + off, ok ? 16u : 0u, stream_pol);
       }
     } else {
-      // codes: 256 slots, 4 chunks per row, eight rows per instruction
-      // (the swizzle of slot s0 + sub only depends on sub, as s0 steps by 8)
-      const int sub = lane >> 2, ch = lane & 3;
-      const uint32_t dst0 = code_off(sub, ch);
+      // codes: 256 slots, CC chunks per row, 32 / CC rows per instruction (the
+      // swizzle of slot s0 + sub only depends on sub, as s0 steps by a multiple of 8)
+      constexpr int CC = C::kCodeRow / 16;
+      const int sub = lane / CC, ch = lane % CC;
+      const uint32_t dst0 = code_off<C::kCodeRow>(sub, ch);
       const char* kb = kbase + ch * 16;
       const char* vb = vbase + ch * 16;
 #pragma unroll 4
-      for (int s0 = 0; s0 < kQKeys; s0 += 8) {
+      for (int s0 = 0; s0 < kQKeys; s0 += 32 / CC) {
         const uint32_t row = rows[s0 + sub];
         const bool ok = row != kNoRow;
         const size_t off = static_cast<size_t>(ok ? row : 0u) * C::kCodeRow;
@@ -360,23 +379,27 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool 
         cp_async16(kt + dst, kb + off, ok ? 16u : 0u, stream_pol);
         cp_async16(vt + dst, vb + off, ok ? 16u : 0u, stream_pol);
       }
-      // per-key V qparams
+      // per-key V qparams (one or two 16-byte chunks)
       const uint32_t vq = kt + C::kOffVQ;
 #pragma unroll 1
       for (int s = lane; s < kQKeys; s += 32) {
         const uint32_t row = rows[s];
         const bool ok = row != kNoRow;
-        cp_async16(vq + 16 * s, vqbase + static_cast<size_t>(ok ? row : 0u) * 16, ok ? 16u : 0u, stream_pol);
+        const char* src = vqbase + static_cast<size_t>(ok ? row : 0u) * C::kVQB;
+#pragma unroll
+        for (int i = 0; i < C::kVQB / 16; ++i)
+          cp_async16(vq + C::kVQB * s + 16 * i, src + 16 * i, ok ? 16u : 0u, stream_pol);
       }
-      // K-group qparams table: group k (lane k's description) -> 32 chunks of 16 bytes
+      // K-group qparams table: group k (lane k's description) -> D / 4 chunks of 16 bytes
       const uint32_t gt = kt + C::kOffGT;
       const WorkItem it = w.rec(c0.ii).it;
       const int n_g = stage_groups_of(it, c0.j0, c0.j1, sh.gsh).n;
       for (int g = 0; g < n_g && g < kMaxGroups; ++g) {
         const uint32_t grow = __shfl_sync(kAll, r0.grow, g);
         const bool ok = grow != kNoRow;
-        cp_async16(gt + g * kD * 4 + lane * 16, kqbase + static_cast<size_t>(ok ? grow : 0u) * kD * 4 + lane * 16,
-                   ok ? 16u : 0u, stream_pol);
+        if (lane < D / 4)
+          cp_async16(gt + g * D * 4 + lane * 16, kqbase + static_cast<size_t>(ok ? grow : 0u) * D * 4 + lane * 16,
+                     ok ? 16u : 0u, stream_pol);
       }
     }
     const uint32_t fb = full0 + 8 * st;
@@ -434,16 +457,18 @@ __device__ __forceinline__ float fma_q_zhi(uint32_t q, uint32_t zw, float c) {
 // (32 c + 8 t4 + k, 32 c + 8 t4 + k + 4); the pairs k = 0, 2 (which meet
 // low-nibble codes) carry 16 q.  A row whose largest |q| exceeds 2^10 is
 // scaled by a power of two wq (qinv = 1 / wq) so that 16 q stays in range.
+template <int D>
 struct QRow {
-  uint32_t qh[kD / 32][4];
+  uint32_t qh[D / 32][4];
   float qinv;
 };
 
-__device__ __forceinline__ void load_qrow(const __nv_bfloat16* qrow, bool ok, QRow& r, int t4) {
-  float qf[kD / 4];
+template <int D>
+__device__ __forceinline__ void load_qrow(const __nv_bfloat16* qrow, bool ok, QRow<D>& r, int t4) {
+  float qf[D / 4];
   float mx = 0.f;
 #pragma unroll
-  for (int c = 0; c < kD / 32; ++c) {
+  for (int c = 0; c < D / 32; ++c) {
     uint4 wq = make_uint4(0u, 0u, 0u, 0u);
     if (ok) wq = *reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * t4);
     const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
@@ -460,7 +485,7 @@ __device__ __forceinline__ void load_qrow(const __nv_bfloat16* qrow, bool ok, QR
   const float wq = mx > 1024.f ? exp2f(10.f - ceilf(__log2f(mx))) : 1.f;
   r.qinv = 1.f / wq;
 #pragma unroll
-  for (int c = 0; c < kD / 32; ++c)
+  for (int c = 0; c < D / 32; ++c)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float f = (k & 1) ? wq : 16.f * wq;
@@ -476,21 +501,21 @@ __device__ __forceinline__ void load_qrow(const __nv_bfloat16* qrow, bool ok, QR
 // the hi parts and lo the lo parts of rows 0-7.  Per-row terms for rows ra,
 // rb: off = sum_c q_c z_gc and inv = 2^20 / (wq w), w a power of two that
 // keeps a row's hi parts finite (1 unless a product nears the f16 limit).
-template <bool PACKED>
+template <int D, bool PACKED>
 struct QPrime {
-  uint32_t b[kD / 16][2];
-  uint32_t lo[PACKED ? 1 : kD / 16][2];
+  uint32_t b[D / 16][2];
+  uint32_t lo[PACKED ? 1 : D / 16][2];
   float offa, offb, inva, invb;
 };
 
-template <bool PACKED>
-__device__ __forceinline__ void make_qprime(const QRow& q, const uint8_t* gt_row, int t4, bool lo_lane, int ra,
-                                            QPrime<PACKED>& out) {
-  uint32_t hi[kD / 32][4], lo[kD / 32][4];
+template <int D, bool PACKED>
+__device__ __forceinline__ void make_qprime(const QRow<D>& q, const uint8_t* gt_row, int t4, bool lo_lane, int ra,
+                                            QPrime<D, PACKED>& out) {
+  uint32_t hi[D / 32][4], lo[D / 32][4];
   float offe = 0.f, offo = 0.f;   // sum q z over the pairs carrying 16 q, and over the others
   uint32_t mx2 = 0u;
 #pragma unroll
-  for (int c = 0; c < kD / 32; ++c) {
+  for (int c = 0; c < D / 32; ++c) {
     // (s, z) of channels 32 c + 8 t4 + 0..7
     const uint4 w0 = *reinterpret_cast<const uint4*>(gt_row + (32 * c + 8 * t4) * 4);
     const uint4 w1 = *reinterpret_cast<const uint4*>(gt_row + (32 * c + 8 * t4) * 4 + 16);
@@ -515,7 +540,7 @@ __device__ __forceinline__ void make_qprime(const QRow& q, const uint8_t* gt_row
     // rare: a product reached the f16 limit; redo the row's split in f32 at a scale w
     float pm = 0.f;
 #pragma unroll
-    for (int c = 0; c < kD / 32; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
       const uint4 w0 = *reinterpret_cast<const uint4*>(gt_row + (32 * c + 8 * t4) * 4);
       const uint4 w1 = *reinterpret_cast<const uint4*>(gt_row + (32 * c + 8 * t4) * 4 + 16);
       const uint32_t sz[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -529,7 +554,7 @@ __device__ __forceinline__ void make_qprime(const QRow& q, const uint8_t* gt_row
     pm = fmaxf(pm, __shfl_xor_sync(kAll, pm, 2));
     w = pm > 16384.f ? exp2f(14.f - ceilf(__log2f(pm))) : 1.f;
 #pragma unroll
-    for (int c = 0; c < kD / 32; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
       const uint4 w0 = *reinterpret_cast<const uint4*>(gt_row + (32 * c + 8 * t4) * 4);
       const uint4 w1 = *reinterpret_cast<const uint4*>(gt_row + (32 * c + 8 * t4) * 4 + 16);
       const uint32_t sz[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -544,7 +569,7 @@ __device__ __forceinline__ void make_qprime(const QRow& q, const uint8_t* gt_row
     }
   }
 #pragma unroll
-  for (int c = 0; c < kD / 32; ++c) {
+  for (int c = 0; c < D / 32; ++c) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int ks = 2 * c + (k >> 1), r = k & 1;
@@ -570,17 +595,17 @@ __device__ __forceinline__ void make_qprime(const QRow& q, const uint8_t* gt_row
 
 // Raw S'^T (16 keys x 8 columns) = codes . B for the 16 keys at slot "base",
 // in 2^-20 units; separate accumulators keep the mma chains short.
-template <bool PACKED>
-__device__ __forceinline__ void k_mma(uint32_t kt, int base, int lrow, int lmat, const QPrime<PACKED>& q,
+template <int D, bool PACKED>
+__device__ __forceinline__ void k_mma(uint32_t kt, int base, int lrow, int lmat, const QPrime<D, PACKED>& q,
                                       float (&s)[4]) {
   constexpr int NA = PACKED ? 2 : 4;
   float acc[NA][4];
 #pragma unroll
   for (int x = 0; x < NA; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
 #pragma unroll
-  for (int c2 = 0; c2 < kD / 64; ++c2) {
+  for (int c2 = 0; c2 < D / 64; ++c2) {
     uint32_t v[4];
-    ldsm_x4(kt + code_off(base + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1], v[2], v[3]);
+    ldsm_x4(kt + code_off<D / 2>(base + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1], v[2], v[3]);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int c = 2 * c2 + hh;
@@ -608,11 +633,11 @@ __device__ __forceinline__ void k_mma(uint32_t kt, int base, int lrow, int lmat,
   }
 }
 
-template <bool PACKED>
+template <int D, int GV, bool PACKED>
 __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
-  using C = Q4;
-  constexpr int NT = kD / 16;                 // output tiles (8)
-  constexpr int kCg = kD / 32;                // V channel groups (Gv = 32)
+  using C = Q4<D, GV>;
+  constexpr int NT = D / 16;                  // output tiles
+  constexpr int kCg = D / GV;                 // V channel groups
   constexpr int NS = PACKED ? 2 : 1;          // 16-key sub-blocks per step
   const PartialParams& p = w.p;
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
@@ -621,21 +646,31 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
 
   constexpr int ng = 2;
   constexpr int wps = kConsumerWarps / ng;
-  const int sgrp = cw / wps, ts = cw % wps;
-  const int my_state = cw;
+  // row blocks of 8 rows (PACKED: one block of at most 4) split a stage's keys
+  // among the four warps of a stage group: 1 block, a quarter of the keys a
+  // warp; 2 blocks, a half; 4 blocks, all of them
+  const int nrb = PACKED || p.rows <= 8 ? 1 : p.rows <= 16 ? 2 : 4;
+  const int sgrp = cw / wps, wi = cw % wps;
+  const int rbk = wi % nrb, ts = wi / nrb;
+  const int splits = wps / nrb;
+  const int my_state = sgrp * splits + ts;
   const int g4 = lane >> 2, t4 = lane & 3;
   // rows of the lane's score, probability and output fragments (PACKED: lanes
-  // t4 = 2, 3 repeat the rows of lanes t4 = 0, 1 and write nothing)
-  const int ra = PACKED ? 2 * (t4 & 1) : 2 * t4, rb = ra + 1;
+  // t4 = 2, 3 repeat the rows of lanes t4 = 0, 1 and write nothing); lra is
+  // the row within the block
+  const int lra = PACKED ? 2 * (t4 & 1) : 2 * t4;
+  const int ra = 8 * rbk + lra, rb = ra + 1;
   const bool writer = !PACKED || t4 < 2;
   const bool oka = ra < p.rows, okb = rb < p.rows;
   const int qia = ra / p.g, qib = rb / p.g;
   // query row of the lane's B fragments
-  const int rq = PACKED ? (g4 & 3) : g4;
+  const int rq = PACKED ? (g4 & 3) : 8 * rbk + g4;
   const bool okq = rq < p.rows, lo_lane = PACKED && g4 >= 4;
   const int lrow = lane & 7, lmat = lane >> 3;
   const float sc = p.scale_log2;
   const int gsh = p.kivi_G == 32 ? 5 : 6;   // log2 G
+  // Gv = 16: the lane's V code rows belong to channel group 2 c (g4 < 4) or 2 c + 1
+  const uint32_t gmask_lo = g4 < 4 ? kNibLo : 0u, gmask_hi = g4 < 4 ? kNibHi : 0u;
 
   uint32_t k = 0;
   bool dead = false;
@@ -644,8 +679,8 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
     const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
     const int jq = residual_start(p, it);
     const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
-                                ((static_cast<long long>(it.b) * p.S_q + rq / p.g) * p.H_q + it.h * p.g + rq % p.g) * kD;
-    QRow qr;
+                                ((static_cast<long long>(it.b) * p.S_q + rq / p.g) * p.H_q + it.h * p.g + rq % p.g) * D;
+    QRow<D> qr;
     load_qrow(qrow, okq, qr, t4);
     float o[NT][4];
 #pragma unroll
@@ -654,7 +689,7 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
     float za[kCg], zb[kCg];   // per V channel group and row: sum_t p_t z_t
 #pragma unroll
     for (int x = 0; x < kCg; ++x) za[x] = zb[x] = 0.f;
-    QPrime<PACKED> qp;
+    QPrime<D, PACKED> qp;
     int cur_gid = -1;         // K group whose Q' is in qp
 
     for (int j0 = it.a; j0 < it.e; ++k) {
@@ -684,7 +719,7 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
       const StageGroups sg = stage_groups_of(it, j0, j1, gsh);
       const uint8_t* gt = stage + C::kOffGT;
       const uint8_t* vq = stage + C::kOffVQ;
-      const int slice = resid ? kRKeys / wps : kQKeys / wps;
+      const int slice = resid ? kRKeys / splits : kQKeys / splits;
 
       for (int b0 = 0; b0 < slice; b0 += 16 * NS) {
         const int base0 = ts * slice + b0;
@@ -713,12 +748,12 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
           }
           for (int sel = sel0; sel <= sel1; ++sel) {
             if (sg.gid(sel) != cur_gid) {
-              make_qprime<PACKED>(qr, gt + sel * kD * 4, t4, lo_lane, ra, qp);
+              make_qprime<D, PACKED>(qr, gt + sel * D * 4, t4, lo_lane, lra, qp);
               cur_gid = sg.gid(sel);
             }
             float t[NS][4];
 #pragma unroll
-            for (int u = 0; u < NS; ++u) k_mma<PACKED>(kt, base0 + 16 * u, lrow, lmat, qp, t[u]);
+            for (int u = 0; u < NS; ++u) k_mma<D, PACKED>(kt, base0 + 16 * u, lrow, lmat, qp, t[u]);
 #pragma unroll
             for (int u = 0; u < NS; ++u) {
               if (selx[u] == sel) {
@@ -737,9 +772,9 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
           const uint32_t* qw = reinterpret_cast<const uint32_t*>(qrow);
           const bool okb16 = okq && !lo_lane;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
+          for (int kk = 0; kk < D / 16; ++kk) {
             uint32_t a[4];
-            ldsm_x4(kt + tile_off<kD * 2>(base0 + (lmat & 1) * 8 + lrow, 2 * kk + (lmat >> 1)), a[0], a[1], a[2], a[3]);
+            ldsm_x4(kt + tile_off<D * 2>(base0 + (lmat & 1) * 8 + lrow, 2 * kk + (lmat >> 1)), a[0], a[1], a[2], a[3]);
             mma_bf16(s[0], a, okb16 ? qw[8 * kk + t4] : 0u, okb16 ? qw[8 * kk + 4 + t4] : 0u);
           }
           if constexpr (PACKED) {
@@ -823,9 +858,9 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
           for (int u = 0; u < NS; ++u) {
             const int kx = base0 + 16 * u + g4, ky = kx + 8;
             // per channel group: P' = p s_v (f16 pairs) as the B operand, sum p z_v aside
-            const uint4 vqx = *reinterpret_cast<const uint4*>(vq + 16 * kx);
-            const uint4 vqy = *reinterpret_cast<const uint4*>(vq + 16 * ky);
-            const uint32_t sx[4] = {vqx.x, vqx.y, vqx.z, vqx.w}, sy[4] = {vqy.x, vqy.y, vqy.z, vqy.w};
+            uint32_t sx[kCg], sy[kCg];
+            load_vq<kCg>(vq + C::kVQB * kx, sx);
+            load_vq<kCg>(vq + C::kVQB * ky, sy);
             // rows (ra, rb) of keys g4 and g4 + 8
             const uint32_t px = pack_f16(pr[u][0], pr[u][1]), py = pack_f16(pr[u][2], pr[u][3]);
             uint32_t pb[kCg][2];
@@ -838,20 +873,34 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
             }
             // O'^T += V^T codes . P'^T
 #pragma unroll
-            for (int c2 = 0; c2 < kD / 64; ++c2) {
+            for (int c2 = 0; c2 < D / 64; ++c2) {
               uint32_t v[4];
-              ldsm_x4_trans(vt + code_off(base0 + 16 * u + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1],
+              ldsm_x4_trans(vt + code_off<D / 2>(base0 + 16 * u + (lmat & 1) * 8 + lrow, 2 * c2 + (lmat >> 1)), v[0], v[1],
                             v[2], v[3]);
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
-                const int c = 2 * c2 + hh;   // code chunk c = V channel group c
+                const int c = 2 * c2 + hh;   // code chunk c: channels 32 c .. 32 c + 31
                 const uint32_t lo_keys = v[2 * hh], hi_keys = v[2 * hh + 1];
                 const uint32_t lo8 = lo_keys >> 8, hi8 = hi_keys >> 8;
                 // M rows g4 (even channel, low nibble) and g4 + 8 (odd channel, high nibble: 16 x)
-                const uint32_t a0[4] = {lo_keys & kNibLo, lo_keys & kNibHi, hi_keys & kNibLo, hi_keys & kNibHi};
-                mma_f16(o[2 * c], a0, pb[c][0], pb[c][1]);
-                const uint32_t a1[4] = {lo8 & kNibLo, lo8 & kNibHi, hi8 & kNibLo, hi8 & kNibHi};
-                mma_f16(o[2 * c + 1], a1, pb[c][0], pb[c][1]);
+                if constexpr (GV == 32) {   // chunk c is channel group c
+                  const uint32_t a0[4] = {lo_keys & kNibLo, lo_keys & kNibHi, hi_keys & kNibLo, hi_keys & kNibHi};
+                  mma_f16(o[2 * c], a0, pb[c][0], pb[c][1]);
+                  const uint32_t a1[4] = {lo8 & kNibLo, lo8 & kNibHi, hi8 & kNibLo, hi8 & kNibHi};
+                  mma_f16(o[2 * c + 1], a1, pb[c][0], pb[c][1]);
+                } else {
+                  // Gv = 16: the M rows of lanes g4 < 4 (channels 32 c + 0..15) are group
+                  // 2 c, those of lanes g4 >= 4 group 2 c + 1; each group's mma sees the
+                  // other group's rows as zero codes
+#pragma unroll
+                  for (int e = 0; e < 2; ++e) {
+                    const uint32_t ml = e ? kNibLo ^ gmask_lo : gmask_lo, mh = e ? kNibHi ^ gmask_hi : gmask_hi;
+                    const uint32_t a0[4] = {lo_keys & ml, lo_keys & mh, hi_keys & ml, hi_keys & mh};
+                    mma_f16(o[2 * c], a0, pb[2 * c + e][0], pb[2 * c + e][1]);
+                    const uint32_t a1[4] = {lo8 & ml, lo8 & mh, hi8 & ml, hi8 & mh};
+                    mma_f16(o[2 * c + 1], a1, pb[2 * c + e][0], pb[2 * c + e][1]);
+                  }
+                }
               }
             }
           }
@@ -863,14 +912,14 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
           // V^T in the quantized tiles' channel order: keys 2 t4, 2 t4 + 1 (and + 8)
           // at channels 32 c + 4 g4 + 0..3 (8 bytes of a bf16 row)
           const int ka = base0 + 2 * t4, kb2 = base0 + 8 + 2 * t4;
-          const uint8_t* rv = stage + kRKeys * kD * 2;
+          const uint8_t* rv = stage + kRKeys * D * 2;
 #pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             const int chunk = 4 * c + (g4 >> 1), boff = 8 * (g4 & 1);
-            const uint2 wa = *reinterpret_cast<const uint2*>(rv + tile_off<kD * 2>(ka, chunk) + boff);
-            const uint2 wb = *reinterpret_cast<const uint2*>(rv + tile_off<kD * 2>(ka + 1, chunk) + boff);
-            const uint2 wc = *reinterpret_cast<const uint2*>(rv + tile_off<kD * 2>(kb2, chunk) + boff);
-            const uint2 wd = *reinterpret_cast<const uint2*>(rv + tile_off<kD * 2>(kb2 + 1, chunk) + boff);
+            const uint2 wa = *reinterpret_cast<const uint2*>(rv + tile_off<D * 2>(ka, chunk) + boff);
+            const uint2 wb = *reinterpret_cast<const uint2*>(rv + tile_off<D * 2>(ka + 1, chunk) + boff);
+            const uint2 wc = *reinterpret_cast<const uint2*>(rv + tile_off<D * 2>(kb2, chunk) + boff);
+            const uint2 wd = *reinterpret_cast<const uint2*>(rv + tile_off<D * 2>(kb2 + 1, chunk) + boff);
             // M rows g4 + 8 carry the factor 16 of the quantized tiles' high nibbles
             const uint32_t a0[4] = {__byte_perm(wa.x, wb.x, 0x5410u), times16_bf16x2(__byte_perm(wa.x, wb.x, 0x7632u)),
                                     __byte_perm(wc.x, wd.x, 0x5410u), times16_bf16x2(__byte_perm(wc.x, wd.x, 0x7632u))};
@@ -905,11 +954,15 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
         const float m = rr ? mb : ma, l = rr ? lb : la;
         const int i = row / p.g, hq = it.h * p.g + row % p.g;
         const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
-        float val[kD / 32][4];
+        float val[D / 32][4];
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
-          // accumulator rows g4 in 2^-24 units, rows g4 + 8 in 2^-20 units
-          const float add = rr ? zb[c] : za[c];
+        for (int c = 0; c < D / 32; ++c) {
+          // accumulator rows g4 in 2^-24 units, rows g4 + 8 in 2^-20 units; the lane's
+          // channels 32 c + 4 g4 + 0..3 lie in V channel group c (Gv = 32) or
+          // 2 c + (g4 >= 4) (Gv = 16)
+          float add;
+          if constexpr (GV == 32) add = rr ? zb[c] : za[c];
+          else add = g4 < 4 ? (rr ? zb[2 * c] : za[2 * c]) : (rr ? zb[2 * c + 1] : za[2 * c + 1]);
           val[c][0] = fmaf(o[2 * c][rr], kCodeUnit, add);
           val[c][1] = fmaf(o[2 * c][2 + rr], kCodeUnit / 16.f, add);
           val[c][2] = fmaf(o[2 * c + 1][rr], kCodeUnit, add);
@@ -917,9 +970,9 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
         }
         if (it.slot < 0) {
           const float inv = l > 0.f ? 1.f / l : 0.f;
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * kD;
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
 #pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + 32 * c + 4 * g4);
             dst[0] = __floats2bfloat162_rn(val[c][0] * inv, val[c][1] * inv);
             dst[1] = __floats2bfloat162_rn(val[c][2] * inv, val[c][3] * inv);
@@ -927,9 +980,9 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
           if (g4 == 0 && p.lse) p.lse[orow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         } else {
           const long long srow = static_cast<long long>(it.slot + my_state) * p.rows + row;
-          float* u = p.u + srow * kD;
+          float* u = p.u + srow * D;
 #pragma unroll
-          for (int c = 0; c < kD / 32; ++c)
+          for (int c = 0; c < D / 32; ++c)
             *reinterpret_cast<float4*>(u + 32 * c + 4 * g4) = make_float4(val[c][0], val[c][1], val[c][2], val[c][3]);
           if (g4 == 0) p.ml[srow] = make_float2(l > 0.f ? m : -INFINITY, l);
         }
@@ -941,8 +994,9 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
   }
 }
 
+template <int D, int GV>
 __global__ void __launch_bounds__(kThreads, 1) partial_q4_kernel(const __grid_constant__ PartialParams p) {
-  using C = Q4;
+  using C = Q4<D, GV>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may be scheduled now; it waits for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -965,22 +1019,21 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ4ProducerRegs));
-    produce_q4(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    produce_q4<D, GV>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ4ConsumerRegs));
   dependency_wait(!complete_now);   // before Q and the state writes
-  if (p.rows <= 4) consume_q4<true>(w, smem, warp, lane);
-  else consume_q4<false>(w, smem, warp, lane);
+  if (p.rows <= 4) consume_q4<D, GV, true>(w, smem, warp, lane);
+  else consume_q4<D, GV, false>(w, smem, warp, lane);
 }
 
-}  // namespace
-
-int launch_partial_q4(const PartialParams& p, int n_ctas, void* stream) {
-  const size_t smem = Q4::kTotal;
+template <int D, int GV>
+int launch_d(const PartialParams& p, int n_ctas, void* stream) {
+  const size_t smem = Q4<D, GV>::kTotal;
   // the register budget check and the shared-memory opt-in, once per device
   static std::atomic<unsigned long long> ready{0};
-  cudaError_t err = prepare_kernel_once(partial_q4_kernel, smem, 128 * kQ4ProducerRegs + 32 * kConsumerWarps * kQ4ConsumerRegs, ready);
+  cudaError_t err = prepare_kernel_once(partial_q4_kernel<D, GV>, smem, 128 * kQ4ProducerRegs + 32 * kConsumerWarps * kQ4ConsumerRegs, ready);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
@@ -992,8 +1045,15 @@ int launch_partial_q4(const PartialParams& p, int n_ctas, void* stream) {
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, partial_q4_kernel, p);
+  err = cudaLaunchKernelEx(&cfg, partial_q4_kernel<D, GV>, p);
   return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_partial_q4(const PartialParams& p, int d, int n_ctas, void* stream) {
+  if (d == 64) return launch_d<64, 16>(p, n_ctas, stream);
+  return p.kivi_Gv == 16 ? launch_d<128, 16>(p, n_ctas, stream) : launch_d<128, 32>(p, n_ctas, stream);
 }
 
 }  // namespace dattn

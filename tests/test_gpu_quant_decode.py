@@ -132,18 +132,47 @@ def test_quantized_full_size_all_rows(fmt):
     (1, 16, 8, "sink_window", 64, 3, 160),     # 2 rows
     (1, 64, 8, "causal", 64, 7, 64),           # a power-of-two residual ring
     (2, 8, 2, "sink_window", 0, 152, 96),      # a residual ring of three groups
+    (4, 32, 8, "causal", 0, 152, 160),         # 16 rows: two row blocks share a stage's keys
+    (3, 32, 8, "sink_window", 50, 4, 96),      # 12 rows: a ragged second row block
+    (4, 64, 8, "sink_window", 0, 152, 160),    # 32 rows: four row blocks, a warp per stage
+    (5, 32, 8, "causal", 64, 7, 160),          # 20 rows: four blocks, the last nearly empty
 ])
 def test_int4_kivi_tensor_core_rows_and_windows(S_q, H_q, H_kv, mask, chunk, num_sms, R):
-    """d = 128, Gv = 32, at most 8 rows: K groups that straddle 16-key blocks
-    (window starts off the group grid), stages of two runs touching up to ten
-    groups, residual-only and just-closed-group requests, residual rings of
-    several lengths R."""
+    """d = 128, Gv = 32, 1 to 32 rows (one to four row blocks of 8): K groups
+    that straddle 16-key blocks (window starts off the group grid), stages of
+    two runs touching up to ten groups, residual-only and just-closed-group
+    requests, residual rings of several lengths R."""
     lens = [2000, 1999, 1777, 300, 129, 7]
     w = W.quantized_history("q4t", B=len(lens), S_q=S_q, H_q=H_q, H_kv=H_kv, d=128, lens=lens, P=16, seed=26,
                             device="cuda", fmt="int4_kivi", pool_pages=sum(-(-t // 16) for t in lens) + 3)
     w.problem = dict(w.problem, mask=mask, n_sink=34, window=1000, kivi_residual=R)
     p, cache = append_history(w, "int4_kivi", [[900, 1500], [], [1000], [160], [], []])
     O, L, info = _run(w, "int4_kivi", p, cache, chunk_tokens=chunk, num_sms=num_sms)
+    assert info["rows"] == S_q * H_q // H_kv
+    _compare(O, L, w, p, _oracle_cache(w, "int4_kivi"), H.all_rows(p))
+
+
+@pytest.mark.parametrize("d,Gv,P,S_q,H_q,H_kv,mask", [
+    (128, 16, 16, 1, 32, 8, "causal"),         # Gv = 16: two channel groups per 32-channel chunk
+    (128, 16, 16, 3, 32, 8, "sink_window"),    # Gv = 16, 12 rows
+    (64, 16, 16, 1, 32, 8, "sink_window"),     # d = 64 (Gv <= d / 4), 4 rows
+    (64, 16, 16, 4, 32, 8, "causal"),          # d = 64, 16 rows
+    (64, 16, 32, 4, 64, 8, "sink_window"),     # d = 64, 32 rows, a page per K group
+    (128, 32, 64, 1, 32, 8, "sink_window"),    # two K groups per page
+    (128, 32, 8, 2, 32, 8, "causal"),          # four pages per K group
+    (128, 32, 96, 1, 32, 8, "sink_window"),    # P = 96, not a power of two: byte-format kernel
+    (64, 16, 96, 4, 16, 2, "causal"),          # the same at d = 64 with 32 rows
+])
+def test_int4_kivi_head_dims_groups_and_pages(d, Gv, P, S_q, H_q, H_kv, mask):
+    """KIVI shapes beyond d = 128 / Gv = 32 / P = 16: head dimension 64, V channel
+    groups of 16, K groups that span several pages or share one, and page sizes
+    that are not a power of two; every query row against the oracle."""
+    lens = [1500, 777, 160, 33, 2]
+    w = W.quantized_history("q4s", B=len(lens), S_q=S_q, H_q=H_q, H_kv=H_kv, d=d, lens=lens, P=P, seed=27,
+                            device="cuda", fmt="int4_kivi", pool_pages=sum(-(-t // P) for t in lens) + 3)
+    w.problem = dict(w.problem, mask=mask, n_sink=34, window=600, kivi_v_group=Gv)
+    p, cache = append_history(w, "int4_kivi", [[700], [400, 500], [], [32], []])
+    O, L, info = _run(w, "int4_kivi", p, cache, chunk_tokens=0, num_sms=152)
     assert info["rows"] == S_q * H_q // H_kv
     _compare(O, L, w, p, _oracle_cache(w, "int4_kivi"), H.all_rows(p))
 

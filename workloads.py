@@ -274,12 +274,15 @@ def packed_view(w: Workload) -> Workload:
                     index_indptr=w.index_indptr, index_list=w.index_list, meta=dict(w.meta))
 
 
-def quantized(device="cpu", fmt="int8", B=32, lo=2048, hi=32768, S_q=1):
+def quantized(device="cpu", fmt="int8", B=32, lo=2048, hi=32768, S_q=1, d=128, P=16):
+    """The quantized-cache workload; KIVI V channel groups are 32 wide, 16 at d = 64."""
     meta = torch.Generator().manual_seed(4)
     lens = torch.randint(lo, hi + 1, (B,), generator=meta).tolist()
-    rows = f" S_q={S_q}" if S_q != 1 else ""
-    return quantized_history(f"quantized KV ({fmt}) B={B} T~U[{lo},{hi}]{rows}", B=B, S_q=S_q, H_q=32,
-                             H_kv=8, d=128, lens=lens, P=16, seed=4, device=device, fmt=fmt)
+    extra = (f" S_q={S_q}" if S_q != 1 else "") + (f" d={d}" if d != 128 else "") + (f" P={P}" if P != 16 else "")
+    w = quantized_history(f"quantized KV ({fmt}) B={B} T~U[{lo},{hi}]{extra}", B=B, S_q=S_q, H_q=32,
+                          H_kv=8, d=d, lens=lens, P=P, seed=4, device=device, fmt=fmt)
+    w.problem["kivi_v_group"] = min(32, d // 4)
+    return w
 
 
 def _dfs_tree_intervals(S_q: int, gen) -> list:
