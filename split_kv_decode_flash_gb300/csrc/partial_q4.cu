@@ -53,8 +53,18 @@ constexpr int kMaxGroups = 11;        // K groups a stage of two runs may touch 
 constexpr int kQ4ProducerRegs = 104;
 constexpr int kQ4ConsumerRegs = 200;
 static_assert(128 * kQ4ProducerRegs + 32 * kConsumerWarps * kQ4ConsumerRegs <= kThreads * 168, "register split");
+// The FlashMask instance's producers also load and reduce each slot's column
+// intervals: they get more of the register file.
+constexpr int kQ4FmProducerRegs = 120;
+constexpr int kQ4FmConsumerRegs = 192;
+static_assert(128 * kQ4FmProducerRegs + 32 * kConsumerWarps * kQ4FmConsumerRegs <= kThreads * 168, "register split");
+template <bool FM>
+constexpr int q4_producer_regs() { return FM ? kQ4FmProducerRegs : kQ4ProducerRegs; }
+template <bool FM>
+constexpr int q4_consumer_regs() { return FM ? kQ4FmConsumerRegs : kQ4ConsumerRegs; }
 
-template <int D, int GV>
+// FM: the FlashMask instance, whose ring also carries each key column's row bits.
+template <int D, int GV, bool FM>
 struct Q4 {
   static constexpr int kStagesN = 4;               // even: stage groups alternate
   static constexpr int kCodeRow = D / 2;           // bytes of a key's codes
@@ -69,7 +79,8 @@ struct Q4 {
   static_assert(kStage >= 2 * kRKeys * D * 2, "a residual stage fits in a stage slot");
   static constexpr int kPos = kStagesN * kStage;   // int32 [stages][kQKeys]: logical key per slot
   static constexpr int kRows = kPos + kStagesN * kQKeys * 4;   // uint32 [stages][kQKeys]: source row per slot
-  static constexpr int kFlags = kRows + kStagesN * kQKeys * 4;
+  static constexpr int kVis = kRows + kStagesN * kQKeys * 4;    // FM: uint32 [stages][kQKeys] row bits
+  static constexpr int kFlags = kVis + (FM ? kStagesN * kQKeys * 4 : 0);
   static constexpr int kSeq = kFlags + kStagesN * 4;
   static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
@@ -184,6 +195,7 @@ __device__ __forceinline__ int qsel_of(const StageGroups& sg, const WorkItem& it
 struct Q4Desc {
   int t[kQSlots];          // logical key (-1: none)
   uint32_t row[kQSlots];   // codes row (quantized) or ring row (residual); kNoRow: none
+  uint32_t vis[kQSlots];   // FlashMask: bit i set when query row i sees the key
   int gpg;                 // lane k < groups: page of group k's first token (-2: none)
   uint32_t grow;           // lane k < groups: row of group k's qparams (kNoRow: none)
   bool full, resid;
@@ -229,6 +241,7 @@ __device__ __forceinline__ void q4_pages(const Walk& w, const QCur& c, const int
   }
 }
 
+template <bool FM>
 __device__ __forceinline__ Q4Desc q4_rows(const Walk& w, const QCur& c, const int (&t)[kQSlots],
                                           const int (&pi)[kQSlots], int gpi, int lane, const Q4Shapes& sh) {
   const PartialParams& p = w.p;
@@ -237,6 +250,7 @@ __device__ __forceinline__ Q4Desc q4_rows(const Walk& w, const QCur& c, const in
   for (int h = 0; h < kQSlots; ++h) {
     d.t[h] = -1;
     d.row[h] = kNoRow;
+    d.vis[h] = 0u;
   }
   d.gpg = gpi;
   d.grow = kNoRow;
@@ -289,13 +303,35 @@ __device__ __forceinline__ Q4Desc q4_rows(const Walk& w, const QCur& c, const in
     }
   }
   if (err) atomicOr(p.status, err);
+  if constexpr (FM) {
+    // FlashMask: the column's two hidden row intervals; a column hidden from
+    // every query row is not loaded.  FULL: every slot holds a key every row sees.
+    const uint32_t all_rows = row_bits(0, r.nq);
+    bool all = true;
+#pragma unroll
+    for (int h = 0; h < kQSlots; ++h) {
+      uint32_t v = 0u;
+      if (d.t[h] >= 0) {
+        const int4 iv = *reinterpret_cast<const int4*>(p.fm_intervals + 4ll * (r.it.x1 + d.t[h]));
+        v = all_rows & ~(row_bits(iv.x, iv.y) | row_bits(iv.z, iv.w));
+      }
+      if (v == 0u) {
+        d.t[h] = -1;
+        d.row[h] = kNoRow;
+      }
+      d.vis[h] = v;
+      if (c.j0 + lane + 32 * h < c.j1) all = all && v == all_rows;
+    }
+    d.full = __all_sync(kAll, all);
+    return d;
+  }
   d.full = stage_is_full(p, r.it, r.nq, c.j0, c.j1, tmax, -1);
   return d;
 }
 
-template <int D, int GV>
+template <int D, int GV, bool FM>
 __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
-  using C = Q4<D, GV>;
+  using C = Q4<D, GV, FM>;
   const PartialParams& p = w.p;
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
   const uint32_t empty0 = smem_u32(smem + C::kEmptyBar);
@@ -324,7 +360,7 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool 
   q4_pages(w, c0, t0, lane, sh, pi0, g0i);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
-    const Q4Desc r0 = q4_rows(w, c0, t0, pi0, g0i, lane, sh);
+    const Q4Desc r0 = q4_rows<FM>(w, c0, t0, pi0, g0i, lane, sh);
     q4_pages(w, c1, t1, lane, sh, pi0, g0i);   // next stage's page ids, in flight until then
     QCur c2 = c1;
     qc_advance(w, c2, kProducerWarps);
@@ -340,6 +376,11 @@ __device__ void produce_q4(const Walk& w, uint8_t* smem, int lane, int pw, bool 
     for (int h = 0; h < kQSlots; ++h) {
       pos[lane + 32 * h] = r0.t[h];
       rows[lane + 32 * h] = r0.row[h];
+    }
+    if constexpr (FM) {
+      uint32_t* vis = reinterpret_cast<uint32_t*>(smem + C::kVis) + st * kQKeys;
+#pragma unroll
+      for (int h = 0; h < kQSlots; ++h) vis[lane + 32 * h] = r0.vis[h];
     }
     __syncwarp();
     if (lane == 0) {
@@ -633,9 +674,9 @@ __device__ __forceinline__ void k_mma(uint32_t kt, int base, int lrow, int lmat,
   }
 }
 
-template <int D, int GV, bool PACKED>
+template <int D, int GV, bool FM, bool PACKED>
 __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
-  using C = Q4<D, GV>;
+  using C = Q4<D, GV, FM>;
   constexpr int NT = D / 16;                  // output tiles
   constexpr int kCg = D / GV;                 // V channel groups
   constexpr int NS = PACKED ? 2 : 1;          // 16-key sub-blocks per step
@@ -661,11 +702,10 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
   const int lra = PACKED ? 2 * (t4 & 1) : 2 * t4;
   const int ra = 8 * rbk + lra, rb = ra + 1;
   const bool writer = !PACKED || t4 < 2;
-  const bool oka = ra < p.rows, okb = rb < p.rows;
   const int qia = ra / p.g, qib = rb / p.g;
   // query row of the lane's B fragments
   const int rq = PACKED ? (g4 & 3) : 8 * rbk + g4;
-  const bool okq = rq < p.rows, lo_lane = PACKED && g4 >= 4;
+  const bool lo_lane = PACKED && g4 >= 4;
   const int lrow = lane & 7, lmat = lane >> 3;
   const float sc = p.scale_log2;
   const int gsh = p.kivi_G == 32 ? 5 : 6;   // log2 G
@@ -676,10 +716,14 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
   bool dead = false;
   for (int ii = w.begin; ii < w.end; ++ii) {
     const WorkItem it = w.rec(ii).it;
-    const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+    // the request's query rows are packed rows qo .. qo + nq - 1 (a mixed batch,
+    // M4.5 §0x08F); rows past g nq have a zero query and are never written
+    const int qo = w.rec(ii).qo, nq = w.rec(ii).nq;
+    const MaskCtx mc{p.mask, nq, it.T, p.n_sink, p.window};
+    const bool oka = ra < p.g * nq, okb = rb < p.g * nq, okq = rq < p.g * nq;
     const int jq = residual_start(p, it);
     const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
-                                ((static_cast<long long>(it.b) * p.S_q + rq / p.g) * p.H_q + it.h * p.g + rq % p.g) * D;
+                                ((static_cast<long long>(qo) + rq / p.g) * p.H_q + it.h * p.g + rq % p.g) * D;
     QRow<D> qr;
     load_qrow(qrow, okq, qr, t4);
     float o[NT][4];
@@ -800,10 +844,20 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
             const bool live = !resid || u == 0;
             const int kx = base0 + 16 * u + g4, ky = kx + 8;
             const int tx = live ? pos[kx] : -1, ty = live ? pos[ky] : -1;
-            const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
-            const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
-            const bool vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
-            const bool vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
+            bool vxa, vxb, vya, vyb;
+            if constexpr (FM) {   // FlashMask: the producer's row bits of the columns
+              const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kQKeys;
+              const uint32_t bx = live ? vis[kx] : 0u, by = live ? vis[ky] : 0u;
+              vxa = tx >= 0 && oka && (full || ((bx >> qia) & 1u));
+              vxb = tx >= 0 && okb && (full || ((bx >> qib) & 1u));
+              vya = ty >= 0 && oka && (full || ((by >> qia) & 1u));
+              vyb = ty >= 0 && okb && (full || ((by >> qib) & 1u));
+            } else {
+              vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
+              vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
+              vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
+              vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
+            }
             s[u][0] = vxa ? s[u][0] * sc : -INFINITY;
             s[u][1] = vxb ? s[u][1] * sc : -INFINITY;
             s[u][2] = vya ? s[u][2] * sc : -INFINITY;
@@ -953,7 +1007,7 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
         if (!(rr ? okb : oka)) continue;
         const float m = rr ? mb : ma, l = rr ? lb : la;
         const int i = row / p.g, hq = it.h * p.g + row % p.g;
-        const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
+        const long long orow = (static_cast<long long>(qo) + i) * p.H_q + hq;
         float val[D / 32][4];
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -994,9 +1048,9 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
   }
 }
 
-template <int D, int GV>
+template <int D, int GV, bool FM>
 __global__ void __launch_bounds__(kThreads, 1) partial_q4_kernel(const __grid_constant__ PartialParams p) {
-  using C = Q4<D, GV>;
+  using C = Q4<D, GV, FM>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may be scheduled now; it waits for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1018,22 +1072,23 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4_kernel(const __grid_co
   const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ4ProducerRegs));
-    produce_q4<D, GV>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(q4_producer_regs<FM>()));
+    produce_q4<D, GV, FM>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ4ConsumerRegs));
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(q4_consumer_regs<FM>()));
   dependency_wait(!complete_now);   // before Q and the state writes
-  if (p.rows <= 4) consume_q4<D, GV, true>(w, smem, warp, lane);
-  else consume_q4<D, GV, false>(w, smem, warp, lane);
+  if (p.rows <= 4) consume_q4<D, GV, FM, true>(w, smem, warp, lane);
+  else consume_q4<D, GV, FM, false>(w, smem, warp, lane);
 }
 
-template <int D, int GV>
+template <int D, int GV, bool FM>
 int launch_d(const PartialParams& p, int n_ctas, void* stream) {
-  const size_t smem = Q4<D, GV>::kTotal;
+  const size_t smem = Q4<D, GV, FM>::kTotal;
   // the register budget check and the shared-memory opt-in, once per device
   static std::atomic<unsigned long long> ready{0};
-  cudaError_t err = prepare_kernel_once(partial_q4_kernel<D, GV>, smem, 128 * kQ4ProducerRegs + 32 * kConsumerWarps * kQ4ConsumerRegs, ready);
+  cudaError_t err = prepare_kernel_once(partial_q4_kernel<D, GV, FM>, smem,
+                                        128 * q4_producer_regs<FM>() + 32 * kConsumerWarps * q4_consumer_regs<FM>(), ready);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
@@ -1045,15 +1100,19 @@ int launch_d(const PartialParams& p, int n_ctas, void* stream) {
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, partial_q4_kernel<D, GV>, p);
+  err = cudaLaunchKernelEx(&cfg, partial_q4_kernel<D, GV, FM>, p);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace
 
 int launch_partial_q4(const PartialParams& p, int d, int n_ctas, void* stream) {
-  if (d == 64) return launch_d<64, 16>(p, n_ctas, stream);
-  return p.kivi_Gv == 16 ? launch_d<128, 16>(p, n_ctas, stream) : launch_d<128, 32>(p, n_ctas, stream);
+  if (p.mask == DATTN_MASK_FLASHMASK) {
+    if (d == 64) return launch_d<64, 16, true>(p, n_ctas, stream);
+    return p.kivi_Gv == 16 ? launch_d<128, 16, true>(p, n_ctas, stream) : launch_d<128, 32, true>(p, n_ctas, stream);
+  }
+  if (d == 64) return launch_d<64, 16, false>(p, n_ctas, stream);
+  return p.kivi_Gv == 16 ? launch_d<128, 16, false>(p, n_ctas, stream) : launch_d<128, 32, false>(p, n_ctas, stream);
 }
 
 }  // namespace dattn

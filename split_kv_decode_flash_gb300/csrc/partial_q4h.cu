@@ -43,12 +43,20 @@ constexpr int kHS = kHK / 32;         // slots per producer lane
 constexpr int kHProducerRegs = 104;
 constexpr int kHConsumerRegs = 200;
 static_assert(128 * kHProducerRegs + 32 * kConsumerWarps * kHConsumerRegs <= kThreads * 168, "register split");
+// The FlashMask instance's producers carry four interval ends for each of
+// their 8 slots a stage ahead: it keeps the launch's even split (168 each).
+template <bool FM>
+constexpr int q4h_producer_regs() { return FM ? 168 : kHProducerRegs; }
+template <bool FM>
+constexpr int q4h_consumer_regs() { return FM ? 168 : kHConsumerRegs; }
 
-template <int D>
+// FM: the FlashMask instance, whose ring also carries each key column's row
+// bits (two stages fewer, to make room for them).
+template <int D, bool FM = false>
 struct Q4H {
   // Even depth: with two consumer stage groups taking alternate stages, every
   // ring slot always belongs to the same group (no mbarrier parity alias).
-  static constexpr int kStagesN = D == 128 ? 6 : 10;
+  static constexpr int kStagesN = D == 128 ? (FM ? 4 : 6) : (FM ? 8 : 10);
   static_assert(kStagesN % 2 == 0, "ring depth must be even");
   static constexpr int kRowB = D / 2;              // code bytes of one key row
   static constexpr int kChunks = kRowB / 16;
@@ -56,7 +64,8 @@ struct Q4H {
   static constexpr int kQp = kHK * 4;              // one tensor's (s, o) pairs
   static constexpr int kStage = 2 * kTile + 2 * kQp;
   static constexpr int kPos = kStagesN * kStage;   // int32 [stages][kHK]
-  static constexpr int kFlags = kPos + kStagesN * kHK * 4;
+  static constexpr int kVis = kPos + kStagesN * kHK * 4;   // FM: uint32 [stages][kHK] row bits
+  static constexpr int kFlags = kVis + (FM ? kStagesN * kHK * 4 : 0);
   static constexpr int kSeq = kFlags + kStagesN * 4;
   static constexpr int kFullBar = align16(kSeq + kStagesN * 4);
   static constexpr int kEmptyBar = kFullBar + kStagesN * 8;
@@ -90,9 +99,9 @@ __device__ __forceinline__ float2 h2_to_f2(uint32_t w) { return __half22float2(*
 
 // ---- producer ---------------------------------------------------------------------------
 
-template <int D>
+template <int D, bool FM>
 __device__ void produce_q4h(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
-  using C = Q4H<D>;
+  using C = Q4H<D, FM>;
   const PartialParams& p = w.p;
   constexpr int kSlotsPerPass = 32 / C::kChunks;   // key rows per warp instruction
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
@@ -112,14 +121,14 @@ __device__ void produce_q4h(const Walk& w, uint8_t* smem, int lane, int pw, bool
   pc_advance<kHK>(w, c1, kProducerWarps);
   PCur c2 = c1;
   pc_advance<kHK>(w, c2, kProducerWarps);
-  index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
-  const SlotKeys<kHS> k0 = slot_keys<kHS>(w, c0, lane);
-  SlotKeys<kHS> k1 = slot_keys<kHS>(w, c1, lane);
+  if constexpr (!FM) index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
+  const SlotKeys<kHS> k0 = slot_keys<kHS, !FM>(w, c0, lane);
+  SlotKeys<kHS> k1 = slot_keys<kHS, !FM>(w, c1, lane);
   dependency_wait(dep_wait);   // the page table is a device input
-  const SlotPages<kHS> g0 = slot_pages<kHS>(w, c0, k0);
-  SlotPages<kHS> g1 = slot_pages<kHS>(w, c1, k1);
-  SlotKeys<kHS> k2 = slot_keys<kHS>(w, c2, lane);
-  SlotRows<kHS> r0 = slot_rows<kHS>(w, c0, k0, g0, lane);
+  const SlotPages<kHS, FM> g0 = slot_pages<kHS, FM>(w, c0, k0);
+  SlotPages<kHS, FM> g1 = slot_pages<kHS, FM>(w, c1, k1);
+  SlotKeys<kHS> k2 = slot_keys<kHS, !FM>(w, c2, lane);
+  SlotRows<kHS, FM> r0 = slot_rows<kHS, FM>(w, c0, k0, g0, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
@@ -128,6 +137,11 @@ __device__ void produce_q4h(const Walk& w, uint8_t* smem, int lane, int pw, bool
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kHK;
 #pragma unroll
     for (int h = 0; h < kHS; ++h) pos[lane + 32 * h] = r0.t[h];
+    if constexpr (FM) {
+      uint32_t* vis = reinterpret_cast<uint32_t*>(smem + C::kVis) + st * kHK;
+#pragma unroll
+      for (int h = 0; h < kHS; ++h) vis[lane + 32 * h] = r0.vis[h];
+    }
     if (lane == 0) {
       reinterpret_cast<int*>(smem + C::kFlags)[st] = r0.full ? kFlagFull : 0;
       reinterpret_cast<int*>(smem + C::kSeq)[st] = static_cast<int>(k);
@@ -157,20 +171,20 @@ __device__ void produce_q4h(const Walk& w, uint8_t* smem, int lane, int pw, bool
     __syncwarp();
     if (lane == 0) mbar_arrive(fb);     // publishes pos / flags / stamp; the copies complete the phase
 
-    r0 = slot_rows<kHS>(w, c1, k1, g1, lane);
+    r0 = slot_rows<kHS, FM>(w, c1, k1, g1, lane);
     c0 = c1;
-    g1 = slot_pages<kHS>(w, c2, k2);
+    g1 = slot_pages<kHS, FM>(w, c2, k2);
     k1 = k2;
     c1 = c2;
     pc_advance<kHK>(w, c2, kProducerWarps);
-    k2 = slot_keys<kHS>(w, c2, lane);
+    k2 = slot_keys<kHS, !FM>(w, c2, lane);
   }
   asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
 }
 
 template <int D>
 __device__ void produce_q4h_runs(const Walk& w, uint8_t* smem, int lane, int pw, bool dep_wait) {
-  using C = Q4H<D>;
+  using C = Q4H<D, false>;
   const PartialParams& p = w.p;
   constexpr int kSlotsPerPass = 32 / C::kChunks;   // key rows per warp instruction
   const uint32_t full0 = smem_u32(smem + C::kFullBar);
@@ -261,12 +275,14 @@ struct QH {
   float qsum0, qsum1, unit0, unit1;
 };
 
+// rec: the item's record; its request's query rows are packed rows rec.qo ..
+// rec.qo + rec.nq - 1 (a mixed batch, M4.5 §0x08F), and rows past g rec.nq are zero.
 template <int D>
-__device__ __forceinline__ void load_q4h(const PartialParams& p, const WorkItem& it, int row, int t4, QH<D>& q) {
+__device__ __forceinline__ void load_q4h(const PartialParams& p, const ItemRec& rec, int row, int t4, QH<D>& q) {
   constexpr int NCH = D / 32;
-  const bool ok = row < p.rows;
+  const bool ok = row < p.g * rec.nq;
   const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(p.q) +
-                            ((static_cast<long long>(it.b) * p.S_q + row / p.g) * p.H_q + it.h * p.g + row % p.g) * D;
+                            ((static_cast<long long>(rec.qo) + row / p.g) * p.H_q + rec.it.h * p.g + row % p.g) * D;
   float v[NCH][8];
   float mx = 0.f, sum = 0.f;
 #pragma unroll
@@ -314,9 +330,9 @@ __device__ __forceinline__ void load_q4h(const PartialParams& p, const WorkItem&
 // share the row maxima and the rescale.  Row blocks of 8 split a stage's keys
 // among the four warps of a stage group: 1 block, 64 keys a warp; 2 blocks,
 // 128; 4 blocks, 256, so that an item leaves 8, 4 or 2 states per row.
-template <int D>
+template <int D, bool FM>
 __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
-  using C = Q4H<D>;
+  using C = Q4H<D, FM>;
   constexpr int NCH = D / 32;   // 32-channel chunks
   constexpr int NT = D / 16;    // output tiles (16 channels x 8 rows)
   const PartialParams& p = w.p;
@@ -333,7 +349,6 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
   const int keys_per_warp = kHK / splits;
   const int g4 = lane >> 2, t4 = lane & 3;
   const int ra = 8 * rb + 2 * t4, rb1 = ra + 1;  // the lane's accumulator rows
-  const bool oka = ra < p.rows, okb = rb1 < p.rows;
   const int qia = ra / p.g, qib = rb1 / p.g;
   const int lrow = lane & 7, lmat = lane >> 3;
   const float sc = p.scale_log2;
@@ -341,12 +356,14 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
   uint32_t k = 0;
   bool dead = false;
   QH<D> qn;
-  if (w.begin < w.end) load_q4h<D>(p, w.rec(w.begin).it, 8 * rb + g4, t4, qn);
+  if (w.begin < w.end) load_q4h<D>(p, w.rec(w.begin), 8 * rb + g4, t4, qn);
   for (int ii = w.begin; ii < w.end; ++ii) {
     const WorkItem it = w.rec(ii).it;
-    const MaskCtx mc{p.mask, p.S_q, it.T, p.n_sink, p.window};
+    const int nq = w.rec(ii).nq;                  // the request's query rows
+    const MaskCtx mc{p.mask, nq, it.T, p.n_sink, p.window};
+    const bool oka = ra < p.g * nq, okb = rb1 < p.g * nq;
     const QH<D> q = qn;
-    if (ii + 1 < w.end) load_q4h<D>(p, w.rec(ii + 1).it, 8 * rb + g4, t4, qn);
+    if (ii + 1 < w.end) load_q4h<D>(p, w.rec(ii + 1), 8 * rb + g4, t4, qn);
     // log2-unit score = s_t (sc 2^24 / f) S' + z_t (sc sum q), per row
     const float ku0 = sc * q.unit0, ku1 = sc * q.unit1, kz0 = sc * q.qsum0, kz1 = sc * q.qsum1;
     float o[NT][4];
@@ -418,10 +435,20 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
           vsy[bb] = vqy.x;
           voy[bb] = vqy.y;
           const float zx = -ksx.y * ksx.x, zy = -ksy.y * ksy.x;   // exact: fp16 x fp16
-          const bool vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
-          const bool vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
-          const bool vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
-          const bool vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
+          bool vxa, vxb, vya, vyb;
+          if constexpr (FM) {   // FlashMask: the producer's row bits of the columns
+            const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kHK;
+            const uint32_t bx = vis[kx], by = vis[ky];
+            vxa = tx >= 0 && oka && (full || ((bx >> qia) & 1u));
+            vxb = tx >= 0 && okb && (full || ((bx >> qib) & 1u));
+            vya = ty >= 0 && oka && (full || ((by >> qia) & 1u));
+            vyb = ty >= 0 && okb && (full || ((by >> qib) & 1u));
+          } else {
+            vxa = tx >= 0 && oka && (full || key_visible(mc, qia, tx));
+            vxb = tx >= 0 && okb && (full || key_visible(mc, qib, tx));
+            vya = ty >= 0 && oka && (full || key_visible(mc, qia, ty));
+            vyb = ty >= 0 && okb && (full || key_visible(mc, qib, ty));
+          }
           s[bb][0] = vxa ? fmaf(ksx.x * ku0, s[bb][0], zx * kz0) : -INFINITY;
           s[bb][1] = vxb ? fmaf(ksx.x * ku1, s[bb][1], zx * kz1) : -INFINITY;
           s[bb][2] = vya ? fmaf(ksy.x * ku0, s[bb][2], zy * kz0) : -INFINITY;
@@ -511,7 +538,7 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
         if (!(rr ? okb : oka)) continue;
         const float m = rr ? mb : ma, l = rr ? lb : la, z = rr ? zb : za;
         const int i = row / p.g, hq = it.h * p.g + row % p.g;
-        const long long orow = (static_cast<long long>(it.b) * p.S_q + i) * p.H_q + hq;
+        const long long orow = (static_cast<long long>(w.rec(ii).qo) + i) * p.H_q + hq;
         if (it.slot < 0) {
           const float inv = l > 0.f ? 1.f / l : 0.f;
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + orow * D;
@@ -551,9 +578,9 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
   }
 }
 
-template <int D>
+template <int D, bool FM>
 __global__ void __launch_bounds__(kThreads, 1) partial_q4h_kernel(const __grid_constant__ PartialParams p) {
-  using C = Q4H<D>;
+  using C = Q4H<D, FM>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // the merge kernel may be scheduled now; it waits for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -575,22 +602,24 @@ __global__ void __launch_bounds__(kThreads, 1) partial_q4h_kernel(const __grid_c
   const Walk w{p, cache, it_begin, it_end, policy_evict_last()};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= kConsumerWarps) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kHProducerRegs));
-    if (runs_apply<kHK>(p)) produce_q4h_runs<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
-    else produce_q4h<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    if constexpr (!FM) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(q4h_producer_regs<FM>()));
+    if constexpr (FM) produce_q4h<D, true>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    else if (runs_apply<kHK>(p)) produce_q4h_runs<D>(w, smem, lane, warp - kConsumerWarps, !complete_now);
+    else produce_q4h<D, false>(w, smem, lane, warp - kConsumerWarps, !complete_now);
     return;
   }
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kHConsumerRegs));
+  if constexpr (!FM) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(q4h_consumer_regs<FM>()));
   dependency_wait(!complete_now);   // before Q and the state writes
-  consume_q4h<D>(w, smem, warp, lane);
+  consume_q4h<D, FM>(w, smem, warp, lane);
 }
 
-template <int D>
+template <int D, bool FM>
 int launch_q4h(const PartialParams& p, int n_ctas, void* stream) {
-  const size_t smem = Q4H<D>::kTotal;
+  const size_t smem = Q4H<D, FM>::kTotal;
   // the register budget check and the shared-memory opt-in, once per device
   static std::atomic<unsigned long long> ready{0};
-  cudaError_t err = prepare_kernel_once(partial_q4h_kernel<D>, smem, 128 * kHProducerRegs + 32 * kConsumerWarps * kHConsumerRegs, ready);
+  cudaError_t err = prepare_kernel_once(partial_q4h_kernel<D, FM>, smem,
+                                        128 * q4h_producer_regs<FM>() + 32 * kConsumerWarps * q4h_consumer_regs<FM>(), ready);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
@@ -602,14 +631,16 @@ int launch_q4h(const PartialParams& p, int n_ctas, void* stream) {
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, partial_q4h_kernel<D>, p);
+  err = cudaLaunchKernelEx(&cfg, partial_q4h_kernel<D, FM>, p);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace
 
 int launch_partial_q4h(const PartialParams& p, int d, int n_ctas, void* stream) {
-  return d == 64 ? launch_q4h<64>(p, n_ctas, stream) : launch_q4h<128>(p, n_ctas, stream);
+  if (p.mask == DATTN_MASK_FLASHMASK)
+    return d == 64 ? launch_q4h<64, true>(p, n_ctas, stream) : launch_q4h<128, true>(p, n_ctas, stream);
+  return d == 64 ? launch_q4h<64, false>(p, n_ctas, stream) : launch_q4h<128, false>(p, n_ctas, stream);
 }
 
 }  // namespace dattn

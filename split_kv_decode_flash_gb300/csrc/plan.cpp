@@ -64,9 +64,6 @@ void check_problem(const dattn_problem* p, Checker& c) {
   }
   if (p->fmt < DATTN_FMT_BF16 || p->fmt > DATTN_FMT_INT4_HEAD) c.fail(DATTN_EINVAL, "unknown format");
   if (p->mask < DATTN_MASK_CAUSAL || p->mask > DATTN_MASK_FLASHMASK) c.fail(DATTN_EINVAL, "unknown mask");
-  if (p->mask == DATTN_MASK_FLASHMASK && p->fmt != DATTN_FMT_BF16 && p->fmt != DATTN_FMT_INT8_TOKEN &&
-      p->fmt != DATTN_FMT_FP8_E4M3 && p->fmt != DATTN_FMT_FP8_E5M2)
-    c.fail(DATTN_EUNSUPPORTED, "flashmask runs on bf16, INT8 and FP8 K/V");
   // K/V rows (one kv head, one token) are addressed with 32-bit row indices
   const long long kMaxPoolRows = 0xFFFFFFFFll;
   if (p->layout == DATTN_KV_PAGED_HND) {
@@ -90,7 +87,10 @@ void check_problem(const dattn_problem* p, Checker& c) {
     if (G != 32 && G != 64) c.fail(DATTN_EUNSUPPORTED, "kivi_group must be 32 or 64");
     if (Gv != 16 && Gv != 32 && Gv != 64) c.fail(DATTN_EUNSUPPORTED, "kivi_v_group must be 16, 32 or 64");
     else if (4 * Gv > p->d_h) c.fail(DATTN_EUNSUPPORTED, "kivi_v_group must be at most d_h / 4");
-    if (p->mask == DATTN_MASK_INDEX_LIST) c.fail(DATTN_EUNSUPPORTED, "INT4 KIVI reads causal or sink+window streams");
+    if (p->mask == DATTN_MASK_INDEX_LIST)
+      c.fail(DATTN_EUNSUPPORTED, "INT4 KIVI reads causal, sink+window or flashmask streams");
+    if (p->mask == DATTN_MASK_FLASHMASK && p->page_size >= 1 && (p->page_size & (p->page_size - 1)) != 0)
+      c.fail(DATTN_EUNSUPPORTED, "flashmask on INT4 KIVI needs a power-of-two page_size");
     if (G >= 1 && (R < G || R % G)) c.fail(DATTN_EINVAL, "kivi_residual must be a positive multiple of kivi_group");
     if (G >= 1 && p->page_size >= 1 && p->page_size % G && G % p->page_size)
       c.fail(DATTN_EUNSUPPORTED, "page_size and kivi_group must divide one another");
@@ -238,9 +238,9 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
                                  " query rows; 0 <= C_b <= S_q");
       mixed = mixed || cb != p.S_q;
     }
-    if (mixed && p.fmt != DATTN_FMT_BF16 && p.fmt != DATTN_FMT_INT8_TOKEN && p.fmt != DATTN_FMT_FP8_E4M3 &&
-        p.fmt != DATTN_FMT_FP8_E5M2)
-      c.fail(DATTN_EUNSUPPORTED, "mixed query-row counts run on bf16, INT8 and FP8 K/V");
+    // the KIVI byte-format kernel (page sizes that are not a power of two) reads uniform batches
+    if (mixed && p.fmt == DATTN_FMT_INT4_KIVI && (p.page_size & (p.page_size - 1)) != 0)
+      c.fail(DATTN_EUNSUPPORTED, "mixed query-row counts on INT4 KIVI need a power-of-two page_size");
   }
   if (p.mask == DATTN_MASK_FLASHMASK) {
     long long keys = 0;

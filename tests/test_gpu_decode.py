@@ -436,12 +436,6 @@ def test_flashmask_tree_verify_full_size_all_rows():
     assert H.compare_all_rows(O, L, w)["rows"] == 16 * 8 * 32
 
 
-def test_flashmask_rejected_for_int4_formats():
-    p = dict(B=1, S_q=1, H_q=8, H_kv=2, d=128, layout="paged", fmt="int4_head", P=16, num_pages=4, mask="flashmask")
-    with pytest.raises(dattn.DattnError, match="flashmask runs on bf16, INT8 and FP8"):
-        dattn.dattn_plan(p, [10], page_indptr=np.array([0, 1], np.int32), num_sms=4)
-
-
 # ---- mixed prefill / append / decode batches (per-request query rows) -------------------
 
 

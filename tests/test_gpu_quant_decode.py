@@ -269,7 +269,7 @@ def test_quantized_bounds_check_flags_out_of_pool_page(fmt):
     _compare(o.float().cpu(), lse.cpu(), w, p, _oracle_cache(w, fmt), [(1, 0, h) for h in range(8)])
 
 
-# ---- mixed batches and FlashMask columns on INT8 / FP8 codes (M4.5 §0x08F, §0x06A-§0x06D) ----
+# ---- mixed batches and FlashMask columns on the quantized formats (M4.5 §0x08F, §0x06A-§0x06D) ----
 
 def _packed_run(w, fmt, p, cache, qo_indptr=None, **plan_kw):
     """dattn_run with the query, O and LSE packed by qo_indptr (uniform when None)."""
@@ -287,11 +287,12 @@ def _packed_run(w, fmt, p, cache, qo_indptr=None, **plan_kw):
     return o.float().cpu(), lse.cpu()
 
 
-@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "fp8_e5m2", "int4_head", "int4_kivi"])
 @pytest.mark.parametrize("H_q,H_kv,chunk,num_sms", [(32, 8, 64, 7), (32, 8, 0, 152), (8, 8, 64, 5)])
 def test_byte_codes_mixed_batch_all_rows(fmt, H_q, H_kv, chunk, num_sms):
-    """Prefill, append, decode and idle requests in one launch over INT8 / FP8 codes: 32 rows
-    per kv head for the widest request (two 16-row tiles) and 8 (keys on the mma M side)."""
+    """Prefill, append, decode and idle requests in one launch over INT8 / FP8 / INT4 codes:
+    32 rows per kv head for the widest request (two 16-row tiles, or four row blocks of 8 on
+    the INT4 kernels) and 8 (keys on the mma M side)."""
     TC = [(0, 8), (130, 1), (0, 1), (65, 3), (7, 0), (300, 8), (1, 2), (64, 5), (200, 1)]
     lens = [t + c for t, c in TC]
     w = W.quantized_history("mixq", B=len(TC), S_q=8, H_q=H_q, H_kv=H_kv, d=128, lens=lens, P=16, seed=51,
@@ -305,11 +306,11 @@ def test_byte_codes_mixed_batch_all_rows(fmt, H_q, H_kv, chunk, num_sms):
     assert H.compare(O, L, w2, cache=_oracle_cache(w, fmt))["rows"] == int(qo[-1]) * H_q
 
 
-@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "fp8_e5m2", "int4_head", "int4_kivi"])
 @pytest.mark.parametrize("S_q,H_q,H_kv", [(4, 16, 2), (3, 16, 4), (8, 8, 8), (2, 8, 2)])
 def test_byte_codes_flashmask_random_intervals(fmt, S_q, H_q, H_kv):
-    """FlashMask two-interval columns over INT8 / FP8 codes: columns hidden from every row,
-    columns every row sees, and a request whose only key is hidden; 32, 12 and 8 rows."""
+    """FlashMask two-interval columns over INT8 / FP8 / INT4 codes: columns hidden from every
+    row, columns every row sees, and a request whose only key is hidden; 32, 12 and 8 rows."""
     from tests.test_gpu_decode import _random_fm_intervals
     lens = [300, 65, 1, 0, 130]
     w = W.quantized_history("fmq", B=len(lens), S_q=S_q, H_q=H_q, H_kv=H_kv, d=128, lens=lens, P=16, seed=53,
@@ -327,10 +328,10 @@ def test_byte_codes_flashmask_random_intervals(fmt, S_q, H_q, H_kv):
     H.compare(O, L, w2, cache=_oracle_cache(w, fmt))
 
 
-@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3"])
+@pytest.mark.parametrize("fmt", ["int8", "fp8_e4m3", "int4_head", "int4_kivi"])
 def test_byte_codes_tree_verify_full_size_all_rows(fmt):
     """The speculative-tree verify workload (B=16, prefixes U[1024, 8192], 8 DFS-ordered draft
-    rows, FlashMask intervals) over INT8 / FP8 codes, every row."""
+    rows, FlashMask intervals) over INT8 / FP8 / INT4 codes, every row."""
     from tests import oracle_pool
     t = W.tree_verify("cpu")
     w = W.quantized_history("treeq", B=16, S_q=8, H_q=32, H_kv=8, d=128, lens=t.kv_len.tolist(), P=16, seed=55,

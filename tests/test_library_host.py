@@ -324,18 +324,32 @@ def test_mixed_batch_validation():
         dattn.dattn_plan(prob, T, qo_indptr=np.array([0, 5, 6, 7], np.int32), num_sms=4)
     with pytest.raises(dattn.DattnError, match="0 <= C_b"):
         dattn.dattn_plan(prob, T, qo_indptr=np.array([0, 2, 1, 3], np.int32), num_sms=4)
-    # non-uniform C_b: bf16, INT8 and FP8 codes; the INT4 formats take uniform batches only
-    for fmt in ("int8", "fp8_e4m3", "fp8_e5m2"):
-        dattn.dattn_plan(_problem(B=3, S_q=4, fmt=fmt), T, page_indptr=np.array([0, 1, 2, 3], np.int32),
+    # non-uniform C_b on every format; KIVI only with a power-of-two page size (the
+    # byte-format kernel that serves other page sizes takes uniform batches)
+    kivi = dict(kivi_group=32, kivi_v_group=32, kivi_residual=64)
+    for fmt in ("int8", "fp8_e4m3", "fp8_e5m2", "int4_head", "int4_kivi"):
+        dattn.dattn_plan(_problem(B=3, S_q=4, fmt=fmt, **kivi), T, page_indptr=np.array([0, 1, 2, 3], np.int32),
                          qo_indptr=np.array([0, 1, 2, 4], np.int32), num_sms=4)
-    q4 = _problem(B=3, S_q=4, fmt="int4_head")
-    with pytest.raises(dattn.DattnError) as e:
-        dattn.dattn_plan(q4, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
+    k96 = _problem(B=3, S_q=4, fmt="int4_kivi", P=96, **kivi)
+    with pytest.raises(dattn.DattnError, match="power-of-two page_size") as e:
+        dattn.dattn_plan(k96, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
                          qo_indptr=np.array([0, 1, 2, 4], np.int32), num_sms=4)
     assert dattn.STATUS[e.value.status] == "DATTN_EUNSUPPORTED"
-    # a uniform qo_indptr is the plain batch, for every format
-    dattn.dattn_plan(q4, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
+    # a uniform qo_indptr is the plain batch, for every format and page size
+    dattn.dattn_plan(k96, T, page_indptr=np.array([0, 1, 2, 3], np.int32),
                      qo_indptr=np.array([0, 4, 8, 12], np.int32), num_sms=4)
+
+
+def test_flashmask_on_every_format_kivi_needs_power_of_two_pages():
+    T = [5, 6]
+    kivi = dict(kivi_group=32, kivi_v_group=32, kivi_residual=64)
+    for fmt in ("bf16", "int8", "fp8_e4m3", "fp8_e5m2", "int4_head", "int4_kivi"):
+        dattn.dattn_plan(_problem(fmt=fmt, mask="flashmask", **kivi), T, page_indptr=np.array([0, 1, 2], np.int32),
+                         num_sms=4)
+    with pytest.raises(dattn.DattnError, match="flashmask on INT4 KIVI needs a power-of-two page_size") as e:
+        dattn.dattn_plan(_problem(fmt="int4_kivi", mask="flashmask", P=96, **kivi), T,
+                         page_indptr=np.array([0, 1, 2], np.int32), num_sms=4)
+    assert dattn.STATUS[e.value.status] == "DATTN_EUNSUPPORTED"
 
 
 def test_step_host_sizes_and_rejections_without_a_gpu():
