@@ -118,8 +118,9 @@ typedef enum {
  *                          LTS_j <= i < LTE_j, with (UTS, UTE, LTS, LTE)_j =
  *                          fm_intervals[off_b + j], off_b = T_0 + ... + T_{b-1}
  *                          (device int32 [sum T_b, 4], one set per request, shared
- *                          by its heads).  No causal limit applies.  bf16, INT8
- *                          and FP8 K/V. */
+ *                          by its heads).  No causal limit applies.  Every format;
+ *                          INT4 KIVI with a power-of-two page_size (else
+ *                          EUNSUPPORTED). */
 typedef enum {
   DATTN_MASK_CAUSAL = 0,
   DATTN_MASK_SINK_WINDOW = 1,
@@ -176,8 +177,9 @@ typedef struct {
                                    (0 <= C_b <= S_q), packed rows qo_indptr[b] .. of q, o
                                    and lse ([qo_indptr[B], H_q, d] and [qo_indptr[B], H_q]),
                                    at positions T_b - C_b + i (bottom-right).  NULL: C_b =
-                                   S_q for every request.  Non-uniform C_b: bf16, INT8 and
-                                   FP8 K/V (the INT4 formats: EUNSUPPORTED) */
+                                   S_q for every request.  Non-uniform C_b: every format;
+                                   INT4 KIVI with a power-of-two page_size (else
+                                   EUNSUPPORTED) */
   int32_t item_cost_keys;       /* default (equal-segment) mode: the fixed cost of a work
                                    item, in keys, charged when the concatenated streams are
                                    cut into one segment per CTA, so that a CTA holding many
