@@ -49,7 +49,9 @@ MIN_SAMPLES = 50
 # extra workloads --workload can time alone.
 CONFIGS = ("tiny", "long-s1", "long-s4", "sink-window", "index-list", "int8", "int4-kivi")
 OTHER_WORKLOADS = ("tiny", "long-s1", "long-s4", "sink-window", "index-list", "packed", "tree-verify", "mixed",
-                   "int8", "fp8", "fp8-e5m2", "int4-head", "int4-kivi", "int4-kivi-s4", "int4-kivi-d64", "int4-kivi-p96")
+                   "int8", "fp8", "fp8-e5m2", "int4-head", "int4-kivi", "int4-kivi-s4", "int4-kivi-d64", "int4-kivi-p96",
+                   "tree-verify@int8", "tree-verify@int4-head", "tree-verify@int4-kivi",
+                   "mixed@int8", "mixed@int4-head", "mixed@int4-kivi")
 CONFIG_LABEL = {"tiny": "1 tiny contiguous", "long-s1": "3 long context S_q=1", "long-s4": "3 long context S_q=4",
                 "sink-window": "4a sink + window", "index-list": "4b index lists", "int8": "5a INT8",
                 "int4-kivi": "5b KIVI INT4"}
@@ -121,7 +123,7 @@ def stream_bytes(p, info, lens):
         return info["stream_keys"] * (d + 8)
     G, Gv, R = p["kivi_group"], p["kivi_v_group"], p["kivi_residual"]
     total = 0
-    for T in lens:      # causal, S_q = 1: the stream is the whole history
+    for T in lens:      # causal (the last query row sees every stored key) or FlashMask: the whole history
         nq = G * -(-max(0, T - R) // G)
         total += nq * (d + 4 * d // Gv) + (nq // G) * 4 * d + (T - nq) * 4 * d
     return total * p["H_kv"]
@@ -419,6 +421,22 @@ def quantized_cache(dattn, w, fmt, dev):
 def build_workload(dattn, name, dev):
     """(workload, problem, device cache tensors) of a named workload."""
     import workloads as W
+    if "@" in name:
+        # BASE@FMT: the tree-verify or mixed workload (its lengths, query, FlashMask intervals
+        # and qo_indptr) over a cache of format FMT written by kv_append from bf16 history
+        base, fq = name.split("@")
+        src = {"tree-verify": W.tree_verify, "mixed": W.mixed_batch}[base]("cpu")
+        fmt, p0 = QUANT[fq], src.problem
+        w = W.quantized_history(f"{src.name}, {fmt} K/V", B=p0["B"], S_q=p0["S_q"], H_q=p0["H_q"],
+                                H_kv=p0["H_kv"], d=p0["d"], lens=src.kv_len.tolist(), P=p0["P"], seed=7,
+                                device=dev, fmt=fmt)
+        w.problem = dict(w.problem, mask=p0["mask"])
+        w.q, w.qo_indptr, w.fm_intervals = src.q.to(dev), src.qo_indptr, src.fm_intervals
+        p, cache = quantized_cache(dattn, w, fmt, dev)
+        if w.fm_intervals is not None:
+            cache["fm_intervals"] = w.fm_intervals.to(dev).contiguous()
+        w.k_rows = w.v_rows = None
+        return w, p, cache
     if name in QUANT:
         # int4-kivi-s4: the quantized workload with 4 verify rows per request (16 rows per kv
         # head); int4-kivi-d64: 64-channel heads (V channel groups of 16); int4-kivi-p96:
@@ -857,7 +875,11 @@ def run_other(args):
     s = summary(samples)
     fallbacks = dattn.dattn_shift_fallbacks(step.ws, step.stream) if args.shared_shift else None
     tl = timeline(step)
-    nb = stream_bytes(p, step.info, w.kv_len.tolist())
+    lens = w.kv_len.tolist()
+    if w.qo_indptr is not None:      # an idle request (C_b = 0) reads nothing
+        qo = [int(x) for x in w.qo_indptr]
+        lens = [t if qo[b + 1] > qo[b] else 0 for b, t in enumerate(lens)]
+    nb = stream_bytes(p, step.info, lens)
     peak, peak_src = measured_peak()
     print(json.dumps({"workload": w.name, "us_per_step": total_ms * 1e3 / max(MIN_SAMPLES, args.steps),
                       "us_per_step_samples": s, "kv_bytes_per_step": nb, "GBps": nb / s["median"] / 1e3,
