@@ -597,8 +597,11 @@ def timeline(step, n_steps=40, skip=10):
                 "stream_median_cta_us": (np.median(end) - np.median(wait)) / 1e3,
                 "tail_last_cta_us": (end.max() - np.median(end)) / 1e3,
                 "cta_end_spread_p5_p95_us": (np.percentile(end, 95) - np.percentile(end, 5)) / 1e3,
+                # the merge of a group starts once its states are tagged, so it may begin
+                # before the last partial CTA ends (a negative wait)
                 "merge_wait_after_last_cta_us": (merge_start - end.max()) / 1e3,
                 "merge_us": (merge_end - merge_start) / 1e3,
+                "merge_end_after_last_cta_us": (merge_end - end.max()) / 1e3,
                 "period_us": (merge_end - prev_merge_end) / 1e3,
             })
         prev_merge_end = merge_end

@@ -185,6 +185,14 @@ typedef struct {
                                    cut into one segment per CTA, so that a CTA holding many
                                    short items (tiny requests) gets fewer keys.  0 = library
                                    default (about 48 KB of K/V per item); < 0 = none     */
+  int32_t merge_tags;           /* bf16 plans with an LSE-merge kernel: 1 = every partial
+                                   warp tags its state rows with the run's number once
+                                   written (after one gpu-scope fence), and the merge folds
+                                   each group as soon as its states carry the tag, while the
+                                   rest of the partial grid still runs; -1 = the merge waits
+                                   for the whole partial grid; 0 = library default (tags
+                                   when the merge folds at least 2048 group rows).  Ignored
+                                   for the other formats and for fused_merge plans        */
 } dattn_plan_inputs;
 
 typedef struct dattn_plan_s dattn_plan_t;
@@ -222,7 +230,7 @@ typedef struct {
   int64_t max_cta_keys;     /* keys of the most loaded CTA                             */
   int32_t fused_merge;      /* 1: the last CTA to finish a group's chunks merges it     */
                             /*    inside the partial kernel (no merge launch)          */
-  int32_t reserved;
+  int32_t merge_tags;       /* 1: the merge waits for state-row tags (see merge_tags)  */
 } dattn_plan_info;
 
 /* One work item as planned: keys [a, e) of the visible stream of (b, h_kv).

@@ -52,7 +52,7 @@ class PlanInputs(ctypes.Structure):
                 ("index_indptr", ctypes.c_void_p), ("index_list", ctypes.c_void_p),
                 ("num_sms", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("chunk_tokens", ctypes.c_int32), ("fused_merge", ctypes.c_int32),
-                ("qo_indptr", ctypes.c_void_p), ("item_cost_keys", ctypes.c_int32)]
+                ("qo_indptr", ctypes.c_void_p), ("item_cost_keys", ctypes.c_int32), ("merge_tags", ctypes.c_int32)]
 
 
 class HostStep(ctypes.Structure):
@@ -72,7 +72,7 @@ class PlanInfo(ctypes.Structure):
                 ("n_items", ctypes.c_int32), ("n_ctas", ctypes.c_int32), ("n_slots", ctypes.c_int32),
                 ("n_merge_groups", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("rows", ctypes.c_int32), ("stream_keys", ctypes.c_int64),
-                ("max_cta_keys", ctypes.c_int64), ("fused_merge", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("max_cta_keys", ctypes.c_int64), ("fused_merge", ctypes.c_int32), ("merge_tags", ctypes.c_int32)]
 
 
 class WorkItem(ctypes.Structure):
@@ -234,7 +234,8 @@ class Plan:
 
 
 def dattn_plan(problem, kv_len, *, page_indptr=None, index_indptr=None, index_list=None, num_sms=None,
-               ctas_per_sm=0, chunk_tokens=0, fused_merge=False, qo_indptr=None, item_cost_keys=0) -> Plan:
+               ctas_per_sm=0, chunk_tokens=0, fused_merge=False, qo_indptr=None, item_cost_keys=0,
+               merge_tags=0) -> Plan:
     """Host-only planning (see dattn_plan in dattn.h).  Arrays are host int32."""
     lib = load()
     prob = problem if isinstance(problem, Problem) else make_problem(problem)
@@ -245,7 +246,7 @@ def dattn_plan(problem, kv_len, *, page_indptr=None, index_indptr=None, index_li
             _i32_host(qo_indptr)]
     inp = PlanInputs(_ptr(keep[0]), _ptr(keep[1]), _ptr(keep[2]), _ptr(keep[3]), int(num_sms),
                      int(ctas_per_sm), int(chunk_tokens), int(bool(fused_merge)), _ptr(keep[4]),
-                     int(item_cost_keys))
+                     int(item_cost_keys), int(merge_tags))
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     _check(lib.dattn_plan(ctypes.byref(prob), ctypes.byref(inp), ctypes.byref(handle), ctypes.byref(ws)),

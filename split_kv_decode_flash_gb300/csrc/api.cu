@@ -2,6 +2,8 @@
 // dattn_device_status and the bit-exact debug hooks.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -171,6 +173,15 @@ void bind_blob(const dattn_plan_t* plan, void* ws, PartialParams& k) {
   k.groups = reinterpret_cast<const MergeGroup*>(base + h->off_merge);
   k.group_count = reinterpret_cast<int32_t*>(base + h->off_count);
   k.fused = h->fused;
+  k.state_seq = h->tags ? reinterpret_cast<int32_t*>(base + h->off_seq) : nullptr;
+}
+
+// A tag no earlier run of this process carried (never 0, the uploaded value).
+int32_t next_run_seq() {
+  static std::atomic<uint32_t> seq{0};
+  uint32_t s = seq.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (s == 0) s = seq.fetch_add(1, std::memory_order_relaxed) + 1;
+  return static_cast<int32_t>(s);
 }
 
 dattn_status upload_blob(const dattn_plan_t* plan, void* ws, cudaStream_t s, PartialParams& k) {
@@ -260,6 +271,8 @@ dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const
     st = upload_blob(plan, workspace, s, k);
     if (st != DATTN_OK) return st;
   }
+  k.run_seq = next_run_seq();
+  k.n_slots = plan->info.n_slots;
   if ((st = record(events, 0, s)) != DATTN_OK) return st;
   if (plan->info.n_ctas > 0) {
     const int err = launch_partial(k, prob->d_h, plan->info.n_ctas, stream);
@@ -282,6 +295,12 @@ dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const
     m.H_q = k.H_q;
     m.mean_states = plan->info.n_slots / plan->info.n_merge_groups;
     m.trace = trace ? trace + static_cast<size_t>(plan->info.n_ctas) * kTraceSlots : nullptr;
+    // the merge warps wait for their states' tags; the limit only bounds a failure, as a
+    // group's states may take the whole partial kernel to complete
+    m.state_seq = k.state_seq;
+    m.run_seq = k.run_seq;
+    m.n_slots = k.n_slots;
+    m.wait_ns = std::max<uint64_t>(2 * k.wait_ns, 4000000000ull);
     const int err = launch_merge(m, prob->d_h, stream);
     if (err != cudaSuccess) return cuda_fail("dattn_run merge kernel", err);
   }

@@ -92,11 +92,12 @@ struct BlobHeader {
   int32_t n_items, n_ctas, n_merge, rows, n_slots;
   int32_t fused;         // merge groups merged inside the partial kernel
   int32_t shift_fallbacks;   // warps that left the shared-shift frame, zeroed by the upload
-  int32_t pad0;
+  int32_t tags;          // the separate merge waits for state-row tags, not for the whole grid
   int64_t off_items, off_cta_indptr, off_cta_items, off_merge, off_ml, off_u, off_cta_recs;
   int64_t off_count;     // int32 [n_merge]: finished items per merge group (fused merge)
+  int64_t off_seq;       // int32 [rows][n_slots]: run tag of every state row (when tags), zeroed
 };
-static_assert(sizeof(BlobHeader) == 104, "BlobHeader layout");
+static_assert(sizeof(BlobHeader) == 112, "BlobHeader layout");
 
 // Arguments of the partial kernel (passed by value as a grid constant).
 struct PartialParams {
@@ -136,6 +137,12 @@ struct PartialParams {
   uint64_t wait_ns;       // limit of every bounded mbarrier wait
   int32_t skip_arrival;   // test hook (bf16 kernel): CTA 0 never completes its first stage
   uint64_t* trace;        // timeline trace (bf16 kernel): kTraceSlots %globaltimer stamps per CTA, or null
+  // Separate merge: the tag of each state row, [rows][n_slots] (a row's tags of
+  // consecutive states are adjacent, as the merge polls them), stored once the
+  // row's (m, l, u) is written; null when no merge kernel follows.
+  int32_t* state_seq;
+  int32_t run_seq;        // this run's tag (never 0)
+  int32_t n_slots;
 };
 
 // Timeline trace of the bf16 partial kernel: per CTA, kTraceSlots words of
@@ -159,7 +166,11 @@ struct MergeParams {
   int32_t* status;
   int32_t n_groups, rows, g, S_q, H_q;
   int32_t mean_states;   // partial states per merge group, on average (chooses the warps per row)
-  uint64_t* trace;       // two stamps per block (past the wait, done), or null
+  uint64_t* trace;       // two stamps per block (its states ready, done), or null
+  const int32_t* state_seq;   // the partial kernel's state-row tags ([rows][n_slots]), or null (then wait
+                              // for the whole grid)
+  int32_t run_seq, n_slots;
+  uint64_t wait_ns;      // limit of a warp's wait for its states' tags
 };
 
 // Kernel launchers (partial*.cu, merge.cu); return cudaError_t as int.

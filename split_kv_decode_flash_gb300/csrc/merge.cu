@@ -14,9 +14,13 @@
 // (group, row).  A warp's lanes fetch (m, l) of up to 32 states at once, the
 // warp agrees on the frame, and the u vectors of the live states are then
 // read a batch at a time with the loads in flight (each lane owns d / 32
-// channels).  The kernel is launched as a programmatic
-// dependent of the partial kernel: it is resident before the partial kernel
-// ends and waits (griddepcontrol.wait) for its states to be complete.
+// channels).  The kernel is launched as a programmatic dependent of the
+// partial kernel, whose warps tag each state row with the run's number once
+// it is written (release); a merge warp waits (acquire) for the tags of its
+// own states only, so the groups that finish early are merged while the
+// partial grid's last CTAs still run.  Each block ends with griddepcontrol.wait,
+// so that the merge grid completes after the partial grid.  Without tags the
+// whole grid is awaited first.
 #include <cuda_runtime.h>
 
 #include "merge.cuh"
@@ -33,10 +37,20 @@ __device__ __forceinline__ unsigned long long merge_clock_ns() {
   return t;
 }
 
-// Timeline trace: the block's time past its wait, and (latest warp) done.
-__device__ __forceinline__ void merge_trace_done(const MergeParams& p, int lane) {
+// Timeline trace (TAGS): the time the block's (first warp's) states were
+// ready and folded.
+__device__ __forceinline__ void merge_trace_ready(const MergeParams& p, int lane) {
+  if (p.trace && lane == 0) atomicCAS(reinterpret_cast<unsigned long long*>(p.trace) + 2 * blockIdx.x, 0ull, merge_clock_ns());
+}
+
+// A warp's last step: its trace stamp (latest warp: done), then (TAGS) the
+// wait for the partial grid, so that this grid's completion implies the
+// partial grid's.
+template <bool TAGS>
+__device__ __forceinline__ void merge_end(const MergeParams& p, int lane) {
   if (p.trace && lane == 0)
     atomicMax(reinterpret_cast<unsigned long long*>(p.trace) + 2 * blockIdx.x + 1, merge_clock_ns());
+  if constexpr (TAGS) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // WPR = 4: one block of four warps per (group, row); warp w folds states w,
@@ -44,8 +58,9 @@ __device__ __forceinline__ void merge_trace_done(const MergeParams& p, int lane)
 // states).  WPR = 1: one warp per (group, row), four rows per block, each
 // warp folding all of its row's states (many rows, few states each: the
 // combine and its barrier would cost more than the fold).
-// KB: u vectors read per batch.
-template <int D, int WPR, int KB>
+// KB: u vectors read per batch.  TAGS: the warps wait for their states' tags
+// instead of the whole partial grid.
+template <int D, int WPR, int KB, bool TAGS>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_constant__ MergeParams p) {
   constexpr int C = D / 32;
   constexpr int kRowsPerBlock = kMergeWarps / WPR;
@@ -58,33 +73,35 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
   // the merge groups are part of the plan, copied before the partial kernel started:
   // they may be read before the wait
   const MergeGroup grp = p.groups[gi];
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the partial kernel's states are complete
+  const StateTags tg{p.state_seq, p.run_seq, p.n_slots, p.wait_ns, p.status};
+  if constexpr (!TAGS) asm volatile("griddepcontrol.wait;" ::: "memory");   // the partial kernel's states are complete
   // a programmatically launched successor may be scheduled; it waits for this grid
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (p.trace && threadIdx.x == 0) p.trace[2 * blockIdx.x] = merge_clock_ns();
+  if (!TAGS && p.trace && threadIdx.x == 0) p.trace[2 * blockIdx.x] = merge_clock_ns();
   const int i = row / p.g, hq = grp.h * p.g + row % p.g;
   const long long orow = (static_cast<long long>(grp.qo) + i) * p.H_q + hq;
   if constexpr (WPR == 1) {
     if (row >= p.g * grp.nq) {   // the request has fewer query rows than the widest one
-      merge_trace_done(p, lane);
+      merge_end<TAGS>(p, lane);
       return;
     }
     RowFold<D> f;
     fold_init(f);
-    fold_states<D, KB>(p.ml, p.u, p.rows, row, grp.slot0, grp.n, 1, lane, f);
+    fold_states<D, KB, TAGS>(p.ml, p.u, p.rows, row, grp.slot0, grp.n, 1, lane, f, tg);
+    if (TAGS) merge_trace_ready(p, lane);
     if (!f.bad) write_folded_row<D>(p.o, p.lse, orow, f, lane);   // rows with an unwritten state stay unwritten
-    merge_trace_done(p, lane);
+    merge_end<TAGS>(p, lane);
     return;
   } else {
     if (row >= p.g * grp.nq) {
-      merge_trace_done(p, lane);
+      merge_end<TAGS>(p, lane);
       return;
     }
     // warp w folds states w, w + kMergeWarps, ...
     RowFold<D> f;
     fold_init(f);
     const int n_mine = grp.n > w ? (grp.n - w + kMergeWarps - 1) / kMergeWarps : 0;
-    fold_states<D, KB>(p.ml, p.u, p.rows, row, grp.slot0 + w, n_mine, kMergeWarps, lane, f);
+    fold_states<D, KB, TAGS>(p.ml, p.u, p.rows, row, grp.slot0 + w, n_mine, kMergeWarps, lane, f, tg);
     // combine the warps' folds
 #pragma unroll
     for (int c = 0; c < C; ++c) sm_u[w][lane * C + c] = f.U[c];
@@ -94,9 +111,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
     }
     __syncthreads();
     if (w != 0) {
-      merge_trace_done(p, lane);
+      merge_end<TAGS>(p, lane);
       return;
     }
+    if (TAGS) merge_trace_ready(p, lane);
     RowFold<D> t;
     fold_init(t);
 #pragma unroll
@@ -115,7 +133,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
       }
     }
     if (!t.bad) write_folded_row<D>(p.o, p.lse, orow, t, lane);
-    merge_trace_done(p, lane);
+    merge_end<TAGS>(p, lane);
   }
 }
 
@@ -141,7 +159,8 @@ cudaError_t launch_d(const MergeParams& p, void* stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<D, WPR, KB>, p);
+  return p.state_seq ? cudaLaunchKernelEx(&cfg, merge_kernel<D, WPR, KB, true>, p)
+                     : cudaLaunchKernelEx(&cfg, merge_kernel<D, WPR, KB, false>, p);
 }
 
 }  // namespace

@@ -33,19 +33,67 @@ __device__ __forceinline__ void fold_init(RowFold<D>& f) {
   for (int c = 0; c < D / 32; ++c) f.U[c] = 0.f;
 }
 
+// The state-row tags a merge warp waits for (see store_release_gpu): null
+// when the whole partial grid is complete before the merge reads (then every
+// state is).  A warp that sees no tag of this run for "limit_ns" gives up:
+// status kStTimeout, and the row is not written.
+struct StateTags {
+  const int32_t* seq;   // [rows][n_slots]
+  int32_t run_seq, n_slots;
+  uint64_t limit_ns;
+  int32_t* status;
+};
+
+__device__ __forceinline__ unsigned long long merge_now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits until the lane's state (lane < n) carries this run's tag in its row
+// (the row's tags of consecutive states are adjacent: a warp's poll reads a
+// few sectors); false when the wait gave up.  The acquire loads and the
+// __syncwarp order every lane's later reads of the states after their tags.
+__device__ __forceinline__ bool wait_state_tags(const StateTags& tg, long long tag, bool mine, int lane) {
+  constexpr unsigned kAll = 0xffffffffu;
+  bool ready = !mine || load_acquire_gpu(tg.seq + tag) == tg.run_seq;
+  if (!__all_sync(kAll, ready)) {
+    const unsigned long long t0 = merge_now_ns();
+    for (;;) {
+      __nanosleep(128);
+      if (!ready) ready = load_acquire_gpu(tg.seq + tag) == tg.run_seq;
+      if (__all_sync(kAll, ready)) break;
+      if (merge_now_ns() - t0 > tg.limit_ns) {
+        if (lane == 0) atomicOr(tg.status, kStTimeout);
+        return false;
+      }
+    }
+  }
+  __syncwarp();
+  return true;
+}
+
 // Folds states s_first + s_stride * i, i in [0, n), of row "row" into f.
-// Lanes fetch (m, l) of 32 states at a time; the u vectors of the live ones
-// are then read kBatch at a time with all loads in flight (a batch is
-// unrolled: its unused slots still cost their predicated instructions).
-template <int D, int kBatch = 8>
+// Lanes fetch (m, l) of 32 states at a time (TAGS: first waiting for their
+// tags); the u vectors of the live ones are then read kBatch at a time with
+// all loads in flight (a batch is unrolled: its unused slots still cost their
+// predicated instructions).
+template <int D, int kBatch = 8, bool TAGS = false>
 __device__ __forceinline__ void fold_states(const float2* ml, const float* u, int rows, int row, int s_first,
-                                            int n_states, int s_stride, int lane, RowFold<D>& f) {
+                                            int n_states, int s_stride, int lane, RowFold<D>& f,
+                                            const StateTags& tg = StateTags{}) {
   constexpr unsigned kAll = 0xffffffffu;
   constexpr int C = D / 32;
   const long long stride = static_cast<long long>(s_stride) * rows * D;   // between consecutive states
   for (int i0 = 0; i0 < n_states; i0 += 32) {
     const int n = min(32, n_states - i0);
     const int s0 = s_first + s_stride * i0;
+    if constexpr (TAGS) {
+      if (!wait_state_tags(tg, static_cast<long long>(row) * tg.n_slots + s0 + s_stride * lane, lane < n, lane)) {
+        f.bad = true;
+        return;
+      }
+    }
     float2 v = make_float2(-INFINITY, 0.f);
     if (lane < n) v = __ldcg(ml + static_cast<long long>(s0 + s_stride * lane) * rows + row);
     if (__any_sync(kAll, v.y != v.y)) f.bad = true;    // a state marked unwritten

@@ -564,6 +564,22 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
   }
 }
 
+// A consumer warp's states are written (or marked): tag them for the merge.
+// Its rows of an item follow the item's layout, as in consume_bf16.
+__device__ __forceinline__ void publish_bf16_states(const Walk& w, int cw, int lane) {
+  const PartialParams& p = w.p;
+  publish_warp_states(w, [&](const ItemRec& rec, int& st, int& ra, int& rb) {
+    if (p.rows > 16 && p.g * rec.nq > 16) {
+      const WarpRole<32> role(cw, lane);
+      st = role.my_state, ra = role.r0, rb = role.r1;
+    } else {
+      const WarpRole<16> role(cw, lane);
+      st = role.my_state, ra = role.r0, rb = role.r1;
+    }
+    return (lane & 3) == 0;
+  });
+}
+
 // Fused LSE merge (M4.5 §0x02B-§0x02C, as in the merge kernel): after the
 // consumers have written their states, the CTA counts its finished items per
 // merge group; the CTA that completes a group's count merges that group.  The
@@ -653,7 +669,9 @@ __device__ void fused_merge(const Walk& w, uint8_t* smem, int cw, int lane) {
   }
 }
 
-template <int D, bool HK>
+// TAGS: the instance for plans whose merge waits for state-row tags (see
+// state_tags_fence); the other instances compile none of it.
+template <int D, bool HK, bool TAGS>
 __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_constant__ PartialParams p) {
   using C = Bf<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -697,16 +715,17 @@ __global__ void __launch_bounds__(kThreads, 1) partial_bf16_kernel(const __grid_
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBfConsumerRegs));
   if (p.shift_on) consume_bf16<D, true, HK>(w, smem, warp, lane, !complete_now);
   else consume_bf16<D, false, HK>(w, smem, warp, lane, !complete_now);
+  if constexpr (TAGS) publish_bf16_states(w, warp, lane);
   if (HK && lane == 0) trace_stamp(p, kTrConsumerEnd + warp);
   if (p.fused) fused_merge<D>(w, smem, warp, lane);
 }
 
-template <int D, bool HK>
+template <int D, bool HK, bool TAGS>
 int launch_bf16_inst(const PartialParams& p, int n_ctas, void* stream) {
   const size_t smem = Bf<D>::kTotal;
   // the register budget check and the shared-memory opt-in, once per device
   static std::atomic<unsigned long long> ready{0};
-  cudaError_t err = prepare_kernel_once(partial_bf16_kernel<D, HK>, smem, 128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs, ready);
+  cudaError_t err = prepare_kernel_once(partial_bf16_kernel<D, HK, TAGS>, smem, 128 * kBfProducerRegs + 32 * kConsumerWarps * kBfConsumerRegs, ready);
   if (err != cudaSuccess) return err;
   // programmatic launch: the prologue overlaps the tail of the preceding kernel
   cudaLaunchConfig_t cfg = {};
@@ -719,14 +738,16 @@ int launch_bf16_inst(const PartialParams& p, int n_ctas, void* stream) {
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, partial_bf16_kernel<D, HK>, p);
+  err = cudaLaunchKernelEx(&cfg, partial_bf16_kernel<D, HK, TAGS>, p);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 template <int D>
 int launch_bf16(const PartialParams& p, int n_ctas, void* stream) {
-  return p.trace || p.skip_arrival ? launch_bf16_inst<D, true>(p, n_ctas, stream)
-                                   : launch_bf16_inst<D, false>(p, n_ctas, stream);
+  const bool hk = p.trace || p.skip_arrival;
+  if (p.state_seq)
+    return hk ? launch_bf16_inst<D, true, true>(p, n_ctas, stream) : launch_bf16_inst<D, false, true>(p, n_ctas, stream);
+  return hk ? launch_bf16_inst<D, true, false>(p, n_ctas, stream) : launch_bf16_inst<D, false, false>(p, n_ctas, stream);
 }
 
 }  // namespace

@@ -453,7 +453,17 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   hdr.off_cta_recs = off;
   off = align_up(off + sizeof(ItemRec) * n_items, 16);
   hdr.off_count = off;
-  off = align_up(off + sizeof(int32_t) * merges.size(), kWsAlign);
+  off = align_up(off + sizeof(int32_t) * merges.size(), 16);
+  // State-row tags of the separate merge, zero (no run's tag) in every upload (bf16).
+  // When the merge has many rows to fold (at least 2048 group rows) it gains from
+  // starting on each group as soon as its states are tagged; with fewer, the fence that
+  // orders a warp's state writes before its tags (about 1.4 us on the last CTA) costs
+  // more than that saves, and the merge waits for the whole grid instead.
+  hdr.tags = !merges.empty() && !hdr.fused && p.fmt == DATTN_FMT_BF16 &&
+             (in->merge_tags > 0 || (in->merge_tags == 0 && static_cast<long long>(merges.size()) * rows >= 2048));
+  hdr.off_seq = off;
+  if (hdr.tags) off += sizeof(int32_t) * static_cast<size_t>(n_slots) * rows;
+  off = align_up(off, kWsAlign);
   const size_t blob_bytes = off;
   hdr.off_ml = off;
   off = align_up(off + sizeof(float) * 2 * static_cast<size_t>(n_slots) * rows, kWsAlign);
@@ -503,6 +513,7 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   info.n_slots = n_slots;
   info.n_merge_groups = static_cast<int>(merges.size());
   info.fused_merge = hdr.fused;
+  info.merge_tags = hdr.tags;
   info.max_splits = max_splits;
   info.rows = rows;
   info.stream_keys = W;

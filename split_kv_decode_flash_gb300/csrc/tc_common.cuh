@@ -70,6 +70,26 @@ struct Walk {
   }
 };
 
+// The end of a consumer warp (separate merge): tags of every state row it
+// wrote, after one fence (see state_tags_fence).  rows_of(rec, state, ra, rb)
+// gives, for an item, the warp's state index and the lane's two rows (-1:
+// none), and whether this lane wrote their (m, l).
+template <typename RowsOf>
+__device__ __forceinline__ void publish_warp_states(const Walk& w, RowsOf rows_of) {
+  const PartialParams& p = w.p;
+  if (!p.state_seq) return;
+  __syncwarp();
+  state_tags_fence();
+  for (int ii = w.begin; ii < w.end; ++ii) {
+    const ItemRec rec = w.rec(ii);
+    if (rec.it.slot < 0) continue;
+    int st, ra, rb;
+    if (!rows_of(rec, st, ra, rb)) continue;
+    tag_state_row(p, rec.it.slot + st, ra, rec.nq);
+    tag_state_row(p, rec.it.slot + st, rb, rec.nq);
+  }
+}
+
 // ---- PTX wrappers -----------------------------------------------------------------------
 
 // L2 eviction policies: K/V rows are streamed once (evict first); the page

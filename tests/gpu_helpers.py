@@ -81,13 +81,15 @@ def device_tensors(w, o, lse, dev="cuda"):
     return kw
 
 
-def run_gpu(w, *, num_sms=None, ctas_per_sm=0, chunk_tokens=0, problem=None, keep=None, fused_merge=False):
+def run_gpu(w, *, num_sms=None, ctas_per_sm=0, chunk_tokens=0, problem=None, keep=None, fused_merge=False,
+            merge_tags=0):
     """One dattn_run over workload ``w``; returns (O fp32 cpu, LSE cpu, plan info, status flags)."""
     p = problem or w.problem
     B, S_q, H_q, d = p["B"], p["S_q"], p["H_q"], p["d"]
     plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, index_indptr=w.index_indptr,
                             index_list=w.index_list, num_sms=num_sms, ctas_per_sm=ctas_per_sm,
-                            chunk_tokens=chunk_tokens, fused_merge=fused_merge, qo_indptr=w.qo_indptr)
+                            chunk_tokens=chunk_tokens, fused_merge=fused_merge, qo_indptr=w.qo_indptr,
+                            merge_tags=merge_tags)
     n_rows = B * S_q if w.qo_indptr is None else int(w.qo_indptr[-1])
     o = torch.full((n_rows, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((n_rows, H_q), float("nan"), dtype=torch.float32, device="cuda")

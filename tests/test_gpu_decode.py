@@ -162,20 +162,28 @@ def test_index_lists_full_size_all_rows():
 
 # ---- fail-closed bounded waits (M4.5 §0x07B) ----------------------------------------------
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_bounded_wait_gives_up_and_the_step_fails_closed(fused):
+@pytest.mark.parametrize("fused,S_q", [(False, 1), (True, 1), (False, 4)])
+def test_bounded_wait_gives_up_and_the_step_fails_closed(fused, S_q):
     """The test hook withholds the completion of CTA 0's first ring stage: its consumers'
     wait runs out after 1 ms, the CTA stops and the status word gets the timeout bit (16).
     No output row may come from the states it left unwritten: its warps mark their state
     slots unwritten (merge kernel) or count none of their items (fused merge), so the rows
-    of every group CTA 0 took part in stay unwritten, and every other row is exact.  The
-    context stays usable: the next step on the same workspace gives every row exactly."""
-    w = W.paged_ragged_gqa("cuda", B=4, lo=300, hi=900, pool_pages=300)
+    of every group CTA 0 took part in stay unwritten, and every other row is exact.  With
+    S_q = 4 (16 rows per kv head) the merge waits for each state's tag rather than for the
+    whole grid (merge_tags), and the marked states come tagged.  The context stays usable: the next
+    step on the same workspace gives every row exactly."""
+    if S_q == 1:
+        w = W.paged_ragged_gqa("cuda", B=4, lo=300, hi=900, pool_pages=300)
+    else:
+        w = W.paged_bf16("verify", B=4, S_q=S_q, H_q=32, H_kv=8, d=128, lens=[900, 310, 640, 505], P=16,
+                         seed=9, device="cuda", pool_pages=300)
     p = w.problem
-    plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, num_sms=6, fused_merge=fused)
+    plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, num_sms=6, fused_merge=fused,
+                            merge_tags=1 if S_q > 1 else -1)
     assert plan.info["n_merge_groups"] > 0 and bool(plan.info["fused_merge"]) == fused
-    o = torch.full((p["B"], 1, p["H_q"], p["d"]), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lse = torch.full((p["B"], 1, p["H_q"]), float("nan"), dtype=torch.float32, device="cuda")
+    assert plan.info["merge_tags"] == (1 if S_q > 1 else 0)
+    o = torch.full((p["B"], S_q, p["H_q"], p["d"]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((p["B"], S_q, p["H_q"]), float("nan"), dtype=torch.float32, device="cuda")
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
     t = dattn.tensors_from(**H.device_tensors(w, o, lse))
     dattn.dattn_run_ex(plan, p, t, ws, wait_limit_us=1000, test_skip_arrival=True)
@@ -188,8 +196,8 @@ def test_bounded_wait_gives_up_and_the_step_fails_closed(fused):
     assert cta0
     g = p["H_q"] // p["H_kv"]
     for b, h in cta0:          # groups that CTA 0 took part in: never written
-        assert not written[b, 0, h * g:(h + 1) * g].any()
-    rows = [(b, 0, h) for b in range(p["B"]) for h in range(p["H_q"]) if written[b, 0, h]]
+        assert not written[b, :, h * g:(h + 1) * g].any()
+    rows = [(b, i, h) for b in range(p["B"]) for i in range(S_q) for h in range(p["H_q"]) if written[b, i, h]]
     assert rows
     H.compare(O, L, w, rows)
     dattn.dattn_run(plan, p, t, ws)         # uploads the plan again (fresh counters and status)
@@ -198,13 +206,20 @@ def test_bounded_wait_gives_up_and_the_step_fails_closed(fused):
     H.compare(o.float().cpu(), lse.cpu(), w)
 
 
-def test_timeline_trace_is_ordered_and_leaves_the_outputs_unchanged():
+@pytest.mark.parametrize("S_q", [1, 4])
+def test_timeline_trace_is_ordered_and_leaves_the_outputs_unchanged(S_q):
     """dattn_run_options.trace: per CTA the stamps come in pipeline order, every merge block
-    starts after the last partial CTA ended, and the traced step gives the same bits."""
-    w = W.paged_ragged_gqa("cuda", B=6, lo=200, hi=2000, pool_pages=800)
+    finds its states ready after the partial kernel began (with merge tags the merge of a
+    group starts once its states carry the run's tag, possibly before the last partial CTA
+    ends; without, it waits for the whole grid), and the traced step gives the same bits."""
+    if S_q == 1:
+        w = W.paged_ragged_gqa("cuda", B=6, lo=200, hi=2000, pool_pages=800)
+    else:
+        w = W.paged_bf16("verify", B=6, S_q=S_q, H_q=32, H_kv=8, d=128, lens=[1900, 240, 1333, 777, 2000, 450],
+                         P=16, seed=10, device="cuda", pool_pages=800)
     keep = {}
-    O, L, info, flags = H.run_gpu(w, num_sms=16, keep=keep)
-    assert flags == 0 and info["n_merge_groups"] > 0
+    O, L, info, flags = H.run_gpu(w, num_sms=16, keep=keep, merge_tags=1 if S_q > 1 else -1)
+    assert flags == 0 and info["n_merge_groups"] > 0 and info["merge_tags"] == (1 if S_q > 1 else 0)
     n = info["n_ctas"]
     buf = torch.zeros(16 * n + 2 * info["n_merge_groups"] * info["rows"], dtype=torch.int64, device="cuda")
     keep["kw"]["o"].fill_(float("nan"))
@@ -219,7 +234,9 @@ def test_timeline_trace_is_ordered_and_leaves_the_outputs_unchanged():
     assert (P[:, 8:16] >= P[:, 4:5]).all()
     M = t[16 * n:].reshape(-1, 2)
     M = M[M[:, 0] > 0]
-    assert len(M) and (M[:, 0] >= P[:, 8:16].max()).all() and (M[:, 1] >= M[:, 0]).all()
+    assert len(M) and (M[:, 0] >= P[:, 0].min()).all() and (M[:, 1] >= M[:, 0]).all()
+    if S_q == 1:      # no tags: every merge block waits for the whole partial grid
+        assert (M[:, 0] >= P[:, 8:16].max()).all()
 
 
 def test_wait_limit_options_are_checked():
@@ -232,6 +249,27 @@ def test_wait_limit_options_are_checked():
     for limit in (0, 200000):
         with pytest.raises(dattn.DattnError, match="wait limit"):
             dattn.dattn_run_ex(plan, p, t, ws, wait_limit_us=limit, test_skip_arrival=True)
+
+
+@pytest.mark.parametrize("kind", ["decode", "verify", "mixed"])
+def test_merge_tags_give_the_rows_of_the_whole_grid_wait(kind):
+    """merge_tags = 1 (the merge folds each group once its states carry the run's tag) and
+    -1 (it waits for the whole partial grid) give the same bits on every row, equal to the
+    oracle's: 4 rows per kv head, 16 (S_q = 4) and a mixed batch of up to 32."""
+    if kind == "decode":
+        w = W.paged_ragged_gqa("cuda", B=5, lo=300, hi=3000, pool_pages=1000)
+    elif kind == "verify":
+        w = W.paged_bf16("verify", B=5, S_q=4, H_q=32, H_kv=8, d=128, lens=[2900, 40, 1500, 801, 3000],
+                         P=16, seed=11, device="cuda", pool_pages=1000)
+    else:
+        w = W.mixed_batch("cuda", B=8, lo=200, hi=2500)
+    outs = {}
+    for tags in (1, -1):
+        O, L, info, flags = H.run_gpu(w, num_sms=24, merge_tags=tags)
+        assert flags == 0 and info["n_merge_groups"] > 0 and info["merge_tags"] == (tags > 0)
+        outs[tags] = (O, L)
+    assert torch.equal(outs[1][0], outs[-1][0]) and torch.equal(outs[1][1], outs[-1][1])
+    H.compare_all_rows(outs[1][0], outs[1][1], w)
 
 
 # ---- bit-exact debug hooks --------------------------------------------------------------
