@@ -72,6 +72,8 @@ def parse():
     ap.add_argument("--no-configs", action="store_true", help="headline only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunk", type=int, default=0, help="planner chunk width (0 = default)")
+    ap.add_argument("--merge-tags", type=int, default=0, choices=(-1, 0, 1),
+                    help="the plan's merge_tags (0 = library default)")
     ap.add_argument("--shared-shift", default=None, metavar="PHI,LO,HI",
                     help="bf16 partials in the common frame PHI with the guard LO < s - PHI < HI")
     ap.add_argument("--workload", choices=("paged",) + OTHER_WORKLOADS, default="paged",
@@ -468,12 +470,12 @@ def build_workload(dattn, name, dev):
 class Step:
     """A planned decode step of one workload with its buffers, uploaded once."""
 
-    def __init__(self, dattn, w, p, cache, dev, num_sms, chunk=0, shift=None):
+    def __init__(self, dattn, w, p, cache, dev, num_sms, chunk=0, shift=None, merge_tags=0):
         import torch
         self.dattn, self.p, self.shift = dattn, p, shift
         self.plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, index_indptr=w.index_indptr,
                                      index_list=w.index_list, num_sms=num_sms, chunk_tokens=chunk,
-                                     qo_indptr=w.qo_indptr)
+                                     qo_indptr=w.qo_indptr, merge_tags=merge_tags)
         self.info = self.plan.info
         n_rows = p["B"] * p["S_q"] if w.qo_indptr is None else int(w.qo_indptr[-1])   # packed query rows
         self.o = torch.empty((n_rows, p["H_q"], p["d"]), dtype=torch.bfloat16, device=dev)
@@ -744,7 +746,7 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(dev)
     num_sms = props.multi_processor_count
     w, p, cache = build_workload(dattn, "paged", dev)
-    step = Step(dattn, w, p, cache, dev, num_sms, chunk=args.chunk, shift=_shift(args))
+    step = Step(dattn, w, p, cache, dev, num_sms, chunk=args.chunk, shift=_shift(args), merge_tags=args.merge_tags)
     info = step.info
     ab = algorithmic_bytes(w, info, step.plan.items())
     for _ in range(max(3, args.warmup)):
@@ -868,7 +870,8 @@ def run_other(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     props = torch.cuda.get_device_properties(dev)
     w, p, cache = build_workload(dattn, args.workload, dev)
-    step = Step(dattn, w, p, cache, dev, props.multi_processor_count, chunk=args.chunk, shift=_shift(args))
+    step = Step(dattn, w, p, cache, dev, props.multi_processor_count, chunk=args.chunk, shift=_shift(args),
+                merge_tags=args.merge_tags)
     for _ in range(3):
         step.run()
     torch.cuda.synchronize()
@@ -887,7 +890,8 @@ def run_other(args):
     print(json.dumps({"workload": w.name, "us_per_step": total_ms * 1e3 / max(MIN_SAMPLES, args.steps),
                       "us_per_step_samples": s, "kv_bytes_per_step": nb, "GBps": nb / s["median"] / 1e3,
                       "frac": nb / s["median"] / 1e3 / peak, "peak": peak, "peak_source": peak_src,
-                      "rows": step.info["rows"], "n_items": step.info["n_items"], "steps": args.steps,
+                      "rows": step.info["rows"], "n_items": step.info["n_items"], "merge_tags": step.info["merge_tags"],
+                      "steps": args.steps,
                       "shared_shift": _shift(args), "shift_fallbacks": fallbacks, "timeline": tl,
                       "timing": "us_per_step: CUDA events around K back-to-back decode steps (partial + merge); "
                                 "samples: a second region of K steps with an event after every K/50; GBps and "

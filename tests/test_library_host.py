@@ -316,25 +316,21 @@ def test_equal_segments_weigh_the_keys_of_wide_bf16_requests():
 
 
 def test_merge_tags_follow_the_plan_inputs():
-    """merge_tags: 1 forces state-row tags on a bf16 plan with a merge kernel, -1 turns them
-    off, 0 takes them when the merge folds at least 2048 group rows; never for the other
-    formats, fused merges or plans without merge groups; the blob then holds one zeroed
-    int32 tag per state row."""
+    """merge_tags: state-row tags on a bf16 plan with a merge kernel unless -1 turns them
+    off; never for the other formats or fused merges; the blob then holds one zeroed int32
+    tag per state row."""
     T = [4096, 3587]
     prob = _problem(fixed_splits=8)
     base = dattn.dattn_plan(prob, T, num_sms=152, merge_tags=-1).info
     on = dattn.dattn_plan(prob, T, num_sms=152, merge_tags=1).info
     assert base["merge_tags"] == 0 and on["merge_tags"] == 1
-    assert dattn.dattn_plan(prob, T, num_sms=152).info["merge_tags"] == 0      # 2 x 2 groups x 4 rows
+    assert dattn.dattn_plan(prob, T, num_sms=152).info["merge_tags"] == 1
     assert on["blob_bytes"] >= base["blob_bytes"] + 4 * on["n_slots"] * on["rows"]
     assert on["blob_bytes"] - base["blob_bytes"] < 4 * on["n_slots"] * on["rows"] + 256
     assert dattn.dattn_plan(prob, T, num_sms=152, merge_tags=1, fused_merge=True).info["merge_tags"] == 0
     q8 = _problem(fixed_splits=8, fmt="int8")
     assert dattn.dattn_plan(q8, T, page_indptr=np.array([0, 256, 481], np.int32), num_sms=152,
                             merge_tags=1).info["merge_tags"] == 0
-    # 16 requests x 8 kv heads x 32 rows, every group split: the default takes the tags
-    wide = _problem(B=16, S_q=8, H_q=32, H_kv=8, fixed_splits=4)
-    assert dattn.dattn_plan(wide, [600] * 16, num_sms=152).info["merge_tags"] == 1
 
 
 def test_mixed_batch_validation():
