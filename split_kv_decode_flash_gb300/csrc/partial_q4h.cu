@@ -422,12 +422,14 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
           }
         }
         // block bb: keys base + 16 bb + g4 (s0, s1) and + 8 (s2, s3); rows ra (s0, s2), rb1 (s1, s3).
-        // q . k_hat = s_t 2^24 S' - o_t s_t sum(q), in log2 units; -inf where masked
+        // q . k_hat = s_t 2^24 S' - o_t s_t sum(q), in log2 units; -inf where masked.  A
+        // step of a FULL stage whose 32 slots all hold keys needs no visibility (rows past
+        // the request's have a zero query, stay finite and are never written).
+        const bool all_seen = full && base + 32 <= j1 - j0;
         float vsx[2], vsy[2], vox[2], voy[2];
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           const int kx = base + 16 * bb + g4, ky = kx + 8;
-          const int tx = pos[kx], ty = pos[ky];
           const float2 ksx = h2_to_f2(kqp[kx]), ksy = h2_to_f2(kqp[ky]);
           const float2 vqx = h2_to_f2(vqp[kx]), vqy = h2_to_f2(vqp[ky]);
           vsx[bb] = vqx.x;
@@ -435,6 +437,14 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
           vsy[bb] = vqy.x;
           voy[bb] = vqy.y;
           const float zx = -ksx.y * ksx.x, zy = -ksy.y * ksy.x;   // exact: fp16 x fp16
+          if (all_seen) {
+            s[bb][0] = fmaf(ksx.x * ku0, s[bb][0], zx * kz0);
+            s[bb][1] = fmaf(ksx.x * ku1, s[bb][1], zx * kz1);
+            s[bb][2] = fmaf(ksy.x * ku0, s[bb][2], zy * kz0);
+            s[bb][3] = fmaf(ksy.x * ku1, s[bb][3], zy * kz1);
+            continue;
+          }
+          const int tx = pos[kx], ty = pos[ky];
           bool vxa, vxb, vya, vyb;
           if constexpr (FM) {   // FlashMask: the producer's row bits of the columns
             const uint32_t* vis = reinterpret_cast<const uint32_t*>(smem + C::kVis) + st * kHK;
