@@ -276,8 +276,10 @@ dattn_status dattn_plan_get_items(const dattn_plan_t* plan, dattn_work_item* ite
  * DATTN_RUN_REUSE_UPLOAD) afterwards.  "prob" must equal the planned problem
  * (else ESTALE_PLAN).  Device-side bounds checks (page id < num_pages, block
  * inside the request's page list, list entry inside [0, T_b), cache row <
- * B_cache) skip the offending rows and raise a flag that dattn_device_status
- * reports. */
+ * B_cache) raise a flag that dattn_device_status reports; the offending rows
+ * are never read (they are skipped, or taken as zero rows), so the outputs of
+ * the groups they belong to are undefined.  Device list bounds that disagree
+ * with the plan drop the group's keys: its rows come out all-masked. */
 dattn_status dattn_run(const dattn_plan_t* plan, const dattn_problem* prob,
                        const dattn_tensors* t, void* workspace, size_t workspace_bytes,
                        void* stream);

@@ -442,7 +442,9 @@ __device__ __forceinline__ SlotRows<S, FM> slot_rows(const Walk& w, const PCur& 
       if (c.j0 + lane + 32 * h < c.j1) all = all && d.vis[h] == row_bits(0, r.nq);
     d.full = __all_sync(kAll, all);
   } else {
-    d.full = stage_is_full(p, r.it, r.nq, c.j0, c.j1, tmax, -1);
+    // list bounds that disagree with the plan drop every key of the stage, which must
+    // then stay masked: only the consumers' per-key path does that
+    d.full = stage_is_full(p, r.it, r.nq, c.j0, c.j1, tmax, -1) && !k.bad;
   }
   return d;
 }
