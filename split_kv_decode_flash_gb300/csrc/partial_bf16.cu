@@ -181,14 +181,15 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
   if constexpr (HK) {
     if (pw == 0 && lane == 0) trace_stamp(p, kTrWaitDone);
   }
-  int pid0 = run_stage_page(w, s0, lane);
-  int pid1 = run_stage_page(w, s1, lane);
+  StagePage g0 = run_stage_page(w, s0, lane);
+  StagePage g1 = run_stage_page(w, s1, lane);
 
   for (uint32_t k = pw; c0.ii < w.end; k += kProducerWarps) {
     const int st = k % C::kStagesN;
     const uint32_t use = k / C::kStagesN;
     if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     const ItemRec rec = w.rec(c0.ii);
+    const int pid0 = check_stage_page(p, g0);   // loaded a stage ago
     uint32_t rows[2];
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
 #pragma unroll
@@ -224,10 +225,10 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
 
     c0 = c1;
     s0 = s1;
-    pid0 = pid1;
+    g0 = g1;
     pc_advance<kTK>(w, c1, kProducerWarps);
     s1 = run_stage(w, c1);
-    pid1 = run_stage_page(w, s1, lane);
+    g1 = run_stage_page(w, s1, lane);
   }
   asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy of this thread outlives it
 }

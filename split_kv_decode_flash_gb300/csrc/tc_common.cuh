@@ -481,26 +481,40 @@ __device__ __forceinline__ RunStage run_stage(const Walk& w, const PCur& c) {
   return r;
 }
 
-// The lane's page id for stage r (-1: the lane holds none; -2: invalid, reported).
-__device__ __forceinline__ int run_stage_page(const Walk& w, const RunStage& r, int lane) {
-  if (r.ii >= w.end) return -1;
+// The lane's page id for stage r, its load issued without waiting for it: the
+// value is checked (check_stage_page) when the stage is described, a stage
+// later, so that the load's latency overlaps the previous stage.  state: 0
+// loaded, 1 the lane holds none, 2 the block lies outside the request's page
+// list (reported).
+struct StagePage {
+  int pid, state;
+};
+
+__device__ __forceinline__ StagePage run_stage_page(const Walk& w, const RunStage& r, int lane) {
+  if (r.ii >= w.end) return {0, 1};
   const PartialParams& p = w.p;
   const ItemRec rec = w.rec(r.ii);
   const int np2 = r.n2 ? ((r.q0 + r.n2 - 1) >> p.P_shift) - r.b2 + 1 : 0;
   int blk;
   if (lane < r.np1) blk = r.b1 + lane;
   else if (lane < r.np1 + np2) blk = r.b2 + (lane - r.np1);
-  else return -1;
+  else return {0, 1};
   if (blk >= rec.hi - rec.lo) {
     atomicOr(p.status, kStBlockRange);
-    return -2;
+    return {0, 2};
   }
-  const int pid = ld_keep(p.page_indices + rec.lo + blk, w.keep);
-  if (pid < 0 || pid >= p.num_pages) {
+  return {ld_keep(p.page_indices + rec.lo + blk, w.keep), 0};
+}
+
+// The page id as run_slot takes it: -1 the lane holds none, -2 invalid (reported).
+__device__ __forceinline__ int check_stage_page(const PartialParams& p, const StagePage& g) {
+  if (g.state == 1) return -1;
+  if (g.state == 2) return -2;
+  if (g.pid < 0 || g.pid >= p.num_pages) {
     atomicOr(p.status, kStPageRange);
     return -2;
   }
-  return pid;
+  return g.pid;
 }
 
 // Key (-1: none) and K/V row (kNoRow: none) of slot s of stage r; every lane
