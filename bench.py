@@ -594,6 +594,8 @@ def timeline(step, n_steps=40, skip=10):
         if prev_merge_end is not None and k >= skip:
             rows.append({
                 "wait_after_prev_step_us": (np.median(wait) - prev_merge_end) / 1e3,
+                "first_page_after_wait_us": (np.median(P[live & (P[:, 6] > 0), 6] - P[live & (P[:, 6] > 0), 2]) / 1e3
+                                             if (live & (P[:, 6] > 0)).any() else None),
                 "first_copy_after_wait_us": np.median(P[live, 3] - wait) / 1e3,
                 "first_stage_after_wait_us": np.median(P[live & (P[:, 4] > 0), 4] - P[live & (P[:, 4] > 0), 2]) / 1e3,
                 "stream_median_cta_us": (np.median(end) - np.median(wait)) / 1e3,

@@ -148,11 +148,13 @@ struct PartialParams {
 // Timeline trace of the bf16 partial kernel: per CTA, kTraceSlots words of
 // %globaltimer (ns): entry, records read, producer warp 0 past the wait for the
 // preceding grid, its first stage's copies issued, the first stage landed for
-// consumer warp 0, the SM the CTA runs on (slot 5, %smid, not a time), and
-// the end of each consumer warp (slots 8 + warp).  The
-// merge kernel follows with two words per block: past its wait, and done.
+// consumer warp 0, the SM the CTA runs on (slot 5, %smid, not a time), the
+// first stage's page ids checked by producer warp 0 (slot 6, page-run
+// producer), and the end of each consumer warp (slots 8 + warp).  The merge
+// kernel follows with two words per block: past its wait (or, with state tags,
+// its states ready), and done.
 enum TraceSlot : int { kTrEntry = 0, kTrRecords = 1, kTrWaitDone = 2, kTrFirstCopy = 3, kTrFirstStage = 4,
-                       kTrSm = 5, kTrConsumerEnd = 8 };
+                       kTrSm = 5, kTrFirstPage = 6, kTrConsumerEnd = 8 };
 constexpr int kTraceSlots = 16;
 
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s

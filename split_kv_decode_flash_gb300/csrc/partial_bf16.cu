@@ -190,6 +190,9 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
     if (use > 0 && !mbar_wait(empty0 + 8 * st, (use - 1) & 1, abort_flag, p.status)) break;
     const ItemRec rec = w.rec(c0.ii);
     const int pid0 = check_stage_page(p, g0);   // loaded a stage ago
+    if constexpr (HK) {
+      if (k == 0 && lane == 0) trace_stamp(p, kTrFirstPage);
+    }
     uint32_t rows[2];
     int* pos = reinterpret_cast<int*>(smem + C::kPos) + st * kTK;
 #pragma unroll
