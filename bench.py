@@ -74,6 +74,7 @@ def parse():
     ap.add_argument("--chunk", type=int, default=0, help="planner chunk width (0 = default)")
     ap.add_argument("--merge-tags", type=int, default=0, choices=(-1, 0, 1),
                     help="the plan's merge_tags (0 = library default)")
+    ap.add_argument("--fused-merge", action="store_true", help="--workload: plan with fused_merge")
     ap.add_argument("--shared-shift", default=None, metavar="PHI,LO,HI",
                     help="bf16 partials in the common frame PHI with the guard LO < s - PHI < HI")
     ap.add_argument("--workload", choices=("paged",) + OTHER_WORKLOADS, default="paged",
@@ -470,12 +471,12 @@ def build_workload(dattn, name, dev):
 class Step:
     """A planned decode step of one workload with its buffers, uploaded once."""
 
-    def __init__(self, dattn, w, p, cache, dev, num_sms, chunk=0, shift=None, merge_tags=0):
+    def __init__(self, dattn, w, p, cache, dev, num_sms, chunk=0, shift=None, merge_tags=0, fused_merge=False):
         import torch
         self.dattn, self.p, self.shift = dattn, p, shift
         self.plan = dattn.dattn_plan(p, w.kv_len, page_indptr=w.page_indptr, index_indptr=w.index_indptr,
                                      index_list=w.index_list, num_sms=num_sms, chunk_tokens=chunk,
-                                     qo_indptr=w.qo_indptr, merge_tags=merge_tags)
+                                     qo_indptr=w.qo_indptr, merge_tags=merge_tags, fused_merge=fused_merge)
         self.info = self.plan.info
         n_rows = p["B"] * p["S_q"] if w.qo_indptr is None else int(w.qo_indptr[-1])   # packed query rows
         self.o = torch.empty((n_rows, p["H_q"], p["d"]), dtype=torch.bfloat16, device=dev)
@@ -611,7 +612,10 @@ def timeline(step, n_steps=40, skip=10):
         prev_merge_end = merge_end
     if not rows:
         return None
-    out = {k: float(np.median([r[k] for r in rows])) for k in rows[0]}
+    out = {}
+    for k in rows[0]:      # a phase the step's producer does not stamp is None
+        vals = [r[k] for r in rows if r[k] is not None]
+        out[k] = float(np.median(vals)) if vals else None
     # how much of the CTAs' spread belongs to the SM (same SM slow in every step) rather than
     # to the step: the variance of the per-SM means over the variance of all samples
     allv = [x for v in per_sm.values() for x in v]
@@ -873,7 +877,7 @@ def run_other(args):
     props = torch.cuda.get_device_properties(dev)
     w, p, cache = build_workload(dattn, args.workload, dev)
     step = Step(dattn, w, p, cache, dev, props.multi_processor_count, chunk=args.chunk, shift=_shift(args),
-                merge_tags=args.merge_tags)
+                merge_tags=args.merge_tags, fused_merge=args.fused_merge)
     for _ in range(3):
         step.run()
     torch.cuda.synchronize()

@@ -190,7 +190,8 @@ typedef struct {
                                    written (after one gpu-scope fence), and the merge folds
                                    each group as soon as its states carry the tag, while the
                                    rest of the partial grid still runs; -1 = the merge waits
-                                   for the whole partial grid; 0 = library default (tags).
+                                   for the whole partial grid; 0 = library default (tags
+                                   when the merge folds at least 64 group rows).
                                    Ignored for the other formats (their merge waits for
                                    the grid) and for fused_merge plans                    */
 } dattn_plan_inputs;

@@ -458,8 +458,10 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   // the merge starts on each group as soon as its states are tagged.  Measured on GB300
   // against the merge waiting for the whole grid: mixed batch -3.0 us, long context
   // S_q = 1 -1.3 us, tree verify -1.0 us, sink + window -0.4 us, index lists -0.2 us,
-  // the headline unchanged, long context S_q = 4 +0.2 us.
-  hdr.tags = !merges.empty() && !hdr.fused && p.fmt == DATTN_FMT_BF16 && in->merge_tags >= 0;
+  // the headline unchanged, long context S_q = 4 +0.2 us; a merge of fewer than 64 group
+  // rows (the 8 of the tiny decode) gains nothing to make up for the fence, +0.2 us.
+  hdr.tags = !merges.empty() && !hdr.fused && p.fmt == DATTN_FMT_BF16 &&
+             (in->merge_tags > 0 || (in->merge_tags == 0 && static_cast<long long>(merges.size()) * rows >= 64));
   hdr.off_seq = off;
   if (hdr.tags) off += sizeof(int32_t) * static_cast<size_t>(n_slots) * rows;
   off = align_up(off, kWsAlign);

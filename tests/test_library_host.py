@@ -316,15 +316,17 @@ def test_equal_segments_weigh_the_keys_of_wide_bf16_requests():
 
 
 def test_merge_tags_follow_the_plan_inputs():
-    """merge_tags: state-row tags on a bf16 plan with a merge kernel unless -1 turns them
-    off; never for the other formats or fused merges; the blob then holds one zeroed int32
-    tag per state row."""
+    """merge_tags: 1 forces state-row tags on a bf16 plan with a merge kernel, -1 turns them
+    off, 0 takes them when the merge folds at least 64 group rows; never for the other
+    formats or fused merges; the blob then holds one zeroed int32 tag per state row."""
     T = [4096, 3587]
     prob = _problem(fixed_splits=8)
     base = dattn.dattn_plan(prob, T, num_sms=152, merge_tags=-1).info
     on = dattn.dattn_plan(prob, T, num_sms=152, merge_tags=1).info
     assert base["merge_tags"] == 0 and on["merge_tags"] == 1
-    assert dattn.dattn_plan(prob, T, num_sms=152).info["merge_tags"] == 1
+    assert dattn.dattn_plan(prob, T, num_sms=152).info["merge_tags"] == 0      # 4 groups x 4 rows
+    wide = _problem(B=16, S_q=1, H_q=32, H_kv=8, fixed_splits=4)
+    assert dattn.dattn_plan(wide, [600] * 16, num_sms=152).info["merge_tags"] == 1   # 128 groups x 4 rows
     assert on["blob_bytes"] >= base["blob_bytes"] + 4 * on["n_slots"] * on["rows"]
     assert on["blob_bytes"] - base["blob_bytes"] < 4 * on["n_slots"] * on["rows"] + 256
     assert dattn.dattn_plan(prob, T, num_sms=152, merge_tags=1, fused_merge=True).info["merge_tags"] == 0
