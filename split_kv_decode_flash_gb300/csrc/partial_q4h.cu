@@ -356,15 +356,16 @@ __device__ void consume_q4h(const Walk& w, uint8_t* smem, int cw, int lane) {
 
   uint32_t k = 0;
   bool dead = false;
-  QH<D> qn;
-  if (w.begin < w.end) load_q4h<D>(p, w.rec(w.begin), 8 * rb + g4, t4, qn);
+
   for (int ii = w.begin; ii < w.end; ++ii) {
     const WorkItem it = w.rec(ii).it;
     const int nq = w.rec(ii).nq;                  // the request's query rows
     const MaskCtx mc{p.mask, nq, it.T, p.n_sink, p.window};
     const bool oka = ra < p.g * nq, okb = rb1 < p.g * nq;
-    const QH<D> q = qn;
-    if (ii + 1 < w.end) load_q4h<D>(p, w.rec(ii + 1), 8 * rb + g4, t4, qn);
+    // the item's query (loading the next item's during this one held its registers
+    // through the whole item: 0.6 us slower per step, 1 us on a mixed batch)
+    QH<D> q;
+    load_q4h<D>(p, w.rec(ii), 8 * rb + g4, t4, q);
     // log2-unit score = s_t (sc 2^24 / f) S' + z_t (sc sum q), per row
     const float ku0 = sc * q.unit0, ku1 = sc * q.unit1, kz0 = sc * q.qsum0, kz1 = sc * q.qsum1;
     float o[NT][4];
