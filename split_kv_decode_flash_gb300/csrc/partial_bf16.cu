@@ -540,10 +540,11 @@ __device__ __forceinline__ void consume_item(const Walk& w, uint8_t* smem, const
   }
 }
 
-// Items of a call with at most 16 rows run the one-tile layout, with the next
-// item's query fragments loaded while the current one runs.  In a call with
-// more rows (a mixed batch's widest request, or a uniform batch of 17 to 32
-// rows) each item takes the layout of its own request's g C_b rows.
+// Items of a call with at most 16 rows run the one-tile layout, each loading
+// its query fragments at its start (loading the next item's during the current
+// one was no faster: headline 52.10 against 51.94 us).  In a call with more
+// rows (a mixed batch's widest request, or a uniform batch of 17 to 32 rows)
+// each item takes the layout of its own request's g C_b rows.
 // SHIFT: shared-shift partials; the synchronized path is compiled without them.
 template <int D, bool SHIFT, bool HK>
 __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, bool dep_wait) {
@@ -555,15 +556,9 @@ __device__ void consume_bf16(const Walk& w, uint8_t* smem, int cw, int lane, boo
   bool dead = false;   // a bounded wait gave up: stop consuming, write nothing
   if (p.rows <= 16) {
     const WarpRole<16> role(cw, lane);
-    uint32_t qn[KS][4];
-    if (w.begin < w.end) load_q<D>(p, w.rec(w.begin), role.r0, role.r1, t4, qn);
     for (int ii = w.begin; ii < w.end; ++ii) {
       uint32_t qa[KS][4];
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk)
-#pragma unroll
-        for (int x = 0; x < 4; ++x) qa[kk][x] = qn[kk][x];
-      if (ii + 1 < w.end) load_q<D>(p, w.rec(ii + 1), role.r0, role.r1, t4, qn);
+      load_q<D>(p, w.rec(ii), role.r0, role.r1, t4, qa);
       consume_item<D, 16, SHIFT, HK>(w, smem, w.rec(ii), qa, cw, lane, k, dead);
     }
   } else {
