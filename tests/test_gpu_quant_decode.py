@@ -177,6 +177,28 @@ def test_int4_kivi_head_dims_groups_and_pages(d, Gv, P, S_q, H_q, H_kv, mask):
     _compare(O, L, w, p, _oracle_cache(w, "int4_kivi"), H.all_rows(p))
 
 
+@pytest.mark.parametrize("fmt,qmul,kmul", [
+    ("int4_kivi", 600.0, 40.0),    # 16 q s_g beyond 2^15 (and |q| > 2^10): the rescaled Q' split
+    ("int4_head", 20000.0, 1.0),   # |q| beyond 2^14: the query divided by a power of two
+    ("int8", 20000.0, 1.0),        # the same on the INT8 kernels (f16 queries)
+])
+@pytest.mark.parametrize("S_q,H_q,H_kv", [(1, 32, 8), (4, 16, 2)])
+def test_quantized_large_magnitudes_take_the_scaled_paths(fmt, qmul, kmul, S_q, H_q, H_kv):
+    """Queries and keys far outside the unit range, with sm_scale small enough to keep the
+    scores moderate: the kernels' power-of-two rescaling of f16 query operands (and KIVI's
+    f32 redo of the Q' split) must give the oracle's rows."""
+    lens = [700, 233, 90]
+    w = W.quantized_history("big", B=len(lens), S_q=S_q, H_q=H_q, H_kv=H_kv, d=128, lens=lens, P=16, seed=29,
+                            device="cuda", fmt=fmt, pool_pages=sum(-(-t // 16) for t in lens) + 2)
+    w.q = (w.q.float() * qmul).to(torch.bfloat16)
+    w.k_rows = (w.k_rows.float() * kmul).to(torch.bfloat16)
+    w.problem = dict(w.problem, sm_scale=2e-5)
+    p, cache = append_history(w, fmt, [[300], [], []])
+    O, L, info = _run(w, fmt, p, cache, chunk_tokens=128, num_sms=5)
+    assert torch.isfinite(L).all()
+    _compare(O, L, w, p, _oracle_cache(w, fmt), H.all_rows(p))
+
+
 @pytest.mark.parametrize("P", [4, 64])
 def test_int8_decode_page_sizes(P):
     lens = [300, 70, 5]
