@@ -495,9 +495,10 @@ __device__ __forceinline__ float fma_q_zhi(uint32_t q, uint32_t zw, float c) {
 }
 
 // A lane's query row for the K side as f16 pairs: qh[c][k] holds channels
-// (32 c + 8 t4 + k, 32 c + 8 t4 + k + 4); the pairs k = 0, 2 (which meet
-// low-nibble codes) carry 16 q.  A row whose largest |q| exceeds 2^10 is
-// scaled by a power of two wq (qinv = 1 / wq) so that 16 q stays in range.
+// (32 c' + 8 t4 + k, 32 c' + 8 t4 + k + 4) of true chunk c' = c ^ cswap (cswap
+// = d / 64 on the lo lanes of the PACKED layout, else 0); the pairs k = 0, 2
+// (which meet low-nibble codes) carry 16 q.  A row whose largest |q| exceeds
+// 2^10 is scaled by a power of two wq (qinv = 1 / wq) so that 16 q stays in range.
 template <int D>
 struct QRow {
   uint32_t qh[D / 32][4];
@@ -505,13 +506,13 @@ struct QRow {
 };
 
 template <int D>
-__device__ __forceinline__ void load_qrow(const __nv_bfloat16* qrow, bool ok, QRow<D>& r, int t4) {
+__device__ __forceinline__ void load_qrow(const __nv_bfloat16* qrow, bool ok, QRow<D>& r, int t4, int cswap) {
   float qf[D / 4];
   float mx = 0.f;
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
     uint4 wq = make_uint4(0u, 0u, 0u, 0u);
-    if (ok) wq = *reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * t4);
+    if (ok) wq = *reinterpret_cast<const uint4*>(qrow + 32 * (c ^ cswap) + 8 * t4);   // stored chunk c: true c ^ cswap
     const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -569,19 +570,25 @@ __device__ __forceinline__ void pack_qprime(const uint32_t (&hi)[D / 32][4], con
 }
 
 // Q' of one K group without a branch: the f16 split of q s_g, the offsets and
-// the factors for w = 1.  Returns whether the lane's quad kept every hi part
-// below 2^15; when some quad did not, qprime_rescaled must redo the split.
+// the factors for w = 1.  Returns whether the lane's row kept every hi part
+// below 2^15; when some row did not, qprime_rescaled must redo the split.
+// PACKED: lane L and lane L ^ 16 hold the same row (hi and lo columns); each
+// splits the products of its own half of the chunks (its stored chunks 0 ..
+// d / 64 - 1, see QRow) and the two trade the parts the other one keeps.
 template <int D, bool PACKED>
 __device__ __forceinline__ bool qprime_fast(const QRow<D>& q, const uint8_t* gt_row, int t4, bool lo_lane, int ra,
                                             QPrime<D, PACKED>& out) {
-  uint32_t hi[D / 32][4], lo[D / 32][4];
+  constexpr int NCH = PACKED ? D / 64 : D / 32;   // chunks this lane splits
+  uint32_t hi[NCH][4], lo[NCH][4];
   float offe = 0.f, offo = 0.f;   // sum q z over the pairs carrying 16 q, and over the others
   uint32_t mx2 = 0u;
+  const int cofs = PACKED && lo_lane ? D / 64 : 0;   // true chunk of stored chunk 0
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    // (s, z) of channels 32 c + 8 t4 + 0..7
-    const uint4 w0 = *reinterpret_cast<const uint4*>(gt_row + (32 * c + 8 * t4) * 4);
-    const uint4 w1 = *reinterpret_cast<const uint4*>(gt_row + (32 * c + 8 * t4) * 4 + 16);
+  for (int c = 0; c < NCH; ++c) {
+    // (s, z) of channels 32 c' + 8 t4 + 0..7 of true chunk c' = c + cofs
+    const uint8_t* g = gt_row + (32 * (c + cofs) + 8 * t4) * 4;
+    const uint4 w0 = *reinterpret_cast<const uint4*>(g);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(g + 16);
     const uint32_t sz[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -596,10 +603,26 @@ __device__ __forceinline__ bool qprime_fast(const QRow<D>& q, const uint8_t* gt_
   }
   const float2 m2 = h2f2(mx2);
   float mx = fmaxf(m2.x, m2.y);
+  float off = fmaf(offe, 1.f / 16.f, offo);
+  if constexpr (PACKED) {
+    mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 16));
+    off += __shfl_xor_sync(kAll, off, 16);
+    // the hi lane keeps hi parts, the lo lane lo parts: each sends the other kind
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t mine = lo_lane ? lo[c][k] : hi[c][k];
+        const uint32_t theirs = __shfl_xor_sync(kAll, lo_lane ? hi[c][k] : lo[c][k], 16);
+        // true chunks c (the hi lane's own) and c + NCH (the lo lane's own)
+        out.b[2 * c + (k >> 1)][k & 1] = lo_lane ? theirs : mine;
+        out.b[2 * (c + NCH) + (k >> 1)][k & 1] = lo_lane ? mine : theirs;
+      }
+  } else {
+    pack_qprime<D, PACKED>(hi, lo, lo_lane, out);
+  }
   mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
-  pack_qprime<D, PACKED>(hi, lo, lo_lane, out);
-  float off = fmaf(offe, 1.f / 16.f, offo);
   off += __shfl_xor_sync(kAll, off, 1);
   off += __shfl_xor_sync(kAll, off, 2);
   off *= q.qinv;
@@ -617,8 +640,14 @@ __device__ __forceinline__ bool qprime_fast(const QRow<D>& q, const uint8_t* gt_
 // (With this path and the fast one in a single function the KIVI step took
 // 5 % longer: the split leaves the fast part without a branch.)
 template <int D, bool PACKED>
-__device__ void qprime_rescaled(const QRow<D>& q, const uint8_t* gt_row, int t4, bool lo_lane, int ra,
+__device__ void qprime_rescaled(const QRow<D>& qs, const uint8_t* gt_row, int t4, bool lo_lane, int ra,
                                 QPrime<D, PACKED>& out) {
+  QRow<D> q;   // the query in true chunk order (PACKED lo lanes store their halves swapped)
+  q.qinv = qs.qinv;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q.qh[c][k] = PACKED && lo_lane ? qs.qh[c ^ (D / 64)][k] : qs.qh[c][k];
   uint32_t hi[D / 32][4], lo[D / 32][4];
   float pm = 0.f;
 #pragma unroll
@@ -734,6 +763,10 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
   // query row of the lane's B fragments
   const int rq = PACKED ? (g4 & 3) : 8 * rbk + g4;
   const bool lo_lane = PACKED && g4 >= 4;
+  // PACKED: a lane and its partner lane ^ 16 hold the same row; each splits the
+  // Q' products of half of the chunks, the lo lane's query stored with its
+  // halves swapped (stored chunk c is true chunk c ^ cswap)
+  const int cswap = lo_lane ? D / 64 : 0;
   const int lrow = lane & 7, lmat = lane >> 3;
   const float sc = p.scale_log2;
   const int gsh = p.kivi_G == 32 ? 5 : 6;   // log2 G
@@ -753,7 +786,7 @@ __device__ void consume_q4(const Walk& w, uint8_t* smem, int cw, int lane) {
     const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
                                 ((static_cast<long long>(qo) + rq / p.g) * p.H_q + it.h * p.g + rq % p.g) * D;
     QRow<D> qr;
-    load_qrow(qrow, okq, qr, t4);
+    load_qrow(qrow, okq, qr, t4, cswap);
     float o[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
