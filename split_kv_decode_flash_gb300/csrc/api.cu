@@ -300,6 +300,7 @@ dattn_status run_impl(const dattn_plan_t* plan, const dattn_problem* prob, const
     m.state_seq = k.state_seq;
     m.run_seq = k.run_seq;
     m.n_slots = k.n_slots;
+    m.end_wait = plan->direct_items > 0 ? 1 : 0;
     m.wait_ns = std::max<uint64_t>(2 * k.wait_ns, 4000000000ull);
     const int err = launch_merge(m, prob->d_h, stream);
     if (err != cudaSuccess) return cuda_fail("dattn_run merge kernel", err);

@@ -172,6 +172,8 @@ struct MergeParams {
   const int32_t* state_seq;   // the partial kernel's state-row tags ([rows][n_slots]), or null (then wait
                               // for the whole grid)
   int32_t run_seq, n_slots;
+  int32_t end_wait;      // with tags: wait for the partial grid before completing (some item
+                         // writes O directly, which only the grid's completion makes visible)
   uint64_t wait_ns;      // limit of a warp's wait for its states' tags
 };
 

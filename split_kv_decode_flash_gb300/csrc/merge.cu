@@ -43,14 +43,18 @@ __device__ __forceinline__ void merge_trace_ready(const MergeParams& p, int lane
   if (p.trace && lane == 0) atomicCAS(reinterpret_cast<unsigned long long*>(p.trace) + 2 * blockIdx.x, 0ull, merge_clock_ns());
 }
 
-// A warp's last step: its trace stamp (latest warp: done), then (TAGS) the
-// wait for the partial grid, so that this grid's completion implies the
-// partial grid's.
+// A warp's last step: its trace stamp (latest warp: done), then (TAGS, when
+// some item of the plan writes O directly) the wait for the partial grid, so
+// that this grid's completion implies those writes too.  When every item
+// leaves partial states, the merge has read every one of them, all written and
+// fenced before their tags: nothing of the partial grid remains to wait for.
 template <bool TAGS>
 __device__ __forceinline__ void merge_end(const MergeParams& p, int lane) {
   if (p.trace && lane == 0)
     atomicMax(reinterpret_cast<unsigned long long*>(p.trace) + 2 * blockIdx.x + 1, merge_clock_ns());
-  if constexpr (TAGS) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if constexpr (TAGS) {
+    if (p.end_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
 }
 
 // WPR = 4: one block of four warps per (group, row); warp w folds states w,

@@ -512,6 +512,8 @@ extern "C" dattn_status dattn_plan(const dattn_problem* prob, const dattn_plan_i
   info.n_items = n_items;
   info.n_ctas = n_ctas;
   info.n_slots = n_slots;
+  plan->direct_items = 0;
+  for (const WorkItem& w : items) plan->direct_items += w.slot < 0 ? 1 : 0;
   info.n_merge_groups = static_cast<int>(merges.size());
   info.fused_merge = hdr.fused;
   info.merge_tags = hdr.tags;

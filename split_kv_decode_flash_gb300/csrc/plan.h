@@ -13,6 +13,7 @@ struct dattn_plan_s {
   std::vector<int32_t> item_cta;
   std::vector<uint8_t> blob;              // header + work list, copied by every run
   dattn_plan_info info;
+  int32_t direct_items = 0;               // items that write O directly (no partial state)
 };
 
 namespace dattn {
