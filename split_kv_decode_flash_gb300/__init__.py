@@ -55,6 +55,11 @@ class PlanInputs(ctypes.Structure):
                 ("qo_indptr", ctypes.c_void_p), ("item_cost_keys", ctypes.c_int32), ("merge_tags", ctypes.c_int32)]
 
 
+class StepCopies(ctypes.Structure):
+    _fields_ = [("copy_stream", ctypes.c_void_p), ("inputs_event", ctypes.c_void_p),
+                ("kernels_event", ctypes.c_void_p)]
+
+
 class HostStep(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("kv_len", ctypes.c_void_p), ("page_indptr", ctypes.c_void_p),
                 ("page_indices", ctypes.c_void_p), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
@@ -143,6 +148,9 @@ def load():
                                          _VP, ctypes.c_size_t, _VP, ctypes.c_size_t, _VP, _VP]),
         "dattn_step_host_finish": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(HostStep), _VP, ctypes.c_size_t,
                                          _VP]),
+        "dattn_step_host_submit_ex": (_ST, [ctypes.POINTER(Problem), ctypes.POINTER(HostStep),
+                                            ctypes.POINTER(Tensors), _VP, ctypes.c_size_t, _VP, ctypes.c_size_t,
+                                            _VP, _VP, ctypes.POINTER(StepCopies)]),
         "dattn_last_error": (ctypes.c_char_p, []),
         "dattn_version": (ctypes.c_int32, []),
     }
@@ -452,6 +460,22 @@ def dattn_step_host_submit(problem, io: HostStep, cache: Tensors, staging, works
                                          staging.data_ptr(), staging.numel(), workspace.data_ptr(),
                                          workspace.numel(), _stream_ptr(stream), done_event.cuda_event),
            "dattn_step_host_submit")
+
+
+def dattn_step_host_submit_ex(problem, io: HostStep, cache: Tensors, staging, workspace, done_event,
+                              copy_stream, inputs_event, kernels_event, stream=None) -> None:
+    """dattn_step_host_submit with the transfers on ``copy_stream`` (a torch.cuda.Stream),
+    ordered against the kernels by ``inputs_event`` and ``kernels_event`` (torch.cuda.Event);
+    ``done_event`` is recorded on the copy stream after the output transfer (see dattn.h)."""
+    prob = problem if isinstance(problem, Problem) else make_problem(problem)
+    for ev in (done_event, inputs_event, kernels_event):
+        if not ev.cuda_event:          # torch creates the CUDA event at its first record
+            ev.record(copy_stream)
+    cp = StepCopies(copy_stream.cuda_stream, inputs_event.cuda_event, kernels_event.cuda_event)
+    _check(load().dattn_step_host_submit_ex(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache),
+                                            staging.data_ptr(), staging.numel(), workspace.data_ptr(),
+                                            workspace.numel(), _stream_ptr(stream), done_event.cuda_event,
+                                            ctypes.byref(cp)), "dattn_step_host_submit_ex")
 
 
 def dattn_step_host_finish(problem, io: HostStep, staging, done_event) -> None:

@@ -531,9 +531,12 @@ size_t staging_out_off(const StepLayout& L, size_t staging_bytes) {
   return staging_bytes >= out ? (staging_bytes - out) / 16 * 16 : 0;
 }
 
+// cp (optional): the transfers go on cp->copy_stream, ordered against the kernels
+// on "stream" by events, so that they overlap the kernels of the step before.
 dattn_status step_submit(const dattn_problem* prob, const dattn_host_step* io, const dattn_tensors* cache,
                          void* staging, size_t staging_bytes, void* workspace, size_t workspace_bytes,
-                         void* stream, void* done_event, const char* where) {
+                         void* stream, void* done_event, const char* where,
+                         const dattn_step_copies* cp = nullptr) {
   dattn_status st = check_step(prob, io, true, where);
   if (st != DATTN_OK) return st;
   if (!cache || !staging) {
@@ -555,10 +558,16 @@ dattn_status step_submit(const dattn_problem* prob, const dattn_host_step* io, c
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint8_t* sg = static_cast<uint8_t*>(staging);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the stream of the transfers: with cp, it first waits for the last use of this
+  // workspace and staging buffer (done_event's previous record) to be finished
+  const cudaStream_t cs = cp ? static_cast<cudaStream_t>(cp->copy_stream) : s;
+  cudaError_t err = cudaSuccess;
+  if (cp) err = cudaStreamWaitEvent(cs, static_cast<cudaEvent_t>(done_event), 0);
+  if (err != cudaSuccess) return cuda_fail("host step copy-stream order", err);
   std::memcpy(sg, io->q, L0.q_bytes);
   if (L0.pi_bytes) std::memcpy(sg + L0.pi_off, io->page_indptr, L0.pi_bytes);
   if (L0.px_bytes) std::memcpy(sg + L0.px_off, io->page_indices, L0.px_bytes);
-  cudaError_t err = cudaMemcpyAsync(ws, sg, L0.plan_off, cudaMemcpyHostToDevice, s);
+  err = cudaMemcpyAsync(ws, sg, L0.plan_off, cudaMemcpyHostToDevice, cs);
   if (err != cudaSuccess) return cuda_fail("host step input transfer", err);
 
   dattn_plan_t* plan = nullptr;
@@ -587,7 +596,11 @@ dattn_status step_submit(const dattn_problem* prob, const dattn_host_step* io, c
   // the work list (the staging copy of the inputs may still be in flight: that
   // part of the staging buffer is not touched again before the step is done)
   std::memcpy(sg + L.plan_off, plan->blob.data(), plan->blob.size());
-  err = cudaMemcpyAsync(ws + L.plan_off, sg + L.plan_off, plan->blob.size(), cudaMemcpyHostToDevice, s);
+  err = cudaMemcpyAsync(ws + L.plan_off, sg + L.plan_off, plan->blob.size(), cudaMemcpyHostToDevice, cs);
+  if (err == cudaSuccess && cp) {   // the kernels wait for the step's inputs
+    err = cudaEventRecord(static_cast<cudaEvent_t>(cp->inputs_event), cs);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(cp->inputs_event), 0);
+  }
   if (err != cudaSuccess) {
     dattn_plan_destroy(plan);
     return cuda_fail("host step work-list transfer", err);
@@ -597,10 +610,16 @@ dattn_status step_submit(const dattn_problem* prob, const dattn_host_step* io, c
   st = run_impl(plan, prob, &t, ws + L.plan_off, plan_ws, stream, &opt, where);
   dattn_plan_destroy(plan);
   if (st != DATTN_OK) return st;
-  // outputs: one device->host transfer into the end of the staging buffer
+  // outputs: one device->host transfer into the end of the staging buffer (with cp,
+  // on the copy stream once the kernels are done)
+  if (cp) {
+    err = cudaEventRecord(static_cast<cudaEvent_t>(cp->kernels_event), s);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(cs, static_cast<cudaEvent_t>(cp->kernels_event), 0);
+    if (err != cudaSuccess) return cuda_fail("host step output order", err);
+  }
   err = cudaMemcpyAsync(sg + staging_out_off(L, staging_bytes), ws + L.o_off, align_ws(L.o_bytes) + L.lse_bytes,
-                        cudaMemcpyDeviceToHost, s);
-  if (err == cudaSuccess && done_event) err = cudaEventRecord(static_cast<cudaEvent_t>(done_event), s);
+                        cudaMemcpyDeviceToHost, cs);
+  if (err == cudaSuccess && done_event) err = cudaEventRecord(static_cast<cudaEvent_t>(done_event), cs);
   if (err != cudaSuccess) return cuda_fail("host step output transfer", err);
   return DATTN_OK;
 }
@@ -637,6 +656,18 @@ extern "C" dattn_status dattn_step_host_submit(const dattn_problem* prob, const 
   }
   return step_submit(prob, io, cache, staging, staging_bytes, workspace, workspace_bytes, stream, done_event,
                      "dattn_step_host_submit");
+}
+
+extern "C" dattn_status dattn_step_host_submit_ex(const dattn_problem* prob, const dattn_host_step* io,
+                                                  const dattn_tensors* cache, void* staging, size_t staging_bytes,
+                                                  void* workspace, size_t workspace_bytes, void* stream,
+                                                  void* done_event, const dattn_step_copies* copies) {
+  if (!done_event || (copies && (!copies->copy_stream || !copies->inputs_event || !copies->kernels_event))) {
+    set_error("dattn_step_host_submit_ex: done_event and, when copies is given, its stream and events are required");
+    return DATTN_EINVAL;
+  }
+  return step_submit(prob, io, cache, staging, staging_bytes, workspace, workspace_bytes, stream, done_event,
+                     "dattn_step_host_submit_ex", copies);
 }
 
 extern "C" dattn_status dattn_step_host_finish(const dattn_problem* prob, const dattn_host_step* io,

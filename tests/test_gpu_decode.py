@@ -582,10 +582,12 @@ def _step_host(w, mask_args=None, num_sms=152):
     return p, o_host.float(), lse_host
 
 
-def test_step_host_submit_finish_pipelined_equals_the_synchronous_step():
-    """Four steps submitted two deep (two staging buffers and events, one workspace, one
-    stream): each step's O and LSE are the synchronous dattn_step_host's bits, and the
-    first matches the oracle on every row."""
+@pytest.mark.parametrize("copy_stream", [False, True])
+def test_step_host_submit_finish_pipelined_equals_the_synchronous_step(copy_stream):
+    """Four steps submitted two deep (two staging buffers and events, one stream; with
+    copy_stream, the transfers on a second stream and one workspace per slot): each step's
+    O and LSE are the synchronous dattn_step_host's bits, and the first matches the oracle
+    on every row."""
     w = W.paged_ragged_gqa("cuda", B=6, lo=100, hi=3000, pool_pages=1200)
     p = w.problem
     B, H_q, d = p["B"], p["H_q"], p["d"]
@@ -596,20 +598,33 @@ def test_step_host_submit_finish_pipelined_equals_the_synchronous_step():
     ios = [dattn.host_step(q, w.kv_len, o, lse=l, page_indptr=w.page_indptr, page_indices=w.page_indices)
            for q, (o, l) in zip(qs, outs)]
     ws_bytes, sg_bytes = dattn.dattn_step_host_sizes(p, ios[0])
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    wss = [torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") for _ in range(2 if copy_stream else 1)]
     staging = [torch.empty(sg_bytes + 4096, dtype=torch.uint8).pin_memory() for _ in range(2)]
     events = [torch.cuda.Event(), torch.cuda.Event()]
-    dattn.dattn_step_host_submit(p, ios[0], cache, staging[0], ws, events[0])
+    cs = torch.cuda.Stream()
+    side = [(torch.cuda.Event(), torch.cuda.Event()) for _ in range(2)]
+
+    def submit(k):
+        slot = k % 2
+        ws = wss[slot % len(wss)]
+        if copy_stream:
+            dattn.dattn_step_host_submit_ex(p, ios[k], cache, staging[slot], ws, events[slot], cs, *side[slot])
+        else:
+            dattn.dattn_step_host_submit(p, ios[k], cache, staging[slot], ws, events[slot])
+
+    submit(0)
     for k in range(1, len(qs) + 1):
         if k < len(qs):
-            dattn.dattn_step_host_submit(p, ios[k], cache, staging[k % 2], ws, events[k % 2])
+            submit(k)
         dattn.dattn_step_host_finish(p, ios[k - 1], staging[(k - 1) % 2], events[(k - 1) % 2])
-    assert dattn.dattn_step_host_status(p, ios[0], ws) == 0
+    torch.cuda.synchronize()
+    for i, ws in enumerate(wss):
+        assert dattn.dattn_step_host_status(p, ios[i], ws) == 0
     for q, (o, l) in zip(qs, outs):
         o1 = torch.full_like(o, float("nan"))
         l1 = torch.full_like(l, float("nan"))
         io1 = dattn.host_step(q, w.kv_len, o1, lse=l1, page_indptr=w.page_indptr, page_indices=w.page_indices)
-        dattn.dattn_step_host(p, io1, cache, staging[0], ws)
+        dattn.dattn_step_host(p, io1, cache, staging[0], wss[0])
         assert torch.equal(o.view(torch.int16), o1.view(torch.int16)) and torch.equal(l, l1)
     H.compare(outs[0][0].float(), outs[0][1], w)
 

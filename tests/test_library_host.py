@@ -404,6 +404,14 @@ def test_step_host_sizes_and_rejections_without_a_gpu():
     io2 = dattn.host_step(q, T, o, num_sms=8)       # paged without host page tables
     assert lib.dattn_step_host_sizes(ctypes.byref(prob), ctypes.byref(io2), ctypes.byref(ctypes.c_size_t()),
                                      ctypes.byref(ctypes.c_size_t())) == 1
+    # the copy-stream submit wants its done event and every field of its copies
+    cp = dattn.StepCopies(fake, 0, fake)
+    st = lib.dattn_step_host_submit_ex(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache), fake, sg, fake * 4,
+                                       ws, None, fake, ctypes.byref(cp))
+    assert st == 1 and "copies" in dattn.dattn_last_error()
+    st = lib.dattn_step_host_submit_ex(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache), fake, sg, fake * 4,
+                                       ws, None, None, None)
+    assert st == 1 and "done_event" in dattn.dattn_last_error()
 
 
 def test_packed_view_layout_validation():
