@@ -410,24 +410,28 @@ dattn_status dattn_step_host_submit(const dattn_problem* prob, const dattn_host_
 dattn_status dattn_step_host_finish(const dattn_problem* prob, const dattn_host_step* io, const void* staging,
                                     size_t staging_bytes, void* done_event);
 
-/* The step's transfers on a stream of their own (dattn_step_host_submit_ex).
- * Every field is required (cudaStream_t / cudaEvent_t as void*, caller-owned). */
+/* The step's transfers on streams of their own (dattn_step_host_submit_ex).
+ * Every field is required (cudaStream_t / cudaEvent_t as void*, caller-owned).
+ * The two directions take two streams: on one stream, step k+1's inputs would
+ * queue behind step k's outputs, which wait for step k's kernels. */
 typedef struct {
-  void* copy_stream;    /* carries the host->device and device->host transfers      */
-  void* inputs_event;   /* recorded on copy_stream once the step's inputs are sent;
+  void* h2d_stream;     /* carries the host->device transfers                       */
+  void* d2h_stream;     /* carries the device->host transfer                        */
+  void* inputs_event;   /* recorded on h2d_stream once the step's inputs are sent;
                            "stream" waits for it before the kernels                  */
-  void* kernels_event;  /* recorded on "stream" after the kernels; copy_stream waits
+  void* kernels_event;  /* recorded on "stream" after the kernels; d2h_stream waits
                            for it before the output transfer                         */
 } dattn_step_copies;
 
-/* dattn_step_host_submit with the transfers on copies->copy_stream (NULL copies:
- * dattn_step_host_submit).  The copy stream first waits for done_event's
- * previous record, the last step that used this staging buffer and workspace,
- * then sends the inputs; the kernels run on "stream" after them; the outputs
- * come back on the copy stream, after which done_event is recorded there.  A
- * caller that alternates two (staging, workspace, event set) slots thus sends
- * step k+1's inputs and receives step k-1's outputs while step k's kernels
- * run.  Steps that share a workspace must not be in flight together. */
+/* dattn_step_host_submit with the transfers on the streams of "copies" (NULL
+ * copies: dattn_step_host_submit).  The host->device stream first waits for
+ * done_event's previous record, the last step that used this staging buffer
+ * and workspace, then sends the inputs; the kernels run on "stream" after
+ * them; the outputs come back on the device->host stream, after which
+ * done_event is recorded there.  A caller that alternates two (staging,
+ * workspace, event set) slots thus sends step k+1's inputs and receives step
+ * k-1's outputs while step k's kernels run.  Steps that share a workspace
+ * must not be in flight together. */
 dattn_status dattn_step_host_submit_ex(const dattn_problem* prob, const dattn_host_step* io,
                                        const dattn_tensors* cache, void* staging, size_t staging_bytes,
                                        void* workspace, size_t workspace_bytes, void* stream, void* done_event,

@@ -56,8 +56,8 @@ class PlanInputs(ctypes.Structure):
 
 
 class StepCopies(ctypes.Structure):
-    _fields_ = [("copy_stream", ctypes.c_void_p), ("inputs_event", ctypes.c_void_p),
-                ("kernels_event", ctypes.c_void_p)]
+    _fields_ = [("h2d_stream", ctypes.c_void_p), ("d2h_stream", ctypes.c_void_p),
+                ("inputs_event", ctypes.c_void_p), ("kernels_event", ctypes.c_void_p)]
 
 
 class HostStep(ctypes.Structure):
@@ -463,15 +463,17 @@ def dattn_step_host_submit(problem, io: HostStep, cache: Tensors, staging, works
 
 
 def dattn_step_host_submit_ex(problem, io: HostStep, cache: Tensors, staging, workspace, done_event,
-                              copy_stream, inputs_event, kernels_event, stream=None) -> None:
-    """dattn_step_host_submit with the transfers on ``copy_stream`` (a torch.cuda.Stream),
-    ordered against the kernels by ``inputs_event`` and ``kernels_event`` (torch.cuda.Event);
-    ``done_event`` is recorded on the copy stream after the output transfer (see dattn.h)."""
+                              h2d_stream, d2h_stream, inputs_event, kernels_event, stream=None) -> None:
+    """dattn_step_host_submit with the transfers on ``h2d_stream`` and ``d2h_stream``
+    (torch.cuda.Stream), ordered against the kernels by ``inputs_event`` and
+    ``kernels_event`` (torch.cuda.Event); ``done_event`` is recorded on the device->host
+    stream after the output transfer (see dattn.h)."""
     prob = problem if isinstance(problem, Problem) else make_problem(problem)
     for ev in (done_event, inputs_event, kernels_event):
         if not ev.cuda_event:          # torch creates the CUDA event at its first record
-            ev.record(copy_stream)
-    cp = StepCopies(copy_stream.cuda_stream, inputs_event.cuda_event, kernels_event.cuda_event)
+            ev.record(h2d_stream)
+    cp = StepCopies(h2d_stream.cuda_stream, d2h_stream.cuda_stream, inputs_event.cuda_event,
+                    kernels_event.cuda_event)
     _check(load().dattn_step_host_submit_ex(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache),
                                             staging.data_ptr(), staging.numel(), workspace.data_ptr(),
                                             workspace.numel(), _stream_ptr(stream), done_event.cuda_event,

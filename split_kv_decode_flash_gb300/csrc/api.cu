@@ -531,8 +531,8 @@ size_t staging_out_off(const StepLayout& L, size_t staging_bytes) {
   return staging_bytes >= out ? (staging_bytes - out) / 16 * 16 : 0;
 }
 
-// cp (optional): the transfers go on cp->copy_stream, ordered against the kernels
-// on "stream" by events, so that they overlap the kernels of the step before.
+// cp (optional): the transfers go on cp's two streams, ordered against the kernels
+// on "stream" by events, so that they overlap the kernels of the neighbouring steps.
 dattn_status step_submit(const dattn_problem* prob, const dattn_host_step* io, const dattn_tensors* cache,
                          void* staging, size_t staging_bytes, void* workspace, size_t workspace_bytes,
                          void* stream, void* done_event, const char* where,
@@ -558,9 +558,10 @@ dattn_status step_submit(const dattn_problem* prob, const dattn_host_step* io, c
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint8_t* sg = static_cast<uint8_t*>(staging);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the stream of the transfers: with cp, it first waits for the last use of this
-  // workspace and staging buffer (done_event's previous record) to be finished
-  const cudaStream_t cs = cp ? static_cast<cudaStream_t>(cp->copy_stream) : s;
+  // the streams of the transfers: with cp, the inputs' stream first waits for the
+  // last use of this workspace and staging buffer (done_event's previous record)
+  const cudaStream_t cs = cp ? static_cast<cudaStream_t>(cp->h2d_stream) : s;
+  const cudaStream_t os = cp ? static_cast<cudaStream_t>(cp->d2h_stream) : s;
   cudaError_t err = cudaSuccess;
   if (cp) err = cudaStreamWaitEvent(cs, static_cast<cudaEvent_t>(done_event), 0);
   if (err != cudaSuccess) return cuda_fail("host step copy-stream order", err);
@@ -611,15 +612,15 @@ dattn_status step_submit(const dattn_problem* prob, const dattn_host_step* io, c
   dattn_plan_destroy(plan);
   if (st != DATTN_OK) return st;
   // outputs: one device->host transfer into the end of the staging buffer (with cp,
-  // on the copy stream once the kernels are done)
+  // on the device->host stream once the kernels are done)
   if (cp) {
     err = cudaEventRecord(static_cast<cudaEvent_t>(cp->kernels_event), s);
-    if (err == cudaSuccess) err = cudaStreamWaitEvent(cs, static_cast<cudaEvent_t>(cp->kernels_event), 0);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(os, static_cast<cudaEvent_t>(cp->kernels_event), 0);
     if (err != cudaSuccess) return cuda_fail("host step output order", err);
   }
   err = cudaMemcpyAsync(sg + staging_out_off(L, staging_bytes), ws + L.o_off, align_ws(L.o_bytes) + L.lse_bytes,
-                        cudaMemcpyDeviceToHost, cs);
-  if (err == cudaSuccess && done_event) err = cudaEventRecord(static_cast<cudaEvent_t>(done_event), cs);
+                        cudaMemcpyDeviceToHost, os);
+  if (err == cudaSuccess && done_event) err = cudaEventRecord(static_cast<cudaEvent_t>(done_event), os);
   if (err != cudaSuccess) return cuda_fail("host step output transfer", err);
   return DATTN_OK;
 }
@@ -662,8 +663,9 @@ extern "C" dattn_status dattn_step_host_submit_ex(const dattn_problem* prob, con
                                                   const dattn_tensors* cache, void* staging, size_t staging_bytes,
                                                   void* workspace, size_t workspace_bytes, void* stream,
                                                   void* done_event, const dattn_step_copies* copies) {
-  if (!done_event || (copies && (!copies->copy_stream || !copies->inputs_event || !copies->kernels_event))) {
-    set_error("dattn_step_host_submit_ex: done_event and, when copies is given, its stream and events are required");
+  if (!done_event || (copies && (!copies->h2d_stream || !copies->d2h_stream || !copies->inputs_event ||
+                                 !copies->kernels_event))) {
+    set_error("dattn_step_host_submit_ex: done_event and, when copies is given, its streams and events are required");
     return DATTN_EINVAL;
   }
   return step_submit(prob, io, cache, staging, staging_bytes, workspace, workspace_bytes, stream, done_event,

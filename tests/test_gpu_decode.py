@@ -585,7 +585,7 @@ def _step_host(w, mask_args=None, num_sms=152):
 @pytest.mark.parametrize("copy_stream", [False, True])
 def test_step_host_submit_finish_pipelined_equals_the_synchronous_step(copy_stream):
     """Four steps submitted two deep (two staging buffers and events, one stream; with
-    copy_stream, the transfers on a second stream and one workspace per slot): each step's
+    copy_stream, the transfers on two streams of their own and one workspace per slot): each step's
     O and LSE are the synchronous dattn_step_host's bits, and the first matches the oracle
     on every row."""
     w = W.paged_ragged_gqa("cuda", B=6, lo=100, hi=3000, pool_pages=1200)
@@ -601,14 +601,14 @@ def test_step_host_submit_finish_pipelined_equals_the_synchronous_step(copy_stre
     wss = [torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") for _ in range(2 if copy_stream else 1)]
     staging = [torch.empty(sg_bytes + 4096, dtype=torch.uint8).pin_memory() for _ in range(2)]
     events = [torch.cuda.Event(), torch.cuda.Event()]
-    cs = torch.cuda.Stream()
+    cs = (torch.cuda.Stream(), torch.cuda.Stream())
     side = [(torch.cuda.Event(), torch.cuda.Event()) for _ in range(2)]
 
     def submit(k):
         slot = k % 2
         ws = wss[slot % len(wss)]
         if copy_stream:
-            dattn.dattn_step_host_submit_ex(p, ios[k], cache, staging[slot], ws, events[slot], cs, *side[slot])
+            dattn.dattn_step_host_submit_ex(p, ios[k], cache, staging[slot], ws, events[slot], *cs, *side[slot])
         else:
             dattn.dattn_step_host_submit(p, ios[k], cache, staging[slot], ws, events[slot])
 

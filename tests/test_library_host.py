@@ -405,7 +405,7 @@ def test_step_host_sizes_and_rejections_without_a_gpu():
     assert lib.dattn_step_host_sizes(ctypes.byref(prob), ctypes.byref(io2), ctypes.byref(ctypes.c_size_t()),
                                      ctypes.byref(ctypes.c_size_t())) == 1
     # the copy-stream submit wants its done event and every field of its copies
-    cp = dattn.StepCopies(fake, 0, fake)
+    cp = dattn.StepCopies(fake, fake, 0, fake)
     st = lib.dattn_step_host_submit_ex(ctypes.byref(prob), ctypes.byref(io), ctypes.byref(cache), fake, sg, fake * 4,
                                        ws, None, fake, ctypes.byref(cp))
     assert st == 1 and "copies" in dattn.dattn_last_error()
