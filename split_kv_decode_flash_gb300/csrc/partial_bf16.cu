@@ -92,7 +92,8 @@ __device__ void produce_bf16(const Walk& w, uint8_t* smem, int lane, int pw, boo
   pc_advance<kTK>(w, c1, kProducerWarps);
   PCur c2 = c1;
   pc_advance<kTK>(w, c2, kProducerWarps);
-  if constexpr (!FM) index_list_prologue(w, c0, lane, dep_wait);   // index lists: list entries are device inputs
+  if constexpr (!FM)   // index lists: list entries are device inputs
+    index_list_prologue<2>(w, c0, lane, dep_wait, kbase, vbase, C::kRowB);
   const SlotKeys<2> k0 = slot_keys<2, !FM>(w, c0, lane);
   SlotKeys<2> k1 = slot_keys<2, !FM>(w, c1, lane);
   SlotKeys<2> k2 = slot_keys<2, !FM>(w, c2, lane);
@@ -177,6 +178,11 @@ __device__ void produce_bf16_runs(const Walk& w, uint8_t* smem, int lane, int pw
   pc_advance<kTK>(w, c1, kProducerWarps);
   RunStage s0 = run_stage(w, c0);
   RunStage s1 = run_stage(w, c1);
+  if (dep_wait) {   // this warp's first two stages go into L2
+    const RunHint h0 = run_hint(w, s0, lane), h1 = run_hint(w, s1, lane);
+    prefetch_run(p, h0, kbase, vbase, C::kRowB);
+    prefetch_run(p, h1, kbase, vbase, C::kRowB);
+  }
   dependency_wait(dep_wait);   // the page table is a device input
   if constexpr (HK) {
     if (pw == 0 && lane == 0) trace_stamp(p, kTrWaitDone);

@@ -332,16 +332,101 @@ __device__ __forceinline__ SlotKeys<S> slot_keys(const Walk& w, const PCur& c, i
   return k;
 }
 
+// ---- L2 prefetch before the wait for the preceding grid ----------------------------------
+// A producer warp, before that wait, puts the K/V rows of its first stages into
+// L2, so that DRAM works while that grid ends and the stages' copies after the
+// wait hit L2: page-run stages (two per warp, a bulk prefetch per page and
+// operand) and the first stage of an index list (line hints per lone row).
+// Stages of arithmetic keys described slot by slot (FlashMask, contiguous
+// caches) are not prefetched: their page-id loads before the wait delayed the
+// wait by more than the prefetch won.  Device inputs (page ids, list entries)
+// are read here without ordering against that grid and past L1: a stale value
+// only prefetches another row of the cache (values outside it are skipped),
+// and the stages' own values are loaded after the wait.  Nothing read here
+// decides a result.
+
+__device__ __forceinline__ int ld_hint(const int* p) {
+  int v;
+  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void prefetch_l2(const char* a, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(bytes) : "memory");
+}
+
+// A key's prefetch in two steps, so that all of a warp's page-id loads are in
+// flight before its first prefetch needs one: hint_key issues the load,
+// hint_row turns the value into the key's K/V row (kNoRow: none; the
+// packed-row layout is not prefetched).
+struct HintKey {
+  int t, pid;
+  bool ok;
+};
+
+__device__ __forceinline__ HintKey hint_key(const PartialParams& p, const ItemRec& r, int t) {
+  HintKey h{t, 0, false};
+  if (t < 0 || t >= r.it.T) return h;
+  if (p.layout == DATTN_KV_PAGED_HND) {
+    const int blk = blk_of(p, t);
+    if (blk >= r.hi - r.lo) return h;
+    h.pid = ld_hint(p.page_indices + r.lo + blk);
+    h.ok = true;
+  } else if (p.layout == DATTN_KV_CONTIG_NHD && r.crow >= 0 && t < p.T_cap) {
+    h.ok = true;
+  }
+  return h;
+}
+
+__device__ __forceinline__ uint32_t hint_row(const PartialParams& p, const ItemRec& r, const HintKey& h) {
+  if (!h.ok) return kNoRow;
+  if (p.layout == DATTN_KV_PAGED_HND) {
+    if (h.pid < 0 || h.pid >= p.num_pages) return kNoRow;
+    return (static_cast<uint32_t>(h.pid) * p.H_kv + r.it.h) * p.P + row_of(p, h.t);
+  }
+  return (static_cast<uint32_t>(r.crow) * p.T_cap + h.t) * p.H_kv + r.it.h;
+}
+
+// One key row: a line hint per 128 bytes (a bulk prefetch per lone row costs
+// more issue than the rows are worth).
+__device__ __forceinline__ void prefetch_row(const char* kbase, const char* vbase, uint32_t row, uint32_t row_bytes) {
+  if (row == kNoRow) return;
+  const char* k = kbase + static_cast<size_t>(row) * row_bytes;
+  const char* v = vbase + static_cast<size_t>(row) * row_bytes;
+  for (uint32_t o = 0; o < row_bytes; o += 128) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(k + o) : "memory");
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(v + o) : "memory");
+  }
+}
+
 // Index lists: a producer warp's first keys are list entries, device inputs.
 // Their lines, the group's list bounds and the request's page-table lines are
-// prefetched into L2 (plan addresses only, nothing read), then the warp waits
-// for the preceding grid before slot_keys reads them.  No-op for the other
-// programs, whose keys are arithmetic.
-__device__ __forceinline__ void index_list_prologue(const Walk& w, const PCur& c0, int lane, bool dep_wait) {
+// prefetched into L2 (plan addresses only), then the warp waits for the
+// preceding grid before slot_keys reads them.  With row_bytes > 0 the K/V rows
+// of the first stage's keys (S per lane) are prefetched too, from list entries
+// and page ids read as hints.  No-op for the other programs, whose keys are
+// arithmetic.
+template <int S = 2>
+__device__ __forceinline__ void index_list_prologue(const Walk& w, const PCur& c0, int lane, bool dep_wait,
+                                                    const char* kbase = nullptr, const char* vbase = nullptr,
+                                                    uint32_t row_bytes = 0) {
   const PartialParams& p = w.p;
   if (p.mask != DATTN_MASK_INDEX_LIST) return;
   if (c0.ii < w.end) {
     const ItemRec r = w.rec(c0.ii);
+    if (dep_wait && row_bytes) {   // entries, then page ids, then rows: each step's loads together
+      int t[S];
+      HintKey hk[S];
+#pragma unroll
+      for (int h = 0; h < S; ++h) {
+        const int j = c0.j0 + lane + 32 * h;
+        t[h] = j < c0.j1 ? ld_hint(p.index_list + r.it.x0 + j) : -1;
+      }
+#pragma unroll
+      for (int h = 0; h < S; ++h) hk[h] = hint_key(p, r, t[h]);
+#pragma unroll
+      for (int h = 0; h < S; ++h) prefetch_row(kbase, vbase, hint_row(p, r, hk[h]), row_bytes);
+    }
     const int j = c0.j0 + 32 * lane;                         // 32 entries (one line) per lane
     if (j < r.it.e) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.index_list + r.it.x0 + j));
     if (lane == 0)
@@ -504,6 +589,52 @@ __device__ __forceinline__ StagePage run_stage_page(const Walk& w, const RunStag
     return {0, 2};
   }
   return {ld_keep(p.page_indices + rec.lo + blk, w.keep), 0};
+}
+
+// The K/V rows of a page-run stage, one range per page and operand, in two
+// steps like hint_key / hint_row: run_hint loads the lane's page id, and
+// prefetch_run issues its ranges.
+struct RunHint {
+  int pid, row0, n;   // the page, its first row in the stage's keys and their count (n = 0: none)
+  int h;
+};
+
+__device__ __forceinline__ RunHint run_hint(const Walk& w, const RunStage& r, int lane) {
+  RunHint g{0, 0, 0, 0};
+  if (r.ii >= w.end) return g;
+  const PartialParams& p = w.p;
+  const ItemRec rec = w.rec(r.ii);
+  const int np2 = r.n2 ? ((r.q0 + r.n2 - 1) >> p.P_shift) - r.b2 + 1 : 0;
+  int blk, t0, t1;   // the lane's page and the stage's keys [t0, t1) in its run
+  if (lane < r.np1) {
+    blk = r.b1 + lane;
+    t0 = r.p0;
+    t1 = r.p0 + r.n1;
+  } else if (lane < r.np1 + np2) {
+    blk = r.b2 + (lane - r.np1);
+    t0 = r.q0;
+    t1 = r.q0 + r.n2;
+  } else {
+    return g;
+  }
+  if (blk >= rec.hi - rec.lo) return g;
+  t0 = max(t0, blk << p.P_shift);
+  t1 = min(min(t1, (blk + 1) << p.P_shift), rec.it.T);
+  if (t1 <= t0) return g;
+  g.pid = ld_hint(p.page_indices + rec.lo + blk);
+  g.row0 = t0 & (p.P - 1);
+  g.n = t1 - t0;
+  g.h = rec.it.h;
+  return g;
+}
+
+__device__ __forceinline__ void prefetch_run(const PartialParams& p, const RunHint& g, const char* kbase,
+                                             const char* vbase, uint32_t row_bytes) {
+  if (g.n == 0 || g.pid < 0 || g.pid >= p.num_pages) return;
+  const size_t off = ((static_cast<size_t>(g.pid) * p.H_kv + g.h) * p.P + g.row0) * row_bytes;
+  const uint32_t bytes = static_cast<uint32_t>(g.n) * row_bytes;
+  prefetch_l2(kbase + off, bytes);
+  prefetch_l2(vbase + off, bytes);
 }
 
 // The page id as run_slot takes it: -1 the lane holds none, -2 invalid (reported).
