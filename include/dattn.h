@@ -431,7 +431,8 @@ typedef struct {
  * done_event is recorded there.  A caller that alternates two (staging,
  * workspace, event set) slots thus sends step k+1's inputs and receives step
  * k-1's outputs while step k's kernels run.  Steps that share a workspace
- * must not be in flight together. */
+ * must not be in flight together.  EINVAL when done_event, or a field of a
+ * non-NULL copies, is NULL; otherwise errors as for dattn_step_host. */
 dattn_status dattn_step_host_submit_ex(const dattn_problem* prob, const dattn_host_step* io,
                                        const dattn_tensors* cache, void* staging, size_t staging_bytes,
                                        void* workspace, size_t workspace_bytes, void* stream, void* done_event,
